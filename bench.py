@@ -1,0 +1,471 @@
+"""Benchmark of the forward FP8 MLP down-projection on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload gpt2s] [--no-extras]
+
+One step is one pass of the forward path over one batch: cast W [K,N] to
+E4M3 (transposed operand), fused ReLU^2 + BF16 copy + E4M3 cast + amax of H
+[M,K], FP8 GEMM Y = X_q W_q / (s_x s_w) -> BF16, and the two delayed-scale
+history updates.  The default workload is the GPT-2-small down-projection
+(M = 8192 tokens, K = 3072, N = 768, margin 2.0, history length 1).
+
+Timing: W untimed warm-up steps, then exactly K steps; before each step a
+256 MiB buffer is written to flush L2 (outside the timed events); each step is
+timed on its stream with CUDA events, kernel by kernel.  `value` is whole-job
+TFLOP/s (2 M N K per step and GPU) over the summed step times, max over ranks.
+`e2e` repeats the step through the same public API with H and W copied in
+from pinned host memory and Y copied back inside the timed region.
+
+`--impl reference` times the CPU oracle (the plain C reference the tests check
+against) on a bounded sample of rows of the same workload and reports it in the
+same metric and unit.
+
+Prints one JSON line on rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from quantize_fp8_gemm_gb300 import workloads as WL  # noqa: E402
+
+METRIC = "FP8 down-proj fwd TFLOP/s (fused quant+GEMM); quant kernel HBM GB/s"
+UNIT = "TFLOP/s"
+PROFILES = os.path.join(ROOT, "profiles")
+L2_FLUSH_BYTES = 256 << 20
+
+
+# ----------------------------------------------------------------- helpers --
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def reduce_over_ranks(local_ms: float, local_units: float, world: int):
+    """Max step time over ranks and the units all ranks processed (weak scaling)."""
+    if world == 1:
+        return local_ms, local_units
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([local_ms], dtype=torch.float64, device=dev)
+    u = torch.tensor([local_units], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling while the timed loop runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+        return False
+
+    def summary(self) -> dict:
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            p = [x.strip() for x in l.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm.append(float(p[1]))
+                smax = float(p[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, p[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        loaded = [s for s in sm if smax and s >= 0.5 * smax] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def file_sha(path: str) -> str:
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def profiled_traffic(kernel_key: str, source: str):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel source
+    is unchanged since the capture (profiles/<key>.txt: 'source_sha' and
+    'dram_bytes_per_launch' lines)."""
+    p = os.path.join(PROFILES, f"{kernel_key}.txt")
+    if not os.path.exists(p):
+        return None
+    kv = {}
+    for line in open(p):
+        if ":" in line and not line.startswith("#"):
+            k, v = line.split(":", 1)
+            kv[k.strip()] = v.strip()
+    if kv.get("source_sha") != file_sha(source):
+        return None
+    try:
+        return float(kv["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# -------------------------------------------------------------- reference --
+def run_reference(args, world, rank):
+    """The CPU oracle, timed on this host's cores on a bounded sample of rows."""
+    if rank != 0:
+        return
+    import oracle as O
+    w = WL.WORKLOADS[args.workload]
+    threads = O.default_threads()
+    h = WL.h_preact(w, 0)
+    Wb = WL.w_down(w)
+    sw = O.delayed_scale(O.amax(Wb, O.ACT_IDENTITY), w.margin, O.E4M3)
+    wq = O.quant(Wb, O.ACT_IDENTITY, O.E4M3, sw, want_act=False, nthreads=threads)["q"]
+    rows_per_step = max(1, args.ref_rows)
+    sx = O.delayed_scale(O.amax(h[:rows_per_step], O.ACT_RELU2), w.margin, O.E4M3)
+    rng = np.random.default_rng(0)
+
+    def one_step():
+        r0 = int(rng.integers(0, w.M - rows_per_step + 1))
+        hs = h[r0:r0 + rows_per_step]
+        rq = O.quant(hs, O.ACT_RELU2, O.E4M3, sx, nthreads=threads)
+        O.gemm_fwd(rq["q"], wq, sx, sw, nthreads=threads)
+
+    for _ in range(args.warmup):
+        one_step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        one_step()
+    dt = time.perf_counter() - t0
+    flops = 2.0 * rows_per_step * w.N * w.K * args.steps
+    value = flops / dt / 1e12
+    sample = (f"{rows_per_step} random rows of H per step (fused quantize + double-precision GEMM "
+              f"over those rows against all {w.N} columns); W cast once outside the timed steps")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded numpy normals rounded to BF16)",
+        "config": {"workload": args.workload, "M": w.M, "K": w.K, "N": w.N, "act": "relu2",
+                   "margin": w.margin, "l2": "sampled rows on the CPU"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(w, h_bits, w_bits, rows: int) -> dict:
+    import oracle as O
+    threads = O.default_threads()
+    sw = O.delayed_scale(O.amax(w_bits, O.ACT_IDENTITY), w.margin, O.E4M3)
+    t0 = time.perf_counter()
+    wq = O.quant(w_bits, O.ACT_IDENTITY, O.E4M3, sw, want_act=False, nthreads=threads)["q"]
+    hs = h_bits[:rows]
+    sx = O.delayed_scale(O.amax(hs, O.ACT_RELU2), w.margin, O.E4M3)
+    rq = O.quant(hs, O.ACT_RELU2, O.E4M3, sx, nthreads=threads)
+    O.gemm_fwd(rq["q"], wq, sx, sw, nthreads=threads)
+    dt = time.perf_counter() - t0
+    return {"value": 2.0 * rows * w.N * w.K / dt / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"first {rows} rows of H: W cast, fused quantize of the rows, double-precision GEMM "
+                      f"of the rows against all {w.N} columns; {dt:.2f} s"}
+
+
+# --------------------------------------------------------------------- ours --
+def run_ours(args, world, rank, local):
+    from quantize_fp8_gemm_gb300 import binding as B
+    from quantize_fp8_gemm_gb300.downproj import Fp8DownProj
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = WL.WORKLOADS[args.workload]
+    M, K, N = w.M, w.K, w.N
+    peaks = measured_peaks()
+    fp8_peak = 2.0 * peaks["bf16_tflops"]  # dense FP8 = 2 x dense BF16 (nominal ratio)
+
+    # inputs: seeded host tensors, resident in HBM before timing
+    h_bits = [WL.h_preact(w, s) for s in range(2)]
+    w_bits = WL.w_down(w)
+    H = [WL.bf16_tensor(b).to(dev) for b in h_bits]
+    Wt = WL.bf16_tensor(w_bits).to(dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+
+    dp = Fp8DownProj(M, K, N, margin=w.margin, history_len=w.history_len, device=dev)
+    dp.calibrate(H[0], Wt)
+
+    names = ["w_cast", "quant", "gemm", "history"]
+
+    def step(i, evs=None):
+        if evs is not None:
+            evs[0].record()
+        dp.cast_weight(Wt)
+        if evs is not None:
+            evs[1].record()
+        dp.quantize(H[i % 2])
+        if evs is not None:
+            evs[2].record()
+        dp.gemm()
+        if evs is not None:
+            evs[3].record()
+        dp.update_scales()
+        if evs is not None:
+            evs[4].record()
+
+    for i in range(args.warmup):
+        flush.zero_()
+        step(i)
+    torch.cuda.synchronize()
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        wall0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.zero_()
+            step(i, evs[i])
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+    barrier(world)
+    per = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(4)] for i in range(args.steps)])
+    step_ms = per.sum(axis=1)
+    local_ms = float(step_ms.mean())
+    flops_step = 2.0 * M * N * K
+    ms, total_flops = reduce_over_ranks(local_ms, flops_step, world)
+    value = total_flops / (ms * 1e-3) / 1e12
+
+    kern_ms = {n: float(per[:, j].mean()) for j, n in enumerate(names)}
+    quant_bytes = 5.0 * M * K
+    quant_gbs = quant_bytes / (kern_ms["quant"] * 1e-3) / 1e9
+    gemm_tflops = flops_step / (kern_ms["gemm"] * 1e-3) / 1e12
+    quant_src = os.path.join(ROOT, "quantize_fp8_gemm_gb300", "csrc", "quant.cu")
+    gemm_src = os.path.join(ROOT, "quantize_fp8_gemm_gb300", "csrc", "gemm.cu")
+    roof_quant = {"bound": "hbm", "kernel": "quant_stream_kernel (fp8_quant_fused)", "achieved": quant_gbs,
+                  "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": quant_gbs / peaks["hbm_gbs"],
+                  "traffic": profiled_traffic(f"quant_stream_{args.workload}", quant_src),
+                  "algorithmic_bytes": quant_bytes, "peak_source": peaks["source"]}
+    roof_gemm = {"bound": "tensor", "kernel": "fp8_gemm_kernel (fp8_gemm_fwd)", "achieved": gemm_tflops,
+                 "peak": fp8_peak, "unit": "TFLOP/s", "frac": gemm_tflops / fp8_peak,
+                 "traffic": profiled_traffic(f"fp8_gemm_{args.workload}", gemm_src),
+                 "algorithmic_flops": flops_step,
+                 "peak_source": f"{peaks['source']} bf16 burst x 2 (nominal FP8:BF16 ratio)"}
+    dominant = roof_quant if kern_ms["quant"] >= kern_ms["gemm"] else roof_gemm
+
+    st = int(dp.gemm_status.item())
+    if st != 0:
+        raise RuntimeError(f"GEMM reported device status {st}")
+
+    extras = {}
+    if not args.no_extras:
+        extras = measure_extras(args, dp, H, Wt, flush, kern_ms, w, dev)
+
+    e2e = measure_e2e(args, dp, h_bits, w_bits, flush, w, dev)
+
+    if rank != 0:
+        return
+    clocks = clk.summary()
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e4m3 x e4m3 -> f32 accumulate -> bf16",
+        "data": "synthetic (seeded numpy normals rounded to BF16, uploaded before timing)",
+        "config": {"workload": args.workload, "M": M, "K": K, "N": N, "act": "relu2",
+                   "scaling": "per-tensor delayed", "margin": w.margin, "history": w.history_len,
+                   "l2": "flushed before every step (256 MiB write, untimed)",
+                   "step": "W cast + fused quant + FP8 GEMM + 2 history updates"},
+        "kernel_ms": kern_ms,
+        "quant_hbm_gbs": quant_gbs,
+        "gemm_tflops": gemm_tflops,
+        "roofline": dominant,
+        "roofline_quant": roof_quant,
+        "roofline_gemm": roof_gemm,
+        "cpu_baseline": cpu_baseline(w, h_bits[0], w_bits, args.cpu_rows) if world == 1 else None,
+        "e2e": e2e,
+        "gpu_launches": 5 * args.steps,
+        "clocks": clocks,
+        "wall_s_timed_loop": wall,
+        "extras": extras,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def timed(fn, flush, reps: int) -> float:
+    """Mean device ms of fn() over reps, L2 flushed before each."""
+    ts = []
+    for _ in range(reps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        ts.append((a, b))
+    torch.cuda.synchronize()
+    return float(np.mean([a.elapsed_time(b) for a, b in ts]))
+
+
+def measure_extras(args, dp, H, Wt, flush, kern_ms, w, dev) -> dict:
+    """Comparators: the unfused three-pass quantize and cuBLAS BF16."""
+    from quantize_fp8_gemm_gb300 import binding as B
+    M, K, N = w.M, w.K, w.N
+    reps = max(20, min(200, args.steps))
+    a_naive = torch.empty(M, K, dtype=torch.bfloat16, device=dev)
+    q_naive = torch.empty(M, K, dtype=torch.uint8, device=dev)
+    amax = torch.zeros(1, device=dev)
+
+    def naive():
+        B.fp8q_naive_act(H[0], B.ACT_RELU2, a_naive)
+        B.fp8q_naive_amax(a_naive, amax)
+        B.fp8q_naive_cast(a_naive, B.E4M3, amax, w.margin, q_naive)
+
+    def bf16_act():
+        B.fp8q_naive_act(H[0], B.ACT_RELU2, a_naive)
+
+    Wbf = Wt  # [K,N] BF16
+    y16 = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+
+    def bf16_gemm():
+        torch.matmul(a_naive, Wbf, out=y16)
+
+    def bf16_path():
+        bf16_act()
+        bf16_gemm()
+
+    for f in (naive, bf16_gemm, bf16_path):
+        f()
+    torch.cuda.synchronize()
+    t_naive = timed(naive, flush, reps)
+    t_bf16_gemm = timed(bf16_gemm, flush, reps)
+    t_bf16_path = timed(bf16_path, flush, reps)
+    t_fused = kern_ms["quant"]
+    t_fp8_path = kern_ms["quant"] + kern_ms["gemm"]
+    flops = 2.0 * M * N * K
+    return {
+        "naive_3pass_ms": t_naive, "fused_quant_ms": t_fused,
+        "fused_vs_naive_speedup": t_naive / t_fused, "fused_vs_naive_ideal": 9.0 / 5.0,
+        "bf16_gemm_ms": t_bf16_gemm, "bf16_gemm_tflops": flops / (t_bf16_gemm * 1e-3) / 1e12,
+        "fp8_vs_bf16_gemm_speedup": t_bf16_gemm / kern_ms["gemm"],
+        "bf16_path_ms (act write + cuBLAS BF16 GEMM)": t_bf16_path,
+        "fp8_path_ms (fused quant + FP8 GEMM)": t_fp8_path,
+        "fp8_vs_bf16_end_to_end_speedup": t_bf16_path / t_fp8_path,
+    }
+
+
+def measure_e2e(args, dp, h_bits, w_bits, flush, w, dev) -> dict:
+    """The step through the public API with host buffers: H, W in from pinned
+    memory, Y back to pinned memory, all inside the timed region."""
+    M, K, N = w.M, w.K, w.N
+    H_host = [WL.bf16_tensor(b).pin_memory() for b in h_bits]
+    W_host = WL.bf16_tensor(w_bits).pin_memory()
+    Y_host = torch.empty(M, N, dtype=torch.bfloat16).pin_memory()
+    Hd = torch.empty(M, K, dtype=torch.bfloat16, device=dev)
+    Wd = torch.empty(K, N, dtype=torch.bfloat16, device=dev)
+    steps = max(3, min(args.steps, 100))
+
+    def e2e_step(i):
+        Hd.copy_(H_host[i % 2], non_blocking=True)
+        Wd.copy_(W_host, non_blocking=True)
+        y = dp.step(Hd, Wd)
+        Y_host.copy_(y, non_blocking=True)
+
+    for i in range(3):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    ts = []
+    for i in range(steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        e2e_step(i)
+        b.record()
+        ts.append((a, b))
+    torch.cuda.synchronize()
+    ms = float(np.mean([a.elapsed_time(b) for a, b in ts]))
+    return {"value": 2.0 * M * N * K / (ms * 1e-3) / 1e12, "unit": UNIT,
+            "h2d_bytes_per_step": 2 * M * K + 2 * K * N, "d2h_bytes_per_step": 2 * M * N,
+            "ms_per_step": ms, "steps": steps}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WL.WORKLOADS), default="gpt2s")
+    ap.add_argument("--cpu-rows", type=int, default=256, help="rows of H the CPU baseline processes")
+    ap.add_argument("--ref-rows", type=int, default=16, help="rows of H per reference-arm step")
+    ap.add_argument("--no-extras", action="store_true", help="skip the comparator measurements")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        ap.error("--warmup must be at least 3")
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "ours" and torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    try:
+        if args.impl == "reference":
+            run_reference(args, world, rank)
+        else:
+            run_ours(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,192 @@
+/*
+ * fp8q.h -- C ABI of libfp8q.so: the forward FP8 MLP down-projection on one
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The path, per training step:
+ *   1. fp8_quant_fused      BF16 pre-activation H -> act(H) in registers ->
+ *                           BF16 copy for backward + FP8 copy + amax
+ *   2. fp8_gemm_fwd         Y = X_q W_q / (s_x s_w), FP32 accumulate, BF16 out
+ *   3. amax_history_update  push this step's amax; scale for the next step
+ *   (fp8_gemm_dgrad         dX = dY_q W_q^T / (s_dy s_w), the gradient shape)
+ *
+ * Conventions shared by every call:
+ *  - All tensor pointers are DEVICE pointers to caller-owned memory; the
+ *    library allocates nothing, frees nothing and never synchronises.  Work is
+ *    enqueued on `stream` (0 = the legacy default stream) and the call returns
+ *    as soon as it is enqueued.
+ *  - Matrices are row-major and densely packed (leading dimension = number of
+ *    columns).  Tensor pointers must be 16-byte aligned.
+ *  - FP8 tensors are raw bytes (E4M3 "fn" variant: max 448, no infinity;
+ *    E5M2: IEEE-like, max 57344).  BF16 tensors are raw 16-bit patterns.
+ *  - Scales are multipliers: q = FP8(x * s); dequantisation divides by s.
+ *  - Return value: FP8Q_OK, or an fp8q_status describing the first argument
+ *    error found (detected on the host, before anything is enqueued), or
+ *    FP8Q_ERR_CUDA when a CUDA call or a launch fails.  Conditions only the
+ *    GPU can see are OR-ed as FP8Q_DEV_* bits into the caller's optional
+ *    device status word.  No call aborts the process or traps the GPU.
+ *
+ * Sources (page title, section):
+ *  [fused]  "Paradigma Details FP8 and Optimizer Tricks Behind NanoGPT
+ *           Records", second paragraph -- one fused kernel writes the BF16
+ *           copy needed for backward, emits the FP8 copy and keeps running
+ *           maxima; the scale uses the previous step's maximum times a safety
+ *           margin, so the large tensor is never reread.
+ *  [scale]  "FP8 training: what it is and how it works", Step 2 -- scale =
+ *           format max / amax; Step 1 -- E4M3 for activations and weights,
+ *           E5M2 for gradients; Step 3 -- FP8 inputs, a wider running sum.
+ *  [tiles]  same page, Trade-offs and edge cases -- amax computed online per
+ *           1x128 activation tile and per 128x128 weight block.
+ *  [gemms]  "FP8 Training & Inference", FP8 Training Recipe -- Y = X x W in
+ *           E4M3; dX = dY x W^T with dY in E5M2 and W in E4M3; Per-Tensor
+ *           Scaling for FP8 -- the scales are factored out of the matmul and
+ *           the output is rescaled to BF16/FP32; Delayed Scaling -- use the
+ *           previous iteration's maximum.
+ */
+#ifndef FP8Q_H
+#define FP8Q_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FP8Q_OK = 0,
+    FP8Q_ERR_NULL = 1,        /* a required pointer is NULL                       */
+    FP8Q_ERR_ALIGN = 2,       /* a tensor pointer is not 16-byte aligned          */
+    FP8Q_ERR_SHAPE = 3,       /* a size is out of range or breaks a multiple rule */
+    FP8Q_ERR_UNSUPPORTED = 4, /* bad enum value, or the device is not sm_103      */
+    FP8Q_ERR_CUDA = 5         /* a CUDA call or kernel launch failed              */
+} fp8q_status;
+
+/* Bits OR-ed into the optional device status word. */
+#define FP8Q_DEV_TIMEOUT 1  /* a bounded wait inside the GEMM gave up; output invalid */
+#define FP8Q_DEV_BAD_AMAX 2 /* history update kept the previous scale (amax 0/inf/NaN) */
+
+typedef enum { FP8Q_E4M3 = 0, FP8Q_E5M2 = 1 } fp8q_format;
+typedef enum { FP8Q_ACT_IDENTITY = 0, FP8Q_ACT_RELU = 1, FP8Q_ACT_RELU2 = 2 } fp8q_act;
+
+/* Width of one scale group along the contraction dimension. */
+#define FP8Q_GROUP 128
+
+/*
+ * fp8_quant_fused -- fused activation + BF16 copy + FP8 cast + amax  [fused]
+ *
+ * For every element of the BF16 tensor h [M,K]:
+ *     a   = act(h)            ReLU(h) = h > 0 ? h : +0;  ReLU^2 = ReLU(h)^2
+ *     abf = BF16(a)           round to nearest even          -> act_out[i,k]
+ *     v   = float32(abf * s)                                  (s: see below)
+ *     q   = FP8(v)            round to nearest even, saturate to +-max
+ *                                                            -> q_out[i,k]
+ *                                                            -> q_t_out[k,i]
+ *     amax_out  = max |abf| over the tensor (exact: a BF16 value)
+ *     sat_count = #{ |v| > format max }
+ *
+ * Scale modes:
+ *   group_scales_out == NULL  per-tensor: s = *scale (device, 1 float; the
+ *                             delayed scale of [fused]/[gemms]).
+ *   group_scales_out != NULL  group mode [tiles]: blocks of group_rows x 128
+ *                             elements (group_rows = 1: 1x128 activation
+ *                             tiles; 128: 128x128 weight blocks).  Each block
+ *                             gets s_g = float32(max / amax_g), 1 for an
+ *                             all-zero block, clamped to FLT_MAX; written to
+ *                             group_scales_out[ceil(M/group_rows), K/128].
+ *                             `scale` is ignored (may be NULL).  K % 128 == 0.
+ *
+ * Arguments:
+ *   h                 device [M,K] BF16, 16-byte aligned.  Required unless M == 0.
+ *   M, K              M >= 0, K >= 16, K % 16 == 0.  M == 0 only zeroes
+ *                     amax_out and sat_count.
+ *   act, fmt          fp8q_act, fp8q_format.
+ *   act_out           device [M,K] BF16 or NULL (W and dY casts skip it).
+ *   q_out             device [M,K] FP8 or NULL.
+ *   q_t_out           device [K,M] FP8 (transposed copy) or NULL; needs
+ *                     M % 16 == 0.  Used for the weight: W [K,N] is cast to
+ *                     W^T [N,K], the forward GEMM's K-major operand.
+ *   amax_out          device float or NULL; zeroed by this call, stream-ordered.
+ *   sat_count         device uint64 or NULL; zeroed by this call.
+ *   stream            CUDA stream.
+ * The tensors must not overlap each other.
+ */
+int fp8_quant_fused(const void* h, int64_t M, int64_t K, int act, int fmt,
+                    const float* scale,
+                    void* act_out, void* q_out, void* q_t_out,
+                    float* amax_out, unsigned long long* sat_count,
+                    float* group_scales_out, int group_rows,
+                    cudaStream_t stream);
+
+/*
+ * fp8_gemm_fwd -- Y = (X_q . W_q) / (s_x s_w), FP32 accumulation, BF16 out  [gemms][scale]
+ *
+ *   x_q     device [M,K] E4M3 (the activation, K contiguous).
+ *   wt_q    device [N,K] E4M3: the weight W [K,N] stored transposed, i.e. the
+ *           q_t_out of fp8_quant_fused run on W.
+ *   scale_x, scale_w
+ *           group_mode 0: device, 1 float each (the scales X and W were cast with).
+ *           group_mode 1: scale_x = device [M, K/128] (1x128 tiles of X),
+ *                         scale_w = device [K/128, ceil(N/128)] (128x128 blocks
+ *                         of W [K,N]); each 128-long slice of the contraction
+ *                         is rescaled by its own pair before it is added to the
+ *                         FP32 sum.  Needs K % 128 == 0.
+ *   y       device [M,N] BF16:  y[i,j] = BF16( (sum_k x[i,k] w[k,j]) / (s_x s_w) ).
+ *   M, N, K M >= 0 (M == 0: nothing is enqueued; x_q and y may then be
+ *           NULL); N >= 16, N % 16 == 0; K >= 16, K % 16 == 0.
+ *   status  device int or NULL: FP8Q_DEV_TIMEOUT is OR-ed in if a bounded
+ *           internal wait gives up (the kernel then exits cleanly; y is invalid).
+ * Runs on tcgen05 tensor cores with TMA-fed shared-memory tiles; needs sm_103.
+ */
+int fp8_gemm_fwd(const void* x_q, const void* wt_q,
+                 const float* scale_x, const float* scale_w, int group_mode,
+                 void* y, int64_t M, int64_t N, int64_t K,
+                 int* status, cudaStream_t stream);
+
+/*
+ * fp8_gemm_dgrad -- dX = (dY_q . W_q^T) / (s_dy s_w), FP32 accumulation, BF16 out  [gemms]
+ *
+ *   dy_q    device [M,N] E5M2 (the output gradient, N contiguous).
+ *   w_q     device [K,N] E4M3: the weight in its own layout (q_out of
+ *           fp8_quant_fused run on W).
+ *   scale_dy, scale_w  device, 1 float each.
+ *   dx      device [M,K] BF16:  dx[i,k] = BF16( (sum_n dy[i,n] w[k,n]) / (s_dy s_w) ).
+ *   M, N, K M >= 0 (M == 0: nothing is enqueued); N >= 16, N % 16 == 0 (the
+ *           contraction); K >= 16, K % 16 == 0.
+ *   status  as for fp8_gemm_fwd.
+ */
+int fp8_gemm_dgrad(const void* dy_q, const void* w_q,
+                   const float* scale_dy, const float* scale_w,
+                   void* dx, int64_t M, int64_t N, int64_t K,
+                   int* status, cudaStream_t stream);
+
+/*
+ * amax_history_update -- delayed per-tensor scale for the next step  [fused][gemms]
+ *
+ * history[0..L-1] (device floats) is a ring whose newest entry is
+ * history[*head] (device int).  One call, in stream order:
+ *     *head = (*head + 1) % L;  history[*head] = *amax_new;
+ *     amax_ref = max(history[0..L-1]);
+ *     s = float32( fmt_max / float32(margin * amax_ref) );
+ *     *scale_out = s                 if amax_ref and s are positive and finite,
+ *     otherwise *scale_out is left as it was and FP8Q_DEV_BAD_AMAX is OR-ed
+ *     into *status (when status != NULL).
+ * With L = 1 the scale depends on the previous step's amax alone.
+ *   L         1 <= L <= 4096.
+ *   margin    host float, positive and finite (multiplicative safety margin).
+ *   fmt       fp8q_format (fmt_max = 448 or 57344).
+ */
+int amax_history_update(float* history, int L, int* head, const float* amax_new,
+                        float margin, int fmt, float* scale_out, int* status,
+                        cudaStream_t stream);
+
+/* Human-readable name of an fp8q_status value (static string). */
+const char* fp8q_status_string(int status);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int fp8q_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8Q_H */

@@ -1,0 +1,165 @@
+"""ctypes binding of libfp8q.so: the C ABI of include/fp8q.h, same names.
+
+Argument marshalling only.  Each function checks that the tensors it is given
+are CUDA tensors of the byte sizes the C call will touch (so a wrong shape is
+a Python error, not an out-of-bounds access on the GPU), passes raw device
+pointers and the current CUDA stream, and raises ``Fp8qError`` on a non-zero
+status.  Every step of the computation runs in the library's CUDA kernels;
+there is no fallback: if the library is missing, the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libfp8q.so")
+
+E4M3, E5M2 = 0, 1
+ACT_IDENTITY, ACT_RELU, ACT_RELU2 = 0, 1, 2
+DEV_TIMEOUT, DEV_BAD_AMAX = 1, 2
+GROUP = 128
+
+_lib = None
+
+
+class Fp8qError(RuntimeError):
+    """A libfp8q call returned a non-zero fp8q_status."""
+
+    def __init__(self, fn: str, status: int, msg: str):
+        super().__init__(f"{fn}: status {status} ({msg})")
+        self.status = status
+
+
+def lib() -> ctypes.CDLL:
+    """Load libfp8q.so (built in-tree); raise if it is missing."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is not built: run quantize_fp8_gemm_gb300.build.build() "
+                "(or python -c 'import __graft_entry__ as g; g.build()') first")
+        L = ctypes.CDLL(LIB_PATH)
+        P, i64, i32, f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
+        L.fp8_quant_fused.argtypes = [P, i64, i64, i32, i32, P, P, P, P, P, P, P, i32, P]
+        L.fp8_gemm_fwd.argtypes = [P, P, P, P, i32, P, i64, i64, i64, P, P]
+        L.fp8_gemm_dgrad.argtypes = [P, P, P, P, P, i64, i64, i64, P, P]
+        L.amax_history_update.argtypes = [P, i32, P, P, f32, i32, P, P, P]
+        L.fp8q_naive_act.argtypes = [P, i64, i64, i32, P, P]
+        L.fp8q_naive_amax.argtypes = [P, i64, P, P]
+        L.fp8q_naive_cast.argtypes = [P, i64, i32, P, f32, P, P, P]
+        L.fp8q_status_string.argtypes = [i32]
+        L.fp8q_status_string.restype = ctypes.c_char_p
+        L.fp8q_version.restype = i32
+        for fn in ("fp8_quant_fused", "fp8_gemm_fwd", "fp8_gemm_dgrad", "amax_history_update",
+                   "fp8q_naive_act", "fp8q_naive_amax", "fp8q_naive_cast"):
+            getattr(L, fn).restype = i32
+        _lib = L
+    return _lib
+
+
+def _check(fn: str, status: int) -> None:
+    if status != 0:
+        raise Fp8qError(fn, status, lib().fp8q_status_string(status).decode())
+
+
+def _ptr(t, nbytes: int | None, name: str):
+    """Device pointer of an optional CUDA tensor holding at least nbytes."""
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    have = t.numel() * t.element_size()
+    if nbytes is not None and have < nbytes:
+        raise ValueError(f"{name} holds {have} bytes, the call needs {nbytes}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def fp8_quant_fused(h: torch.Tensor, act: int, fmt: int, scale: torch.Tensor | None = None, *,
+                    act_out=None, q_out=None, q_t_out=None, amax_out=None, sat_count=None,
+                    group_scales_out=None, group_rows: int = 1, stream=None) -> None:
+    """Fused activation + BF16 copy + FP8 cast + amax of a [M,K] BF16 tensor."""
+    M, K = h.shape
+    n = M * K
+    ng = ((M + group_rows - 1) // max(group_rows, 1)) * (K // GROUP) if group_scales_out is not None else 0
+    st = lib().fp8_quant_fused(
+        _ptr(h, 2 * n, "h"), M, K, act, fmt, _ptr(scale, 4, "scale"),
+        _ptr(act_out, 2 * n, "act_out"), _ptr(q_out, n, "q_out"), _ptr(q_t_out, n, "q_t_out"),
+        _ptr(amax_out, 4, "amax_out"), _ptr(sat_count, 8, "sat_count"),
+        _ptr(group_scales_out, 4 * ng, "group_scales_out"), group_rows, _stream(stream))
+    _check("fp8_quant_fused", st)
+
+
+def fp8_gemm_fwd(x_q: torch.Tensor, wt_q: torch.Tensor, scale_x: torch.Tensor, scale_w: torch.Tensor,
+                 y: torch.Tensor, *, group_mode: int = 0, status=None, stream=None) -> None:
+    """y[M,N] = BF16((x_q[M,K] . wt_q[N,K]^T) / (s_x s_w)) on the tensor cores."""
+    M, K = x_q.shape
+    N = wt_q.shape[0]
+    if wt_q.shape[1] != K:
+        raise ValueError("x_q [M,K] and wt_q [N,K] disagree on K")
+    if group_mode:
+        sx, sw = 4 * M * (K // GROUP), 4 * (K // GROUP) * ((N + GROUP - 1) // GROUP)
+    else:
+        sx, sw = 4, 4
+    st = lib().fp8_gemm_fwd(
+        _ptr(x_q, M * K, "x_q"), _ptr(wt_q, N * K, "wt_q"), _ptr(scale_x, sx, "scale_x"),
+        _ptr(scale_w, sw, "scale_w"), group_mode, _ptr(y, 2 * M * N, "y"), M, N, K,
+        _ptr(status, 4, "status"), _stream(stream))
+    _check("fp8_gemm_fwd", st)
+
+
+def fp8_gemm_dgrad(dy_q: torch.Tensor, w_q: torch.Tensor, scale_dy: torch.Tensor, scale_w: torch.Tensor,
+                   dx: torch.Tensor, *, status=None, stream=None) -> None:
+    """dx[M,K] = BF16((dy_q[M,N] . w_q[K,N]^T) / (s_dy s_w)) on the tensor cores."""
+    M, N = dy_q.shape
+    K = w_q.shape[0]
+    if w_q.shape[1] != N:
+        raise ValueError("dy_q [M,N] and w_q [K,N] disagree on N")
+    st = lib().fp8_gemm_dgrad(
+        _ptr(dy_q, M * N, "dy_q"), _ptr(w_q, K * N, "w_q"), _ptr(scale_dy, 4, "scale_dy"),
+        _ptr(scale_w, 4, "scale_w"), _ptr(dx, 2 * M * K, "dx"), M, N, K,
+        _ptr(status, 4, "status"), _stream(stream))
+    _check("fp8_gemm_dgrad", st)
+
+
+def amax_history_update(history: torch.Tensor, head: torch.Tensor, amax_new: torch.Tensor, margin: float,
+                        fmt: int, scale_out: torch.Tensor, *, status=None, stream=None) -> None:
+    """Push amax_new into the device ring; scale_out = fmt_max / (margin * max(history))."""
+    L = history.numel()
+    st = lib().amax_history_update(
+        _ptr(history, 4 * L, "history"), L, _ptr(head, 4, "head"), _ptr(amax_new, 4, "amax_new"),
+        float(margin), fmt, _ptr(scale_out, 4, "scale_out"), _ptr(status, 4, "status"), _stream(stream))
+    _check("amax_history_update", st)
+
+
+# -- the unfused three-pass comparator (include/fp8q_naive.h) -----------------
+def fp8q_naive_act(h, act: int, act_out, *, stream=None) -> None:
+    M, K = h.shape
+    _check("fp8q_naive_act", lib().fp8q_naive_act(
+        _ptr(h, 2 * M * K, "h"), M, K, act, _ptr(act_out, 2 * M * K, "act_out"), _stream(stream)))
+
+
+def fp8q_naive_amax(x, amax_out, *, stream=None) -> None:
+    n = x.numel()
+    _check("fp8q_naive_amax", lib().fp8q_naive_amax(
+        _ptr(x, 2 * n, "x"), n, _ptr(amax_out, 4, "amax_out"), _stream(stream)))
+
+
+def fp8q_naive_cast(x, fmt: int, amax, margin: float, q_out, *, scale_out=None, stream=None) -> None:
+    n = x.numel()
+    _check("fp8q_naive_cast", lib().fp8q_naive_cast(
+        _ptr(x, 2 * n, "x"), n, fmt, _ptr(amax, 4, "amax"), float(margin),
+        _ptr(scale_out, 4, "scale_out"), _ptr(q_out, n, "q_out"), _stream(stream)))
+
+
+def version() -> int:
+    return lib().fp8q_version()

@@ -1,0 +1,376 @@
+// quant.cu -- the fused activation + quantize step and its C entry point.
+//
+// "Paradigma Details FP8 and Optimizer Tricks Behind NanoGPT Records" (second
+// paragraph): one kernel applies the activation while the values sit in
+// registers, writes the BF16 copy kept for the backward pass, emits the FP8
+// copy under a scale taken from the previous step's amax times a margin, and
+// keeps small running maxima, so the large tensor is never read twice.
+// "FP8 training: what it is and how it works", Step 2 (scale = max / amax) and
+// Trade-offs (online amax per 1x128 activation tile / 128x128 weight block).
+//
+// Per element:  a = act(h);  abf = BF16(a);  v = abf * s (float32);
+//               q = FP8(v) (round to nearest even, saturate);  amax = max |abf|.
+//
+// Kernels:
+//   quant_stream_kernel  per-tensor scale, or 1x128 groups; row-major outputs.
+//                        HBM-bound: 16-byte loads/stores, several loads in
+//                        flight per thread, persistent grid over all SMs,
+//                        amax by warp reduce -> shared memory -> 1 atomic/CTA.
+//   quant_tile_kernel    128x128 tiles through shared memory: the transposed
+//                        FP8 copy (the weight's K-major GEMM operand) and the
+//                        128x128 block scales.
+#include "common.cuh"
+
+#include <algorithm>
+#include <cfloat>
+
+namespace fp8q {
+
+namespace {
+
+constexpr int kThreads = 256;
+
+template <int ACT>
+__device__ __forceinline__ float act_f32(float h) {
+    if constexpr (ACT == FP8Q_ACT_IDENTITY) {
+        return h;
+    } else {
+        float r = h > 0.0f ? h : 0.0f;  // ReLU: +0 for h <= 0, -0 and NaN
+        if constexpr (ACT == FP8Q_ACT_RELU) return r;
+        return __fmul_rn(r, r);         // exact: a BF16 square fits in float32
+    }
+}
+
+// act + BF16 rounding of 8 packed BF16 inputs; returns the packed BF16 results
+// and folds their magnitudes into `amax2` (two 16-bit lanes).
+template <int ACT>
+__device__ __forceinline__ uint4 act8(uint4 x, uint32_t& amax2) {
+    uint32_t in[4] = {x.x, x.y, x.z, x.w};
+    uint32_t out[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        if constexpr (ACT == FP8Q_ACT_IDENTITY) {
+            out[j] = in[j];
+        } else {
+            out[j] = cvt_bf16x2(act_f32<ACT>(bf16lo_to_f32(in[j])), act_f32<ACT>(bf16hi_to_f32(in[j])));
+        }
+        amax2 = __vmaxu2(amax2, out[j] & 0x7FFF7FFFu);
+    }
+    return make_uint4(out[0], out[1], out[2], out[3]);
+}
+
+// scale + FP8 cast of 8 packed BF16 values; counts |v| > max into `nsat`.
+template <int FMT>
+__device__ __forceinline__ uint2 cast8(uint4 a, float s, uint32_t& nsat) {
+    constexpr float fmax = fp8_max_value(FMT);
+    uint32_t in[4] = {a.x, a.y, a.z, a.w};
+    uint32_t q[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        float v0 = __fmul_rn(bf16lo_to_f32(in[j]), s);
+        float v1 = __fmul_rn(bf16hi_to_f32(in[j]), s);
+        nsat += (fabsf(v0) > fmax) + (fabsf(v1) > fmax);
+        q[j] = cvt_fp8x2<FMT>(v0, v1);
+    }
+    return make_uint2(q[0] | (q[1] << 16), q[2] | (q[3] << 16));
+}
+
+__device__ __forceinline__ uint32_t max16x2(uint32_t a2) { return max(a2 & 0xFFFFu, a2 >> 16); }
+
+// Online group scale: max / amax_g (IEEE division), 1 for an all-zero group,
+// clamped to FLT_MAX when the quotient overflows.
+template <int FMT>
+__device__ __forceinline__ float group_scale(uint32_t amax_bf16_bits) {
+    if (amax_bf16_bits == 0) return 1.0f;
+    float s = __fdiv_rn(fp8_max_value(FMT), __uint_as_float(amax_bf16_bits << 16));
+    return s > FLT_MAX ? FLT_MAX : s;
+}
+
+// CTA-wide reduction of (amax bits, saturation count), then one atomic each.
+__device__ __forceinline__ void block_reduce_publish(uint32_t amax16, uint32_t nsat,
+                                                     float* amax_out, unsigned long long* sat_out) {
+    __shared__ uint32_t s_amax[kThreads / 32], s_sat[kThreads / 32];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    amax16 = __reduce_max_sync(0xFFFFFFFFu, amax16);
+    nsat = __reduce_add_sync(0xFFFFFFFFu, nsat);
+    if (lane == 0) { s_amax[warp] = amax16; s_sat[warp] = nsat; }
+    __syncthreads();
+    if (warp == 0) {
+        const int nw = blockDim.x >> 5;
+        uint32_t a = lane < nw ? s_amax[lane] : 0u;
+        uint32_t c = lane < nw ? s_sat[lane] : 0u;
+        a = __reduce_max_sync(0xFFFFFFFFu, a);
+        c = __reduce_add_sync(0xFFFFFFFFu, c);
+        if (lane == 0) {
+            // a non-negative float orders like its bit pattern
+            if (amax_out && a) atomicMax(reinterpret_cast<unsigned int*>(amax_out), a << 16);
+            if (sat_out && c) atomicAdd(sat_out, static_cast<unsigned long long>(c));
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Streaming kernel.  GROUP = false: per-tensor scale, each thread owns 8-element
+// chunks (16 B in) on a grid-stride loop, four loads in flight.  GROUP = true:
+// 1x128 groups, a half-warp owns one group (16 lanes x 8 elements), the group
+// amax is a 16-lane shuffle reduction, two groups in flight per half-warp.
+// ---------------------------------------------------------------------------
+template <int ACT, int FMT, bool GROUP>
+__global__ void __launch_bounds__(kThreads)
+quant_stream_kernel(const uint4* __restrict__ h, int64_t nchunks, const float* __restrict__ scale,
+                    uint4* __restrict__ act_out, uint2* __restrict__ q_out,
+                    float* __restrict__ gscale, float* __restrict__ amax_out,
+                    unsigned long long* __restrict__ sat_out) {
+    uint32_t amax2 = 0, nsat = 0;
+    const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
+
+    if constexpr (!GROUP) {
+        const float s = *scale;
+        constexpr int U = 4;
+        int64_t i = tid;
+        for (; i + (U - 1) * nthreads < nchunks; i += U * nthreads) {
+            uint4 x[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) x[u] = ld_stream_v4(h + i + u * nthreads);
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                uint4 a = act8<ACT>(x[u], amax2);
+                if (act_out) st_stream_v4(act_out + i + u * nthreads, a);
+                uint2 q = cast8<FMT>(a, s, nsat);
+                if (q_out) st_v2(q_out + i + u * nthreads, q);
+            }
+        }
+        for (; i < nchunks; i += nthreads) {
+            uint4 a = act8<ACT>(ld_stream_v4(h + i), amax2);
+            if (act_out) st_stream_v4(act_out + i, a);
+            uint2 q = cast8<FMT>(a, s, nsat);
+            if (q_out) st_v2(q_out + i, q);
+        }
+    } else {
+        // chunk index = group * 16 + l16.  The loop is warp-uniform so all 32
+        // lanes take part in the shuffles; a warp handles 2*U consecutive
+        // groups per trip (half-warp `half` takes every other one).
+        const int l16 = threadIdx.x & 15, half = (threadIdx.x >> 4) & 1;
+        const int64_t ngroups = nchunks >> 4;
+        const int64_t warp_id = tid >> 5, nwarps = nthreads >> 5;
+        constexpr int U = 2;
+        for (int64_t wg = warp_id; wg * (2 * U) < ngroups; wg += nwarps) {
+            uint4 x[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t g = wg * (2 * U) + u * 2 + half;
+                x[u] = g < ngroups ? ld_stream_v4(h + g * 16 + l16) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t g = wg * (2 * U) + u * 2 + half;
+                uint32_t m2 = 0;
+                uint4 a = act8<ACT>(x[u], m2);
+                uint32_t m = max16x2(m2);
+                m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 8));
+                m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
+                m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+                m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+                const float s = group_scale<FMT>(m);
+                if (g < ngroups) {
+                    amax2 = __vmaxu2(amax2, m);
+                    if (act_out) st_stream_v4(act_out + g * 16 + l16, a);
+                    uint2 q = cast8<FMT>(a, s, nsat);
+                    if (q_out) st_v2(q_out + g * 16 + l16, q);
+                    if (l16 == 0 && gscale) gscale[g] = s;
+                }
+            }
+        }
+    }
+    block_reduce_publish(max16x2(amax2), nsat, amax_out, sat_out);
+}
+
+// ---------------------------------------------------------------------------
+// Tiled kernel: one CTA per 128x128 tile of h [M,K].  Chunk c = it*256 + tid
+// (it = 0..7) is row c/16, columns (c%16)*8..+7 of the tile, so a half-warp
+// holds one 128-wide row segment (a 1x128 group when the tile is aligned).
+// ---------------------------------------------------------------------------
+constexpr int kTile = 128;
+constexpr int kTqPitch = kTile + 8;  // bytes per row of the FP8 tile in shared memory
+
+template <int ACT, int FMT>
+__global__ void __launch_bounds__(kThreads)
+quant_tile_kernel(const uint16_t* __restrict__ h, int64_t M, int64_t K, const float* __restrict__ scale,
+                  uint16_t* __restrict__ act_out, uint8_t* __restrict__ q_out,
+                  uint8_t* __restrict__ q_t_out, float* __restrict__ gscale, int group_rows,
+                  float* __restrict__ amax_out, unsigned long long* __restrict__ sat_out) {
+    __shared__ __align__(16) uint8_t tq[kTile * kTqPitch];
+    __shared__ uint32_t s_blk[kThreads / 32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, l16 = tid & 15;
+    const int64_t row0 = static_cast<int64_t>(blockIdx.y) * kTile;
+    const int64_t col0 = static_cast<int64_t>(blockIdx.x) * kTile;
+    const int64_t kgroups = K / kTile;
+
+    uint4 a[8];
+    uint32_t m16[8];
+    uint32_t amax2 = 0, nsat = 0;
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+        const int c = it * kThreads + tid;
+        const int64_t row = row0 + (c >> 4), col = col0 + (c & 15) * 8;
+        const bool ok = row < M && col < K;
+        uint4 x = ok ? ld_stream_v4(h + row * K + col) : make_uint4(0, 0, 0, 0);
+        uint32_t m2 = 0;
+        a[it] = act8<ACT>(x, m2);
+        m16[it] = max16x2(m2);
+        amax2 = __vmaxu2(amax2, m2);
+        if (ok && act_out) st_stream_v4(act_out + row * K + col, a[it]);
+    }
+
+    float s_tensor = 1.0f;
+    if (gscale == nullptr) {
+        s_tensor = *scale;
+    } else if (group_rows == kTile) {
+        uint32_t m = __reduce_max_sync(0xFFFFFFFFu, max16x2(amax2));
+        if (lane == 0) s_blk[warp] = m;
+        __syncthreads();
+        m = 0;
+#pragma unroll
+        for (int w = 0; w < kThreads / 32; ++w) m = max(m, s_blk[w]);
+        s_tensor = group_scale<FMT>(m);
+        if (tid == 0) gscale[blockIdx.y * kgroups + blockIdx.x] = s_tensor;
+    }
+
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+        const int c = it * kThreads + tid;
+        const int r = c >> 4;
+        const int64_t row = row0 + r, col = col0 + (c & 15) * 8;
+        const bool ok = row < M && col < K;
+        float s = s_tensor;
+        if (gscale != nullptr && group_rows == 1) {
+            uint32_t m = m16[it];
+            m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 8));
+            m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
+            m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+            m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+            s = group_scale<FMT>(m);
+            if (ok && l16 == 0) gscale[row * kgroups + blockIdx.x] = s;
+        }
+        uint32_t ns = 0;
+        uint2 q = cast8<FMT>(a[it], s, ns);
+        if (ok) {
+            nsat += ns;
+            if (q_out) st_v2(q_out + row * K + col, q);
+        }
+        if (q_t_out) *reinterpret_cast<uint2*>(tq + r * kTqPitch + (c & 15) * 8) = q;
+    }
+
+    if (q_t_out) {
+        __syncthreads();
+        // output row k = col0 + kk of q_t [K,M]: 16-byte piece rc holds tile rows rc*16..+15
+#pragma unroll
+        for (int it = 0; it < 4; ++it) {
+            const int c = it * kThreads + tid;
+            const int rc = c & 7, kk = c >> 3;
+            const int64_t krow = col0 + kk, mcol = row0 + rc * 16;
+            uint32_t w[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint8_t* p = tq + (rc * 16 + j * 4) * kTqPitch + kk;
+                w[j] = static_cast<uint32_t>(p[0]) | (static_cast<uint32_t>(p[kTqPitch]) << 8) |
+                       (static_cast<uint32_t>(p[2 * kTqPitch]) << 16) |
+                       (static_cast<uint32_t>(p[3 * kTqPitch]) << 24);
+            }
+            if (krow < K && mcol < M)
+                st_v4(q_t_out + krow * M + mcol, make_uint4(w[0], w[1], w[2], w[3]));
+        }
+    }
+    block_reduce_publish(max16x2(amax2), nsat, amax_out, sat_out);
+}
+
+template <int ACT, int FMT>
+int launch_quant(const void* h, int64_t M, int64_t K, const float* scale, void* act_out,
+                 void* q_out, void* q_t_out, float* amax_out, unsigned long long* sat_count,
+                 float* gscale, int group_rows, cudaStream_t stream) {
+    const bool tiled = (q_t_out != nullptr) || (gscale != nullptr && group_rows == kTile);
+    if (tiled) {
+        dim3 grid(static_cast<unsigned>((K + kTile - 1) / kTile), static_cast<unsigned>((M + kTile - 1) / kTile));
+        quant_tile_kernel<ACT, FMT><<<grid, kThreads, 0, stream>>>(
+            static_cast<const uint16_t*>(h), M, K, scale, static_cast<uint16_t*>(act_out),
+            static_cast<uint8_t*>(q_out), static_cast<uint8_t*>(q_t_out), gscale, group_rows,
+            amax_out, sat_count);
+    } else {
+        const int64_t nchunks = M * K / 8;
+        const int64_t per_cta = gscale ? kThreads * 2 : kThreads * 4;  // chunks per CTA per pass
+        const int64_t want = (nchunks + per_cta - 1) / per_cta;
+        const int64_t cap = static_cast<int64_t>(sm_count()) * (2048 / kThreads);
+        const unsigned grid = static_cast<unsigned>(std::max<int64_t>(1, std::min(want, cap)));
+        if (gscale)
+            quant_stream_kernel<ACT, FMT, true><<<grid, kThreads, 0, stream>>>(
+                static_cast<const uint4*>(h), nchunks, scale, static_cast<uint4*>(act_out),
+                static_cast<uint2*>(q_out), gscale, amax_out, sat_count);
+        else
+            quant_stream_kernel<ACT, FMT, false><<<grid, kThreads, 0, stream>>>(
+                static_cast<const uint4*>(h), nchunks, scale, static_cast<uint4*>(act_out),
+                static_cast<uint2*>(q_out), nullptr, amax_out, sat_count);
+    }
+    FP8Q_CHECK_LAUNCH();
+    return FP8Q_OK;
+}
+
+template <int ACT>
+int launch_quant_fmt(int fmt, const void* h, int64_t M, int64_t K, const float* scale, void* act_out,
+                     void* q_out, void* q_t_out, float* amax_out, unsigned long long* sat_count,
+                     float* gscale, int group_rows, cudaStream_t stream) {
+    if (fmt == FP8Q_E5M2)
+        return launch_quant<ACT, FP8Q_E5M2>(h, M, K, scale, act_out, q_out, q_t_out, amax_out,
+                                            sat_count, gscale, group_rows, stream);
+    return launch_quant<ACT, FP8Q_E4M3>(h, M, K, scale, act_out, q_out, q_t_out, amax_out,
+                                        sat_count, gscale, group_rows, stream);
+}
+
+}  // namespace
+
+}  // namespace fp8q
+
+using namespace fp8q;
+
+extern "C" int fp8_quant_fused(const void* h, int64_t M, int64_t K, int act, int fmt,
+                               const float* scale, void* act_out, void* q_out, void* q_t_out,
+                               float* amax_out, unsigned long long* sat_count,
+                               float* group_scales_out, int group_rows, cudaStream_t stream) {
+    if (h == nullptr && M != 0) return FP8Q_ERR_NULL;  // an empty tensor may have no storage
+    if (act < FP8Q_ACT_IDENTITY || act > FP8Q_ACT_RELU2) return FP8Q_ERR_UNSUPPORTED;
+    if (fmt != FP8Q_E4M3 && fmt != FP8Q_E5M2) return FP8Q_ERR_UNSUPPORTED;
+    const bool group = group_scales_out != nullptr;
+    if (group) {
+        if (group_rows != 1 && group_rows != FP8Q_GROUP) return FP8Q_ERR_UNSUPPORTED;
+        if (K % FP8Q_GROUP != 0) return FP8Q_ERR_SHAPE;
+    } else if (scale == nullptr) {
+        return FP8Q_ERR_NULL;
+    }
+    if (M < 0 || K < 16 || K % 16 != 0) return FP8Q_ERR_SHAPE;
+    if (q_t_out != nullptr && M % 16 != 0) return FP8Q_ERR_SHAPE;
+    if ((M + 127) / 128 > 65535 && (q_t_out != nullptr || (group && group_rows == FP8Q_GROUP)))
+        return FP8Q_ERR_SHAPE;
+    if (!aligned16(h) || !aligned16(act_out) || !aligned16(q_out) || !aligned16(q_t_out))
+        return FP8Q_ERR_ALIGN;
+    if ((reinterpret_cast<uintptr_t>(amax_out) & 3u) || (reinterpret_cast<uintptr_t>(group_scales_out) & 3u) ||
+        (reinterpret_cast<uintptr_t>(sat_count) & 7u))
+        return FP8Q_ERR_ALIGN;
+    if (!device_is_sm103()) return FP8Q_ERR_UNSUPPORTED;
+
+    if (amax_out && cudaMemsetAsync(amax_out, 0, sizeof(float), stream) != cudaSuccess) return FP8Q_ERR_CUDA;
+    if (sat_count && cudaMemsetAsync(sat_count, 0, sizeof(unsigned long long), stream) != cudaSuccess)
+        return FP8Q_ERR_CUDA;
+    if (M == 0) return FP8Q_OK;
+
+    switch (act) {
+        case FP8Q_ACT_IDENTITY:
+            return launch_quant_fmt<FP8Q_ACT_IDENTITY>(fmt, h, M, K, scale, act_out, q_out, q_t_out, amax_out,
+                                                       sat_count, group_scales_out, group_rows, stream);
+        case FP8Q_ACT_RELU:
+            return launch_quant_fmt<FP8Q_ACT_RELU>(fmt, h, M, K, scale, act_out, q_out, q_t_out, amax_out,
+                                                   sat_count, group_scales_out, group_rows, stream);
+        default:
+            return launch_quant_fmt<FP8Q_ACT_RELU2>(fmt, h, M, K, scale, act_out, q_out, q_t_out, amax_out,
+                                                    sat_count, group_scales_out, group_rows, stream);
+    }
+}

@@ -1,0 +1,136 @@
+"""Host-side driver of one FP8 down-projection step (device buffers + order of calls).
+
+One training step of the forward FP8 MLP down-projection, as the pages lay it
+out ("Paradigma Details FP8 and Optimizer Tricks Behind NanoGPT Records",
+second paragraph; "FP8 Training & Inference", FP8 Training Recipe and
+Delayed Scaling):
+
+    a7  W [K,N] BF16 -> W_q^T [N,K] E4M3 (+ W_q [K,N] for the gradient GEMM)
+    a1-a5  H [M,K] BF16 -> ReLU^2 -> BF16 copy + X_q E4M3 + amax (+ saturations)
+    a9  Y = X_q W_q / (s_x s_w)  -> BF16 [M,N]
+    a6  push amax(X), amax(W) into their histories -> scales for the next step
+
+Every step runs in libfp8q's kernels through the C ABI; this module only owns
+the device buffers and issues the calls in order on the current stream.  The
+scale a tensor was cast with stays in place until the history update at the
+end of the step, so the GEMM dequantises with the scale actually used.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import binding as B
+
+
+class DelayedScale:
+    """Device-resident delayed-scaling state of one tensor role.
+
+    history [L] (ring, newest at ``head``), the scale to use for the next cast,
+    the amax the next cast writes, and a status word for FP8Q_DEV_* flags.
+    """
+
+    def __init__(self, fmt: int, margin: float, history_len: int = 1, device="cuda"):
+        self.fmt, self.margin, self.L = fmt, float(margin), int(history_len)
+        self.history = torch.zeros(self.L, dtype=torch.float32, device=device)
+        self.head = torch.zeros(1, dtype=torch.int32, device=device)
+        self.scale = torch.ones(1, dtype=torch.float32, device=device)
+        self.amax = torch.zeros(1, dtype=torch.float32, device=device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=device)
+
+    def update(self) -> None:
+        """Push this step's amax; the scale becomes the one for the next step."""
+        B.amax_history_update(self.history, self.head, self.amax, self.margin, self.fmt, self.scale,
+                              status=self.status)
+
+    def seed(self, amax: float) -> None:
+        """Start the history from a known previous amax (e.g. a calibration pass)."""
+        self.amax.fill_(float(amax))
+        self.update()
+
+
+class Fp8DownProj:
+    """Buffers and call order for Y = fp8(act(H)) . fp8(W) -> BF16 on one GPU.
+
+    group=False: per-tensor delayed scales for X and W.
+    group=True : online 1x128 scales for X and 128x128 block scales for W
+                 (needs K % 128 == 0 and N % 128 == 0).
+    """
+
+    def __init__(self, M: int, K: int, N: int, *, act: int = B.ACT_RELU2, margin: float = 2.0,
+                 history_len: int = 1, group: bool = False, with_dgrad: bool = False,
+                 keep_act: bool = True, device="cuda"):
+        self.M, self.K, self.N, self.act, self.group = M, K, N, act, group
+        dev = device
+        self.x = DelayedScale(B.E4M3, margin, history_len, dev)
+        self.w = DelayedScale(B.E4M3, margin, history_len, dev)
+        self.act_bf16 = torch.empty(M, K, dtype=torch.bfloat16, device=dev) if keep_act else None
+        self.x_q = torch.empty(M, K, dtype=torch.uint8, device=dev)
+        self.wt_q = torch.empty(N, K, dtype=torch.uint8, device=dev)
+        self.w_q = torch.empty(K, N, dtype=torch.uint8, device=dev) if with_dgrad else None
+        self.y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+        self.sat = torch.zeros(1, dtype=torch.int64, device=dev)
+        self.gemm_status = torch.zeros(1, dtype=torch.int32, device=dev)
+        if group:
+            if K % B.GROUP or N % B.GROUP:
+                raise ValueError("group scales need K % 128 == 0 and N % 128 == 0")
+            self.x_gscale = torch.empty(M, K // B.GROUP, dtype=torch.float32, device=dev)
+            self.w_gscale = torch.empty(K // B.GROUP, N // B.GROUP, dtype=torch.float32, device=dev)
+
+    # -- a7 -------------------------------------------------------------------
+    def cast_weight(self, W: torch.Tensor) -> None:
+        """W [K,N] BF16 -> W_q^T [N,K] (forward operand) and, if kept, W_q [K,N]."""
+        if self.group:
+            B.fp8_quant_fused(W, B.ACT_IDENTITY, B.E4M3, None, q_out=self.w_q, q_t_out=self.wt_q,
+                              amax_out=self.w.amax, group_scales_out=self.w_gscale,
+                              group_rows=B.GROUP)
+        else:
+            B.fp8_quant_fused(W, B.ACT_IDENTITY, B.E4M3, self.w.scale, q_out=self.w_q,
+                              q_t_out=self.wt_q, amax_out=self.w.amax)
+
+    # -- a1-a5 ----------------------------------------------------------------
+    def quantize(self, H: torch.Tensor) -> None:
+        if self.group:
+            B.fp8_quant_fused(H, self.act, B.E4M3, None, act_out=self.act_bf16, q_out=self.x_q,
+                              amax_out=self.x.amax, sat_count=self.sat,
+                              group_scales_out=self.x_gscale, group_rows=1)
+        else:
+            B.fp8_quant_fused(H, self.act, B.E4M3, self.x.scale, act_out=self.act_bf16,
+                              q_out=self.x_q, amax_out=self.x.amax, sat_count=self.sat)
+
+    # -- a9 -------------------------------------------------------------------
+    def gemm(self) -> torch.Tensor:
+        if self.group:
+            B.fp8_gemm_fwd(self.x_q, self.wt_q, self.x_gscale, self.w_gscale, self.y, group_mode=1,
+                           status=self.gemm_status)
+        else:
+            B.fp8_gemm_fwd(self.x_q, self.wt_q, self.x.scale, self.w.scale, self.y,
+                           status=self.gemm_status)
+        return self.y
+
+    # -- a6 -------------------------------------------------------------------
+    def update_scales(self) -> None:
+        if not self.group:
+            self.x.update()
+            self.w.update()
+
+    def step(self, H: torch.Tensor, W: torch.Tensor) -> torch.Tensor:
+        """One forward step: cast W, fused quantize of H, FP8 GEMM, history update."""
+        self.cast_weight(W)
+        self.quantize(H)
+        y = self.gemm()
+        self.update_scales()
+        return y
+
+    def calibrate(self, H: torch.Tensor, W: torch.Tensor) -> None:
+        """Bootstrap the delayed scales from step 0's own tensors (one amax pass each).
+
+        The casts run with a placeholder scale; only their amax is kept, and it
+        seeds each history so step 0 already has a scale."""
+        if self.group:
+            return
+        self.x.scale.fill_(1.0)
+        self.w.scale.fill_(1.0)
+        self.cast_weight(W)
+        self.quantize(H)
+        self.x.update()
+        self.w.update()

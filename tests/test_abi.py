@@ -1,0 +1,124 @@
+"""The C ABI library builds, loads and exports every function include/*.h
+declares; its host-side argument checks return the documented status codes.
+No kernel is launched: with no sm_103 device visible, valid arguments end in
+FP8Q_ERR_UNSUPPORTED, and invalid ones are rejected before any CUDA call.
+The pointers passed here are never dereferenced on the host.
+"""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from tests.conftest import ROOT
+
+INCLUDE = os.path.join(ROOT, "include")
+
+OK, ERR_NULL, ERR_ALIGN, ERR_SHAPE, ERR_UNSUPPORTED, ERR_CUDA = range(6)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from quantize_fp8_gemm_gb300 import build
+    path = build.build()
+    from quantize_fp8_gemm_gb300 import binding
+    return binding.lib()
+
+
+def declared_functions():
+    names = []
+    for h in sorted(os.listdir(INCLUDE)):
+        if h.endswith(".h"):
+            text = open(os.path.join(INCLUDE, h)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_\s\*]*?\b([a-z][a-z0-9_]*)\s*\(", text, re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_four_calls():
+    names = declared_functions()
+    for fn in ("fp8_quant_fused", "fp8_gemm_fwd", "fp8_gemm_dgrad", "amax_history_update"):
+        assert fn in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from quantize_fp8_gemm_gb300 import binding
+    out = subprocess.run(["nm", "-D", "--defined-only", binding.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\s[TW]\s+(\S+)$", out, re.M))
+    for fn in declared_functions():
+        assert fn in exported, f"{fn} declared in include/ but not exported"
+        assert hasattr(lib, fn)
+
+
+def test_status_strings_and_version(lib):
+    assert lib.fp8q_version() >= 100
+    for s in range(6):
+        assert lib.fp8q_status_string(s)
+
+
+A = 1 << 20  # a 16-byte aligned fake device address (never dereferenced)
+
+
+def quant(lib, h=A, M=64, K=256, act=2, fmt=0, scale=A, act_out=A, q=A, qt=None, amax=A, sat=A,
+          gs=None, grows=1):
+    return lib.fp8_quant_fused(h, M, K, act, fmt, scale, act_out, q, qt, amax, sat, gs, grows, None)
+
+
+def test_quant_argument_checks(lib):
+    assert quant(lib, h=None) == ERR_NULL
+    assert quant(lib, scale=None) == ERR_NULL
+    assert quant(lib, act=3) == ERR_UNSUPPORTED
+    assert quant(lib, fmt=2) == ERR_UNSUPPORTED
+    assert quant(lib, K=8) == ERR_SHAPE
+    assert quant(lib, K=40) == ERR_SHAPE
+    assert quant(lib, M=-1) == ERR_SHAPE
+    assert quant(lib, qt=A, M=65) == ERR_SHAPE
+    assert quant(lib, h=A + 8) == ERR_ALIGN
+    assert quant(lib, q=A + 4) == ERR_ALIGN
+    assert quant(lib, sat=A + 4) == ERR_ALIGN
+    assert quant(lib, gs=A, K=192) == ERR_SHAPE
+    assert quant(lib, gs=A, grows=2) == ERR_UNSUPPORTED
+    # well-formed: only the device check remains, and there is no sm_103 here
+    assert quant(lib) == ERR_UNSUPPORTED
+    assert quant(lib, scale=None, gs=A, grows=128) == ERR_UNSUPPORTED
+
+
+def gemm(lib, a=A, b=A, sa=A, sb=A, grp=0, d=A, M=128, N=256, K=512, st=None):
+    return lib.fp8_gemm_fwd(a, b, sa, sb, grp, d, M, N, K, st, None)
+
+
+def test_gemm_argument_checks(lib):
+    assert gemm(lib, a=None) == ERR_NULL
+    assert gemm(lib, sb=None) == ERR_NULL
+    assert gemm(lib, N=8) == ERR_SHAPE
+    assert gemm(lib, N=24) == ERR_SHAPE
+    assert gemm(lib, K=40) == ERR_SHAPE
+    assert gemm(lib, M=-5) == ERR_SHAPE
+    assert gemm(lib, d=A + 2) == ERR_ALIGN
+    assert gemm(lib, st=A + 2) == ERR_ALIGN
+    assert gemm(lib) == ERR_UNSUPPORTED
+    dg = lib.fp8_gemm_dgrad
+    assert dg(A, A, A, A, A, 128, 24, 256, None, None) == ERR_SHAPE      # contraction N % 16
+    assert dg(A, A, A, A, None, 128, 32, 256, None, None) == ERR_NULL
+    assert dg(A, A, A, A, A, 128, 32, 256, None, None) == ERR_UNSUPPORTED
+
+
+def test_history_argument_checks(lib):
+    f = lib.amax_history_update
+    assert f(None, 1, A, A, 2.0, 0, A, None, None) == ERR_NULL
+    assert f(A, 0, A, A, 2.0, 0, A, None, None) == ERR_SHAPE
+    assert f(A, 5000, A, A, 2.0, 0, A, None, None) == ERR_SHAPE
+    assert f(A, 1, A, A, 0.0, 0, A, None, None) == ERR_SHAPE
+    assert f(A, 1, A, A, float("nan"), 0, A, None, None) == ERR_SHAPE
+    assert f(A, 1, A, A, 2.0, 7, A, None, None) == ERR_UNSUPPORTED
+    assert f(A, 1, A + 2, A, 2.0, 0, A, None, None) == ERR_ALIGN
+    assert f(A, 4, A, A, 2.0, 0, A, None, None) == ERR_UNSUPPORTED
+
+
+def test_binding_refuses_host_tensors(lib):
+    import torch
+    from quantize_fp8_gemm_gb300 import binding as B
+    h = torch.zeros(16, 16, dtype=torch.bfloat16)
+    with pytest.raises(TypeError):
+        B.fp8_quant_fused(h, B.ACT_RELU2, B.E4M3, torch.ones(1))

@@ -1,0 +1,125 @@
+"""Parity of the tcgen05 FP8 GEMMs (fp8_gemm_fwd, fp8_gemm_dgrad) with the
+oracle's double-precision GEMM over the dequantised FP8 values.
+
+Floating point: every output must satisfy
+    |y_gpu - y_ref| <= ulp_bf16(y_ref) + 1e-5 * sum_k |a_ik b_kj| / (s_a s_b)
+(tests/parity.py).  Operands are produced by the oracle's own encoder, so the
+two sides share no code.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from quantize_fp8_gemm_gb300 import binding as B
+from tests.parity import assert_gemm_close, dev_f32, dev_u8
+
+pytestmark = pytest.mark.gpu
+
+
+def _codes(x, fmt):
+    return O.fp8_encode(np.asarray(x, np.float32), fmt)
+
+
+def rand_e4m3(shape, seed, scale=1.0):
+    x = np.random.default_rng(seed).standard_normal(shape) * scale
+    return _codes(x, O.E4M3)
+
+
+def run_fwd(xq, wq, sx, sw, group=False):
+    """xq [M,K], wq [K,N] (oracle layout); the GPU gets W^T [N,K]."""
+    M, K = xq.shape
+    N = wq.shape[1]
+    y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.fp8_gemm_fwd(dev_u8(xq), dev_u8(np.ascontiguousarray(wq.T)), dev_f32(sx), dev_f32(sw), y,
+                   group_mode=int(group), status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    return y
+
+
+def test_matmul_worked_example_padded():
+    """X = [1, 2], W = [[1,2,3,4],[5,6,7,8]] -> [11, 14, 17, 20], padded to 16 x 16."""
+    x = np.zeros((1, 16)); x[0, :2] = [1, 2]
+    w = np.zeros((16, 16)); w[0, :4] = [1, 2, 3, 4]; w[1, :4] = [5, 6, 7, 8]
+    y = run_fwd(_codes(x, O.E4M3), _codes(w, O.E4M3), 1.0, 1.0)
+    assert y[0, :4].float().cpu().tolist() == [11.0, 14.0, 17.0, 20.0]
+    assert float(y[0, 4:].abs().max()) == 0.0
+
+
+def test_small_integers_exact():
+    """Integer-valued operands: the FP32 sum is exact, so Y is BF16(exact) bit for bit."""
+    rng = np.random.default_rng(5)
+    M, K, N = 150, 512, 272
+    xi = rng.integers(-8, 9, (M, K))
+    wi = rng.integers(-8, 9, (K, N))
+    y = run_fwd(_codes(xi, O.E4M3), _codes(wi, O.E4M3), 1.0, 1.0)
+    exact = torch.from_numpy((xi @ wi).astype(np.float32)).to(torch.bfloat16)
+    assert torch.equal(y.cpu().view(torch.int16), exact.view(torch.int16))
+
+
+def test_tiny_workload():
+    from quantize_fp8_gemm_gb300 import workloads as WL
+    w = WL.WORKLOADS["tiny"]
+    h = WL.h_preact(w)
+    W = WL.w_down(w)
+    sx = O.delayed_scale(w.prev_amax, w.margin, O.E4M3)
+    rx = O.quant(h, O.ACT_RELU2, O.E4M3, sx)
+    sw = O.delayed_scale(O.amax(W, O.ACT_IDENTITY), w.margin, O.E4M3)
+    rw = O.quant(W, O.ACT_IDENTITY, O.E4M3, sw)
+    Yr, S = O.gemm_fwd(rx["q"], rw["q"], sx, sw)
+    y = run_fwd(rx["q"], rw["q"], sx, sw)
+    assert_gemm_close(y, Yr, S)
+
+
+@pytest.mark.parametrize("M,N,K", [
+    (64, 64, 256), (128, 128, 128), (200, 272, 384), (129, 144, 1600), (300, 512, 16),
+    (1, 16, 48), (513, 768, 3072), (1000, 1600, 640),
+])
+def test_fwd_shapes(M, N, K):
+    xq = rand_e4m3((M, K), seed=M + N + K, scale=30.0)
+    wq = rand_e4m3((K, N), seed=M * N + K, scale=30.0)
+    sx, sw = 3.5, 0.75
+    Yr, S = O.gemm_fwd(xq, wq, sx, sw)
+    y = run_fwd(xq, wq, sx, sw)
+    assert_gemm_close(y, Yr, S)
+
+
+@pytest.mark.parametrize("M,N,K", [(130, 160, 272), (64, 1600, 512), (300, 256, 6400)])
+def test_dgrad_shapes(M, N, K):
+    rng = np.random.default_rng(M + N + K)
+    dyq = _codes(rng.standard_normal((M, N)) * 1000.0, O.E5M2)
+    wq = rand_e4m3((K, N), seed=K, scale=50.0)
+    sdy, sw = 2.0 ** 10, 5.0
+    Yr, S = O.gemm_dgrad(dyq, wq, sdy, sw)
+    dx = torch.empty(M, K, dtype=torch.bfloat16, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.fp8_gemm_dgrad(dev_u8(dyq), dev_u8(wq), dev_f32(sdy), dev_f32(sw), dx, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert_gemm_close(dx, Yr, S)
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 128, 128), (300, 384, 512), (1, 256, 1024)])
+def test_group_scaled_fwd(M, N, K):
+    rng = np.random.default_rng(M * 3 + N + K)
+    xq = rand_e4m3((M, K), seed=M + 1, scale=30.0)
+    wq = rand_e4m3((K, N), seed=N + 2, scale=30.0)
+    sx = (2.0 ** rng.uniform(-4, 4, (M, K // 128))).astype(np.float32)
+    sw = (2.0 ** rng.uniform(-4, 4, (K // 128, N // 128))).astype(np.float32)
+    Yr, S = O.gemm_fwd(xq, wq, sx, sw, group=True)
+    y = run_fwd(xq, wq, sx, sw, group=True)
+    assert_gemm_close(y, Yr, S)
+
+
+def test_constant_sign_long_contraction():
+    """All-positive operands over K = 6400: the accumulation error does not cancel,
+    which exposes a reduced-precision accumulator."""
+    M, N, K = 128, 160, 6400
+    rng = np.random.default_rng(77)
+    xq = _codes(np.abs(rng.standard_normal((M, K))) * 100 + 1, O.E4M3)
+    wq = _codes(np.abs(rng.standard_normal((K, N))) * 100 + 1, O.E4M3)
+    Yr, S = O.gemm_fwd(xq, wq, 1.0, 1.0)
+    y = run_fwd(xq, wq, 1.0, 1.0)
+    assert_gemm_close(y, Yr, S)
