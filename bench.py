@@ -10,8 +10,10 @@ history updates.  The default workload is the GPT-2-small down-projection
 (M = 8192 tokens, K = 3072, N = 768, margin 2.0, history length 1).
 
 Timing: W untimed warm-up steps, then exactly K steps; before each step a
-256 MiB buffer is written to flush L2 (outside the timed events); each step is
-timed on its stream with CUDA events, kernel by kernel.  `value` is whole-job
+256 MiB buffer is written and read back to flush L2 (outside the timed
+events); each step (a CUDA graph: the weight cast runs beside the quantize)
+is
+timed on its stream with CUDA events at the phase boundaries.  `value` is whole-job
 TFLOP/s (2 M N K per step and GPU) over the summed step times, max over ranks.
 `e2e` repeats the step through the same public API with H and W copied in
 from pinned host memory and Y copied back inside the timed region.
@@ -45,6 +47,13 @@ METRIC = "FP8 down-proj fwd TFLOP/s (fused quant+GEMM); quant kernel HBM GB/s"
 UNIT = "TFLOP/s"
 PROFILES = os.path.join(ROOT, "profiles")
 L2_FLUSH_BYTES = 256 << 20
+
+
+def flush_l2(buf: torch.Tensor) -> None:
+    """Write, then read back, a buffer twice the size of L2: the next step
+    starts with none of its inputs in L2 and no dirty lines left to write back."""
+    buf.zero_()
+    buf.sum()
 
 
 # ----------------------------------------------------------------- helpers --
@@ -246,48 +255,62 @@ def run_ours(args, world, rank, local):
     dp = Fp8DownProj(M, K, N, margin=w.margin, history_len=w.history_len, device=dev)
     dp.calibrate(H[0], Wt)
 
-    names = ["w_cast", "quant", "gemm", "history"]
+    # Headline: the whole step as one CUDA graph (no host work between its
+    # kernels), timed with events recorded around each replay on the launching
+    # stream.  A torch build that cannot capture falls back to eager launches.
+    for i in range(args.warmup):
+        flush_l2(flush)
+        dp.step(H[i % 2], Wt)
+    torch.cuda.synchronize()
+    graphs = None
+    timing_mode = "eager"
+    if not args.eager:
+        try:
+            graphs = [dp.capture(H[b], Wt) for b in range(2)]
+            timing_mode = "cuda-graph"
+        except RuntimeError as exc:  # capture refused
+            timing_mode = f"eager (graph capture unavailable: {exc})"[:200]
+            graphs = None
 
-    def step(i, evs=None):
-        if evs is not None:
-            evs[0].record()
-        dp.cast_weight(Wt)
-        if evs is not None:
-            evs[1].record()
-        dp.quantize(H[i % 2])
-        if evs is not None:
-            evs[2].record()
-        dp.gemm()
-        if evs is not None:
-            evs[3].record()
-        dp.update_scales()
-        if evs is not None:
-            evs[4].record()
+    def run_step(i):
+        if graphs is not None:
+            graphs[i % 2].replay()
+        else:
+            dp.step(H[i % 2], Wt)
 
     for i in range(args.warmup):
-        flush.zero_()
-        step(i)
+        flush_l2(flush)
+        run_step(i)
     torch.cuda.synchronize()
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         wall0 = time.perf_counter()
         for i in range(args.steps):
-            flush.zero_()
-            step(i, evs[i])
+            flush_l2(flush)
+            pairs[i][0].record()
+            run_step(i)
+            pairs[i][1].record()
         torch.cuda.synchronize()
         wall = time.perf_counter() - wall0
+        # each kernel of the step alone (L2 flushed before each), for the rooflines
+        kern_reps = max(10, min(args.steps, 200))
+        kern_ms = {
+            "w_cast": timed(lambda: dp.cast_weight(Wt), flush, kern_reps),
+            "quant": timed(lambda: dp.quantize(H[0]), flush, kern_reps),
+            "gemm": timed(lambda: dp.gemm(), flush, kern_reps),
+            "history (one tensor)": timed(lambda: dp.x.update(), flush, kern_reps),
+        }
     barrier(world)
-    per = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(4)] for i in range(args.steps)])
-    step_ms = per.sum(axis=1)
+    step_ms = np.array([a.elapsed_time(b) for a, b in pairs])
     local_ms = float(step_ms.mean())
     flops_step = 2.0 * M * N * K
     ms, total_flops = reduce_over_ranks(local_ms, flops_step, world)
     value = total_flops / (ms * 1e-3) / 1e12
+    kern_ms["step"] = local_ms
 
-    kern_ms = {n: float(per[:, j].mean()) for j, n in enumerate(names)}
     quant_bytes = 5.0 * M * K
     quant_gbs = quant_bytes / (kern_ms["quant"] * 1e-3) / 1e9
     gemm_tflops = flops_step / (kern_ms["gemm"] * 1e-3) / 1e12
@@ -312,7 +335,7 @@ def run_ours(args, world, rank, local):
     if not args.no_extras:
         extras = measure_extras(args, dp, H, Wt, flush, kern_ms, w, dev)
 
-    e2e = measure_e2e(args, dp, h_bits, w_bits, flush, w, dev)
+    e2e = measure_e2e(args, dp, h_bits, w_bits, flush, w, dev, use_graph=graphs is not None)
 
     if rank != 0:
         return
@@ -324,7 +347,7 @@ def run_ours(args, world, rank, local):
         "data": "synthetic (seeded numpy normals rounded to BF16, uploaded before timing)",
         "config": {"workload": args.workload, "M": M, "K": K, "N": N, "act": "relu2",
                    "scaling": "per-tensor delayed", "margin": w.margin, "history": w.history_len,
-                   "l2": "flushed before every step (256 MiB write, untimed)",
+                   "l2": "flushed before every step (256 MiB write + read, untimed)",
                    "step": "W cast + fused quant + FP8 GEMM + 2 history updates"},
         "kernel_ms": kern_ms,
         "quant_hbm_gbs": quant_gbs,
@@ -335,6 +358,8 @@ def run_ours(args, world, rank, local):
         "cpu_baseline": cpu_baseline(w, h_bits[0], w_bits, args.cpu_rows) if world == 1 else None,
         "e2e": e2e,
         "gpu_launches": 5 * args.steps,
+        "kernel_ms_note": "each kernel timed alone with L2 flushed; includes the call's stream-ordered zeroing",
+        "timing": timing_mode,
         "clocks": clocks,
         "wall_s_timed_loop": wall,
         "extras": extras,
@@ -346,7 +371,7 @@ def timed(fn, flush, reps: int) -> float:
     """Mean device ms of fn() over reps, L2 flushed before each."""
     ts = []
     for _ in range(reps):
-        flush.zero_()
+        flush_l2(flush)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
         fn()
@@ -403,21 +428,25 @@ def measure_extras(args, dp, H, Wt, flush, kern_ms, w, dev) -> dict:
     }
 
 
-def measure_e2e(args, dp, h_bits, w_bits, flush, w, dev) -> dict:
+def measure_e2e(args, dp, h_bits, w_bits, flush, w, dev, use_graph=True) -> dict:
     """The step through the public API with host buffers: H, W in from pinned
-    memory, Y back to pinned memory, all inside the timed region."""
+    memory, the step (as its CUDA graph), Y back to pinned memory, all inside
+    the timed region."""
     M, K, N = w.M, w.K, w.N
     H_host = [WL.bf16_tensor(b).pin_memory() for b in h_bits]
     W_host = WL.bf16_tensor(w_bits).pin_memory()
     Y_host = torch.empty(M, N, dtype=torch.bfloat16).pin_memory()
     Hd = torch.empty(M, K, dtype=torch.bfloat16, device=dev)
     Wd = torch.empty(K, N, dtype=torch.bfloat16, device=dev)
-    steps = max(3, min(args.steps, 100))
+    Hd.copy_(H_host[0])
+    Wd.copy_(W_host)
+    g = dp.capture(Hd, Wd) if use_graph else None
+    steps = max(3, min(args.steps, 200))
 
     def e2e_step(i):
         Hd.copy_(H_host[i % 2], non_blocking=True)
         Wd.copy_(W_host, non_blocking=True)
-        y = dp.step(Hd, Wd)
+        y = g.replay() if g is not None else dp.step(Hd, Wd)
         Y_host.copy_(y, non_blocking=True)
 
     for i in range(3):
@@ -425,7 +454,7 @@ def measure_e2e(args, dp, h_bits, w_bits, flush, w, dev) -> dict:
     torch.cuda.synchronize()
     ts = []
     for i in range(steps):
-        flush.zero_()
+        flush_l2(flush)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
         e2e_step(i)
@@ -448,6 +477,8 @@ def main():
     ap.add_argument("--cpu-rows", type=int, default=256, help="rows of H the CPU baseline processes")
     ap.add_argument("--ref-rows", type=int, default=16, help="rows of H per reference-arm step")
     ap.add_argument("--no-extras", action="store_true", help="skip the comparator measurements")
+    ap.add_argument("--eager", action="store_true",
+                    help="launch the step kernel by kernel instead of as a CUDA graph")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be at least 3")

@@ -179,6 +179,20 @@ int amax_history_update(float* history, int L, int* head, const float* amax_new,
                         float margin, int fmt, float* scale_out, int* status,
                         cudaStream_t stream);
 
+/*
+ * fp8q_gemm_set_tile -- pin the GEMM tile shape (a tuning knob; "FP8 training:
+ * what it is and how it works", Trade-offs and edge cases: tile size is a
+ * tuning knob).  Process-wide; affects later per-tensor fp8_gemm_fwd /
+ * fp8_gemm_dgrad calls (the group-scaled GEMM always uses 1-CTA 128-wide
+ * tiles).
+ *   pair  -1: automatic choice (the default; bn ignored)
+ *          0: one CTA per 128 x bn tile           bn in {128, 160, 192, 256}
+ *          1: a CTA pair per 256 x bn tile (2-SM)  bn in {128, 160, 192, 224, 256}
+ *             (pairs are used only when M > 128; smaller M falls back to one CTA)
+ * Returns FP8Q_ERR_UNSUPPORTED for any other combination (nothing changes).
+ */
+int fp8q_gemm_set_tile(int pair, int bn);
+
 /* Human-readable name of an fp8q_status value (static string). */
 const char* fp8q_status_string(int status);
 

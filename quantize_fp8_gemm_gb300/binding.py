@@ -53,6 +53,8 @@ def lib() -> ctypes.CDLL:
         L.fp8q_status_string.argtypes = [i32]
         L.fp8q_status_string.restype = ctypes.c_char_p
         L.fp8q_version.restype = i32
+        L.fp8q_gemm_set_tile.argtypes = [i32, i32]
+        L.fp8q_gemm_set_tile.restype = i32
         for fn in ("fp8_quant_fused", "fp8_gemm_fwd", "fp8_gemm_dgrad", "amax_history_update",
                    "fp8q_naive_act", "fp8q_naive_amax", "fp8q_naive_cast"):
             getattr(L, fn).restype = i32
@@ -159,6 +161,11 @@ def fp8q_naive_cast(x, fmt: int, amax, margin: float, q_out, *, scale_out=None, 
     _check("fp8q_naive_cast", lib().fp8q_naive_cast(
         _ptr(x, 2 * n, "x"), n, fmt, _ptr(amax, 4, "amax"), float(margin),
         _ptr(scale_out, 4, "scale_out"), _ptr(q_out, n, "q_out"), _stream(stream)))
+
+
+def fp8q_gemm_set_tile(pair: int, bn: int = 0) -> None:
+    """Pin the GEMM tile shape (pair -1 = automatic, 0 = 1-CTA, 1 = 2-SM pair)."""
+    _check("fp8q_gemm_set_tile", lib().fp8q_gemm_set_tile(pair, bn))
 
 
 def version() -> int:

@@ -13,20 +13,30 @@
 //   forward: A = X_q [M,K],   B = W_q^T [N,K]
 //   dgrad:   A = dY_q [M,N],  B = W_q [K,N]   (the contraction runs over N)
 //
-// CTA = 6 warps, persistent over 128 x BN output tiles (static round robin):
+// CTA = 6 warps, persistent over output tiles (static round robin):
 //   warp 0     TMA producer: one elected lane streams A/B k-blocks (128 B of
 //              K per row, 128-byte swizzle) into a STAGES-deep ring.
 //   warp 1     MMA issuer: allocates TMEM; one lane issues 4 x
-//              tcgen05.mma.kind::f8f6f4 (M=128, N=BN, K=32) per k-block and
-//              commits each stage back to the producer.
+//              tcgen05.mma.kind::f8f6f4 (K=32) per k-block and commits each
+//              stage back to the producer.
 //   warps 2-5  epilogue: tcgen05.ld the FP32 accumulator (each warp its 32
 //              TMEM lanes), scale by 1/(s_a s_b), round to BF16, store.
 // Two TMEM accumulators let the epilogue of tile i overlap the main loop of
-// tile i+1.  Every mbarrier wait is bounded; on time-out the CTA sets
-// FP8Q_DEV_TIMEOUT, drains its in-flight copies and MMAs and exits.
+// tile i+1.
+//
+// PAIR = true: a cluster of two CTAs on two SMs computes a 256 x BN tile with
+// tcgen05.mma.cta_group::2 (M = 256).  Each CTA loads its own 128 rows of A
+// and one half (BN/2 rows) of B, so each SM fills and reads half the B bytes
+// of a 1-CTA 128 x BN tile; both CTAs' copies complete on the leader's
+// barrier, the leader's single thread issues the MMAs, and its commits
+// arrive on the barriers of both CTAs.  Each CTA's TMEM holds its 128 rows.
+//
+// Every mbarrier wait is bounded; on time-out the CTA sets FP8Q_DEV_TIMEOUT,
+// waits (bounded) for its copies and MMAs in flight, frees TMEM and exits.
 #include "common.cuh"
 
 #include <algorithm>
+#include <atomic>
 #include <cudaTypedefs.h>
 #include <mutex>
 
@@ -34,36 +44,36 @@ namespace fp8q {
 
 namespace {
 
-constexpr int BM = 128;            // tile rows (MMA M, TMEM lanes)
+constexpr int BM = 128;            // rows per CTA (MMA rows per SM, TMEM lanes)
 constexpr int BK = 128;            // K bytes per stage = one 128-byte swizzle row
 constexpr int UMMA_K = 32;         // K per tcgen05.mma for 8-bit operands
 constexpr int kThreadsGemm = 192;  // 6 warps
 constexpr int kEpiWarps = 4;
+constexpr int kEpiChunkBytes = 32 * 32 * 2;  // one warp's 32 rows x 32 BF16 columns
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per wait: far above any real wait
 
-template <int BN>
+template <int BN, bool PAIR>
 struct Cfg {
+    static constexpr int B_ROWS = PAIR ? BN / 2 : BN;  // rows of B this CTA loads
     static constexpr int A_BYTES = BM * BK;
-    static constexpr int B_BYTES = BN * BK;
+    static constexpr int B_BYTES = B_ROWS * BK;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int STAGES = (220 * 1024) / STAGE_BYTES < 8 ? (220 * 1024) / STAGE_BYTES : 8;
+    static constexpr int TX_BYTES = STAGE_BYTES * (PAIR ? 2 : 1);  // bytes one stage's barrier awaits
+    static constexpr int EPI_BYTES = kEpiWarps * 2 * kEpiChunkBytes;  // double-buffered store staging
+    static constexpr int RING_BUDGET = 220 * 1024 - EPI_BYTES;
+    static constexpr int STAGES = RING_BUDGET / STAGE_BYTES < 8 ? RING_BUDGET / STAGE_BYTES : 8;
     static constexpr int TMEM_COLS = (2 * BN <= 256) ? 256 : 512;  // two accumulators, power of 2
     static constexpr int BAR_BYTES = 256;
-    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + BAR_BYTES + 1024;  // + alignment slack
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES + 1024;  // + alignment slack
+    static constexpr int MMA_M = PAIR ? 2 * BM : BM;
+    static constexpr int TILE_M = MMA_M;                              // output rows per tile
+    static constexpr int EPI_ARRIVALS = kEpiWarps * (PAIR ? 2 : 1);   // per accumulator drain
     static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "BN: multiple of 32 in [64, 256]");
+    static_assert(B_ROWS % 8 == 0, "B rows: whole 8-row swizzle atoms");
+    static_assert(B_BYTES % 1024 == 0, "stage tiles stay 1024-byte aligned");
     static_assert(STAGES >= 2, "at least a double-buffered ring");
     static_assert((2 * STAGES + 5) * 8 + 16 <= BAR_BYTES, "barrier area");
-};
-
-struct SharedCtl {
-    // lives at the end of the dynamic shared memory, after the stage ring
-    uint64_t* full;
-    uint64_t* empty;
-    uint64_t* tfull;
-    uint64_t* tempty;
-    uint64_t* drain;
-    uint32_t* tmem_holder;
-    int* abort_flag;
+    static_assert(SMEM_BYTES <= 232448, "dynamic shared memory per CTA");
 };
 
 // Bounded wait on an mbarrier phase.  Returns false when this thread gave up
@@ -93,79 +103,106 @@ __device__ __forceinline__ void wait_phase_drain(uint64_t* bar, uint32_t parity)
     }
 }
 
-__device__ __forceinline__ void store_bf16x32(__nv_bfloat16* __restrict__ D, int64_t row, int64_t col0,
-                                              int64_t M, int64_t N, const float (&v)[32]) {
-    if (row >= M) return;
+// One warp's 32 rows x 32 columns of output: round to BF16, stage in shared
+// memory with the 64-byte swizzle (row r's 16-byte piece j sits at piece
+// j ^ ((r >> 1) & 3), so the warp's writes spread over all banks) and write
+// it with one TMA store; the box is clipped at the edges of D.  Two staging
+// buffers per warp alternate; a buffer is reused once the store issued from
+// it two chunks earlier has finished reading it.
+__device__ __forceinline__ void epi_store_chunk(const CUtensorMap* tmD, uint8_t* warp_stage, int& nchunk,
+                                                int lane, const float (&v)[32], int32_t col0, int32_t row0,
+                                                int64_t M, int64_t N) {
+    uint8_t* buf = warp_stage + (nchunk & 1) * kEpiChunkBytes;
+    if (nchunk >= 2) {
+        if (lane == 0) bulk_wait_group_read<1>();
+        __syncwarp();
+    }
+    const int sw = (lane >> 1) & 3;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        const int64_t col = col0 + 8 * j;
-        if (col < N) {
-            uint4 p;
-            p.x = cvt_bf16x2(v[8 * j + 0], v[8 * j + 1]);
-            p.y = cvt_bf16x2(v[8 * j + 2], v[8 * j + 3]);
-            p.z = cvt_bf16x2(v[8 * j + 4], v[8 * j + 5]);
-            p.w = cvt_bf16x2(v[8 * j + 6], v[8 * j + 7]);
-            st_v4(D + row * N + col, p);
-        }
+        uint4 p;
+        p.x = cvt_bf16x2(v[8 * j + 0], v[8 * j + 1]);
+        p.y = cvt_bf16x2(v[8 * j + 2], v[8 * j + 3]);
+        p.z = cvt_bf16x2(v[8 * j + 4], v[8 * j + 5]);
+        p.w = cvt_bf16x2(v[8 * j + 6], v[8 * j + 7]);
+        *reinterpret_cast<uint4*>(buf + lane * 64 + ((j ^ sw) << 4)) = p;
     }
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0 && row0 < M && col0 < N) {  // a box wholly outside D is not stored
+        tma_store_2d(tmD, smem_u32(buf), col0, row0);
+        bulk_commit_group();
+    }
+    ++nchunk;
 }
 
 // GROUP = false: per-tensor scales, one accumulation per tile.
-// GROUP = true : BN must be 128; each 128-long K slice is accumulated into a
+// GROUP = true : 1-CTA, BN = 128; each 128-long K slice is accumulated into a
 //                fresh TMEM buffer and promoted into FP32 registers with its
 //                own 1/(s_a[row, kb] * s_b[kb, n_blk]).
-template <int BN, bool GROUP>
+// PAIR = true  : 2-SM tiles (see the file header); per-tensor scales only.
+template <int BN, bool GROUP, bool PAIR>
 __global__ void __launch_bounds__(kThreadsGemm, 1)
 fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const __grid_constant__ CUtensorMap tmD,
                 const float* __restrict__ scale_a, const float* __restrict__ scale_b,
-                __nv_bfloat16* __restrict__ D, int64_t M, int64_t N, int64_t K, uint32_t idesc,
-                int* __restrict__ status) {
-    using C = Cfg<BN>;
-    static_assert(!GROUP || BN == 128, "group mode uses 128-wide tiles");
+                int64_t M, int64_t N, int64_t K, uint32_t idesc, int* __restrict__ status) {
+    using C = Cfg<BN, PAIR>;
+    static_assert(!GROUP || (BN == 128 && !PAIR), "group mode uses 1-CTA 128-wide tiles");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
-    SharedCtl ctl;
-    ctl.full = bars;
-    ctl.empty = bars + C::STAGES;
-    ctl.tfull = bars + 2 * C::STAGES;
-    ctl.tempty = bars + 2 * C::STAGES + 2;
-    ctl.drain = bars + 2 * C::STAGES + 4;
-    ctl.tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * C::STAGES + 5);
-    ctl.abort_flag = reinterpret_cast<int*>(bars + 2 * C::STAGES + 5) + 1;
-    volatile int* abort_flag = ctl.abort_flag;
+    uint8_t* epi_stage = smem + C::STAGES * C::STAGE_BYTES;  // 1024-aligned: STAGE_BYTES is
+    uint64_t* bars = reinterpret_cast<uint64_t*>(epi_stage + C::EPI_BYTES);
+    uint64_t* full = bars;
+    uint64_t* empty = bars + C::STAGES;
+    uint64_t* tfull = bars + 2 * C::STAGES;
+    uint64_t* tempty = bars + 2 * C::STAGES + 2;
+    uint64_t* drain = bars + 2 * C::STAGES + 4;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * C::STAGES + 5);
+    volatile int* abort_flag = reinterpret_cast<int*>(tmem_holder) + 1;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t num_m = (M + BM - 1) / BM;
+    const uint32_t rank = PAIR ? cluster_ctarank() : 0;  // 0 = leader of the pair
+    const bool leader = rank == 0;
+    const int64_t num_m = (M + C::TILE_M - 1) / C::TILE_M;
     const int64_t num_n = (N + BN - 1) / BN;
     const int64_t num_tiles = num_m * num_n;
+    const int64_t first_tile = PAIR ? blockIdx.x / 2 : blockIdx.x;
+    const int64_t tile_stride = PAIR ? gridDim.x / 2 : gridDim.x;
     const int num_kb = static_cast<int>((K + BK - 1) / BK);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
-            mbar_init(smem_u32(&ctl.full[s]), 1);
-            mbar_init(smem_u32(&ctl.empty[s]), 1);
+            mbar_init(smem_u32(&full[s]), 1);
+            mbar_init(smem_u32(&empty[s]), 1);
         }
         for (int a = 0; a < 2; ++a) {
-            mbar_init(smem_u32(&ctl.tfull[a]), 1);
-            mbar_init(smem_u32(&ctl.tempty[a]), kEpiWarps);
+            mbar_init(smem_u32(&tfull[a]), 1);
+            mbar_init(smem_u32(&tempty[a]), C::EPI_ARRIVALS);
         }
-        mbar_init(smem_u32(ctl.drain), 1);
-        *ctl.abort_flag = 0;
+        mbar_init(smem_u32(drain), 1);
+        *abort_flag = 0;
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
+        tma_prefetch_desc(&tmD);
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(ctl.tmem_holder), C::TMEM_COLS);
-        tmem_relinquish();
+        if constexpr (PAIR) {
+            tmem_alloc_pair(smem_u32(tmem_holder), C::TMEM_COLS);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(smem_u32(tmem_holder), C::TMEM_COLS);
+            tmem_relinquish();
+        }
     }
     tc_fence_before();
     __syncthreads();
+    if constexpr (PAIR) cluster_sync_all();  // the peer's barriers exist before any copy signals them
     tc_fence_after();
-    const uint32_t tmem_base = *ctl.tmem_holder;
+    const uint32_t tmem_base = *tmem_holder;
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
@@ -174,49 +211,60 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             uint32_t phase = 0;
             int64_t issued = 0;
             bool ok = true;
-            for (int64_t tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-                const int32_t m0 = static_cast<int32_t>((tile / num_n) * BM);
-                const int32_t n0 = static_cast<int32_t>((tile % num_n) * BN);
+            for (int64_t tile = first_tile; tile < num_tiles && ok; tile += tile_stride) {
+                const int32_t m0 = static_cast<int32_t>((tile / num_n) * C::TILE_M + rank * BM);
+                const int32_t n0 = static_cast<int32_t>((tile % num_n) * BN + rank * C::B_ROWS);
                 for (int kb = 0; kb < num_kb; ++kb) {
-                    if (!wait_phase(&ctl.empty[stage], phase ^ 1u, abort_flag, status)) { ok = false; break; }
-                    const uint32_t fb = smem_u32(&ctl.full[stage]);
+                    if (!wait_phase(&empty[stage], phase ^ 1u, abort_flag, status)) { ok = false; break; }
                     uint8_t* sa = smem + stage * C::STAGE_BYTES;
-                    mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
-                    tma_load_2d(smem_u32(sa), &tmA, fb, kb * BK, m0);
-                    tma_load_2d(smem_u32(sa + C::A_BYTES), &tmB, fb, kb * BK, n0);
+                    if constexpr (PAIR) {
+                        // both CTAs' copies complete on the leader's barrier
+                        const uint32_t fb = mapa_shared(smem_u32(&full[stage]), 0);
+                        if (leader) mbar_arrive_expect_tx(smem_u32(&full[stage]), C::TX_BYTES);
+                        tma_load_2d_pair(smem_u32(sa), &tmA, fb, kb * BK, m0);
+                        tma_load_2d_pair(smem_u32(sa + C::A_BYTES), &tmB, fb, kb * BK, n0);
+                    } else {
+                        const uint32_t fb = smem_u32(&full[stage]);
+                        mbar_arrive_expect_tx(fb, C::TX_BYTES);
+                        tma_load_2d(smem_u32(sa), &tmA, fb, kb * BK, m0);
+                        tma_load_2d(smem_u32(sa + C::A_BYTES), &tmB, fb, kb * BK, n0);
+                    }
                     ++issued;
                     if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
                 }
             }
-            // Make sure no copy is still landing in shared memory when the CTA
-            // exits: wait for the last (up to STAGES) loads to complete.
-            const int64_t tail = issued < C::STAGES ? issued : C::STAGES;
-            for (int64_t j = 1; j <= tail; ++j) {
-                int s = stage - static_cast<int>(j);
-                uint32_t ph = phase;
-                if (s < 0) { s += C::STAGES; ph ^= 1u; }
-                wait_phase_drain(&ctl.full[s], ph);
+            // No copy may still be landing in shared memory when the CTA exits:
+            // wait for the last (up to STAGES) loads.  In a pair the leader's
+            // barriers also count the peer's bytes.
+            if (!PAIR || leader) {
+                const int64_t tail = issued < C::STAGES ? issued : C::STAGES;
+                for (int64_t j = 1; j <= tail; ++j) {
+                    int s = stage - static_cast<int>(j);
+                    uint32_t ph = phase;
+                    if (s < 0) { s += C::STAGES; ph ^= 1u; }
+                    wait_phase_drain(&full[s], ph);
+                }
             }
         }
     } else if (warp == 1) {
         // -------------------------------------------------------- MMA issuer
-        if (lane == 0) {
+        if (lane == 0 && (!PAIR || leader)) {
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true;
-            for (int64_t tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+            for (int64_t tile = first_tile; tile < num_tiles && ok; tile += tile_stride) {
                 if (!GROUP) {
-                    if (!wait_phase(&ctl.tempty[acc], acc_phase ^ 1u, abort_flag, status)) { ok = false; break; }
+                    if (!wait_phase(&tempty[acc], acc_phase ^ 1u, abort_flag, status)) { ok = false; break; }
                     tc_fence_after();
                 }
                 for (int kb = 0; kb < num_kb; ++kb) {
                     if (GROUP) {
-                        if (!wait_phase(&ctl.tempty[acc], acc_phase ^ 1u, abort_flag, status)) { ok = false; break; }
+                        if (!wait_phase(&tempty[acc], acc_phase ^ 1u, abort_flag, status)) { ok = false; break; }
                         tc_fence_after();
                     }
-                    if (!wait_phase(&ctl.full[stage], phase, abort_flag, status)) { ok = false; break; }
+                    if (!wait_phase(&full[stage], phase, abort_flag, status)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
                     const uint32_t a_addr = smem_u32(smem + stage * C::STAGE_BYTES);
@@ -224,31 +272,43 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 #pragma unroll
                     for (int k = 0; k < BK / UMMA_K; ++k) {
                         const uint32_t accumulate = GROUP ? (k > 0) : (kb > 0 || k > 0);
-                        mma_f8f6f4(d_tmem, smem_desc_k_sw128(a_addr + k * UMMA_K),
-                                   smem_desc_k_sw128(b_addr + k * UMMA_K), idesc, accumulate);
+                        const uint64_t ad = smem_desc_k_sw128(a_addr + k * UMMA_K);
+                        const uint64_t bd = smem_desc_k_sw128(b_addr + k * UMMA_K);
+                        if constexpr (PAIR) mma_f8f6f4_pair(d_tmem, ad, bd, idesc, accumulate);
+                        else mma_f8f6f4(d_tmem, ad, bd, idesc, accumulate);
                     }
-                    mma_commit(smem_u32(&ctl.empty[stage]));  // stage free once these MMAs finish
+                    // the stage is free (in both CTAs of a pair) once these MMAs finish
+                    if constexpr (PAIR) mma_commit_pair_mc(smem_u32(&empty[stage]), 0x3);
+                    else mma_commit(smem_u32(&empty[stage]));
                     if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
                     if (GROUP) {
-                        mma_commit(smem_u32(&ctl.tfull[acc]));
+                        mma_commit(smem_u32(&tfull[acc]));
                         acc ^= 1;
                         if (acc == 0) acc_phase ^= 1u;
                     }
                 }
                 if (!GROUP && ok) {
-                    mma_commit(smem_u32(&ctl.tfull[acc]));  // accumulator ready for the epilogue
+                    // accumulator ready for the epilogue(s)
+                    if constexpr (PAIR) mma_commit_pair_mc(smem_u32(&tfull[acc]), 0x3);
+                    else mma_commit(smem_u32(&tfull[acc]));
                     acc ^= 1;
                     if (acc == 0) acc_phase ^= 1u;
                 }
             }
             // all MMAs of this thread complete before TMEM is released
-            mma_commit(smem_u32(ctl.drain));
-            wait_phase_drain(ctl.drain, 0);
+            if constexpr (PAIR) mma_commit_pair(smem_u32(drain));
+            else mma_commit(smem_u32(drain));
+            wait_phase_drain(drain, 0);
         }
     } else {
         // ---------------------------------------------------------- epilogue
         const int q = warp & 3;  // TMEM lane quarter this warp may access
         const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+        // drained accumulators are reported to the leader's barrier
+        const uint32_t tempty0 = PAIR ? mapa_shared(smem_u32(&tempty[0]), 0) : smem_u32(&tempty[0]);
+        const uint32_t tempty1 = PAIR ? mapa_shared(smem_u32(&tempty[1]), 0) : smem_u32(&tempty[1]);
+        uint8_t* warp_stage = epi_stage + (warp - 2) * 2 * kEpiChunkBytes;
+        int nchunk = 0;
         int acc = 0;
         uint32_t acc_phase = 0;
         bool ok = true;
@@ -256,11 +316,12 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         if (!GROUP) inv = 1.0f / (__ldg(scale_a) * __ldg(scale_b));
         const int64_t kg = K / BK;                    // group mode: K % 128 == 0
         const int64_t ng = (N + 127) / 128;
-        for (int64_t tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+        for (int64_t tile = first_tile; tile < num_tiles && ok; tile += tile_stride) {
             const int64_t m_blk = tile / num_n, n_blk = tile % num_n;
-            const int64_t row = m_blk * BM + q * 32 + lane;
+            const int64_t row0 = m_blk * C::TILE_M + rank * BM + q * 32;  // this warp's first row
+            const int64_t row = row0 + lane;
             if (!GROUP) {
-                ok = wait_phase(&ctl.tfull[acc], acc_phase, abort_flag, status);
+                ok = wait_phase(&tfull[acc], acc_phase, abort_flag, status);
                 ok = __all_sync(0xFFFFFFFFu, ok);
                 if (!ok) break;
                 tc_fence_after();
@@ -272,11 +333,15 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     float v[32];
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]) * inv;
-                    store_bf16x32(D, row, n_blk * BN + c * 32, M, N, v);
+                    epi_store_chunk(&tmD, warp_stage, nchunk, lane, v, static_cast<int32_t>(n_blk * BN + c * 32),
+                                    static_cast<int32_t>(row0), M, N);
                 }
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&ctl.tempty[acc]));
+                if (lane == 0) {
+                    if constexpr (PAIR) mbar_arrive_cluster(acc ? tempty1 : tempty0);
+                    else mbar_arrive(acc ? tempty1 : tempty0);
+                }
                 acc ^= 1;
                 if (acc == 0) acc_phase ^= 1u;
             } else {
@@ -288,7 +353,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     const float sa = __ldg(scale_a + srow * kg + kb);
                     const float sb = __ldg(scale_b + kb * ng + n_blk);
                     const float ginv = 1.0f / (sa * sb);
-                    ok = wait_phase(&ctl.tfull[acc], acc_phase, abort_flag, status);
+                    ok = wait_phase(&tfull[acc], acc_phase, abort_flag, status);
                     ok = __all_sync(0xFFFFFFFFu, ok);
                     if (!ok) break;
                     tc_fence_after();
@@ -302,7 +367,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     }
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(smem_u32(&ctl.tempty[acc]));
+                    if (lane == 0) mbar_arrive(acc ? tempty1 : tempty0);
                     acc ^= 1;
                     if (acc == 0) acc_phase ^= 1u;
                 }
@@ -312,17 +377,25 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     float v[32];
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v[j] = sum[c * 32 + j];
-                    store_bf16x32(D, row, n_blk * BN + c * 32, M, N, v);
+                    epi_store_chunk(&tmD, warp_stage, nchunk, lane, v, static_cast<int32_t>(n_blk * BN + c * 32),
+                                    static_cast<int32_t>(row0), M, N);
                 }
             }
         }
+        // every store has finished reading shared memory and writing D
+        if (lane == 0) bulk_wait_group_all();
+        __syncwarp();
     }
 
     tc_fence_before();
     __syncthreads();
+    // a pair frees TMEM only after the leader's MMAs into both CTAs drained and
+    // no arrival to the leader's barriers is still in flight
+    if constexpr (PAIR) cluster_sync_all();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, C::TMEM_COLS);
+        if constexpr (PAIR) tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+        else tmem_dealloc(tmem_base, C::TMEM_COLS);
     }
 }
 
@@ -356,39 +429,133 @@ bool make_kmajor_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K
     return r == CUDA_SUCCESS;
 }
 
-template <int BN, bool GROUP>
+// BF16 output D [rows, cols]: box = 32 columns x 32 rows, 64-byte swizzle (stores).
+bool make_out_map(CUtensorMap* map, void* base, int64_t rows, int64_t cols) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * 2)};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                    CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+struct LaunchInfo {
+    cudaError_t attr_err = cudaSuccess;
+    int max_clusters = 0;  // co-resident 2-CTA clusters (PAIR only)
+};
+
+template <int BN, bool GROUP, bool PAIR>
+const LaunchInfo& launch_info() {
+    using C = Cfg<BN, PAIR>;
+    static LaunchInfo info;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        auto kern = fp8_gemm_kernel<BN, GROUP, PAIR>;
+        info.attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+        if (PAIR && info.attr_err == cudaSuccess) {
+            cudaLaunchConfig_t cfg = {};
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = 2;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.gridDim = dim3(2 * sm_count());
+            cfg.blockDim = dim3(kThreadsGemm);
+            cfg.dynamicSmemBytes = C::SMEM_BYTES;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+                (void)cudaGetLastError();
+                n = 0;
+            }
+            info.max_clusters = n;
+        }
+    });
+    return info;
+}
+
+template <int BN, bool GROUP, bool PAIR>
 int launch_gemm(const void* a, const void* b, const float* sa, const float* sb, void* d, int64_t M,
                 int64_t N, int64_t K, uint32_t afmt, uint32_t bfmt, int* status, cudaStream_t stream) {
-    using C = Cfg<BN>;
-    static std::once_flag attr_once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(fp8_gemm_kernel<BN, GROUP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        C::SMEM_BYTES);
-    });
-    if (attr_err != cudaSuccess) return FP8Q_ERR_CUDA;
-    alignas(64) CUtensorMap mapA, mapB;
-    if (!make_kmajor_map(&mapA, a, M, K, BM) || !make_kmajor_map(&mapB, b, N, K, BN)) return FP8Q_ERR_CUDA;
-    const int64_t tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
-    const int grid = static_cast<int>(std::min<int64_t>(tiles, sm_count()));
-    const uint32_t idesc = idesc_f8(afmt, bfmt, BM, BN);
-    fp8_gemm_kernel<BN, GROUP><<<grid, kThreadsGemm, C::SMEM_BYTES, stream>>>(
-        mapA, mapB, sa, sb, static_cast<__nv_bfloat16*>(d), M, N, K, idesc, status);
+    using C = Cfg<BN, PAIR>;
+    const LaunchInfo& info = launch_info<BN, GROUP, PAIR>();
+    if (info.attr_err != cudaSuccess) return FP8Q_ERR_CUDA;
+    alignas(64) CUtensorMap mapA, mapB, mapD;
+    if (!make_kmajor_map(&mapA, a, M, K, BM) || !make_kmajor_map(&mapB, b, N, K, C::B_ROWS) ||
+        !make_out_map(&mapD, d, M, N))
+        return FP8Q_ERR_CUDA;
+    const int64_t tiles = ((M + C::TILE_M - 1) / C::TILE_M) * ((N + BN - 1) / BN);
+    const uint32_t idesc = idesc_f8(afmt, bfmt, C::MMA_M, BN);
+    auto kern = fp8_gemm_kernel<BN, GROUP, PAIR>;
+    if constexpr (PAIR) {
+        if (info.max_clusters < 1) return FP8Q_ERR_CUDA;
+        const int clusters = static_cast<int>(std::min<int64_t>(tiles, info.max_clusters));
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.gridDim = dim3(2 * clusters);
+        cfg.blockDim = dim3(kThreadsGemm);
+        cfg.dynamicSmemBytes = C::SMEM_BYTES;
+        cfg.stream = stream;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, kern, mapA, mapB, mapD, sa, sb, M, N, K, idesc, status) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return FP8Q_ERR_CUDA;
+        }
+    } else {
+        const int grid = static_cast<int>(std::min<int64_t>(tiles, sm_count()));
+        kern<<<grid, kThreadsGemm, C::SMEM_BYTES, stream>>>(mapA, mapB, mapD, sa, sb, M, N, K, idesc, status);
+    }
     FP8Q_CHECK_LAUNCH();
     return FP8Q_OK;
 }
 
-// Tile width: the candidate with the least work on the busiest SM
-// (ceil(tiles / SMs) * BN); ties go to the wider tile.
-int pick_bn(int64_t M, int64_t N) {
-    const int cands[] = {256, 192, 160, 128};
+// Tile shape.  A tile's time depends only weakly on its width (the tensor
+// core is much less efficient on narrow tiles), so each candidate is scored
+// as (tiles per SM or SM pair, rounded up) x its measured time per tile.  The
+// per-tile times are relative to the 2-SM 256-wide tile, from sweeps of this
+// kernel over the workloads' shapes on GB300 (K-bound runs, TFLOP/s per tile
+// width); ties go to the earlier candidate.
+struct Shape {
+    bool pair;
+    int bn;
+};
+
+// fp8q_gemm_set_tile: -1 = automatic, else (pair << 16) | bn
+std::atomic<int> g_tile_override{-1};
+
+Shape pick_shape(int64_t M, int64_t N) {
+    const int ov = g_tile_override.load(std::memory_order_relaxed);
+    if (ov >= 0) {
+        const bool pair = (ov >> 16) != 0;
+        const int bn = ov & 0xFFFF;
+        if (!pair || M > BM) return Shape{pair, bn};
+        return Shape{false, bn == 224 ? 256 : bn};
+    }
+    struct Cand { bool pair; int bn; double t; };
+    static constexpr Cand kCands[] = {
+        {true, 256, 1.000}, {true, 224, 0.946}, {true, 192, 0.909}, {true, 160, 0.837}, {true, 128, 0.858},
+        {false, 192, 0.897}, {false, 160, 0.834}, {false, 128, 0.843}, {false, 256, 1.102},
+    };
     const int64_t sms = sm_count();
-    int best = 128;
-    int64_t best_cost = -1;
-    for (int bn : cands) {
-        const int64_t tiles = ((M + BM - 1) / BM) * ((N + bn - 1) / bn);
-        const int64_t cost = ((tiles + sms - 1) / sms) * bn;
-        if (best_cost < 0 || cost < best_cost) { best_cost = cost; best = bn; }
+    Shape best{false, 128};
+    double best_cost = -1.0;
+    for (const Cand& c : kCands) {
+        if (c.pair && M <= BM) continue;
+        const int64_t tile_m = c.pair ? 2 * BM : BM;
+        const int64_t units = c.pair ? sms / 2 : sms;
+        const int64_t tiles = ((M + tile_m - 1) / tile_m) * ((N + c.bn - 1) / c.bn);
+        const double cost = static_cast<double>((tiles + units - 1) / units) * c.t;
+        if (best_cost < 0 || cost < best_cost) { best_cost = cost; best = Shape{c.pair, c.bn}; }
     }
     return best;
 }
@@ -396,12 +563,22 @@ int pick_bn(int64_t M, int64_t N) {
 int gemm_dispatch(const void* a, const void* b, const float* sa, const float* sb, int group, void* d,
                   int64_t M, int64_t N, int64_t K, uint32_t afmt, uint32_t bfmt, int* status,
                   cudaStream_t stream) {
-    if (group) return launch_gemm<128, true>(a, b, sa, sb, d, M, N, K, afmt, bfmt, status, stream);
-    switch (pick_bn(M, N)) {
-        case 256: return launch_gemm<256, false>(a, b, sa, sb, d, M, N, K, afmt, bfmt, status, stream);
-        case 192: return launch_gemm<192, false>(a, b, sa, sb, d, M, N, K, afmt, bfmt, status, stream);
-        case 160: return launch_gemm<160, false>(a, b, sa, sb, d, M, N, K, afmt, bfmt, status, stream);
-        default: return launch_gemm<128, false>(a, b, sa, sb, d, M, N, K, afmt, bfmt, status, stream);
+    if (group) return launch_gemm<128, true, false>(a, b, sa, sb, d, M, N, K, afmt, bfmt, status, stream);
+    const Shape s = pick_shape(M, N);
+    if (s.pair) {
+        switch (s.bn) {
+            case 256: return launch_gemm<256, false, true>(a, b, sa, sb, d, M, N, K, afmt, bfmt, status, stream);
+            case 224: return launch_gemm<224, false, true>(a, b, sa, sb, d, M, N, K, afmt, bfmt, status, stream);
+            case 192: return launch_gemm<192, false, true>(a, b, sa, sb, d, M, N, K, afmt, bfmt, status, stream);
+            case 160: return launch_gemm<160, false, true>(a, b, sa, sb, d, M, N, K, afmt, bfmt, status, stream);
+            default: return launch_gemm<128, false, true>(a, b, sa, sb, d, M, N, K, afmt, bfmt, status, stream);
+        }
+    }
+    switch (s.bn) {
+        case 256: return launch_gemm<256, false, false>(a, b, sa, sb, d, M, N, K, afmt, bfmt, status, stream);
+        case 192: return launch_gemm<192, false, false>(a, b, sa, sb, d, M, N, K, afmt, bfmt, status, stream);
+        case 160: return launch_gemm<160, false, false>(a, b, sa, sb, d, M, N, K, afmt, bfmt, status, stream);
+        default: return launch_gemm<128, false, false>(a, b, sa, sb, d, M, N, K, afmt, bfmt, status, stream);
     }
 }
 
@@ -410,7 +587,7 @@ int check_gemm_args(const void* a, const void* b, const float* sa, const float* 
     if (!b || !sa || !sb) return FP8Q_ERR_NULL;
     if ((!a || !d) && M != 0) return FP8Q_ERR_NULL;  // an empty A / D may have no storage
     if (M < 0 || N < 16 || K < 16 || N % 16 != 0 || K % 16 != 0) return FP8Q_ERR_SHAPE;
-    if (M > (int64_t(1) << 31) - BM || N > (int64_t(1) << 31) - 256 || K > (int64_t(1) << 31) - BK)
+    if (M > (int64_t(1) << 31) - 2 * BM || N > (int64_t(1) << 31) - 256 || K > (int64_t(1) << 31) - BK)
         return FP8Q_ERR_SHAPE;
     if (!aligned16(a) || !aligned16(b) || !aligned16(d)) return FP8Q_ERR_ALIGN;
     if ((reinterpret_cast<uintptr_t>(sa) | reinterpret_cast<uintptr_t>(sb) |
@@ -425,6 +602,18 @@ int check_gemm_args(const void* a, const void* b, const float* sa, const float* 
 }  // namespace fp8q
 
 using namespace fp8q;
+
+extern "C" int fp8q_gemm_set_tile(int pair, int bn) {
+    if (pair == -1) {
+        g_tile_override.store(-1);
+        return FP8Q_OK;
+    }
+    const bool ok1 = pair == 0 && (bn == 128 || bn == 160 || bn == 192 || bn == 256);
+    const bool ok2 = pair == 1 && (bn == 128 || bn == 160 || bn == 192 || bn == 224 || bn == 256);
+    if (!ok1 && !ok2) return FP8Q_ERR_UNSUPPORTED;
+    g_tile_override.store((pair << 16) | bn);
+    return FP8Q_OK;
+}
 
 extern "C" int fp8_gemm_fwd(const void* x_q, const void* wt_q, const float* scale_x, const float* scale_w,
                             int group_mode, void* y, int64_t M, int64_t N, int64_t K, int* status,

@@ -27,14 +27,16 @@ amax_history_kernel(float* __restrict__ history, int L, int* __restrict__ head,
                     const float* __restrict__ amax_new, float margin, float fmt_max,
                     float* __restrict__ scale_out, int* __restrict__ status) {
     const int lane = threadIdx.x;
-    const int slot = (*head + 1) % L;
+    // the three loads are independent: issue them together
+    const int h0 = *head;
     const float a_new = *amax_new;
-    __syncwarp();
+    float first = lane < L ? history[lane] : 0.0f;
+    const int slot = (h0 + 1) % L;
     // |x| as an ordered key: bit patterns of non-negative floats sort like the
     // floats, and a NaN magnitude sorts above infinity
     uint32_t key = 0;
     for (int i = lane; i < L; i += 32) {
-        const float v = (i == slot) ? a_new : history[i];
+        const float v = (i == slot) ? a_new : (i == lane ? first : history[i]);
         key = max(key, __float_as_uint(v) & 0x7FFFFFFFu);
     }
     key = __reduce_max_sync(0xFFFFFFFFu, key);

@@ -210,14 +210,20 @@ quant_tile_kernel(const uint16_t* __restrict__ h, int64_t M, int64_t K, const fl
     uint4 a[8];
     uint32_t m16[8];
     uint32_t amax2 = 0, nsat = 0;
+    // all eight loads are issued before any store, so they overlap in flight
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+        const int c = it * kThreads + tid;
+        const int64_t row = row0 + (c >> 4), col = col0 + (c & 15) * 8;
+        a[it] = (row < M && col < K) ? ld_stream_v4(h + row * K + col) : make_uint4(0, 0, 0, 0);
+    }
 #pragma unroll
     for (int it = 0; it < 8; ++it) {
         const int c = it * kThreads + tid;
         const int64_t row = row0 + (c >> 4), col = col0 + (c & 15) * 8;
         const bool ok = row < M && col < K;
-        uint4 x = ok ? ld_stream_v4(h + row * K + col) : make_uint4(0, 0, 0, 0);
         uint32_t m2 = 0;
-        a[it] = act8<ACT>(x, m2);
+        a[it] = act8<ACT>(a[it], m2);
         m16[it] = max16x2(m2);
         amax2 = __vmaxu2(amax2, m2);
         if (ok && act_out) st_stream_v4(act_out + row * K + col, a[it]);

@@ -70,6 +70,7 @@ class Fp8DownProj:
         self.y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
         self.sat = torch.zeros(1, dtype=torch.int64, device=dev)
         self.gemm_status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self._side = torch.cuda.Stream(device=dev)  # the weight branch of a step
         if group:
             if K % B.GROUP or N % B.GROUP:
                 raise ValueError("group scales need K % 128 == 0 and N % 128 == 0")
@@ -113,13 +114,57 @@ class Fp8DownProj:
             self.x.update()
             self.w.update()
 
-    def step(self, H: torch.Tensor, W: torch.Tensor) -> torch.Tensor:
-        """One forward step: cast W, fused quantize of H, FP8 GEMM, history update."""
-        self.cast_weight(W)
+    PHASE_EVENTS = ("start", "w_cast_start", "w_cast_end", "quant_end", "gemm_start", "gemm_end", "end")
+
+    def step(self, H: torch.Tensor, W: torch.Tensor, events=None) -> torch.Tensor:
+        """One forward step: cast W, fused quantize of H, FP8 GEMM, history update.
+
+        Two branches: the weight cast runs on a side stream while the fused
+        quantize runs on the current stream; the GEMM waits for both; then the
+        two history updates run side by side.  ``events``: optional dict of
+        CUDA events keyed by PHASE_EVENTS, recorded at the phase boundaries."""
+        ev = events or {}
+        main, side = torch.cuda.current_stream(), self._side
+
+        def mark(key):
+            if key in ev:
+                ev[key].record()
+
+        mark("start")
+        side.wait_stream(main)
+        with torch.cuda.stream(side):
+            mark("w_cast_start")
+            self.cast_weight(W)
+            mark("w_cast_end")
         self.quantize(H)
+        mark("quant_end")
+        main.wait_stream(side)
+        mark("gemm_start")
         y = self.gemm()
-        self.update_scales()
+        mark("gemm_end")
+        if not self.group:
+            side.wait_stream(main)
+            with torch.cuda.stream(side):
+                self.w.update()
+            self.x.update()
+            main.wait_stream(side)
+        mark("end")
         return y
+
+    @staticmethod
+    def phase_ms(ev: dict) -> dict:
+        """Durations (ms) of the phases from events recorded by step()."""
+        return {
+            "w_cast": ev["w_cast_start"].elapsed_time(ev["w_cast_end"]),
+            "quant": ev["start"].elapsed_time(ev["quant_end"]),
+            "gemm": ev["gemm_start"].elapsed_time(ev["gemm_end"]),
+            "history": ev["gemm_end"].elapsed_time(ev["end"]),
+            "step": ev["start"].elapsed_time(ev["end"]),
+        }
+
+    def capture(self, H: torch.Tensor, W: torch.Tensor, timed: bool = False) -> "StepGraph":
+        """Capture one step on fixed H / W buffers as a CUDA graph (see StepGraph)."""
+        return StepGraph(self, H, W, timed)
 
     def calibrate(self, H: torch.Tensor, W: torch.Tensor) -> None:
         """Bootstrap the delayed scales from step 0's own tensors (one amax pass each).
@@ -134,3 +179,37 @@ class Fp8DownProj:
         self.quantize(H)
         self.x.update()
         self.w.update()
+
+
+class StepGraph:
+    """One down-projection step captured as a CUDA graph.
+
+    All buffers are allocated beforehand, so replaying the graph re-runs the
+    same kernels on the same device pointers with no host work between them.
+    The delayed scales live in device memory, so consecutive replays carry
+    the amax history forward exactly as eager steps do.  Run at least one
+    eager step first (it performs the one-time per-kernel set-up).
+
+    timed=True records CUDA events inside the graph (external event nodes)
+    at the phase boundaries of the step; ``phase_ms()`` reads them after a
+    replay has completed.
+    """
+
+    def __init__(self, dp: Fp8DownProj, H: torch.Tensor, W: torch.Tensor, timed: bool = False):
+        self.events = None
+        if timed:
+            self.events = {k: torch.cuda.Event(enable_timing=True, external=True) for k in dp.PHASE_EVENTS}
+        self.graph = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            with torch.cuda.graph(self.graph, stream=side):
+                self.y = dp.step(H, W, self.events)
+        torch.cuda.current_stream().wait_stream(side)
+
+    def replay(self) -> torch.Tensor:
+        self.graph.replay()
+        return self.y
+
+    def phase_ms(self) -> dict:
+        return Fp8DownProj.phase_ms(self.events)

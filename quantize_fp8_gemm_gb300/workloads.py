@@ -140,11 +140,17 @@ def dy_grad(w: Workload) -> np.ndarray:
     return to_bf16_bits(x).reshape(w.M, w.N)
 
 
-def sample_rows(M: int, n: int, seed: int, tile: int = 128) -> np.ndarray:
-    """A seeded, sorted set of output rows: n random rows plus every tile edge."""
+def sample_rows(M: int, n: int, seed: int, tile: int = 128, edge_tiles: int = 8) -> np.ndarray:
+    """A seeded, sorted set of output rows: n random rows plus the first and
+    last row of a few 128-row tiles (the first two, the last two and up to
+    edge_tiles - 4 random ones)."""
     rng = np.random.default_rng(np.random.SeedSequence([seed, 99]))
+    ntiles = (M + tile - 1) // tile
+    picks = {0, 1, ntiles - 2, ntiles - 1}
+    if ntiles > 4:
+        picks |= set(rng.choice(ntiles, size=min(ntiles, max(0, edge_tiles - 4)), replace=False).tolist())
     edges = []
-    for t in range(0, M, tile):
-        edges += [t, min(M - 1, t + tile - 1)]
+    for t in sorted(p for p in picks if 0 <= p < ntiles):
+        edges += [t * tile, min(M - 1, t * tile + tile - 1)]
     pick = rng.choice(M, size=min(n, M), replace=False)
     return np.unique(np.concatenate([pick, np.array(edges, dtype=np.int64)])).astype(np.int64)

@@ -122,3 +122,12 @@ def test_binding_refuses_host_tensors(lib):
     h = torch.zeros(16, 16, dtype=torch.bfloat16)
     with pytest.raises(TypeError):
         B.fp8_quant_fused(h, B.ACT_RELU2, B.E4M3, torch.ones(1))
+
+
+def test_gemm_tile_knob_arguments(lib):
+    assert lib.fp8q_gemm_set_tile(0, 96) == ERR_UNSUPPORTED
+    assert lib.fp8q_gemm_set_tile(0, 224) == ERR_UNSUPPORTED
+    assert lib.fp8q_gemm_set_tile(2, 128) == ERR_UNSUPPORTED
+    assert lib.fp8q_gemm_set_tile(1, 224) == OK
+    assert lib.fp8q_gemm_set_tile(0, 160) == OK
+    assert lib.fp8q_gemm_set_tile(-1, 0) == OK

@@ -123,3 +123,30 @@ def test_constant_sign_long_contraction():
     Yr, S = O.gemm_fwd(xq, wq, 1.0, 1.0)
     y = run_fwd(xq, wq, 1.0, 1.0)
     assert_gemm_close(y, Yr, S)
+
+
+TILES = [(0, 128), (0, 160), (0, 192), (0, 256), (1, 128), (1, 160), (1, 192), (1, 224), (1, 256)]
+
+
+@pytest.mark.parametrize("pair,bn", TILES)
+def test_every_tile_shape_on_ragged_problems(pair, bn):
+    """Each tile shape (1-CTA and 2-SM pair, every width) on problems whose M, N
+    and K all leave partial tiles, forward and dgrad."""
+    try:
+        B.fp8q_gemm_set_tile(pair, bn)
+        for M, N, K in [(1000, 1600, 640), (300, 272, 400), (129, 144, 1600), (513, 96, 48)]:
+            xq = rand_e4m3((M, K), seed=M + 7 * N + K, scale=30.0)
+            wq = rand_e4m3((K, N), seed=3 * M + N + K, scale=30.0)
+            Yr, S = O.gemm_fwd(xq, wq, 2.5, 0.5)
+            assert_gemm_close(run_fwd(xq, wq, 2.5, 0.5), Yr, S)
+        M, N, K = 520, 160, 400
+        rng = np.random.default_rng(pair * 1000 + bn)
+        dyq = _codes(rng.standard_normal((M, N)) * 1000.0, O.E5M2)
+        wq = rand_e4m3((K, N), seed=bn, scale=50.0)
+        Dr, Sd = O.gemm_dgrad(dyq, wq, 1024.0, 5.0)
+        dx = torch.empty(M, K, dtype=torch.bfloat16, device="cuda")
+        B.fp8_gemm_dgrad(dev_u8(dyq), dev_u8(wq), dev_f32(1024.0), dev_f32(5.0), dx)
+        torch.cuda.synchronize()
+        assert_gemm_close(dx, Dr, Sd)
+    finally:
+        B.fp8q_gemm_set_tile(-1)

@@ -1,0 +1,171 @@
+"""Multi-step delayed scaling on the GPU against the oracle's recurrence.
+
+Each step: the fused quantize runs with the scale the history produced, then
+the history takes this step's amax.  Scales, amax, saturation counts and FP8
+bytes must equal the oracle's bit for bit at every step ("Paradigma Details
+FP8 and Optimizer Tricks Behind NanoGPT Records", second paragraph: previous
+step's amax times a margin; "FP8 Training & Inference", Delayed Scaling).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from quantize_fp8_gemm_gb300 import binding as B
+from quantize_fp8_gemm_gb300 import workloads as WL
+from quantize_fp8_gemm_gb300.downproj import Fp8DownProj
+from tests.parity import assert_gemm_close, host_u8
+
+pytestmark = pytest.mark.gpu
+
+
+class OracleRecurrence:
+    """The oracle's side of the delayed-scaling loop for one tensor."""
+
+    def __init__(self, L, margin, fmt=O.E4M3):
+        self.hist = np.zeros(L, np.float32)
+        self.head = 0
+        self.scale = 1.0
+        self.margin, self.fmt = margin, fmt
+
+    def push(self, amax):
+        st, self.hist, self.head, self.scale = O.history_update(self.hist, self.head, amax, self.margin,
+                                                                self.fmt, self.scale)
+        return st
+
+
+def test_gpt2s_ten_steps_fresh_inputs():
+    w = WL.WORKLOADS["gpt2s"]
+    W_bits = WL.w_down(w)
+    H0 = WL.h_preact(w, 0)
+    dp = Fp8DownProj(w.M, w.K, w.N, margin=w.margin, history_len=w.history_len)
+    Wd = WL.bf16_tensor(W_bits).cuda()
+    dp.calibrate(WL.bf16_tensor(H0).cuda(), Wd)
+    ox, ow = OracleRecurrence(w.history_len, w.margin), OracleRecurrence(w.history_len, w.margin)
+    ox.push(O.amax(H0, O.ACT_RELU2))
+    ow.push(O.amax(W_bits, O.ACT_IDENTITY))
+    rows = WL.sample_rows(w.M, 64, seed=11)
+    for t in range(w.steps):
+        h = WL.h_preact(w, t)
+        sx_used, sw_used = float(dp.x.scale.item()), float(dp.w.scale.item())
+        assert (sx_used, sw_used) == (ox.scale, ow.scale), f"step {t}"
+        y = dp.step(WL.bf16_tensor(h).cuda(), Wd)
+        torch.cuda.synchronize()
+        rx = O.quant(h, O.ACT_RELU2, O.E4M3, ox.scale)
+        assert np.array_equal(host_u8(dp.x_q), rx["q"]), f"step {t}: E4M3 codes"
+        assert int(dp.sat.item()) == rx["sat"], f"step {t}: saturations"
+        assert float(dp.x.history[0].item()) == rx["amax"], f"step {t}: amax"
+        if t in (0, w.steps - 1):
+            rw = O.quant(W_bits, O.ACT_IDENTITY, O.E4M3, ow.scale, want_act=False)
+            Yr, S = O.gemm_fwd(rx["q"][rows], rw["q"], ox.scale, ow.scale)
+            assert_gemm_close(y, Yr, S, rows=rows)
+        ox.push(rx["amax"])
+        ow.push(O.amax(W_bits, O.ACT_IDENTITY))
+    assert int(dp.x.status.item()) == 0 and int(dp.gemm_status.item()) == 0
+
+
+def test_gpt2s_batch_drift_and_saturation():
+    """20 steps with the std of H drifting 1.0 -> 1.5: the delayed scale lags,
+    so saturations appear; each step's count must match the oracle exactly and
+    is zero whenever this step's amax stays below margin x the previous one."""
+    w = WL.WORKLOADS["gpt2s_batch"]
+    W_bits = WL.w_down(w)
+    Wd = WL.bf16_tensor(W_bits).cuda()
+    dp = Fp8DownProj(w.M, w.K, w.N, margin=w.margin, history_len=w.history_len, keep_act=False)
+    H0 = WL.h_preact(w, 0, WL.drift_std(w, 0))
+    dp.calibrate(WL.bf16_tensor(H0).cuda(), Wd)
+    ox = OracleRecurrence(w.history_len, w.margin)
+    ox.push(O.amax(H0, O.ACT_RELU2))
+    prev_amax = ox.hist[ox.head]
+    rows = WL.sample_rows(w.M, 48, seed=12)
+    for t in range(w.steps):
+        h = WL.h_preact(w, t, WL.drift_std(w, t))
+        assert float(dp.x.scale.item()) == ox.scale, f"step {t}"
+        dp.quantize(WL.bf16_tensor(h).cuda())
+        dp.update_scales()
+        torch.cuda.synchronize()
+        rx = O.quant(h, O.ACT_RELU2, O.E4M3, ox.scale, want_act=False)
+        assert int(dp.sat.item()) == rx["sat"], f"step {t}: saturations"
+        assert float(dp.x.history[0].item()) == rx["amax"], f"step {t}: amax"
+        q = host_u8(dp.x_q)
+        assert np.array_equal(q[rows], rx["q"][rows]), f"step {t}: codes"
+        if rx["amax"] < w.margin * prev_amax:
+            assert rx["sat"] == 0
+        prev_amax = rx["amax"]
+        ox.push(rx["amax"])
+
+
+def test_checkpoint_resume_is_bit_identical():
+    """The only state is the device history / head / scale: save after step 5,
+    restore into a fresh instance, and steps 6-9 repeat bit for bit."""
+    w = WL.WORKLOADS["gpt2s"]
+    M, K, N = 1024, w.K, w.N
+    W_bits = WL.w_down(w)
+    Wd = WL.bf16_tensor(W_bits).cuda()
+    hs = [WL.bf16_tensor(WL.h_preact(w, t)[:M]).cuda() for t in range(10)]
+    a = Fp8DownProj(M, K, N, margin=w.margin, history_len=3)
+    a.calibrate(hs[0], Wd)
+    saved = None
+    outs_a = []
+    for t in range(10):
+        y = a.step(hs[t], Wd).clone()
+        if t == 5:
+            saved = {k: (getattr(a, r).history.clone(), getattr(a, r).head.clone(), getattr(a, r).scale.clone())
+                     for k, r in (("x", "x"), ("w", "w"))}
+        if t > 5:
+            outs_a.append((y, a.x_q.clone()))
+    b = Fp8DownProj(M, K, N, margin=w.margin, history_len=3)
+    for r in ("x", "w"):
+        hist, head, scale = saved[r]
+        getattr(b, r).history.copy_(hist)
+        getattr(b, r).head.copy_(head)
+        getattr(b, r).scale.copy_(scale)
+    for i, t in enumerate(range(6, 10)):
+        y = b.step(hs[t], Wd)
+        torch.cuda.synchronize()
+        assert torch.equal(y.view(torch.int16), outs_a[i][0].view(torch.int16))
+        assert torch.equal(b.x_q, outs_a[i][1])
+
+
+def test_graph_replay_matches_eager_steps():
+    w = WL.WORKLOADS["gpt2s"]
+    M, K, N = 2048, w.K, w.N
+    Wd = WL.bf16_tensor(WL.w_down(w)).cuda()
+    hs = [WL.bf16_tensor(WL.h_preact(w, t)[:M]).cuda() for t in range(4)]
+    e = Fp8DownProj(M, K, N, margin=w.margin)
+    g = Fp8DownProj(M, K, N, margin=w.margin)
+    e.calibrate(hs[0], Wd)
+    g.calibrate(hs[0], Wd)
+    g.step(hs[0], Wd)  # one eager step on each before capture
+    e.step(hs[0], Wd)
+    buf = torch.empty_like(hs[0])
+    graph = g.capture(buf, Wd)
+    for t in range(1, 4):
+        ye = e.step(hs[t], Wd)
+        buf.copy_(hs[t])
+        yg = graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(ye.view(torch.int16), yg.view(torch.int16)), f"step {t}"
+        assert torch.equal(e.x.scale, g.x.scale)
+
+
+def test_bad_amax_keeps_scale_and_flags():
+    hist = torch.zeros(1, device="cuda")
+    head = torch.zeros(1, dtype=torch.int32, device="cuda")
+    scale = torch.full((1,), 7.0, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for bad in (0.0, float("inf"), float("nan")):
+        B.amax_history_update(hist, head, torch.tensor([bad], device="cuda"), 2.0, B.E4M3, scale, status=st)
+        torch.cuda.synchronize()
+        assert scale.item() == 7.0
+        assert st.item() & B.DEV_BAD_AMAX
+    # a ring of 4: window max and head match the oracle
+    hist = torch.zeros(4, device="cuda")
+    head = torch.zeros(1, dtype=torch.int32, device="cuda")
+    o = OracleRecurrence(4, 1.5)
+    for a in [3.0, 100.0, 2.0, 0.5, 0.25, 0.125, 7.0]:
+        B.amax_history_update(hist, head, torch.tensor([a], device="cuda"), 1.5, B.E4M3, scale)
+        o.push(a)
+        torch.cuda.synchronize()
+        assert scale.item() == o.scale and int(head.item()) == o.head
+        assert np.array_equal(hist.cpu().numpy(), o.hist)
