@@ -13,8 +13,8 @@
 //
 // Kernels:
 //   quant_stream_kernel  per-tensor scale, or 1x128 groups; row-major outputs.
-//                        HBM-bound: 16-byte loads/stores, several loads in
-//                        flight per thread, persistent grid over all SMs,
+//                        HBM-bound: 16-byte loads/stores, four loads in
+//                        flight per thread, one pass over the tensor,
 //                        amax by warp reduce -> shared memory -> 1 atomic/CTA.
 //   quant_tile_kernel    128x128 tiles through shared memory: the transposed
 //                        FP8 copy (the weight's K-major GEMM operand) and the
@@ -111,7 +111,8 @@ __device__ __forceinline__ void block_reduce_publish(uint32_t amax16, uint32_t n
 
 // ---------------------------------------------------------------------------
 // Streaming kernel.  GROUP = false: per-tensor scale, each thread owns 8-element
-// chunks (16 B in) on a grid-stride loop, four loads in flight.  GROUP = true:
+// chunks (16 B in), four loads in flight (a grid-stride loop covers grids
+// smaller than the tensor).  GROUP = true:
 // 1x128 groups, a half-warp owns one group (16 lanes x 8 elements), the group
 // amax is a 16-lane shuffle reduction, two groups in flight per half-warp.
 // ---------------------------------------------------------------------------
@@ -303,10 +304,14 @@ int launch_quant(const void* h, int64_t M, int64_t K, const float* scale, void* 
             static_cast<uint8_t*>(q_out), static_cast<uint8_t*>(q_t_out), gscale, group_rows,
             amax_out, sat_count);
     } else {
+        // One pass: enough CTAs that each thread handles one batch of loads
+        // (4 chunks per tensor pass, 2 groups per half-warp); the hardware
+        // refills SMs as CTAs retire.  Measured faster than a persistent
+        // grid-stride grid on GB300 (0.99 vs 0.89 of the copy rate at 4 GB).
         const int64_t nchunks = M * K / 8;
-        const int64_t per_cta = gscale ? kThreads * 2 : kThreads * 4;  // chunks per CTA per pass
+        const int64_t per_cta = gscale ? kThreads * 2 : kThreads * 4;  // chunks per CTA
         const int64_t want = (nchunks + per_cta - 1) / per_cta;
-        const int64_t cap = static_cast<int64_t>(sm_count()) * (2048 / kThreads);
+        const int64_t cap = int64_t(1) << 30;
         const unsigned grid = static_cast<unsigned>(std::max<int64_t>(1, std::min(want, cap)));
         if (gscale)
             quant_stream_kernel<ACT, FMT, true><<<grid, kThreads, 0, stream>>>(

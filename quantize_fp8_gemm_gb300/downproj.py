@@ -25,22 +25,37 @@ from . import binding as B
 class DelayedScale:
     """Device-resident delayed-scaling state of one tensor role.
 
-    history [L] (ring, newest at ``head``), the scale to use for the next cast,
-    the amax the next cast writes, and a status word for FP8Q_DEV_* flags.
+    history [L] (ring, newest at ``head``), the amax the next cast writes, a
+    status word for FP8Q_DEV_* flags, and two scale slots.  A step casts with
+    the current slot and the GEMM dequantises with it, while the history
+    update writes the next step's scale into the other slot; the two can
+    therefore run concurrently.  ``update()`` then makes the other slot
+    current (a host-side switch).
     """
 
     def __init__(self, fmt: int, margin: float, history_len: int = 1, device="cuda"):
         self.fmt, self.margin, self.L = fmt, float(margin), int(history_len)
         self.history = torch.zeros(self.L, dtype=torch.float32, device=device)
         self.head = torch.zeros(1, dtype=torch.int32, device=device)
-        self.scale = torch.ones(1, dtype=torch.float32, device=device)
+        self.scales = torch.ones(2, dtype=torch.float32, device=device)
+        self.slot = 0
         self.amax = torch.zeros(1, dtype=torch.float32, device=device)
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
 
+    @property
+    def scale(self) -> torch.Tensor:
+        """The scale the next cast uses (a 1-element view of the current slot)."""
+        return self.scales[self.slot:self.slot + 1]
+
     def update(self) -> None:
-        """Push this step's amax; the scale becomes the one for the next step."""
-        B.amax_history_update(self.history, self.head, self.amax, self.margin, self.fmt, self.scale,
+        """Push this step's amax; write the next step's scale into the other
+        slot (which first takes the current scale, kept if the amax is
+        unusable) and make that slot current."""
+        nxt = self.scales[1 - self.slot:2 - self.slot]
+        nxt.copy_(self.scale)
+        B.amax_history_update(self.history, self.head, self.amax, self.margin, self.fmt, nxt,
                               status=self.status)
+        self.slot ^= 1
 
     def seed(self, amax: float) -> None:
         """Start the history from a known previous amax (e.g. a calibration pass)."""
@@ -78,33 +93,37 @@ class Fp8DownProj:
             self.w_gscale = torch.empty(K // B.GROUP, N // B.GROUP, dtype=torch.float32, device=dev)
 
     # -- a7 -------------------------------------------------------------------
-    def cast_weight(self, W: torch.Tensor) -> None:
+    def cast_weight(self, W: torch.Tensor, scale: torch.Tensor | None = None) -> None:
         """W [K,N] BF16 -> W_q^T [N,K] (forward operand) and, if kept, W_q [K,N]."""
+        scale = self.w.scale if scale is None else scale
         if self.group:
             B.fp8_quant_fused(W, B.ACT_IDENTITY, B.E4M3, None, q_out=self.w_q, q_t_out=self.wt_q,
                               amax_out=self.w.amax, group_scales_out=self.w_gscale,
                               group_rows=B.GROUP)
         else:
-            B.fp8_quant_fused(W, B.ACT_IDENTITY, B.E4M3, self.w.scale, q_out=self.w_q,
+            B.fp8_quant_fused(W, B.ACT_IDENTITY, B.E4M3, scale, q_out=self.w_q,
                               q_t_out=self.wt_q, amax_out=self.w.amax)
 
     # -- a1-a5 ----------------------------------------------------------------
-    def quantize(self, H: torch.Tensor) -> None:
+    def quantize(self, H: torch.Tensor, scale: torch.Tensor | None = None) -> None:
+        scale = self.x.scale if scale is None else scale
         if self.group:
             B.fp8_quant_fused(H, self.act, B.E4M3, None, act_out=self.act_bf16, q_out=self.x_q,
                               amax_out=self.x.amax, sat_count=self.sat,
                               group_scales_out=self.x_gscale, group_rows=1)
         else:
-            B.fp8_quant_fused(H, self.act, B.E4M3, self.x.scale, act_out=self.act_bf16,
+            B.fp8_quant_fused(H, self.act, B.E4M3, scale, act_out=self.act_bf16,
                               q_out=self.x_q, amax_out=self.x.amax, sat_count=self.sat)
 
     # -- a9 -------------------------------------------------------------------
-    def gemm(self) -> torch.Tensor:
+    def gemm(self, scale_x: torch.Tensor | None = None, scale_w: torch.Tensor | None = None) -> torch.Tensor:
+        scale_x = self.x.scale if scale_x is None else scale_x
+        scale_w = self.w.scale if scale_w is None else scale_w
         if self.group:
             B.fp8_gemm_fwd(self.x_q, self.wt_q, self.x_gscale, self.w_gscale, self.y, group_mode=1,
                            status=self.gemm_status)
         else:
-            B.fp8_gemm_fwd(self.x_q, self.wt_q, self.x.scale, self.w.scale, self.y,
+            B.fp8_gemm_fwd(self.x_q, self.wt_q, scale_x, scale_w, self.y,
                            status=self.gemm_status)
         return self.y
 
@@ -117,14 +136,16 @@ class Fp8DownProj:
     PHASE_EVENTS = ("start", "w_cast_start", "w_cast_end", "quant_end", "gemm_start", "gemm_end", "end")
 
     def step(self, H: torch.Tensor, W: torch.Tensor, events=None) -> torch.Tensor:
-        """One forward step: cast W, fused quantize of H, FP8 GEMM, history update.
+        """One forward step: cast W, fused quantize of H, FP8 GEMM, history updates.
 
-        Two branches: the weight cast runs on a side stream while the fused
-        quantize runs on the current stream; the GEMM waits for both; then the
-        two history updates run side by side.  ``events``: optional dict of
-        CUDA events keyed by PHASE_EVENTS, recorded at the phase boundaries."""
+        The current stream runs the fused quantize and then the GEMM; a side
+        stream runs the weight cast and its history update beside the
+        quantize, and the activation's history update beside the GEMM (the
+        updates write the other scale slot, so they never race the reads).
+        ``events``: optional dict of CUDA events keyed by PHASE_EVENTS."""
         ev = events or {}
         main, side = torch.cuda.current_stream(), self._side
+        sx, sw = self.x.scale, self.w.scale  # this step's slots
 
         def mark(key):
             if key in ev:
@@ -134,20 +155,23 @@ class Fp8DownProj:
         side.wait_stream(main)
         with torch.cuda.stream(side):
             mark("w_cast_start")
-            self.cast_weight(W)
+            self.cast_weight(W, sw)
             mark("w_cast_end")
-        self.quantize(H)
+            if not self.group:
+                self.w.update()
+        self.quantize(H, sx)
         mark("quant_end")
+        quant_done = torch.cuda.Event()
+        quant_done.record(main)
         main.wait_stream(side)
         mark("gemm_start")
-        y = self.gemm()
+        y = self.gemm(sx, sw)
         mark("gemm_end")
         if not self.group:
-            side.wait_stream(main)
+            side.wait_event(quant_done)
             with torch.cuda.stream(side):
-                self.w.update()
-            self.x.update()
-            main.wait_stream(side)
+                self.x.update()
+        main.wait_stream(side)
         mark("end")
         return y
 
@@ -162,9 +186,10 @@ class Fp8DownProj:
             "step": ev["start"].elapsed_time(ev["end"]),
         }
 
-    def capture(self, H: torch.Tensor, W: torch.Tensor, timed: bool = False) -> "StepGraph":
-        """Capture one step on fixed H / W buffers as a CUDA graph (see StepGraph)."""
-        return StepGraph(self, H, W, timed)
+    def capture(self, H: torch.Tensor, W: torch.Tensor, H_next: torch.Tensor | None = None,
+                timed: bool = False) -> "StepGraph":
+        """Capture the step as CUDA graphs on fixed buffers (see StepGraph)."""
+        return StepGraph(self, H, W, H_next, timed)
 
     def calibrate(self, H: torch.Tensor, W: torch.Tensor) -> None:
         """Bootstrap the delayed scales from step 0's own tensors (one amax pass each).
@@ -173,8 +198,8 @@ class Fp8DownProj:
         seeds each history so step 0 already has a scale."""
         if self.group:
             return
-        self.x.scale.fill_(1.0)
-        self.w.scale.fill_(1.0)
+        self.x.scales.fill_(1.0)
+        self.w.scales.fill_(1.0)
         self.cast_weight(W)
         self.quantize(H)
         self.x.update()
@@ -182,34 +207,58 @@ class Fp8DownProj:
 
 
 class StepGraph:
-    """One down-projection step captured as a CUDA graph.
+    """The down-projection step captured as CUDA graphs.
 
-    All buffers are allocated beforehand, so replaying the graph re-runs the
-    same kernels on the same device pointers with no host work between them.
-    The delayed scales live in device memory, so consecutive replays carry
-    the amax history forward exactly as eager steps do.  Run at least one
-    eager step first (it performs the one-time per-kernel set-up).
+    All buffers are allocated beforehand, so a replay re-runs the same
+    kernels on the same device pointers with no host work between them.
+    Consecutive steps use alternating scale slots, so two graphs are
+    captured (one per slot); ``replay()`` runs the one matching the current
+    slot and switches slots, so replays and eager steps mix freely.  The
+    graph for the slot current at capture reads H, the other H_next
+    (default H).  The amax histories live in
+    device memory, so replays carry the delayed scaling forward exactly as
+    eager steps do.  Run at least one eager step first (it performs the
+    one-time per-kernel set-up).
 
-    timed=True records CUDA events inside the graph (external event nodes)
-    at the phase boundaries of the step; ``phase_ms()`` reads them after a
-    replay has completed.
+    timed=True records CUDA events inside the graphs (external event nodes)
+    at the phase boundaries; ``phase_ms()`` reads those of the last replay
+    once it has completed.  The event nodes themselves add a few
+    microseconds per step.
     """
 
-    def __init__(self, dp: Fp8DownProj, H: torch.Tensor, W: torch.Tensor, timed: bool = False):
-        self.events = None
-        if timed:
-            self.events = {k: torch.cuda.Event(enable_timing=True, external=True) for k in dp.PHASE_EVENTS}
-        self.graph = torch.cuda.CUDAGraph()
+    def __init__(self, dp: Fp8DownProj, H: torch.Tensor, W: torch.Tensor,
+                 H_next: torch.Tensor | None = None, timed: bool = False):
+        self.dp = dp
+        self.slot0 = dp.x.slot  # the scale slot graph 0 reads; graph 1 reads the other
+        self.graphs, self.events = [], []
         side = torch.cuda.Stream()
         side.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.stream(side):
-            with torch.cuda.graph(self.graph, stream=side):
-                self.y = dp.step(H, W, self.events)
+        for h in (H, H if H_next is None else H_next):
+            ev = None
+            if timed:
+                ev = {k: torch.cuda.Event(enable_timing=True, external=True) for k in dp.PHASE_EVENTS}
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(side):
+                with torch.cuda.graph(g, stream=side):
+                    self.y = dp.step(h, W, ev)
+            self.graphs.append(g)
+            self.events.append(ev)
         torch.cuda.current_stream().wait_stream(side)
+        self._next = 0
+        self._last = 0
 
     def replay(self) -> torch.Tensor:
-        self.graph.replay()
+        """Run one step: the graph whose scale slot is current, then switch
+        the host-side slots as an eager step would."""
+        dp = self.dp
+        k = self._next if dp.group else int(dp.x.slot != self.slot0)
+        self.graphs[k].replay()
+        self._last = k
+        self._next = k ^ 1
+        if not dp.group:
+            dp.x.slot ^= 1
+            dp.w.slot ^= 1
         return self.y
 
     def phase_ms(self) -> dict:
-        return Fp8DownProj.phase_ms(self.events)
+        return Fp8DownProj.phase_ms(self.events[self._last])
