@@ -411,6 +411,7 @@ def measure_extras(args, dp, H, Wt, flush, kern_ms, w, dev) -> dict:
     for f in (naive, bf16_gemm, bf16_path):
         f()
     torch.cuda.synchronize()
+    rows = measure_other_rows(w, dev, flush, reps, H[0], Wt)
     t_naive = timed(naive, flush, reps)
     t_bf16_gemm = timed(bf16_gemm, flush, reps)
     t_bf16_path = timed(bf16_path, flush, reps)
@@ -425,7 +426,48 @@ def measure_extras(args, dp, H, Wt, flush, kern_ms, w, dev) -> dict:
         "bf16_path_ms (act write + cuBLAS BF16 GEMM)": t_bf16_path,
         "fp8_path_ms (fused quant + FP8 GEMM)": t_fp8_path,
         "fp8_vs_bf16_end_to_end_speedup": t_bf16_path / t_fp8_path,
+        "other_rows": rows,
     }
+
+
+def measure_other_rows(w, dev, flush, reps, H, Wt) -> dict:
+    """The path's other rows on the same shapes, each kernel alone (L2 flushed):
+    the W cast in both layouts, the E5M2 gradient cast and the dgrad GEMM
+    dX = dY W^T, the 1x128 group quantize and the group-scaled GEMM."""
+    from quantize_fp8_gemm_gb300 import binding as B
+    M, K, N = w.M, w.K, w.N
+    out = {}
+    one = torch.ones(1, device=dev)
+    w_q = torch.empty(K, N, dtype=torch.uint8, device=dev)
+    wt_q = torch.empty(N, K, dtype=torch.uint8, device=dev)
+    amax = torch.zeros(1, device=dev)
+    t = timed(lambda: B.fp8_quant_fused(Wt, B.ACT_IDENTITY, B.E4M3, one, q_out=w_q, q_t_out=wt_q,
+                                        amax_out=amax), flush, reps)
+    out["w_cast_both_layouts"] = {"ms": t, "GB/s": 4.0 * K * N / (t * 1e-3) / 1e9}
+    g = torch.Generator(device=dev).manual_seed(w.seed)
+    dY = (torch.randn(M, N, device=dev, generator=g) * 1e-3).to(torch.bfloat16)
+    dyq = torch.empty(M, N, dtype=torch.uint8, device=dev)
+    sdy = torch.full((1,), 2.0 ** 14, device=dev)
+    t = timed(lambda: B.fp8_quant_fused(dY, B.ACT_IDENTITY, B.E5M2, sdy, q_out=dyq, amax_out=amax),
+              flush, reps)
+    out["dy_cast_e5m2"] = {"ms": t, "GB/s": 3.0 * M * N / (t * 1e-3) / 1e9}
+    dx = torch.empty(M, K, dtype=torch.bfloat16, device=dev)
+    t = timed(lambda: B.fp8_gemm_dgrad(dyq, w_q, sdy, one, dx), flush, reps)
+    out["gemm_dgrad"] = {"ms": t, "TFLOP/s": 2.0 * M * N * K / (t * 1e-3) / 1e12}
+    if K % 128 == 0 and N % 128 == 0:
+        xq = torch.empty(M, K, dtype=torch.uint8, device=dev)
+        act = torch.empty(M, K, dtype=torch.bfloat16, device=dev)
+        gsx = torch.empty(M, K // 128, device=dev)
+        gsw = torch.empty(K // 128, N // 128, device=dev)
+        t = timed(lambda: B.fp8_quant_fused(H, B.ACT_RELU2, B.E4M3, None, act_out=act, q_out=xq, amax_out=amax,
+                                            group_scales_out=gsx, group_rows=1), flush, reps)
+        out["quant_group_1x128"] = {"ms": t, "GB/s": 5.0 * M * K / (t * 1e-3) / 1e9}
+        B.fp8_quant_fused(Wt, B.ACT_IDENTITY, B.E4M3, None, q_t_out=wt_q, amax_out=amax,
+                          group_scales_out=gsw, group_rows=128)
+        y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+        t = timed(lambda: B.fp8_gemm_fwd(xq, wt_q, gsx, gsw, y, group_mode=1), flush, reps)
+        out["gemm_group_scaled"] = {"ms": t, "TFLOP/s": 2.0 * M * N * K / (t * 1e-3) / 1e12}
+    return out
 
 
 def measure_e2e(args, dp, h_bits, w_bits, flush, w, dev, use_graph=True) -> dict:

@@ -117,6 +117,26 @@ int fp8_quant_fused(const void* h, int64_t M, int64_t K, int act, int fmt,
                     float* group_scales_out, int group_rows,
                     cudaStream_t stream);
 
+/* Flags of fp8_quant_fused_ex. */
+#define FP8Q_ACCUMULATE 1 /* fold into amax_out / sat_count instead of zeroing them first */
+
+/*
+ * fp8_quant_fused_ex -- fp8_quant_fused with flags.
+ *
+ * FP8Q_ACCUMULATE: amax_out and sat_count are not zeroed; this call's
+ * maximum and count are folded into the values already there.  A caller that
+ * quantizes a tensor in row blocks (to overlap each block's GEMM with the
+ * next block's quantize) zeroes on the first block and accumulates on the
+ * rest, and the result equals one call over the whole tensor.  flags = 0 is
+ * fp8_quant_fused.  Unknown flag bits give FP8Q_ERR_UNSUPPORTED.
+ */
+int fp8_quant_fused_ex(const void* h, int64_t M, int64_t K, int act, int fmt,
+                       const float* scale,
+                       void* act_out, void* q_out, void* q_t_out,
+                       float* amax_out, unsigned long long* sat_count,
+                       float* group_scales_out, int group_rows,
+                       unsigned flags, cudaStream_t stream);
+
 /*
  * fp8_gemm_fwd -- Y = (X_q . W_q) / (s_x s_w), FP32 accumulation, BF16 out  [gemms][scale]
  *
@@ -192,6 +212,15 @@ int amax_history_update(float* history, int L, int* head, const float* amax_new,
  * Returns FP8Q_ERR_UNSUPPORTED for any other combination (nothing changes).
  */
 int fp8q_gemm_set_tile(int pair, int bn);
+
+/*
+ * fp8q_gemm_test_hold_loads -- failure-path test hook.  While on != 0, the
+ * GEMM kernels launched afterwards issue no operand loads, so their first
+ * bounded wait runs out (after about 2 s): the kernel ORs FP8Q_DEV_TIMEOUT
+ * into the status word, releases its resources and exits, leaving the CUDA
+ * context usable.  Process-wide; turn it off again with on = 0.
+ */
+void fp8q_gemm_test_hold_loads(int on);
 
 /* Human-readable name of an fp8q_status value (static string). */
 const char* fp8q_status_string(int status);

@@ -20,6 +20,7 @@ LIB_PATH = os.path.join(PKG, "libfp8q.so")
 E4M3, E5M2 = 0, 1
 ACT_IDENTITY, ACT_RELU, ACT_RELU2 = 0, 1, 2
 DEV_TIMEOUT, DEV_BAD_AMAX = 1, 2
+ACCUMULATE = 1  # fp8_quant_fused_ex flag
 GROUP = 128
 
 _lib = None
@@ -44,6 +45,7 @@ def lib() -> ctypes.CDLL:
         L = ctypes.CDLL(LIB_PATH)
         P, i64, i32, f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
         L.fp8_quant_fused.argtypes = [P, i64, i64, i32, i32, P, P, P, P, P, P, P, i32, P]
+        L.fp8_quant_fused_ex.argtypes = [P, i64, i64, i32, i32, P, P, P, P, P, P, P, i32, ctypes.c_uint, P]
         L.fp8_gemm_fwd.argtypes = [P, P, P, P, i32, P, i64, i64, i64, P, P]
         L.fp8_gemm_dgrad.argtypes = [P, P, P, P, P, i64, i64, i64, P, P]
         L.amax_history_update.argtypes = [P, i32, P, P, f32, i32, P, P, P]
@@ -53,9 +55,11 @@ def lib() -> ctypes.CDLL:
         L.fp8q_status_string.argtypes = [i32]
         L.fp8q_status_string.restype = ctypes.c_char_p
         L.fp8q_version.restype = i32
+        L.fp8q_gemm_test_hold_loads.argtypes = [i32]
+        L.fp8q_gemm_test_hold_loads.restype = None
         L.fp8q_gemm_set_tile.argtypes = [i32, i32]
         L.fp8q_gemm_set_tile.restype = i32
-        for fn in ("fp8_quant_fused", "fp8_gemm_fwd", "fp8_gemm_dgrad", "amax_history_update",
+        for fn in ("fp8_quant_fused", "fp8_quant_fused_ex", "fp8_gemm_fwd", "fp8_gemm_dgrad", "amax_history_update",
                    "fp8q_naive_act", "fp8q_naive_amax", "fp8q_naive_cast"):
             getattr(L, fn).restype = i32
         _lib = L
@@ -90,15 +94,25 @@ def fp8_quant_fused(h: torch.Tensor, act: int, fmt: int, scale: torch.Tensor | N
                     act_out=None, q_out=None, q_t_out=None, amax_out=None, sat_count=None,
                     group_scales_out=None, group_rows: int = 1, stream=None) -> None:
     """Fused activation + BF16 copy + FP8 cast + amax of a [M,K] BF16 tensor."""
+    fp8_quant_fused_ex(h, act, fmt, scale, act_out=act_out, q_out=q_out, q_t_out=q_t_out,
+                       amax_out=amax_out, sat_count=sat_count, group_scales_out=group_scales_out,
+                       group_rows=group_rows, flags=0, stream=stream)
+
+
+def fp8_quant_fused_ex(h: torch.Tensor, act: int, fmt: int, scale: torch.Tensor | None = None, *,
+                       act_out=None, q_out=None, q_t_out=None, amax_out=None, sat_count=None,
+                       group_scales_out=None, group_rows: int = 1, flags: int = 0, stream=None) -> None:
+    """fp8_quant_fused with flags (ACCUMULATE: fold into amax_out / sat_count)."""
     M, K = h.shape
     n = M * K
     ng = ((M + group_rows - 1) // max(group_rows, 1)) * (K // GROUP) if group_scales_out is not None else 0
-    st = lib().fp8_quant_fused(
+    name = "fp8_quant_fused" if flags == 0 else "fp8_quant_fused_ex"
+    st = lib().fp8_quant_fused_ex(
         _ptr(h, 2 * n, "h"), M, K, act, fmt, _ptr(scale, 4, "scale"),
         _ptr(act_out, 2 * n, "act_out"), _ptr(q_out, n, "q_out"), _ptr(q_t_out, n, "q_t_out"),
         _ptr(amax_out, 4, "amax_out"), _ptr(sat_count, 8, "sat_count"),
-        _ptr(group_scales_out, 4 * ng, "group_scales_out"), group_rows, _stream(stream))
-    _check("fp8_quant_fused", st)
+        _ptr(group_scales_out, 4 * ng, "group_scales_out"), group_rows, flags, _stream(stream))
+    _check(name, st)
 
 
 def fp8_gemm_fwd(x_q: torch.Tensor, wt_q: torch.Tensor, scale_x: torch.Tensor, scale_w: torch.Tensor,
@@ -166,6 +180,11 @@ def fp8q_naive_cast(x, fmt: int, amax, margin: float, q_out, *, scale_out=None, 
 def fp8q_gemm_set_tile(pair: int, bn: int = 0) -> None:
     """Pin the GEMM tile shape (pair -1 = automatic, 0 = 1-CTA, 1 = 2-SM pair)."""
     _check("fp8q_gemm_set_tile", lib().fp8q_gemm_set_tile(pair, bn))
+
+
+def fp8q_gemm_test_hold_loads(on: bool) -> None:
+    """Failure-path test hook: later GEMMs issue no loads and report FP8Q_DEV_TIMEOUT."""
+    lib().fp8q_gemm_test_hold_loads(1 if on else 0)
 
 
 def version() -> int:

@@ -6,6 +6,8 @@
 #pragma once
 
 #include <cstdint>
+#include <mutex>
+#include <utility>
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
@@ -29,6 +31,49 @@ bool device_is_sm103();
             return FP8Q_ERR_CUDA;                               \
         }                                                       \
     } while (0)
+
+// ------------------------------------------------- programmatic dependent launch --
+// A kernel launched with the programmatic-serialization attribute may start
+// while the previous kernel in its stream is still running; it must call
+// pdl_wait() before touching memory that kernel (or anything earlier)
+// produces or consumes.  Without the attribute both are no-ops.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Let the next kernel in the stream begin launching (its pdl_wait() still
+// waits for this whole grid to finish and its writes to be visible).
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Ask for the largest shared-memory carveout for a kernel that itself needs
+// little shared memory: an SM can change its L1 / shared-memory split only
+// when idle, so SMs running such a kernel stay ready to take a GEMM CTA
+// (~214 KB of shared memory) beside it instead of draining first.
+template <typename... KArgs>
+inline void prefer_shared_carveout(void (*kern)(KArgs...)) {
+    static std::once_flag once;
+    std::call_once(once, [kern] {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared) != cudaSuccess)
+            (void)cudaGetLastError();
+    });
+}
+
+// Launch `kern` on `stream` with programmatic stream serialization, so its
+// prologue overlaps the tail of the previous kernel.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              Args&&... args) {
+    prefer_shared_carveout(kern);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 // -------------------------------------------------------------- format info --
 __host__ __device__ constexpr float fp8_max_value(int fmt) {

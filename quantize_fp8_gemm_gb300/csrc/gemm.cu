@@ -146,7 +146,8 @@ __global__ void __launch_bounds__(kThreadsGemm, 1)
 fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmD,
                 const float* __restrict__ scale_a, const float* __restrict__ scale_b,
-                int64_t M, int64_t N, int64_t K, uint32_t idesc, int* __restrict__ status) {
+                int64_t M, int64_t N, int64_t K, uint32_t idesc, int* __restrict__ status,
+                int hold_loads) {
     using C = Cfg<BN, PAIR>;
     static_assert(!GROUP || (BN == 128 && !PAIR), "group mode uses 1-CTA 128-wide tiles");
     extern __shared__ uint8_t smem_raw[];
@@ -203,6 +204,10 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     if constexpr (PAIR) cluster_sync_all();  // the peer's barriers exist before any copy signals them
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
+    // the prologue above overlaps the previous kernel; operands, scales and
+    // D are touched only after it has finished
+    pdl_launch_dependents();
+    pdl_wait();
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
@@ -211,7 +216,8 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             uint32_t phase = 0;
             int64_t issued = 0;
             bool ok = true;
-            for (int64_t tile = first_tile; tile < num_tiles && ok; tile += tile_stride) {
+            // hold_loads (test hook): issue nothing, so the MMA issuer's first wait runs out
+            for (int64_t tile = first_tile; tile < num_tiles && ok && !hold_loads; tile += tile_stride) {
                 const int32_t m0 = static_cast<int32_t>((tile / num_n) * C::TILE_M + rank * BM);
                 const int32_t n0 = static_cast<int32_t>((tile % num_n) * BN + rank * C::B_ROWS);
                 for (int kb = 0; kb < num_kb; ++kb) {
@@ -382,8 +388,9 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 }
             }
         }
-        // every store has finished reading shared memory and writing D
-        if (lane == 0) bulk_wait_group_all();
+        // every store has finished reading shared memory (the writes to D
+        // complete on their own and are visible when the grid finishes)
+        if (lane == 0) bulk_wait_group_read<0>();
         __syncwarp();
     }
 
@@ -443,6 +450,8 @@ bool make_out_map(CUtensorMap* map, void* base, int64_t rows, int64_t cols) {
     return r == CUDA_SUCCESS;
 }
 
+std::atomic<int> g_hold_loads{0};  // fp8q_gemm_test_hold_loads
+
 struct LaunchInfo {
     cudaError_t attr_err = cudaSuccess;
     int max_clusters = 0;  // co-resident 2-CTA clusters (PAIR only)
@@ -496,24 +505,31 @@ int launch_gemm(const void* a, const void* b, const float* sa, const float* sb, 
         if (info.max_clusters < 1) return FP8Q_ERR_CUDA;
         const int clusters = static_cast<int>(std::min<int64_t>(tiles, info.max_clusters));
         cudaLaunchConfig_t cfg = {};
-        cudaLaunchAttribute attr[1];
+        cudaLaunchAttribute attr[2];
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = 2;
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
         cfg.gridDim = dim3(2 * clusters);
         cfg.blockDim = dim3(kThreadsGemm);
         cfg.dynamicSmemBytes = C::SMEM_BYTES;
         cfg.stream = stream;
         cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        if (cudaLaunchKernelEx(&cfg, kern, mapA, mapB, mapD, sa, sb, M, N, K, idesc, status) != cudaSuccess) {
+        cfg.numAttrs = 2;
+        if (cudaLaunchKernelEx(&cfg, kern, mapA, mapB, mapD, sa, sb, M, N, K, idesc, status,
+                               g_hold_loads.load()) != cudaSuccess) {
             (void)cudaGetLastError();
             return FP8Q_ERR_CUDA;
         }
     } else {
         const int grid = static_cast<int>(std::min<int64_t>(tiles, sm_count()));
-        kern<<<grid, kThreadsGemm, C::SMEM_BYTES, stream>>>(mapA, mapB, mapD, sa, sb, M, N, K, idesc, status);
+        if (launch_pdl(kern, dim3(grid), dim3(kThreadsGemm), C::SMEM_BYTES, stream, mapA, mapB, mapD, sa, sb, M,
+                       N, K, idesc, status, g_hold_loads.load()) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return FP8Q_ERR_CUDA;
+        }
     }
     FP8Q_CHECK_LAUNCH();
     return FP8Q_OK;
@@ -602,6 +618,8 @@ int check_gemm_args(const void* a, const void* b, const float* sa, const float* 
 }  // namespace fp8q
 
 using namespace fp8q;
+
+extern "C" void fp8q_gemm_test_hold_loads(int on) { g_hold_loads.store(on != 0 ? 1 : 0); }
 
 extern "C" int fp8q_gemm_set_tile(int pair, int bn) {
     if (pair == -1) {

@@ -27,6 +27,8 @@ amax_history_kernel(float* __restrict__ history, int L, int* __restrict__ head,
                     const float* __restrict__ amax_new, float margin, float fmt_max,
                     float* __restrict__ scale_out, int* __restrict__ status) {
     const int lane = threadIdx.x;
+    pdl_launch_dependents();
+    pdl_wait();
     // the three loads are independent: issue them together
     const int h0 = *head;
     const float a_new = *amax_new;
@@ -105,9 +107,11 @@ extern "C" int amax_history_update(float* history, int L, int* head, const float
          reinterpret_cast<uintptr_t>(status)) & 3u)
         return FP8Q_ERR_ALIGN;
     if (!device_is_sm103()) return FP8Q_ERR_UNSUPPORTED;
-    amax_history_kernel<<<1, 32, 0, stream>>>(history, L, head, amax_new, margin, fp8_max_value(fmt),
-                                              scale_out, status);
-    FP8Q_CHECK_LAUNCH();
+    if (launch_pdl(amax_history_kernel, dim3(1), dim3(32), 0, stream, history, L, head, amax_new, margin,
+                   fp8_max_value(fmt), scale_out, status) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return FP8Q_ERR_CUDA;
+    }
     return FP8Q_OK;
 }
 

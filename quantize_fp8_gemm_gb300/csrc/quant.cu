@@ -125,6 +125,7 @@ quant_stream_kernel(const uint4* __restrict__ h, int64_t nchunks, const float* _
     uint32_t amax2 = 0, nsat = 0;
     const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    pdl_wait();
 
     if constexpr (!GROUP) {
         const float s = *scale;
@@ -184,6 +185,7 @@ quant_stream_kernel(const uint4* __restrict__ h, int64_t nchunks, const float* _
             }
         }
     }
+    pdl_launch_dependents();  // late: the next kernel's CTAs fill SMs as this grid drains
     block_reduce_publish(max16x2(amax2), nsat, amax_out, sat_out);
 }
 
@@ -207,6 +209,8 @@ quant_tile_kernel(const uint16_t* __restrict__ h, int64_t M, int64_t K, const fl
     const int64_t row0 = static_cast<int64_t>(blockIdx.y) * kTile;
     const int64_t col0 = static_cast<int64_t>(blockIdx.x) * kTile;
     const int64_t kgroups = K / kTile;
+    pdl_launch_dependents();
+    pdl_wait();
 
     uint4 a[8];
     uint32_t m16[8];
@@ -299,10 +303,13 @@ int launch_quant(const void* h, int64_t M, int64_t K, const float* scale, void* 
     const bool tiled = (q_t_out != nullptr) || (gscale != nullptr && group_rows == kTile);
     if (tiled) {
         dim3 grid(static_cast<unsigned>((K + kTile - 1) / kTile), static_cast<unsigned>((M + kTile - 1) / kTile));
-        quant_tile_kernel<ACT, FMT><<<grid, kThreads, 0, stream>>>(
-            static_cast<const uint16_t*>(h), M, K, scale, static_cast<uint16_t*>(act_out),
-            static_cast<uint8_t*>(q_out), static_cast<uint8_t*>(q_t_out), gscale, group_rows,
-            amax_out, sat_count);
+        if (launch_pdl(quant_tile_kernel<ACT, FMT>, grid, dim3(kThreads), 0, stream,
+                       static_cast<const uint16_t*>(h), M, K, scale, static_cast<uint16_t*>(act_out),
+                       static_cast<uint8_t*>(q_out), static_cast<uint8_t*>(q_t_out), gscale, group_rows,
+                       amax_out, sat_count) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return FP8Q_ERR_CUDA;
+        }
     } else {
         // One pass: enough CTAs that each thread handles one batch of loads
         // (4 chunks per tensor pass, 2 groups per half-warp); the hardware
@@ -313,14 +320,19 @@ int launch_quant(const void* h, int64_t M, int64_t K, const float* scale, void* 
         const int64_t want = (nchunks + per_cta - 1) / per_cta;
         const int64_t cap = int64_t(1) << 30;
         const unsigned grid = static_cast<unsigned>(std::max<int64_t>(1, std::min(want, cap)));
+        cudaError_t e;
         if (gscale)
-            quant_stream_kernel<ACT, FMT, true><<<grid, kThreads, 0, stream>>>(
-                static_cast<const uint4*>(h), nchunks, scale, static_cast<uint4*>(act_out),
-                static_cast<uint2*>(q_out), gscale, amax_out, sat_count);
+            e = launch_pdl(quant_stream_kernel<ACT, FMT, true>, dim3(grid), dim3(kThreads), 0, stream,
+                           static_cast<const uint4*>(h), nchunks, scale, static_cast<uint4*>(act_out),
+                           static_cast<uint2*>(q_out), gscale, amax_out, sat_count);
         else
-            quant_stream_kernel<ACT, FMT, false><<<grid, kThreads, 0, stream>>>(
-                static_cast<const uint4*>(h), nchunks, scale, static_cast<uint4*>(act_out),
-                static_cast<uint2*>(q_out), nullptr, amax_out, sat_count);
+            e = launch_pdl(quant_stream_kernel<ACT, FMT, false>, dim3(grid), dim3(kThreads), 0, stream,
+                           static_cast<const uint4*>(h), nchunks, scale, static_cast<uint4*>(act_out),
+                           static_cast<uint2*>(q_out), static_cast<float*>(nullptr), amax_out, sat_count);
+        if (e != cudaSuccess) {
+            (void)cudaGetLastError();
+            return FP8Q_ERR_CUDA;
+        }
     }
     FP8Q_CHECK_LAUNCH();
     return FP8Q_OK;
@@ -347,6 +359,16 @@ extern "C" int fp8_quant_fused(const void* h, int64_t M, int64_t K, int act, int
                                const float* scale, void* act_out, void* q_out, void* q_t_out,
                                float* amax_out, unsigned long long* sat_count,
                                float* group_scales_out, int group_rows, cudaStream_t stream) {
+    return fp8_quant_fused_ex(h, M, K, act, fmt, scale, act_out, q_out, q_t_out, amax_out, sat_count,
+                              group_scales_out, group_rows, 0u, stream);
+}
+
+extern "C" int fp8_quant_fused_ex(const void* h, int64_t M, int64_t K, int act, int fmt,
+                                  const float* scale, void* act_out, void* q_out, void* q_t_out,
+                                  float* amax_out, unsigned long long* sat_count,
+                                  float* group_scales_out, int group_rows, unsigned flags,
+                                  cudaStream_t stream) {
+    if (flags & ~static_cast<unsigned>(FP8Q_ACCUMULATE)) return FP8Q_ERR_UNSUPPORTED;
     if (h == nullptr && M != 0) return FP8Q_ERR_NULL;  // an empty tensor may have no storage
     if (act < FP8Q_ACT_IDENTITY || act > FP8Q_ACT_RELU2) return FP8Q_ERR_UNSUPPORTED;
     if (fmt != FP8Q_E4M3 && fmt != FP8Q_E5M2) return FP8Q_ERR_UNSUPPORTED;
@@ -368,8 +390,10 @@ extern "C" int fp8_quant_fused(const void* h, int64_t M, int64_t K, int act, int
         return FP8Q_ERR_ALIGN;
     if (!device_is_sm103()) return FP8Q_ERR_UNSUPPORTED;
 
-    if (amax_out && cudaMemsetAsync(amax_out, 0, sizeof(float), stream) != cudaSuccess) return FP8Q_ERR_CUDA;
-    if (sat_count && cudaMemsetAsync(sat_count, 0, sizeof(unsigned long long), stream) != cudaSuccess)
+    const bool zero = !(flags & FP8Q_ACCUMULATE);
+    if (zero && amax_out && cudaMemsetAsync(amax_out, 0, sizeof(float), stream) != cudaSuccess)
+        return FP8Q_ERR_CUDA;
+    if (zero && sat_count && cudaMemsetAsync(sat_count, 0, sizeof(unsigned long long), stream) != cudaSuccess)
         return FP8Q_ERR_CUDA;
     if (M == 0) return FP8Q_OK;
 

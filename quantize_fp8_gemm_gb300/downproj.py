@@ -73,8 +73,13 @@ class Fp8DownProj:
 
     def __init__(self, M: int, K: int, N: int, *, act: int = B.ACT_RELU2, margin: float = 2.0,
                  history_len: int = 1, group: bool = False, with_dgrad: bool = False,
-                 keep_act: bool = True, device="cuda"):
+                 keep_act: bool = True, chunks: int | None = None, device="cuda"):
         self.M, self.K, self.N, self.act, self.group = M, K, N, act, group
+        if chunks is None:  # measured on GB300: overlapping row blocks does not pay off
+            chunks = 1
+        if chunks < 1 or M % chunks or (chunks > 1 and (M // chunks) % 256):
+            raise ValueError("chunks must split M into row blocks that are multiples of 256")
+        self.chunks = chunks
         dev = device
         self.x = DelayedScale(B.E4M3, margin, history_len, dev)
         self.w = DelayedScale(B.E4M3, margin, history_len, dev)
@@ -85,7 +90,9 @@ class Fp8DownProj:
         self.y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
         self.sat = torch.zeros(1, dtype=torch.int64, device=dev)
         self.gemm_status = torch.zeros(1, dtype=torch.int32, device=dev)
-        self._side = torch.cuda.Stream(device=dev)  # the weight branch of a step
+        self._side = torch.cuda.Stream(device=dev)  # weight branch and history updates
+        hi = torch.cuda.Stream.priority_range()[1]
+        self._gemm = torch.cuda.Stream(device=dev, priority=hi)  # GEMM blocks, ahead of quantize blocks
         if group:
             if K % B.GROUP or N % B.GROUP:
                 raise ValueError("group scales need K % 128 == 0 and N % 128 == 0")
@@ -105,25 +112,34 @@ class Fp8DownProj:
                               q_t_out=self.wt_q, amax_out=self.w.amax)
 
     # -- a1-a5 ----------------------------------------------------------------
-    def quantize(self, H: torch.Tensor, scale: torch.Tensor | None = None) -> None:
+    def quantize(self, H: torch.Tensor, scale: torch.Tensor | None = None, rows=None) -> None:
+        """Fused quantize of H (or of its row block rows = (r0, r1); blocks after
+        the first fold into the amax / saturation count instead of resetting them)."""
         scale = self.x.scale if scale is None else scale
+        r0, r1 = (0, self.M) if rows is None else rows
+        flags = B.ACCUMULATE if r0 > 0 else 0
+        act_out = None if self.act_bf16 is None else self.act_bf16[r0:r1]
         if self.group:
-            B.fp8_quant_fused(H, self.act, B.E4M3, None, act_out=self.act_bf16, q_out=self.x_q,
-                              amax_out=self.x.amax, sat_count=self.sat,
-                              group_scales_out=self.x_gscale, group_rows=1)
+            B.fp8_quant_fused_ex(H[r0:r1], self.act, B.E4M3, None, act_out=act_out, q_out=self.x_q[r0:r1],
+                                 amax_out=self.x.amax, sat_count=self.sat,
+                                 group_scales_out=self.x_gscale[r0:r1], group_rows=1, flags=flags)
         else:
-            B.fp8_quant_fused(H, self.act, B.E4M3, scale, act_out=self.act_bf16,
-                              q_out=self.x_q, amax_out=self.x.amax, sat_count=self.sat)
+            B.fp8_quant_fused_ex(H[r0:r1], self.act, B.E4M3, scale, act_out=act_out,
+                                 q_out=self.x_q[r0:r1], amax_out=self.x.amax, sat_count=self.sat,
+                                 flags=flags)
 
     # -- a9 -------------------------------------------------------------------
-    def gemm(self, scale_x: torch.Tensor | None = None, scale_w: torch.Tensor | None = None) -> torch.Tensor:
+    def gemm(self, scale_x: torch.Tensor | None = None, scale_w: torch.Tensor | None = None,
+             rows=None) -> torch.Tensor:
+        """Y = X_q W_q / (s_x s_w) for all rows, or for the row block rows = (r0, r1)."""
         scale_x = self.x.scale if scale_x is None else scale_x
         scale_w = self.w.scale if scale_w is None else scale_w
+        r0, r1 = (0, self.M) if rows is None else rows
         if self.group:
-            B.fp8_gemm_fwd(self.x_q, self.wt_q, self.x_gscale, self.w_gscale, self.y, group_mode=1,
-                           status=self.gemm_status)
+            B.fp8_gemm_fwd(self.x_q[r0:r1], self.wt_q, self.x_gscale[r0:r1], self.w_gscale, self.y[r0:r1],
+                           group_mode=1, status=self.gemm_status)
         else:
-            B.fp8_gemm_fwd(self.x_q, self.wt_q, scale_x, scale_w, self.y,
+            B.fp8_gemm_fwd(self.x_q[r0:r1], self.wt_q, scale_x, scale_w, self.y[r0:r1],
                            status=self.gemm_status)
         return self.y
 
@@ -133,63 +149,45 @@ class Fp8DownProj:
             self.x.update()
             self.w.update()
 
-    PHASE_EVENTS = ("start", "w_cast_start", "w_cast_end", "quant_end", "gemm_start", "gemm_end", "end")
-
-    def step(self, H: torch.Tensor, W: torch.Tensor, events=None) -> torch.Tensor:
+    def step(self, H: torch.Tensor, W: torch.Tensor) -> torch.Tensor:
         """One forward step: cast W, fused quantize of H, FP8 GEMM, history updates.
 
-        The current stream runs the fused quantize and then the GEMM; a side
-        stream runs the weight cast and its history update beside the
-        quantize, and the activation's history update beside the GEMM (the
-        updates write the other scale slot, so they never race the reads).
-        ``events``: optional dict of CUDA events keyed by PHASE_EVENTS."""
-        ev = events or {}
-        main, side = torch.cuda.current_stream(), self._side
+        The batch is processed in ``chunks`` row blocks.  The current stream
+        quantizes the blocks one after the other; a high-priority stream runs
+        each block's GEMM as soon as that block is quantized, so the
+        compute-bound GEMM of block i overlaps the memory-bound quantize of
+        block i+1.  A side stream casts W and updates its history beside the
+        first quantize, then updates the activation's history once the last
+        block is quantized (the updates write the other scale slot, so they
+        never race the GEMMs' reads).  All branches join the current stream."""
+        main, side, gs = torch.cuda.current_stream(), self._side, self._gemm
         sx, sw = self.x.scale, self.w.scale  # this step's slots
-
-        def mark(key):
-            if key in ev:
-                ev[key].record()
-
-        mark("start")
         side.wait_stream(main)
         with torch.cuda.stream(side):
-            mark("w_cast_start")
             self.cast_weight(W, sw)
-            mark("w_cast_end")
             if not self.group:
                 self.w.update()
-        self.quantize(H, sx)
-        mark("quant_end")
-        quant_done = torch.cuda.Event()
-        quant_done.record(main)
-        main.wait_stream(side)
-        mark("gemm_start")
-        y = self.gemm(sx, sw)
-        mark("gemm_end")
+        gs.wait_stream(side)  # W_q^T ready (and everything before this step)
+        block = self.M // self.chunks
+        for i in range(self.chunks):
+            rows = (i * block, (i + 1) * block)
+            self.quantize(H, sx, rows)
+            done = torch.cuda.Event()
+            done.record(main)
+            gs.wait_event(done)
+            with torch.cuda.stream(gs):
+                self.gemm(sx, sw, rows)
         if not self.group:
-            side.wait_event(quant_done)
+            side.wait_stream(main)  # every block quantized: this step's amax is final
             with torch.cuda.stream(side):
                 self.x.update()
+        main.wait_stream(gs)
         main.wait_stream(side)
-        mark("end")
-        return y
+        return self.y
 
-    @staticmethod
-    def phase_ms(ev: dict) -> dict:
-        """Durations (ms) of the phases from events recorded by step()."""
-        return {
-            "w_cast": ev["w_cast_start"].elapsed_time(ev["w_cast_end"]),
-            "quant": ev["start"].elapsed_time(ev["quant_end"]),
-            "gemm": ev["gemm_start"].elapsed_time(ev["gemm_end"]),
-            "history": ev["gemm_end"].elapsed_time(ev["end"]),
-            "step": ev["start"].elapsed_time(ev["end"]),
-        }
-
-    def capture(self, H: torch.Tensor, W: torch.Tensor, H_next: torch.Tensor | None = None,
-                timed: bool = False) -> "StepGraph":
+    def capture(self, H: torch.Tensor, W: torch.Tensor, H_next: torch.Tensor | None = None) -> "StepGraph":
         """Capture the step as CUDA graphs on fixed buffers (see StepGraph)."""
-        return StepGraph(self, H, W, H_next, timed)
+        return StepGraph(self, H, W, H_next)
 
     def calibrate(self, H: torch.Tensor, W: torch.Tensor) -> None:
         """Bootstrap the delayed scales from step 0's own tensors (one amax pass each).
@@ -215,37 +213,25 @@ class StepGraph:
     captured (one per slot); ``replay()`` runs the one matching the current
     slot and switches slots, so replays and eager steps mix freely.  The
     graph for the slot current at capture reads H, the other H_next
-    (default H).  The amax histories live in
-    device memory, so replays carry the delayed scaling forward exactly as
-    eager steps do.  Run at least one eager step first (it performs the
-    one-time per-kernel set-up).
-
-    timed=True records CUDA events inside the graphs (external event nodes)
-    at the phase boundaries; ``phase_ms()`` reads those of the last replay
-    once it has completed.  The event nodes themselves add a few
-    microseconds per step.
+    (default H).  The amax histories live in device memory, so replays carry
+    the delayed scaling forward exactly as eager steps do.  Run at least one
+    eager step first (it performs the one-time per-kernel set-up).
     """
 
-    def __init__(self, dp: Fp8DownProj, H: torch.Tensor, W: torch.Tensor,
-                 H_next: torch.Tensor | None = None, timed: bool = False):
+    def __init__(self, dp: Fp8DownProj, H: torch.Tensor, W: torch.Tensor, H_next: torch.Tensor | None = None):
         self.dp = dp
         self.slot0 = dp.x.slot  # the scale slot graph 0 reads; graph 1 reads the other
-        self.graphs, self.events = [], []
+        self.graphs = []
         side = torch.cuda.Stream()
         side.wait_stream(torch.cuda.current_stream())
         for h in (H, H if H_next is None else H_next):
-            ev = None
-            if timed:
-                ev = {k: torch.cuda.Event(enable_timing=True, external=True) for k in dp.PHASE_EVENTS}
             g = torch.cuda.CUDAGraph()
             with torch.cuda.stream(side):
                 with torch.cuda.graph(g, stream=side):
-                    self.y = dp.step(h, W, ev)
+                    self.y = dp.step(h, W)
             self.graphs.append(g)
-            self.events.append(ev)
         torch.cuda.current_stream().wait_stream(side)
         self._next = 0
-        self._last = 0
 
     def replay(self) -> torch.Tensor:
         """Run one step: the graph whose scale slot is current, then switch
@@ -253,12 +239,8 @@ class StepGraph:
         dp = self.dp
         k = self._next if dp.group else int(dp.x.slot != self.slot0)
         self.graphs[k].replay()
-        self._last = k
         self._next = k ^ 1
         if not dp.group:
             dp.x.slot ^= 1
             dp.w.slot ^= 1
         return self.y
-
-    def phase_ms(self) -> dict:
-        return Fp8DownProj.phase_ms(self.events[self._last])

@@ -131,3 +131,15 @@ def test_gemm_tile_knob_arguments(lib):
     assert lib.fp8q_gemm_set_tile(1, 224) == OK
     assert lib.fp8q_gemm_set_tile(0, 160) == OK
     assert lib.fp8q_gemm_set_tile(-1, 0) == OK
+
+
+def test_quant_ex_flags(lib):
+    lib.fp8_quant_fused_ex.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+                                       ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                       ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+                                       ctypes.c_uint, ctypes.c_void_p]
+    f = lambda flags: lib.fp8_quant_fused_ex(A, 64, 256, 2, 0, A, A, A, None, A, A, None, 1, flags, None)
+    assert f(2) == ERR_UNSUPPORTED
+    assert f(1) == ERR_UNSUPPORTED  # valid flags: only the missing sm_103 device is left
+    assert f(0) == ERR_UNSUPPORTED
+    assert lib.fp8_quant_fused_ex(None, 64, 256, 2, 0, A, A, A, None, A, A, None, 1, 1, None) == ERR_NULL

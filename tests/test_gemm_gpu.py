@@ -150,3 +150,27 @@ def test_every_tile_shape_on_ragged_problems(pair, bn):
         assert_gemm_close(dx, Dr, Sd)
     finally:
         B.fp8q_gemm_set_tile(-1)
+
+
+@pytest.mark.parametrize("pair,bn", [(0, 192), (1, 256)])
+def test_bounded_wait_reports_timeout_and_context_survives(pair, bn):
+    """With the loads held back nothing ever fills the MMA's first stage: the
+    bounded wait runs out, the kernel reports FP8Q_DEV_TIMEOUT through the
+    status word and exits, and the next GEMM on the same context is correct."""
+    M, N, K = 512, 256, 256
+    xq = rand_e4m3((M, K), seed=31, scale=30.0)
+    wq = rand_e4m3((K, N), seed=32, scale=30.0)
+    y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    try:
+        B.fp8q_gemm_set_tile(pair, bn)
+        B.fp8q_gemm_test_hold_loads(True)
+        B.fp8_gemm_fwd(dev_u8(xq), dev_u8(np.ascontiguousarray(wq.T)), dev_f32(1.0), dev_f32(1.0), y,
+                       status=st)
+        torch.cuda.synchronize()
+        assert st.item() & B.DEV_TIMEOUT
+    finally:
+        B.fp8q_gemm_test_hold_loads(False)
+        B.fp8q_gemm_set_tile(-1)
+    Yr, S = O.gemm_fwd(xq, wq, 1.0, 1.0)
+    assert_gemm_close(run_fwd(xq, wq, 1.0, 1.0), Yr, S)

@@ -169,3 +169,26 @@ def test_bad_amax_keeps_scale_and_flags():
         torch.cuda.synchronize()
         assert scale.item() == o.scale and int(head.item()) == o.head
         assert np.array_equal(hist.cpu().numpy(), o.hist)
+
+
+@pytest.mark.parametrize("chunks", [2, 4])
+def test_row_blocks_match_one_block(chunks):
+    """Quantizing in row blocks (accumulating amax and saturations) with each
+    block's GEMM overlapped gives exactly the one-block results."""
+    w = WL.WORKLOADS["gpt2s"]
+    M, K, N = 4096, w.K, w.N
+    Wd = WL.bf16_tensor(WL.w_down(w)).cuda()
+    hs = [WL.bf16_tensor(WL.h_preact(w, t)[:M]).cuda() for t in range(3)]
+    one = Fp8DownProj(M, K, N, margin=w.margin, chunks=1)
+    blk = Fp8DownProj(M, K, N, margin=w.margin, chunks=chunks)
+    one.calibrate(hs[0], Wd)
+    blk.calibrate(hs[0], Wd)
+    for t in range(3):
+        y1 = one.step(hs[t], Wd).clone()
+        y2 = blk.step(hs[t], Wd)
+        torch.cuda.synchronize()
+        assert torch.equal(y1.view(torch.int16), y2.view(torch.int16)), f"step {t}: Y"
+        assert torch.equal(one.x_q, blk.x_q) and torch.equal(one.act_bf16.view(torch.int16),
+                                                             blk.act_bf16.view(torch.int16))
+        assert one.sat.item() == blk.sat.item() and one.x.amax.item() == blk.x.amax.item()
+        assert torch.equal(one.x.scale, blk.x.scale) and torch.equal(one.w.scale, blk.w.scale)
