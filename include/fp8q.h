@@ -6,6 +6,7 @@
  *   1. fp8_quant_fused      BF16 pre-activation H -> act(H) in registers ->
  *                           BF16 copy for backward + FP8 copy + amax
  *   2. fp8_gemm_fwd         Y = X_q W_q / (s_x s_w), FP32 accumulate, BF16 out
+ *      (fp8_downproj_fwd    1 and 2 fused in one kernel)
  *   3. amax_history_update  push this step's amax; scale for the next step
  *   (fp8_gemm_dgrad         dX = dY_q W_q^T / (s_dy s_w), the gradient shape)
  *
@@ -178,6 +179,33 @@ int fp8_gemm_dgrad(const void* dy_q, const void* w_q,
                    const float* scale_dy, const float* scale_w,
                    void* dx, int64_t M, int64_t N, int64_t K,
                    int* status, cudaStream_t stream);
+
+/*
+ * fp8_downproj_fwd -- the fused quantize + forward GEMM in one kernel  [fused][gemms]
+ *
+ * Computes exactly what fp8_quant_fused(h, act, E4M3, scale_x, act_out, x_q,
+ * amax_out, sat_count) followed by fp8_gemm_fwd(x_q, wt_q, scale_x, scale_w, y)
+ * compute, in one persistent kernel: extra warps of every CTA quantize H in
+ * 16-row units and count finished units per 128-row block in `workspace`;
+ * the GEMM loads a tile's rows of x_q once their block is complete, so the
+ * GEMM of early rows overlaps the quantize of later ones and the large tensor
+ * is read once.  act_out, amax_out, sat_count may be NULL; x_q is required
+ * (it is the GEMM's operand and the E4M3 copy).
+ *   workspace  device scratch of at least fp8_downproj_workspace_bytes(M)
+ *              bytes, 4-byte aligned, owned by the caller; zeroed by this call
+ *              (stream-ordered).  Two fused calls must not share it
+ *              concurrently.
+ * The kernel occupies every SM with one CTA and its CTAs wait on each
+ * other's quantize work (bounded: a wait that runs out sets
+ * FP8Q_DEV_TIMEOUT), so do not run two of them on the GPU at the same time.
+ * Same shape, alignment and error rules as fp8_quant_fused / fp8_gemm_fwd.
+ */
+size_t fp8_downproj_workspace_bytes(int64_t M);
+int fp8_downproj_fwd(const void* h, const void* wt_q, int64_t M, int64_t N, int64_t K, int act,
+                     const float* scale_x, const float* scale_w,
+                     void* act_out, void* x_q, float* amax_out, unsigned long long* sat_count,
+                     void* y, void* workspace, size_t workspace_bytes,
+                     int* status, cudaStream_t stream);
 
 /*
  * amax_history_update -- delayed per-tensor scale for the next step  [fused][gemms]

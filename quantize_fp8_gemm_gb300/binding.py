@@ -49,6 +49,9 @@ def lib() -> ctypes.CDLL:
         L.fp8_gemm_fwd.argtypes = [P, P, P, P, i32, P, i64, i64, i64, P, P]
         L.fp8_gemm_dgrad.argtypes = [P, P, P, P, P, i64, i64, i64, P, P]
         L.amax_history_update.argtypes = [P, i32, P, P, f32, i32, P, P, P]
+        L.fp8_downproj_workspace_bytes.argtypes = [i64]
+        L.fp8_downproj_workspace_bytes.restype = ctypes.c_size_t
+        L.fp8_downproj_fwd.argtypes = [P, P, i64, i64, i64, i32, P, P, P, P, P, P, P, P, ctypes.c_size_t, P, P]
         L.fp8q_naive_act.argtypes = [P, i64, i64, i32, P, P]
         L.fp8q_naive_amax.argtypes = [P, i64, P, P]
         L.fp8q_naive_cast.argtypes = [P, i64, i32, P, f32, P, P, P]
@@ -59,7 +62,7 @@ def lib() -> ctypes.CDLL:
         L.fp8q_gemm_test_hold_loads.restype = None
         L.fp8q_gemm_set_tile.argtypes = [i32, i32]
         L.fp8q_gemm_set_tile.restype = i32
-        for fn in ("fp8_quant_fused", "fp8_quant_fused_ex", "fp8_gemm_fwd", "fp8_gemm_dgrad", "amax_history_update",
+        for fn in ("fp8_quant_fused", "fp8_quant_fused_ex", "fp8_downproj_fwd", "fp8_gemm_fwd", "fp8_gemm_dgrad", "amax_history_update",
                    "fp8q_naive_act", "fp8q_naive_amax", "fp8q_naive_cast"):
             getattr(L, fn).restype = i32
         _lib = L
@@ -145,6 +148,28 @@ def fp8_gemm_dgrad(dy_q: torch.Tensor, w_q: torch.Tensor, scale_dy: torch.Tensor
         _ptr(scale_w, 4, "scale_w"), _ptr(dx, 2 * M * K, "dx"), M, N, K,
         _ptr(status, 4, "status"), _stream(stream))
     _check("fp8_gemm_dgrad", st)
+
+
+def fp8_downproj_workspace_bytes(M: int) -> int:
+    return int(lib().fp8_downproj_workspace_bytes(M))
+
+
+def fp8_downproj_fwd(h: torch.Tensor, wt_q: torch.Tensor, scale_x: torch.Tensor, scale_w: torch.Tensor,
+                     x_q: torch.Tensor, y: torch.Tensor, workspace: torch.Tensor, *, act: int = ACT_RELU2,
+                     act_out=None, amax_out=None, sat_count=None, status=None, stream=None) -> None:
+    """Fused quantize of H [M,K] + forward GEMM with W_q^T [N,K] -> y [M,N], one kernel."""
+    M, K = h.shape
+    N = wt_q.shape[0]
+    if wt_q.shape[1] != K:
+        raise ValueError("h [M,K] and wt_q [N,K] disagree on K")
+    ws = fp8_downproj_workspace_bytes(M)
+    st = lib().fp8_downproj_fwd(
+        _ptr(h, 2 * M * K, "h"), _ptr(wt_q, N * K, "wt_q"), M, N, K, act, _ptr(scale_x, 4, "scale_x"),
+        _ptr(scale_w, 4, "scale_w"), _ptr(act_out, 2 * M * K, "act_out"), _ptr(x_q, M * K, "x_q"),
+        _ptr(amax_out, 4, "amax_out"), _ptr(sat_count, 8, "sat_count"), _ptr(y, 2 * M * N, "y"),
+        _ptr(workspace, ws, "workspace"), workspace.numel() * workspace.element_size(),
+        _ptr(status, 4, "status"), _stream(stream))
+    _check("fp8_downproj_fwd", st)
 
 
 def amax_history_update(history: torch.Tensor, head: torch.Tensor, amax_new: torch.Tensor, margin: float,

@@ -34,6 +34,7 @@
 // Every mbarrier wait is bounded; on time-out the CTA sets FP8Q_DEV_TIMEOUT,
 // waits (bounded) for its copies and MMAs in flight, frees TMEM and exits.
 #include "common.cuh"
+#include "quant_ops.cuh"
 
 #include <algorithm>
 #include <atomic>
@@ -51,6 +52,29 @@ constexpr int kThreadsGemm = 192;  // 6 warps
 constexpr int kEpiWarps = 4;
 constexpr int kEpiChunkBytes = 32 * 32 * 2;  // one warp's 32 rows x 32 BF16 columns
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per wait: far above any real wait
+
+// Fused quantize (FUSED = true): extra warps per CTA turn the BF16
+// pre-activation into the GEMM's E4M3 A operand, 16-row units at a time.
+constexpr int kQuantWarps = 16;
+constexpr int kQuantThreads = kQuantWarps * 32;
+constexpr int kUnitRows = 16;   // rows per quantize unit (a 128-row block has 8)
+constexpr int kQuantBatch = 12; // 16-byte loads in flight per quantize thread
+
+template <bool FUSED>
+constexpr int gemm_threads() { return kThreadsGemm + (FUSED ? kQuantThreads : 0); }
+
+// Operands of the fused quantize.  ready[b] counts the 16-row units of 128-row
+// block b whose E4M3 rows are written; the GEMM's producer loads a tile's A
+// rows once its block is complete.
+struct FusedArgs {
+    const uint4* h;               // H [M,K] BF16, 8 elements per 16 bytes
+    uint4* act_out;               // [M,K] BF16 activation copy, or nullptr
+    uint2* x_q;                   // [M,K] E4M3: the GEMM's A operand
+    float* amax_out;              // or nullptr; zeroed before the launch
+    unsigned long long* sat_out;  // or nullptr; zeroed before the launch
+    unsigned* ready;              // [ceil(M/128)], zeroed before the launch
+    int act;                      // fp8q_act
+};
 
 template <int BN, bool PAIR>
 struct Cfg {
@@ -103,6 +127,76 @@ __device__ __forceinline__ void wait_phase_drain(uint64_t* bar, uint32_t parity)
     }
 }
 
+// Bounded wait until a GPU-scope counter reaches `need` (acquire).
+__device__ __forceinline__ bool wait_ready(const unsigned* counter, unsigned need, volatile int* abort_flag,
+                                           int* status) {
+    if (ld_acquire(counter) >= need) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        __nanosleep(64);
+        if (ld_acquire(counter) >= need) return true;
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > kTimeoutNs) {
+            *abort_flag = 1;
+            if (status) atomicOr(status, FP8Q_DEV_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ uint4 act8_any(int act, uint4 x, uint32_t& amax2) {
+    if (act == FP8Q_ACT_RELU2) return act8<FP8Q_ACT_RELU2>(x, amax2);
+    if (act == FP8Q_ACT_RELU) return act8<FP8Q_ACT_RELU>(x, amax2);
+    return act8<FP8Q_ACT_IDENTITY>(x, amax2);
+}
+
+// The quantize warps of one CTA (fused kernel): units u = blockIdx.x,
+// blockIdx.x + gridDim.x, ... in row order; after each unit one thread
+// publishes it with a release increment of its block's ready count.
+__device__ __forceinline__ void fused_quantize(const FusedArgs& fz, const float* scale, int64_t M, int64_t K) {
+    const int qt = threadIdx.x - kThreadsGemm;
+    const int64_t total = M * (K / 8);
+    const int64_t unit_chunks = int64_t(kUnitRows) * (K / 8);
+    const int64_t num_units = (M + kUnitRows - 1) / kUnitRows;
+    const float s = __ldg(scale);
+    uint32_t amax2 = 0, nsat = 0;
+    for (int64_t u = blockIdx.x; u < num_units; u += gridDim.x) {
+        const int64_t c_end = min(u * unit_chunks + unit_chunks, total);
+        for (int64_t c0 = u * unit_chunks + qt; c0 < c_end; c0 += int64_t(kQuantThreads) * kQuantBatch) {
+            uint4 x[kQuantBatch];
+#pragma unroll
+            for (int j = 0; j < kQuantBatch; ++j) {
+                const int64_t c = c0 + int64_t(j) * kQuantThreads;
+                x[j] = c < c_end ? ld_stream_v4(fz.h + c) : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int j = 0; j < kQuantBatch; ++j) {
+                const int64_t c = c0 + int64_t(j) * kQuantThreads;
+                if (c < c_end) {
+                    const uint4 a = act8_any(fz.act, x[j], amax2);
+                    if (fz.act_out) st_stream_v4(fz.act_out + c, a);
+                    st_v2(fz.x_q + c, cast8<FP8Q_E4M3>(a, s, nsat));
+                }
+            }
+        }
+        // this unit's E4M3 rows are written by every quantize thread: order them
+        // before the count, which the producer reads before its TMA loads
+        fence_proxy_async_global();
+        named_barrier(1, kQuantThreads);
+        if (qt == 0) red_release_add(fz.ready + (u * kUnitRows) / BM, 1u);
+    }
+    __shared__ uint32_t s_amax[kQuantWarps], s_sat[kQuantWarps];
+    uint32_t m = __reduce_max_sync(0xFFFFFFFFu, max16x2(amax2));
+    uint32_t c = __reduce_add_sync(0xFFFFFFFFu, nsat);
+    if ((qt & 31) == 0) { s_amax[qt >> 5] = m; s_sat[qt >> 5] = c; }
+    named_barrier(1, kQuantThreads);
+    if (qt == 0) {
+        for (int w = 1; w < kQuantWarps; ++w) { m = max(m, s_amax[w]); c += s_sat[w]; }
+        if (fz.amax_out && m) atomicMax(reinterpret_cast<unsigned int*>(fz.amax_out), m << 16);
+        if (fz.sat_out && c) atomicAdd(fz.sat_out, static_cast<unsigned long long>(c));
+    }
+}
+
 // One warp's 32 rows x 32 columns of output: round to BF16, stage in shared
 // memory with the 64-byte swizzle (row r's 16-byte piece j sits at piece
 // j ^ ((r >> 1) & 3), so the warp's writes spread over all banks) and write
@@ -141,15 +235,19 @@ __device__ __forceinline__ void epi_store_chunk(const CUtensorMap* tmD, uint8_t*
 //                fresh TMEM buffer and promoted into FP32 registers with its
 //                own 1/(s_a[row, kb] * s_b[kb, n_blk]).
 // PAIR = true  : 2-SM tiles (see the file header); per-tensor scales only.
-template <int BN, bool GROUP, bool PAIR>
-__global__ void __launch_bounds__(kThreadsGemm, 1)
+// FUSED = true : the fused quantize + GEMM (per-tensor scales): the extra
+//                quantize warps produce A = X_q from H while the GEMM consumes
+//                finished 128-row blocks.
+template <int BN, bool GROUP, bool PAIR, bool FUSED>
+__global__ void __launch_bounds__(gemm_threads<FUSED>(), 1)
 fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmD,
                 const float* __restrict__ scale_a, const float* __restrict__ scale_b,
                 int64_t M, int64_t N, int64_t K, uint32_t idesc, int* __restrict__ status,
-                int hold_loads) {
+                int hold_loads, const FusedArgs fz) {
     using C = Cfg<BN, PAIR>;
     static_assert(!GROUP || (BN == 128 && !PAIR), "group mode uses 1-CTA 128-wide tiles");
+    static_assert(!(GROUP && FUSED), "the fused quantize feeds the per-tensor GEMM");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* epi_stage = smem + C::STAGES * C::STAGE_BYTES;  // 1024-aligned: STAGE_BYTES is
@@ -220,6 +318,16 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             for (int64_t tile = first_tile; tile < num_tiles && ok && !hold_loads; tile += tile_stride) {
                 const int32_t m0 = static_cast<int32_t>((tile / num_n) * C::TILE_M + rank * BM);
                 const int32_t n0 = static_cast<int32_t>((tile % num_n) * BN + rank * C::B_ROWS);
+                if constexpr (FUSED) {
+                    // this tile's A rows exist once every unit of their block is quantized
+                    if (m0 < M) {
+                        const int64_t blk = m0 / BM;
+                        const int64_t rows = M - blk * BM < BM ? M - blk * BM : BM;
+                        const unsigned need = static_cast<unsigned>((rows + kUnitRows - 1) / kUnitRows);
+                        if (!wait_ready(fz.ready + blk, need, abort_flag, status)) { ok = false; break; }
+                        fence_proxy_async_global();
+                    }
+                }
                 for (int kb = 0; kb < num_kb; ++kb) {
                     if (!wait_phase(&empty[stage], phase ^ 1u, abort_flag, status)) { ok = false; break; }
                     uint8_t* sa = smem + stage * C::STAGE_BYTES;
@@ -306,6 +414,9 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             else mma_commit(smem_u32(drain));
             wait_phase_drain(drain, 0);
         }
+    } else if (warp >= 2 + kEpiWarps) {
+        // ---------------------------------------------------- fused quantize
+        if constexpr (FUSED) fused_quantize(fz, scale_a, M, K);
     } else {
         // ---------------------------------------------------------- epilogue
         const int q = warp & 3;  // TMEM lane quarter this warp may access
@@ -457,13 +568,13 @@ struct LaunchInfo {
     int max_clusters = 0;  // co-resident 2-CTA clusters (PAIR only)
 };
 
-template <int BN, bool GROUP, bool PAIR>
+template <int BN, bool GROUP, bool PAIR, bool FUSED>
 const LaunchInfo& launch_info() {
     using C = Cfg<BN, PAIR>;
     static LaunchInfo info;
     static std::once_flag once;
     std::call_once(once, [] {
-        auto kern = fp8_gemm_kernel<BN, GROUP, PAIR>;
+        auto kern = fp8_gemm_kernel<BN, GROUP, PAIR, FUSED>;
         info.attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
         if (PAIR && info.attr_err == cudaSuccess) {
             cudaLaunchConfig_t cfg = {};
@@ -473,7 +584,7 @@ const LaunchInfo& launch_info() {
             attr[0].val.clusterDim.y = 1;
             attr[0].val.clusterDim.z = 1;
             cfg.gridDim = dim3(2 * sm_count());
-            cfg.blockDim = dim3(kThreadsGemm);
+            cfg.blockDim = dim3(gemm_threads<FUSED>());
             cfg.dynamicSmemBytes = C::SMEM_BYTES;
             cfg.attrs = attr;
             cfg.numAttrs = 1;
@@ -488,11 +599,12 @@ const LaunchInfo& launch_info() {
     return info;
 }
 
-template <int BN, bool GROUP, bool PAIR>
+template <int BN, bool GROUP, bool PAIR, bool FUSED>
 int launch_gemm(const void* a, const void* b, const float* sa, const float* sb, void* d, int64_t M,
-                int64_t N, int64_t K, uint32_t afmt, uint32_t bfmt, int* status, cudaStream_t stream) {
+                int64_t N, int64_t K, uint32_t afmt, uint32_t bfmt, int* status, cudaStream_t stream,
+                const FusedArgs& fz) {
     using C = Cfg<BN, PAIR>;
-    const LaunchInfo& info = launch_info<BN, GROUP, PAIR>();
+    const LaunchInfo& info = launch_info<BN, GROUP, PAIR, FUSED>();
     if (info.attr_err != cudaSuccess) return FP8Q_ERR_CUDA;
     alignas(64) CUtensorMap mapA, mapB, mapD;
     if (!make_kmajor_map(&mapA, a, M, K, BM) || !make_kmajor_map(&mapB, b, N, K, C::B_ROWS) ||
@@ -500,10 +612,10 @@ int launch_gemm(const void* a, const void* b, const float* sa, const float* sb, 
         return FP8Q_ERR_CUDA;
     const int64_t tiles = ((M + C::TILE_M - 1) / C::TILE_M) * ((N + BN - 1) / BN);
     const uint32_t idesc = idesc_f8(afmt, bfmt, C::MMA_M, BN);
-    auto kern = fp8_gemm_kernel<BN, GROUP, PAIR>;
+    auto kern = fp8_gemm_kernel<BN, GROUP, PAIR, FUSED>;
     if constexpr (PAIR) {
         if (info.max_clusters < 1) return FP8Q_ERR_CUDA;
-        const int clusters = static_cast<int>(std::min<int64_t>(tiles, info.max_clusters));
+        const int clusters = static_cast<int>(FUSED ? info.max_clusters : std::min<int64_t>(tiles, info.max_clusters));
         cudaLaunchConfig_t cfg = {};
         cudaLaunchAttribute attr[2];
         attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -513,20 +625,22 @@ int launch_gemm(const void* a, const void* b, const float* sa, const float* sb, 
         attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[1].val.programmaticStreamSerializationAllowed = 1;
         cfg.gridDim = dim3(2 * clusters);
-        cfg.blockDim = dim3(kThreadsGemm);
+        cfg.blockDim = dim3(gemm_threads<FUSED>());
         cfg.dynamicSmemBytes = C::SMEM_BYTES;
         cfg.stream = stream;
         cfg.attrs = attr;
         cfg.numAttrs = 2;
         if (cudaLaunchKernelEx(&cfg, kern, mapA, mapB, mapD, sa, sb, M, N, K, idesc, status,
-                               g_hold_loads.load()) != cudaSuccess) {
+                               g_hold_loads.load(), fz) != cudaSuccess) {
             (void)cudaGetLastError();
             return FP8Q_ERR_CUDA;
         }
     } else {
-        const int grid = static_cast<int>(std::min<int64_t>(tiles, sm_count()));
-        if (launch_pdl(kern, dim3(grid), dim3(kThreadsGemm), C::SMEM_BYTES, stream, mapA, mapB, mapD, sa, sb, M,
-                       N, K, idesc, status, g_hold_loads.load()) != cudaSuccess) {
+        // the fused kernel needs every CTA resident at once (the producers wait on
+        // quantize work spread over all CTAs): one CTA per SM, never more
+        const int grid = static_cast<int>(FUSED ? sm_count() : std::min<int64_t>(tiles, sm_count()));
+        if (launch_pdl(kern, dim3(grid), dim3(gemm_threads<FUSED>()), C::SMEM_BYTES, stream, mapA, mapB, mapD, sa,
+                       sb, M, N, K, idesc, status, g_hold_loads.load(), fz) != cudaSuccess) {
             (void)cudaGetLastError();
             return FP8Q_ERR_CUDA;
         }
@@ -576,26 +690,39 @@ Shape pick_shape(int64_t M, int64_t N) {
     return best;
 }
 
-int gemm_dispatch(const void* a, const void* b, const float* sa, const float* sb, int group, void* d,
-                  int64_t M, int64_t N, int64_t K, uint32_t afmt, uint32_t bfmt, int* status,
-                  cudaStream_t stream) {
-    if (group) return launch_gemm<128, true, false>(a, b, sa, sb, d, M, N, K, afmt, bfmt, status, stream);
+template <bool FUSED>
+int gemm_dispatch_t(const void* a, const void* b, const float* sa, const float* sb, int group, void* d,
+                    int64_t M, int64_t N, int64_t K, uint32_t afmt, uint32_t bfmt, int* status,
+                    cudaStream_t stream, const FusedArgs& fz) {
+    if constexpr (!FUSED) {
+        if (group)
+            return launch_gemm<128, true, false, false>(a, b, sa, sb, d, M, N, K, afmt, bfmt, status, stream, fz);
+    }
     const Shape s = pick_shape(M, N);
+#define FP8Q_LAUNCH(BNV, PR) \
+    return launch_gemm<BNV, false, PR, FUSED>(a, b, sa, sb, d, M, N, K, afmt, bfmt, status, stream, fz)
     if (s.pair) {
         switch (s.bn) {
-            case 256: return launch_gemm<256, false, true>(a, b, sa, sb, d, M, N, K, afmt, bfmt, status, stream);
-            case 224: return launch_gemm<224, false, true>(a, b, sa, sb, d, M, N, K, afmt, bfmt, status, stream);
-            case 192: return launch_gemm<192, false, true>(a, b, sa, sb, d, M, N, K, afmt, bfmt, status, stream);
-            case 160: return launch_gemm<160, false, true>(a, b, sa, sb, d, M, N, K, afmt, bfmt, status, stream);
-            default: return launch_gemm<128, false, true>(a, b, sa, sb, d, M, N, K, afmt, bfmt, status, stream);
+            case 256: FP8Q_LAUNCH(256, true);
+            case 224: FP8Q_LAUNCH(224, true);
+            case 192: FP8Q_LAUNCH(192, true);
+            case 160: FP8Q_LAUNCH(160, true);
+            default: FP8Q_LAUNCH(128, true);
         }
     }
     switch (s.bn) {
-        case 256: return launch_gemm<256, false, false>(a, b, sa, sb, d, M, N, K, afmt, bfmt, status, stream);
-        case 192: return launch_gemm<192, false, false>(a, b, sa, sb, d, M, N, K, afmt, bfmt, status, stream);
-        case 160: return launch_gemm<160, false, false>(a, b, sa, sb, d, M, N, K, afmt, bfmt, status, stream);
-        default: return launch_gemm<128, false, false>(a, b, sa, sb, d, M, N, K, afmt, bfmt, status, stream);
+        case 256: FP8Q_LAUNCH(256, false);
+        case 192: FP8Q_LAUNCH(192, false);
+        case 160: FP8Q_LAUNCH(160, false);
+        default: FP8Q_LAUNCH(128, false);
     }
+#undef FP8Q_LAUNCH
+}
+
+int gemm_dispatch(const void* a, const void* b, const float* sa, const float* sb, int group, void* d,
+                  int64_t M, int64_t N, int64_t K, uint32_t afmt, uint32_t bfmt, int* status,
+                  cudaStream_t stream) {
+    return gemm_dispatch_t<false>(a, b, sa, sb, group, d, M, N, K, afmt, bfmt, status, stream, FusedArgs{});
 }
 
 int check_gemm_args(const void* a, const void* b, const float* sa, const float* sb, const void* d,
@@ -652,4 +779,39 @@ extern "C" int fp8_gemm_dgrad(const void* dy_q, const void* w_q, const float* sc
     if (st != FP8Q_OK) return st;
     if (M == 0) return FP8Q_OK;
     return gemm_dispatch(dy_q, w_q, scale_dy, scale_w, 0, dx, M, K, N, FP8Q_E5M2, FP8Q_E4M3, status, stream);
+}
+
+extern "C" size_t fp8_downproj_workspace_bytes(int64_t M) {
+    if (M <= 0) return 0;
+    const size_t blocks = static_cast<size_t>((M + BM - 1) / BM);
+    return (blocks * sizeof(unsigned) + 255) / 256 * 256;
+}
+
+extern "C" int fp8_downproj_fwd(const void* h, const void* wt_q, int64_t M, int64_t N, int64_t K, int act,
+                                const float* scale_x, const float* scale_w, void* act_out, void* x_q,
+                                float* amax_out, unsigned long long* sat_count, void* y, void* workspace,
+                                size_t workspace_bytes, int* status, cudaStream_t stream) {
+    if (act < FP8Q_ACT_IDENTITY || act > FP8Q_ACT_RELU2) return FP8Q_ERR_UNSUPPORTED;
+    if ((!h || !x_q || !workspace) && M != 0) return FP8Q_ERR_NULL;
+    if (!aligned16(h) || !aligned16(act_out) || (reinterpret_cast<uintptr_t>(workspace) & 3u) ||
+        (reinterpret_cast<uintptr_t>(amax_out) & 3u) || (reinterpret_cast<uintptr_t>(sat_count) & 7u))
+        return FP8Q_ERR_ALIGN;
+    if (workspace_bytes < fp8_downproj_workspace_bytes(M)) return FP8Q_ERR_SHAPE;
+    int st = check_gemm_args(x_q, wt_q, scale_x, scale_w, y, M, N, K, status);  // ends with the device check
+    if (st != FP8Q_OK) return st;
+    if (amax_out && cudaMemsetAsync(amax_out, 0, sizeof(float), stream) != cudaSuccess) return FP8Q_ERR_CUDA;
+    if (sat_count && cudaMemsetAsync(sat_count, 0, sizeof(unsigned long long), stream) != cudaSuccess)
+        return FP8Q_ERR_CUDA;
+    if (M == 0) return FP8Q_OK;
+    if (cudaMemsetAsync(workspace, 0, fp8_downproj_workspace_bytes(M), stream) != cudaSuccess) return FP8Q_ERR_CUDA;
+    FusedArgs fz;
+    fz.h = static_cast<const uint4*>(h);
+    fz.act_out = static_cast<uint4*>(act_out);
+    fz.x_q = static_cast<uint2*>(x_q);
+    fz.amax_out = amax_out;
+    fz.sat_out = sat_count;
+    fz.ready = static_cast<unsigned*>(workspace);
+    fz.act = act;
+    return gemm_dispatch_t<true>(x_q, wt_q, scale_x, scale_w, 0, y, M, N, K, FP8Q_E4M3, FP8Q_E4M3, status, stream,
+                                 fz);
 }

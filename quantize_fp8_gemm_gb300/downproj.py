@@ -73,8 +73,13 @@ class Fp8DownProj:
 
     def __init__(self, M: int, K: int, N: int, *, act: int = B.ACT_RELU2, margin: float = 2.0,
                  history_len: int = 1, group: bool = False, with_dgrad: bool = False,
-                 keep_act: bool = True, chunks: int | None = None, device="cuda"):
+                 keep_act: bool = True, chunks: int | None = None, fused: bool | None = None,
+                 device="cuda"):
         self.M, self.K, self.N, self.act, self.group = M, K, N, act, group
+        # the fused quantize + GEMM kernel (opt-in) serves the per-tensor path in one block
+        self.fused = False if fused is None else fused
+        if self.fused and (group or (chunks or 1) != 1):
+            raise ValueError("the fused kernel runs the per-tensor path over the whole batch")
         if chunks is None:  # measured on GB300: overlapping row blocks does not pay off
             chunks = 1
         if chunks < 1 or M % chunks or (chunks > 1 and (M // chunks) % 256):
@@ -90,6 +95,9 @@ class Fp8DownProj:
         self.y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
         self.sat = torch.zeros(1, dtype=torch.int64, device=dev)
         self.gemm_status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.workspace = None
+        if self.fused:
+            self.workspace = torch.empty(max(1, B.fp8_downproj_workspace_bytes(M)), dtype=torch.uint8, device=dev)
         self._side = torch.cuda.Stream(device=dev)  # weight branch and history updates
         hi = torch.cuda.Stream.priority_range()[1]
         self._gemm = torch.cuda.Stream(device=dev, priority=hi)  # GEMM blocks, ahead of quantize blocks
@@ -143,6 +151,16 @@ class Fp8DownProj:
                            status=self.gemm_status)
         return self.y
 
+    def quantize_and_gemm(self, H: torch.Tensor, scale_x: torch.Tensor | None = None,
+                          scale_w: torch.Tensor | None = None) -> torch.Tensor:
+        """a1-a5 and a9 in the fused kernel (same results as quantize() then gemm())."""
+        scale_x = self.x.scale if scale_x is None else scale_x
+        scale_w = self.w.scale if scale_w is None else scale_w
+        B.fp8_downproj_fwd(H, self.wt_q, scale_x, scale_w, self.x_q, self.y, self.workspace, act=self.act,
+                           act_out=self.act_bf16, amax_out=self.x.amax, sat_count=self.sat,
+                           status=self.gemm_status)
+        return self.y
+
     # -- a6 -------------------------------------------------------------------
     def update_scales(self) -> None:
         if not self.group:
@@ -152,7 +170,9 @@ class Fp8DownProj:
     def step(self, H: torch.Tensor, W: torch.Tensor) -> torch.Tensor:
         """One forward step: cast W, fused quantize of H, FP8 GEMM, history updates.
 
-        The batch is processed in ``chunks`` row blocks.  The current stream
+        With ``fused`` (per-tensor scales only) the quantize and the GEMM are
+        one kernel (fp8_downproj_fwd).  Otherwise the batch is
+        processed in ``chunks`` row blocks.  The current stream
         quantizes the blocks one after the other; a high-priority stream runs
         each block's GEMM as soon as that block is quantized, so the
         compute-bound GEMM of block i overlaps the memory-bound quantize of
@@ -163,10 +183,20 @@ class Fp8DownProj:
         main, side, gs = torch.cuda.current_stream(), self._side, self._gemm
         sx, sw = self.x.scale, self.w.scale  # this step's slots
         side.wait_stream(main)
+        w_ready = torch.cuda.Event()
         with torch.cuda.stream(side):
             self.cast_weight(W, sw)
+            w_ready.record(side)
             if not self.group:
                 self.w.update()
+        if self.fused:
+            main.wait_event(w_ready)  # W_q^T ready; W's history update runs beside the kernel
+            self.quantize_and_gemm(H, sx, sw)
+            side.wait_stream(main)  # this step's amax is final
+            with torch.cuda.stream(side):
+                self.x.update()
+            main.wait_stream(side)
+            return self.y
         gs.wait_stream(side)  # W_q^T ready (and everything before this step)
         block = self.M // self.chunks
         for i in range(self.chunks):

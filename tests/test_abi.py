@@ -143,3 +143,23 @@ def test_quant_ex_flags(lib):
     assert f(1) == ERR_UNSUPPORTED  # valid flags: only the missing sm_103 device is left
     assert f(0) == ERR_UNSUPPORTED
     assert lib.fp8_quant_fused_ex(None, 64, 256, 2, 0, A, A, A, None, A, A, None, 1, 1, None) == ERR_NULL
+
+
+def test_fused_argument_checks(lib):
+    f = lambda ws=A, wsb=1 << 20, h=A, M=256, act=2: lib.fp8_downproj_fwd(
+        h, A, M, 128, 256, act, A, A, A, A, A, A, A, ws, wsb, None, None)
+    lib.fp8_downproj_fwd.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64,
+                                     ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p,
+                                     ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,
+                                     ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p,
+                                     ctypes.c_void_p]
+    lib.fp8_downproj_workspace_bytes.argtypes = [ctypes.c_int64]
+    lib.fp8_downproj_workspace_bytes.restype = ctypes.c_size_t
+    assert lib.fp8_downproj_workspace_bytes(256) == 256
+    assert lib.fp8_downproj_workspace_bytes(129 * 128) == 768
+    assert f(ws=None) == ERR_NULL
+    assert f(h=None) == ERR_NULL
+    assert f(wsb=4) == ERR_SHAPE
+    assert f(act=5) == ERR_UNSUPPORTED
+    assert f(h=A + 8) == ERR_ALIGN
+    assert f() == ERR_UNSUPPORTED  # no sm_103 device here

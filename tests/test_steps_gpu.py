@@ -34,11 +34,14 @@ class OracleRecurrence:
         return st
 
 
-def test_gpt2s_ten_steps_fresh_inputs():
+@pytest.mark.parametrize("fused", [False, True])
+def test_gpt2s_ten_steps_fresh_inputs(fused):
+    """Ten steps with the separate quantize and GEMM kernels, and with the
+    fused kernel (fp8_downproj_fwd) in their place."""
     w = WL.WORKLOADS["gpt2s"]
     W_bits = WL.w_down(w)
     H0 = WL.h_preact(w, 0)
-    dp = Fp8DownProj(w.M, w.K, w.N, margin=w.margin, history_len=w.history_len)
+    dp = Fp8DownProj(w.M, w.K, w.N, margin=w.margin, history_len=w.history_len, fused=fused)
     Wd = WL.bf16_tensor(W_bits).cuda()
     dp.calibrate(WL.bf16_tensor(H0).cuda(), Wd)
     ox, ow = OracleRecurrence(w.history_len, w.margin), OracleRecurrence(w.history_len, w.margin)
