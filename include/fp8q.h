@@ -208,6 +208,37 @@ int fp8_downproj_fwd(const void* h, const void* wt_q, int64_t M, int64_t N, int6
                      int* status, cudaStream_t stream);
 
 /*
+ * fp8_downproj_fwd_noalloc -- fp8_downproj_fwd without a caller workspace
+ *
+ * No counterpart in the method's sources: a variant for callers that must
+ * not allocate device memory.  Such callers include a plugin that a host
+ * application hands only its input and output buffers (the host owns every
+ * other byte of device memory under a fixed budget); code on a latency path,
+ * where cudaFree (and, when the pool must grow, cudaMalloc) synchronizes the
+ * whole device and stalls other streams; and code that runs while a stream is
+ * being captured, where allocation calls are not allowed.
+ *
+ * Same arguments, results and error rules as fp8_downproj_fwd, minus
+ * `workspace`: the per-block ready counts live in a fixed array of this
+ * library's own device memory (FP8Q_NOALLOC_MAX_M / 128 counters, 8 KiB),
+ * which every device that loads the library holds until the process exits.
+ *   M > FP8Q_NOALLOC_MAX_M  -> FP8Q_ERR_SHAPE (use fp8_downproj_fwd)
+ * The call allocates nothing: no cudaMalloc / cudaFree, no allocating
+ * library routine.  The first call with M > 0 on a device looks the array's
+ * address up (cudaGetSymbolAddress, with that device current) and keeps it;
+ * make that first call before any stream capture.  Every call clears the
+ * counters it uses (stream-ordered) before its kernel starts, since the array
+ * keeps the previous call's counts.  All calls on a device share the one
+ * array: calls that overlap on the GPU race on it and give wrong results, so
+ * order them on one stream (or with events).
+ */
+#define FP8Q_NOALLOC_MAX_M 262144
+int fp8_downproj_fwd_noalloc(const void* h, const void* wt_q, int64_t M, int64_t N, int64_t K, int act,
+                             const float* scale_x, const float* scale_w,
+                             void* act_out, void* x_q, float* amax_out, unsigned long long* sat_count,
+                             void* y, int* status, cudaStream_t stream);
+
+/*
  * amax_history_update -- delayed per-tensor scale for the next step  [fused][gemms]
  *
  * history[0..L-1] (device floats) is a ring whose newest entry is

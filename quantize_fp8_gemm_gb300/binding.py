@@ -22,6 +22,7 @@ ACT_IDENTITY, ACT_RELU, ACT_RELU2 = 0, 1, 2
 DEV_TIMEOUT, DEV_BAD_AMAX = 1, 2
 ACCUMULATE = 1  # fp8_quant_fused_ex flag
 GROUP = 128
+NOALLOC_MAX_M = 262144  # FP8Q_NOALLOC_MAX_M
 
 _lib = None
 
@@ -52,6 +53,7 @@ def lib() -> ctypes.CDLL:
         L.fp8_downproj_workspace_bytes.argtypes = [i64]
         L.fp8_downproj_workspace_bytes.restype = ctypes.c_size_t
         L.fp8_downproj_fwd.argtypes = [P, P, i64, i64, i64, i32, P, P, P, P, P, P, P, P, ctypes.c_size_t, P, P]
+        L.fp8_downproj_fwd_noalloc.argtypes = [P, P, i64, i64, i64, i32, P, P, P, P, P, P, P, P, P]
         L.fp8q_naive_act.argtypes = [P, i64, i64, i32, P, P]
         L.fp8q_naive_amax.argtypes = [P, i64, P, P]
         L.fp8q_naive_cast.argtypes = [P, i64, i32, P, f32, P, P, P]
@@ -62,8 +64,8 @@ def lib() -> ctypes.CDLL:
         L.fp8q_gemm_test_hold_loads.restype = None
         L.fp8q_gemm_set_tile.argtypes = [i32, i32]
         L.fp8q_gemm_set_tile.restype = i32
-        for fn in ("fp8_quant_fused", "fp8_quant_fused_ex", "fp8_downproj_fwd", "fp8_gemm_fwd", "fp8_gemm_dgrad", "amax_history_update",
-                   "fp8q_naive_act", "fp8q_naive_amax", "fp8q_naive_cast"):
+        for fn in ("fp8_quant_fused", "fp8_quant_fused_ex", "fp8_downproj_fwd", "fp8_downproj_fwd_noalloc",
+                   "fp8_gemm_fwd", "fp8_gemm_dgrad", "amax_history_update", "fp8q_naive_act", "fp8q_naive_amax", "fp8q_naive_cast"):
             getattr(L, fn).restype = i32
         _lib = L
     return _lib
@@ -170,6 +172,22 @@ def fp8_downproj_fwd(h: torch.Tensor, wt_q: torch.Tensor, scale_x: torch.Tensor,
         _ptr(workspace, ws, "workspace"), workspace.numel() * workspace.element_size(),
         _ptr(status, 4, "status"), _stream(stream))
     _check("fp8_downproj_fwd", st)
+
+
+def fp8_downproj_fwd_noalloc(h: torch.Tensor, wt_q: torch.Tensor, scale_x: torch.Tensor, scale_w: torch.Tensor,
+                             x_q: torch.Tensor, y: torch.Tensor, *, act: int = ACT_RELU2, act_out=None,
+                             amax_out=None, sat_count=None, status=None, stream=None) -> None:
+    """fp8_downproj_fwd with the library's own static scratch (M <= NOALLOC_MAX_M); allocates nothing."""
+    M, K = h.shape
+    N = wt_q.shape[0]
+    if wt_q.shape[1] != K:
+        raise ValueError("h [M,K] and wt_q [N,K] disagree on K")
+    st = lib().fp8_downproj_fwd_noalloc(
+        _ptr(h, 2 * M * K, "h"), _ptr(wt_q, N * K, "wt_q"), M, N, K, act, _ptr(scale_x, 4, "scale_x"),
+        _ptr(scale_w, 4, "scale_w"), _ptr(act_out, 2 * M * K, "act_out"), _ptr(x_q, M * K, "x_q"),
+        _ptr(amax_out, 4, "amax_out"), _ptr(sat_count, 8, "sat_count"), _ptr(y, 2 * M * N, "y"),
+        _ptr(status, 4, "status"), _stream(stream))
+    _check("fp8_downproj_fwd_noalloc", st)
 
 
 def amax_history_update(history: torch.Tensor, head: torch.Tensor, amax_new: torch.Tensor, margin: float,

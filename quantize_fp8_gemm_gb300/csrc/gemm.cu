@@ -815,3 +815,72 @@ extern "C" int fp8_downproj_fwd(const void* h, const void* wt_q, int64_t M, int6
     return gemm_dispatch_t<true>(x_q, wt_q, scale_x, scale_w, 0, y, M, N, K, FP8Q_E4M3, FP8Q_E4M3, status, stream,
                                  fz);
 }
+
+// ---------------------------------------------------------------------------
+// fp8_downproj_fwd_noalloc: the fused kernel with its ready counts in this
+// library's own device memory, for callers that cannot allocate (see
+// include/fp8q.h).  The array lives in the module's global memory on every
+// device that loads the library, until the process exits.  In host code
+// g_noalloc_ready only names the symbol: its device address comes from
+// cudaGetSymbolAddress, once per device, with that device current.
+
+static __device__ __align__(256) unsigned g_noalloc_ready[FP8Q_NOALLOC_MAX_M / BM];
+
+static_assert(FP8Q_NOALLOC_MAX_M % BM == 0, "whole 128-row blocks");
+static_assert(sizeof(g_noalloc_ready) % 256 == 0, "the workspace size rounds to 256 bytes");
+
+namespace {
+
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+unsigned* g_noalloc_ptr[kNoAllocMaxDevices] = {};
+
+// The array's device address on the current device (set up on first use).
+int noalloc_scratch(unsigned** out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) return FP8Q_ERR_CUDA;
+    if (dev < 0 || dev >= kNoAllocMaxDevices) return FP8Q_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (!g_noalloc_ptr[dev]) {
+        unsigned* ptr = nullptr;
+        if (cudaGetSymbolAddress(reinterpret_cast<void**>(&ptr), g_noalloc_ready) != cudaSuccess || !ptr)
+            return FP8Q_ERR_CUDA;
+        g_noalloc_ptr[dev] = ptr;
+    }
+    *out = g_noalloc_ptr[dev];
+    return FP8Q_OK;
+}
+
+}  // namespace
+
+extern "C" int fp8_downproj_fwd_noalloc(const void* h, const void* wt_q, int64_t M, int64_t N, int64_t K, int act,
+                                        const float* scale_x, const float* scale_w, void* act_out, void* x_q,
+                                        float* amax_out, unsigned long long* sat_count, void* y, int* status,
+                                        cudaStream_t stream) {
+    if (act < FP8Q_ACT_IDENTITY || act > FP8Q_ACT_RELU2) return FP8Q_ERR_UNSUPPORTED;
+    if ((!h || !x_q) && M != 0) return FP8Q_ERR_NULL;
+    if (!aligned16(h) || !aligned16(act_out) || (reinterpret_cast<uintptr_t>(amax_out) & 3u) ||
+        (reinterpret_cast<uintptr_t>(sat_count) & 7u))
+        return FP8Q_ERR_ALIGN;
+    if (M > FP8Q_NOALLOC_MAX_M) return FP8Q_ERR_SHAPE;  // more row blocks than the array counts
+    int st = check_gemm_args(x_q, wt_q, scale_x, scale_w, y, M, N, K, status);  // ends with the device check
+    if (st != FP8Q_OK) return st;
+    unsigned* ready = nullptr;
+    if (M != 0 && (st = noalloc_scratch(&ready)) != FP8Q_OK) return st;
+    if (amax_out && cudaMemsetAsync(amax_out, 0, sizeof(float), stream) != cudaSuccess) return FP8Q_ERR_CUDA;
+    if (sat_count && cudaMemsetAsync(sat_count, 0, sizeof(unsigned long long), stream) != cudaSuccess)
+        return FP8Q_ERR_CUDA;
+    if (M == 0) return FP8Q_OK;
+    // the previous call's counts are still there: this call's blocks start from zero
+    if (cudaMemsetAsync(ready, 0, fp8_downproj_workspace_bytes(M), stream) != cudaSuccess) return FP8Q_ERR_CUDA;
+    FusedArgs fz;
+    fz.h = static_cast<const uint4*>(h);
+    fz.act_out = static_cast<uint4*>(act_out);
+    fz.x_q = static_cast<uint2*>(x_q);
+    fz.amax_out = amax_out;
+    fz.sat_out = sat_count;
+    fz.ready = ready;
+    fz.act = act;
+    return gemm_dispatch_t<true>(x_q, wt_q, scale_x, scale_w, 0, y, M, N, K, FP8Q_E4M3, FP8Q_E4M3, status, stream,
+                                 fz);
+}

@@ -163,3 +163,13 @@ def test_fused_argument_checks(lib):
     assert f(act=5) == ERR_UNSUPPORTED
     assert f(h=A + 8) == ERR_ALIGN
     assert f() == ERR_UNSUPPORTED  # no sm_103 device here
+
+
+def test_noalloc_argument_checks(lib):
+    f = lambda M=256, h=A, act=2: lib.fp8_downproj_fwd_noalloc(h, A, M, 128, 256, act, A, A, A, A, A, A, A,
+                                                               None, None)
+    assert f(h=None) == ERR_NULL
+    assert f(act=5) == ERR_UNSUPPORTED
+    assert f(h=A + 8) == ERR_ALIGN
+    assert f(M=262144 + 1) == ERR_SHAPE  # beyond the static array's row blocks
+    assert f(M=262144) == ERR_UNSUPPORTED  # at the limit: only the missing sm_103 device is left
