@@ -185,8 +185,8 @@ int fp8_gemm_dgrad(const void* dy_q, const void* w_q,
  *
  * Computes exactly what fp8_quant_fused(h, act, E4M3, scale_x, act_out, x_q,
  * amax_out, sat_count) followed by fp8_gemm_fwd(x_q, wt_q, scale_x, scale_w, y)
- * compute, in one persistent kernel: extra warps of every CTA quantize H in
- * 16-row units and count finished units per 128-row block in `workspace`;
+ * compute, in one persistent kernel: extra warps of every CTA quantize H a
+ * few rows at a time and count finished rows per 128-row block in `workspace`;
  * the GEMM loads a tile's rows of x_q once their block is complete, so the
  * GEMM of early rows overlaps the quantize of later ones and the large tensor
  * is read once.  act_out, amax_out, sat_count may be NULL; x_q is required

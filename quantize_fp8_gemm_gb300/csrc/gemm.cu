@@ -54,18 +54,18 @@ constexpr int kEpiChunkBytes = 32 * 32 * 2;  // one warp's 32 rows x 32 BF16 col
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per wait: far above any real wait
 
 // Fused quantize (FUSED = true): extra warps per CTA turn the BF16
-// pre-activation into the GEMM's E4M3 A operand, 16-row units at a time.
-constexpr int kQuantWarps = 16;
+// pre-activation into the GEMM's E4M3 A operand, a few rows at a time.
+constexpr int kQuantWarps = 24;
 constexpr int kQuantThreads = kQuantWarps * 32;
-constexpr int kUnitRows = 16;   // rows per quantize unit (a 128-row block has 8)
-constexpr int kQuantBatch = 12; // 16-byte loads in flight per quantize thread
+constexpr int kUnitRows = 16;   // rows per quantize unit in the full rounds
+constexpr int kQuantBatch = 8;  // 16-byte loads in flight per quantize thread
 
 template <bool FUSED>
 constexpr int gemm_threads() { return kThreadsGemm + (FUSED ? kQuantThreads : 0); }
 
-// Operands of the fused quantize.  ready[b] counts the 16-row units of 128-row
-// block b whose E4M3 rows are written; the GEMM's producer loads a tile's A
-// rows once its block is complete.
+// Operands of the fused quantize.  ready[b] counts the rows of 128-row block b
+// whose E4M3 codes are written; the GEMM's producer loads a tile's A rows once
+// its block is complete.
 struct FusedArgs {
     const uint4* h;               // H [M,K] BF16, 8 elements per 16 bytes
     uint4* act_out;               // [M,K] BF16 activation copy, or nullptr
@@ -150,41 +150,62 @@ __device__ __forceinline__ uint4 act8_any(int act, uint4 x, uint32_t& amax2) {
     return act8<FP8Q_ACT_IDENTITY>(x, amax2);
 }
 
-// The quantize warps of one CTA (fused kernel): units u = blockIdx.x,
-// blockIdx.x + gridDim.x, ... in row order; after each unit one thread
-// publishes it with a release increment of its block's ready count.
-__device__ __forceinline__ void fused_quantize(const FusedArgs& fz, const float* scale, int64_t M, int64_t K) {
+// One unit of the fused quantize: rows [r0, r1) by all quantize threads of
+// the CTA, then one thread publishes the rows with a release add to the count
+// of each 128-row block they touch.
+__device__ __forceinline__ void fused_quantize_rows(const FusedArgs& fz, float s, int64_t r0, int64_t r1,
+                                                    int64_t K, uint32_t& amax2, uint32_t& nsat) {
     const int qt = threadIdx.x - kThreadsGemm;
-    const int64_t total = M * (K / 8);
-    const int64_t unit_chunks = int64_t(kUnitRows) * (K / 8);
-    const int64_t num_units = (M + kUnitRows - 1) / kUnitRows;
-    const float s = __ldg(scale);
-    uint32_t amax2 = 0, nsat = 0;
-    for (int64_t u = blockIdx.x; u < num_units; u += gridDim.x) {
-        const int64_t c_end = min(u * unit_chunks + unit_chunks, total);
-        for (int64_t c0 = u * unit_chunks + qt; c0 < c_end; c0 += int64_t(kQuantThreads) * kQuantBatch) {
-            uint4 x[kQuantBatch];
+    const int64_t c_end = r1 * (K / 8);
+    for (int64_t c0 = r0 * (K / 8) + qt; c0 < c_end; c0 += int64_t(kQuantThreads) * kQuantBatch) {
+        uint4 x[kQuantBatch];
 #pragma unroll
-            for (int j = 0; j < kQuantBatch; ++j) {
-                const int64_t c = c0 + int64_t(j) * kQuantThreads;
-                x[j] = c < c_end ? ld_stream_v4(fz.h + c) : make_uint4(0, 0, 0, 0);
-            }
+        for (int j = 0; j < kQuantBatch; ++j) {
+            const int64_t c = c0 + int64_t(j) * kQuantThreads;
+            x[j] = c < c_end ? ld_stream_v4(fz.h + c) : make_uint4(0, 0, 0, 0);
+        }
 #pragma unroll
-            for (int j = 0; j < kQuantBatch; ++j) {
-                const int64_t c = c0 + int64_t(j) * kQuantThreads;
-                if (c < c_end) {
-                    const uint4 a = act8_any(fz.act, x[j], amax2);
-                    if (fz.act_out) st_stream_v4(fz.act_out + c, a);
-                    st_v2(fz.x_q + c, cast8<FP8Q_E4M3>(a, s, nsat));
-                }
+        for (int j = 0; j < kQuantBatch; ++j) {
+            const int64_t c = c0 + int64_t(j) * kQuantThreads;
+            if (c < c_end) {
+                const uint4 a = act8_any(fz.act, x[j], amax2);
+                if (fz.act_out) st_stream_v4(fz.act_out + c, a);
+                st_v2(fz.x_q + c, cast8<FP8Q_E4M3>(a, s, nsat));
             }
         }
-        // this unit's E4M3 rows are written by every quantize thread: order them
-        // before the count, which the producer reads before its TMA loads
-        fence_proxy_async_global();
-        named_barrier(1, kQuantThreads);
-        if (qt == 0) red_release_add(fz.ready + (u * kUnitRows) / BM, 1u);
     }
+    // the unit's E4M3 codes are written by every quantize thread: order them
+    // before the counts, which the producer reads before its TMA loads
+    fence_proxy_async_global();
+    named_barrier(1, kQuantThreads);
+    if (qt == 0) {
+        for (int64_t b = r0 / BM; b * BM < r1; ++b) {
+            const int64_t lo = b * BM > r0 ? b * BM : r0;
+            const int64_t hi = (b + 1) * BM < r1 ? (b + 1) * BM : r1;
+            red_release_add(fz.ready + b, static_cast<unsigned>(hi - lo));
+        }
+    }
+}
+
+// The quantize warps of the fused kernel.  Full rounds: every CTA takes one
+// 16-row unit per round, units in row order (CTA c: units c, c + gridDim.x,
+// ...), so rows finish in order across the GPU.  The rows left after the last
+// full round are split evenly over all CTAs (at most 17 rows each), so no SM
+// carries a whole extra unit at the end.
+__device__ __forceinline__ void fused_quantize(const FusedArgs& fz, const float* scale, int64_t M, int64_t K) {
+    const float s = __ldg(scale);
+    uint32_t amax2 = 0, nsat = 0;
+    const int64_t rounds = (M / kUnitRows) / gridDim.x;
+    for (int64_t k = 0; k < rounds; ++k) {
+        const int64_t r0 = (k * gridDim.x + blockIdx.x) * kUnitRows;
+        fused_quantize_rows(fz, s, r0, r0 + kUnitRows, K, amax2, nsat);
+    }
+    const int64_t t0 = rounds * gridDim.x * kUnitRows;
+    const int64_t share = (M - t0 + gridDim.x - 1) / gridDim.x;
+    const int64_t r0 = t0 + blockIdx.x * share;
+    const int64_t r1 = r0 + share < M ? r0 + share : M;
+    if (r0 < r1) fused_quantize_rows(fz, s, r0, r1, K, amax2, nsat);
+    const int qt = threadIdx.x - kThreadsGemm;
     __shared__ uint32_t s_amax[kQuantWarps], s_sat[kQuantWarps];
     uint32_t m = __reduce_max_sync(0xFFFFFFFFu, max16x2(amax2));
     uint32_t c = __reduce_add_sync(0xFFFFFFFFu, nsat);
@@ -323,7 +344,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     if (m0 < M) {
                         const int64_t blk = m0 / BM;
                         const int64_t rows = M - blk * BM < BM ? M - blk * BM : BM;
-                        const unsigned need = static_cast<unsigned>((rows + kUnitRows - 1) / kUnitRows);
+                        const unsigned need = static_cast<unsigned>(rows);
                         if (!wait_ready(fz.ready + blk, need, abort_flag, status)) { ok = false; break; }
                         fence_proxy_async_global();
                     }

@@ -1,7 +1,8 @@
 """The fused quantize + GEMM kernel (fp8_downproj_fwd) against the separate
 fp8_quant_fused + fp8_gemm_fwd calls (bit for bit: same arithmetic, same GEMM
-tiles) and against the oracle.  Shapes leave partial 16-row units, 128-row
-blocks and tiles; every tile shape the dispatcher offers is pinned in turn."""
+tiles) and against the oracle.  Shapes leave partial quantize units (a warp's
+unit is 1 to 128 rows, depending on K), 128-row blocks and tiles; every tile
+shape the dispatcher offers is pinned in turn."""
 import numpy as np
 import pytest
 import torch
@@ -56,7 +57,8 @@ def test_fused_equals_separate_calls(pair, bn):
     try:
         if pair >= 0:
             B.fp8q_gemm_set_tile(pair, bn)
-        for (M, N, K) in [(1000, 1600, 640), (300, 272, 400), (129, 144, 1600), (2048, 768, 3072), (16, 64, 96)]:
+        for (M, N, K) in [(1000, 1600, 640), (300, 272, 400), (129, 144, 1600), (2048, 768, 3072), (16, 64, 96),
+                          (1001, 160, 48), (130, 32, 16)]:
             h, w = _inputs(M, N, K, seed=M + N + K + bn)
             r = _run_both(h, w, B.ACT_RELU2, 20.0, 300.0)
             a1, q1, y1, am1, s1, _ = r["separate"]
