@@ -139,7 +139,46 @@ int fp8_quant_fused_ex(const void* h, int64_t M, int64_t K, int act, int fmt,
                        unsigned flags, cudaStream_t stream);
 
 /*
- * fp8_gemm_fwd -- Y = (X_q . W_q) / (s_x s_w), FP32 accumulation, BF16 out  [gemms][scale]
+ * fp8_quant_fused_batch -- several per-tensor fp8_quant_fused_ex calls in one
+ * kernel launch  [fused][scale]
+ *
+ * The same per-element arithmetic as fp8_quant_fused ("Paradigma Details FP8
+ * and Optimizer Tricks Behind NanoGPT Records", second paragraph; "FP8
+ * training: what it is and how it works", Step 4: the weight's 8-bit copy is
+ * cast from the master copy at every step), applied to n tensors by one grid:
+ * the CTAs of args[0] come first, then those of args[1], and so on.  A
+ * training step casts its weight (transposed copy, identity activation) and
+ * quantizes its activation together, so the GEMM that follows waits on one
+ * kernel instead of two.
+ *   args[i]   the arguments of one fp8_quant_fused_ex call (fields of the same
+ *             names and meaning); group_scales_out must be NULL (per-tensor
+ *             scales only), flags 0 or FP8Q_ACCUMULATE.
+ *   n         1 .. FP8Q_BATCH_MAX.
+ * Results equal the n separate calls.  The tensors run concurrently, so no
+ * entry may read what another entry writes, and outputs must not overlap.
+ * Every entry is checked before anything is enqueued: the first failing
+ * entry's status is returned and nothing runs.  amax_out / sat_count of an
+ * entry without FP8Q_ACCUMULATE are zeroed (stream-ordered) before the launch.
+ */
+#define FP8Q_BATCH_MAX 4
+typedef struct fp8q_quant_args {
+    const void* h;
+    int64_t M, K;
+    int act, fmt;
+    const float* scale;
+    void* act_out;
+    void* q_out;
+    void* q_t_out;
+    float* amax_out;
+    unsigned long long* sat_count;
+    float* group_scales_out;
+    int group_rows;
+    unsigned flags;
+} fp8q_quant_args;
+int fp8_quant_fused_batch(const fp8q_quant_args* args, int n, cudaStream_t stream);
+
+/*
+ * fp8_gemm_fwd --Y = (X_q . W_q) / (s_x s_w), FP32 accumulation, BF16 out  [gemms][scale]
  *
  *   x_q     device [M,K] E4M3 (the activation, K contiguous).
  *   wt_q    device [N,K] E4M3: the weight W [K,N] stored transposed, i.e. the

@@ -21,6 +21,7 @@ E4M3, E5M2 = 0, 1
 ACT_IDENTITY, ACT_RELU, ACT_RELU2 = 0, 1, 2
 DEV_TIMEOUT, DEV_BAD_AMAX = 1, 2
 ACCUMULATE = 1  # fp8_quant_fused_ex flag
+BATCH_MAX = 4  # FP8Q_BATCH_MAX
 GROUP = 128
 NOALLOC_MAX_M = 262144  # FP8Q_NOALLOC_MAX_M
 
@@ -48,6 +49,7 @@ def lib() -> ctypes.CDLL:
         L.fp8_quant_fused.argtypes = [P, i64, i64, i32, i32, P, P, P, P, P, P, P, i32, P]
         L.fp8_quant_fused_ex.argtypes = [P, i64, i64, i32, i32, P, P, P, P, P, P, P, i32, ctypes.c_uint, P]
         L.fp8_gemm_fwd.argtypes = [P, P, P, P, i32, P, i64, i64, i64, P, P]
+        L.fp8_quant_fused_batch.argtypes = [P, i32, P]
         L.fp8_gemm_dgrad.argtypes = [P, P, P, P, P, i64, i64, i64, P, P]
         L.amax_history_update.argtypes = [P, i32, P, P, f32, i32, P, P, P]
         L.fp8_downproj_workspace_bytes.argtypes = [i64]
@@ -64,8 +66,9 @@ def lib() -> ctypes.CDLL:
         L.fp8q_gemm_test_hold_loads.restype = None
         L.fp8q_gemm_set_tile.argtypes = [i32, i32]
         L.fp8q_gemm_set_tile.restype = i32
-        for fn in ("fp8_quant_fused", "fp8_quant_fused_ex", "fp8_downproj_fwd", "fp8_downproj_fwd_noalloc",
-                   "fp8_gemm_fwd", "fp8_gemm_dgrad", "amax_history_update", "fp8q_naive_act", "fp8q_naive_amax", "fp8q_naive_cast"):
+        for fn in ("fp8_quant_fused", "fp8_quant_fused_ex", "fp8_quant_fused_batch", "fp8_downproj_fwd",
+                   "fp8_downproj_fwd_noalloc", "fp8_gemm_fwd", "fp8_gemm_dgrad", "amax_history_update",
+                   "fp8q_naive_act", "fp8q_naive_amax", "fp8q_naive_cast"):
             getattr(L, fn).restype = i32
         _lib = L
     return _lib
@@ -118,6 +121,36 @@ def fp8_quant_fused_ex(h: torch.Tensor, act: int, fmt: int, scale: torch.Tensor 
         _ptr(amax_out, 4, "amax_out"), _ptr(sat_count, 8, "sat_count"),
         _ptr(group_scales_out, 4 * ng, "group_scales_out"), group_rows, flags, _stream(stream))
     _check(name, st)
+
+
+class QuantArgs(ctypes.Structure):
+    """fp8q_quant_args: the arguments of one quantize call in fp8_quant_fused_batch."""
+    _fields_ = [("h", ctypes.c_void_p), ("M", ctypes.c_int64), ("K", ctypes.c_int64), ("act", ctypes.c_int),
+                ("fmt", ctypes.c_int), ("scale", ctypes.c_void_p), ("act_out", ctypes.c_void_p),
+                ("q_out", ctypes.c_void_p), ("q_t_out", ctypes.c_void_p), ("amax_out", ctypes.c_void_p),
+                ("sat_count", ctypes.c_void_p), ("group_scales_out", ctypes.c_void_p),
+                ("group_rows", ctypes.c_int), ("flags", ctypes.c_uint)]
+
+
+def quant_args(h: torch.Tensor, act: int, fmt: int, scale: torch.Tensor, *, act_out=None, q_out=None,
+               q_t_out=None, amax_out=None, sat_count=None, flags: int = 0) -> QuantArgs:
+    """One entry of fp8_quant_fused_batch (per-tensor scale), with the byte-size
+    checks of fp8_quant_fused.  The entry holds references to its tensors, so
+    temporaries passed here live as long as the entry."""
+    M, K = h.shape
+    n = M * K
+    v = lambda t, nb, name: (lambda p: None if p is None else p.value)(_ptr(t, nb, name))
+    a = QuantArgs(v(h, 2 * n, "h"), M, K, act, fmt, v(scale, 4, "scale"), v(act_out, 2 * n, "act_out"),
+                  v(q_out, n, "q_out"), v(q_t_out, n, "q_t_out"), v(amax_out, 4, "amax_out"),
+                  v(sat_count, 8, "sat_count"), None, 1, flags)
+    a._tensors = (h, scale, act_out, q_out, q_t_out, amax_out, sat_count)
+    return a
+
+
+def fp8_quant_fused_batch(entries, stream=None) -> None:
+    """Several per-tensor quantize calls (QuantArgs from quant_args) in one launch."""
+    arr = (QuantArgs * len(entries))(*entries)
+    _check("fp8_quant_fused_batch", lib().fp8_quant_fused_batch(arr, len(entries), _stream(stream)))
 
 
 def fp8_gemm_fwd(x_q: torch.Tensor, wt_q: torch.Tensor, scale_x: torch.Tensor, scale_w: torch.Tensor,

@@ -28,12 +28,14 @@ FUSED_MIN_ROWS = 32768  # default switch to the fused kernel (per-tensor scales)
 class DelayedScale:
     """Device-resident delayed-scaling state of one tensor role.
 
-    history [L] (ring, newest at ``head``), the amax the next cast writes, a
-    status word for FP8Q_DEV_* flags, and two scale slots.  A step casts with
-    the current slot and the GEMM dequantises with it, while the history
-    update writes the next step's scale into the other slot; the two can
-    therefore run concurrently.  ``update()`` then makes the other slot
-    current (a host-side switch).
+    history [L] (ring, newest at ``head``), a status word for FP8Q_DEV_*
+    flags, and two slots of (scale, amax, saturation count).  A step casts
+    with the current slot's scale into the current slot's amax / count, and
+    the GEMM dequantises with that scale, while the history update writes the
+    next step's scale into the other slot; the two can therefore run
+    concurrently.  ``update()`` also zeroes the other slot's amax and count,
+    so the next step's cast can accumulate into them without clearing them
+    first, and then makes the other slot current (a host-side switch).
     """
 
     def __init__(self, fmt: int, margin: float, history_len: int = 1, device="cuda"):
@@ -42,8 +44,30 @@ class DelayedScale:
         self.head = torch.zeros(1, dtype=torch.int32, device=device)
         self.scales = torch.ones(2, dtype=torch.float32, device=device)
         self.slot = 0
-        self.amax = torch.zeros(1, dtype=torch.float32, device=device)
+        self.amaxes = torch.zeros(2, dtype=torch.float32, device=device)
+        self.sats = torch.zeros(2, dtype=torch.int64, device=device)
         self.status = torch.zeros(1, dtype=torch.int32, device=device)
+        self.clean = True  # the current slot's amax and count are zero
+
+    @property
+    def amax(self) -> torch.Tensor:
+        """The amax the next cast writes (current slot)."""
+        return self.amaxes[self.slot:self.slot + 1]
+
+    @property
+    def sat(self) -> torch.Tensor:
+        """The saturation count the next cast writes (current slot)."""
+        return self.sats[self.slot:self.slot + 1]
+
+    @property
+    def last_amax(self) -> torch.Tensor:
+        """The amax the last update() pushed into the history."""
+        return self.amaxes[1 - self.slot:2 - self.slot]
+
+    @property
+    def last_sat(self) -> torch.Tensor:
+        """The saturation count of the cast before the last update()."""
+        return self.sats[1 - self.slot:2 - self.slot]
 
     @property
     def scale(self) -> torch.Tensor:
@@ -58,11 +82,15 @@ class DelayedScale:
         nxt.copy_(self.scale)
         B.amax_history_update(self.history, self.head, self.amax, self.margin, self.fmt, nxt,
                               status=self.status)
+        self.amaxes[1 - self.slot:2 - self.slot].zero_()
+        self.sats[1 - self.slot:2 - self.slot].zero_()
         self.slot ^= 1
+        self.clean = True
 
     def seed(self, amax: float) -> None:
         """Start the history from a known previous amax (e.g. a calibration pass)."""
         self.amax.fill_(float(amax))
+        self.clean = False
         self.update()
 
 
@@ -102,7 +130,6 @@ class Fp8DownProj:
         self.wt_q = torch.empty(N, K, dtype=torch.uint8, device=dev)
         self.w_q = torch.empty(K, N, dtype=torch.uint8, device=dev) if with_dgrad else None
         self.y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
-        self.sat = torch.zeros(1, dtype=torch.int64, device=dev)
         self.gemm_status = torch.zeros(1, dtype=torch.int32, device=dev)
         self.workspace = None
         if self.fused:
@@ -116,10 +143,16 @@ class Fp8DownProj:
             self.x_gscale = torch.empty(M, K // B.GROUP, dtype=torch.float32, device=dev)
             self.w_gscale = torch.empty(K // B.GROUP, N // B.GROUP, dtype=torch.float32, device=dev)
 
+    @property
+    def sat(self) -> torch.Tensor:
+        """Saturation count of the most recent quantize of H."""
+        return self.x.last_sat if self.x.clean else self.x.sat
+
     # -- a7 -------------------------------------------------------------------
     def cast_weight(self, W: torch.Tensor, scale: torch.Tensor | None = None) -> None:
         """W [K,N] BF16 -> W_q^T [N,K] (forward operand) and, if kept, W_q [K,N]."""
         scale = self.w.scale if scale is None else scale
+        self.w.clean = False
         if self.group:
             B.fp8_quant_fused(W, B.ACT_IDENTITY, B.E4M3, None, q_out=self.w_q, q_t_out=self.wt_q,
                               amax_out=self.w.amax, group_scales_out=self.w_gscale,
@@ -135,14 +168,15 @@ class Fp8DownProj:
         scale = self.x.scale if scale is None else scale
         r0, r1 = (0, self.M) if rows is None else rows
         flags = B.ACCUMULATE if r0 > 0 else 0
+        self.x.clean = False
         act_out = None if self.act_bf16 is None else self.act_bf16[r0:r1]
         if self.group:
             B.fp8_quant_fused_ex(H[r0:r1], self.act, B.E4M3, None, act_out=act_out, q_out=self.x_q[r0:r1],
-                                 amax_out=self.x.amax, sat_count=self.sat,
+                                 amax_out=self.x.amax, sat_count=self.x.sat,
                                  group_scales_out=self.x_gscale[r0:r1], group_rows=1, flags=flags)
         else:
             B.fp8_quant_fused_ex(H[r0:r1], self.act, B.E4M3, scale, act_out=act_out,
-                                 q_out=self.x_q[r0:r1], amax_out=self.x.amax, sat_count=self.sat,
+                                 q_out=self.x_q[r0:r1], amax_out=self.x.amax, sat_count=self.x.sat,
                                  flags=flags)
 
     # -- a9 -------------------------------------------------------------------
@@ -165,8 +199,9 @@ class Fp8DownProj:
         """a1-a5 and a9 in the fused kernel (same results as quantize() then gemm())."""
         scale_x = self.x.scale if scale_x is None else scale_x
         scale_w = self.w.scale if scale_w is None else scale_w
+        self.x.clean = False
         B.fp8_downproj_fwd(H, self.wt_q, scale_x, scale_w, self.x_q, self.y, self.workspace, act=self.act,
-                           act_out=self.act_bf16, amax_out=self.x.amax, sat_count=self.sat,
+                           act_out=self.act_bf16, amax_out=self.x.amax, sat_count=self.x.sat,
                            status=self.gemm_status)
         return self.y
 
@@ -189,6 +224,8 @@ class Fp8DownProj:
         first quantize, then updates the activation's history once the last
         block is quantized (the updates write the other scale slot, so they
         never race the GEMMs' reads).  All branches join the current stream."""
+        if not self.fused and not self.group and self.chunks == 1:
+            return self._step_one_launch_cast(H, W)
         main, side, gs = torch.cuda.current_stream(), self._side, self._gemm
         sx, sw = self.x.scale, self.w.scale  # this step's slots
         side.wait_stream(main)
@@ -221,6 +258,34 @@ class Fp8DownProj:
             with torch.cuda.stream(side):
                 self.x.update()
         main.wait_stream(gs)
+        main.wait_stream(side)
+        return self.y
+
+    def _step_one_launch_cast(self, H: torch.Tensor, W: torch.Tensor) -> torch.Tensor:
+        """The per-tensor step with separate quantize and GEMM kernels: the W cast
+        and the quantize of H share one launch (fp8_quant_fused_batch), and the
+        GEMM follows on the same stream, so its set-up overlaps the quantize's
+        last CTAs.  Both casts accumulate into their slot's amax / count, which
+        the previous update() zeroed (no memset ahead of the cast).  The
+        history updates run on the side stream beside the GEMM."""
+        main, side = torch.cuda.current_stream(), self._side
+        sx, sw = self.x.scale, self.w.scale
+        fx = B.ACCUMULATE if self.x.clean else 0
+        fw = B.ACCUMULATE if self.w.clean else 0
+        B.fp8_quant_fused_batch([
+            B.quant_args(W, B.ACT_IDENTITY, B.E4M3, sw, q_out=self.w_q, q_t_out=self.wt_q,
+                         amax_out=self.w.amax, flags=fw),
+            B.quant_args(H, self.act, B.E4M3, sx, act_out=self.act_bf16, q_out=self.x_q,
+                         amax_out=self.x.amax, sat_count=self.x.sat, flags=fx),
+        ])
+        self.x.clean = self.w.clean = False
+        cast_done = torch.cuda.Event()
+        cast_done.record(main)
+        self.gemm(sx, sw)
+        side.wait_event(cast_done)  # this step's amaxes are final
+        with torch.cuda.stream(side):
+            self.x.update()
+            self.w.update()
         main.wait_stream(side)
         return self.y
 

@@ -173,3 +173,24 @@ def test_noalloc_argument_checks(lib):
     assert f(h=A + 8) == ERR_ALIGN
     assert f(M=262144 + 1) == ERR_SHAPE  # beyond the static array's row blocks
     assert f(M=262144) == ERR_UNSUPPORTED  # at the limit: only the missing sm_103 device is left
+
+
+def test_batch_quant_argument_checks(lib):
+    from quantize_fp8_gemm_gb300 import binding as B
+    lib.fp8_quant_fused_batch.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p]
+    assert ctypes.sizeof(B.QuantArgs) == 96
+    good = B.QuantArgs(A, 64, 256, 2, 0, A, A, A, None, A, A, None, 1, 0)
+    arr = (B.QuantArgs * 2)(good, good)
+    assert lib.fp8_quant_fused_batch(None, 1, None) == ERR_NULL
+    assert lib.fp8_quant_fused_batch(arr, 0, None) == ERR_SHAPE
+    assert lib.fp8_quant_fused_batch(arr, 5, None) == ERR_SHAPE
+    arr[1].K = 40
+    assert lib.fp8_quant_fused_batch(arr, 2, None) == ERR_SHAPE  # the second entry's own check
+    arr[1].K = 256
+    arr[1].group_scales_out = A
+    assert lib.fp8_quant_fused_batch(arr, 2, None) == ERR_UNSUPPORTED  # per-tensor entries only
+    arr[1].group_scales_out = None
+    arr[1].flags = 2
+    assert lib.fp8_quant_fused_batch(arr, 2, None) == ERR_UNSUPPORTED
+    arr[1].flags = 1
+    assert lib.fp8_quant_fused_batch(arr, 2, None) == ERR_UNSUPPORTED  # valid: no sm_103 device here

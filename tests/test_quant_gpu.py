@@ -183,3 +183,74 @@ def test_full_size_workload_bit_exact(name):
         gg = run_quant(h, B.ACT_IDENTITY, B.E4M3, None, want_act=False, group_rows=1)
         rg = O.quant_group(h, O.ACT_IDENTITY, O.E4M3, 1, want_act=False)
         assert_same(gg, rg, ["q", "amax", "sat", "scales"])
+
+
+def _outs(M, K, act=True, q=True, qt=False):
+    return dict(a=torch.empty(M, K, dtype=torch.bfloat16, device="cuda") if act else None,
+                q=torch.empty(M, K, dtype=torch.uint8, device="cuda") if q else None,
+                qt=torch.empty(K, M, dtype=torch.uint8, device="cuda") if qt else None,
+                amax=torch.full((1,), -1.0, device="cuda"),
+                sat=torch.full((1,), 7, dtype=torch.int64, device="cuda"))
+
+
+def test_batch_equals_separate_calls():
+    """fp8_quant_fused_batch over a weight (identity, transposed and row-major
+    copies), an activation (ReLU^2 + BF16 copy), a gradient (E5M2), an empty
+    tensor and a ragged ReLU tensor: every output equals its own
+    fp8_quant_fused call bit for bit, and ACCUMULATE folds into the values
+    already there."""
+    cases = [  # (M, K, act, fmt, scale, want act_out, want q_t_out, flags)
+        (3072, 768, B.ACT_IDENTITY, B.E4M3, 2667.0, False, True, 0),
+        (1000, 640, B.ACT_RELU2, B.E4M3, 20.0, True, False, 0),
+        (0, 256, B.ACT_RELU, B.E4M3, 1.0, True, False, 0),
+        (517, 48, B.ACT_RELU, B.E5M2, 9000.0, True, False, B.ACCUMULATE),
+    ]
+    ins, sep, bat, entries = [], [], [], []
+    for i, (M, K, act, fmt, sc, wa, wqt, flags) in enumerate(cases):
+        h = dev_bf16(_rand_bits(M, K, seed=100 + i, std=1.5))
+        s = dev_f32(sc)
+        r, b = _outs(M, K, wa, True, wqt), _outs(M, K, wa, True, wqt)
+        if flags:
+            for d in (r, b):
+                d["amax"].fill_(0.5)
+                d["sat"].fill_(3)
+        B.fp8_quant_fused_ex(h, act, fmt, s, act_out=r["a"], q_out=r["q"], q_t_out=r["qt"], amax_out=r["amax"],
+                             sat_count=r["sat"], flags=flags)
+        entries.append(B.quant_args(h, act, fmt, s, act_out=b["a"], q_out=b["q"], q_t_out=b["qt"],
+                                    amax_out=b["amax"], sat_count=b["sat"], flags=flags))
+        ins.append((h, s))
+        sep.append(r)
+        bat.append(b)
+    B.fp8_quant_fused_batch(entries)
+    torch.cuda.synchronize()
+    for (M, K, *_), r, b in zip(cases, sep, bat):
+        for key in ("a", "q", "qt"):
+            if r[key] is not None and M:
+                assert torch.equal(r[key].view(torch.uint8), b[key].view(torch.uint8)), (M, K, key)
+        assert r["amax"].item() == b["amax"].item() and r["sat"].item() == b["sat"].item(), (M, K)
+    assert sep[2]["amax"].item() == 0.0 and sep[2]["sat"].item() == 0  # empty entry: zeroed
+    assert sep[3]["amax"].item() >= 0.5 and sep[3]["sat"].item() >= 3  # accumulated
+
+
+def test_batch_against_oracle():
+    """The step's pair (W transposed cast + H ReLU^2 quantize) in one launch, against the oracle."""
+    w_bits = _rand_bits(384, 272, seed=7, std=0.05)
+    h_bits = _rand_bits(300, 384, seed=8, std=1.2)
+    sw, sx = 3000.0, 25.0
+    W, H = dev_bf16(w_bits), dev_bf16(h_bits)
+    wt = torch.empty(272, 384, dtype=torch.uint8, device="cuda")
+    o = _outs(300, 384)
+    aw = torch.zeros(1, device="cuda")
+    B.fp8_quant_fused_batch([
+        B.quant_args(W, B.ACT_IDENTITY, B.E4M3, dev_f32(sw), q_t_out=wt, amax_out=aw),
+        B.quant_args(H, B.ACT_RELU2, B.E4M3, dev_f32(sx), act_out=o["a"], q_out=o["q"], amax_out=o["amax"],
+                     sat_count=o["sat"]),
+    ])
+    torch.cuda.synchronize()
+    rw = O.quant(w_bits, O.ACT_IDENTITY, O.E4M3, sw, want_act=False)
+    rx = O.quant(h_bits, O.ACT_RELU2, O.E4M3, sx)
+    assert np.array_equal(host_u8(wt), rw["q"].T)
+    assert aw.item() == rw["amax"]
+    assert np.array_equal(host_u8(o["q"]), rx["q"])
+    assert np.array_equal(host_bits16(o["a"]), rx["act"])
+    assert o["amax"].item() == rx["amax"] and o["sat"].item() == rx["sat"]

@@ -193,5 +193,5 @@ def test_row_blocks_match_one_block(chunks):
         assert torch.equal(y1.view(torch.int16), y2.view(torch.int16)), f"step {t}: Y"
         assert torch.equal(one.x_q, blk.x_q) and torch.equal(one.act_bf16.view(torch.int16),
                                                              blk.act_bf16.view(torch.int16))
-        assert one.sat.item() == blk.sat.item() and one.x.amax.item() == blk.x.amax.item()
+        assert one.sat.item() == blk.sat.item() and one.x.last_amax.item() == blk.x.last_amax.item()
         assert torch.equal(one.x.scale, blk.x.scale) and torch.equal(one.w.scale, blk.w.scale)
