@@ -232,8 +232,8 @@ int fp8_gemm_dgrad(const void* dy_q, const void* w_q,
  * (it is the GEMM's operand and the E4M3 copy).
  *   workspace  device scratch of at least fp8_downproj_workspace_bytes(M)
  *              bytes, 4-byte aligned, owned by the caller; zeroed by this call
- *              (stream-ordered).  Two fused calls must not share it
- *              concurrently.
+ *              (stream-ordered), and left zero by the kernel when it
+ *              finishes.  Two fused calls must not share it concurrently.
  * The kernel occupies every SM with one CTA and its CTAs wait on each
  * other's quantize work (bounded: a wait that runs out sets
  * FP8Q_DEV_TIMEOUT), so do not run two of them on the GPU at the same time.
@@ -245,6 +245,53 @@ int fp8_downproj_fwd(const void* h, const void* wt_q, int64_t M, int64_t N, int6
                      void* act_out, void* x_q, float* amax_out, unsigned long long* sat_count,
                      void* y, void* workspace, size_t workspace_bytes,
                      int* status, cudaStream_t stream);
+
+/*
+ * fp8_downproj_fwd_ex -- the whole forward step's casts and GEMM in one kernel
+ * [fused][gemms], with the weight cast folded in and no clearing ahead of it
+ *
+ * As fp8_downproj_fwd, plus:
+ *   w        device W [K,N] BF16 (the master weight), or NULL.  When set, the
+ *            kernel first casts it exactly as fp8_quant_fused(w, K, N,
+ *            IDENTITY, E4M3, scale_w, q_out = w_q, q_t_out = wt_q, amax_out =
+ *            amax_w) would ("FP8 training: what it is and how it works", Step
+ *            4: the 8-bit weight copy is cast from the master copy every
+ *            step), and the GEMM reads the W_q^T it wrote: wt_q is then an
+ *            OUTPUT.  When NULL, wt_q is the GEMM's input as before and w_q,
+ *            amax_w are ignored.
+ *   w_q      device [K,N] E4M3 (the dgrad operand) or NULL.
+ *   amax_w   device float or NULL: max |W|.
+ *   flags    0, or FP8Q_ACCUMULATE: nothing is zeroed before the kernel
+ *            (amax_x, sat_count, amax_w fold into their values; the workspace
+ *            must already be zero -- zero-filled before first use, then kept
+ *            zero by the kernel).  After a call that reported FP8Q_DEV_TIMEOUT
+ *            the workspace may hold counts: zero it again.
+ *   hist_x, hist_w  NULL, or the arguments of amax_history_update_ex for X
+ *            (amax_new = amax_x) and for W (amax_new = amax_w; needs w): the
+ *            last CTA of the kernel runs these updates on the final amax
+ *            values, so a delayed-scaling step is this one launch.  The
+ *            structs are read during the call only.  Need M > 0.
+ * Results equal fp8_quant_fused_ex on W and H followed by fp8_gemm_fwd (and
+ * amax_history_update_ex on X and W).
+ */
+typedef struct fp8q_history_args {
+    float* history;                 /* as amax_history_update_ex            */
+    int L;
+    int* head;
+    float margin;
+    int fmt;
+    const float* scale_prev;        /* or NULL                               */
+    float* scale_out;
+    int* status;                    /* or NULL                               */
+    float* amax_clear;              /* or NULL                               */
+    unsigned long long* sat_clear;  /* or NULL                               */
+} fp8q_history_args;
+int fp8_downproj_fwd_ex(const void* h, const void* w, void* wt_q, int64_t M, int64_t N, int64_t K,
+                        int act, const float* scale_x, const float* scale_w,
+                        void* act_out, void* x_q, float* amax_x, unsigned long long* sat_count,
+                        void* w_q, float* amax_w, void* y, void* workspace, size_t workspace_bytes,
+                        const fp8q_history_args* hist_x, const fp8q_history_args* hist_w,
+                        unsigned flags, int* status, cudaStream_t stream);
 
 /*
  * fp8_downproj_fwd_noalloc -- fp8_downproj_fwd without a caller workspace
@@ -259,7 +306,8 @@ int fp8_downproj_fwd(const void* h, const void* wt_q, int64_t M, int64_t N, int6
  *
  * Same arguments, results and error rules as fp8_downproj_fwd, minus
  * `workspace`: the per-block ready counts live in a fixed array of this
- * library's own device memory (FP8Q_NOALLOC_MAX_M / 128 counters, 8 KiB),
+ * library's own device memory (FP8Q_NOALLOC_MAX_M / 128 + 64 counters, 8,448
+ * bytes),
  * which every device that loads the library holds until the process exits.
  *   M > FP8Q_NOALLOC_MAX_M  -> FP8Q_ERR_SHAPE (use fp8_downproj_fwd)
  * The call allocates nothing: no cudaMalloc / cudaFree, no allocating
@@ -296,6 +344,24 @@ int fp8_downproj_fwd_noalloc(const void* h, const void* wt_q, int64_t M, int64_t
 int amax_history_update(float* history, int L, int* head, const float* amax_new,
                         float margin, int fmt, float* scale_out, int* status,
                         cudaStream_t stream);
+
+/*
+ * amax_history_update_ex -- amax_history_update for a step that keeps its
+ * scale, amax and saturation count in two alternating slots  [fused][gemms]
+ *
+ * The same update, plus, in the same launch:
+ *   scale_prev  device float or NULL.  When the amax is unusable, *scale_out
+ *               gets *scale_prev (the scale the step just used) instead of
+ *               being left alone, so scale_out may be the other slot.
+ *   amax_clear  device float or NULL: set to 0 (the next step's cast folds
+ *               its maximum into it).  Must not be amax_new.
+ *   sat_clear   device uint64 or NULL: set to 0.
+ * amax_history_update(...) is amax_history_update_ex with the three NULL.
+ */
+int amax_history_update_ex(float* history, int L, int* head, const float* amax_new,
+                           float margin, int fmt, const float* scale_prev, float* scale_out,
+                           int* status, float* amax_clear, unsigned long long* sat_clear,
+                           cudaStream_t stream);
 
 /*
  * fp8q_gemm_set_tile -- pin the GEMM tile shape (a tuning knob; "FP8 training:

@@ -52,9 +52,12 @@ def lib() -> ctypes.CDLL:
         L.fp8_quant_fused_batch.argtypes = [P, i32, P]
         L.fp8_gemm_dgrad.argtypes = [P, P, P, P, P, i64, i64, i64, P, P]
         L.amax_history_update.argtypes = [P, i32, P, P, f32, i32, P, P, P]
+        L.amax_history_update_ex.argtypes = [P, i32, P, P, f32, i32, P, P, P, P, P, P]
         L.fp8_downproj_workspace_bytes.argtypes = [i64]
         L.fp8_downproj_workspace_bytes.restype = ctypes.c_size_t
         L.fp8_downproj_fwd.argtypes = [P, P, i64, i64, i64, i32, P, P, P, P, P, P, P, P, ctypes.c_size_t, P, P]
+        L.fp8_downproj_fwd_ex.argtypes = [P, P, P, i64, i64, i64, i32, P, P, P, P, P, P, P, P, P, P,
+                                          ctypes.c_size_t, P, P, ctypes.c_uint, P, P]
         L.fp8_downproj_fwd_noalloc.argtypes = [P, P, i64, i64, i64, i32, P, P, P, P, P, P, P, P, P]
         L.fp8q_naive_act.argtypes = [P, i64, i64, i32, P, P]
         L.fp8q_naive_amax.argtypes = [P, i64, P, P]
@@ -67,8 +70,8 @@ def lib() -> ctypes.CDLL:
         L.fp8q_gemm_set_tile.argtypes = [i32, i32]
         L.fp8q_gemm_set_tile.restype = i32
         for fn in ("fp8_quant_fused", "fp8_quant_fused_ex", "fp8_quant_fused_batch", "fp8_downproj_fwd",
-                   "fp8_downproj_fwd_noalloc", "fp8_gemm_fwd", "fp8_gemm_dgrad", "amax_history_update",
-                   "fp8q_naive_act", "fp8q_naive_amax", "fp8q_naive_cast"):
+                   "fp8_downproj_fwd_noalloc", "fp8_downproj_fwd_ex", "fp8_gemm_fwd", "fp8_gemm_dgrad", "amax_history_update",
+                   "amax_history_update_ex", "fp8q_naive_act", "fp8q_naive_amax", "fp8q_naive_cast"):
             getattr(L, fn).restype = i32
         _lib = L
     return _lib
@@ -207,6 +210,49 @@ def fp8_downproj_fwd(h: torch.Tensor, wt_q: torch.Tensor, scale_x: torch.Tensor,
     _check("fp8_downproj_fwd", st)
 
 
+class HistoryArgs(ctypes.Structure):
+    """fp8q_history_args: one delayed-scale update run inside fp8_downproj_fwd_ex."""
+    _fields_ = [("history", ctypes.c_void_p), ("L", ctypes.c_int), ("head", ctypes.c_void_p),
+                ("margin", ctypes.c_float), ("fmt", ctypes.c_int), ("scale_prev", ctypes.c_void_p),
+                ("scale_out", ctypes.c_void_p), ("status", ctypes.c_void_p), ("amax_clear", ctypes.c_void_p),
+                ("sat_clear", ctypes.c_void_p)]
+
+
+def history_args(history: torch.Tensor, head: torch.Tensor, margin: float, fmt: int, scale_out: torch.Tensor, *,
+                 scale_prev=None, status=None, amax_clear=None, sat_clear=None) -> HistoryArgs:
+    """The arguments of amax_history_update_ex (amax_new is the kernel's own amax)."""
+    v = lambda t, nb, name: (lambda p: None if p is None else p.value)(_ptr(t, nb, name))
+    L = history.numel()
+    a = HistoryArgs(v(history, 4 * L, "history"), L, v(head, 4, "head"), float(margin), fmt,
+                    v(scale_prev, 4, "scale_prev"), v(scale_out, 4, "scale_out"), v(status, 4, "status"),
+                    v(amax_clear, 4, "amax_clear"), v(sat_clear, 8, "sat_clear"))
+    a._tensors = (history, head, scale_out, scale_prev, status, amax_clear, sat_clear)
+    return a
+
+
+def fp8_downproj_fwd_ex(h: torch.Tensor, wt_q: torch.Tensor, scale_x: torch.Tensor, scale_w: torch.Tensor,
+                        x_q: torch.Tensor, y: torch.Tensor, workspace: torch.Tensor, *, w=None, w_q=None,
+                        amax_w=None, act: int = ACT_RELU2, act_out=None, amax_out=None, sat_count=None,
+                        hist_x=None, hist_w=None, flags: int = 0, status=None, stream=None) -> None:
+    """fp8_downproj_fwd with the weight cast (w [K,N] -> wt_q, w_q, amax_w) in the same kernel;
+    hist_x / hist_w (HistoryArgs): the delayed-scale updates, run by the kernel's last CTA;
+    flags=ACCUMULATE: nothing is zeroed first (the workspace must be zero)."""
+    M, K = h.shape
+    N = wt_q.shape[0]
+    if wt_q.shape[1] != K or (w is not None and tuple(w.shape) != (K, N)):
+        raise ValueError("h [M,K], wt_q [N,K] and w [K,N] disagree")
+    ws = fp8_downproj_workspace_bytes(M)
+    st = lib().fp8_downproj_fwd_ex(
+        _ptr(h, 2 * M * K, "h"), _ptr(w, 2 * K * N, "w"), _ptr(wt_q, N * K, "wt_q"), M, N, K, act,
+        _ptr(scale_x, 4, "scale_x"), _ptr(scale_w, 4, "scale_w"), _ptr(act_out, 2 * M * K, "act_out"),
+        _ptr(x_q, M * K, "x_q"), _ptr(amax_out, 4, "amax_out"), _ptr(sat_count, 8, "sat_count"),
+        _ptr(w_q, K * N, "w_q"), _ptr(amax_w, 4, "amax_w"), _ptr(y, 2 * M * N, "y"),
+        _ptr(workspace, ws, "workspace"), workspace.numel() * workspace.element_size(),
+        None if hist_x is None else ctypes.byref(hist_x), None if hist_w is None else ctypes.byref(hist_w), flags,
+        _ptr(status, 4, "status"), _stream(stream))
+    _check("fp8_downproj_fwd_ex", st)
+
+
 def fp8_downproj_fwd_noalloc(h: torch.Tensor, wt_q: torch.Tensor, scale_x: torch.Tensor, scale_w: torch.Tensor,
                              x_q: torch.Tensor, y: torch.Tensor, *, act: int = ACT_RELU2, act_out=None,
                              amax_out=None, sat_count=None, status=None, stream=None) -> None:
@@ -231,6 +277,19 @@ def amax_history_update(history: torch.Tensor, head: torch.Tensor, amax_new: tor
         _ptr(history, 4 * L, "history"), L, _ptr(head, 4, "head"), _ptr(amax_new, 4, "amax_new"),
         float(margin), fmt, _ptr(scale_out, 4, "scale_out"), _ptr(status, 4, "status"), _stream(stream))
     _check("amax_history_update", st)
+
+
+def amax_history_update_ex(history: torch.Tensor, head: torch.Tensor, amax_new: torch.Tensor, margin: float,
+                           fmt: int, scale_out: torch.Tensor, *, scale_prev=None, status=None, amax_clear=None,
+                           sat_clear=None, stream=None) -> None:
+    """amax_history_update; a bad amax copies scale_prev into scale_out; zeroes amax_clear / sat_clear."""
+    L = history.numel()
+    st = lib().amax_history_update_ex(
+        _ptr(history, 4 * L, "history"), L, _ptr(head, 4, "head"), _ptr(amax_new, 4, "amax_new"),
+        float(margin), fmt, _ptr(scale_prev, 4, "scale_prev"), _ptr(scale_out, 4, "scale_out"),
+        _ptr(status, 4, "status"), _ptr(amax_clear, 4, "amax_clear"), _ptr(sat_clear, 8, "sat_clear"),
+        _stream(stream))
+    _check("amax_history_update_ex", st)
 
 
 # -- the unfused three-pass comparator (include/fp8q_naive.h) -----------------

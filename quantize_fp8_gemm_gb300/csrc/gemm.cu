@@ -35,6 +35,7 @@
 // waits (bounded) for its copies and MMAs in flight, frees TMEM and exits.
 #include "common.cuh"
 #include "quant_ops.cuh"
+#include "history_ops.cuh"
 
 #include <algorithm>
 #include <atomic>
@@ -65,15 +66,31 @@ constexpr int gemm_threads() { return kThreadsGemm + (FUSED ? kQuantThreads : 0)
 
 // Operands of the fused quantize.  ready[b] counts the rows of 128-row block b
 // whose E4M3 codes are written; the GEMM's producer loads a tile's A rows once
-// its block is complete.
+// its block is complete.  With w set, the quantize warps first cast the weight
+// W [K,N] into the GEMM's B operand W_q^T [N,K] (and W_q [K,N]); w_ready counts
+// finished weight units and every producer waits for all of them before its
+// first B load.  The CTA that finishes last resets ready, w_ready and done, so
+// the workspace is zero again for the next launch, and then runs the
+// delayed-scale history updates of X and W on the final amax values.
 struct FusedArgs {
     const uint4* h;               // H [M,K] BF16, 8 elements per 16 bytes
     uint4* act_out;               // [M,K] BF16 activation copy, or nullptr
     uint2* x_q;                   // [M,K] E4M3: the GEMM's A operand
-    float* amax_out;              // or nullptr; zeroed before the launch
-    unsigned long long* sat_out;  // or nullptr; zeroed before the launch
-    unsigned* ready;              // [ceil(M/128)], zeroed before the launch
+    float* amax_out;              // or nullptr; zero at the launch
+    unsigned long long* sat_out;  // or nullptr; zero at the launch
+    unsigned* ready;              // [nblocks], zero at the launch
     int act;                      // fp8q_act
+    int64_t nblocks;              // ceil(M / 128)
+    unsigned* done;               // CTAs finished; zero at the launch
+    const uint4* w;               // W [K,N] BF16, or nullptr (W_q^T is then an input)
+    const float* scale_w;         // W's scale (the GEMM's scale_b)
+    uint8_t* wt_q;                // [N,K] E4M3, written when w is set
+    uint8_t* w_q;                 // [K,N] E4M3 or nullptr
+    float* amax_w;                // or nullptr; zero at the launch
+    int64_t wn;                   // N
+    unsigned* w_ready;            // epilogue warps done with the weight; zero at the launch
+    unsigned w_units;             // epilogue warps of the launch (set by launch_gemm)
+    HistoryArgs hx, hw;           // delayed-scale updates the last CTA runs (history == nullptr: none)
 };
 
 template <int BN, bool PAIR>
@@ -192,6 +209,66 @@ __device__ __forceinline__ void fused_quantize_rows(const FusedArgs& fz, float s
 // ...), so rows finish in order across the GPU.  The rows left after the last
 // full round are split evenly over all CTAs (at most 17 rows each), so no SM
 // carries a whole extra unit at the end.
+// The last CTA's history update (once per launch: kept out of line).
+__device__ __noinline__ void history_update_once(const HistoryArgs& a, const float* amax_new) {
+    history_update_warp(a, amax_new);
+}
+
+// The weight cast of the fused kernel ("FP8 training: what it is and how it
+// works", Step 4: the weight's 8-bit copy is cast from the master copy each
+// step): W [K,N] BF16 -> W_q^T [N,K] (and W_q [K,N]) E4M3 with the scale s_w.
+// The epilogue warps do it at the start of the kernel, while they would
+// otherwise wait for their first accumulator.  A unit is 8 rows of W x 256
+// columns, one warp, each lane 8 columns: the lane loads its 8 x 8 block row
+// by row, casts it, and writes the block's transpose as 8 eight-byte pieces
+// (8 consecutive k of one output row n).  Warp slot ew * gridDim.x + cta
+// takes units slot, slot + all epilogue warps, ...  Every epilogue warp then
+// adds 1 to w_ready with release semantics, once, after all its units (the
+// producers wait for the whole weight, so one drain of the scattered stores
+// per warp is enough).  The warp's max |W| goes to amax_w with one atomic.
+__device__ __forceinline__ void fused_cast_w(const FusedArgs& fz, int64_t K, int ew, int lane) {
+    const int64_t N = fz.wn;
+    const int64_t nbn = (N + 255) / 256;
+    const int64_t units = (K / 8) * nbn;
+    const int64_t num_warps = int64_t(gridDim.x) * kEpiWarps;
+    const float s = __ldg(fz.scale_w);
+    uint32_t amax2w = 0;
+    for (int64_t u = int64_t(ew) * gridDim.x + blockIdx.x; u < units; u += num_warps) {
+        const int64_t k0 = (u / nbn) * 8;
+        const int64_t n = (u % nbn) * 256 + lane * 8;
+        if (n < N) {
+            uint4 x[8];
+#pragma unroll
+            for (int r = 0; r < 8; ++r) x[r] = ld_stream_v4(fz.w + ((k0 + r) * N + n) / 8);
+            uint2 q[8];
+            uint32_t nsat_unused = 0;
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+                const uint4 a = act8<FP8Q_ACT_IDENTITY>(x[r], amax2w);
+                q[r] = cast8<FP8Q_E4M3>(a, s, nsat_unused);
+                if (fz.w_q) st_v2(reinterpret_cast<uint2*>(fz.w_q + (k0 + r) * N + n), q[r]);
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                uint32_t lo = 0, hi = 0;
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    lo |= (((j < 4 ? q[r].x : q[r].y) >> (8 * (j & 3))) & 0xFFu) << (8 * r);
+                    hi |= (((j < 4 ? q[r + 4].x : q[r + 4].y) >> (8 * (j & 3))) & 0xFFu) << (8 * r);
+                }
+                st_v2(reinterpret_cast<uint2*>(fz.wt_q + (n + j) * K + k0), make_uint2(lo, hi));
+            }
+        }
+    }
+    // the warp's codes, written by all lanes, are ordered before the count,
+    // which every producer reads before its TMA loads of W_q^T
+    fence_proxy_async_global();
+    __syncwarp();
+    if (lane == 0) red_release_add(fz.w_ready, 1u);
+    const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, max16x2(amax2w));
+    if (lane == 0 && fz.amax_w && m) atomicMax(reinterpret_cast<unsigned int*>(fz.amax_w), m << 16);
+}
+
 __device__ __forceinline__ void fused_quantize(const FusedArgs& fz, const float* scale, int64_t M, int64_t K) {
     const float s = __ldg(scale);
     uint32_t amax2 = 0, nsat = 0;
@@ -335,6 +412,13 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             uint32_t phase = 0;
             int64_t issued = 0;
             bool ok = true;
+            if constexpr (FUSED) {
+                // the weight cast of this launch is complete before any B load
+                if (fz.w && !hold_loads) {
+                    ok = wait_ready(fz.w_ready, fz.w_units, abort_flag, status);
+                    fence_proxy_async_global();
+                }
+            }
             // hold_loads (test hook): issue nothing, so the MMA issuer's first wait runs out
             for (int64_t tile = first_tile; tile < num_tiles && ok && !hold_loads; tile += tile_stride) {
                 const int32_t m0 = static_cast<int32_t>((tile / num_n) * C::TILE_M + rank * BM);
@@ -440,6 +524,9 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         if constexpr (FUSED) fused_quantize(fz, scale_a, M, K);
     } else {
         // ---------------------------------------------------------- epilogue
+        if constexpr (FUSED) {
+            if (fz.w) fused_cast_w(fz, K, warp - 2, lane);
+        }
         const int q = warp & 3;  // TMEM lane quarter this warp may access
         const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
         // drained accumulators are reported to the leader's barrier
@@ -528,6 +615,31 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 
     tc_fence_before();
     __syncthreads();
+    if constexpr (FUSED) {
+        // every wait of this CTA on the counters is over and its amax / count
+        // atomics are done: the last CTA to get here resets the counters for
+        // the next launch and pushes the final amax values into the histories
+        __shared__ int s_last_cta;
+        if (threadIdx.x == 0) {
+            int last = 0;
+            if (fz.done) {
+                __threadfence();
+                last = atomicAdd(fz.done, 1u) == gridDim.x - 1;
+                if (last) __threadfence();
+            }
+            s_last_cta = last;
+        }
+        __syncthreads();
+        if (s_last_cta && warp == 0) {
+            for (int64_t b = lane; b < fz.nblocks; b += 32) fz.ready[b] = 0u;
+            if (lane == 0) {
+                if (fz.w_ready) *fz.w_ready = 0u;
+                *fz.done = 0u;
+            }
+            if (fz.hx.history) history_update_once(fz.hx, fz.amax_out);
+            if (fz.hw.history) history_update_once(fz.hw, fz.amax_w);
+        }
+    }
     // a pair frees TMEM only after the leader's MMAs into both CTAs drained and
     // no arrival to the leader's barriers is still in flight
     if constexpr (PAIR) cluster_sync_all();
@@ -637,6 +749,8 @@ int launch_gemm(const void* a, const void* b, const float* sa, const float* sb, 
     if constexpr (PAIR) {
         if (info.max_clusters < 1) return FP8Q_ERR_CUDA;
         const int clusters = static_cast<int>(FUSED ? info.max_clusters : std::min<int64_t>(tiles, info.max_clusters));
+        FusedArgs f = fz;
+        if (f.w) f.w_units = static_cast<unsigned>(2 * clusters * kEpiWarps);  // each epilogue warp reports once
         cudaLaunchConfig_t cfg = {};
         cudaLaunchAttribute attr[2];
         attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -652,7 +766,7 @@ int launch_gemm(const void* a, const void* b, const float* sa, const float* sb, 
         cfg.attrs = attr;
         cfg.numAttrs = 2;
         if (cudaLaunchKernelEx(&cfg, kern, mapA, mapB, mapD, sa, sb, M, N, K, idesc, status,
-                               g_hold_loads.load(), fz) != cudaSuccess) {
+                               g_hold_loads.load(), f) != cudaSuccess) {
             (void)cudaGetLastError();
             return FP8Q_ERR_CUDA;
         }
@@ -660,8 +774,10 @@ int launch_gemm(const void* a, const void* b, const float* sa, const float* sb, 
         // the fused kernel needs every CTA resident at once (the producers wait on
         // quantize work spread over all CTAs): one CTA per SM, never more
         const int grid = static_cast<int>(FUSED ? sm_count() : std::min<int64_t>(tiles, sm_count()));
+        FusedArgs f = fz;
+        if (f.w) f.w_units = static_cast<unsigned>(grid * kEpiWarps);  // each epilogue warp reports once
         if (launch_pdl(kern, dim3(grid), dim3(gemm_threads<FUSED>()), C::SMEM_BYTES, stream, mapA, mapB, mapD, sa,
-                       sb, M, N, K, idesc, status, g_hold_loads.load(), fz) != cudaSuccess) {
+                       sb, M, N, K, idesc, status, g_hold_loads.load(), f) != cudaSuccess) {
             (void)cudaGetLastError();
             return FP8Q_ERR_CUDA;
         }
@@ -805,34 +921,121 @@ extern "C" int fp8_gemm_dgrad(const void* dy_q, const void* w_q, const float* sc
 extern "C" size_t fp8_downproj_workspace_bytes(int64_t M) {
     if (M <= 0) return 0;
     const size_t blocks = static_cast<size_t>((M + BM - 1) / BM);
-    return (blocks * sizeof(unsigned) + 255) / 256 * 256;
+    return ((blocks + 2) * sizeof(unsigned) + 255) / 256 * 256;  // ready[blocks], w_ready, done
 }
 
-extern "C" int fp8_downproj_fwd(const void* h, const void* wt_q, int64_t M, int64_t N, int64_t K, int act,
-                                const float* scale_x, const float* scale_w, void* act_out, void* x_q,
-                                float* amax_out, unsigned long long* sat_count, void* y, void* workspace,
-                                size_t workspace_bytes, int* status, cudaStream_t stream) {
-    if (act < FP8Q_ACT_IDENTITY || act > FP8Q_ACT_RELU2) return FP8Q_ERR_UNSUPPORTED;
-    if ((!h || !x_q || !workspace) && M != 0) return FP8Q_ERR_NULL;
-    if (!aligned16(h) || !aligned16(act_out) || (reinterpret_cast<uintptr_t>(workspace) & 3u) ||
-        (reinterpret_cast<uintptr_t>(amax_out) & 3u) || (reinterpret_cast<uintptr_t>(sat_count) & 7u))
-        return FP8Q_ERR_ALIGN;
-    if (workspace_bytes < fp8_downproj_workspace_bytes(M)) return FP8Q_ERR_SHAPE;
-    int st = check_gemm_args(x_q, wt_q, scale_x, scale_w, y, M, N, K, status);  // ends with the device check
-    if (st != FP8Q_OK) return st;
-    if (amax_out && cudaMemsetAsync(amax_out, 0, sizeof(float), stream) != cudaSuccess) return FP8Q_ERR_CUDA;
-    if (sat_count && cudaMemsetAsync(sat_count, 0, sizeof(unsigned long long), stream) != cudaSuccess)
-        return FP8Q_ERR_CUDA;
-    if (M == 0) return FP8Q_OK;
-    if (cudaMemsetAsync(workspace, 0, fp8_downproj_workspace_bytes(M), stream) != cudaSuccess) return FP8Q_ERR_CUDA;
-    FusedArgs fz;
+namespace {
+
+FusedArgs fused_args(const void* h, int act, void* act_out, void* x_q, float* amax_out,
+                     unsigned long long* sat_count, unsigned* ws, int64_t M) {
+    FusedArgs fz = {};
     fz.h = static_cast<const uint4*>(h);
     fz.act_out = static_cast<uint4*>(act_out);
     fz.x_q = static_cast<uint2*>(x_q);
     fz.amax_out = amax_out;
     fz.sat_out = sat_count;
-    fz.ready = static_cast<unsigned*>(workspace);
     fz.act = act;
+    fz.nblocks = (M + BM - 1) / BM;
+    fz.ready = ws;
+    fz.w_ready = ws + fz.nblocks;
+    fz.done = ws + fz.nblocks + 1;
+    return fz;
+}
+
+}  // namespace
+
+extern "C" int fp8_downproj_fwd(const void* h, const void* wt_q, int64_t M, int64_t N, int64_t K, int act,
+                                const float* scale_x, const float* scale_w, void* act_out, void* x_q,
+                                float* amax_out, unsigned long long* sat_count, void* y, void* workspace,
+                                size_t workspace_bytes, int* status, cudaStream_t stream) {
+    return fp8_downproj_fwd_ex(h, nullptr, const_cast<void*>(wt_q), M, N, K, act, scale_x, scale_w, act_out, x_q,
+                               amax_out, sat_count, nullptr, nullptr, y, workspace, workspace_bytes, nullptr,
+                               nullptr, 0u, status, stream);
+}
+
+namespace {
+
+// Host checks of one history update (as amax_history_update_ex) and its device form.
+int check_history(const fp8q_history_args* h, const float* amax_new, HistoryArgs* out) {
+    if (!h->history || !h->head || !h->scale_out || !amax_new) return FP8Q_ERR_NULL;
+    if (h->L < 1 || h->L > 4096) return FP8Q_ERR_SHAPE;
+    if (h->fmt != FP8Q_E4M3 && h->fmt != FP8Q_E5M2) return FP8Q_ERR_UNSUPPORTED;
+    if (!(h->margin > 0.0f) || h->margin > 3.402823466e38f) return FP8Q_ERR_SHAPE;
+    if ((reinterpret_cast<uintptr_t>(h->history) | reinterpret_cast<uintptr_t>(h->head) |
+         reinterpret_cast<uintptr_t>(h->scale_out) | reinterpret_cast<uintptr_t>(h->scale_prev) |
+         reinterpret_cast<uintptr_t>(h->status) | reinterpret_cast<uintptr_t>(h->amax_clear)) & 3u)
+        return FP8Q_ERR_ALIGN;
+    if (reinterpret_cast<uintptr_t>(h->sat_clear) & 7u) return FP8Q_ERR_ALIGN;
+    if (h->amax_clear && h->amax_clear == amax_new) return FP8Q_ERR_SHAPE;
+    out->history = h->history;
+    out->L = h->L;
+    out->head = h->head;
+    out->margin = h->margin;
+    out->fmt_max = fp8_max_value(h->fmt);
+    out->scale_prev = h->scale_prev;
+    out->scale_out = h->scale_out;
+    out->status = h->status;
+    out->amax_clear = h->amax_clear;
+    out->sat_clear = h->sat_clear;
+    return FP8Q_OK;
+}
+
+}  // namespace
+
+extern "C" int fp8_downproj_fwd_ex(const void* h, const void* w, void* wt_q, int64_t M, int64_t N, int64_t K,
+                                   int act, const float* scale_x, const float* scale_w, void* act_out, void* x_q,
+                                   float* amax_x, unsigned long long* sat_count, void* w_q, float* amax_w, void* y,
+                                   void* workspace, size_t workspace_bytes, const fp8q_history_args* hist_x,
+                                   const fp8q_history_args* hist_w, unsigned flags, int* status,
+                                   cudaStream_t stream) {
+    if (flags & ~static_cast<unsigned>(FP8Q_ACCUMULATE)) return FP8Q_ERR_UNSUPPORTED;
+    if (act < FP8Q_ACT_IDENTITY || act > FP8Q_ACT_RELU2) return FP8Q_ERR_UNSUPPORTED;
+    if ((!h || !x_q || !workspace) && M != 0) return FP8Q_ERR_NULL;
+    if (!aligned16(h) || !aligned16(act_out) || !aligned16(w) || !aligned16(w_q) ||
+        (reinterpret_cast<uintptr_t>(workspace) & 3u) || (reinterpret_cast<uintptr_t>(amax_x) & 3u) ||
+        (reinterpret_cast<uintptr_t>(amax_w) & 3u) || (reinterpret_cast<uintptr_t>(sat_count) & 7u))
+        return FP8Q_ERR_ALIGN;
+    if (workspace_bytes < fp8_downproj_workspace_bytes(M)) return FP8Q_ERR_SHAPE;
+    HistoryArgs hx = {}, hw = {};
+    if (hist_w && !w) return FP8Q_ERR_NULL;  // W's amax exists only when the kernel casts W
+    if (hist_x) {
+        const int hs = check_history(hist_x, amax_x, &hx);
+        if (hs != FP8Q_OK) return hs;
+    }
+    if (hist_w) {
+        const int hs = check_history(hist_w, amax_w, &hw);
+        if (hs != FP8Q_OK) return hs;
+    }
+    if ((hist_x || hist_w) && M == 0) return FP8Q_ERR_SHAPE;  // no kernel to run them in
+    int st = check_gemm_args(x_q, wt_q, scale_x, scale_w, y, M, N, K, status);  // ends with the device check
+    if (st != FP8Q_OK) return st;
+    const bool zero = !(flags & FP8Q_ACCUMULATE);
+    if (zero) {
+        if (amax_x && cudaMemsetAsync(amax_x, 0, sizeof(float), stream) != cudaSuccess) return FP8Q_ERR_CUDA;
+        if (sat_count && cudaMemsetAsync(sat_count, 0, sizeof(unsigned long long), stream) != cudaSuccess)
+            return FP8Q_ERR_CUDA;
+        if (w && amax_w && cudaMemsetAsync(amax_w, 0, sizeof(float), stream) != cudaSuccess) return FP8Q_ERR_CUDA;
+    }
+    if (M == 0) {
+        // no GEMM: a weight to cast still is (the step's W_q^T and amax stay defined)
+        if (!w) return FP8Q_OK;
+        return fp8_quant_fused_ex(w, K, N, FP8Q_ACT_IDENTITY, FP8Q_E4M3, scale_w, nullptr, w_q, wt_q,
+                                  amax_w, nullptr, nullptr, 1, FP8Q_ACCUMULATE, stream);
+    }
+    if (zero && cudaMemsetAsync(workspace, 0, fp8_downproj_workspace_bytes(M), stream) != cudaSuccess)
+        return FP8Q_ERR_CUDA;
+    FusedArgs fz = fused_args(h, act, act_out, x_q, amax_x, sat_count, static_cast<unsigned*>(workspace), M);
+    if (w) {
+        fz.w = static_cast<const uint4*>(w);
+        fz.scale_w = scale_w;
+        fz.wt_q = static_cast<uint8_t*>(wt_q);
+        fz.w_q = static_cast<uint8_t*>(w_q);
+        fz.amax_w = amax_w;
+        fz.wn = N;
+        fz.w_units = 0;  // set at launch: the number of epilogue warps, which each report once
+    }
+    fz.hx = hx;
+    fz.hw = hw;
     return gemm_dispatch_t<true>(x_q, wt_q, scale_x, scale_w, 0, y, M, N, K, FP8Q_E4M3, FP8Q_E4M3, status, stream,
                                  fz);
 }
@@ -845,10 +1048,11 @@ extern "C" int fp8_downproj_fwd(const void* h, const void* wt_q, int64_t M, int6
 // g_noalloc_ready only names the symbol: its device address comes from
 // cudaGetSymbolAddress, once per device, with that device current.
 
-static __device__ __align__(256) unsigned g_noalloc_ready[FP8Q_NOALLOC_MAX_M / BM];
+static __device__ __align__(256) unsigned g_noalloc_ready[FP8Q_NOALLOC_MAX_M / BM + 64];
 
 static_assert(FP8Q_NOALLOC_MAX_M % BM == 0, "whole 128-row blocks");
-static_assert(sizeof(g_noalloc_ready) % 256 == 0, "the workspace size rounds to 256 bytes");
+static_assert(sizeof(g_noalloc_ready) == ((FP8Q_NOALLOC_MAX_M / BM + 2) * sizeof(unsigned) + 255) / 256 * 256,
+              "the array is exactly the workspace of the largest M");
 
 namespace {
 
@@ -894,14 +1098,7 @@ extern "C" int fp8_downproj_fwd_noalloc(const void* h, const void* wt_q, int64_t
     if (M == 0) return FP8Q_OK;
     // the previous call's counts are still there: this call's blocks start from zero
     if (cudaMemsetAsync(ready, 0, fp8_downproj_workspace_bytes(M), stream) != cudaSuccess) return FP8Q_ERR_CUDA;
-    FusedArgs fz;
-    fz.h = static_cast<const uint4*>(h);
-    fz.act_out = static_cast<uint4*>(act_out);
-    fz.x_q = static_cast<uint2*>(x_q);
-    fz.amax_out = amax_out;
-    fz.sat_out = sat_count;
-    fz.ready = ready;
-    fz.act = act;
+    const FusedArgs fz = fused_args(h, act, act_out, x_q, amax_out, sat_count, ready, M);
     return gemm_dispatch_t<true>(x_q, wt_q, scale_x, scale_w, 0, y, M, N, K, FP8Q_E4M3, FP8Q_E4M3, status, stream,
                                  fz);
 }

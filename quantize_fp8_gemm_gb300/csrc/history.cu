@@ -11,8 +11,11 @@
 // One warp: the newest amax goes into the next ring slot, the window maximum
 // is a warp reduction over the L entries, and the scale is
 //     s = float32( fmt_max / float32(margin * amax_ref) ),
-// written only when amax_ref and s are positive and finite.
+// written only when amax_ref and s are positive and finite (else the previous
+// scale is kept, copied from scale_prev when one is given).  The same launch
+// can zero the accumulators the next step's cast folds into.
 #include "common.cuh"
+#include "history_ops.cuh"
 
 #include <mutex>
 
@@ -25,38 +28,22 @@ constexpr int kMaxDevices = 64;
 __global__ void __launch_bounds__(32)
 amax_history_kernel(float* __restrict__ history, int L, int* __restrict__ head,
                     const float* __restrict__ amax_new, float margin, float fmt_max,
-                    float* __restrict__ scale_out, int* __restrict__ status) {
-    const int lane = threadIdx.x;
+                    float* __restrict__ scale_out, int* __restrict__ status, const float* scale_prev,
+                    float* amax_clear, unsigned long long* sat_clear) {
     pdl_launch_dependents();
     pdl_wait();
-    // the three loads are independent: issue them together
-    const int h0 = *head;
-    const float a_new = *amax_new;
-    float first = lane < L ? history[lane] : 0.0f;
-    const int slot = (h0 + 1) % L;
-    // |x| as an ordered key: bit patterns of non-negative floats sort like the
-    // floats, and a NaN magnitude sorts above infinity
-    uint32_t key = 0;
-    for (int i = lane; i < L; i += 32) {
-        const float v = (i == slot) ? a_new : (i == lane ? first : history[i]);
-        key = max(key, __float_as_uint(v) & 0x7FFFFFFFu);
-    }
-    key = __reduce_max_sync(0xFFFFFFFFu, key);
-    __syncwarp();
-    if (lane == 0) {
-        history[slot] = a_new;
-        *head = slot;
-        const float ref = __uint_as_float(key);
-        bool ok = ref > 0.0f && ref <= 3.402823466e38f;
-        float s = 0.0f;
-        if (ok) {
-            const float d = __fmul_rn(margin, ref);
-            s = __fdiv_rn(fmt_max, d);
-            ok = s > 0.0f && s <= 3.402823466e38f;
-        }
-        if (ok) *scale_out = s;
-        else if (status) atomicOr(status, FP8Q_DEV_BAD_AMAX);
-    }
+    HistoryArgs a;
+    a.history = history;
+    a.L = L;
+    a.head = head;
+    a.margin = margin;
+    a.fmt_max = fmt_max;
+    a.scale_prev = scale_prev;
+    a.scale_out = scale_out;
+    a.status = status;
+    a.amax_clear = amax_clear;
+    a.sat_clear = sat_clear;
+    history_update_warp(a, amax_new);
 }
 
 struct DeviceInfo {
@@ -98,17 +85,27 @@ using namespace fp8q;
 extern "C" int amax_history_update(float* history, int L, int* head, const float* amax_new,
                                    float margin, int fmt, float* scale_out, int* status,
                                    cudaStream_t stream) {
+    return amax_history_update_ex(history, L, head, amax_new, margin, fmt, nullptr, scale_out, status, nullptr,
+                                  nullptr, stream);
+}
+
+extern "C" int amax_history_update_ex(float* history, int L, int* head, const float* amax_new, float margin,
+                                      int fmt, const float* scale_prev, float* scale_out, int* status,
+                                      float* amax_clear, unsigned long long* sat_clear, cudaStream_t stream) {
     if (!history || !head || !amax_new || !scale_out) return FP8Q_ERR_NULL;
     if (L < 1 || L > 4096) return FP8Q_ERR_SHAPE;
     if (fmt != FP8Q_E4M3 && fmt != FP8Q_E5M2) return FP8Q_ERR_UNSUPPORTED;
     if (!(margin > 0.0f) || margin > 3.402823466e38f) return FP8Q_ERR_SHAPE;
     if ((reinterpret_cast<uintptr_t>(history) | reinterpret_cast<uintptr_t>(head) |
          reinterpret_cast<uintptr_t>(amax_new) | reinterpret_cast<uintptr_t>(scale_out) |
-         reinterpret_cast<uintptr_t>(status)) & 3u)
+         reinterpret_cast<uintptr_t>(status) | reinterpret_cast<uintptr_t>(scale_prev) |
+         reinterpret_cast<uintptr_t>(amax_clear)) & 3u)
         return FP8Q_ERR_ALIGN;
+    if (reinterpret_cast<uintptr_t>(sat_clear) & 7u) return FP8Q_ERR_ALIGN;
+    if (amax_clear && amax_clear == amax_new) return FP8Q_ERR_SHAPE;  // it is read, not cleared
     if (!device_is_sm103()) return FP8Q_ERR_UNSUPPORTED;
     if (launch_pdl(amax_history_kernel, dim3(1), dim3(32), 0, stream, history, L, head, amax_new, margin,
-                   fp8_max_value(fmt), scale_out, status) != cudaSuccess) {
+                   fp8_max_value(fmt), scale_out, status, scale_prev, amax_clear, sat_clear) != cudaSuccess) {
         (void)cudaGetLastError();
         return FP8Q_ERR_CUDA;
     }

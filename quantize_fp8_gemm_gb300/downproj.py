@@ -78,12 +78,23 @@ class DelayedScale:
         """Push this step's amax; write the next step's scale into the other
         slot (which first takes the current scale, kept if the amax is
         unusable) and make that slot current."""
-        nxt = self.scales[1 - self.slot:2 - self.slot]
-        nxt.copy_(self.scale)
-        B.amax_history_update(self.history, self.head, self.amax, self.margin, self.fmt, nxt,
-                              status=self.status)
-        self.amaxes[1 - self.slot:2 - self.slot].zero_()
-        self.sats[1 - self.slot:2 - self.slot].zero_()
+        o = 1 - self.slot
+        B.amax_history_update_ex(self.history, self.head, self.amax, self.margin, self.fmt, self.scales[o:o + 1],
+                                 scale_prev=self.scale, status=self.status, amax_clear=self.amaxes[o:o + 1],
+                                 sat_clear=self.sats[o:o + 1])
+        self.slot ^= 1
+        self.clean = True
+
+    def kernel_update_args(self) -> "B.HistoryArgs":
+        """The update() of this step as arguments for a kernel that runs it
+        itself (fp8_downproj_fwd_ex); call advance() once it is enqueued."""
+        o = 1 - self.slot
+        return B.history_args(self.history, self.head, self.margin, self.fmt, self.scales[o:o + 1],
+                              scale_prev=self.scale, status=self.status, amax_clear=self.amaxes[o:o + 1],
+                              sat_clear=self.sats[o:o + 1])
+
+    def advance(self) -> None:
+        """The host side of update() when a kernel ran the update."""
         self.slot ^= 1
         self.clean = True
 
@@ -107,11 +118,12 @@ class Fp8DownProj:
                  keep_act: bool = True, chunks: int | None = None, fused: bool | None = None,
                  device="cuda"):
         self.M, self.K, self.N, self.act, self.group = M, K, N, act, group
-        # The fused quantize + GEMM kernel serves the per-tensor path in one block.
-        # Measured per step on GB300 (CUDA graph): it wins on large batches
-        # (65,536 x 3072 -> 768: 226 vs 263 us; 131,072 x 6400 -> 1600: 1232 vs
-        # 1437 us) and loses at 8,192 rows (59 vs 51 us), where the W cast in
-        # front of it and its last tiles are not hidden.
+        # The fused kernel (W cast + quantize + GEMM + history updates, one
+        # launch) serves the per-tensor path in one block.  Measured per step
+        # on GB300 (CUDA graph, L2 flushed): it wins on large batches (65,536 x
+        # 3072 -> 768: 212 vs 259 us; 131,072 x 6400 -> 1600: 1227 vs 1437 us)
+        # and loses at 8,192 rows (46.8 vs 45.0 us), where its last wave of
+        # tiles, which waits for the last rows, is not hidden.
         if fused is None:
             fused = not group and (chunks or 1) == 1 and M >= FUSED_MIN_ROWS
         self.fused = fused
@@ -133,7 +145,8 @@ class Fp8DownProj:
         self.gemm_status = torch.zeros(1, dtype=torch.int32, device=dev)
         self.workspace = None
         if self.fused:
-            self.workspace = torch.empty(max(1, B.fp8_downproj_workspace_bytes(M)), dtype=torch.uint8, device=dev)
+            # zero-filled once; the fused kernel leaves it zero
+            self.workspace = torch.zeros(max(1, B.fp8_downproj_workspace_bytes(M)), dtype=torch.uint8, device=dev)
         self._side = torch.cuda.Stream(device=dev)  # weight branch and history updates
         hi = torch.cuda.Stream.priority_range()[1]
         self._gemm = torch.cuda.Stream(device=dev, priority=hi)  # GEMM blocks, ahead of quantize blocks
@@ -214,8 +227,10 @@ class Fp8DownProj:
     def step(self, H: torch.Tensor, W: torch.Tensor) -> torch.Tensor:
         """One forward step: cast W, fused quantize of H, FP8 GEMM, history updates.
 
-        With ``fused`` (per-tensor scales only) the quantize and the GEMM are
-        one kernel (fp8_downproj_fwd).  Otherwise the batch is
+        With ``fused`` (per-tensor scales only) the W cast, the quantize and
+        the GEMM are one kernel (fp8_downproj_fwd_ex; see _step_fused).  With
+        one row block the W cast and the quantize share one launch and the
+        GEMM follows (_step_one_launch_cast).  Otherwise the batch is
         processed in ``chunks`` row blocks.  The current stream
         quantizes the blocks one after the other; a high-priority stream runs
         each block's GEMM as soon as that block is quantized, so the
@@ -224,7 +239,9 @@ class Fp8DownProj:
         first quantize, then updates the activation's history once the last
         block is quantized (the updates write the other scale slot, so they
         never race the GEMMs' reads).  All branches join the current stream."""
-        if not self.fused and not self.group and self.chunks == 1:
+        if self.fused:
+            return self._step_fused(H, W)
+        if not self.group and self.chunks == 1:
             return self._step_one_launch_cast(H, W)
         main, side, gs = torch.cuda.current_stream(), self._side, self._gemm
         sx, sw = self.x.scale, self.w.scale  # this step's slots
@@ -235,14 +252,6 @@ class Fp8DownProj:
             w_ready.record(side)
             if not self.group:
                 self.w.update()
-        if self.fused:
-            main.wait_event(w_ready)  # W_q^T ready; W's history update runs beside the kernel
-            self.quantize_and_gemm(H, sx, sw)
-            side.wait_stream(main)  # this step's amax is final
-            with torch.cuda.stream(side):
-                self.x.update()
-            main.wait_stream(side)
-            return self.y
         gs.wait_stream(side)  # W_q^T ready (and everything before this step)
         block = self.M // self.chunks
         for i in range(self.chunks):
@@ -259,6 +268,22 @@ class Fp8DownProj:
                 self.x.update()
         main.wait_stream(gs)
         main.wait_stream(side)
+        return self.y
+
+    def _step_fused(self, H: torch.Tensor, W: torch.Tensor) -> torch.Tensor:
+        """The per-tensor step as one kernel (fp8_downproj_fwd_ex): the W cast,
+        the quantize of H and the GEMM, accumulating into this slot's amax /
+        count (zeroed by the previous update()) with a workspace the kernel
+        leaves zero, so nothing runs ahead of it; the kernel's last CTA also
+        runs both history updates, so the step is one launch."""
+        sx, sw = self.x.scale, self.w.scale
+        flags = B.ACCUMULATE if (self.x.clean and self.w.clean) else 0
+        B.fp8_downproj_fwd_ex(H, self.wt_q, sx, sw, self.x_q, self.y, self.workspace, w=W, w_q=self.w_q,
+                              amax_w=self.w.amax, act=self.act, act_out=self.act_bf16, amax_out=self.x.amax,
+                              sat_count=self.x.sat, hist_x=self.x.kernel_update_args(),
+                              hist_w=self.w.kernel_update_args(), flags=flags, status=self.gemm_status)
+        self.x.advance()
+        self.w.advance()
         return self.y
 
     def _step_one_launch_cast(self, H: torch.Tensor, W: torch.Tensor) -> torch.Tensor:

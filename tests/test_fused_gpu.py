@@ -100,3 +100,101 @@ def test_fused_without_optional_outputs():
     torch.cuda.synchronize()
     ro = O.quant(h, O.ACT_RELU2, O.E4M3, 20.0, want_act=False)
     assert np.array_equal(host_u8(q), ro["q"])
+
+
+@pytest.mark.parametrize("pair,bn", [(-1, 0), (0, 192), (1, 256)])
+def test_fused_weight_cast_equals_separate_calls(pair, bn):
+    """fp8_downproj_fwd_ex with the master weight: the kernel's own W cast
+    (W_q^T, W_q, amax_w) and the GEMM that reads it equal fp8_quant_fused on W
+    followed by the separate quantize and GEMM, bit for bit.  Shapes leave a
+    partial 256-column weight unit (N = 272, 144) and 8-row groups over K."""
+    try:
+        if pair >= 0:
+            B.fp8q_gemm_set_tile(pair, bn)
+        for (M, N, K) in [(1000, 272, 640), (2048, 768, 3072), (129, 144, 1600), (0, 272, 256)]:
+            h, w = _inputs(max(M, 1), N, K, seed=M + N + K)
+            h = h[:M]
+            H, Wd = dev_bf16(h), dev_bf16(w)
+            sx, sw = dev_f32(20.0), dev_f32(300.0)
+            # separate: W cast, H quantize, GEMM
+            wt1 = torch.empty(N, K, dtype=torch.uint8, device="cuda")
+            wq1 = torch.empty(K, N, dtype=torch.uint8, device="cuda")
+            aw1 = torch.zeros(1, device="cuda")
+            B.fp8_quant_fused(Wd, B.ACT_IDENTITY, B.E4M3, sw, q_out=wq1, q_t_out=wt1, amax_out=aw1)
+            a1 = torch.empty(M, K, dtype=torch.bfloat16, device="cuda")
+            q1 = torch.empty(M, K, dtype=torch.uint8, device="cuda")
+            y1 = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+            ax1, s1 = torch.zeros(1, device="cuda"), torch.zeros(1, dtype=torch.int64, device="cuda")
+            B.fp8_quant_fused(H, B.ACT_RELU2, B.E4M3, sx, act_out=a1, q_out=q1, amax_out=ax1, sat_count=s1)
+            if M:
+                B.fp8_gemm_fwd(q1, wt1, sx, sw, y1)
+            # one kernel, twice in a row on one workspace: flags 0, then ACCUMULATE on zeroed accumulators
+            ws = torch.full((max(B.fp8_downproj_workspace_bytes(M), 256),), 0x5A, dtype=torch.uint8, device="cuda")
+            for flags in (0, B.ACCUMULATE):
+                wt2 = torch.full((N, K), 7, dtype=torch.uint8, device="cuda")
+                wq2 = torch.empty(K, N, dtype=torch.uint8, device="cuda")
+                aw2 = torch.full((1,), -1.0 if flags == 0 else 0.0, device="cuda")
+                a2 = torch.empty(M, K, dtype=torch.bfloat16, device="cuda")
+                q2 = torch.empty(M, K, dtype=torch.uint8, device="cuda")
+                y2 = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+                ax2 = torch.full((1,), -1.0 if flags == 0 else 0.0, device="cuda")
+                s2 = torch.full((1,), 9 if flags == 0 else 0, dtype=torch.int64, device="cuda")
+                st = torch.zeros(1, dtype=torch.int32, device="cuda")
+                B.fp8_downproj_fwd_ex(H, wt2, sx, sw, q2, y2, ws, w=Wd, w_q=wq2, amax_w=aw2, act=B.ACT_RELU2,
+                                      act_out=a2, amax_out=ax2, sat_count=s2, flags=flags, status=st)
+                torch.cuda.synchronize()
+                assert st.item() == 0
+                assert torch.equal(wt1, wt2) and torch.equal(wq1, wq2) and aw1.item() == aw2.item(), (M, N, K)
+                assert torch.equal(q1, q2) and torch.equal(a1.view(torch.int16), a2.view(torch.int16))
+                assert ax1.item() == ax2.item() and s1.item() == s2.item()
+                assert torch.equal(y1.view(torch.int16), y2.view(torch.int16)), (M, N, K, flags)
+            assert int(ws[:B.fp8_downproj_workspace_bytes(M)].sum().item()) == 0, "the kernel leaves its counts at zero"
+    finally:
+        B.fp8q_gemm_set_tile(-1)
+
+
+def test_fused_step_runs_history_updates():
+    """The kernel's last CTA runs both delayed-scale updates: a good amax gives
+    the oracle's next scale and clears the other slot's accumulators; an
+    all-negative H under ReLU^2 (amax 0) keeps the previous scale and flags
+    FP8Q_DEV_BAD_AMAX."""
+    M, N, K = 600, 272, 512
+    h, w = _inputs(M, N, K, seed=41)
+    for bad in (False, True):
+        hb = h.copy()
+        if bad:
+            hb = WL.to_bf16_bits(-np.abs(WL.bf16_tensor(h).float().numpy()) - 1.0)
+        H, Wd = dev_bf16(hb), dev_bf16(w)
+        scales_x = torch.tensor([20.0, 1.0], device="cuda")
+        scales_w = torch.tensor([300.0, 1.0], device="cuda")
+        hist_x, hist_w = torch.zeros(2, device="cuda"), torch.zeros(2, device="cuda")
+        head_x, head_w = torch.zeros(1, dtype=torch.int32, device="cuda"), torch.zeros(1, dtype=torch.int32, device="cuda")
+        amax_x = torch.zeros(2, device="cuda")
+        amax_w = torch.zeros(2, device="cuda")
+        amax_x[1] = 5.0  # the other slot: must be cleared
+        sats = torch.tensor([0, 77], dtype=torch.int64, device="cuda")
+        st_x, st_w = torch.zeros(1, dtype=torch.int32, device="cuda"), torch.zeros(1, dtype=torch.int32, device="cuda")
+        wt = torch.empty(N, K, dtype=torch.uint8, device="cuda")
+        q = torch.empty(M, K, dtype=torch.uint8, device="cuda")
+        y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+        ws = torch.zeros(B.fp8_downproj_workspace_bytes(M), dtype=torch.uint8, device="cuda")
+        hx = B.history_args(hist_x, head_x, 2.0, B.E4M3, scales_x[1:2], scale_prev=scales_x[0:1], status=st_x,
+                            amax_clear=amax_x[1:2], sat_clear=sats[1:2])
+        hw = B.history_args(hist_w, head_w, 2.0, B.E4M3, scales_w[1:2], scale_prev=scales_w[0:1], status=st_w,
+                            amax_clear=amax_w[1:2])
+        B.fp8_downproj_fwd_ex(H, wt, scales_x[0:1], scales_w[0:1], q, y, ws, w=Wd, amax_w=amax_w[0:1],
+                              amax_out=amax_x[0:1], sat_count=sats[0:1], hist_x=hx, hist_w=hw,
+                              flags=B.ACCUMULATE)
+        torch.cuda.synchronize()
+        ro = O.quant(hb, O.ACT_RELU2, O.E4M3, 20.0, want_act=False)
+        rw_amax = O.amax(w, O.ACT_IDENTITY)
+        assert amax_x[0].item() == ro["amax"] and amax_w[0].item() == rw_amax
+        assert amax_x[1].item() == 0.0 and sats[1].item() == 0
+        assert scales_w[1].item() == O.delayed_scale(rw_amax, 2.0, O.E4M3) and st_w.item() == 0
+        assert int(head_x.item()) == 1 and hist_x[1].item() == ro["amax"]
+        if bad:
+            assert ro["amax"] == 0.0
+            assert scales_x[1].item() == 20.0 and st_x.item() & B.DEV_BAD_AMAX
+        else:
+            assert scales_x[1].item() == O.delayed_scale(ro["amax"], 2.0, O.E4M3) and st_x.item() == 0
+        assert int(ws.sum().item()) == 0
