@@ -371,8 +371,10 @@ int amax_history_update_ex(float* history, int L, int* head, const float* amax_n
  * tiles).
  *   pair  -1: automatic choice (the default; bn ignored)
  *          0: one CTA per 128 x bn tile           bn in {128, 160, 192, 256}
- *          1: a CTA pair per 256 x bn tile (2-SM)  bn in {128, 160, 192, 224, 256}
- *             (pairs are used only when M > 128; smaller M falls back to one CTA)
+ *          1: a CTA pair per 256 x bn tile (2-SM)  bn in {128, 160, 192, 224, 256, 384}
+ *             (pairs are used only when M > 128; smaller M falls back to one CTA;
+ *             384 is two 192-wide MMAs into one accumulator, plain GEMMs only:
+ *             fp8_downproj_fwd takes 256 instead)
  * Returns FP8Q_ERR_UNSUPPORTED for any other combination (nothing changes).
  */
 int fp8q_gemm_set_tile(int pair, int bn);

@@ -95,7 +95,13 @@ struct FusedArgs {
 
 template <int BN, bool PAIR>
 struct Cfg {
+    // A tile wider than 256 columns takes two MMAs per k-step (N <= 256 each)
+    // into one accumulator; B then arrives as one box per MMA.
+    static constexpr int NSPLIT = BN > 256 ? 2 : 1;
+    static constexpr int MMA_N = BN / NSPLIT;
     static constexpr int B_ROWS = PAIR ? BN / 2 : BN;  // rows of B this CTA loads
+    static constexpr int B_BOX = B_ROWS / NSPLIT;      // rows of B per TMA box (one per MMA)
+    static constexpr int ACCS = 2 * BN <= 512 ? 2 : 1; // TMEM accumulators (512 columns)
     static constexpr int A_BYTES = BM * BK;
     static constexpr int B_BYTES = B_ROWS * BK;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -103,19 +109,31 @@ struct Cfg {
     static constexpr int EPI_BYTES = kEpiWarps * 2 * kEpiChunkBytes;  // double-buffered store staging
     static constexpr int RING_BUDGET = 220 * 1024 - EPI_BYTES;
     static constexpr int STAGES = RING_BUDGET / STAGE_BYTES < 8 ? RING_BUDGET / STAGE_BYTES : 8;
-    static constexpr int TMEM_COLS = (2 * BN <= 256) ? 256 : 512;  // two accumulators, power of 2
+    static constexpr int TMEM_COLS = (ACCS * BN <= 256) ? 256 : 512;  // power of 2
     static constexpr int BAR_BYTES = 256;
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES + 1024;  // + alignment slack
     static constexpr int MMA_M = PAIR ? 2 * BM : BM;
     static constexpr int TILE_M = MMA_M;                              // output rows per tile
     static constexpr int EPI_ARRIVALS = kEpiWarps * (PAIR ? 2 : 1);   // per accumulator drain
-    static_assert(BN % 32 == 0 && BN >= 64 && BN <= 256, "BN: multiple of 32 in [64, 256]");
-    static_assert(B_ROWS % 8 == 0, "B rows: whole 8-row swizzle atoms");
+    static_assert(BN % 32 == 0 && BN >= 64 && BN <= 384, "BN: multiple of 32 in [64, 384]");
+    static_assert(MMA_N % 16 == 0 && MMA_N <= 256, "MMA N: multiple of 16, at most 256");
+    static_assert(B_BOX % 8 == 0 && (B_BOX * BK) % 1024 == 0, "B boxes: whole 8-row swizzle atoms");
     static_assert(B_BYTES % 1024 == 0, "stage tiles stay 1024-byte aligned");
     static_assert(STAGES >= 2, "at least a double-buffered ring");
     static_assert((2 * STAGES + 5) * 8 + 16 <= BAR_BYTES, "barrier area");
     static_assert(SMEM_BYTES <= 232448, "dynamic shared memory per CTA");
 };
+
+// Next accumulator (of ACCS) and the phase its barriers are in.
+template <int ACCS>
+__device__ __forceinline__ void next_acc(int& acc, uint32_t& acc_phase) {
+    if constexpr (ACCS == 2) {
+        acc ^= 1;
+        if (acc == 0) acc_phase ^= 1u;
+    } else {
+        acc_phase ^= 1u;
+    }
+}
 
 // Bounded wait on an mbarrier phase.  Returns false when this thread gave up
 // or another role of the CTA already aborted.
@@ -422,7 +440,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             // hold_loads (test hook): issue nothing, so the MMA issuer's first wait runs out
             for (int64_t tile = first_tile; tile < num_tiles && ok && !hold_loads; tile += tile_stride) {
                 const int32_t m0 = static_cast<int32_t>((tile / num_n) * C::TILE_M + rank * BM);
-                const int32_t n0 = static_cast<int32_t>((tile % num_n) * BN + rank * C::B_ROWS);
+                const int32_t n0 = static_cast<int32_t>((tile % num_n) * BN + rank * C::B_BOX);
                 if constexpr (FUSED) {
                     // this tile's A rows exist once every unit of their block is quantized
                     if (m0 < M) {
@@ -441,12 +459,18 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                         const uint32_t fb = mapa_shared(smem_u32(&full[stage]), 0);
                         if (leader) mbar_arrive_expect_tx(smem_u32(&full[stage]), C::TX_BYTES);
                         tma_load_2d_pair(smem_u32(sa), &tmA, fb, kb * BK, m0);
-                        tma_load_2d_pair(smem_u32(sa + C::A_BYTES), &tmB, fb, kb * BK, n0);
+#pragma unroll
+                        for (int j = 0; j < C::NSPLIT; ++j)
+                            tma_load_2d_pair(smem_u32(sa + C::A_BYTES + j * C::B_BOX * BK), &tmB, fb, kb * BK,
+                                             n0 + j * C::MMA_N);
                     } else {
                         const uint32_t fb = smem_u32(&full[stage]);
                         mbar_arrive_expect_tx(fb, C::TX_BYTES);
                         tma_load_2d(smem_u32(sa), &tmA, fb, kb * BK, m0);
-                        tma_load_2d(smem_u32(sa + C::A_BYTES), &tmB, fb, kb * BK, n0);
+#pragma unroll
+                        for (int j = 0; j < C::NSPLIT; ++j)
+                            tma_load_2d(smem_u32(sa + C::A_BYTES + j * C::B_BOX * BK), &tmB, fb, kb * BK,
+                                        n0 + j * C::MMA_N);
                     }
                     ++issued;
                     if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
@@ -492,9 +516,13 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     for (int k = 0; k < BK / UMMA_K; ++k) {
                         const uint32_t accumulate = GROUP ? (k > 0) : (kb > 0 || k > 0);
                         const uint64_t ad = smem_desc_k_sw128(a_addr + k * UMMA_K);
-                        const uint64_t bd = smem_desc_k_sw128(b_addr + k * UMMA_K);
-                        if constexpr (PAIR) mma_f8f6f4_pair(d_tmem, ad, bd, idesc, accumulate);
-                        else mma_f8f6f4(d_tmem, ad, bd, idesc, accumulate);
+#pragma unroll
+                        for (int j = 0; j < C::NSPLIT; ++j) {
+                            const uint64_t bd = smem_desc_k_sw128(b_addr + j * C::B_BOX * BK + k * UMMA_K);
+                            const uint32_t dj = d_tmem + static_cast<uint32_t>(j * C::MMA_N);
+                            if constexpr (PAIR) mma_f8f6f4_pair(dj, ad, bd, idesc, accumulate);
+                            else mma_f8f6f4(dj, ad, bd, idesc, accumulate);
+                        }
                     }
                     // the stage is free (in both CTAs of a pair) once these MMAs finish
                     if constexpr (PAIR) mma_commit_pair_mc(smem_u32(&empty[stage]), 0x3);
@@ -502,16 +530,14 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
                     if (GROUP) {
                         mma_commit(smem_u32(&tfull[acc]));
-                        acc ^= 1;
-                        if (acc == 0) acc_phase ^= 1u;
+                        next_acc<C::ACCS>(acc, acc_phase);
                     }
                 }
                 if (!GROUP && ok) {
                     // accumulator ready for the epilogue(s)
                     if constexpr (PAIR) mma_commit_pair_mc(smem_u32(&tfull[acc]), 0x3);
                     else mma_commit(smem_u32(&tfull[acc]));
-                    acc ^= 1;
-                    if (acc == 0) acc_phase ^= 1u;
+                    next_acc<C::ACCS>(acc, acc_phase);
                 }
             }
             // all MMAs of this thread complete before TMEM is released
@@ -567,8 +593,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     if constexpr (PAIR) mbar_arrive_cluster(acc ? tempty1 : tempty0);
                     else mbar_arrive(acc ? tempty1 : tempty0);
                 }
-                acc ^= 1;
-                if (acc == 0) acc_phase ^= 1u;
+                next_acc<C::ACCS>(acc, acc_phase);
             } else {
                 float sum[BN];
 #pragma unroll
@@ -593,8 +618,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(acc ? tempty1 : tempty0);
-                    acc ^= 1;
-                    if (acc == 0) acc_phase ^= 1u;
+                    next_acc<C::ACCS>(acc, acc_phase);
                 }
                 if (!ok) break;
 #pragma unroll
@@ -740,11 +764,11 @@ int launch_gemm(const void* a, const void* b, const float* sa, const float* sb, 
     const LaunchInfo& info = launch_info<BN, GROUP, PAIR, FUSED>();
     if (info.attr_err != cudaSuccess) return FP8Q_ERR_CUDA;
     alignas(64) CUtensorMap mapA, mapB, mapD;
-    if (!make_kmajor_map(&mapA, a, M, K, BM) || !make_kmajor_map(&mapB, b, N, K, C::B_ROWS) ||
+    if (!make_kmajor_map(&mapA, a, M, K, BM) || !make_kmajor_map(&mapB, b, N, K, C::B_BOX) ||
         !make_out_map(&mapD, d, M, N))
         return FP8Q_ERR_CUDA;
     const int64_t tiles = ((M + C::TILE_M - 1) / C::TILE_M) * ((N + BN - 1) / BN);
-    const uint32_t idesc = idesc_f8(afmt, bfmt, C::MMA_M, BN);
+    const uint32_t idesc = idesc_f8(afmt, bfmt, C::MMA_M, C::MMA_N);
     auto kern = fp8_gemm_kernel<BN, GROUP, PAIR, FUSED>;
     if constexpr (PAIR) {
         if (info.max_clusters < 1) return FP8Q_ERR_CUDA;
@@ -800,24 +824,26 @@ struct Shape {
 // fp8q_gemm_set_tile: -1 = automatic, else (pair << 16) | bn
 std::atomic<int> g_tile_override{-1};
 
-Shape pick_shape(int64_t M, int64_t N) {
+Shape pick_shape(int64_t M, int64_t N, bool wide) {
     const int ov = g_tile_override.load(std::memory_order_relaxed);
     if (ov >= 0) {
         const bool pair = (ov >> 16) != 0;
         const int bn = ov & 0xFFFF;
         if (!pair || M > BM) return Shape{pair, bn};
-        return Shape{false, bn == 224 ? 256 : bn};
+        return Shape{false, bn == 224 || bn == 384 ? 256 : bn};
     }
     struct Cand { bool pair; int bn; double t; };
+    // {true, 384}: one accumulator, so its epilogue is not hidden; 1.70 measured
+    // at 8192 x 3072 -> 768, where its 64 tiles fit one wave of 76 pairs
     static constexpr Cand kCands[] = {
         {true, 256, 1.000}, {true, 224, 0.946}, {true, 192, 0.909}, {true, 160, 0.837}, {true, 128, 0.858},
-        {false, 192, 0.897}, {false, 160, 0.834}, {false, 128, 0.843}, {false, 256, 1.102},
+        {false, 192, 0.897}, {false, 160, 0.834}, {false, 128, 0.843}, {false, 256, 1.102}, {true, 384, 1.700},
     };
     const int64_t sms = sm_count();
     Shape best{false, 128};
     double best_cost = -1.0;
     for (const Cand& c : kCands) {
-        if (c.pair && M <= BM) continue;
+        if ((c.pair && M <= BM) || (c.bn == 384 && !wide)) continue;
         const int64_t tile_m = c.pair ? 2 * BM : BM;
         const int64_t units = c.pair ? sms / 2 : sms;
         const int64_t tiles = ((M + tile_m - 1) / tile_m) * ((N + c.bn - 1) / c.bn);
@@ -835,11 +861,15 @@ int gemm_dispatch_t(const void* a, const void* b, const float* sa, const float* 
         if (group)
             return launch_gemm<128, true, false, false>(a, b, sa, sb, d, M, N, K, afmt, bfmt, status, stream, fz);
     }
-    const Shape s = pick_shape(M, N);
+    Shape s = pick_shape(M, N, !FUSED);
+    if (FUSED && s.bn == 384) s.bn = 256;  // the one-launch step keeps two accumulators
 #define FP8Q_LAUNCH(BNV, PR) \
     return launch_gemm<BNV, false, PR, FUSED>(a, b, sa, sb, d, M, N, K, afmt, bfmt, status, stream, fz)
     if (s.pair) {
         switch (s.bn) {
+            case 384:
+                if constexpr (!FUSED) FP8Q_LAUNCH(384, true);
+                [[fallthrough]];
             case 256: FP8Q_LAUNCH(256, true);
             case 224: FP8Q_LAUNCH(224, true);
             case 192: FP8Q_LAUNCH(192, true);
@@ -891,7 +921,7 @@ extern "C" int fp8q_gemm_set_tile(int pair, int bn) {
         return FP8Q_OK;
     }
     const bool ok1 = pair == 0 && (bn == 128 || bn == 160 || bn == 192 || bn == 256);
-    const bool ok2 = pair == 1 && (bn == 128 || bn == 160 || bn == 192 || bn == 224 || bn == 256);
+    const bool ok2 = pair == 1 && (bn == 128 || bn == 160 || bn == 192 || bn == 224 || bn == 256 || bn == 384);
     if (!ok1 && !ok2) return FP8Q_ERR_UNSUPPORTED;
     g_tile_override.store((pair << 16) | bn);
     return FP8Q_OK;

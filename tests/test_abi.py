@@ -129,6 +129,8 @@ def test_gemm_tile_knob_arguments(lib):
     assert lib.fp8q_gemm_set_tile(0, 224) == ERR_UNSUPPORTED
     assert lib.fp8q_gemm_set_tile(2, 128) == ERR_UNSUPPORTED
     assert lib.fp8q_gemm_set_tile(1, 224) == OK
+    assert lib.fp8q_gemm_set_tile(1, 384) == OK
+    assert lib.fp8q_gemm_set_tile(0, 384) == ERR_UNSUPPORTED
     assert lib.fp8q_gemm_set_tile(0, 160) == OK
     assert lib.fp8q_gemm_set_tile(-1, 0) == OK
 

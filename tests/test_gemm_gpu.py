@@ -125,7 +125,7 @@ def test_constant_sign_long_contraction():
     assert_gemm_close(y, Yr, S)
 
 
-TILES = [(0, 128), (0, 160), (0, 192), (0, 256), (1, 128), (1, 160), (1, 192), (1, 224), (1, 256)]
+TILES = [(0, 128), (0, 160), (0, 192), (0, 256), (1, 128), (1, 160), (1, 192), (1, 224), (1, 256), (1, 384)]
 
 
 @pytest.mark.parametrize("pair,bn", TILES)
