@@ -509,7 +509,7 @@ def measure_extras(args, dp, H, Wt, flush, kern_ms, w, dev) -> dict:
     t_bf16_path = timed_b2b([lambda h=h: (B.fp8q_naive_act(h, B.ACT_RELU2, a_naive),
                                           torch.matmul(a_naive, Wt, out=y16)) for h in Hs], reps)
     del acts, Hs
-    rows = measure_other_rows(w, dev, flush, max(20, min(200, args.steps)), H[0], Wt)
+    rows = measure_other_rows(w, dev, flush, max(24, min(200, args.steps)), H[0], Wt)
     t_fused = kern_ms["quant_h_only"]
     t_fp8_path = kern_ms["quant"] + kern_ms["gemm"]
     flops = 2.0 * M * N * K
@@ -527,44 +527,72 @@ def measure_extras(args, dp, H, Wt, flush, kern_ms, w, dev) -> dict:
 
 
 def measure_other_rows(w, dev, flush, reps, H, Wt) -> dict:
-    """The path's other rows on the same shapes, each call alone with L2 flushed
-    before it (event pair per call, so a few microseconds of launch latency are
-    included):
-    the W cast in both layouts, the E5M2 gradient cast and the dgrad GEMM
-    dX = dY W^T, the 1x128 group quantize and the group-scaled GEMM."""
+    """The path's other rows on the same shapes, each timed like the step's
+    kernels (back-to-back launches in one CUDA graph over rotating input copies
+    that together exceed L2): the W cast in both layouts, the E5M2 gradient
+    cast and the dgrad GEMM dX = dY W^T, the 1x128 group quantize and the
+    group-scaled GEMM.  Each row carries its roofline fraction."""
     from quantize_fp8_gemm_gb300 import binding as B
     M, K, N = w.M, w.K, w.N
+    peaks = measured_peaks()
+    hbm, fp8 = peaks["hbm_gbs"], 2.0 * peaks["bf16_tflops"]
+    l2_bytes = 256 << 20  # copies of each input until they exceed L2 twice over
+
+    def copies(t):
+        n = max(2, -(-l2_bytes // (t.numel() * t.element_size())))
+        return [t] + [t.clone() for _ in range(n - 1)]
+
+    def mem_row(ms, nbytes):
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        return {"ms": ms, "GB/s": gbs, "bound": "hbm", "frac": gbs / hbm}
+
+    def mma_row(ms, flops):
+        tf = flops / (ms * 1e-3) / 1e12
+        return {"ms": ms, "TFLOP/s": tf, "bound": "tensor", "frac": tf / fp8}
+
     out = {}
     one = torch.ones(1, device=dev)
     w_q = torch.empty(K, N, dtype=torch.uint8, device=dev)
     wt_q = torch.empty(N, K, dtype=torch.uint8, device=dev)
     amax = torch.zeros(1, device=dev)
-    t = timed(lambda: B.fp8_quant_fused(Wt, B.ACT_IDENTITY, B.E4M3, one, q_out=w_q, q_t_out=wt_q,
-                                        amax_out=amax), flush, reps)
-    out["w_cast_both_layouts"] = {"ms": t, "GB/s": 4.0 * K * N / (t * 1e-3) / 1e9}
+    Ws = copies(Wt)
+    t = timed_b2b([lambda x=x: B.fp8_quant_fused(x, B.ACT_IDENTITY, B.E4M3, one, q_out=w_q, q_t_out=wt_q,
+                                                 amax_out=amax) for x in Ws], reps)
+    out["w_cast_both_layouts (a7)"] = mem_row(t, 4.0 * K * N)
+    del Ws
     g = torch.Generator(device=dev).manual_seed(w.seed)
     dY = (torch.randn(M, N, device=dev, generator=g) * 1e-3).to(torch.bfloat16)
     dyq = torch.empty(M, N, dtype=torch.uint8, device=dev)
     sdy = torch.full((1,), 2.0 ** 14, device=dev)
-    t = timed(lambda: B.fp8_quant_fused(dY, B.ACT_IDENTITY, B.E5M2, sdy, q_out=dyq, amax_out=amax),
-              flush, reps)
-    out["dy_cast_e5m2"] = {"ms": t, "GB/s": 3.0 * M * N / (t * 1e-3) / 1e9}
+    dYs = copies(dY)
+    t = timed_b2b([lambda x=x: B.fp8_quant_fused(x, B.ACT_IDENTITY, B.E5M2, sdy, q_out=dyq, amax_out=amax)
+                   for x in dYs], reps)
+    out["dy_cast_e5m2 (a10)"] = mem_row(t, 3.0 * M * N)
+    del dYs
+    B.fp8_quant_fused(Wt, B.ACT_IDENTITY, B.E4M3, one, q_out=w_q, q_t_out=wt_q, amax_out=amax)
     dx = torch.empty(M, K, dtype=torch.bfloat16, device=dev)
-    t = timed(lambda: B.fp8_gemm_dgrad(dyq, w_q, sdy, one, dx), flush, reps)
-    out["gemm_dgrad"] = {"ms": t, "TFLOP/s": 2.0 * M * N * K / (t * 1e-3) / 1e12}
+    dyqs = copies(dyq)
+    t = timed_b2b([lambda x=x: B.fp8_gemm_dgrad(x, w_q, sdy, one, dx) for x in dyqs], reps)
+    out["gemm_dgrad (a11)"] = mma_row(t, 2.0 * M * N * K)
+    del dyqs
     if K % 128 == 0 and N % 128 == 0:
         xq = torch.empty(M, K, dtype=torch.uint8, device=dev)
         act = torch.empty(M, K, dtype=torch.bfloat16, device=dev)
         gsx = torch.empty(M, K // 128, device=dev)
         gsw = torch.empty(K // 128, N // 128, device=dev)
-        t = timed(lambda: B.fp8_quant_fused(H, B.ACT_RELU2, B.E4M3, None, act_out=act, q_out=xq, amax_out=amax,
-                                            group_scales_out=gsx, group_rows=1), flush, reps)
-        out["quant_group_1x128"] = {"ms": t, "GB/s": 5.0 * M * K / (t * 1e-3) / 1e9}
+        Hs = copies(H)
+        t = timed_b2b([lambda x=x: B.fp8_quant_fused(x, B.ACT_RELU2, B.E4M3, None, act_out=act, q_out=xq,
+                                                     amax_out=amax, group_scales_out=gsx, group_rows=1)
+                       for x in Hs], reps)
+        out["quant_group_1x128 (a8)"] = mem_row(t, 5.0 * M * K + 4.0 * M * (K // 128))
+        del Hs
         B.fp8_quant_fused(Wt, B.ACT_IDENTITY, B.E4M3, None, q_t_out=wt_q, amax_out=amax,
                           group_scales_out=gsw, group_rows=128)
         y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
-        t = timed(lambda: B.fp8_gemm_fwd(xq, wt_q, gsx, gsw, y, group_mode=1), flush, reps)
-        out["gemm_group_scaled"] = {"ms": t, "TFLOP/s": 2.0 * M * N * K / (t * 1e-3) / 1e12}
+        xqs = copies(xq)
+        t = timed_b2b([lambda x=x: B.fp8_gemm_fwd(x, wt_q, gsx, gsw, y, group_mode=1) for x in xqs], reps)
+        out["gemm_group_scaled (a12)"] = mma_row(t, 2.0 * M * N * K)
+        del xqs
     return out
 
 

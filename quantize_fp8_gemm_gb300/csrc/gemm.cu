@@ -51,6 +51,7 @@ constexpr int BK = 128;            // K bytes per stage = one 128-byte swizzle r
 constexpr int UMMA_K = 32;         // K per tcgen05.mma for 8-bit operands
 constexpr int kThreadsGemm = 192;  // 6 warps
 constexpr int kEpiWarps = 4;
+constexpr int kGroupEpiWarps = 8;  // group mode: two warps per TMEM lane quarter, half the columns each
 constexpr int kEpiChunkBytes = 32 * 32 * 2;  // one warp's 32 rows x 32 BF16 columns
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per wait: far above any real wait
 
@@ -61,8 +62,10 @@ constexpr int kQuantThreads = kQuantWarps * 32;
 constexpr int kUnitRows = 16;   // rows per quantize unit in the full rounds
 constexpr int kQuantBatch = 8;  // 16-byte loads in flight per quantize thread
 
-template <bool FUSED>
-constexpr int gemm_threads() { return kThreadsGemm + (FUSED ? kQuantThreads : 0); }
+template <bool FUSED, bool GROUP = false>
+constexpr int gemm_threads() {
+    return kThreadsGemm + (FUSED ? kQuantThreads : 0) + (GROUP ? (kGroupEpiWarps - kEpiWarps) * 32 : 0);
+}
 
 // Operands of the fused quantize.  ready[b] counts the rows of 128-row block b
 // whose E4M3 codes are written; the GEMM's producer loads a tile's A rows once
@@ -93,7 +96,7 @@ struct FusedArgs {
     HistoryArgs hx, hw;           // delayed-scale updates the last CTA runs (history == nullptr: none)
 };
 
-template <int BN, bool PAIR>
+template <int BN, bool PAIR, int EPI = kEpiWarps, int ACC = (2 * BN <= 512 ? 2 : 1)>
 struct Cfg {
     // A tile wider than 256 columns takes two MMAs per k-step (N <= 256 each)
     // into one accumulator; B then arrives as one box per MMA.
@@ -101,12 +104,13 @@ struct Cfg {
     static constexpr int MMA_N = BN / NSPLIT;
     static constexpr int B_ROWS = PAIR ? BN / 2 : BN;  // rows of B this CTA loads
     static constexpr int B_BOX = B_ROWS / NSPLIT;      // rows of B per TMA box (one per MMA)
-    static constexpr int ACCS = 2 * BN <= 512 ? 2 : 1; // TMEM accumulators (512 columns)
+    static constexpr int ACCS = ACC;                   // TMEM accumulators (512 columns)
     static constexpr int A_BYTES = BM * BK;
     static constexpr int B_BYTES = B_ROWS * BK;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int TX_BYTES = STAGE_BYTES * (PAIR ? 2 : 1);  // bytes one stage's barrier awaits
-    static constexpr int EPI_BYTES = kEpiWarps * 2 * kEpiChunkBytes;  // double-buffered store staging
+    static constexpr int EPI_WARPS = EPI;
+    static constexpr int EPI_BYTES = EPI * 2 * kEpiChunkBytes;  // double-buffered store staging
     static constexpr int RING_BUDGET = 220 * 1024 - EPI_BYTES;
     static constexpr int STAGES = RING_BUDGET / STAGE_BYTES < 8 ? RING_BUDGET / STAGE_BYTES : 8;
     static constexpr int TMEM_COLS = (ACCS * BN <= 256) ? 256 : 512;  // power of 2
@@ -114,23 +118,27 @@ struct Cfg {
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EPI_BYTES + BAR_BYTES + 1024;  // + alignment slack
     static constexpr int MMA_M = PAIR ? 2 * BM : BM;
     static constexpr int TILE_M = MMA_M;                              // output rows per tile
-    static constexpr int EPI_ARRIVALS = kEpiWarps * (PAIR ? 2 : 1);   // per accumulator drain
+    static constexpr int EPI_ARRIVALS = EPI * (PAIR ? 2 : 1);         // per accumulator drain
     static_assert(BN % 32 == 0 && BN >= 64 && BN <= 384, "BN: multiple of 32 in [64, 384]");
     static_assert(MMA_N % 16 == 0 && MMA_N <= 256, "MMA N: multiple of 16, at most 256");
     static_assert(B_BOX % 8 == 0 && (B_BOX * BK) % 1024 == 0, "B boxes: whole 8-row swizzle atoms");
     static_assert(B_BYTES % 1024 == 0, "stage tiles stay 1024-byte aligned");
     static_assert(STAGES >= 2, "at least a double-buffered ring");
-    static_assert((2 * STAGES + 5) * 8 + 16 <= BAR_BYTES, "barrier area");
+    static_assert(ACCS >= 1 && ACCS * BN <= 512, "accumulators fit TMEM's 512 columns");
+    static_assert((2 * STAGES + 2 * ACCS + 1) * 8 + 16 <= BAR_BYTES, "barrier area");
     static_assert(SMEM_BYTES <= 232448, "dynamic shared memory per CTA");
 };
+
+// Group mode promotes every 128-long K slice, so it keeps as many
+// accumulators as TMEM holds: the MMAs run up to three slices ahead.
+template <int BN, bool GROUP, bool PAIR>
+using KernelCfg = Cfg<BN, PAIR, GROUP ? kGroupEpiWarps : kEpiWarps, GROUP ? 512 / BN : (2 * BN <= 512 ? 2 : 1)>;
 
 // Next accumulator (of ACCS) and the phase its barriers are in.
 template <int ACCS>
 __device__ __forceinline__ void next_acc(int& acc, uint32_t& acc_phase) {
-    if constexpr (ACCS == 2) {
-        acc ^= 1;
-        if (acc == 0) acc_phase ^= 1u;
-    } else {
+    if (++acc == ACCS) {
+        acc = 0;
         acc_phase ^= 1u;
     }
 }
@@ -322,6 +330,9 @@ __device__ __forceinline__ void fused_quantize(const FusedArgs& fz, const float*
 __device__ __forceinline__ void epi_store_chunk(const CUtensorMap* tmD, uint8_t* warp_stage, int& nchunk,
                                                 int lane, const float (&v)[32], int32_t col0, int32_t row0,
                                                 int64_t M, int64_t N) {
+    // A box wholly outside D is skipped outright: nchunk counts committed
+    // store groups, so the wait below covers the store that last read `buf`.
+    if (row0 >= M || col0 >= N) return;
     uint8_t* buf = warp_stage + (nchunk & 1) * kEpiChunkBytes;
     if (nchunk >= 2) {
         if (lane == 0) bulk_wait_group_read<1>();
@@ -339,7 +350,7 @@ __device__ __forceinline__ void epi_store_chunk(const CUtensorMap* tmD, uint8_t*
     }
     fence_proxy_async_smem();
     __syncwarp();
-    if (lane == 0 && row0 < M && col0 < N) {  // a box wholly outside D is not stored
+    if (lane == 0) {
         tma_store_2d(tmD, smem_u32(buf), col0, row0);
         bulk_commit_group();
     }
@@ -349,19 +360,21 @@ __device__ __forceinline__ void epi_store_chunk(const CUtensorMap* tmD, uint8_t*
 // GROUP = false: per-tensor scales, one accumulation per tile.
 // GROUP = true : 1-CTA, BN = 128; each 128-long K slice is accumulated into a
 //                fresh TMEM buffer and promoted into FP32 registers with its
-//                own 1/(s_a[row, kb] * s_b[kb, n_blk]).
+//                own 1/(s_a[row, kb] * s_b[kb, n_blk]) by 8 epilogue warps
+//                (two per TMEM lane quarter, 64 columns each), so the
+//                promotion keeps pace with the MMAs.
 // PAIR = true  : 2-SM tiles (see the file header); per-tensor scales only.
 // FUSED = true : the fused quantize + GEMM (per-tensor scales): the extra
 //                quantize warps produce A = X_q from H while the GEMM consumes
 //                finished 128-row blocks.
 template <int BN, bool GROUP, bool PAIR, bool FUSED>
-__global__ void __launch_bounds__(gemm_threads<FUSED>(), 1)
+__global__ void __launch_bounds__(gemm_threads<FUSED, GROUP>(), 1)
 fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmD,
                 const float* __restrict__ scale_a, const float* __restrict__ scale_b,
                 int64_t M, int64_t N, int64_t K, uint32_t idesc, int* __restrict__ status,
                 int hold_loads, const FusedArgs fz) {
-    using C = Cfg<BN, PAIR>;
+    using C = KernelCfg<BN, GROUP, PAIR>;
     static_assert(!GROUP || (BN == 128 && !PAIR), "group mode uses 1-CTA 128-wide tiles");
     static_assert(!(GROUP && FUSED), "the fused quantize feeds the per-tensor GEMM");
     extern __shared__ uint8_t smem_raw[];
@@ -371,9 +384,9 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     uint64_t* full = bars;
     uint64_t* empty = bars + C::STAGES;
     uint64_t* tfull = bars + 2 * C::STAGES;
-    uint64_t* tempty = bars + 2 * C::STAGES + 2;
-    uint64_t* drain = bars + 2 * C::STAGES + 4;
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * C::STAGES + 5);
+    uint64_t* tempty = tfull + C::ACCS;
+    uint64_t* drain = tempty + C::ACCS;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<int*>(tmem_holder) + 1;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -391,7 +404,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             mbar_init(smem_u32(&full[s]), 1);
             mbar_init(smem_u32(&empty[s]), 1);
         }
-        for (int a = 0; a < 2; ++a) {
+        for (int a = 0; a < C::ACCS; ++a) {
             mbar_init(smem_u32(&tfull[a]), 1);
             mbar_init(smem_u32(&tempty[a]), C::EPI_ARRIVALS);
         }
@@ -529,7 +542,8 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     else mma_commit(smem_u32(&empty[stage]));
                     if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
                     if (GROUP) {
-                        mma_commit(smem_u32(&tfull[acc]));
+                        if constexpr (PAIR) mma_commit_pair_mc(smem_u32(&tfull[acc]), 0x3);
+                        else mma_commit(smem_u32(&tfull[acc]));
                         next_acc<C::ACCS>(acc, acc_phase);
                     }
                 }
@@ -545,7 +559,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             else mma_commit(smem_u32(drain));
             wait_phase_drain(drain, 0);
         }
-    } else if (warp >= 2 + kEpiWarps) {
+    } else if (FUSED && warp >= 2 + kEpiWarps) {
         // ---------------------------------------------------- fused quantize
         if constexpr (FUSED) fused_quantize(fz, scale_a, M, K);
     } else {
@@ -557,7 +571,6 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
         // drained accumulators are reported to the leader's barrier
         const uint32_t tempty0 = PAIR ? mapa_shared(smem_u32(&tempty[0]), 0) : smem_u32(&tempty[0]);
-        const uint32_t tempty1 = PAIR ? mapa_shared(smem_u32(&tempty[1]), 0) : smem_u32(&tempty[1]);
         uint8_t* warp_stage = epi_stage + (warp - 2) * 2 * kEpiChunkBytes;
         int nchunk = 0;
         int acc = 0;
@@ -571,7 +584,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             const int64_t m_blk = tile / num_n, n_blk = tile % num_n;
             const int64_t row0 = m_blk * C::TILE_M + rank * BM + q * 32;  // this warp's first row
             const int64_t row = row0 + lane;
-            if (!GROUP) {
+            if constexpr (!GROUP) {
                 ok = wait_phase(&tfull[acc], acc_phase, abort_flag, status);
                 ok = __all_sync(0xFFFFFFFFu, ok);
                 if (!ok) break;
@@ -579,8 +592,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 #pragma unroll 1
                 for (int c = 0; c < BN / 32; ++c) {
                     uint32_t r[32];
-                    tmem_ld_x32(tmem_base + lane_base + static_cast<uint32_t>(acc * BN + c * 32), r);
-                    tmem_ld_wait();
+                    tmem_ld_x32_sync(tmem_base + lane_base + static_cast<uint32_t>(acc * BN + c * 32), r);
                     float v[32];
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]) * inv;
@@ -590,44 +602,62 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
-                    if constexpr (PAIR) mbar_arrive_cluster(acc ? tempty1 : tempty0);
-                    else mbar_arrive(acc ? tempty1 : tempty0);
+                    if constexpr (PAIR) mbar_arrive_cluster(tempty0 + 8u * acc);
+                    else mbar_arrive(tempty0 + 8u * acc);
                 }
                 next_acc<C::ACCS>(acc, acc_phase);
             } else {
-                float sum[BN];
+                // warp (warp - 2) / 4 of its lane quarter promotes columns cbase..cbase + GC - 1,
+                // all in one 128-column block of B's scales
+                constexpr int GC = BN / (C::EPI_WARPS / 4);
+                constexpr int LDB = GC > 64 ? 1 : GC / 32;  // x32 TMEM loads per wait (1 or 2)
+                static_assert(!GROUP || (GC <= 128 && 128 % GC == 0), "a warp's columns share one block scale");
+                const int cbase = ((warp - 2) / 4) * GC;
+                const int64_t nb_raw = (n_blk * BN + cbase) / 128;
+                const int64_t nb = nb_raw < ng ? nb_raw : ng - 1;  // columns past N are never stored
+                float sum[GC];
 #pragma unroll
-                for (int j = 0; j < BN; ++j) sum[j] = 0.0f;
+                for (int j = 0; j < GC; ++j) sum[j] = 0.0f;
                 const int64_t srow = row < M ? row : M - 1;
                 for (int kb = 0; kb < num_kb; ++kb) {
                     const float sa = __ldg(scale_a + srow * kg + kb);
-                    const float sb = __ldg(scale_b + kb * ng + n_blk);
+                    const float sb = __ldg(scale_b + kb * ng + nb);
                     const float ginv = 1.0f / (sa * sb);
                     ok = wait_phase(&tfull[acc], acc_phase, abort_flag, status);
                     ok = __all_sync(0xFFFFFFFFu, ok);
                     if (!ok) break;
                     tc_fence_after();
 #pragma unroll
-                    for (int c = 0; c < BN / 32; ++c) {
-                        uint32_t r[32];
-                        tmem_ld_x32(tmem_base + lane_base + static_cast<uint32_t>(acc * BN + c * 32), r);
-                        tmem_ld_wait();
+                    for (int c0 = 0; c0 < GC / 32; c0 += LDB) {
+                        uint32_t r[LDB][32];
+                        const uint32_t ta = tmem_base + lane_base + static_cast<uint32_t>(acc * BN + cbase + c0 * 32);
+                        if constexpr (LDB == 2) tmem_ld_2x32_sync(ta, ta + 32, r[0], r[1]);
+                        else tmem_ld_x32_sync(ta, r[0]);
+                        if (c0 + LDB == GC / 32) {
+                            // the accumulator is in registers: the MMA may reuse it
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) {
+                                if constexpr (PAIR) mbar_arrive_cluster(tempty0 + 8u * acc);
+                                else mbar_arrive(tempty0 + 8u * acc);
+                            }
+                        }
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) sum[c * 32 + j] = fmaf(__uint_as_float(r[j]), ginv, sum[c * 32 + j]);
+                        for (int b = 0; b < LDB; ++b)
+#pragma unroll
+                            for (int j = 0; j < 32; ++j)
+                                sum[(c0 + b) * 32 + j] = fmaf(__uint_as_float(r[b][j]), ginv, sum[(c0 + b) * 32 + j]);
                     }
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(acc ? tempty1 : tempty0);
                     next_acc<C::ACCS>(acc, acc_phase);
                 }
                 if (!ok) break;
 #pragma unroll
-                for (int c = 0; c < BN / 32; ++c) {
+                for (int c = 0; c < GC / 32; ++c) {
                     float v[32];
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v[j] = sum[c * 32 + j];
-                    epi_store_chunk(&tmD, warp_stage, nchunk, lane, v, static_cast<int32_t>(n_blk * BN + c * 32),
-                                    static_cast<int32_t>(row0), M, N);
+                    epi_store_chunk(&tmD, warp_stage, nchunk, lane, v,
+                                    static_cast<int32_t>(n_blk * BN + cbase + c * 32), static_cast<int32_t>(row0), M, N);
                 }
             }
         }
@@ -727,7 +757,7 @@ struct LaunchInfo {
 
 template <int BN, bool GROUP, bool PAIR, bool FUSED>
 const LaunchInfo& launch_info() {
-    using C = Cfg<BN, PAIR>;
+    using C = KernelCfg<BN, GROUP, PAIR>;
     static LaunchInfo info;
     static std::once_flag once;
     std::call_once(once, [] {
@@ -741,7 +771,7 @@ const LaunchInfo& launch_info() {
             attr[0].val.clusterDim.y = 1;
             attr[0].val.clusterDim.z = 1;
             cfg.gridDim = dim3(2 * sm_count());
-            cfg.blockDim = dim3(gemm_threads<FUSED>());
+            cfg.blockDim = dim3(gemm_threads<FUSED, GROUP>());
             cfg.dynamicSmemBytes = C::SMEM_BYTES;
             cfg.attrs = attr;
             cfg.numAttrs = 1;
@@ -760,7 +790,7 @@ template <int BN, bool GROUP, bool PAIR, bool FUSED>
 int launch_gemm(const void* a, const void* b, const float* sa, const float* sb, void* d, int64_t M,
                 int64_t N, int64_t K, uint32_t afmt, uint32_t bfmt, int* status, cudaStream_t stream,
                 const FusedArgs& fz) {
-    using C = Cfg<BN, PAIR>;
+    using C = KernelCfg<BN, GROUP, PAIR>;
     const LaunchInfo& info = launch_info<BN, GROUP, PAIR, FUSED>();
     if (info.attr_err != cudaSuccess) return FP8Q_ERR_CUDA;
     alignas(64) CUtensorMap mapA, mapB, mapD;
@@ -784,7 +814,7 @@ int launch_gemm(const void* a, const void* b, const float* sa, const float* sb, 
         attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[1].val.programmaticStreamSerializationAllowed = 1;
         cfg.gridDim = dim3(2 * clusters);
-        cfg.blockDim = dim3(gemm_threads<FUSED>());
+        cfg.blockDim = dim3(gemm_threads<FUSED, GROUP>());
         cfg.dynamicSmemBytes = C::SMEM_BYTES;
         cfg.stream = stream;
         cfg.attrs = attr;
@@ -800,7 +830,7 @@ int launch_gemm(const void* a, const void* b, const float* sa, const float* sb, 
         const int grid = static_cast<int>(FUSED ? sm_count() : std::min<int64_t>(tiles, sm_count()));
         FusedArgs f = fz;
         if (f.w) f.w_units = static_cast<unsigned>(grid * kEpiWarps);  // each epilogue warp reports once
-        if (launch_pdl(kern, dim3(grid), dim3(gemm_threads<FUSED>()), C::SMEM_BYTES, stream, mapA, mapB, mapD, sa,
+        if (launch_pdl(kern, dim3(grid), dim3(gemm_threads<FUSED, GROUP>()), C::SMEM_BYTES, stream, mapA, mapB, mapD, sa,
                        sb, M, N, K, idesc, status, g_hold_loads.load(), f) != cudaSuccess) {
             (void)cudaGetLastError();
             return FP8Q_ERR_CUDA;
@@ -858,8 +888,9 @@ int gemm_dispatch_t(const void* a, const void* b, const float* sa, const float* 
                     int64_t M, int64_t N, int64_t K, uint32_t afmt, uint32_t bfmt, int* status,
                     cudaStream_t stream, const FusedArgs& fz) {
     if constexpr (!FUSED) {
-        if (group)
+        if (group) {
             return launch_gemm<128, true, false, false>(a, b, sa, sb, d, M, N, K, afmt, bfmt, status, stream, fz);
+        }
     }
     Shape s = pick_shape(M, N, !FUSED);
     if (FUSED && s.bn == 384) s.bn = 256;  // the one-launch step keeps two accumulators

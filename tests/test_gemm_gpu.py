@@ -113,6 +113,30 @@ def test_group_scaled_fwd(M, N, K):
     assert_gemm_close(y, Yr, S)
 
 
+GROUP_TILES = [(0, 128)]
+
+
+@pytest.mark.parametrize("pair,bn", GROUP_TILES)
+def test_group_scaled_every_tile(pair, bn):
+    """Group-scaled forward on each group-mode tile (1-CTA 128 and 256 wide)
+    over problems whose M and N leave partial tiles; N = 640 puts a 256-wide
+    tile's last scale block past N."""
+    try:
+        B.fp8q_gemm_set_tile(pair, bn)
+        for M, N, K in [(1000, 400, 384), (300, 768, 1152), (129, 144, 256), (257, 640, 128)]:
+            rng = np.random.default_rng(M + 5 * N + K)
+            xq = rand_e4m3((M, K), seed=M + 11, scale=30.0)
+            wq = rand_e4m3((K, N), seed=N + 13, scale=30.0)
+            ng = (N + 127) // 128
+            sx = (2.0 ** rng.uniform(-4, 4, (M, K // 128))).astype(np.float32)
+            sw = (2.0 ** rng.uniform(-4, 4, (K // 128, ng))).astype(np.float32)
+            Yr, S = O.gemm_fwd(xq, wq, sx, sw, group=True)
+            y = run_fwd(xq, wq, sx, sw, group=True)
+            assert_gemm_close(y, Yr, S)
+    finally:
+        B.fp8q_gemm_set_tile(-1)
+
+
 def test_constant_sign_long_contraction():
     """All-positive operands over K = 6400: the accumulation error does not cancel,
     which exposes a reduced-precision accumulator."""
