@@ -509,7 +509,7 @@ def measure_extras(args, dp, H, Wt, flush, kern_ms, w, dev) -> dict:
     t_bf16_path = timed_b2b([lambda h=h: (B.fp8q_naive_act(h, B.ACT_RELU2, a_naive),
                                           torch.matmul(a_naive, Wt, out=y16)) for h in Hs], reps)
     del acts, Hs
-    rows = measure_other_rows(w, dev, flush, max(24, min(200, args.steps)), H[0], Wt)
+    rows = measure_other_rows(dev, max(16, min(64, args.steps)))
     t_fused = kern_ms["quant_h_only"]
     t_fp8_path = kern_ms["quant"] + kern_ms["gemm"]
     flops = 2.0 * M * N * K
@@ -526,73 +526,80 @@ def measure_extras(args, dp, H, Wt, flush, kern_ms, w, dev) -> dict:
     }
 
 
-def measure_other_rows(w, dev, flush, reps, H, Wt) -> dict:
-    """The path's other rows on the same shapes, each timed like the step's
-    kernels (back-to-back launches in one CUDA graph over rotating input copies
-    that together exceed L2): the W cast in both layouts, the E5M2 gradient
-    cast and the dgrad GEMM dX = dY W^T, the 1x128 group quantize and the
-    group-scaled GEMM.  Each row carries its roofline fraction."""
+def measure_other_rows(dev, reps: int) -> dict:
+    """The path's other rows, each on the workload it belongs to and timed like
+    the step's kernels (back-to-back launches captured in one CUDA graph, the
+    inputs larger than L2 or rotated over copies that together exceed it):
+    the weight cast in both layouts, the E5M2 gradient cast and the dgrad GEMM
+    dX = dY W^T on the GPT-2-XL shapes, the 1x128 group quantize and the
+    group-scaled GEMM on the outlier shapes.  Each row carries its roofline
+    fraction of the measured peaks."""
     from quantize_fp8_gemm_gb300 import binding as B
-    M, K, N = w.M, w.K, w.N
     peaks = measured_peaks()
     hbm, fp8 = peaks["hbm_gbs"], 2.0 * peaks["bf16_tflops"]
-    l2_bytes = 256 << 20  # copies of each input until they exceed L2 twice over
+    l2_bytes = 256 << 20  # rotate copies until the inputs exceed L2 twice over
 
     def copies(t):
-        n = max(2, -(-l2_bytes // (t.numel() * t.element_size())))
+        n = max(1, -(-l2_bytes // (t.numel() * t.element_size())))
         return [t] + [t.clone() for _ in range(n - 1)]
 
-    def mem_row(ms, nbytes):
+    def mem_row(ms, nbytes, shape):
         gbs = nbytes / (ms * 1e-3) / 1e9
-        return {"ms": ms, "GB/s": gbs, "bound": "hbm", "frac": gbs / hbm}
+        return {"shape": shape, "ms": ms, "GB/s": gbs, "bound": "hbm", "frac": gbs / hbm,
+                "algorithmic_bytes": nbytes}
 
-    def mma_row(ms, flops):
+    def mma_row(ms, flops, shape):
         tf = flops / (ms * 1e-3) / 1e12
-        return {"ms": ms, "TFLOP/s": tf, "bound": "tensor", "frac": tf / fp8}
+        return {"shape": shape, "ms": ms, "TFLOP/s": tf, "bound": "tensor", "frac": tf / fp8,
+                "algorithmic_flops": flops}
 
     out = {}
-    one = torch.ones(1, device=dev)
-    w_q = torch.empty(K, N, dtype=torch.uint8, device=dev)
-    wt_q = torch.empty(N, K, dtype=torch.uint8, device=dev)
     amax = torch.zeros(1, device=dev)
-    Ws = copies(Wt)
-    t = timed_b2b([lambda x=x: B.fp8_quant_fused(x, B.ACT_IDENTITY, B.E4M3, one, q_out=w_q, q_t_out=wt_q,
-                                                 amax_out=amax) for x in Ws], reps)
-    out["w_cast_both_layouts (a7)"] = mem_row(t, 4.0 * K * N)
+    one = torch.ones(1, device=dev)
+    xl = WL.WORKLOADS["gpt2xl"]
+    M, K, N = xl.M, xl.K, xl.N
+    W = WL.bf16_tensor(WL.w_down(xl)).to(dev)  # [K,N]
+    w_q = torch.empty(K, N, dtype=torch.uint8, device=dev)   # dgrad operand
+    wt_q = torch.empty(N, K, dtype=torch.uint8, device=dev)  # forward operand
+    Ws = copies(W)
+    t = timed_b2b([lambda x=x: B.fp8_quant_fused_ex(x, B.ACT_IDENTITY, B.E4M3, one, q_out=w_q, q_t_out=wt_q,
+                                                    amax_out=amax, flags=B.ACCUMULATE) for x in Ws], reps)
+    out["a7 weight cast, both layouts"] = mem_row(t, 4.0 * K * N, f"W [{K},{N}]")
     del Ws
-    g = torch.Generator(device=dev).manual_seed(w.seed)
-    dY = (torch.randn(M, N, device=dev, generator=g) * 1e-3).to(torch.bfloat16)
+    dY = WL.bf16_tensor(WL.dy_grad(xl)).to(dev)
     dyq = torch.empty(M, N, dtype=torch.uint8, device=dev)
-    sdy = torch.full((1,), 2.0 ** 14, device=dev)
-    dYs = copies(dY)
-    t = timed_b2b([lambda x=x: B.fp8_quant_fused(x, B.ACT_IDENTITY, B.E5M2, sdy, q_out=dyq, amax_out=amax)
-                   for x in dYs], reps)
-    out["dy_cast_e5m2 (a10)"] = mem_row(t, 3.0 * M * N)
-    del dYs
-    B.fp8_quant_fused(Wt, B.ACT_IDENTITY, B.E4M3, one, q_out=w_q, q_t_out=wt_q, amax_out=amax)
+    sdy = torch.full((1,), 4096.0, device=dev)  # 57344 / (margin * ~7): the spikes stay below the E5M2 max
+    t = timed_b2b([lambda: B.fp8_quant_fused_ex(dY, B.ACT_IDENTITY, B.E5M2, sdy, q_out=dyq, amax_out=amax,
+                                                flags=B.ACCUMULATE)], max(4, reps // 4))
+    out["a10 dY cast E5M2"] = mem_row(t, 3.0 * M * N, f"dY [{M},{N}]")
+    del dY, W
     dx = torch.empty(M, K, dtype=torch.bfloat16, device=dev)
-    dyqs = copies(dyq)
-    t = timed_b2b([lambda x=x: B.fp8_gemm_dgrad(x, w_q, sdy, one, dx) for x in dyqs], reps)
-    out["gemm_dgrad (a11)"] = mma_row(t, 2.0 * M * N * K)
-    del dyqs
-    if K % 128 == 0 and N % 128 == 0:
-        xq = torch.empty(M, K, dtype=torch.uint8, device=dev)
-        act = torch.empty(M, K, dtype=torch.bfloat16, device=dev)
-        gsx = torch.empty(M, K // 128, device=dev)
-        gsw = torch.empty(K // 128, N // 128, device=dev)
-        Hs = copies(H)
-        t = timed_b2b([lambda x=x: B.fp8_quant_fused(x, B.ACT_RELU2, B.E4M3, None, act_out=act, q_out=xq,
-                                                     amax_out=amax, group_scales_out=gsx, group_rows=1)
-                       for x in Hs], reps)
-        out["quant_group_1x128 (a8)"] = mem_row(t, 5.0 * M * K + 4.0 * M * (K // 128))
-        del Hs
-        B.fp8_quant_fused(Wt, B.ACT_IDENTITY, B.E4M3, None, q_t_out=wt_q, amax_out=amax,
-                          group_scales_out=gsw, group_rows=128)
-        y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
-        xqs = copies(xq)
-        t = timed_b2b([lambda x=x: B.fp8_gemm_fwd(x, wt_q, gsx, gsw, y, group_mode=1) for x in xqs], reps)
-        out["gemm_group_scaled (a12)"] = mma_row(t, 2.0 * M * N * K)
-        del xqs
+    t = timed_b2b([lambda: B.fp8_gemm_dgrad(dyq, w_q, sdy, one, dx)], max(4, reps // 8))
+    out["a11 dgrad GEMM"] = mma_row(t, 2.0 * M * N * K, f"dY_q [{M},{N}] x W_q [{K},{N}]^T")
+    del dx, dyq, w_q, wt_q
+    ol = WL.WORKLOADS["outlier"]
+    M, K, N = ol.M, ol.K, ol.N
+    H = WL.bf16_tensor(WL.h_preact(ol)).to(dev)
+    xq = torch.empty(M, K, dtype=torch.uint8, device=dev)
+    act = torch.empty(M, K, dtype=torch.bfloat16, device=dev)
+    gsx = torch.empty(M, K // 128, device=dev)
+    Hs = copies(H)
+    t = timed_b2b([lambda x=x: B.fp8_quant_fused_ex(x, B.ACT_RELU2, B.E4M3, None, act_out=act, q_out=xq,
+                                                    amax_out=amax, group_scales_out=gsx, group_rows=1,
+                                                    flags=B.ACCUMULATE) for x in Hs], reps)
+    out["a8 group quantize 1x128"] = mem_row(t, 5.0 * M * K + 4.0 * M * (K // 128), f"H [{M},{K}]")
+    del Hs, H, act
+    W = WL.bf16_tensor(WL.w_down(ol)).to(dev)
+    wt_q = torch.empty(N, K, dtype=torch.uint8, device=dev)
+    gsw = torch.empty(K // 128, (N + 127) // 128, device=dev)
+    B.fp8_quant_fused(W, B.ACT_IDENTITY, B.E4M3, None, q_t_out=wt_q, amax_out=amax, group_scales_out=gsw,
+                      group_rows=128)
+    y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+    xqs = copies(xq)
+    t = timed_b2b([lambda x=x: B.fp8_gemm_fwd(x, wt_q, gsx, gsw, y, group_mode=1) for x in xqs], reps)
+    out["a12 group-scaled GEMM"] = mma_row(t, 2.0 * M * N * K, f"X_q [{M},{K}] x W_q^T [{N},{K}]")
+    del xqs, xq, W, wt_q, y
+    torch.cuda.empty_cache()
     return out
 
 

@@ -149,7 +149,39 @@ quant_stream_kernel(const uint4* __restrict__ h, int64_t nchunks, const float* _
 // holds one 128-wide row segment (a 1x128 group when the tile is aligned).
 // ---------------------------------------------------------------------------
 constexpr int kTile = 128;
-constexpr int kTqPitch = kTile + 8;  // bytes per row of the FP8 tile in shared memory
+constexpr int kTqPitch = kTile;  // bytes per row of the FP8 tile in shared memory
+
+// Write the tile's FP8 codes (tq: kTile rows of kTile bytes in shared memory,
+// complete) transposed into q_t [K,M]: output row k = col0 + j holds tile
+// column j.  Warp w owns tile rows 16w..16w+15 and lane l tile columns
+// 4l..4l+3: each of the warp's sixteen 32-bit reads is one whole tile row
+// (every bank once), and a 4x4 byte transpose in registers (byte_perm) turns
+// the lane's 16 x 4 bytes into four 16-byte pieces, rows 16w..16w+15 of its
+// four output rows.  M % 16 == 0, so a piece is inside q_t whenever its first
+// row is.
+__device__ __forceinline__ void store_transposed(const uint8_t* tq, uint8_t* __restrict__ q_t_out, int64_t M,
+                                                 int64_t K, int64_t row0, int64_t col0) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    static_assert(kThreads / 32 * 16 == kTile && 32 * 4 == kTile, "8 warps x 16 rows, 32 lanes x 4 columns");
+    uint32_t x[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) x[i] = *reinterpret_cast<const uint32_t*>(tq + (warp * 16 + i) * kTqPitch + lane * 4);
+    const int64_t mcol = row0 + warp * 16;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        // byte c of the first word -> byte 0, byte c of the second -> byte 1
+        const uint32_t sel = static_cast<uint32_t>(c) | (static_cast<uint32_t>(4 + c) << 4);
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t lo = __byte_perm(x[4 * j], x[4 * j + 1], sel);
+            const uint32_t hi = __byte_perm(x[4 * j + 2], x[4 * j + 3], sel);
+            o[j] = __byte_perm(lo, hi, 0x5410);  // lo bytes 0,1 then hi bytes 0,1
+        }
+        const int64_t krow = col0 + lane * 4 + c;
+        if (krow < K && mcol < M) st_v4(q_t_out + krow * M + mcol, make_uint4(o[0], o[1], o[2], o[3]));
+    }
+}
 
 // One 128x128 tile (bx, by) of h [M,K]; per-tensor scale, or the tile's
 // 128x128 block scale, or 1x128 row-group scales (gscale, group_rows).
@@ -228,23 +260,7 @@ __device__ __forceinline__ void tile_body(const uint16_t* __restrict__ h, int64_
 
     if (q_t_out) {
         __syncthreads();
-        // output row k = col0 + kk of q_t [K,M]: 16-byte piece rc holds tile rows rc*16..+15
-#pragma unroll
-        for (int it = 0; it < 4; ++it) {
-            const int c = it * kThreads + tid;
-            const int rc = c & 7, kk = c >> 3;
-            const int64_t krow = col0 + kk, mcol = row0 + rc * 16;
-            uint32_t w[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const uint8_t* p = tq + (rc * 16 + j * 4) * kTqPitch + kk;
-                w[j] = static_cast<uint32_t>(p[0]) | (static_cast<uint32_t>(p[kTqPitch]) << 8) |
-                       (static_cast<uint32_t>(p[2 * kTqPitch]) << 16) |
-                       (static_cast<uint32_t>(p[3 * kTqPitch]) << 24);
-            }
-            if (krow < K && mcol < M)
-                st_v4(q_t_out + krow * M + mcol, make_uint4(w[0], w[1], w[2], w[3]));
-        }
+        store_transposed(tq, q_t_out, M, K, row0, col0);
     }
 }
 
@@ -336,23 +352,7 @@ __device__ __forceinline__ void tile_pt_body(const uint16_t* __restrict__ h, int
     }
     if (q_t_out) {
         __syncthreads();
-        // output row k = col0 + kk of q_t [K,M]: 16-byte piece rc holds tile rows rc*16..+15
-#pragma unroll
-        for (int it = 0; it < 4; ++it) {
-            const int c = it * kThreads + tid;
-            const int rc = c & 7, kk = c >> 3;
-            const int64_t krow = col0 + kk, mcol = row0 + rc * 16;
-            uint32_t w[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const uint8_t* p = tq + (rc * 16 + j * 4) * kTqPitch + kk;
-                w[j] = static_cast<uint32_t>(p[0]) | (static_cast<uint32_t>(p[kTqPitch]) << 8) |
-                       (static_cast<uint32_t>(p[2 * kTqPitch]) << 16) |
-                       (static_cast<uint32_t>(p[3 * kTqPitch]) << 24);
-            }
-            if (krow < K && mcol < M)
-                st_v4(q_t_out + krow * M + mcol, make_uint4(w[0], w[1], w[2], w[3]));
-        }
+        store_transposed(tq, q_t_out, M, K, row0, col0);
     }
 }
 
