@@ -13,7 +13,8 @@
 //   forward: A = X_q [M,K],   B = W_q^T [N,K]
 //   dgrad:   A = dY_q [M,N],  B = W_q [K,N]   (the contraction runs over N)
 //
-// CTA = 6 warps, persistent over output tiles (static round robin):
+// CTA = 6 warps (10 with 8 epilogue warps), persistent over output tiles
+// (static round robin):
 //   warp 0     TMA producer: one elected lane streams A/B k-blocks (128 B of
 //              K per row, 128-byte swizzle) into a STAGES-deep ring.
 //   warp 1     MMA issuer: allocates TMEM; one lane issues 4 x
@@ -21,8 +22,10 @@
 //              stage back to the producer.
 //   warps 2-5  epilogue: tcgen05.ld the FP32 accumulator (each warp its 32
 //              TMEM lanes), scale by 1/(s_a s_b), round to BF16, store.
+//              Group mode and the 384-wide tile add warps 6-9, a second
+//              warp per lane quarter taking half of the columns.
 // Two TMEM accumulators let the epilogue of tile i overlap the main loop of
-// tile i+1.
+// tile i+1 (group mode keeps four; the 384-wide tile has room for one).
 //
 // PAIR = true: a cluster of two CTAs on two SMs computes a 256 x BN tile with
 // tcgen05.mma.cta_group::2 (M = 256).  Each CTA loads its own 128 rows of A
@@ -51,7 +54,7 @@ constexpr int BK = 128;            // K bytes per stage = one 128-byte swizzle r
 constexpr int UMMA_K = 32;         // K per tcgen05.mma for 8-bit operands
 constexpr int kThreadsGemm = 192;  // 6 warps
 constexpr int kEpiWarps = 4;
-constexpr int kGroupEpiWarps = 8;  // group mode: two warps per TMEM lane quarter, half the columns each
+constexpr int kWideEpiWarps = 8;  // two warps per TMEM lane quarter, each half the columns
 constexpr int kEpiChunkBytes = 32 * 32 * 2;  // one warp's 32 rows x 32 BF16 columns
 constexpr uint64_t kTimeoutNs = 2000000000ull;  // 2 s per wait: far above any real wait
 
@@ -62,9 +65,17 @@ constexpr int kQuantThreads = kQuantWarps * 32;
 constexpr int kUnitRows = 16;   // rows per quantize unit in the full rounds
 constexpr int kQuantBatch = 8;  // 16-byte loads in flight per quantize thread
 
-template <bool FUSED, bool GROUP = false>
+// Epilogue warps: 8 where the epilogue is exposed -- group mode (a promotion
+// per 128-long K slice) and the 384-wide tile (one accumulator, so its drain is
+// not hidden behind the next tile; 17.2 -> 16.4 us at 8192 x 3072 -> 768) --
+// else 4 (8 would take a stage of the operand ring: 87.6 -> 92.6 us at 65536
+// rows with 256-wide tiles).
+template <int BN, bool GROUP, bool FUSED>
+constexpr int epi_warps() { return !FUSED && (GROUP || BN > 256) ? kWideEpiWarps : kEpiWarps; }
+
+template <int BN, bool GROUP, bool FUSED>
 constexpr int gemm_threads() {
-    return kThreadsGemm + (FUSED ? kQuantThreads : 0) + (GROUP ? (kGroupEpiWarps - kEpiWarps) * 32 : 0);
+    return kThreadsGemm + (FUSED ? kQuantThreads : 0) + (epi_warps<BN, GROUP, FUSED>() - kEpiWarps) * 32;
 }
 
 // Operands of the fused quantize.  ready[b] counts the rows of 128-row block b
@@ -131,8 +142,8 @@ struct Cfg {
 
 // Group mode promotes every 128-long K slice, so it keeps as many
 // accumulators as TMEM holds: the MMAs run up to three slices ahead.
-template <int BN, bool GROUP, bool PAIR>
-using KernelCfg = Cfg<BN, PAIR, GROUP ? kGroupEpiWarps : kEpiWarps, GROUP ? 512 / BN : (2 * BN <= 512 ? 2 : 1)>;
+template <int BN, bool GROUP, bool PAIR, bool FUSED>
+using KernelCfg = Cfg<BN, PAIR, epi_warps<BN, GROUP, FUSED>(), GROUP ? 512 / BN : (2 * BN <= 512 ? 2 : 1)>;
 
 // Next accumulator (of ACCS) and the phase its barriers are in.
 template <int ACCS>
@@ -368,13 +379,13 @@ __device__ __forceinline__ void epi_store_chunk(const CUtensorMap* tmD, uint8_t*
 //                quantize warps produce A = X_q from H while the GEMM consumes
 //                finished 128-row blocks.
 template <int BN, bool GROUP, bool PAIR, bool FUSED>
-__global__ void __launch_bounds__(gemm_threads<FUSED, GROUP>(), 1)
+__global__ void __launch_bounds__(gemm_threads<BN, GROUP, FUSED>(), 1)
 fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmD,
                 const float* __restrict__ scale_a, const float* __restrict__ scale_b,
                 int64_t M, int64_t N, int64_t K, uint32_t idesc, int* __restrict__ status,
                 int hold_loads, const FusedArgs fz) {
-    using C = KernelCfg<BN, GROUP, PAIR>;
+    using C = KernelCfg<BN, GROUP, PAIR, FUSED>;
     static_assert(!GROUP || (BN == 128 && !PAIR), "group mode uses 1-CTA 128-wide tiles");
     static_assert(!(GROUP && FUSED), "the fused quantize feeds the per-tensor GEMM");
     extern __shared__ uint8_t smem_raw[];
@@ -589,8 +600,9 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 ok = __all_sync(0xFFFFFFFFu, ok);
                 if (!ok) break;
                 tc_fence_after();
+                // with 8 epilogue warps the two warps of a lane quarter take alternate chunks
 #pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
+                for (int c = (warp - 2) / 4; c < BN / 32; c += C::EPI_WARPS / 4) {
                     uint32_t r[32];
                     tmem_ld_x32_sync(tmem_base + lane_base + static_cast<uint32_t>(acc * BN + c * 32), r);
                     float v[32];
@@ -757,7 +769,7 @@ struct LaunchInfo {
 
 template <int BN, bool GROUP, bool PAIR, bool FUSED>
 const LaunchInfo& launch_info() {
-    using C = KernelCfg<BN, GROUP, PAIR>;
+    using C = KernelCfg<BN, GROUP, PAIR, FUSED>;
     static LaunchInfo info;
     static std::once_flag once;
     std::call_once(once, [] {
@@ -771,7 +783,7 @@ const LaunchInfo& launch_info() {
             attr[0].val.clusterDim.y = 1;
             attr[0].val.clusterDim.z = 1;
             cfg.gridDim = dim3(2 * sm_count());
-            cfg.blockDim = dim3(gemm_threads<FUSED, GROUP>());
+            cfg.blockDim = dim3(gemm_threads<BN, GROUP, FUSED>());
             cfg.dynamicSmemBytes = C::SMEM_BYTES;
             cfg.attrs = attr;
             cfg.numAttrs = 1;
@@ -790,7 +802,7 @@ template <int BN, bool GROUP, bool PAIR, bool FUSED>
 int launch_gemm(const void* a, const void* b, const float* sa, const float* sb, void* d, int64_t M,
                 int64_t N, int64_t K, uint32_t afmt, uint32_t bfmt, int* status, cudaStream_t stream,
                 const FusedArgs& fz) {
-    using C = KernelCfg<BN, GROUP, PAIR>;
+    using C = KernelCfg<BN, GROUP, PAIR, FUSED>;
     const LaunchInfo& info = launch_info<BN, GROUP, PAIR, FUSED>();
     if (info.attr_err != cudaSuccess) return FP8Q_ERR_CUDA;
     alignas(64) CUtensorMap mapA, mapB, mapD;
@@ -814,7 +826,7 @@ int launch_gemm(const void* a, const void* b, const float* sa, const float* sb, 
         attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[1].val.programmaticStreamSerializationAllowed = 1;
         cfg.gridDim = dim3(2 * clusters);
-        cfg.blockDim = dim3(gemm_threads<FUSED, GROUP>());
+        cfg.blockDim = dim3(gemm_threads<BN, GROUP, FUSED>());
         cfg.dynamicSmemBytes = C::SMEM_BYTES;
         cfg.stream = stream;
         cfg.attrs = attr;
@@ -830,7 +842,7 @@ int launch_gemm(const void* a, const void* b, const float* sa, const float* sb, 
         const int grid = static_cast<int>(FUSED ? sm_count() : std::min<int64_t>(tiles, sm_count()));
         FusedArgs f = fz;
         if (f.w) f.w_units = static_cast<unsigned>(grid * kEpiWarps);  // each epilogue warp reports once
-        if (launch_pdl(kern, dim3(grid), dim3(gemm_threads<FUSED, GROUP>()), C::SMEM_BYTES, stream, mapA, mapB, mapD, sa,
+        if (launch_pdl(kern, dim3(grid), dim3(gemm_threads<BN, GROUP, FUSED>()), C::SMEM_BYTES, stream, mapA, mapB, mapD, sa,
                        sb, M, N, K, idesc, status, g_hold_loads.load(), f) != cudaSuccess) {
             (void)cudaGetLastError();
             return FP8Q_ERR_CUDA;
