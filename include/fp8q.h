@@ -178,6 +178,25 @@ typedef struct fp8q_quant_args {
 int fp8_quant_fused_batch(const fp8q_quant_args* args, int n, cudaStream_t stream);
 
 /*
+ * fp8_cast_f32 -- FP32 -> FP8, elementwise: q[i] = FP8(x[i])  [cast]
+ *
+ * The conversion every quantize call applies to its scaled value v = BF16(act(h))
+ * * s ("FP8 training: what it is and how it works", Step 2: round to the nearest
+ * representable value; Trade-offs and edge cases: saturate instead of
+ * overflowing), exposed on its own so that it can be checked against the
+ * formats' definition over all 2^32 inputs.  Round to nearest even; finite
+ * values beyond the largest finite code and infinities give that code with the
+ * input's sign (448 for E4M3, 57344 for E5M2); NaN gives a NaN code.
+ *   x     device [n] float32, 16-byte aligned.
+ *   q     device [n] bytes (E4M3 or E5M2 codes), 16-byte aligned.
+ *   n     >= 0 (0: nothing is enqueued).
+ *   fmt   FP8Q_E4M3 or FP8Q_E5M2.
+ * Errors: FP8Q_ERR_SHAPE (n < 0), FP8Q_ERR_UNSUPPORTED (fmt, or not sm_103),
+ * FP8Q_ERR_NULL, FP8Q_ERR_ALIGN, FP8Q_ERR_CUDA (launch).
+ */
+int fp8_cast_f32(const float* x, void* q, int64_t n, int fmt, cudaStream_t stream);
+
+/*
  * fp8_gemm_fwd --Y = (X_q . W_q) / (s_x s_w), FP32 accumulation, BF16 out  [gemms][scale]
  *
  *   x_q     device [M,K] E4M3 (the activation, K contiguous).

@@ -50,6 +50,7 @@ def lib() -> ctypes.CDLL:
         L.fp8_quant_fused_ex.argtypes = [P, i64, i64, i32, i32, P, P, P, P, P, P, P, i32, ctypes.c_uint, P]
         L.fp8_gemm_fwd.argtypes = [P, P, P, P, i32, P, i64, i64, i64, P, P]
         L.fp8_quant_fused_batch.argtypes = [P, i32, P]
+        L.fp8_cast_f32.argtypes = [P, P, i64, i32, P]
         L.fp8_gemm_dgrad.argtypes = [P, P, P, P, P, i64, i64, i64, P, P]
         L.amax_history_update.argtypes = [P, i32, P, P, f32, i32, P, P, P]
         L.amax_history_update_ex.argtypes = [P, i32, P, P, f32, i32, P, P, P, P, P, P]
@@ -154,6 +155,17 @@ def fp8_quant_fused_batch(entries, stream=None) -> None:
     """Several per-tensor quantize calls (QuantArgs from quant_args) in one launch."""
     arr = (QuantArgs * len(entries))(*entries)
     _check("fp8_quant_fused_batch", lib().fp8_quant_fused_batch(arr, len(entries), _stream(stream)))
+
+
+def fp8_cast_f32(x: torch.Tensor, fmt: int, q: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """q = FP8(x) elementwise (round to nearest even, saturating): the quantize kernels' conversion."""
+    if x.dtype != torch.float32:
+        raise TypeError("x must be float32")
+    if q is None:
+        q = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    n = x.numel()
+    _check("fp8_cast_f32", lib().fp8_cast_f32(_ptr(x, 4 * n, "x"), _ptr(q, n, "q"), n, fmt, _stream(stream)))
+    return q
 
 
 def fp8_gemm_fwd(x_q: torch.Tensor, wt_q: torch.Tensor, scale_x: torch.Tensor, scale_w: torch.Tensor,

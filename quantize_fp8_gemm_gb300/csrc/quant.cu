@@ -462,11 +462,56 @@ int launch_quant_fmt(int fmt, const void* h, int64_t M, int64_t K, const float* 
                                         sat_count, gscale, group_rows, stream);
 }
 
+// FP32 -> FP8 elementwise (fp8_cast_f32): the conversion the quantize
+// kernels apply to v = BF16(act(h)) * s, four values per thread and step; the
+// thread with i == n4 converts the last n % 4 values one by one.
+template <int FMT>
+__global__ void __launch_bounds__(kThreads)
+cast_f32_kernel(const float4* __restrict__ x, uint32_t* __restrict__ q, int64_t n4, int64_t n) {
+    pdl_launch_dependents();
+    pdl_wait();
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i <= n4; i += stride) {
+        if (i < n4) {
+            const float4 v = x[i];
+            q[i] = static_cast<uint32_t>(cvt_fp8x2<FMT>(v.x, v.y)) |
+                   (static_cast<uint32_t>(cvt_fp8x2<FMT>(v.z, v.w)) << 16);
+        } else {
+            const float* xs = reinterpret_cast<const float*>(x);
+            uint8_t* qs = reinterpret_cast<uint8_t*>(q);
+            for (int64_t j = 4 * n4; j < n; ++j) qs[j] = static_cast<uint8_t>(cvt_fp8x2<FMT>(xs[j], 0.0f) & 0xFFu);
+        }
+    }
+}
+
 }  // namespace
 
 }  // namespace fp8q
 
 using namespace fp8q;
+
+extern "C" int fp8_cast_f32(const float* x, void* q, int64_t n, int fmt, cudaStream_t stream) {
+    if (n < 0) return FP8Q_ERR_SHAPE;
+    if (fmt != FP8Q_E4M3 && fmt != FP8Q_E5M2) return FP8Q_ERR_UNSUPPORTED;
+    if (n == 0) return FP8Q_OK;
+    if (x == nullptr || q == nullptr) return FP8Q_ERR_NULL;
+    if (!aligned16(x) || !aligned16(q)) return FP8Q_ERR_ALIGN;
+    if (!device_is_sm103()) return FP8Q_ERR_UNSUPPORTED;
+    const int64_t n4 = n / 4;
+    const int64_t want = (n4 + kThreads) / kThreads;  // threads for i = 0 .. n4
+    const unsigned grid = static_cast<unsigned>(std::min<int64_t>(want, int64_t(sm_count()) * 16));
+    const float4* xv = reinterpret_cast<const float4*>(x);
+    uint32_t* qv = static_cast<uint32_t*>(q);
+    const cudaError_t e = fmt == FP8Q_E5M2
+        ? launch_pdl(cast_f32_kernel<FP8Q_E5M2>, dim3(grid), dim3(kThreads), 0, stream, xv, qv, n4, n)
+        : launch_pdl(cast_f32_kernel<FP8Q_E4M3>, dim3(grid), dim3(kThreads), 0, stream, xv, qv, n4, n);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return FP8Q_ERR_CUDA;
+    }
+    FP8Q_CHECK_LAUNCH();
+    return FP8Q_OK;
+}
 
 // Argument checks of one quantize call (fp8_quant_fused_ex); the device check is the caller's.
 static int check_quant_args(const void* h, int64_t M, int64_t K, int act, int fmt, const float* scale,

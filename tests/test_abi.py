@@ -135,6 +135,21 @@ def test_gemm_tile_knob_arguments(lib):
     assert lib.fp8q_gemm_set_tile(-1, 0) == OK
 
 
+def test_cast_f32_arguments(lib):
+    """fp8_cast_f32 checks its arguments on the host, before any device work."""
+    f = lib.fp8_cast_f32
+    f.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p]
+    f.restype = ctypes.c_int
+    good = ctypes.c_void_p(1 << 20)
+    assert f(good, good, -1, 0, None) == ERR_SHAPE
+    assert f(good, good, 16, 7, None) == ERR_UNSUPPORTED
+    assert f(good, good, 0, 0, None) == OK  # nothing to do, nothing enqueued
+    assert f(None, good, 16, 0, None) == ERR_NULL
+    assert f(good, None, 16, 1, None) == ERR_NULL
+    assert f(ctypes.c_void_p((1 << 20) + 4), good, 16, 0, None) == ERR_ALIGN
+    assert f(good, ctypes.c_void_p((1 << 20) + 8), 16, 0, None) == ERR_ALIGN
+
+
 def test_quant_ex_flags(lib):
     lib.fp8_quant_fused_ex.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
                                        ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p,

@@ -98,6 +98,50 @@ def test_every_bf16_input(fmt):
         assert_same(g, r, ["q", "amax", "sat"])
 
 
+@pytest.mark.parametrize("fmt", [B.E4M3, B.E5M2])
+def test_cast_every_fp32_pattern(fmt):
+    """The kernels' FP32 -> FP8 conversion over all 2^32 float32 bit patterns
+    against the oracle's encoder, written from the formats' definition: every
+    non-NaN input gives the oracle's code bit for bit, every NaN a NaN code."""
+    import os
+    from concurrent.futures import ThreadPoolExecutor
+    chunk = 1 << 24
+    workers = max(1, min(32, len(os.sched_getaffinity(0))))
+    nan_codes = {0x7F, 0xFF} if fmt == B.E4M3 else {0x7D, 0x7E, 0x7F, 0xFD, 0xFE, 0xFF}
+    base = torch.arange(chunk, dtype=torch.int64, device="cuda")
+    q = torch.empty(chunk, dtype=torch.uint8, device="cuda")
+    piece = chunk // workers
+
+    def encode(x, lo):
+        return O.fp8_encode(x[lo:lo + piece] if lo + piece < x.size else x[lo:], fmt)
+
+    with ThreadPoolExecutor(workers) as ex:
+        for c in range(1 << 8):
+            start = c * chunk
+            bits = (base + start).to(torch.int32) if start + chunk <= (1 << 31) else (base + start - (1 << 32)).to(torch.int32)
+            B.fp8_cast_f32(bits.view(torch.float32), fmt, q)
+            got = q.cpu().numpy()
+            x = (np.arange(chunk, dtype=np.uint64) + start).astype(np.uint32).view(np.float32)
+            want = np.concatenate(list(ex.map(lambda lo: encode(x, lo), range(0, chunk, piece))))
+            nan = np.isnan(x)
+            bad = (got != want) & ~nan
+            assert not bad.any(), (f"chunk {c}: {int(bad.sum())} codes differ, first input bits "
+                                   f"0x{int(x.view(np.uint32)[bad][0]):08x}: gpu 0x{int(got[bad][0]):02x} "
+                                   f"oracle 0x{int(want[bad][0]):02x}")
+            if nan.any():
+                assert set(np.unique(got[nan]).tolist()) <= nan_codes, f"chunk {c}: a NaN gave a non-NaN code"
+
+
+def test_cast_ragged_lengths():
+    """fp8_cast_f32 on lengths that leave 1-3 values after the 4-wide steps."""
+    rng = np.random.default_rng(11)
+    for n in (1, 2, 3, 5, 4099, 1 << 16):
+        x = (rng.standard_normal(n) * 300).astype(np.float32)
+        for fmt in (B.E4M3, B.E5M2):
+            got = B.fp8_cast_f32(torch.from_numpy(x).cuda(), fmt).cpu().numpy()
+            assert np.array_equal(got, O.fp8_encode(x, fmt))
+
+
 @pytest.mark.parametrize("M,K", [(1, 128), (5, 512), (333, 256), (4096, 3072)])
 @pytest.mark.parametrize("act", [B.ACT_IDENTITY, B.ACT_RELU2])
 def test_group_1x128(M, K, act):
