@@ -57,6 +57,32 @@ def flush_l2(buf: torch.Tensor) -> None:
 
 
 # ----------------------------------------------------------------- helpers --
+def fp8_peak(dev) -> dict:
+    """Dense FP8 peak for the GEMM rooflines: the stricter (larger) of 2 x the
+    measured BF16 burst (the nominal FP8:BF16 ratio) and a cuBLASLt E4M3 GEMM
+    (torch._scaled_mm, BF16 out) at 8192^3 timed here as a burst."""
+    peaks = measured_peaks()
+    nominal = 2.0 * peaks["bf16_tflops"]
+    meas = None
+    try:
+        n = 8192
+        g = torch.Generator(device=dev).manual_seed(5)
+        a = torch.randn(n, n, device=dev, generator=g).to(torch.float8_e4m3fn)
+        b = torch.randn(n, n, device=dev, generator=g).to(torch.float8_e4m3fn).t()  # column-major operand
+        one = torch.ones((), device=dev)
+        t = timed_b2b([lambda: torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)], 20)
+        meas = 2.0 * n ** 3 / (t * 1e-3) / 1e12
+        del a, b
+    except (RuntimeError, TypeError, AttributeError) as e:  # no FP8 GEMM in this torch / cuBLASLt
+        return {"tflops": nominal, "cublaslt_e4m3_8192_tflops": None,
+                "source": f"{peaks['source']} bf16 burst x 2 (cuBLASLt E4M3 unavailable: {type(e).__name__})"}
+    if meas > nominal:
+        return {"tflops": meas, "cublaslt_e4m3_8192_tflops": meas,
+                "source": "cuBLASLt E4M3 GEMM burst at 8192^3 (torch._scaled_mm), above 2 x the bf16 burst"}
+    return {"tflops": nominal, "cublaslt_e4m3_8192_tflops": meas,
+            "source": f"{peaks['source']} bf16 burst x 2 (nominal FP8:BF16 ratio), above cuBLASLt E4M3 at 8192^3"}
+
+
 def measured_peaks() -> dict:
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -243,7 +269,8 @@ def run_ours(args, world, rank, local):
     w = WL.WORKLOADS[args.workload]
     M, K, N = w.M, w.K, w.N
     peaks = measured_peaks()
-    fp8_peak = 2.0 * peaks["bf16_tflops"]  # dense FP8 = 2 x dense BF16 (nominal ratio)
+    fp8 = fp8_peak(dev)
+    fp8_peak_tflops = fp8["tflops"]
 
     # inputs: seeded host tensors, resident in HBM before timing
     h_bits = [WL.h_preact(w, s) for s in range(2)]
@@ -317,10 +344,10 @@ def run_ours(args, world, rank, local):
                   "traffic": profiled_traffic(f"quant_batch_{args.workload}", quant_src),
                   "algorithmic_bytes": quant_bytes, "peak_source": peaks["source"]}
     roof_gemm = {"bound": "tensor", "kernel": "fp8_gemm_kernel (fp8_gemm_fwd)", "achieved": gemm_tflops,
-                 "peak": fp8_peak, "unit": "TFLOP/s", "frac": gemm_tflops / fp8_peak,
+                 "peak": fp8_peak_tflops, "unit": "TFLOP/s", "frac": gemm_tflops / fp8_peak_tflops,
                  "traffic": profiled_traffic(f"fp8_gemm_{args.workload}", gemm_src),
                  "algorithmic_flops": flops_step,
-                 "peak_source": f"{peaks['source']} bf16 burst x 2 (nominal FP8:BF16 ratio)"}
+                 "peak_source": fp8["source"]}
     dominant = roof_quant if kern_ms["quant"] >= kern_ms["gemm"] else roof_gemm
     roof_fused = None
     if "fused_step_kernel" in kern_ms:
@@ -349,7 +376,7 @@ def run_ours(args, world, rank, local):
 
     extras = {}
     if not args.no_extras:
-        extras = measure_extras(args, dp, H, Wt, flush, kern_ms, w, dev)
+        extras = measure_extras(args, dp, H, Wt, flush, kern_ms, w, dev, fp8_peak_tflops)
 
     e2e = measure_e2e(args, dp, h_bits, w_bits, flush, w, dev, use_graph=graphs is not None)
 
@@ -371,6 +398,7 @@ def run_ours(args, world, rank, local):
         "roofline": dominant,
         "roofline_quant": roof_quant,
         "roofline_gemm": roof_gemm,
+        "fp8_peak": fp8,
         "roofline_fused": roof_fused,
         "cpu_baseline": cpu_baseline(w, h_bits[0], w_bits, args.cpu_rows) if world == 1 else None,
         "e2e": e2e,
@@ -482,7 +510,7 @@ def timed(fn, flush, reps: int) -> float:
     return float(np.mean([a.elapsed_time(b) for a, b in ts]))
 
 
-def measure_extras(args, dp, H, Wt, flush, kern_ms, w, dev) -> dict:
+def measure_extras(args, dp, H, Wt, flush, kern_ms, w, dev, fp8_peak_tflops: float) -> dict:
     """Comparators, timed like kern_ms (back-to-back over 4 rotating copies of
     H): the unfused three-pass quantize (write the activation, an amax pass, a
     cast pass) against the fused quantize of H alone, and cuBLAS BF16 on the
@@ -509,7 +537,19 @@ def measure_extras(args, dp, H, Wt, flush, kern_ms, w, dev) -> dict:
     t_bf16_path = timed_b2b([lambda h=h: (B.fp8q_naive_act(h, B.ACT_RELU2, a_naive),
                                           torch.matmul(a_naive, Wt, out=y16)) for h in Hs], reps)
     del acts, Hs
-    rows = measure_other_rows(dev, max(16, min(64, args.steps)))
+    # the library's FP8 GEMM (cuBLASLt E4M3 x E4M3 -> BF16 via torch._scaled_mm) on the same
+    # operands, over the same 8 rotating copies of X_q as the FP8 GEMM's own timing
+    t_lib_fp8 = None
+    try:
+        xqs = [dp.x_q.clone().view(torch.float8_e4m3fn) for _ in range(8)]
+        wtq = dp.wt_q.view(torch.float8_e4m3fn).t()  # [K,N], column-major
+        s_x, s_w = (1.0 / dp.x.scale).reshape(()), (1.0 / dp.w.scale).reshape(())  # dequantisation factors
+        t_lib_fp8 = timed_b2b([lambda x=x: torch._scaled_mm(x, wtq, scale_a=s_x, scale_b=s_w,
+                                                            out_dtype=torch.bfloat16) for x in xqs], reps)
+        del xqs
+    except (RuntimeError, TypeError, AttributeError):
+        pass
+    rows = measure_other_rows(dev, max(16, min(64, args.steps)), fp8_peak_tflops)
     t_fused = kern_ms["quant_h_only"]
     t_fp8_path = kern_ms["quant"] + kern_ms["gemm"]
     flops = 2.0 * M * N * K
@@ -518,6 +558,9 @@ def measure_extras(args, dp, H, Wt, flush, kern_ms, w, dev) -> dict:
         "fused_vs_naive_speedup": t_naive / t_fused, "fused_vs_naive_ideal": 9.0 / 5.0,
         "bf16_gemm_ms": t_bf16_gemm, "bf16_gemm_tflops": flops / (t_bf16_gemm * 1e-3) / 1e12,
         "fp8_vs_bf16_gemm_speedup": t_bf16_gemm / kern_ms["gemm"],
+        "cublaslt_fp8_gemm_ms": t_lib_fp8,
+        "cublaslt_fp8_gemm_tflops": flops / (t_lib_fp8 * 1e-3) / 1e12 if t_lib_fp8 else None,
+        "fp8_gemm_vs_cublaslt_fp8_speedup": t_lib_fp8 / kern_ms["gemm"] if t_lib_fp8 else None,
         "bf16_path_ms (BF16 activation write + cuBLAS BF16 GEMM)": t_bf16_path,
         "fp8_path_ms (one-launch W + H cast + FP8 GEMM)": t_fp8_path,
         "fp8_vs_bf16_end_to_end_speedup": t_bf16_path / t_fp8_path,
@@ -526,7 +569,7 @@ def measure_extras(args, dp, H, Wt, flush, kern_ms, w, dev) -> dict:
     }
 
 
-def measure_other_rows(dev, reps: int) -> dict:
+def measure_other_rows(dev, reps: int, fp8_tflops: float) -> dict:
     """The path's other rows, each on the workload it belongs to and timed like
     the step's kernels (back-to-back launches captured in one CUDA graph, the
     inputs larger than L2 or rotated over copies that together exceed it):
@@ -536,7 +579,7 @@ def measure_other_rows(dev, reps: int) -> dict:
     fraction of the measured peaks."""
     from quantize_fp8_gemm_gb300 import binding as B
     peaks = measured_peaks()
-    hbm, fp8 = peaks["hbm_gbs"], 2.0 * peaks["bf16_tflops"]
+    hbm, fp8 = peaks["hbm_gbs"], fp8_tflops
     l2_bytes = 256 << 20  # rotate copies until the inputs exceed L2 twice over
 
     def copies(t):
