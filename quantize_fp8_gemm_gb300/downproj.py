@@ -224,6 +224,21 @@ class Fp8DownProj:
             self.x.update()
             self.w.update()
 
+    def check_status(self) -> int:
+        """Read and clear the device status words of the steps since the last
+        check (this synchronises with the device).  Returns their OR: 0, or
+        B.DEV_TIMEOUT (a bounded wait inside a GEMM ran out, so that step's Y is
+        invalid) and/or B.DEV_BAD_AMAX (a history update kept the previous
+        scale).  After a time-out the fused kernel's workspace may hold counts,
+        so it is zeroed again here and the next step starts clean."""
+        st = int(self.gemm_status.item()) | int(self.x.status.item()) | int(self.w.status.item())
+        if st & B.DEV_TIMEOUT and self.workspace is not None:
+            self.workspace.zero_()
+        self.gemm_status.zero_()
+        self.x.status.zero_()
+        self.w.status.zero_()
+        return st
+
     def step(self, H: torch.Tensor, W: torch.Tensor) -> torch.Tensor:
         """One forward step: cast W, fused quantize of H, FP8 GEMM, history updates.
 

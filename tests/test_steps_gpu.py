@@ -152,6 +152,40 @@ def test_graph_replay_matches_eager_steps():
         assert torch.equal(e.x.scale, g.x.scale)
 
 
+def test_check_status_recovers_after_a_timeout():
+    """A one-launch step whose GEMM loads are held back (a test hook) gives up
+    its bounded waits: check_status reports FP8Q_DEV_TIMEOUT and leaves the
+    workspace zero, and the next step equals that of a run that never timed out
+    (the quantize and the history updates of the failed step still ran)."""
+    M, K, N = 4096, 3072, 768
+    w = WL.WORKLOADS["gpt2s"]
+    g = torch.Generator(device="cuda").manual_seed(21)
+    H = [torch.randn(M, K, device="cuda", generator=g).to(torch.bfloat16) for _ in range(3)]
+    W = (torch.randn(K, N, device="cuda", generator=g) * 0.02).to(torch.bfloat16)
+    bad = Fp8DownProj(M, K, N, margin=w.margin, fused=True)
+    good = Fp8DownProj(M, K, N, margin=w.margin, fused=True)
+    for dp in (bad, good):
+        dp.calibrate(H[0], W)
+        dp.step(H[0], W)
+    assert good.check_status() == 0 and bad.check_status() == 0
+    B.fp8q_gemm_test_hold_loads(True)
+    try:
+        bad.step(H[1], W)
+        torch.cuda.synchronize()
+    finally:
+        B.fp8q_gemm_test_hold_loads(False)
+    good.step(H[1], W)
+    assert bad.check_status() & B.DEV_TIMEOUT
+    assert good.check_status() == 0
+    assert int(bad.workspace.count_nonzero().item()) == 0
+    assert torch.equal(bad.x.scale, good.x.scale) and torch.equal(bad.w.scale, good.w.scale)
+    yb = bad.step(H[2], W).clone()
+    yg = good.step(H[2], W).clone()
+    torch.cuda.synchronize()
+    assert bad.check_status() == 0
+    assert torch.equal(yb.view(torch.int16), yg.view(torch.int16))
+
+
 def test_bad_amax_keeps_scale_and_flags():
     hist = torch.zeros(1, device="cuda")
     head = torch.zeros(1, dtype=torch.int32, device="cuda")
