@@ -573,8 +573,9 @@ def measure_other_rows(dev, reps: int, fp8_tflops: float) -> dict:
     """The path's other rows, each on the workload it belongs to and timed like
     the step's kernels (back-to-back launches captured in one CUDA graph, the
     inputs larger than L2 or rotated over copies that together exceed it):
-    the weight cast in both layouts, the E5M2 gradient cast and the dgrad GEMM
-    dX = dY W^T on the GPT-2-XL shapes, the 1x128 group quantize and the
+    the weight cast in both layouts, the E5M2 gradient cast (row-major and
+    transposed), the dgrad GEMM dX = dY W^T and the weight-gradient GEMM
+    dW = X^T dY on the GPT-2-XL shapes, the 1x128 group quantize and the
     group-scaled GEMM on the outlier shapes.  Each row carries its roofline
     fraction of the measured peaks."""
     from quantize_fp8_gemm_gb300 import binding as B
@@ -615,11 +616,23 @@ def measure_other_rows(dev, reps: int, fp8_tflops: float) -> dict:
     t = timed_b2b([lambda: B.fp8_quant_fused_ex(dY, B.ACT_IDENTITY, B.E5M2, sdy, q_out=dyq, amax_out=amax,
                                                 flags=B.ACCUMULATE)], max(4, reps // 4))
     out["a10 dY cast E5M2"] = mem_row(t, 3.0 * M * N, f"dY [{M},{N}]")
+    # the weight gradient's operand: dY's transposed E5M2 copy (token-contiguous)
+    dyqt = torch.empty(N, M, dtype=torch.uint8, device=dev)
+    t = timed_b2b([lambda: B.fp8_quant_fused_ex(dY, B.ACT_IDENTITY, B.E5M2, sdy, q_t_out=dyqt, amax_out=amax,
+                                                flags=B.ACCUMULATE)], max(4, reps // 4))
+    out["next: dY cast E5M2, transposed copy"] = mem_row(t, 3.0 * M * N, f"dY [{M},{N}] -> dY_q^T [{N},{M}]")
     del dY, W
     dx = torch.empty(M, K, dtype=torch.bfloat16, device=dev)
     t = timed_b2b([lambda: B.fp8_gemm_dgrad(dyq, w_q, sdy, one, dx)], max(4, reps // 8))
     out["a11 dgrad GEMM"] = mma_row(t, 2.0 * M * N * K, f"dY_q [{M},{N}] x W_q [{K},{N}]^T")
     del dx, dyq, w_q, wt_q
+    # wgrad dW = X^T dY: X_q^T [K,M] (E4M3 codes; the GEMM's time does not depend on their values)
+    g = torch.Generator(device=dev).manual_seed(xl.seed)
+    xqt = torch.randint(0, 120, (K, M), dtype=torch.uint8, device=dev, generator=g)
+    dw = torch.empty(K, N, dtype=torch.bfloat16, device=dev)
+    t = timed_b2b([lambda: B.fp8_gemm_wgrad(xqt, dyqt, one, sdy, dw)], max(4, reps // 8))
+    out["next: wgrad GEMM"] = mma_row(t, 2.0 * M * N * K, f"X_q^T [{K},{M}] x dY_q^T [{N},{M}]^T")
+    del xqt, dyqt, dw
     ol = WL.WORKLOADS["outlier"]
     M, K, N = ol.M, ol.K, ol.N
     H = WL.bf16_tensor(WL.h_preact(ol)).to(dev)

@@ -9,6 +9,7 @@
  *      (fp8_downproj_fwd    1 and 2 fused in one kernel)
  *   3. amax_history_update  push this step's amax; scale for the next step
  *   (fp8_gemm_dgrad         dX = dY_q W_q^T / (s_dy s_w), the gradient shape)
+ *   (fp8_gemm_wgrad         dW = X_q^T dY_q / (s_x s_dy), the weight gradient)
  *
  * Conventions shared by every call:
  *  - All tensor pointers are DEVICE pointers to caller-owned memory; the
@@ -236,6 +237,27 @@ int fp8_gemm_fwd(const void* x_q, const void* wt_q,
 int fp8_gemm_dgrad(const void* dy_q, const void* w_q,
                    const float* scale_dy, const float* scale_w,
                    void* dx, int64_t M, int64_t N, int64_t K,
+                   int* status, cudaStream_t stream);
+
+/*
+ * fp8_gemm_wgrad -- dW = (X_q^T . dY_q) / (s_x s_dy), FP32 accumulation, BF16 out  [gemms]
+ *
+ * The weight gradient of the same layer ("FP8 Training & Inference", FP8
+ * Training Recipe: the weight-gradient GEMM takes the E4M3 activation and the
+ * E5M2 output gradient).  Both operands are contracted over the M tokens, so
+ * both come as their transposed, token-contiguous copies: q_t_out of
+ * fp8_quant_fused run on H (the activation) and on dY.
+ *   x_q_t   device [K,M] E4M3: the activation's transposed copy.
+ *   dy_q_t  device [N,M] E5M2: the output gradient's transposed copy.
+ *   scale_x, scale_dy  device, 1 float each.
+ *   dw      device [K,N] BF16:  dw[k,n] = BF16( (sum_m x[m,k] dy[m,n]) / (s_x s_dy) ).
+ *   M, N, K M >= 16, M % 16 == 0 (the contraction); N >= 16, N % 16 == 0;
+ *           K >= 0 (K == 0: nothing is enqueued).
+ *   status  as for fp8_gemm_fwd.
+ */
+int fp8_gemm_wgrad(const void* x_q_t, const void* dy_q_t,
+                   const float* scale_x, const float* scale_dy,
+                   void* dw, int64_t M, int64_t N, int64_t K,
                    int* status, cudaStream_t stream);
 
 /*

@@ -215,5 +215,20 @@ def gemm_dgrad(dy_q, w_q, s_dy: float, s_w: float, *, rows=None, fmt_dy=E5M2, fm
     return dX, S
 
 
+def gemm_wgrad(x_q, dy_q, s_x: float, s_dy: float, *, rows=None, fmt_x=E4M3, fmt_dy=E5M2,
+               nthreads=None):
+    """dW = X^T x dY over dequantised FP8 ("FP8 Training & Inference", FP8
+    Training Recipe: the weight gradient of the E4M3 activation and the E5M2
+    output gradient); X [M,K], dY [M,N] in their own layouts, contracted over
+    the M tokens.  rows: the rows k of dW to compute.  Returns (dW, S): S is
+    sum_m |x[m,k] dy[m,n]| / (s_x s_dy)."""
+    X = _c(x_q, np.uint8)
+    D = _c(dy_q, np.uint8)
+    assert X.shape[0] == D.shape[0]
+    # dW[k, n] = sum_m X^T[k, m] dY[m, n]: the plain GEMM with X^T as its first operand
+    return gemm_fwd(np.ascontiguousarray(X.T), D, s_x, s_dy, rows=rows, fmt_x=fmt_x, fmt_w=fmt_dy,
+                    nthreads=nthreads)
+
+
 def openmp_threads() -> int:
     return lib().oref_openmp_max_threads()

@@ -52,6 +52,7 @@ def lib() -> ctypes.CDLL:
         L.fp8_quant_fused_batch.argtypes = [P, i32, P]
         L.fp8_cast_f32.argtypes = [P, P, i64, i32, P]
         L.fp8_gemm_dgrad.argtypes = [P, P, P, P, P, i64, i64, i64, P, P]
+        L.fp8_gemm_wgrad.argtypes = [P, P, P, P, P, i64, i64, i64, P, P]
         L.amax_history_update.argtypes = [P, i32, P, P, f32, i32, P, P, P]
         L.amax_history_update_ex.argtypes = [P, i32, P, P, f32, i32, P, P, P, P, P, P]
         L.fp8_downproj_workspace_bytes.argtypes = [i64]
@@ -71,7 +72,7 @@ def lib() -> ctypes.CDLL:
         L.fp8q_gemm_set_tile.argtypes = [i32, i32]
         L.fp8q_gemm_set_tile.restype = i32
         for fn in ("fp8_quant_fused", "fp8_quant_fused_ex", "fp8_quant_fused_batch", "fp8_downproj_fwd",
-                   "fp8_downproj_fwd_noalloc", "fp8_downproj_fwd_ex", "fp8_gemm_fwd", "fp8_gemm_dgrad", "amax_history_update",
+                   "fp8_downproj_fwd_noalloc", "fp8_downproj_fwd_ex", "fp8_gemm_fwd", "fp8_gemm_dgrad", "fp8_gemm_wgrad", "amax_history_update",
                    "amax_history_update_ex", "fp8q_naive_act", "fp8q_naive_amax", "fp8q_naive_cast"):
             getattr(L, fn).restype = i32
         _lib = L
@@ -198,6 +199,20 @@ def fp8_gemm_dgrad(dy_q: torch.Tensor, w_q: torch.Tensor, scale_dy: torch.Tensor
         _ptr(scale_w, 4, "scale_w"), _ptr(dx, 2 * M * K, "dx"), M, N, K,
         _ptr(status, 4, "status"), _stream(stream))
     _check("fp8_gemm_dgrad", st)
+
+
+def fp8_gemm_wgrad(x_q_t: torch.Tensor, dy_q_t: torch.Tensor, scale_x: torch.Tensor, scale_dy: torch.Tensor,
+                   dw: torch.Tensor, *, status=None, stream=None) -> None:
+    """dw[K,N] = BF16((x_q_t[K,M] . dy_q_t[N,M]^T) / (s_x s_dy)): the weight gradient X^T dY."""
+    K, M = x_q_t.shape
+    N = dy_q_t.shape[0]
+    if dy_q_t.shape[1] != M:
+        raise ValueError("x_q_t [K,M] and dy_q_t [N,M] disagree on M")
+    st = lib().fp8_gemm_wgrad(
+        _ptr(x_q_t, K * M, "x_q_t"), _ptr(dy_q_t, N * M, "dy_q_t"), _ptr(scale_x, 4, "scale_x"),
+        _ptr(scale_dy, 4, "scale_dy"), _ptr(dw, 2 * K * N, "dw"), M, N, K,
+        _ptr(status, 4, "status"), _stream(stream))
+    _check("fp8_gemm_wgrad", st)
 
 
 def fp8_downproj_workspace_bytes(M: int) -> int:

@@ -991,6 +991,16 @@ extern "C" int fp8_gemm_dgrad(const void* dy_q, const void* w_q, const float* sc
     return gemm_dispatch(dy_q, w_q, scale_dy, scale_w, 0, dx, M, K, N, FP8Q_E5M2, FP8Q_E4M3, status, stream);
 }
 
+extern "C" int fp8_gemm_wgrad(const void* x_q_t, const void* dy_q_t, const float* scale_x,
+                              const float* scale_dy, void* dw, int64_t M, int64_t N, int64_t K, int* status,
+                              cudaStream_t stream) {
+    // D = dW [K,N], A = X_q^T [K,M], B = dY_q^T [N,M] (contraction M)
+    int st = check_gemm_args(x_q_t, dy_q_t, scale_x, scale_dy, dw, K, N, M, status);
+    if (st != FP8Q_OK) return st;
+    if (K == 0) return FP8Q_OK;
+    return gemm_dispatch(x_q_t, dy_q_t, scale_x, scale_dy, 0, dw, K, N, M, FP8Q_E4M3, FP8Q_E5M2, status, stream);
+}
+
 extern "C" size_t fp8_downproj_workspace_bytes(int64_t M) {
     if (M <= 0) return 0;
     const size_t blocks = static_cast<size_t>((M + BM - 1) / BM);

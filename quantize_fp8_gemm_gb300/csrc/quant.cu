@@ -151,22 +151,34 @@ quant_stream_kernel(const uint4* __restrict__ h, int64_t nchunks, const float* _
 constexpr int kTile = 128;
 constexpr int kTqPitch = kTile;  // bytes per row of the FP8 tile in shared memory
 
-// Write the tile's FP8 codes (tq: kTile rows of kTile bytes in shared memory,
-// complete) transposed into q_t [K,M]: output row k = col0 + j holds tile
-// column j.  Warp w owns tile rows 16w..16w+15 and lane l tile columns
-// 4l..4l+3: each of the warp's sixteen 32-bit reads is one whole tile row
-// (every bank once), and a 4x4 byte transpose in registers (byte_perm) turns
-// the lane's 16 x 4 bytes into four 16-byte pieces, rows 16w..16w+15 of its
-// four output rows.  M % 16 == 0, so a piece is inside q_t whenever its first
-// row is.
+// Byte offset of the 8-byte piece j (columns 8j..8j+7) of tile row r in the
+// shared-memory FP8 tile: the 4-byte words of row r are permuted by
+// XOR-ing their index with 4 * ((r / 16) % 8), so that the column-wise reads
+// of store_transposed hit every bank once; an 8-byte piece stays whole.
+__device__ __forceinline__ int tq_offset(int r, int j) {
+    return r * kTqPitch + ((j * 8) ^ (((r >> 4) & 7) << 4));
+}
+
+// Write the tile's FP8 codes (tq: complete, laid out by tq_offset) transposed
+// into q_t [K,M]: output row k = col0 + j holds tile column j.  Thread t takes
+// the 16 tile rows 16p..16p+15 (p = t % 8) of the four tile columns
+// 4q..4q+3 (q = t / 8): sixteen 32-bit reads (one per row; a warp's 32 reads
+// of a row fall in 32 different banks), a 4x4 byte transpose in registers
+// (byte_perm), and four 16-byte stores, one per output row.  The eight threads
+// with the same q write the 128 contiguous bytes m = row0 .. row0 + 127 of
+// each of their output rows, so a warp's store covers four whole lines.
+// M % 16 == 0, so a piece is inside q_t whenever its first row is.
 __device__ __forceinline__ void store_transposed(const uint8_t* tq, uint8_t* __restrict__ q_t_out, int64_t M,
                                                  int64_t K, int64_t row0, int64_t col0) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    static_assert(kThreads / 32 * 16 == kTile && 32 * 4 == kTile, "8 warps x 16 rows, 32 lanes x 4 columns");
+    static_assert(kThreads == 256 && kTile == 128, "256 threads: 8 row groups x 32 column groups");
+    const int p = threadIdx.x & 7, q = threadIdx.x >> 3;
     uint32_t x[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) x[i] = *reinterpret_cast<const uint32_t*>(tq + (warp * 16 + i) * kTqPitch + lane * 4);
-    const int64_t mcol = row0 + warp * 16;
+    for (int i = 0; i < 16; ++i) {
+        const int r = p * 16 + i;
+        x[i] = *reinterpret_cast<const uint32_t*>(tq + r * kTqPitch + ((q ^ (p << 2)) << 2));
+    }
+    const int64_t mcol = row0 + p * 16;
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
         // byte c of the first word -> byte 0, byte c of the second -> byte 1
@@ -178,7 +190,7 @@ __device__ __forceinline__ void store_transposed(const uint8_t* tq, uint8_t* __r
             const uint32_t hi = __byte_perm(x[4 * j + 2], x[4 * j + 3], sel);
             o[j] = __byte_perm(lo, hi, 0x5410);  // lo bytes 0,1 then hi bytes 0,1
         }
-        const int64_t krow = col0 + lane * 4 + c;
+        const int64_t krow = col0 + q * 4 + c;
         if (krow < K && mcol < M) st_v4(q_t_out + krow * M + mcol, make_uint4(o[0], o[1], o[2], o[3]));
     }
 }
@@ -255,7 +267,7 @@ __device__ __forceinline__ void tile_body(const uint16_t* __restrict__ h, int64_
             nsat += ns;
             if (q_out) st_v2(q_out + row * K + col, q);
         }
-        if (q_t_out) *reinterpret_cast<uint2*>(tq + r * kTqPitch + (c & 15) * 8) = q;
+        if (q_t_out) *reinterpret_cast<uint2*>(tq + tq_offset(r, c & 15)) = q;
     }
 
     if (q_t_out) {
@@ -347,7 +359,7 @@ __device__ __forceinline__ void tile_pt_body(const uint16_t* __restrict__ h, int
                 if (act_out) st_stream_v4(act_out + row * K + col, a[it]);
                 if (q_out) st_v2(q_out + row * K + col, q);
             }
-            if (q_t_out) *reinterpret_cast<uint2*>(tq + r * kTqPitch + (c & 15) * 8) = q;
+            if (q_t_out) *reinterpret_cast<uint2*>(tq + tq_offset(r, c & 15)) = q;
         }
     }
     if (q_t_out) {

@@ -102,6 +102,15 @@ def test_gemm_argument_checks(lib):
     assert dg(A, A, A, A, A, 128, 24, 256, None, None) == ERR_SHAPE      # contraction N % 16
     assert dg(A, A, A, A, None, 128, 32, 256, None, None) == ERR_NULL
     assert dg(A, A, A, A, A, 128, 32, 256, None, None) == ERR_UNSUPPORTED
+    wg = lib.fp8_gemm_wgrad
+    wg.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_int64] * 3 + [ctypes.c_void_p] * 2
+    wg.restype = ctypes.c_int
+    assert wg(A, A, A, A, A, 1000, 64, 256, None, None) == ERR_SHAPE     # contraction M % 16
+    assert wg(A, A, A, A, A, 0, 64, 256, None, None) == ERR_SHAPE        # contraction M >= 16
+    assert wg(A, A, A, A, A, 1024, 40, 256, None, None) == ERR_SHAPE     # N % 16
+    assert wg(A, None, A, A, A, 1024, 64, 256, None, None) == ERR_NULL
+    assert wg(A, A, A, A, A + 2, 1024, 64, 256, None, None) == ERR_ALIGN
+    assert wg(A, A, A, A, A, 1024, 64, 256, None, None) == ERR_UNSUPPORTED
 
 
 def test_history_argument_checks(lib):

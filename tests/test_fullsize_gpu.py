@@ -67,9 +67,10 @@ def test_outlier_forward_per_tensor_and_group():
     assert zg < zt
 
 
-def test_gpt2xl_forward_and_dgrad():
+def test_gpt2xl_forward_dgrad_and_wgrad():
     """GPT-2-XL shape: H [131072, 6400] -> Y [131072, 1600]; dY [131072, 1600]
-    in E5M2 -> dX = dY W^T [131072, 6400]."""
+    in E5M2 -> dX = dY W^T [131072, 6400]; the transposed casts of the
+    activation and of dY -> dW = X^T dY [6400, 1600]."""
     w = WL.WORKLOADS["gpt2xl"]
     h_bits, w_bits = WL.h_preact(w, 0), WL.w_down(w)
     H, Wd = WL.bf16_tensor(h_bits).cuda(), WL.bf16_tensor(w_bits).cuda()
@@ -78,7 +79,6 @@ def test_gpt2xl_forward_and_dgrad():
     sx, sw = float(dp.x.scale.item()), float(dp.w.scale.item())
     y = dp.step(H, Wd)
     torch.cuda.synchronize()
-    del H
     rows = WL.sample_rows(w.M, 128, seed=4)
     rx = O.quant(h_bits, O.ACT_RELU2, O.E4M3, sx, want_act=False)
     rw = O.quant(w_bits, O.ACT_IDENTITY, O.E4M3, sw, want_act=False, want_qt=True)
@@ -87,7 +87,13 @@ def test_gpt2xl_forward_and_dgrad():
     assert np.array_equal(host_u8(dp.w_q), rw["q"])
     Yr, S = O.gemm_fwd(rx["q"], rw["q"], sx, sw, rows=rows)
     assert_gemm_close(y, Yr, S, rows=rows)
-    del rx, y
+    del y
+    # the activation's transposed E4M3 copy (the weight gradient's operand), same scale
+    xqt = torch.empty(w.K, w.M, dtype=torch.uint8, device="cuda")
+    B.fp8_quant_fused(H, B.ACT_RELU2, B.E4M3, dev_f32(sx), q_t_out=xqt, amax_out=torch.zeros(1, device="cuda"))
+    torch.cuda.synchronize()
+    del H
+    assert np.array_equal(host_u8(xqt), rx["q"].T)
 
     dy_bits = WL.dy_grad(w)
     s_dy = O.delayed_scale(O.amax(dy_bits, O.ACT_IDENTITY), w.margin, O.E5M2)
@@ -105,3 +111,15 @@ def test_gpt2xl_forward_and_dgrad():
     assert st.item() == 0
     Dr, Sd = O.gemm_dgrad(rdy["q"], rw["q"], s_dy, sw, rows=rows)
     assert_gemm_close(dx, Dr, Sd, rows=rows)
+    del dx
+
+    dyqt = torch.empty(w.N, w.M, dtype=torch.uint8, device="cuda")
+    B.fp8_quant_fused(dY, B.ACT_IDENTITY, B.E5M2, dev_f32(s_dy), q_t_out=dyqt, amax_out=amax)
+    dw = torch.empty(w.K, w.N, dtype=torch.bfloat16, device="cuda")
+    B.fp8_gemm_wgrad(xqt, dyqt, dev_f32(sx), dev_f32(s_dy), dw, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert np.array_equal(host_u8(dyqt), rdy["q"].T)
+    krows = WL.sample_rows(w.K, 48, seed=5)
+    Wr, Sw = O.gemm_wgrad(rx["q"], rdy["q"], sx, s_dy, rows=krows)
+    assert_gemm_close(dw, Wr, Sw, rows=krows)

@@ -86,6 +86,43 @@ def test_fwd_shapes(M, N, K):
     assert_gemm_close(y, Yr, S)
 
 
+def run_wgrad(xq, dyq, sx, sdy):
+    """xq [M,K] E4M3, dyq [M,N] E5M2 (their own layouts); the GPU gets the
+    transposed copies X_q^T [K,M] and dY_q^T [N,M]."""
+    M, K = xq.shape
+    N = dyq.shape[1]
+    dw = torch.empty(K, N, dtype=torch.bfloat16, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.fp8_gemm_wgrad(dev_u8(np.ascontiguousarray(xq.T)), dev_u8(np.ascontiguousarray(dyq.T)), dev_f32(sx),
+                     dev_f32(sdy), dw, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    return dw
+
+
+@pytest.mark.parametrize("M,N,K", [(16, 16, 1), (272, 144, 129), (1008, 1600, 640), (4096, 768, 300),
+                                   (6400, 160, 256)])
+def test_wgrad_shapes(M, N, K):
+    """dW = X^T dY (E4M3 x E5M2, contraction over the M tokens) against the oracle."""
+    rng = np.random.default_rng(3 * M + N + K)
+    xq = rand_e4m3((M, K), seed=M + K, scale=30.0)
+    dyq = _codes(rng.standard_normal((M, N)) * 1000.0, O.E5M2)
+    sx, sdy = 3.5, 2.0 ** 10
+    Wr, S = O.gemm_wgrad(xq, dyq, sx, sdy)
+    assert_gemm_close(run_wgrad(xq, dyq, sx, sdy), Wr, S)
+
+
+def test_wgrad_small_integers_exact():
+    """Integer-valued operands: the FP32 sums are exact, so dW is BF16(exact) bit for bit."""
+    rng = np.random.default_rng(9)
+    M, N, K = 512, 48, 40
+    xi = rng.integers(-8, 9, (M, K))
+    di = rng.integers(-6, 7, (M, N))
+    dw = run_wgrad(_codes(xi, O.E4M3), _codes(di, O.E5M2), 1.0, 1.0)
+    exact = torch.from_numpy((xi.T @ di).astype(np.float32)).to(torch.bfloat16)
+    assert torch.equal(dw.cpu().view(torch.int16), exact.view(torch.int16))
+
+
 @pytest.mark.parametrize("M,N,K", [(130, 160, 272), (64, 1600, 512), (300, 256, 6400)])
 def test_dgrad_shapes(M, N, K):
     rng = np.random.default_rng(M + N + K)
@@ -155,7 +192,7 @@ TILES = [(0, 128), (0, 160), (0, 192), (0, 256), (1, 128), (1, 160), (1, 192), (
 @pytest.mark.parametrize("pair,bn", TILES)
 def test_every_tile_shape_on_ragged_problems(pair, bn):
     """Each tile shape (1-CTA and 2-SM pair, every width) on problems whose M, N
-    and K all leave partial tiles, forward and dgrad."""
+    and K all leave partial tiles: forward, dgrad and wgrad."""
     try:
         B.fp8q_gemm_set_tile(pair, bn)
         for M, N, K in [(1000, 1600, 640), (300, 272, 400), (129, 144, 1600), (513, 96, 48)]:
@@ -172,6 +209,10 @@ def test_every_tile_shape_on_ragged_problems(pair, bn):
         B.fp8_gemm_dgrad(dev_u8(dyq), dev_u8(wq), dev_f32(1024.0), dev_f32(5.0), dx)
         torch.cuda.synchronize()
         assert_gemm_close(dx, Dr, Sd)
+        xq = rand_e4m3((400, 300), seed=bn + 1, scale=30.0)
+        dyq2 = _codes(rng.standard_normal((400, 144)) * 1000.0, O.E5M2)
+        Wr, Sw = O.gemm_wgrad(xq, dyq2, 3.0, 1024.0)
+        assert_gemm_close(run_wgrad(xq, dyq2, 3.0, 1024.0), Wr, Sw)
     finally:
         B.fp8q_gemm_set_tile(-1)
 

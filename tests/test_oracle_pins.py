@@ -425,6 +425,27 @@ def test_gemm_dgrad_is_dy_times_w_transposed():
     assert np.allclose(dX, Yf, rtol=1e-13, atol=1e-13)
 
 
+def test_gemm_wgrad_is_x_transposed_times_dy():
+    """dW = X^T dY: exact on small integers (exactly representable in E4M3 and
+    E5M2, so the sums are exact) against numpy's integer matmul, numpy's matmul
+    of the decoded operands otherwise, and row selection."""
+    rng = np.random.default_rng(24)
+    M, K, N = 40, 24, 33
+    Xi = rng.integers(-8, 9, (M, K))
+    Di = rng.integers(-6, 7, (M, N))
+    dW, S = O.gemm_wgrad(_codes(Xi, O.E4M3), _codes(Di, O.E5M2), 1.0, 1.0)
+    assert np.array_equal(dW, (Xi.T @ Di).astype(np.float64))
+    assert np.array_equal(S, (np.abs(Xi).T @ np.abs(Di)).astype(np.float64))
+    X = _codes(rng.standard_normal((M, K)) * 50, O.E4M3)
+    D = _codes(rng.standard_normal((M, N)) * 1e3, O.E5M2)
+    dW, _ = O.gemm_wgrad(X, D, 4.0, 0.5)
+    ref = O.fp8_decode(X, O.E4M3).T @ O.fp8_decode(D, O.E5M2) / 2.0
+    assert np.allclose(dW, ref, rtol=1e-12, atol=1e-12)
+    rows = np.array([5, 0, 23], np.int64)
+    dWr, _ = O.gemm_wgrad(X, D, 4.0, 0.5, rows=rows)
+    assert np.array_equal(dWr, dW[rows])
+
+
 def test_group_gemm_reductions():
     """Group mode: equal scales reduce to per-tensor; power-of-two scales that
     differ per row, per 128-slice of K and per 128-block of N reduce to numpy's
