@@ -655,6 +655,37 @@ def measure_other_rows(dev, reps: int, fp8_tflops: float) -> dict:
     t = timed_b2b([lambda x=x: B.fp8_gemm_fwd(x, wt_q, gsx, gsw, y, group_mode=1) for x in xqs], reps)
     out["a12 group-scaled GEMM"] = mma_row(t, 2.0 * M * N * K, f"X_q [{M},{K}] x W_q^T [{N},{K}]")
     del xqs, xq, W, wt_q, y
+    # next: the up-projection H = X_in W_up with the activation quantize in its epilogue, against
+    # the same outputs from the unfused pair (the GEMM writing H, then the quantize of H); operands
+    # are E4M3 codes (the GEMM's time does not depend on their values)
+    for wl_name in ("gpt2s", "gpt2xl"):
+        wl = WL.WORKLOADS[wl_name]
+        Mu, Du, Fu = wl.M, wl.N, wl.K  # tokens, model width (the up-projection's K), hidden width
+        g = torch.Generator(device=dev).manual_seed(wl.seed)
+        xs = copies(torch.randint(0, 120, (Mu, Du), dtype=torch.uint8, device=dev, generator=g))
+        wu = torch.randint(0, 100, (Fu, Du), dtype=torch.uint8, device=dev, generator=g)
+        sx_u, sw_u = torch.full((1,), 16.0, device=dev), torch.full((1,), 448.0, device=dev)
+        s_h = torch.full((1,), 100.0, device=dev)
+        act_u = torch.empty(Mu, Fu, dtype=torch.bfloat16, device=dev)
+        q_u = torch.empty(Mu, Fu, dtype=torch.uint8, device=dev)
+        sat_u = torch.zeros(1, dtype=torch.int64, device=dev)
+        r = max(4, reps // (1 if wl_name == "gpt2s" else 8))
+        t = timed_b2b([lambda x=x: B.fp8_upproj_fwd(x, wu, sx_u, sw_u, s_h, q_u, act=B.ACT_RELU2, act_out=act_u,
+                                                    amax_out=amax, sat_count=sat_u, flags=B.ACCUMULATE)
+                       for x in xs], r)
+        nbytes = Mu * Du + Fu * Du + 3.0 * Mu * Fu  # X, W in; activation (BF16) + E4M3 out
+        row = mem_row(t, nbytes, f"X [{Mu},{Du}] x W_up^T [{Fu},{Du}] -> act + E4M3 [{Mu},{Fu}]")
+        row["TFLOP/s"] = 2.0 * Mu * Du * Fu / (t * 1e-3) / 1e12
+        row["tensor_frac"] = row["TFLOP/s"] / fp8
+        h_u = torch.empty(Mu, Fu, dtype=torch.bfloat16, device=dev)
+        t2 = timed_b2b([lambda x=x: (B.fp8_gemm_fwd(x, wu, sx_u, sw_u, h_u),
+                                     B.fp8_quant_fused_ex(h_u, B.ACT_RELU2, B.E4M3, s_h, act_out=act_u, q_out=q_u,
+                                                          amax_out=amax, sat_count=sat_u, flags=B.ACCUMULATE))
+                        for x in xs], r)
+        row["unfused_ms (GEMM writing H, then the quantize of H)"] = t2
+        row["speedup_vs_unfused"] = t2 / t
+        out[f"next: up-projection + activation quantize epilogue ({wl_name})"] = row
+        del xs, wu, act_u, q_u, h_u
     torch.cuda.empty_cache()
     return out
 

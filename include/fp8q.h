@@ -10,6 +10,7 @@
  *   3. amax_history_update  push this step's amax; scale for the next step
  *   (fp8_gemm_dgrad         dX = dY_q W_q^T / (s_dy s_w), the gradient shape)
  *   (fp8_gemm_wgrad         dW = X_q^T dY_q / (s_x s_dy), the weight gradient)
+ *   (fp8_upproj_fwd         the preceding up-projection with 1 in its epilogue)
  *
  * Conventions shared by every call:
  *  - All tensor pointers are DEVICE pointers to caller-owned memory; the
@@ -259,6 +260,35 @@ int fp8_gemm_wgrad(const void* x_q_t, const void* dy_q_t,
                    const float* scale_x, const float* scale_dy,
                    void* dw, int64_t M, int64_t N, int64_t K,
                    int* status, cudaStream_t stream);
+
+/*
+ * fp8_upproj_fwd -- the up-projection GEMM with the activation quantize in its epilogue  [fused][gemms]
+ *
+ * "Paradigma Details FP8 and Optimizer Tricks Behind NanoGPT Records", second
+ * paragraph: the activation and the cast run while the preceding computation
+ * still holds its output in registers.  Here that computation is the FP8
+ * up-projection H = X_q . W_q / (s_x s_w) itself, so H reaches HBM only if
+ * asked for.  Per element of the [M,N] output:
+ *   h = BF16(acc / (s_x s_w));  a = act(h) (float32);  a_bf = BF16(a);
+ *   h_q = E4M3(float32(a_bf * s_h)) (round to nearest even, saturating);
+ *   amax = max |a_bf|;  sat_count += (|a_bf * s_h| > 448)
+ * -- fp8_quant_fused applied to the GEMM's BF16 output, without storing it.
+ *   x_q, wt_q, scale_x, scale_w   as for fp8_gemm_fwd (per-tensor scales).
+ *   act      FP8Q_ACT_IDENTITY, FP8Q_ACT_RELU or FP8Q_ACT_RELU2.
+ *   scale_h  device, 1 float: s_h, the activation's (delayed) scale.
+ *   h_out    device [M,N] BF16 or NULL: H itself.
+ *   act_out  device [M,N] BF16 or NULL: the activation copy kept for backward.
+ *   h_q      device [M,N] E4M3 (required): the next GEMM's operand.
+ *   amax_out, sat_count  device float / uint64 or NULL; zeroed by the call
+ *            (stream-ordered) unless flags has FP8Q_ACCUMULATE.
+ *   M, N, K  as for fp8_gemm_fwd; the E4M3 rows are N bytes (N % 16 == 0).
+ *   flags    0 or FP8Q_ACCUMULATE.
+ *   status   as for fp8_gemm_fwd.
+ */
+int fp8_upproj_fwd(const void* x_q, const void* wt_q, const float* scale_x, const float* scale_w,
+                   int act, const float* scale_h, void* h_out, void* act_out, void* h_q,
+                   float* amax_out, unsigned long long* sat_count, int64_t M, int64_t N, int64_t K,
+                   unsigned flags, int* status, cudaStream_t stream);
 
 /*
  * fp8_downproj_fwd -- the fused quantize + forward GEMM in one kernel  [fused][gemms]

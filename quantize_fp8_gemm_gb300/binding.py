@@ -53,6 +53,7 @@ def lib() -> ctypes.CDLL:
         L.fp8_cast_f32.argtypes = [P, P, i64, i32, P]
         L.fp8_gemm_dgrad.argtypes = [P, P, P, P, P, i64, i64, i64, P, P]
         L.fp8_gemm_wgrad.argtypes = [P, P, P, P, P, i64, i64, i64, P, P]
+        L.fp8_upproj_fwd.argtypes = [P, P, P, P, i32, P, P, P, P, P, P, i64, i64, i64, ctypes.c_uint, P, P]
         L.amax_history_update.argtypes = [P, i32, P, P, f32, i32, P, P, P]
         L.amax_history_update_ex.argtypes = [P, i32, P, P, f32, i32, P, P, P, P, P, P]
         L.fp8_downproj_workspace_bytes.argtypes = [i64]
@@ -72,7 +73,7 @@ def lib() -> ctypes.CDLL:
         L.fp8q_gemm_set_tile.argtypes = [i32, i32]
         L.fp8q_gemm_set_tile.restype = i32
         for fn in ("fp8_quant_fused", "fp8_quant_fused_ex", "fp8_quant_fused_batch", "fp8_downproj_fwd",
-                   "fp8_downproj_fwd_noalloc", "fp8_downproj_fwd_ex", "fp8_gemm_fwd", "fp8_gemm_dgrad", "fp8_gemm_wgrad", "amax_history_update",
+                   "fp8_downproj_fwd_noalloc", "fp8_downproj_fwd_ex", "fp8_gemm_fwd", "fp8_gemm_dgrad", "fp8_gemm_wgrad", "fp8_upproj_fwd", "amax_history_update",
                    "amax_history_update_ex", "fp8q_naive_act", "fp8q_naive_amax", "fp8q_naive_cast"):
             getattr(L, fn).restype = i32
         _lib = L
@@ -213,6 +214,23 @@ def fp8_gemm_wgrad(x_q_t: torch.Tensor, dy_q_t: torch.Tensor, scale_x: torch.Ten
         _ptr(scale_dy, 4, "scale_dy"), _ptr(dw, 2 * K * N, "dw"), M, N, K,
         _ptr(status, 4, "status"), _stream(stream))
     _check("fp8_gemm_wgrad", st)
+
+
+def fp8_upproj_fwd(x_q: torch.Tensor, wt_q: torch.Tensor, scale_x: torch.Tensor, scale_w: torch.Tensor,
+                   scale_h: torch.Tensor, h_q: torch.Tensor, *, act: int = ACT_RELU2, h_out=None, act_out=None,
+                   amax_out=None, sat_count=None, flags: int = 0, status=None, stream=None) -> None:
+    """Up-projection H = x_q[M,K] . wt_q[N,K]^T / (s_x s_w) with the activation quantize in its
+    epilogue: h_q[M,N] = E4M3(BF16(act(BF16(H))) * s_h), and optionally H, the activation, amax, saturations."""
+    M, K = x_q.shape
+    N = wt_q.shape[0]
+    if wt_q.shape[1] != K:
+        raise ValueError("x_q [M,K] and wt_q [N,K] disagree on K")
+    st = lib().fp8_upproj_fwd(
+        _ptr(x_q, M * K, "x_q"), _ptr(wt_q, N * K, "wt_q"), _ptr(scale_x, 4, "scale_x"), _ptr(scale_w, 4, "scale_w"),
+        act, _ptr(scale_h, 4, "scale_h"), _ptr(h_out, 2 * M * N, "h_out"), _ptr(act_out, 2 * M * N, "act_out"),
+        _ptr(h_q, M * N, "h_q"), _ptr(amax_out, 4, "amax_out"), _ptr(sat_count, 8, "sat_count"), M, N, K, flags,
+        _ptr(status, 4, "status"), _stream(stream))
+    _check("fp8_upproj_fwd", st)
 
 
 def fp8_downproj_workspace_bytes(M: int) -> int:

@@ -69,13 +69,14 @@ constexpr int kQuantBatch = 8;  // 16-byte loads in flight per quantize thread
 // per 128-long K slice) and the 384-wide tile (one accumulator, so its drain is
 // not hidden behind the next tile; 17.2 -> 16.4 us at 8192 x 3072 -> 768) --
 // else 4 (8 would take a stage of the operand ring: 87.6 -> 92.6 us at 65536
-// rows with 256-wide tiles).
-template <int BN, bool GROUP, bool FUSED>
-constexpr int epi_warps() { return !FUSED && (GROUP || BN > 256) ? kWideEpiWarps : kEpiWarps; }
+// rows with 256-wide tiles) -- and the activation-quantize epilogue (EQ),
+// whose per-element work is several times a plain epilogue's.
+template <int BN, bool GROUP, bool FUSED, bool EQ = false>
+constexpr int epi_warps() { return !FUSED && (GROUP || EQ || BN > 256) ? kWideEpiWarps : kEpiWarps; }
 
-template <int BN, bool GROUP, bool FUSED>
+template <int BN, bool GROUP, bool FUSED, bool EQ = false>
 constexpr int gemm_threads() {
-    return kThreadsGemm + (FUSED ? kQuantThreads : 0) + (epi_warps<BN, GROUP, FUSED>() - kEpiWarps) * 32;
+    return kThreadsGemm + (FUSED ? kQuantThreads : 0) + (epi_warps<BN, GROUP, FUSED, EQ>() - kEpiWarps) * 32;
 }
 
 // Operands of the fused quantize.  ready[b] counts the rows of 128-row block b
@@ -107,7 +108,20 @@ struct FusedArgs {
     HistoryArgs hx, hw;           // delayed-scale updates the last CTA runs (history == nullptr: none)
 };
 
-template <int BN, bool PAIR, int EPI = kEpiWarps, int ACC = (2 * BN <= 512 ? 2 : 1)>
+// The activation-quantize epilogue (EQ): the GEMM output is the pre-activation
+// H of the next layer's quantize.  Per element: h = BF16(acc / (s_a s_b)),
+// a = act(h), a_bf = BF16(a), q = E4M3(a_bf * s_h); amax = max |a_bf| and the
+// saturation count, as in the standalone quantize.
+struct EpiQuantArgs {
+    const float* scale_h;           // E4M3 scale of the activation
+    float* amax_out;                // or nullptr
+    unsigned long long* sat_out;    // or nullptr
+    int act;                        // fp8q_act
+    int has_h, has_act;             // store H (through tmD) / the activation (through tmE1)
+};
+
+template <int BN, bool PAIR, int EPI = kEpiWarps, int ACC = (2 * BN <= 512 ? 2 : 1),
+          int STAGE_PER_WARP = 2 * kEpiChunkBytes>
 struct Cfg {
     // A tile wider than 256 columns takes two MMAs per k-step (N <= 256 each)
     // into one accumulator; B then arrives as one box per MMA.
@@ -121,7 +135,8 @@ struct Cfg {
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int TX_BYTES = STAGE_BYTES * (PAIR ? 2 : 1);  // bytes one stage's barrier awaits
     static constexpr int EPI_WARPS = EPI;
-    static constexpr int EPI_BYTES = EPI * 2 * kEpiChunkBytes;  // double-buffered store staging
+    static constexpr int EPI_STAGE = STAGE_PER_WARP;          // store staging per epilogue warp
+    static constexpr int EPI_BYTES = EPI * STAGE_PER_WARP;
     static constexpr int RING_BUDGET = 220 * 1024 - EPI_BYTES;
     static constexpr int STAGES = RING_BUDGET / STAGE_BYTES < 8 ? RING_BUDGET / STAGE_BYTES : 8;
     static constexpr int TMEM_COLS = (ACCS * BN <= 256) ? 256 : 512;  // power of 2
@@ -142,8 +157,12 @@ struct Cfg {
 
 // Group mode promotes every 128-long K slice, so it keeps as many
 // accumulators as TMEM holds: the MMAs run up to three slices ahead.
-template <int BN, bool GROUP, bool PAIR, bool FUSED>
-using KernelCfg = Cfg<BN, PAIR, epi_warps<BN, GROUP, FUSED>(), GROUP ? 512 / BN : (2 * BN <= 512 ? 2 : 1)>;
+// EQ (the activation-quantize epilogue) stages two outputs per warp: the
+// activation (BF16) and the E4M3 codes (64-column boxes), each double-buffered;
+// H, when asked for, goes through the activation's buffer first.
+template <int BN, bool GROUP, bool PAIR, bool FUSED, bool EQ = false>
+using KernelCfg = Cfg<BN, PAIR, epi_warps<BN, GROUP, FUSED, EQ>(), GROUP ? 512 / BN : (2 * BN <= 512 ? 2 : 1),
+                      (EQ ? 4 : 2) * kEpiChunkBytes>;
 
 // Next accumulator (of ACCS) and the phase its barriers are in.
 template <int ACCS>
@@ -368,6 +387,96 @@ __device__ __forceinline__ void epi_store_chunk(const CUtensorMap* tmD, uint8_t*
     ++nchunk;
 }
 
+// The activation-quantize epilogue (EQ) of one warp's 32 rows: the 64-column
+// chunk pairs pair0, pair0 + pair_step, ... of the BN-wide accumulator (TMEM
+// address taddr).  Per 32-column chunk: H = BF16(acc * inv), the activation
+// (BF16) through a double-buffered 2 KB staging block (the 64-byte swizzle of
+// epi_store_chunk) to one TMA store; the E4M3 codes of a pair fill one
+// 64-column box (32 bytes of each 64-byte row per chunk), stored after the
+// pair's second chunk.  Each chunk's stores are one bulk group, and a buffer
+// is rewritten only after the group that last read it finished: activation
+// buffers alternate with nchunk, E4M3 boxes with nq (E4M3 stores so far);
+// between a box's store and its reuse there is always the group of the other
+// box, so the wait for "at most one group pending" covers both.  H, when asked
+// for, is staged in the activation buffer and stored (and drained) first.
+// Boxes wholly outside D are skipped and counted nowhere.  amax2 / nsat
+// collect this thread's maximum and saturations.
+template <int BN>
+__device__ __forceinline__ void epi_quant_tile(const CUtensorMap* tmH, const CUtensorMap* tmAct,
+                                               const CUtensorMap* tmQ, const EpiQuantArgs& eq, uint8_t* warp_stage,
+                                               int& nchunk, int& nq, int lane, uint32_t taddr, float inv, float s_h,
+                                               int pair0, int pair_step, int64_t col_base, int64_t row0, int64_t M,
+                                               int64_t N, uint32_t& amax2, uint32_t& nsat) {
+    static_assert(BN % 64 == 0, "E4M3 boxes are 64 columns: whole chunk pairs");
+    uint8_t* abuf = warp_stage;
+    uint8_t* qbuf = warp_stage + 2 * kEpiChunkBytes;
+    const int sw = (lane >> 1) & 3;
+    if (row0 >= M) return;  // the warp's rows lie outside D
+#pragma unroll 1
+    for (int p = pair0; p < BN / 64; p += pair_step) {
+        if (col_base + p * 64 >= N) break;  // this and the later pairs lie outside D
+#pragma unroll 1
+        for (int half = 0; half < 2; ++half) {
+            const int64_t col0 = col_base + p * 64 + half * 32;
+            if (col0 >= N) break;
+            uint32_t r[32];
+            tmem_ld_x32_sync(taddr + static_cast<uint32_t>(p * 64 + half * 32), r);
+            uint32_t hb[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                hb[j] = cvt_bf16x2(__uint_as_float(r[2 * j]) * inv, __uint_as_float(r[2 * j + 1]) * inv);
+            uint4 a4[4];
+            uint2 q2[4];
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                a4[g] = act8_any(eq.act, make_uint4(hb[4 * g], hb[4 * g + 1], hb[4 * g + 2], hb[4 * g + 3]), amax2);
+                q2[g] = cast8<FP8Q_E4M3>(a4[g], s_h, nsat);
+            }
+            if (nchunk >= 2) {
+                if (lane == 0) bulk_wait_group_read<1>();
+                __syncwarp();
+            }
+            uint8_t* ab_s = abuf + (nchunk & 1) * kEpiChunkBytes;
+            uint8_t* qb_s = qbuf + (nq & 1) * kEpiChunkBytes;
+            if (eq.has_h) {
+#pragma unroll
+                for (int g = 0; g < 4; ++g)
+                    *reinterpret_cast<uint4*>(ab_s + lane * 64 + ((g ^ sw) << 4)) =
+                        make_uint4(hb[4 * g], hb[4 * g + 1], hb[4 * g + 2], hb[4 * g + 3]);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_2d(tmH, smem_u32(ab_s), static_cast<int32_t>(col0), static_cast<int32_t>(row0));
+                    bulk_commit_group();
+                    bulk_wait_group_read<0>();  // the buffer is free for the activation
+                }
+                __syncwarp();
+            }
+            if (eq.has_act) {
+#pragma unroll
+                for (int g = 0; g < 4; ++g) *reinterpret_cast<uint4*>(ab_s + lane * 64 + ((g ^ sw) << 4)) = a4[g];
+            }
+            *reinterpret_cast<uint4*>(qb_s + lane * 64 + (((2 * half) ^ sw) << 4)) =
+                make_uint4(q2[0].x, q2[0].y, q2[1].x, q2[1].y);
+            *reinterpret_cast<uint4*>(qb_s + lane * 64 + (((2 * half + 1) ^ sw) << 4)) =
+                make_uint4(q2[2].x, q2[2].y, q2[3].x, q2[3].y);
+            fence_proxy_async_smem();
+            __syncwarp();
+            const bool box_done = half == 1 || col0 + 32 >= N;  // the box's last chunk inside D
+            if (lane == 0) {
+                if (eq.has_act)
+                    tma_store_2d(tmAct, smem_u32(ab_s), static_cast<int32_t>(col0), static_cast<int32_t>(row0));
+                if (box_done)
+                    tma_store_2d(tmQ, smem_u32(qb_s), static_cast<int32_t>(col0 - half * 32),
+                                 static_cast<int32_t>(row0));
+                bulk_commit_group();
+            }
+            if (box_done) ++nq;
+            ++nchunk;
+        }
+    }
+}
+
 // GROUP = false: per-tensor scales, one accumulation per tile.
 // GROUP = true : 1-CTA, BN = 128; each 128-long K slice is accumulated into a
 //                fresh TMEM buffer and promoted into FP32 registers with its
@@ -378,14 +487,17 @@ __device__ __forceinline__ void epi_store_chunk(const CUtensorMap* tmD, uint8_t*
 // FUSED = true : the fused quantize + GEMM (per-tensor scales): the extra
 //                quantize warps produce A = X_q from H while the GEMM consumes
 //                finished 128-row blocks.
-template <int BN, bool GROUP, bool PAIR, bool FUSED>
-__global__ void __launch_bounds__(gemm_threads<BN, GROUP, FUSED>(), 1)
+template <int BN, bool GROUP, bool PAIR, bool FUSED, bool EQ>
+__global__ void __launch_bounds__(gemm_threads<BN, GROUP, FUSED, EQ>(), 1)
 fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmD,
                 const float* __restrict__ scale_a, const float* __restrict__ scale_b,
                 int64_t M, int64_t N, int64_t K, uint32_t idesc, int* __restrict__ status,
-                int hold_loads, const FusedArgs fz) {
-    using C = KernelCfg<BN, GROUP, PAIR, FUSED>;
+                int hold_loads, const FusedArgs fz, const __grid_constant__ CUtensorMap tmE1,
+                const __grid_constant__ CUtensorMap tmE2, const EpiQuantArgs eq) {
+    using C = KernelCfg<BN, GROUP, PAIR, FUSED, EQ>;
+    static_assert(!EQ || (!GROUP && !FUSED && BN % 64 == 0 && BN <= 256),
+                  "the activation-quantize epilogue: per-tensor tiles of whole 64-column pairs, two accumulators");
     static_assert(!GROUP || (BN == 128 && !PAIR), "group mode uses 1-CTA 128-wide tiles");
     static_assert(!(GROUP && FUSED), "the fused quantize feeds the per-tensor GEMM");
     extern __shared__ uint8_t smem_raw[];
@@ -427,6 +539,10 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
         tma_prefetch_desc(&tmD);
+        if constexpr (EQ) {
+            tma_prefetch_desc(&tmE1);
+            tma_prefetch_desc(&tmE2);
+        }
     }
     if (warp == 1) {
         if constexpr (PAIR) {
@@ -582,7 +698,10 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
         // drained accumulators are reported to the leader's barrier
         const uint32_t tempty0 = PAIR ? mapa_shared(smem_u32(&tempty[0]), 0) : smem_u32(&tempty[0]);
-        uint8_t* warp_stage = epi_stage + (warp - 2) * 2 * kEpiChunkBytes;
+        uint8_t* warp_stage = epi_stage + (warp - 2) * C::EPI_STAGE;
+        int nq = 0;                        // EQ: E4M3 boxes stored by this warp
+        uint32_t eq_amax2 = 0, eq_nsat = 0;  // EQ: this thread's maximum and saturations
+        const float s_h = EQ ? __ldg(eq.scale_h) : 1.0f;
         int nchunk = 0;
         int acc = 0;
         uint32_t acc_phase = 0;
@@ -600,9 +719,14 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 ok = __all_sync(0xFFFFFFFFu, ok);
                 if (!ok) break;
                 tc_fence_after();
+                if constexpr (EQ) {
+                    epi_quant_tile<BN>(&tmD, &tmE1, &tmE2, eq, warp_stage, nchunk, nq, lane,
+                                       tmem_base + lane_base + static_cast<uint32_t>(acc * BN), inv, s_h,
+                                       (warp - 2) / 4, C::EPI_WARPS / 4, n_blk * BN, row0, M, N, eq_amax2, eq_nsat);
+                }
                 // with 8 epilogue warps the two warps of a lane quarter take alternate chunks
 #pragma unroll 1
-                for (int c = (warp - 2) / 4; c < BN / 32; c += C::EPI_WARPS / 4) {
+                for (int c = (warp - 2) / 4; c < (EQ ? 0 : BN / 32); c += C::EPI_WARPS / 4) {
                     uint32_t r[32];
                     tmem_ld_x32_sync(tmem_base + lane_base + static_cast<uint32_t>(acc * BN + c * 32), r);
                     float v[32];
@@ -677,6 +801,15 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         // complete on their own and are visible when the grid finishes)
         if (lane == 0) bulk_wait_group_read<0>();
         __syncwarp();
+        if constexpr (EQ) {
+            const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, max16x2(eq_amax2));
+            const uint32_t c = __reduce_add_sync(0xFFFFFFFFu, eq_nsat);
+            if (lane == 0) {
+                // a non-negative float orders like its bit pattern
+                if (eq.amax_out && m) atomicMax(reinterpret_cast<unsigned int*>(eq.amax_out), m << 16);
+                if (eq.sat_out && c) atomicAdd(eq.sat_out, static_cast<unsigned long long>(c));
+            }
+        }
     }
 
     tc_fence_before();
@@ -760,6 +893,20 @@ bool make_out_map(CUtensorMap* map, void* base, int64_t rows, int64_t cols) {
     return r == CUDA_SUCCESS;
 }
 
+// E4M3 output Q [rows, cols]: box = 64 bytes x 32 rows, 64-byte swizzle (stores).
+bool make_q_out_map(CUtensorMap* map, void* base, int64_t rows, int64_t cols) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols)};
+    cuuint32_t box[2] = {64, 32};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                    CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 std::atomic<int> g_hold_loads{0};  // fp8q_gemm_test_hold_loads
 
 struct LaunchInfo {
@@ -767,13 +914,13 @@ struct LaunchInfo {
     int max_clusters = 0;  // co-resident 2-CTA clusters (PAIR only)
 };
 
-template <int BN, bool GROUP, bool PAIR, bool FUSED>
+template <int BN, bool GROUP, bool PAIR, bool FUSED, bool EQ = false>
 const LaunchInfo& launch_info() {
-    using C = KernelCfg<BN, GROUP, PAIR, FUSED>;
+    using C = KernelCfg<BN, GROUP, PAIR, FUSED, EQ>;
     static LaunchInfo info;
     static std::once_flag once;
     std::call_once(once, [] {
-        auto kern = fp8_gemm_kernel<BN, GROUP, PAIR, FUSED>;
+        auto kern = fp8_gemm_kernel<BN, GROUP, PAIR, FUSED, EQ>;
         info.attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
         if (PAIR && info.attr_err == cudaSuccess) {
             cudaLaunchConfig_t cfg = {};
@@ -783,7 +930,7 @@ const LaunchInfo& launch_info() {
             attr[0].val.clusterDim.y = 1;
             attr[0].val.clusterDim.z = 1;
             cfg.gridDim = dim3(2 * sm_count());
-            cfg.blockDim = dim3(gemm_threads<BN, GROUP, FUSED>());
+            cfg.blockDim = dim3(gemm_threads<BN, GROUP, FUSED, EQ>());
             cfg.dynamicSmemBytes = C::SMEM_BYTES;
             cfg.attrs = attr;
             cfg.numAttrs = 1;
@@ -798,20 +945,42 @@ const LaunchInfo& launch_info() {
     return info;
 }
 
-template <int BN, bool GROUP, bool PAIR, bool FUSED>
+// Outputs of the activation-quantize epilogue (EQ): d is H (or nullptr).
+struct EpiQuantHost {
+    void* act_out;  // BF16 [M,N] or nullptr
+    void* q_out;    // E4M3 [M,N]
+    EpiQuantArgs args;
+};
+
+template <int BN, bool GROUP, bool PAIR, bool FUSED, bool EQ = false>
 int launch_gemm(const void* a, const void* b, const float* sa, const float* sb, void* d, int64_t M,
                 int64_t N, int64_t K, uint32_t afmt, uint32_t bfmt, int* status, cudaStream_t stream,
-                const FusedArgs& fz) {
-    using C = KernelCfg<BN, GROUP, PAIR, FUSED>;
-    const LaunchInfo& info = launch_info<BN, GROUP, PAIR, FUSED>();
+                const FusedArgs& fz, const EpiQuantHost* eqh = nullptr) {
+    using C = KernelCfg<BN, GROUP, PAIR, FUSED, EQ>;
+    const LaunchInfo& info = launch_info<BN, GROUP, PAIR, FUSED, EQ>();
     if (info.attr_err != cudaSuccess) return FP8Q_ERR_CUDA;
-    alignas(64) CUtensorMap mapA, mapB, mapD;
-    if (!make_kmajor_map(&mapA, a, M, K, BM) || !make_kmajor_map(&mapB, b, N, K, C::B_BOX) ||
-        !make_out_map(&mapD, d, M, N))
-        return FP8Q_ERR_CUDA;
+    alignas(64) CUtensorMap mapA, mapB, mapD, mapE1, mapE2;
+    if (!make_kmajor_map(&mapA, a, M, K, BM) || !make_kmajor_map(&mapB, b, N, K, C::B_BOX)) return FP8Q_ERR_CUDA;
+    EpiQuantArgs eq = {};
+    if constexpr (EQ) {
+        // every map handed to the kernel is a valid one: an output not asked
+        // for takes the E4M3 map, which the kernel then never stores through
+        eq = eqh->args;
+        if (!make_q_out_map(&mapE2, eqh->q_out, M, N)) return FP8Q_ERR_CUDA;
+        mapE1 = mapE2;
+        mapD = mapE2;
+        if (eqh->act_out && !make_out_map(&mapE1, eqh->act_out, M, N)) return FP8Q_ERR_CUDA;
+        if (d && !make_out_map(&mapD, d, M, N)) return FP8Q_ERR_CUDA;
+        eq.has_act = eqh->act_out != nullptr;
+        eq.has_h = d != nullptr;
+    } else {
+        if (!make_out_map(&mapD, d, M, N)) return FP8Q_ERR_CUDA;
+        mapE1 = mapD;
+        mapE2 = mapD;
+    }
     const int64_t tiles = ((M + C::TILE_M - 1) / C::TILE_M) * ((N + BN - 1) / BN);
     const uint32_t idesc = idesc_f8(afmt, bfmt, C::MMA_M, C::MMA_N);
-    auto kern = fp8_gemm_kernel<BN, GROUP, PAIR, FUSED>;
+    auto kern = fp8_gemm_kernel<BN, GROUP, PAIR, FUSED, EQ>;
     if constexpr (PAIR) {
         if (info.max_clusters < 1) return FP8Q_ERR_CUDA;
         const int clusters = static_cast<int>(FUSED ? info.max_clusters : std::min<int64_t>(tiles, info.max_clusters));
@@ -826,13 +995,13 @@ int launch_gemm(const void* a, const void* b, const float* sa, const float* sb, 
         attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[1].val.programmaticStreamSerializationAllowed = 1;
         cfg.gridDim = dim3(2 * clusters);
-        cfg.blockDim = dim3(gemm_threads<BN, GROUP, FUSED>());
+        cfg.blockDim = dim3(gemm_threads<BN, GROUP, FUSED, EQ>());
         cfg.dynamicSmemBytes = C::SMEM_BYTES;
         cfg.stream = stream;
         cfg.attrs = attr;
         cfg.numAttrs = 2;
         if (cudaLaunchKernelEx(&cfg, kern, mapA, mapB, mapD, sa, sb, M, N, K, idesc, status,
-                               g_hold_loads.load(), f) != cudaSuccess) {
+                               g_hold_loads.load(), f, mapE1, mapE2, eq) != cudaSuccess) {
             (void)cudaGetLastError();
             return FP8Q_ERR_CUDA;
         }
@@ -842,8 +1011,8 @@ int launch_gemm(const void* a, const void* b, const float* sa, const float* sb, 
         const int grid = static_cast<int>(FUSED ? sm_count() : std::min<int64_t>(tiles, sm_count()));
         FusedArgs f = fz;
         if (f.w) f.w_units = static_cast<unsigned>(grid * kEpiWarps);  // each epilogue warp reports once
-        if (launch_pdl(kern, dim3(grid), dim3(gemm_threads<BN, GROUP, FUSED>()), C::SMEM_BYTES, stream, mapA, mapB, mapD, sa,
-                       sb, M, N, K, idesc, status, g_hold_loads.load(), f) != cudaSuccess) {
+        if (launch_pdl(kern, dim3(grid), dim3(gemm_threads<BN, GROUP, FUSED, EQ>()), C::SMEM_BYTES, stream, mapA, mapB, mapD, sa,
+                       sb, M, N, K, idesc, status, g_hold_loads.load(), f, mapE1, mapE2, eq) != cudaSuccess) {
             (void)cudaGetLastError();
             return FP8Q_ERR_CUDA;
         }
@@ -950,6 +1119,49 @@ int check_gemm_args(const void* a, const void* b, const float* sa, const float* 
     return FP8Q_OK;
 }
 
+// Tile for the activation-quantize epilogue: whole 64-column pairs and two
+// accumulators, so widths 128, 192 and 256, scored like pick_shape.  A tile
+// override names one of these or is ignored.
+Shape pick_shape_eq(int64_t M, int64_t N) {
+    const int ov = g_tile_override.load(std::memory_order_relaxed);
+    if (ov >= 0) {
+        const bool pair = (ov >> 16) != 0;
+        const int bn = ov & 0xFFFF;
+        if (bn % 64 == 0 && bn <= 256) return Shape{pair && M > BM, bn};
+    }
+    struct Cand { bool pair; int bn; double t; };
+    static constexpr Cand kCands[] = {{true, 256, 1.000}, {true, 192, 0.909}, {true, 128, 0.858},
+                                      {false, 192, 0.897}, {false, 128, 0.843}, {false, 256, 1.102}};
+    const int64_t sms = sm_count();
+    Shape best{false, 128};
+    double best_cost = -1.0;
+    for (const Cand& c : kCands) {
+        if (c.pair && M <= BM) continue;
+        const int64_t tile_m = c.pair ? 2 * BM : BM;
+        const int64_t units = c.pair ? sms / 2 : sms;
+        const int64_t tiles = ((M + tile_m - 1) / tile_m) * ((N + c.bn - 1) / c.bn);
+        const double cost = static_cast<double>((tiles + units - 1) / units) * c.t;
+        if (best_cost < 0 || cost < best_cost) { best_cost = cost; best = Shape{c.pair, c.bn}; }
+    }
+    return best;
+}
+
+int launch_eq(const Shape& s, const void* a, const void* b, const float* sa, const float* sb, void* h,
+              int64_t M, int64_t N, int64_t K, int* status, cudaStream_t stream, const EpiQuantHost& e) {
+#define FP8Q_LAUNCH_EQ(BNV, PR) \
+    return launch_gemm<BNV, false, PR, false, true>(a, b, sa, sb, h, M, N, K, FP8Q_E4M3, FP8Q_E4M3, status, stream, \
+                                                    FusedArgs{}, &e)
+    if (s.pair) {
+        if (s.bn == 256) FP8Q_LAUNCH_EQ(256, true);
+        if (s.bn == 192) FP8Q_LAUNCH_EQ(192, true);
+        FP8Q_LAUNCH_EQ(128, true);
+    }
+    if (s.bn == 256) FP8Q_LAUNCH_EQ(256, false);
+    if (s.bn == 192) FP8Q_LAUNCH_EQ(192, false);
+    FP8Q_LAUNCH_EQ(128, false);
+#undef FP8Q_LAUNCH_EQ
+}
+
 }  // namespace
 
 }  // namespace fp8q
@@ -989,6 +1201,29 @@ extern "C" int fp8_gemm_dgrad(const void* dy_q, const void* w_q, const float* sc
     if (st != FP8Q_OK) return st;
     if (M == 0) return FP8Q_OK;
     return gemm_dispatch(dy_q, w_q, scale_dy, scale_w, 0, dx, M, K, N, FP8Q_E5M2, FP8Q_E4M3, status, stream);
+}
+
+extern "C" int fp8_upproj_fwd(const void* x_q, const void* wt_q, const float* scale_x, const float* scale_w,
+                              int act, const float* scale_h, void* h_out, void* act_out, void* h_q,
+                              float* amax_out, unsigned long long* sat_count, int64_t M, int64_t N, int64_t K,
+                              unsigned flags, int* status, cudaStream_t stream) {
+    if (flags & ~static_cast<unsigned>(FP8Q_ACCUMULATE)) return FP8Q_ERR_UNSUPPORTED;
+    if (act < FP8Q_ACT_IDENTITY || act > FP8Q_ACT_RELU2) return FP8Q_ERR_UNSUPPORTED;
+    if (scale_h == nullptr) return FP8Q_ERR_NULL;
+    if (!aligned16(h_out) || !aligned16(act_out) || (reinterpret_cast<uintptr_t>(amax_out) & 3u) ||
+        (reinterpret_cast<uintptr_t>(sat_count) & 7u) || (reinterpret_cast<uintptr_t>(scale_h) & 3u))
+        return FP8Q_ERR_ALIGN;
+    // D = the E4M3 copy [M,N] (required); H and the activation copy are optional
+    int st = check_gemm_args(x_q, wt_q, scale_x, scale_w, h_q, M, N, K, status);
+    if (st != FP8Q_OK) return st;
+    if (!(flags & FP8Q_ACCUMULATE)) {
+        if (amax_out && cudaMemsetAsync(amax_out, 0, sizeof(float), stream) != cudaSuccess) return FP8Q_ERR_CUDA;
+        if (sat_count && cudaMemsetAsync(sat_count, 0, sizeof(unsigned long long), stream) != cudaSuccess)
+            return FP8Q_ERR_CUDA;
+    }
+    if (M == 0) return FP8Q_OK;
+    const EpiQuantHost e{act_out, h_q, EpiQuantArgs{scale_h, amax_out, sat_count, act, 0, 0}};
+    return launch_eq(pick_shape_eq(M, N), x_q, wt_q, scale_x, scale_w, h_out, M, N, K, status, stream, e);
 }
 
 extern "C" int fp8_gemm_wgrad(const void* x_q_t, const void* dy_q_t, const float* scale_x,

@@ -113,6 +113,27 @@ def test_gemm_argument_checks(lib):
     assert wg(A, A, A, A, A, 1024, 64, 256, None, None) == ERR_UNSUPPORTED
 
 
+def test_upproj_argument_checks(lib):
+    """fp8_upproj_fwd checks its arguments on the host, before any device work."""
+    f = lib.fp8_upproj_fwd
+    P, i64 = ctypes.c_void_p, ctypes.c_int64
+    f.argtypes = [P, P, P, P, ctypes.c_int, P, P, P, P, P, P, i64, i64, i64, ctypes.c_uint, P, P]
+    f.restype = ctypes.c_int
+
+    def call(act=2, sh=A, h=None, a=None, q=A, amax=None, M=128, N=256, K=256, flags=0):
+        return f(A, A, A, A, act, sh, h, a, q, amax, None, M, N, K, flags, None, None)
+
+    assert call(act=3) == ERR_UNSUPPORTED
+    assert call(flags=2) == ERR_UNSUPPORTED
+    assert call(sh=None) == ERR_NULL
+    assert call(q=None) == ERR_NULL
+    assert call(a=A + 8) == ERR_ALIGN
+    assert call(amax=A + 2) == ERR_ALIGN
+    assert call(N=200) == ERR_SHAPE
+    assert call(K=40) == ERR_SHAPE
+    assert call() == ERR_UNSUPPORTED  # valid arguments, no sm_103 device here
+
+
 def test_history_argument_checks(lib):
     f = lib.amax_history_update
     assert f(None, 1, A, A, 2.0, 0, A, None, None) == ERR_NULL
