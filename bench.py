@@ -625,7 +625,26 @@ def measure_other_rows(dev, reps: int, fp8_tflops: float) -> dict:
     dx = torch.empty(M, K, dtype=torch.bfloat16, device=dev)
     t = timed_b2b([lambda: B.fp8_gemm_dgrad(dyq, w_q, sdy, one, dx)], max(4, reps // 8))
     out["a11 dgrad GEMM"] = mma_row(t, 2.0 * M * N * K, f"dY_q [{M},{N}] x W_q [{K},{N}]^T")
-    del dx, dyq, w_q, wt_q
+    # next: the ReLU^2 backward in the dgrad epilogue, dH = dX * 2 max(H, 0) (H read, dX never stored)
+    g = torch.Generator(device=dev).manual_seed(xl.seed)
+    Hb = torch.randn(M, K, device=dev, generator=g).to(torch.bfloat16)
+    t = timed_b2b([lambda: B.fp8_gemm_dgrad_act(dyq, w_q, sdy, one, Hb, dx, act=B.ACT_RELU2)], max(4, reps // 8))
+    row = mma_row(t, 2.0 * M * N * K, f"dY_q [{M},{N}] x W_q [{K},{N}]^T, H [{M},{K}] -> dH")
+    row["vs_dgrad_alone"] = out["a11 dgrad GEMM"]["ms"] / t
+    # the unfused pair it replaces: the dgrad writing dX, then dH = dX * 2 relu(H) elementwise (torch)
+    dh, tmp = torch.empty_like(dx), torch.empty_like(dx)
+
+    def unfused():
+        B.fp8_gemm_dgrad(dyq, w_q, sdy, one, dx)
+        torch.clamp(Hb, min=0, out=tmp)
+        tmp.mul_(2.0)
+        torch.mul(dx, tmp, out=dh)
+
+    t2 = timed_b2b([unfused], max(4, reps // 8))
+    row["unfused_ms (dgrad writing dX, then dH = dX * 2 relu(H) elementwise)"] = t2
+    row["speedup_vs_unfused"] = t2 / t
+    out["next: dgrad with the ReLU^2 backward epilogue"] = row
+    del Hb, dx, dh, tmp, dyq, w_q, wt_q
     # wgrad dW = X^T dY: X_q^T [K,M] (E4M3 codes; the GEMM's time does not depend on their values)
     g = torch.Generator(device=dev).manual_seed(xl.seed)
     xqt = torch.randint(0, 120, (K, M), dtype=torch.uint8, device=dev, generator=g)

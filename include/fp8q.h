@@ -11,6 +11,7 @@
  *   (fp8_gemm_dgrad         dX = dY_q W_q^T / (s_dy s_w), the gradient shape)
  *   (fp8_gemm_wgrad         dW = X_q^T dY_q / (s_x s_dy), the weight gradient)
  *   (fp8_upproj_fwd         the preceding up-projection with 1 in its epilogue)
+ *   (fp8_gemm_dgrad_act     dgrad with the activation backward in its epilogue)
  *
  * Conventions shared by every call:
  *  - All tensor pointers are DEVICE pointers to caller-owned memory; the
@@ -239,6 +240,25 @@ int fp8_gemm_dgrad(const void* dy_q, const void* w_q,
                    const float* scale_dy, const float* scale_w,
                    void* dx, int64_t M, int64_t N, int64_t K,
                    int* status, cudaStream_t stream);
+
+/*
+ * fp8_gemm_dgrad_act -- dH = dX * act'(H): the activation backward in the dgrad epilogue  [gemms][fused]
+ *
+ * dX = (dY_q . W_q^T) / (s_dy s_w) as in fp8_gemm_dgrad, multiplied in the
+ * epilogue, while still in FP32, by the derivative of the activation at the
+ * BF16 pre-activation H ("Paradigma Details FP8 and Optimizer Tricks Behind
+ * NanoGPT Records", second paragraph: the activation whose BF16 copy the
+ * forward keeps): act'(h) = 2 max(h, 0) for ReLU^2, (h > 0) for ReLU, 1 for
+ * identity.  dX itself never reaches HBM.
+ *   dy_q, w_q, scale_dy, scale_w, M, N, K, status  as for fp8_gemm_dgrad.
+ *   h       device [M,K] BF16: the pre-activation (16-byte aligned).
+ *   act     FP8Q_ACT_IDENTITY, FP8Q_ACT_RELU or FP8Q_ACT_RELU2.
+ *   dh      device [M,K] BF16:  dh[i,k] = BF16( dX[i,k] (float32) * act'(h[i,k]) ).
+ */
+int fp8_gemm_dgrad_act(const void* dy_q, const void* w_q,
+                       const float* scale_dy, const float* scale_w,
+                       const void* h, int act, void* dh, int64_t M, int64_t N, int64_t K,
+                       int* status, cudaStream_t stream);
 
 /*
  * fp8_gemm_wgrad -- dW = (X_q^T . dY_q) / (s_x s_dy), FP32 accumulation, BF16 out  [gemms]

@@ -5,7 +5,10 @@ CPU-baseline leg of ``bench.py`` may import this package.  The product path
 (``quantize_fp8_gemm_gb300``) never imports, links or runs it.
 
 This module is argument marshalling around ``oref.c`` (numpy arrays in,
-numpy arrays out).  All arithmetic lives in the C file, written from the pages:
+numpy arrays out).  The arithmetic lives in the C file, except two plain numpy
+steps stated where they are used (the weight gradient's transposed operand in
+``gemm_wgrad``, the activation derivative in ``act_grad``); written from the
+pages:
 
 * "FP8 training: what it is and how it works" -- Step 1 (E4M3/E5M2), Step 2
   (scale = format max / amax), Step 3 (FP8 inputs, wide sums), Worked example
@@ -213,6 +216,32 @@ def gemm_dgrad(dy_q, w_q, s_dy: float, s_w: float, *, rows=None, fmt_dy=E5M2, fm
     lib().oref_gemm_dgrad(_p(D), fmt_dy, _p(W), fmt_w, M, N, K, float(s_dy), float(s_w),
                           _p(rows), rows.size, _p(dX), _p(S), nthreads or default_threads())
     return dX, S
+
+
+def act_grad(h_bf16, act_kind: int):
+    """d act(h) / dh at the BF16 values h (float64): ReLU^2 -> 2 max(h, 0), ReLU
+    -> 1 where h > 0 else 0, identity -> 1 (the derivatives of the activations
+    of "Paradigma Details FP8 and Optimizer Tricks Behind NanoGPT Records",
+    second paragraph; h > 0 is the comparison the forward's ReLU uses)."""
+    h = bf16_to_f32(_c(h_bf16, np.uint16)).astype(np.float64)
+    if act_kind == ACT_RELU2:
+        return np.where(h > 0, 2.0 * h, 0.0)
+    if act_kind == ACT_RELU:
+        return np.where(h > 0, 1.0, 0.0)
+    return np.ones_like(h)
+
+
+def gemm_dgrad_act(dy_q, w_q, s_dy: float, s_w: float, h_bf16, act_kind: int, *, rows=None, fmt_dy=E5M2,
+                   fmt_w=E4M3, nthreads=None):
+    """The activation backward through the down-projection's dgrad:
+    dH = (dY x W^T) * act'(H) over dequantised FP8, dY [M,N], W [K,N], H [M,K]
+    BF16.  Returns (dH, S): S is the dgrad's sum of |terms| times |act'(H)|."""
+    dX, S = gemm_dgrad(dy_q, w_q, s_dy, s_w, rows=rows, fmt_dy=fmt_dy, fmt_w=fmt_w, nthreads=nthreads)
+    h = _c(h_bf16, np.uint16)
+    if rows is not None:
+        h = h[_c(rows, np.int64)]
+    g = act_grad(h, act_kind)
+    return dX * g, S * np.abs(g)
 
 
 def gemm_wgrad(x_q, dy_q, s_x: float, s_dy: float, *, rows=None, fmt_x=E4M3, fmt_dy=E5M2,

@@ -53,6 +53,7 @@ def lib() -> ctypes.CDLL:
         L.fp8_cast_f32.argtypes = [P, P, i64, i32, P]
         L.fp8_gemm_dgrad.argtypes = [P, P, P, P, P, i64, i64, i64, P, P]
         L.fp8_gemm_wgrad.argtypes = [P, P, P, P, P, i64, i64, i64, P, P]
+        L.fp8_gemm_dgrad_act.argtypes = [P, P, P, P, P, i32, P, i64, i64, i64, P, P]
         L.fp8_upproj_fwd.argtypes = [P, P, P, P, i32, P, P, P, P, P, P, i64, i64, i64, ctypes.c_uint, P, P]
         L.amax_history_update.argtypes = [P, i32, P, P, f32, i32, P, P, P]
         L.amax_history_update_ex.argtypes = [P, i32, P, P, f32, i32, P, P, P, P, P, P]
@@ -73,7 +74,7 @@ def lib() -> ctypes.CDLL:
         L.fp8q_gemm_set_tile.argtypes = [i32, i32]
         L.fp8q_gemm_set_tile.restype = i32
         for fn in ("fp8_quant_fused", "fp8_quant_fused_ex", "fp8_quant_fused_batch", "fp8_downproj_fwd",
-                   "fp8_downproj_fwd_noalloc", "fp8_downproj_fwd_ex", "fp8_gemm_fwd", "fp8_gemm_dgrad", "fp8_gemm_wgrad", "fp8_upproj_fwd", "amax_history_update",
+                   "fp8_downproj_fwd_noalloc", "fp8_downproj_fwd_ex", "fp8_gemm_fwd", "fp8_gemm_dgrad", "fp8_gemm_wgrad", "fp8_gemm_dgrad_act", "fp8_upproj_fwd", "amax_history_update",
                    "amax_history_update_ex", "fp8q_naive_act", "fp8q_naive_amax", "fp8q_naive_cast"):
             getattr(L, fn).restype = i32
         _lib = L
@@ -200,6 +201,21 @@ def fp8_gemm_dgrad(dy_q: torch.Tensor, w_q: torch.Tensor, scale_dy: torch.Tensor
         _ptr(scale_w, 4, "scale_w"), _ptr(dx, 2 * M * K, "dx"), M, N, K,
         _ptr(status, 4, "status"), _stream(stream))
     _check("fp8_gemm_dgrad", st)
+
+
+def fp8_gemm_dgrad_act(dy_q: torch.Tensor, w_q: torch.Tensor, scale_dy: torch.Tensor, scale_w: torch.Tensor,
+                       h: torch.Tensor, dh: torch.Tensor, *, act: int = ACT_RELU2, status=None, stream=None) -> None:
+    """dh[M,K] = BF16(dX * act'(h)): the dgrad dX = dy_q . w_q^T / (s_dy s_w) times the
+    activation derivative at the BF16 pre-activation h [M,K], in the GEMM's epilogue."""
+    M, N = dy_q.shape
+    K = w_q.shape[0]
+    if w_q.shape[1] != N:
+        raise ValueError("dy_q [M,N] and w_q [K,N] disagree on N")
+    st = lib().fp8_gemm_dgrad_act(
+        _ptr(dy_q, M * N, "dy_q"), _ptr(w_q, K * N, "w_q"), _ptr(scale_dy, 4, "scale_dy"),
+        _ptr(scale_w, 4, "scale_w"), _ptr(h, 2 * M * K, "h"), act, _ptr(dh, 2 * M * K, "dh"), M, N, K,
+        _ptr(status, 4, "status"), _stream(stream))
+    _check("fp8_gemm_dgrad_act", st)
 
 
 def fp8_gemm_wgrad(x_q_t: torch.Tensor, dy_q_t: torch.Tensor, scale_x: torch.Tensor, scale_dy: torch.Tensor,

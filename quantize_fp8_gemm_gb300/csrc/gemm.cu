@@ -160,9 +160,12 @@ struct Cfg {
 // EQ (the activation-quantize epilogue) stages two outputs per warp: the
 // activation (BF16) and the E4M3 codes (64-column boxes), each double-buffered;
 // H, when asked for, goes through the activation's buffer first.
-template <int BN, bool GROUP, bool PAIR, bool FUSED, bool EQ = false>
+// DACT (the activation backward in the dgrad epilogue) adds a load buffer for
+// every 32-column chunk of H in the tile (BN / 16 KB) and one mbarrier: 5 KB +
+// BN / 16 KB per warp, keeping each warp's buffers 1024-byte aligned.
+template <int BN, bool GROUP, bool PAIR, bool FUSED, bool EQ = false, bool DACT = false>
 using KernelCfg = Cfg<BN, PAIR, epi_warps<BN, GROUP, FUSED, EQ>(), GROUP ? 512 / BN : (2 * BN <= 512 ? 2 : 1),
-                      (EQ ? 4 : 2) * kEpiChunkBytes>;
+                      EQ ? 4 * kEpiChunkBytes : DACT ? (5 + BN / 16) * 1024 : 2 * kEpiChunkBytes>;
 
 // Next accumulator (of ACCS) and the phase its barriers are in.
 template <int ACCS>
@@ -477,6 +480,70 @@ __device__ __forceinline__ void epi_quant_tile(const CUtensorMap* tmH, const CUt
     }
 }
 
+// The activation backward in the dgrad epilogue (DACT): for the chunks c0,
+// c0 + step, ... of one warp's 32 rows of the accumulator,
+//   dh = BF16( acc * inv * act'(h) ),  act'(h) = 2 max(h, 0) (ReLU^2),
+//   (h > 0) (ReLU) or 1 (identity), h the BF16 pre-activation at the same spot.
+// issue_h_loads asks TMA for all of the warp's H boxes of a tile (32 rows x 32
+// columns each, in the 64-byte swizzle of the store staging, so lane r reads
+// row r) on one mbarrier, before the warp waits for the accumulator: the loads
+// land while the MMAs of the tile run.  ldn counts the warp's tiles of loads
+// (the barrier's phase is ldn & 1); epi_dact_tile waits for them once.
+// Returns false when a bounded wait gave up.
+__device__ __forceinline__ void issue_h_loads(const CUtensorMap* tmH, uint8_t* lbuf, uint64_t* lbar, uint32_t& ldn,
+                                              int lane, int nck, int c0, int step, int64_t col_base, int64_t row0) {
+    fence_proxy_async_smem();  // the buffers' last reads (the previous tile) come first
+    __syncwarp();
+    if (lane == 0) {
+        const uint32_t bar = smem_u32(lbar);
+        int n = 0;
+        for (int c = c0; c < nck; c += step) ++n;
+        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(n) * kEpiChunkBytes);
+        for (int c = c0, i = 0; c < nck; c += step, ++i)
+            tma_load_2d(smem_u32(lbuf + i * kEpiChunkBytes), tmH, bar, static_cast<int32_t>(col_base + c * 32),
+                        static_cast<int32_t>(row0));
+    }
+    ++ldn;
+}
+
+template <int BN>
+__device__ __forceinline__ bool epi_dact_tile(const CUtensorMap* tmD, int act, uint8_t* warp_stage,
+                                              const uint8_t* lbuf, uint64_t* lbar, int& nchunk, uint32_t& ldw,
+                                              int lane, uint32_t taddr, float inv, int c0, int step,
+                                              int64_t col_base, int64_t row0, int64_t M, int64_t N,
+                                              volatile int* abort_flag, int* status) {
+    const int sw = (lane >> 1) & 3;
+    const bool ok = __all_sync(0xFFFFFFFFu, wait_phase(lbar, ldw & 1, abort_flag, status));
+    if (!ok) return false;
+    ++ldw;
+#pragma unroll 1
+    for (int c = c0, i = 0; c < BN / 32; c += step, ++i) {
+        uint32_t r[32];
+        tmem_ld_x32_sync(taddr + static_cast<uint32_t>(c * 32), r);
+        const uint8_t* hrow = lbuf + i * kEpiChunkBytes + lane * 64;
+        float v[32];
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            const uint4 h = *reinterpret_cast<const uint4*>(hrow + ((g ^ sw) << 4));
+            const uint32_t hw[4] = {h.x, h.y, h.z, h.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const float hv = e ? bf16hi_to_f32(hw[k]) : bf16lo_to_f32(hw[k]);
+                    const float d = hv > 0.0f ? (act == FP8Q_ACT_RELU2 ? 2.0f * hv : 1.0f) : 0.0f;
+                    const float f = act == FP8Q_ACT_IDENTITY ? 1.0f : d;
+                    const int j = g * 8 + k * 2 + e;
+                    v[j] = __uint_as_float(r[j]) * inv * f;
+                }
+            }
+        }
+        epi_store_chunk(tmD, warp_stage, nchunk, lane, v, static_cast<int32_t>(col_base + c * 32),
+                        static_cast<int32_t>(row0), M, N);
+    }
+    return true;
+}
+
 // GROUP = false: per-tensor scales, one accumulation per tile.
 // GROUP = true : 1-CTA, BN = 128; each 128-long K slice is accumulated into a
 //                fresh TMEM buffer and promoted into FP32 registers with its
@@ -487,7 +554,7 @@ __device__ __forceinline__ void epi_quant_tile(const CUtensorMap* tmH, const CUt
 // FUSED = true : the fused quantize + GEMM (per-tensor scales): the extra
 //                quantize warps produce A = X_q from H while the GEMM consumes
 //                finished 128-row blocks.
-template <int BN, bool GROUP, bool PAIR, bool FUSED, bool EQ>
+template <int BN, bool GROUP, bool PAIR, bool FUSED, bool EQ, bool DACT>
 __global__ void __launch_bounds__(gemm_threads<BN, GROUP, FUSED, EQ>(), 1)
 fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmD,
@@ -495,7 +562,8 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 int64_t M, int64_t N, int64_t K, uint32_t idesc, int* __restrict__ status,
                 int hold_loads, const FusedArgs fz, const __grid_constant__ CUtensorMap tmE1,
                 const __grid_constant__ CUtensorMap tmE2, const EpiQuantArgs eq) {
-    using C = KernelCfg<BN, GROUP, PAIR, FUSED, EQ>;
+    using C = KernelCfg<BN, GROUP, PAIR, FUSED, EQ, DACT>;
+    static_assert(!DACT || (!GROUP && !FUSED && !EQ), "the activation backward runs in the per-tensor dgrad epilogue");
     static_assert(!EQ || (!GROUP && !FUSED && BN % 64 == 0 && BN <= 256),
                   "the activation-quantize epilogue: per-tensor tiles of whole 64-column pairs, two accumulators");
     static_assert(!GROUP || (BN == 128 && !PAIR), "group mode uses 1-CTA 128-wide tiles");
@@ -702,6 +770,17 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         int nq = 0;                        // EQ: E4M3 boxes stored by this warp
         uint32_t eq_amax2 = 0, eq_nsat = 0;  // EQ: this thread's maximum and saturations
         const float s_h = EQ ? __ldg(eq.scale_h) : 1.0f;
+        // DACT: this warp's H load buffers (after its store staging) and their barrier
+        uint8_t* lbuf = warp_stage + 2 * kEpiChunkBytes;
+        uint64_t* lbar = reinterpret_cast<uint64_t*>(warp_stage + 2 * kEpiChunkBytes + (BN / 32) * kEpiChunkBytes);
+        uint32_t ldn = 0, ldw = 0;  // DACT: tiles of H loads issued / consumed by this warp
+        if constexpr (DACT) {
+            if (lane == 0) {
+                mbar_init(smem_u32(lbar), 1);
+                fence_mbar_init();
+            }
+            __syncwarp();
+        }
         int nchunk = 0;
         int acc = 0;
         uint32_t acc_phase = 0;
@@ -715,6 +794,10 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             const int64_t row0 = m_blk * C::TILE_M + rank * BM + q * 32;  // this warp's first row
             const int64_t row = row0 + lane;
             if constexpr (!GROUP) {
+                // DACT: the first chunk's H is on its way while the accumulator fills
+                if constexpr (DACT)
+                    issue_h_loads(&tmE1, lbuf, lbar, ldn, lane, BN / 32, (warp - 2) / 4, C::EPI_WARPS / 4,
+                                  n_blk * BN, row0);
                 ok = wait_phase(&tfull[acc], acc_phase, abort_flag, status);
                 ok = __all_sync(0xFFFFFFFFu, ok);
                 if (!ok) break;
@@ -724,9 +807,15 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                                        tmem_base + lane_base + static_cast<uint32_t>(acc * BN), inv, s_h,
                                        (warp - 2) / 4, C::EPI_WARPS / 4, n_blk * BN, row0, M, N, eq_amax2, eq_nsat);
                 }
+                if constexpr (DACT) {
+                    ok = epi_dact_tile<BN>(&tmD, eq.act, warp_stage, lbuf, lbar, nchunk, ldw, lane,
+                                           tmem_base + lane_base + static_cast<uint32_t>(acc * BN), inv,
+                                           (warp - 2) / 4, C::EPI_WARPS / 4, n_blk * BN, row0, M, N, abort_flag,
+                                           status);
+                }
                 // with 8 epilogue warps the two warps of a lane quarter take alternate chunks
 #pragma unroll 1
-                for (int c = (warp - 2) / 4; c < (EQ ? 0 : BN / 32); c += C::EPI_WARPS / 4) {
+                for (int c = (warp - 2) / 4; c < ((EQ || DACT) ? 0 : BN / 32); c += C::EPI_WARPS / 4) {
                     uint32_t r[32];
                     tmem_ld_x32_sync(tmem_base + lane_base + static_cast<uint32_t>(acc * BN + c * 32), r);
                     float v[32];
@@ -795,6 +884,13 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     epi_store_chunk(&tmD, warp_stage, nchunk, lane, v,
                                     static_cast<int32_t>(n_blk * BN + cbase + c * 32), static_cast<int32_t>(row0), M, N);
                 }
+            }
+        }
+        if constexpr (DACT) {
+            // no H load may still be landing in shared memory when the CTA exits
+            while (ldw < ldn) {
+                wait_phase_drain(lbar, ldw & 1);
+                ++ldw;
             }
         }
         // every store has finished reading shared memory (the writes to D
@@ -914,13 +1010,13 @@ struct LaunchInfo {
     int max_clusters = 0;  // co-resident 2-CTA clusters (PAIR only)
 };
 
-template <int BN, bool GROUP, bool PAIR, bool FUSED, bool EQ = false>
+template <int BN, bool GROUP, bool PAIR, bool FUSED, bool EQ = false, bool DACT = false>
 const LaunchInfo& launch_info() {
-    using C = KernelCfg<BN, GROUP, PAIR, FUSED, EQ>;
+    using C = KernelCfg<BN, GROUP, PAIR, FUSED, EQ, DACT>;
     static LaunchInfo info;
     static std::once_flag once;
     std::call_once(once, [] {
-        auto kern = fp8_gemm_kernel<BN, GROUP, PAIR, FUSED, EQ>;
+        auto kern = fp8_gemm_kernel<BN, GROUP, PAIR, FUSED, EQ, DACT>;
         info.attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
         if (PAIR && info.attr_err == cudaSuccess) {
             cudaLaunchConfig_t cfg = {};
@@ -952,12 +1048,13 @@ struct EpiQuantHost {
     EpiQuantArgs args;
 };
 
-template <int BN, bool GROUP, bool PAIR, bool FUSED, bool EQ = false>
+template <int BN, bool GROUP, bool PAIR, bool FUSED, bool EQ = false, bool DACT = false>
 int launch_gemm(const void* a, const void* b, const float* sa, const float* sb, void* d, int64_t M,
                 int64_t N, int64_t K, uint32_t afmt, uint32_t bfmt, int* status, cudaStream_t stream,
-                const FusedArgs& fz, const EpiQuantHost* eqh = nullptr) {
-    using C = KernelCfg<BN, GROUP, PAIR, FUSED, EQ>;
-    const LaunchInfo& info = launch_info<BN, GROUP, PAIR, FUSED, EQ>();
+                const FusedArgs& fz, const EpiQuantHost* eqh = nullptr, const void* h_in = nullptr,
+                int act = 0) {
+    using C = KernelCfg<BN, GROUP, PAIR, FUSED, EQ, DACT>;
+    const LaunchInfo& info = launch_info<BN, GROUP, PAIR, FUSED, EQ, DACT>();
     if (info.attr_err != cudaSuccess) return FP8Q_ERR_CUDA;
     alignas(64) CUtensorMap mapA, mapB, mapD, mapE1, mapE2;
     if (!make_kmajor_map(&mapA, a, M, K, BM) || !make_kmajor_map(&mapB, b, N, K, C::B_BOX)) return FP8Q_ERR_CUDA;
@@ -977,10 +1074,15 @@ int launch_gemm(const void* a, const void* b, const float* sa, const float* sb, 
         if (!make_out_map(&mapD, d, M, N)) return FP8Q_ERR_CUDA;
         mapE1 = mapD;
         mapE2 = mapD;
+        if constexpr (DACT) {
+            // H [M,N] (BF16), loaded in the same 32 x 32 boxes the output is stored in
+            if (!make_out_map(&mapE1, const_cast<void*>(h_in), M, N)) return FP8Q_ERR_CUDA;
+            eq.act = act;
+        }
     }
     const int64_t tiles = ((M + C::TILE_M - 1) / C::TILE_M) * ((N + BN - 1) / BN);
     const uint32_t idesc = idesc_f8(afmt, bfmt, C::MMA_M, C::MMA_N);
-    auto kern = fp8_gemm_kernel<BN, GROUP, PAIR, FUSED, EQ>;
+    auto kern = fp8_gemm_kernel<BN, GROUP, PAIR, FUSED, EQ, DACT>;
     if constexpr (PAIR) {
         if (info.max_clusters < 1) return FP8Q_ERR_CUDA;
         const int clusters = static_cast<int>(FUSED ? info.max_clusters : std::min<int64_t>(tiles, info.max_clusters));
@@ -1146,6 +1248,50 @@ Shape pick_shape_eq(int64_t M, int64_t N) {
     return best;
 }
 
+// Tile for the dgrad with the activation backward: the plain GEMM's widths
+// except 384 and 160, scored like pick_shape.  A tile override names one of
+// these or is ignored.
+Shape pick_shape_dact(int64_t M, int64_t N) {
+    const int ov = g_tile_override.load(std::memory_order_relaxed);
+    if (ov >= 0) {
+        const bool pair = (ov >> 16) != 0;
+        const int bn = ov & 0xFFFF;
+        if (bn == 128 || bn == 192 || bn == 256 || (pair && bn == 224)) return Shape{pair && M > BM, bn == 224 && M <= BM ? 256 : bn};
+    }
+    struct Cand { bool pair; int bn; double t; };
+    static constexpr Cand kCands[] = {{true, 256, 1.000}, {true, 224, 0.946}, {true, 192, 0.909}, {true, 128, 0.858},
+                                      {false, 192, 0.897}, {false, 128, 0.843}, {false, 256, 1.102}};
+    const int64_t sms = sm_count();
+    Shape best{false, 128};
+    double best_cost = -1.0;
+    for (const Cand& c : kCands) {
+        if (c.pair && M <= BM) continue;
+        const int64_t tile_m = c.pair ? 2 * BM : BM;
+        const int64_t units = c.pair ? sms / 2 : sms;
+        const int64_t tiles = ((M + tile_m - 1) / tile_m) * ((N + c.bn - 1) / c.bn);
+        const double cost = static_cast<double>((tiles + units - 1) / units) * c.t;
+        if (best_cost < 0 || cost < best_cost) { best_cost = cost; best = Shape{c.pair, c.bn}; }
+    }
+    return best;
+}
+
+int launch_dact(const Shape& s, const void* a, const void* b, const float* sa, const float* sb, void* d, int64_t M,
+                int64_t N, int64_t K, const void* h, int act, int* status, cudaStream_t stream) {
+#define FP8Q_LAUNCH_DACT(BNV, PR) \
+    return launch_gemm<BNV, false, PR, false, false, true>(a, b, sa, sb, d, M, N, K, FP8Q_E5M2, FP8Q_E4M3, status, \
+                                                           stream, FusedArgs{}, nullptr, h, act)
+    if (s.pair) {
+        if (s.bn == 256) FP8Q_LAUNCH_DACT(256, true);
+        if (s.bn == 224) FP8Q_LAUNCH_DACT(224, true);
+        if (s.bn == 192) FP8Q_LAUNCH_DACT(192, true);
+        FP8Q_LAUNCH_DACT(128, true);
+    }
+    if (s.bn == 256) FP8Q_LAUNCH_DACT(256, false);
+    if (s.bn == 192) FP8Q_LAUNCH_DACT(192, false);
+    FP8Q_LAUNCH_DACT(128, false);
+#undef FP8Q_LAUNCH_DACT
+}
+
 int launch_eq(const Shape& s, const void* a, const void* b, const float* sa, const float* sb, void* h,
               int64_t M, int64_t N, int64_t K, int* status, cudaStream_t stream, const EpiQuantHost& e) {
 #define FP8Q_LAUNCH_EQ(BNV, PR) \
@@ -1224,6 +1370,19 @@ extern "C" int fp8_upproj_fwd(const void* x_q, const void* wt_q, const float* sc
     if (M == 0) return FP8Q_OK;
     const EpiQuantHost e{act_out, h_q, EpiQuantArgs{scale_h, amax_out, sat_count, act, 0, 0}};
     return launch_eq(pick_shape_eq(M, N), x_q, wt_q, scale_x, scale_w, h_out, M, N, K, status, stream, e);
+}
+
+extern "C" int fp8_gemm_dgrad_act(const void* dy_q, const void* w_q, const float* scale_dy, const float* scale_w,
+                                  const void* h, int act, void* dh, int64_t M, int64_t N, int64_t K, int* status,
+                                  cudaStream_t stream) {
+    // D = dH [M,K], A = dY [M,N] (contraction N), B = W [K,N]; H [M,K] read in the epilogue
+    if (act < FP8Q_ACT_IDENTITY || act > FP8Q_ACT_RELU2) return FP8Q_ERR_UNSUPPORTED;
+    if (h == nullptr && M != 0) return FP8Q_ERR_NULL;
+    if (!aligned16(h)) return FP8Q_ERR_ALIGN;
+    int st = check_gemm_args(dy_q, w_q, scale_dy, scale_w, dh, M, K, N, status);
+    if (st != FP8Q_OK) return st;
+    if (M == 0) return FP8Q_OK;
+    return launch_dact(pick_shape_dact(M, K), dy_q, w_q, scale_dy, scale_w, dh, M, K, N, h, act, status, stream);
 }
 
 extern "C" int fp8_gemm_wgrad(const void* x_q_t, const void* dy_q_t, const float* scale_x,

@@ -102,6 +102,14 @@ def test_gemm_argument_checks(lib):
     assert dg(A, A, A, A, A, 128, 24, 256, None, None) == ERR_SHAPE      # contraction N % 16
     assert dg(A, A, A, A, None, 128, 32, 256, None, None) == ERR_NULL
     assert dg(A, A, A, A, A, 128, 32, 256, None, None) == ERR_UNSUPPORTED
+    da = lib.fp8_gemm_dgrad_act
+    da.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_int, ctypes.c_void_p] + [ctypes.c_int64] * 3 + [ctypes.c_void_p] * 2
+    da.restype = ctypes.c_int
+    assert da(A, A, A, A, A, 3, A, 128, 32, 256, None, None) == ERR_UNSUPPORTED   # act
+    assert da(A, A, A, A, None, 2, A, 128, 32, 256, None, None) == ERR_NULL       # h
+    assert da(A, A, A, A, A + 8, 2, A, 128, 32, 256, None, None) == ERR_ALIGN     # h alignment
+    assert da(A, A, A, A, A, 2, A, 128, 24, 256, None, None) == ERR_SHAPE         # contraction N % 16
+    assert da(A, A, A, A, A, 2, A, 128, 32, 256, None, None) == ERR_UNSUPPORTED   # no sm_103 device here
     wg = lib.fp8_gemm_wgrad
     wg.argtypes = [ctypes.c_void_p] * 5 + [ctypes.c_int64] * 3 + [ctypes.c_void_p] * 2
     wg.restype = ctypes.c_int

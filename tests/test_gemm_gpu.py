@@ -12,7 +12,7 @@ import torch
 
 import oracle as O
 from quantize_fp8_gemm_gb300 import binding as B
-from tests.parity import assert_gemm_close, dev_f32, dev_u8
+from tests.parity import assert_gemm_close, dev_bf16, dev_f32, dev_u8
 
 pytestmark = pytest.mark.gpu
 
@@ -84,6 +84,54 @@ def test_fwd_shapes(M, N, K):
     Yr, S = O.gemm_fwd(xq, wq, sx, sw)
     y = run_fwd(xq, wq, sx, sw)
     assert_gemm_close(y, Yr, S)
+
+
+def run_dgrad_act(dyq, wq, sdy, sw, h_bits, act):
+    M = dyq.shape[0]
+    K = wq.shape[0]
+    dh = torch.empty(M, K, dtype=torch.bfloat16, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.fp8_gemm_dgrad_act(dev_u8(dyq), dev_u8(wq), dev_f32(sdy), dev_f32(sw), dev_bf16(h_bits), dh, act=act, status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    return dh
+
+
+def _dgrad_act_operands(M, N, K, seed):
+    rng = np.random.default_rng(seed)
+    dyq = _codes(rng.standard_normal((M, N)) * 1000.0, O.E5M2)
+    wq = rand_e4m3((K, N), seed=seed + 1, scale=50.0)
+    h = O.f32_to_bf16((rng.standard_normal((M, K)) * 2.0).astype(np.float32))
+    return dyq, wq, h
+
+
+@pytest.mark.parametrize("act", [B.ACT_RELU2, B.ACT_RELU])
+@pytest.mark.parametrize("M,N,K", [(130, 160, 272), (520, 768, 400), (300, 1600, 640), (64, 64, 3072)])
+def test_dgrad_act_against_oracle(M, N, K, act):
+    """dH = dX * act'(H) in the dgrad epilogue: within the GEMM tolerance of
+    the oracle's double dX times act'(h) (S scaled by |act'(h)|)."""
+    dyq, wq, h = _dgrad_act_operands(M, N, K, seed=M + N + K + act)
+    ref, S = O.gemm_dgrad_act(dyq, wq, 1024.0, 5.0, h, {B.ACT_RELU2: O.ACT_RELU2, B.ACT_RELU: O.ACT_RELU}[act])
+    assert_gemm_close(run_dgrad_act(dyq, wq, 1024.0, 5.0, h, act), ref, S)
+
+
+@pytest.mark.parametrize("pair,bn", [(0, 128), (0, 192), (0, 256), (1, 128), (1, 192), (1, 224), (1, 256)])
+def test_dgrad_act_identity_is_the_dgrad_on_every_tile(pair, bn):
+    """With the identity the factor is 1: dH equals fp8_gemm_dgrad's dX bit for
+    bit on the same tile, and ReLU^2 stays in tolerance, on a ragged problem."""
+    M, N, K = 300, 272, 400
+    dyq, wq, h = _dgrad_act_operands(M, N, K, seed=bn + pair)
+    try:
+        B.fp8q_gemm_set_tile(pair, bn)
+        dh = run_dgrad_act(dyq, wq, 1024.0, 5.0, h, B.ACT_IDENTITY)
+        dx = torch.empty(M, K, dtype=torch.bfloat16, device="cuda")
+        B.fp8_gemm_dgrad(dev_u8(dyq), dev_u8(wq), dev_f32(1024.0), dev_f32(5.0), dx)
+        torch.cuda.synchronize()
+        assert torch.equal(dh.view(torch.int16), dx.view(torch.int16))
+        ref, S = O.gemm_dgrad_act(dyq, wq, 1024.0, 5.0, h, O.ACT_RELU2)
+        assert_gemm_close(run_dgrad_act(dyq, wq, 1024.0, 5.0, h, B.ACT_RELU2), ref, S)
+    finally:
+        B.fp8q_gemm_set_tile(-1)
 
 
 def run_wgrad(xq, dyq, sx, sdy):

@@ -446,6 +446,31 @@ def test_gemm_wgrad_is_x_transposed_times_dy():
     assert np.array_equal(dWr, dW[rows])
 
 
+def test_dgrad_act_closed_forms():
+    """dH = dX * act'(H): identity reduces to the dgrad; ReLU gates it by h > 0
+    (so -0, 0 and negatives give 0); ReLU^2 scales it by 2h; rows select."""
+    rng = np.random.default_rng(25)
+    M, N, K = 9, 48, 20
+    dY = _codes(rng.standard_normal((M, N)) * 100, O.E5M2)
+    W = _codes(rng.standard_normal((K, N)), O.E4M3)
+    dX, S = O.gemm_dgrad(dY, W, 2.0, 8.0)
+    hv = rng.standard_normal((M, K)).astype(np.float32)
+    hv[0, :4] = [0.0, -0.0, -1.0, 3.0]
+    h = O.f32_to_bf16(hv)
+    d0, s0 = O.gemm_dgrad_act(dY, W, 2.0, 8.0, h, O.ACT_IDENTITY)
+    assert np.array_equal(d0, dX) and np.array_equal(s0, S)
+    hf = O.bf16_to_f32(h).astype(np.float64)
+    d1, _ = O.gemm_dgrad_act(dY, W, 2.0, 8.0, h, O.ACT_RELU)
+    assert np.array_equal(d1, np.where(hf > 0, dX, 0.0))
+    assert np.array_equal(d1[0, :3], [0.0, 0.0, 0.0]) and d1[0, 3] == dX[0, 3]
+    d2, s2 = O.gemm_dgrad_act(dY, W, 2.0, 8.0, h, O.ACT_RELU2)
+    assert np.array_equal(d2, np.where(hf > 0, 2.0 * hf * dX, 0.0))
+    assert np.array_equal(s2, S * np.where(hf > 0, 2.0 * hf, 0.0))
+    rows = np.array([4, 0], np.int64)
+    dr, _ = O.gemm_dgrad_act(dY, W, 2.0, 8.0, h, O.ACT_RELU2, rows=rows)
+    assert np.array_equal(dr, d2[rows])
+
+
 def test_group_gemm_reductions():
     """Group mode: equal scales reduce to per-tensor; power-of-two scales that
     differ per row, per 128-slice of K and per 128-block of N reduce to numpy's
