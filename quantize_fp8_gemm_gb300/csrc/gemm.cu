@@ -9,9 +9,14 @@
 // the 1x128 / 128x128 scale groups of Trade-offs and edge cases, whose partial
 // sums are promoted into FP32 registers once per 128-long slice.
 //
-// Both GEMMs are D[M,N] = A[M,K] . B[N,K]^T with A and B K-major:
+// Every GEMM here is D[M,N] = A[M,K] . B[N,K]^T with A and B K-major:
 //   forward: A = X_q [M,K],   B = W_q^T [N,K]
 //   dgrad:   A = dY_q [M,N],  B = W_q [K,N]   (the contraction runs over N)
+//   wgrad:   A = X_q^T [K,M], B = dY_q^T [N,M] (the contraction runs over the tokens)
+// Epilogue modes besides the plain dequantise-and-store: the 1x128 / 128x128
+// group promotion (GROUP), the activation quantize of the next layer's input
+// (EQ: the up-projection), the activation backward dH = dX act'(H) (DACT), and
+// the one-launch step's extra quantize warps (FUSED).
 //
 // CTA = 6 warps (10 with 8 epilogue warps), persistent over output tiles
 // (static round robin):
@@ -36,6 +41,11 @@
 //
 // Every mbarrier wait is bounded; on time-out the CTA sets FP8Q_DEV_TIMEOUT,
 // waits (bounded) for its copies and MMAs in flight, frees TMEM and exits.
+//
+// "FP8 Training & Inference", FP8 Training Recipe also defines the weight
+// gradient (E4M3 activation x E5M2 gradient); "Paradigma Details FP8 and
+// Optimizer Tricks Behind NanoGPT Records", second paragraph, places the
+// quantize in the epilogue of the computation that produces its input.
 #include "common.cuh"
 #include "quant_ops.cuh"
 #include "history_ops.cuh"
