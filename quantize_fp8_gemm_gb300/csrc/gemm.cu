@@ -76,13 +76,17 @@ constexpr int kUnitRows = 16;   // rows per quantize unit in the full rounds
 constexpr int kQuantBatch = 8;  // 16-byte loads in flight per quantize thread
 
 // Epilogue warps: 8 where the epilogue is exposed -- group mode (a promotion
-// per 128-long K slice) and the 384-wide tile (one accumulator, so its drain is
+// per 128-long K slice; 12 and 16 on its 192- and 256-wide tiles, 64 columns
+// per warp) and the 384-wide tile (one accumulator, so its drain is
 // not hidden behind the next tile; 17.2 -> 16.4 us at 8192 x 3072 -> 768) --
 // else 4 (8 would take a stage of the operand ring: 87.6 -> 92.6 us at 65536
 // rows with 256-wide tiles) -- and the activation-quantize epilogue (EQ),
 // whose per-element work is several times a plain epilogue's.
 template <int BN, bool GROUP, bool FUSED, bool EQ = false>
-constexpr int epi_warps() { return !FUSED && (GROUP || EQ || BN > 256) ? kWideEpiWarps : kEpiWarps; }
+constexpr int epi_warps() {
+    // group mode on 192 / 256-wide tiles: three / four promotion warps per lane quarter, 64 columns each
+    return GROUP && BN == 256 ? 16 : GROUP && BN == 192 ? 12 : !FUSED && (GROUP || EQ || BN > 256) ? kWideEpiWarps : kEpiWarps;
+}
 
 template <int BN, bool GROUP, bool FUSED, bool EQ = false>
 constexpr int gemm_threads() {
@@ -576,7 +580,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     static_assert(!DACT || (!GROUP && !FUSED && !EQ), "the activation backward runs in the per-tensor dgrad epilogue");
     static_assert(!EQ || (!GROUP && !FUSED && BN % 64 == 0 && BN <= 256),
                   "the activation-quantize epilogue: per-tensor tiles of whole 64-column pairs, two accumulators");
-    static_assert(!GROUP || (BN == 128 && !PAIR), "group mode uses 1-CTA 128-wide tiles");
+    static_assert(!GROUP || ((BN == 128 || BN == 192 || BN == 256) && !PAIR), "group mode uses 1-CTA tiles, 128-256 wide");
     static_assert(!(GROUP && FUSED), "the fused quantize feeds the per-tensor GEMM");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -845,7 +849,11 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 // warp (warp - 2) / 4 of its lane quarter promotes columns cbase..cbase + GC - 1,
                 // all in one 128-column block of B's scales
                 constexpr int GC = BN / (C::EPI_WARPS / 4);
-                constexpr int LDB = GC > 64 ? 1 : GC / 32;  // x32 TMEM loads per wait (1 or 2)
+                // x32 TMEM loads per wait (1 or 2); with 12 or 16 warps (a 128- or 96-register
+                // cap) x16 loads, one per wait, so the 64 sums and one load fit without spills
+                constexpr bool X16 = C::EPI_WARPS > 8;
+                constexpr int LDB = X16 ? 1 : GC > 64 ? 1 : GC / 32;
+                constexpr int LDW = X16 ? 16 : 32;  // columns per load
                 static_assert(!GROUP || (GC <= 128 && 128 % GC == 0), "a warp's columns share one block scale");
                 const int cbase = ((warp - 2) / 4) * GC;
                 const int64_t nb_raw = (n_blk * BN + cbase) / 128;
@@ -862,8 +870,24 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     ok = __all_sync(0xFFFFFFFFu, ok);
                     if (!ok) break;
                     tc_fence_after();
+                    if constexpr (X16) {
 #pragma unroll
-                    for (int c0 = 0; c0 < GC / 32; c0 += LDB) {
+                        for (int l = 0; l < GC / LDW; ++l) {
+                            uint32_t r16[16];
+                            tmem_ld_x16_sync(tmem_base + lane_base + static_cast<uint32_t>(acc * BN + cbase + l * 16), r16);
+                            if (l + 1 == GC / LDW) {
+                                // the accumulator is in registers: the MMA may reuse it
+                                tc_fence_before();
+                                __syncwarp();
+                                if (lane == 0) mbar_arrive(tempty0 + 8u * acc);
+                            }
+#pragma unroll
+                            for (int j = 0; j < 16; ++j)
+                                sum[l * 16 + j] = fmaf(__uint_as_float(r16[j]), ginv, sum[l * 16 + j]);
+                        }
+                    }
+#pragma unroll
+                    for (int c0 = 0; c0 < (X16 ? 0 : GC / 32); c0 += LDB) {
                         uint32_t r[LDB][32];
                         const uint32_t ta = tmem_base + lane_base + static_cast<uint32_t>(acc * BN + cbase + c0 * 32);
                         if constexpr (LDB == 2) tmem_ld_2x32_sync(ta, ta + 32, r[0], r[1]);
@@ -1176,12 +1200,40 @@ Shape pick_shape(int64_t M, int64_t N, bool wide) {
     return best;
 }
 
+// Group-mode tile width (1-CTA tiles, four accumulators' worth of TMEM): 128
+// with 8 promotion warps, 192 with 12 or 256 with 16 (64 columns per warp, so
+// each warp stays inside one 128-column scale block).  Scored like pick_shape,
+// with per-tile times relative to the 128-wide tile from sweeps of the three
+// widths over the workloads' shapes on GB300 (8192 to 131072 rows, N 768 to
+// 1600).  A tile override (0, 128), (0, 192) or (0, 256) pins it.
+int pick_group_bn(int64_t M, int64_t N) {
+    const int ov = g_tile_override.load(std::memory_order_relaxed);
+    if (ov >= 0 && (ov >> 16) == 0 && ((ov & 0xFFFF) == 256 || (ov & 0xFFFF) == 192 || (ov & 0xFFFF) == 128))
+        return ov & 0xFFFF;
+    struct Cand { int bn; double t; };
+    static constexpr Cand kCands[] = {{128, 1.000}, {192, 1.200}, {256, 1.550}};
+    const int64_t sms = sm_count();
+    int best = 128;
+    double best_cost = -1.0;
+    for (const Cand& c : kCands) {
+        const int64_t tiles = ((M + BM - 1) / BM) * ((N + c.bn - 1) / c.bn);
+        const double cost = static_cast<double>((tiles + sms - 1) / sms) * c.t;
+        if (best_cost < 0 || cost < best_cost) { best_cost = cost; best = c.bn; }
+    }
+    return best;
+}
+
 template <bool FUSED>
 int gemm_dispatch_t(const void* a, const void* b, const float* sa, const float* sb, int group, void* d,
                     int64_t M, int64_t N, int64_t K, uint32_t afmt, uint32_t bfmt, int* status,
                     cudaStream_t stream, const FusedArgs& fz) {
     if constexpr (!FUSED) {
         if (group) {
+            const int gbn = pick_group_bn(M, N);
+            if (gbn == 256)
+                return launch_gemm<256, true, false, false>(a, b, sa, sb, d, M, N, K, afmt, bfmt, status, stream, fz);
+            if (gbn == 192)
+                return launch_gemm<192, true, false, false>(a, b, sa, sb, d, M, N, K, afmt, bfmt, status, stream, fz);
             return launch_gemm<128, true, false, false>(a, b, sa, sb, d, M, N, K, afmt, bfmt, status, stream, fz);
         }
     }

@@ -198,12 +198,12 @@ def test_group_scaled_fwd(M, N, K):
     assert_gemm_close(y, Yr, S)
 
 
-GROUP_TILES = [(0, 128)]
+GROUP_TILES = [(0, 128), (0, 192), (0, 256)]
 
 
 @pytest.mark.parametrize("pair,bn", GROUP_TILES)
 def test_group_scaled_every_tile(pair, bn):
-    """Group-scaled forward on each group-mode tile (1-CTA 128 and 256 wide)
+    """Group-scaled forward on each group-mode tile (1-CTA, 128, 192 and 256 wide)
     over problems whose M and N leave partial tiles; N = 640 puts a 256-wide
     tile's last scale block past N."""
     try:
