@@ -134,8 +134,15 @@ struct EpiQuantArgs {
     int has_h, has_act;             // store H (through tmD) / the activation (through tmE1)
 };
 
+// Shared memory the operand ring and the epilogue staging share by default;
+// the 256-wide group tile, whose staging is single-buffered, takes all but the
+// barrier area, the alignment slack and 512 bytes for the kernel's static
+// shared memory.
+constexpr int kRingTotal = 220 * 1024;
+constexpr int kGroupRingTotal = 232448 - 256 - 1024 - 512;
+
 template <int BN, bool PAIR, int EPI = kEpiWarps, int ACC = (2 * BN <= 512 ? 2 : 1),
-          int STAGE_PER_WARP = 2 * kEpiChunkBytes>
+          int STAGE_PER_WARP = 2 * kEpiChunkBytes, int RING_TOTAL = kRingTotal>
 struct Cfg {
     // A tile wider than 256 columns takes two MMAs per k-step (N <= 256 each)
     // into one accumulator; B then arrives as one box per MMA.
@@ -151,7 +158,7 @@ struct Cfg {
     static constexpr int EPI_WARPS = EPI;
     static constexpr int EPI_STAGE = STAGE_PER_WARP;          // store staging per epilogue warp
     static constexpr int EPI_BYTES = EPI * STAGE_PER_WARP;
-    static constexpr int RING_BUDGET = 220 * 1024 - EPI_BYTES;
+    static constexpr int RING_BUDGET = RING_TOTAL - EPI_BYTES;
     static constexpr int STAGES = RING_BUDGET / STAGE_BYTES < 8 ? RING_BUDGET / STAGE_BYTES : 8;
     static constexpr int TMEM_COLS = (ACCS * BN <= 256) ? 256 : 512;  // power of 2
     static constexpr int BAR_BYTES = 256;
@@ -170,7 +177,11 @@ struct Cfg {
 };
 
 // Group mode promotes every 128-long K slice, so it keeps as many
-// accumulators as TMEM holds: the MMAs run up to three slices ahead.
+// accumulators as TMEM holds: the MMAs run up to three slices ahead (one at
+// 192 and 256 wide).  Its stores come once per tile; on the 256-wide tile
+// each warp stages them in one 2 KB block and the operand ring takes the
+// rest, 4 stages instead of 3 (85.5 against 93.7 us at 16384 x 4096 -> 1024;
+// at 192 wide a fifth stage did not pay for the single staging block).
 // EQ (the activation-quantize epilogue) stages two outputs per warp: the
 // activation (BF16) and the E4M3 codes (64-column boxes), each double-buffered;
 // H, when asked for, goes through the activation's buffer first.
@@ -179,7 +190,8 @@ struct Cfg {
 // BN / 16 KB per warp, keeping each warp's buffers 1024-byte aligned.
 template <int BN, bool GROUP, bool PAIR, bool FUSED, bool EQ = false, bool DACT = false>
 using KernelCfg = Cfg<BN, PAIR, epi_warps<BN, GROUP, FUSED, EQ>(), GROUP ? 512 / BN : (2 * BN <= 512 ? 2 : 1),
-                      EQ ? 4 * kEpiChunkBytes : DACT ? (5 + BN / 16) * 1024 : 2 * kEpiChunkBytes>;
+                      EQ ? 4 * kEpiChunkBytes : DACT ? (5 + BN / 16) * 1024 : GROUP && BN == 256 ? kEpiChunkBytes : 2 * kEpiChunkBytes,
+                      GROUP && BN == 256 ? kGroupRingTotal : kRingTotal>;
 
 // Next accumulator (of ACCS) and the phase its barriers are in.
 template <int ACCS>
@@ -374,15 +386,17 @@ __device__ __forceinline__ void fused_quantize(const FusedArgs& fz, const float*
 // it with one TMA store; the box is clipped at the edges of D.  Two staging
 // buffers per warp alternate; a buffer is reused once the store issued from
 // it two chunks earlier has finished reading it.
+template <int NBUF = 2>
 __device__ __forceinline__ void epi_store_chunk(const CUtensorMap* tmD, uint8_t* warp_stage, int& nchunk,
                                                 int lane, const float (&v)[32], int32_t col0, int32_t row0,
                                                 int64_t M, int64_t N) {
+    static_assert(NBUF == 1 || NBUF == 2, "one or two staging blocks per warp");
     // A box wholly outside D is skipped outright: nchunk counts committed
     // store groups, so the wait below covers the store that last read `buf`.
     if (row0 >= M || col0 >= N) return;
-    uint8_t* buf = warp_stage + (nchunk & 1) * kEpiChunkBytes;
-    if (nchunk >= 2) {
-        if (lane == 0) bulk_wait_group_read<1>();
+    uint8_t* buf = warp_stage + (NBUF == 2 ? (nchunk & 1) * kEpiChunkBytes : 0);
+    if (nchunk >= NBUF) {
+        if (lane == 0) bulk_wait_group_read<NBUF - 1>();
         __syncwarp();
     }
     const int sw = (lane >> 1) & 3;
@@ -915,7 +929,8 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     float v[32];
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v[j] = sum[c * 32 + j];
-                    epi_store_chunk(&tmD, warp_stage, nchunk, lane, v,
+                    // one staging block per warp: these stores come once per tile
+                    epi_store_chunk<C::EPI_STAGE / kEpiChunkBytes>(&tmD, warp_stage, nchunk, lane, v,
                                     static_cast<int32_t>(n_blk * BN + cbase + c * 32), static_cast<int32_t>(row0), M, N);
                 }
             }
@@ -1211,7 +1226,7 @@ int pick_group_bn(int64_t M, int64_t N) {
     if (ov >= 0 && (ov >> 16) == 0 && ((ov & 0xFFFF) == 256 || (ov & 0xFFFF) == 192 || (ov & 0xFFFF) == 128))
         return ov & 0xFFFF;
     struct Cand { int bn; double t; };
-    static constexpr Cand kCands[] = {{128, 1.000}, {192, 1.200}, {256, 1.550}};
+    static constexpr Cand kCands[] = {{128, 1.000}, {192, 1.200}, {256, 1.500}};
     const int64_t sms = sm_count();
     int best = 128;
     double best_cost = -1.0;
