@@ -458,8 +458,8 @@ int amax_history_update_ex(float* history, int L, int* head, const float* amax_n
  * fp8q_gemm_set_tile -- pin the GEMM tile shape (a tuning knob; "FP8 training:
  * what it is and how it works", Trade-offs and edge cases: tile size is a
  * tuning knob).  Process-wide; affects later per-tensor fp8_gemm_fwd /
- * fp8_gemm_dgrad calls (the group-scaled GEMM always uses 1-CTA 128-wide
- * tiles).
+ * fp8_gemm_dgrad calls.  The group-scaled GEMM takes the pins (0, 128),
+ * (0, 192) and (0, 256) and ignores others.
  *   pair  -1: automatic choice (the default; bn ignored)
  *          0: one CTA per 128 x bn tile           bn in {128, 160, 192, 256}
  *          1: a CTA pair per 256 x bn tile (2-SM)  bn in {128, 160, 192, 224, 256, 384}
