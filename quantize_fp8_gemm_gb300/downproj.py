@@ -17,12 +17,28 @@ end of the step, so the GEMM dequantises with the scale actually used.
 """
 from __future__ import annotations
 
+import numpy as np
 import torch
 
 from . import binding as B
 
 
 FUSED_MIN_ROWS = 32768  # default switch to the fused kernel (per-tensor scales)
+
+RECOMPUTE_X, RECOMPUTE_W = 1, 2  # recompute_on_overflow(): which operand was cast again
+
+
+def fp8_overflow(sat_x: int, amax_w: float, scale_w: float, fmt: int = B.E4M3) -> tuple[bool, bool]:
+    """Whether a step's casts overflowed their delayed scales ("FP8 Training &
+    Inference", Delayed Scaling: a scale too large for the step's values is
+    detected and the step recomputed with a corrected scale).  The casts
+    saturate instead of producing infinities, so the signal is a value past
+    the format's maximum: for X the quantize's saturation count, for W its
+    largest value, |v| = fp32(amax_w * s_w) with the cast's own rounded
+    product, against the maximum (448 for E4M3, 57344 for E5M2)."""
+    fmax = np.float32(448.0 if fmt == B.E4M3 else 57344.0)
+    w_over = bool(np.float32(amax_w) * np.float32(scale_w) > fmax)
+    return int(sat_x) > 0, w_over
 
 
 class DelayedScale:
@@ -143,6 +159,16 @@ class Fp8DownProj:
         self.w_q = torch.empty(K, N, dtype=torch.uint8, device=dev) if with_dgrad else None
         self.y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
         self.gemm_status = torch.zeros(1, dtype=torch.int32, device=dev)
+        # recompute_on_overflow(): one-entry histories that turn this step's own
+        # amax into a corrected scale, and the scratch amax / count of the re-cast
+        self._fix_hist = torch.zeros(2, dtype=torch.float32, device=dev)
+        self._fix_head = torch.zeros(2, dtype=torch.int32, device=dev)
+        self._fix_scale = torch.ones(2, dtype=torch.float32, device=dev)
+        self._fix_amax = torch.zeros(1, dtype=torch.float32, device=dev)
+        self._fix_sat = torch.zeros(1, dtype=torch.int64, device=dev)
+        self._fix_status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.x_scale_used = None  # after step(): the scales X_q / W_q were cast with
+        self.w_scale_used = None
         self.workspace = None
         if self.fused:
             # zero-filled once; the fused kernel leaves it zero
@@ -332,6 +358,50 @@ class Fp8DownProj:
     def capture(self, H: torch.Tensor, W: torch.Tensor, H_next: torch.Tensor | None = None) -> "StepGraph":
         """Capture the step as CUDA graphs on fixed buffers (see StepGraph)."""
         return StepGraph(self, H, W, H_next)
+
+    def recompute_on_overflow(self, H: torch.Tensor, W: torch.Tensor) -> int:
+        """Detect-and-recompute ("FP8 Training & Inference", Delayed Scaling:
+        when the delayed scale is too large for this step's values, detect it
+        and recompute with a corrected scale).  Call after step(H, W); reads
+        the step's saturation count and the weight's amax and scale back to
+        the host (one synchronisation).  If the quantize of H saturated, H is
+        cast again with the scale this step's own amax gives under the same
+        rule, 448 / fp32(margin * amax_t) (amax_history_update on a one-entry
+        history; the act copy is unchanged and not rewritten); likewise W
+        (both layouts) when its largest value passed 448.  The GEMM then runs
+        again on the new operands.  The delayed-scale state is untouched: the
+        history update of the step already holds amax_t, so the next step's
+        scale accounts for it.  Returns RECOMPUTE_X | RECOMPUTE_W for what
+        was cast again (0: nothing overflowed, Y stands); x_scale_used and
+        w_scale_used name the scales X_q and W_q now carry.  Group scales are
+        computed from each group's own values and never overflow: 0."""
+        sx_prev, sw_prev = self.x.scales[1 - self.x.slot:2 - self.x.slot], self.w.scales[1 - self.w.slot:2 - self.w.slot]
+        self.x_scale_used, self.w_scale_used = sx_prev, sw_prev
+        if self.group:
+            return 0
+        x_over, w_over = fp8_overflow(int(self.x.last_sat.item()), float(self.w.last_amax.item()),
+                                      float(sw_prev.item()))
+        if not (x_over or w_over):
+            return 0
+        redo = 0
+        if x_over:
+            sx = self._fix_scale[0:1]
+            B.amax_history_update_ex(self._fix_hist[0:1], self._fix_head[0:1], self.x.last_amax, self.x.margin,
+                                     B.E4M3, sx, scale_prev=sx_prev, status=self._fix_status)
+            B.fp8_quant_fused_ex(H, self.act, B.E4M3, sx, q_out=self.x_q, amax_out=self._fix_amax,
+                                 sat_count=self._fix_sat)
+            self.x_scale_used = sx
+            redo |= RECOMPUTE_X
+        if w_over:
+            sw = self._fix_scale[1:2]
+            B.amax_history_update_ex(self._fix_hist[1:2], self._fix_head[1:2], self.w.last_amax, self.w.margin,
+                                     B.E4M3, sw, scale_prev=sw_prev, status=self._fix_status)
+            B.fp8_quant_fused(W, B.ACT_IDENTITY, B.E4M3, sw, q_out=self.w_q, q_t_out=self.wt_q,
+                              amax_out=self._fix_amax)
+            self.w_scale_used = sw
+            redo |= RECOMPUTE_W
+        self.gemm(self.x_scale_used, self.w_scale_used)
+        return redo
 
     def calibrate(self, H: torch.Tensor, W: torch.Tensor) -> None:
         """Bootstrap the delayed scales from step 0's own tensors (one amax pass each).

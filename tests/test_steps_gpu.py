@@ -13,6 +13,7 @@ import torch
 import oracle as O
 from quantize_fp8_gemm_gb300 import binding as B
 from quantize_fp8_gemm_gb300 import workloads as WL
+from quantize_fp8_gemm_gb300 import downproj as dp_mod
 from quantize_fp8_gemm_gb300.downproj import Fp8DownProj
 from tests.parity import assert_gemm_close, host_u8
 
@@ -229,3 +230,87 @@ def test_row_blocks_match_one_block(chunks):
                                                              blk.act_bf16.view(torch.int16))
         assert one.sat.item() == blk.sat.item() and one.x.last_amax.item() == blk.x.last_amax.item()
         assert torch.equal(one.x.scale, blk.x.scale) and torch.equal(one.w.scale, blk.w.scale)
+
+
+# Detect-and-recompute ("FP8 Training & Inference", Delayed Scaling: a scale
+# too large for the step's values is detected and the step recomputed with a
+# corrected scale).
+def _scaled_bits(bits, factor):
+    """BF16 bits of factor * x (a power of two: exact)."""
+    return O.f32_to_bf16(O.bf16_to_f32(bits) * np.float32(factor))
+
+
+def _recompute_fixture(M, fused=False):
+    w = WL.WORKLOADS["gpt2s"]
+    W_bits = WL.w_down(w)
+    H0 = WL.h_preact(w, 0)[:M]
+    dp = Fp8DownProj(M, w.K, w.N, margin=w.margin, fused=fused, with_dgrad=True)
+    Wd = WL.bf16_tensor(W_bits).cuda()
+    dp.calibrate(WL.bf16_tensor(H0).cuda(), Wd)
+    y0 = dp.step(WL.bf16_tensor(H0).cuda(), Wd).clone()
+    assert dp.recompute_on_overflow(WL.bf16_tensor(H0).cuda(), Wd) == 0
+    return w, dp, W_bits, Wd, H0, y0
+
+
+@pytest.mark.parametrize("fused", [False, True])
+def test_recompute_after_activation_overflow(fused):
+    """H grows 8x in one step (its ReLU^2 64x): the delayed scale saturates
+    the cast; the recompute casts H again with 448 / fp32(margin * amax_t),
+    whose codes, count and GEMM match the oracle's for that scale."""
+    M = 2048
+    w, dp, W_bits, Wd, H0, _ = _recompute_fixture(M, fused)
+    H1 = _scaled_bits(H0, 8.0)
+    H1d = WL.bf16_tensor(H1).cuda()
+    dp.step(H1d, Wd)
+    assert dp.recompute_on_overflow(H1d, Wd) == dp_mod.RECOMPUTE_X
+    torch.cuda.synchronize()
+    amax_t = O.amax(H1, O.ACT_RELU2)
+    stale = O.quant(H1, O.ACT_RELU2, O.E4M3, float(dp.x.scales[1 - dp.x.slot].item()), want_act=False)
+    assert int(dp.x.last_sat.item()) == stale["sat"] > 0
+    s_fix = O.delayed_scale(amax_t, w.margin, O.E4M3)
+    assert float(dp.x_scale_used.item()) == s_fix
+    rx = O.quant(H1, O.ACT_RELU2, O.E4M3, s_fix, want_act=False)
+    assert np.array_equal(host_u8(dp.x_q), rx["q"])
+    assert int(dp._fix_sat.item()) == rx["sat"] == 0
+    s_w = float(dp.w_scale_used.item())
+    rw = O.quant(W_bits, O.ACT_IDENTITY, O.E4M3, s_w, want_act=False)
+    rows = WL.sample_rows(M, 64, seed=5)
+    Yr, S = O.gemm_fwd(rx["q"][rows], rw["q"], s_fix, s_w)
+    assert_gemm_close(dp.y, Yr, S, rows=rows)
+    assert int(dp.gemm_status.item()) == 0 and int(dp._fix_status.item()) == 0
+
+
+def test_recompute_after_weight_overflow():
+    """W grows 16x in one step: both of its layouts are cast again with the
+    corrected scale and the GEMM uses them."""
+    M = 2048
+    w, dp, W_bits, Wd, H0, _ = _recompute_fixture(M)
+    W1 = _scaled_bits(W_bits, 16.0)
+    W1d = WL.bf16_tensor(W1).cuda()
+    H0d = WL.bf16_tensor(H0).cuda()
+    dp.step(H0d, W1d)
+    assert dp.recompute_on_overflow(H0d, W1d) == dp_mod.RECOMPUTE_W
+    torch.cuda.synchronize()
+    s_fix = O.delayed_scale(O.amax(W1, O.ACT_IDENTITY), w.margin, O.E4M3)
+    assert float(dp.w_scale_used.item()) == s_fix
+    rw = O.quant(W1, O.ACT_IDENTITY, O.E4M3, s_fix, want_act=False)
+    assert np.array_equal(host_u8(dp.w_q), rw["q"])
+    assert np.array_equal(host_u8(dp.wt_q), np.ascontiguousarray(rw["q"].T))
+    s_x = float(dp.x_scale_used.item())
+    rx = O.quant(H0, O.ACT_RELU2, O.E4M3, s_x, want_act=False)
+    assert rx["sat"] == 0
+    rows = WL.sample_rows(M, 64, seed=6)
+    Yr, S = O.gemm_fwd(rx["q"][rows], rw["q"], s_x, s_fix)
+    assert_gemm_close(dp.y, Yr, S, rows=rows)
+
+
+def test_no_recompute_without_overflow():
+    """A step within its scales: nothing is cast again and Y stands."""
+    M = 2048
+    w, dp, W_bits, Wd, H0, _ = _recompute_fixture(M)
+    H1d = WL.bf16_tensor(WL.h_preact(w, 1)[:M]).cuda()
+    y = dp.step(H1d, Wd).clone()
+    q = dp.x_q.clone()
+    assert dp.recompute_on_overflow(H1d, Wd) == 0
+    torch.cuda.synchronize()
+    assert torch.equal(dp.y.view(torch.int16), y.view(torch.int16)) and torch.equal(dp.x_q, q)
