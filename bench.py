@@ -11,9 +11,8 @@ history updates.  The default workload is the GPT-2-small down-projection
 
 Timing: W untimed warm-up steps, then exactly K steps; before each step a
 256 MiB buffer is written and read back to flush L2 (outside the timed
-events); each step (a CUDA graph: the weight cast runs beside the quantize)
-is
-timed on its stream with CUDA events at the phase boundaries.  `value` is whole-job
+events); each step (a CUDA graph of the step's launches) is timed on its
+stream with CUDA events at the phase boundaries.  `value` is whole-job
 TFLOP/s (2 M N K per step and GPU) over the summed step times, max over ranks.
 `e2e` repeats the step through the same public API with H and W copied in
 from pinned host memory and Y copied back inside the timed region.
@@ -362,11 +361,11 @@ def run_ours(args, world, rank, local):
         dominant = roof_fused
 
     if dp.fused:
-        step_desc = "W cast, fused quantize + FP8 GEMM (one kernel), 2 history updates"
-        launches_per_step = 4
+        step_desc = "W cast, quantize of H, FP8 GEMM and the 2 history updates in one kernel"
+        launches_per_step = 1
     elif dp.chunks == 1:
-        step_desc = "W cast + quantize of H in one launch, FP8 GEMM, 2 history updates"
-        launches_per_step = 4
+        step_desc = "W cast + quantize of H in one launch, then the FP8 GEMM, which also runs the 2 history updates"
+        launches_per_step = 2
     else:
         step_desc = f"W cast, {dp.chunks} x (row-block quantize + its GEMM), 2 history updates"
         launches_per_step = 3 + 2 * dp.chunks

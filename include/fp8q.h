@@ -385,6 +385,38 @@ int fp8_downproj_fwd_ex(const void* h, const void* w, void* wt_q, int64_t M, int
                         unsigned flags, int* status, cudaStream_t stream);
 
 /*
+ * fp8_gemm_fwd_update -- fp8_gemm_fwd (per-tensor scales) that also runs the
+ * step's delayed-scale updates  [gemms][scale]
+ *
+ * The same Y = (X_q . W_q) / (s_x s_w).  In addition, one warp of the first
+ * CTA runs amax_history_update_ex with hist_x on amax_x and with hist_w on
+ * amax_w while the first tile's products accumulate ("Paradigma Details FP8
+ * and Optimizer Tricks Behind NanoGPT Records", second paragraph: the next
+ * step's scale comes from this step's maximum, so it is computed beside this
+ * step's GEMM and nothing waits for it).  The amax values must be final when
+ * the GEMM starts (the casts that wrote them enqueued before it on `stream`).
+ *   x_q, wt_q, scale_x, scale_w, y, M, N, K, status  as for fp8_gemm_fwd with
+ *           group_mode 0.
+ *   amax_x, hist_x / amax_w, hist_w  device float and the arguments of
+ *           amax_history_update_ex for that tensor (amax_new = the float), or
+ *           NULL history arguments for no update.  An update must write a
+ *           scale other than scale_x and scale_w, and clear an amax other than
+ *           amax_x and amax_w (the two-slot layout: this step's scales are
+ *           read while the next step's are written).  The structs are read
+ *           during the call only.
+ * Results equal fp8_gemm_fwd followed by the amax_history_update_ex calls.
+ * Errors: those of fp8_gemm_fwd and amax_history_update_ex; FP8Q_ERR_SHAPE
+ * for an update that would write scale_x / scale_w or clear amax_x / amax_w,
+ * or for M == 0 with an update (nothing is launched to run it).
+ */
+int fp8_gemm_fwd_update(const void* x_q, const void* wt_q,
+                        const float* scale_x, const float* scale_w,
+                        void* y, int64_t M, int64_t N, int64_t K,
+                        float* amax_x, const fp8q_history_args* hist_x,
+                        float* amax_w, const fp8q_history_args* hist_w,
+                        int* status, cudaStream_t stream);
+
+/*
  * fp8_downproj_fwd_noalloc -- fp8_downproj_fwd without a caller workspace
  *
  * No counterpart in the method's sources: a variant for callers that must

@@ -49,6 +49,7 @@ def lib() -> ctypes.CDLL:
         L.fp8_quant_fused.argtypes = [P, i64, i64, i32, i32, P, P, P, P, P, P, P, i32, P]
         L.fp8_quant_fused_ex.argtypes = [P, i64, i64, i32, i32, P, P, P, P, P, P, P, i32, ctypes.c_uint, P]
         L.fp8_gemm_fwd.argtypes = [P, P, P, P, i32, P, i64, i64, i64, P, P]
+        L.fp8_gemm_fwd_update.argtypes = [P, P, P, P, P, i64, i64, i64, P, P, P, P, P, P]
         L.fp8_quant_fused_batch.argtypes = [P, i32, P]
         L.fp8_cast_f32.argtypes = [P, P, i64, i32, P]
         L.fp8_gemm_dgrad.argtypes = [P, P, P, P, P, i64, i64, i64, P, P]
@@ -74,7 +75,7 @@ def lib() -> ctypes.CDLL:
         L.fp8q_gemm_set_tile.argtypes = [i32, i32]
         L.fp8q_gemm_set_tile.restype = i32
         for fn in ("fp8_quant_fused", "fp8_quant_fused_ex", "fp8_quant_fused_batch", "fp8_downproj_fwd",
-                   "fp8_downproj_fwd_noalloc", "fp8_downproj_fwd_ex", "fp8_gemm_fwd", "fp8_gemm_dgrad", "fp8_gemm_wgrad", "fp8_gemm_dgrad_act", "fp8_upproj_fwd", "amax_history_update",
+                   "fp8_downproj_fwd_noalloc", "fp8_downproj_fwd_ex", "fp8_gemm_fwd", "fp8_gemm_fwd_update", "fp8_gemm_dgrad", "fp8_gemm_wgrad", "fp8_gemm_dgrad_act", "fp8_upproj_fwd", "amax_history_update",
                    "amax_history_update_ex", "fp8q_naive_act", "fp8q_naive_amax", "fp8q_naive_cast"):
             getattr(L, fn).restype = i32
         _lib = L
@@ -172,12 +173,26 @@ def fp8_cast_f32(x: torch.Tensor, fmt: int, q: torch.Tensor | None = None, strea
 
 
 def fp8_gemm_fwd(x_q: torch.Tensor, wt_q: torch.Tensor, scale_x: torch.Tensor, scale_w: torch.Tensor,
-                 y: torch.Tensor, *, group_mode: int = 0, status=None, stream=None) -> None:
-    """y[M,N] = BF16((x_q[M,K] . wt_q[N,K]^T) / (s_x s_w)) on the tensor cores."""
+                 y: torch.Tensor, *, group_mode: int = 0, amax_x=None, hist_x=None, amax_w=None, hist_w=None,
+                 status=None, stream=None) -> None:
+    """y[M,N] = BF16((x_q[M,K] . wt_q[N,K]^T) / (s_x s_w)) on the tensor cores.  With
+    hist_x / hist_w (HistoryArgs, per-tensor scales only) the call is
+    fp8_gemm_fwd_update: the GEMM also runs those delayed-scale updates on
+    amax_x / amax_w."""
     M, K = x_q.shape
     N = wt_q.shape[0]
     if wt_q.shape[1] != K:
         raise ValueError("x_q [M,K] and wt_q [N,K] disagree on K")
+    if hist_x is not None or hist_w is not None:
+        if group_mode:
+            raise ValueError("the delayed-scale updates go with per-tensor scales")
+        st = lib().fp8_gemm_fwd_update(
+            _ptr(x_q, M * K, "x_q"), _ptr(wt_q, N * K, "wt_q"), _ptr(scale_x, 4, "scale_x"),
+            _ptr(scale_w, 4, "scale_w"), _ptr(y, 2 * M * N, "y"), M, N, K, _ptr(amax_x, 4, "amax_x"),
+            None if hist_x is None else ctypes.byref(hist_x), _ptr(amax_w, 4, "amax_w"),
+            None if hist_w is None else ctypes.byref(hist_w), _ptr(status, 4, "status"), _stream(stream))
+        _check("fp8_gemm_fwd_update", st)
+        return
     if group_mode:
         sx, sw = 4 * M * (K // GROUP), 4 * (K // GROUP) * ((N + GROUP - 1) // GROUP)
     else:

@@ -789,6 +789,15 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         // ---------------------------------------------------------- epilogue
         if constexpr (FUSED) {
             if (fz.w) fused_cast_w(fz, K, warp - 2, lane);
+        } else {
+            // fp8_gemm_fwd_update: the step's delayed-scale updates, by one warp of
+            // the first CTA while its first accumulator fills (the amax values
+            // are final: the casts completed before pdl_wait returned).  They
+            // write the other scale slot, never the scales this GEMM reads.
+            if (blockIdx.x == 0 && warp == 2) {
+                if (fz.hx.history) history_update_once(fz.hx, fz.amax_out);
+                if (fz.hw.history) history_update_once(fz.hw, fz.amax_w);
+            }
         }
         const int q = warp & 3;  // TMEM lane quarter this warp may access
         const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
@@ -1417,6 +1426,32 @@ extern "C" int fp8_gemm_fwd(const void* x_q, const void* wt_q, const float* scal
                          stream);
 }
 
+extern "C" int fp8_gemm_fwd_update(const void* x_q, const void* wt_q, const float* scale_x, const float* scale_w,
+                                   void* y, int64_t M, int64_t N, int64_t K, float* amax_x,
+                                   const fp8q_history_args* hist_x, float* amax_w, const fp8q_history_args* hist_w,
+                                   int* status, cudaStream_t stream) {
+    FusedArgs fz = {};
+    int st = FP8Q_OK;
+    const fp8q_history_args* hs[2] = {hist_x, hist_w};
+    float* amax[2] = {amax_x, amax_w};
+    HistoryArgs* out[2] = {&fz.hx, &fz.hw};
+    for (int i = 0; i < 2; ++i) {
+        if (!hs[i]) continue;
+        st = check_history(hs[i], amax[i], out[i]);
+        if (st != FP8Q_OK) return st;
+        // the update writes the next step's scale: never one this GEMM reads
+        if (hs[i]->scale_out == scale_x || hs[i]->scale_out == scale_w) return FP8Q_ERR_SHAPE;
+        if (hs[i]->amax_clear && (hs[i]->amax_clear == amax[0] || hs[i]->amax_clear == amax[1])) return FP8Q_ERR_SHAPE;
+    }
+    st = check_gemm_args(x_q, wt_q, scale_x, scale_w, y, M, N, K, status);
+    if (st != FP8Q_OK) return st;
+    if (M == 0) return (hist_x || hist_w) ? FP8Q_ERR_SHAPE : FP8Q_OK;  // the updates ride on the launch
+    fz.amax_out = amax_x;
+    fz.amax_w = amax_w;
+    return gemm_dispatch_t<false>(x_q, wt_q, scale_x, scale_w, 0, y, M, N, K, FP8Q_E4M3, FP8Q_E4M3, status,
+                                  stream, fz);
+}
+
 extern "C" int fp8_gemm_dgrad(const void* dy_q, const void* w_q, const float* scale_dy, const float* scale_w,
                               void* dx, int64_t M, int64_t N, int64_t K, int* status, cudaStream_t stream) {
     // D = dX [M,K], A = dY [M,N] (contraction N), B = W [K,N]
@@ -1510,29 +1545,6 @@ extern "C" int fp8_downproj_fwd(const void* h, const void* wt_q, int64_t M, int6
 namespace {
 
 // Host checks of one history update (as amax_history_update_ex) and its device form.
-int check_history(const fp8q_history_args* h, const float* amax_new, HistoryArgs* out) {
-    if (!h->history || !h->head || !h->scale_out || !amax_new) return FP8Q_ERR_NULL;
-    if (h->L < 1 || h->L > 4096) return FP8Q_ERR_SHAPE;
-    if (h->fmt != FP8Q_E4M3 && h->fmt != FP8Q_E5M2) return FP8Q_ERR_UNSUPPORTED;
-    if (!(h->margin > 0.0f) || h->margin > 3.402823466e38f) return FP8Q_ERR_SHAPE;
-    if ((reinterpret_cast<uintptr_t>(h->history) | reinterpret_cast<uintptr_t>(h->head) |
-         reinterpret_cast<uintptr_t>(h->scale_out) | reinterpret_cast<uintptr_t>(h->scale_prev) |
-         reinterpret_cast<uintptr_t>(h->status) | reinterpret_cast<uintptr_t>(h->amax_clear)) & 3u)
-        return FP8Q_ERR_ALIGN;
-    if (reinterpret_cast<uintptr_t>(h->sat_clear) & 7u) return FP8Q_ERR_ALIGN;
-    if (h->amax_clear && h->amax_clear == amax_new) return FP8Q_ERR_SHAPE;
-    out->history = h->history;
-    out->L = h->L;
-    out->head = h->head;
-    out->margin = h->margin;
-    out->fmt_max = fp8_max_value(h->fmt);
-    out->scale_prev = h->scale_prev;
-    out->scale_out = h->scale_out;
-    out->status = h->status;
-    out->amax_clear = h->amax_clear;
-    out->sat_clear = h->sat_clear;
-    return FP8Q_OK;
-}
 
 }  // namespace
 

@@ -71,4 +71,30 @@ __device__ __forceinline__ void history_update_warp(const HistoryArgs& a, const 
     }
 }
 
+// Host check of one fp8q_history_args (the rules of amax_history_update_ex)
+// and its device form.
+inline int check_history(const fp8q_history_args* h, const float* amax_new, HistoryArgs* out) {
+    if (!h->history || !h->head || !h->scale_out || !amax_new) return FP8Q_ERR_NULL;
+    if (h->L < 1 || h->L > 4096) return FP8Q_ERR_SHAPE;
+    if (h->fmt != FP8Q_E4M3 && h->fmt != FP8Q_E5M2) return FP8Q_ERR_UNSUPPORTED;
+    if (!(h->margin > 0.0f) || h->margin > 3.402823466e38f) return FP8Q_ERR_SHAPE;
+    if ((reinterpret_cast<uintptr_t>(h->history) | reinterpret_cast<uintptr_t>(h->head) |
+         reinterpret_cast<uintptr_t>(h->scale_out) | reinterpret_cast<uintptr_t>(h->scale_prev) |
+         reinterpret_cast<uintptr_t>(h->status) | reinterpret_cast<uintptr_t>(h->amax_clear)) & 3u)
+        return FP8Q_ERR_ALIGN;
+    if (reinterpret_cast<uintptr_t>(h->sat_clear) & 7u) return FP8Q_ERR_ALIGN;
+    if (h->amax_clear && h->amax_clear == amax_new) return FP8Q_ERR_SHAPE;
+    out->history = h->history;
+    out->L = h->L;
+    out->head = h->head;
+    out->margin = h->margin;
+    out->fmt_max = fp8_max_value(h->fmt);
+    out->scale_prev = h->scale_prev;
+    out->scale_out = h->scale_out;
+    out->status = h->status;
+    out->amax_clear = h->amax_clear;
+    out->sat_clear = h->sat_clear;
+    return FP8Q_OK;
+}
+
 }  // namespace fp8q

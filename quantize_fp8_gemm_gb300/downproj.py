@@ -332,9 +332,10 @@ class Fp8DownProj:
         and the quantize of H share one launch (fp8_quant_fused_batch), and the
         GEMM follows on the same stream, so its set-up overlaps the quantize's
         last CTAs.  Both casts accumulate into their slot's amax / count, which
-        the previous update() zeroed (no memset ahead of the cast).  The
-        history updates run on the side stream beside the GEMM."""
-        main, side = torch.cuda.current_stream(), self._side
+        the previous update zeroed (no memset ahead of the cast).  The GEMM
+        also runs both history updates (fp8_gemm_fwd_update: one warp of its
+        first CTA, beside its first tile), so the step is two launches on one
+        stream."""
         sx, sw = self.x.scale, self.w.scale
         fx = B.ACCUMULATE if self.x.clean else 0
         fw = B.ACCUMULATE if self.w.clean else 0
@@ -345,14 +346,10 @@ class Fp8DownProj:
                          amax_out=self.x.amax, sat_count=self.x.sat, flags=fx),
         ])
         self.x.clean = self.w.clean = False
-        cast_done = torch.cuda.Event()
-        cast_done.record(main)
-        self.gemm(sx, sw)
-        side.wait_event(cast_done)  # this step's amaxes are final
-        with torch.cuda.stream(side):
-            self.x.update()
-            self.w.update()
-        main.wait_stream(side)
+        B.fp8_gemm_fwd(self.x_q, self.wt_q, sx, sw, self.y, amax_x=self.x.amax, hist_x=self.x.kernel_update_args(),
+                       amax_w=self.w.amax, hist_w=self.w.kernel_update_args(), status=self.gemm_status)
+        self.x.advance()
+        self.w.advance()
         return self.y
 
     def capture(self, H: torch.Tensor, W: torch.Tensor, H_next: torch.Tensor | None = None) -> "StepGraph":

@@ -88,6 +88,39 @@ def gemm(lib, a=A, b=A, sa=A, sb=A, grp=0, d=A, M=128, N=256, K=512, st=None):
     return lib.fp8_gemm_fwd(a, b, sa, sb, grp, d, M, N, K, st, None)
 
 
+def test_gemm_fwd_update_history_checks(lib):
+    """fp8_gemm_fwd_update: the history arguments are checked first (by the
+    rules of amax_history_update_ex, and against the scales and amax values
+    the GEMM itself uses); a well-formed call then stops at the device check."""
+    import ctypes
+    from quantize_fp8_gemm_gb300 import binding
+    H, S, AX, AW, CLR = A + 4096, A + 8192, A + 12288, A + 16384, A + 20480
+
+    def hist(**kw):
+        h = dict(history=H, L=4, head=A + 24576, margin=2.0, fmt=0, scale_prev=S, scale_out=A + 28672, status=None,
+                 amax_clear=CLR, sat_clear=None)
+        h.update(kw)
+        return binding.HistoryArgs(*[h[f] for f, _ in binding.HistoryArgs._fields_])
+
+    def call(hx=None, hw=None, sx=S, amax_x=AX):
+        return lib.fp8_gemm_fwd_update(A, A, sx, A + 32768, A, 256, 256, 512, amax_x,
+                                       None if hx is None else ctypes.byref(hx), AW,
+                                       None if hw is None else ctypes.byref(hw), None, None)
+
+    assert call(hist(history=None)) == ERR_NULL
+    assert call(hist(L=0)) == ERR_SHAPE
+    assert call(hist(fmt=7)) == ERR_UNSUPPORTED
+    assert call(hist(margin=0.0)) == ERR_SHAPE
+    assert call(hist(head=A + 2)) == ERR_ALIGN
+    assert call(hist(scale_out=S)) == ERR_SHAPE           # would overwrite scale_x
+    assert call(None, hist(scale_out=A + 32768)) == ERR_SHAPE  # would overwrite scale_w
+    assert call(hist(amax_clear=AW)) == ERR_SHAPE         # would clear the other amax
+    assert call(hist(), amax_x=None) == ERR_NULL
+    assert call(hist(), hist(history=A + 36864, head=A + 40960, scale_out=A + 45056, amax_clear=A + 49152)) \
+        == ERR_UNSUPPORTED
+    assert call() == ERR_UNSUPPORTED
+
+
 def test_gemm_argument_checks(lib):
     assert gemm(lib, a=None) == ERR_NULL
     assert gemm(lib, sb=None) == ERR_NULL

@@ -314,3 +314,47 @@ def test_no_recompute_without_overflow():
     assert dp.recompute_on_overflow(H1d, Wd) == 0
     torch.cuda.synchronize()
     assert torch.equal(dp.y.view(torch.int16), y.view(torch.int16)) and torch.equal(dp.x_q, q)
+
+
+def _delayed(amax0, amax_now, sat_now):
+    d = dp_mod.DelayedScale(B.E4M3, 2.0, 3, "cuda")
+    d.seed(amax0)
+    d.amax.fill_(amax_now)
+    d.sat.fill_(sat_now)
+    d.clean = False
+    return d
+
+
+@pytest.mark.parametrize("tile", [(-1, 0), (0, 128), (1, 256)])
+@pytest.mark.parametrize("amax_x", [5.5, float("inf")])
+def test_gemm_fwd_update_equals_gemm_then_updates(tile, amax_x):
+    """fp8_gemm_fwd_update: the Y of fp8_gemm_fwd, and the histories, heads,
+    next scales, cleared slots and status words of the two
+    amax_history_update_ex calls (a non-finite amax keeps the previous scale
+    and flags FP8Q_DEV_BAD_AMAX either way)."""
+    M, K, N = 1000, 768, 512
+    g = torch.Generator(device="cuda").manual_seed(3)
+    xq = torch.randint(0, 120, (M, K), dtype=torch.uint8, device="cuda", generator=g)
+    wt = torch.randint(0, 120, (N, K), dtype=torch.uint8, device="cuda", generator=g)
+    xa, wa = _delayed(3.0, amax_x, 5), _delayed(0.1, 0.07, 0)
+    xb, wb = _delayed(3.0, amax_x, 5), _delayed(0.1, 0.07, 0)
+    ya = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+    yb = torch.empty_like(ya)
+    try:
+        B.fp8q_gemm_set_tile(*tile)
+        B.fp8_gemm_fwd(xq, wt, xa.scale, wa.scale, ya, amax_x=xa.amax, hist_x=xa.kernel_update_args(),
+                       amax_w=wa.amax, hist_w=wa.kernel_update_args())
+        xa.advance()
+        wa.advance()
+        B.fp8_gemm_fwd(xq, wt, xb.scale, wb.scale, yb)
+        xb.update()
+        wb.update()
+        torch.cuda.synchronize()
+    finally:
+        B.fp8q_gemm_set_tile(-1)
+    assert torch.equal(ya.view(torch.int16), yb.view(torch.int16))
+    for a, b in ((xa, xb), (wa, wb)):
+        assert a.slot == b.slot
+        for f in ("history", "head", "scales", "amaxes", "sats", "status"):
+            assert torch.equal(getattr(a, f), getattr(b, f)), f
+    assert bool(int(xa.status.item()) & B.DEV_BAD_AMAX) == (amax_x == float("inf"))
