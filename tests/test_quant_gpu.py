@@ -174,6 +174,30 @@ def test_weight_blocks_128x128(M, K):
     assert_same(g, r, keys)
 
 
+@pytest.mark.parametrize("mode", ["tensor", "relu2_act", "blocks_128x128", "groups_1x128"])
+def test_large_tiled_grid_every_mode(mode):
+    """Grids past two rounds of the register-landing tile kernel run the
+    shared-memory one: 2000 x 10240 is 16 x 80 = 1280 tiles (a ragged last
+    tile row), in each tiled mode, with the transposed copy."""
+    M, K = 2000, 10240
+    h = _rand_bits(M, K, seed=77, std=0.5)
+    h[7, 300] = WL.to_bf16_bits(np.array([60.0], np.float32))[0]
+    if mode == "tensor":
+        g = run_quant(h, B.ACT_IDENTITY, B.E4M3, 4.0, want_act=False, want_qt=True)
+        r = O.quant(h, O.ACT_IDENTITY, O.E4M3, 4.0, want_act=False, want_qt=True)
+        keys = ["q", "q_t", "amax", "sat"]
+    elif mode == "relu2_act":
+        g = run_quant(h, B.ACT_RELU2, B.E5M2, 1000.0, want_qt=True)
+        r = O.quant(h, O.ACT_RELU2, O.E5M2, 1000.0, want_qt=True)
+        keys = ["act", "q", "q_t", "amax", "sat"]
+    else:
+        rows = 128 if mode == "blocks_128x128" else 1
+        g = run_quant(h, B.ACT_IDENTITY, B.E4M3, None, want_act=False, want_qt=True, group_rows=rows)
+        r = O.quant_group(h, O.ACT_IDENTITY, O.E4M3, rows, want_act=False, want_qt=True)
+        keys = ["q", "q_t", "amax", "sat", "scales"]
+    assert_same(g, r, keys)
+
+
 def test_relu2_with_transposed_copy_and_act():
     """The tiled path with an activation and every output at once."""
     h = _rand_bits(256, 384, seed=9)
