@@ -90,6 +90,11 @@ class DelayedScale:
         """The scale the next cast uses (a 1-element view of the current slot)."""
         return self.scales[self.slot:self.slot + 1]
 
+    @property
+    def last_scale(self) -> torch.Tensor:
+        """The scale the cast before the last update() used."""
+        return self.scales[1 - self.slot:2 - self.slot]
+
     def update(self) -> None:
         """Push this step's amax; write the next step's scale into the other
         slot (which first takes the current scale, kept if the amax is
@@ -372,7 +377,7 @@ class Fp8DownProj:
         was cast again (0: nothing overflowed, Y stands); x_scale_used and
         w_scale_used name the scales X_q and W_q now carry.  Group scales are
         computed from each group's own values and never overflow: 0."""
-        sx_prev, sw_prev = self.x.scales[1 - self.x.slot:2 - self.x.slot], self.w.scales[1 - self.w.slot:2 - self.w.slot]
+        sx_prev, sw_prev = self.x.last_scale, self.w.last_scale
         self.x_scale_used, self.w_scale_used = sx_prev, sw_prev
         if self.group:
             return 0

@@ -265,7 +265,7 @@ def test_recompute_after_activation_overflow(fused):
     assert dp.recompute_on_overflow(H1d, Wd) == dp_mod.RECOMPUTE_X
     torch.cuda.synchronize()
     amax_t = O.amax(H1, O.ACT_RELU2)
-    stale = O.quant(H1, O.ACT_RELU2, O.E4M3, float(dp.x.scales[1 - dp.x.slot].item()), want_act=False)
+    stale = O.quant(H1, O.ACT_RELU2, O.E4M3, float(dp.x.last_scale.item()), want_act=False)
     assert int(dp.x.last_sat.item()) == stale["sat"] > 0
     s_fix = O.delayed_scale(amax_t, w.margin, O.E4M3)
     assert float(dp.x_scale_used.item()) == s_fix
