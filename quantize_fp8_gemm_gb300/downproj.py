@@ -137,16 +137,20 @@ class Fp8DownProj:
     def __init__(self, M: int, K: int, N: int, *, act: int = B.ACT_RELU2, margin: float = 2.0,
                  history_len: int = 1, group: bool = False, with_dgrad: bool = False,
                  keep_act: bool = True, chunks: int | None = None, fused: bool | None = None,
-                 device="cuda"):
+                 with_backward: bool = False, device="cuda"):
         self.M, self.K, self.N, self.act, self.group = M, K, N, act, group
+        self.with_backward = with_backward
+        if with_backward and (group or (chunks or 1) != 1 or fused):
+            raise ValueError("backward() runs after the per-tensor one-block step (not fused, not grouped)")
+        with_dgrad = with_dgrad or with_backward
         # The fused kernel (W cast + quantize + GEMM + history updates, one
         # launch) serves the per-tensor path in one block.  Measured per step
         # on GB300 (CUDA graph, L2 flushed): it wins on large batches (65,536 x
         # 3072 -> 768: 212 vs 259 us; 131,072 x 6400 -> 1600: 1227 vs 1437 us)
-        # and loses at 8,192 rows (46.8 vs 45.0 us), where its last wave of
+        # and loses at 8,192 rows (47.6 vs 40.6 us), where its last wave of
         # tiles, which waits for the last rows, is not hidden.
         if fused is None:
-            fused = not group and (chunks or 1) == 1 and M >= FUSED_MIN_ROWS
+            fused = not group and (chunks or 1) == 1 and M >= FUSED_MIN_ROWS and not with_backward
         self.fused = fused
         if self.fused and (group or (chunks or 1) != 1):
             raise ValueError("the fused kernel runs the per-tensor path over the whole batch")
@@ -172,8 +176,18 @@ class Fp8DownProj:
         self._fix_amax = torch.zeros(1, dtype=torch.float32, device=dev)
         self._fix_sat = torch.zeros(1, dtype=torch.int64, device=dev)
         self._fix_status = torch.zeros(1, dtype=torch.int32, device=dev)
-        self.x_scale_used = None  # after step(): the scales X_q / W_q were cast with
+        self.x_scale_used = None  # after recompute_on_overflow(): the scales X_q / W_q now carry
         self.w_scale_used = None
+        # backward(): X_q^T cached by the forward's quantize, the gradient's
+        # delayed scale (E5M2) and the outputs
+        self.x_q_t = self.g = None
+        if with_backward:
+            self.x_q_t = torch.empty(K, M, dtype=torch.uint8, device=dev)
+            self.g = DelayedScale(B.E5M2, margin, history_len, dev)
+            self.dy_q = torch.empty(M, N, dtype=torch.uint8, device=dev)
+            self.dy_q_t = torch.empty(N, M, dtype=torch.uint8, device=dev)
+            self.dh = torch.empty(M, K, dtype=torch.bfloat16, device=dev)
+            self.dw = torch.empty(K, N, dtype=torch.bfloat16, device=dev)
         self.workspace = None
         if self.fused:
             # zero-filled once; the fused kernel leaves it zero
@@ -285,6 +299,7 @@ class Fp8DownProj:
         first quantize, then updates the activation's history once the last
         block is quantized (the updates write the other scale slot, so they
         never race the GEMMs' reads).  All branches join the current stream."""
+        self.x_scale_used = self.w_scale_used = None
         if self.fused:
             return self._step_fused(H, W)
         if not self.group and self.chunks == 1:
@@ -347,7 +362,7 @@ class Fp8DownProj:
         B.fp8_quant_fused_batch([
             B.quant_args(W, B.ACT_IDENTITY, B.E4M3, sw, q_out=self.w_q, q_t_out=self.wt_q,
                          amax_out=self.w.amax, flags=fw),
-            B.quant_args(H, self.act, B.E4M3, sx, act_out=self.act_bf16, q_out=self.x_q,
+            B.quant_args(H, self.act, B.E4M3, sx, act_out=self.act_bf16, q_out=self.x_q, q_t_out=self.x_q_t,
                          amax_out=self.x.amax, sat_count=self.x.sat, flags=fx),
         ])
         self.x.clean = self.w.clean = False
@@ -390,8 +405,8 @@ class Fp8DownProj:
             sx = self._fix_scale[0:1]
             B.amax_history_update_ex(self._fix_hist[0:1], self._fix_head[0:1], self.x.last_amax, self.x.margin,
                                      B.E4M3, sx, scale_prev=sx_prev, status=self._fix_status)
-            B.fp8_quant_fused_ex(H, self.act, B.E4M3, sx, q_out=self.x_q, amax_out=self._fix_amax,
-                                 sat_count=self._fix_sat)
+            B.fp8_quant_fused_ex(H, self.act, B.E4M3, sx, q_out=self.x_q, q_t_out=self.x_q_t,
+                                 amax_out=self._fix_amax, sat_count=self._fix_sat)
             self.x_scale_used = sx
             redo |= RECOMPUTE_X
         if w_over:
@@ -404,6 +419,44 @@ class Fp8DownProj:
             redo |= RECOMPUTE_W
         self.gemm(self.x_scale_used, self.w_scale_used)
         return redo
+
+    def backward(self, dY: torch.Tensor, H: torch.Tensor) -> tuple[torch.Tensor, torch.Tensor]:
+        """The down-projection's backward on the forward's FP8 operands ("FP8
+        Training & Inference", FP8 Training Recipe: gradients in E5M2, weights
+        and activations in E4M3), after step(H, W) and before the next step:
+
+            dY [M,N] BF16 -> dY_q (E5M2, delayed scale) and dY_q^T, one pass
+            dH = (dY_q . W_q^T) / (s_dy s_w) * act'(H)   -> [M,K] BF16 (dX never stored)
+            dW = (X_q^T . dY_q) / (s_x s_dy)              -> [K,N] BF16
+            push amax(dY) into the gradient's history
+
+        X_q^T is the transposed copy the forward's quantize cached, W_q the
+        weight's own layout; both carry the scales they were cast with (the
+        recompute's, if recompute_on_overflow() ran).  H is the forward's BF16
+        pre-activation.  Needs with_backward.  Returns views of (dH, dW)."""
+        if not self.with_backward:
+            raise RuntimeError("backward() needs Fp8DownProj(..., with_backward=True)")
+        sx = self.x_scale_used if self.x_scale_used is not None else self.x.last_scale
+        sw = self.w_scale_used if self.w_scale_used is not None else self.w.last_scale
+        sdy = self.g.scale
+        fl = B.ACCUMULATE if self.g.clean else 0
+        B.fp8_quant_fused_ex(dY, B.ACT_IDENTITY, B.E5M2, sdy, q_out=self.dy_q, q_t_out=self.dy_q_t,
+                             amax_out=self.g.amax, sat_count=self.g.sat, flags=fl)
+        self.g.clean = False
+        B.fp8_gemm_dgrad_act(self.dy_q, self.w_q, sdy, sw, H, self.dh, act=self.act, status=self.gemm_status)
+        B.fp8_gemm_wgrad(self.x_q_t, self.dy_q_t, sx, sdy, self.dw, status=self.gemm_status)
+        self.g.update()
+        return self.dh, self.dw
+
+    def calibrate_backward(self, dY: torch.Tensor) -> None:
+        """Bootstrap the gradient's delayed scale from a first dY (one amax pass),
+        as calibrate() does for X and W."""
+        if not self.with_backward:
+            raise RuntimeError("calibrate_backward() needs Fp8DownProj(..., with_backward=True)")
+        self.g.scales.fill_(1.0)
+        B.fp8_quant_fused(dY, B.ACT_IDENTITY, B.E5M2, self.g.scale, q_out=self.dy_q, amax_out=self.g.amax)
+        self.g.clean = False
+        self.g.update()
 
     def calibrate(self, H: torch.Tensor, W: torch.Tensor) -> None:
         """Bootstrap the delayed scales from step 0's own tensors (one amax pass each).

@@ -358,3 +358,43 @@ def test_gemm_fwd_update_equals_gemm_then_updates(tile, amax_x):
         for f in ("history", "head", "scales", "amaxes", "sats", "status"):
             assert torch.equal(getattr(a, f), getattr(b, f)), f
     assert bool(int(xa.status.item()) & B.DEV_BAD_AMAX) == (amax_x == float("inf"))
+
+
+def test_backward_after_a_step_against_the_oracle():
+    """Fp8DownProj.backward after a forward step: dY cast to E5M2 with its
+    delayed scale (both layouts bit for bit), dH = dgrad * act'(H) and
+    dW = X_q^T dY_q from the forward's cached X_q^T, both within the GEMM
+    tolerance of the oracle on sampled rows; the gradient's history takes
+    amax(dY)."""
+    w = WL.WORKLOADS["gpt2s"]
+    M, K, N = 2048, w.K, w.N
+    W_bits = WL.w_down(w)
+    Wd = WL.bf16_tensor(W_bits).cuda()
+    H0, H1 = WL.h_preact(w, 0)[:M], WL.h_preact(w, 1)[:M]
+    rng = np.random.default_rng(8)
+    dY0, dY1 = (WL.to_bf16_bits((rng.standard_normal((M, N)) * 1e-3).astype(np.float32)) for _ in range(2))
+    dp = Fp8DownProj(M, K, N, margin=w.margin, with_backward=True)
+    assert not dp.fused
+    dp.calibrate(WL.bf16_tensor(H0).cuda(), Wd)
+    dp.calibrate_backward(WL.bf16_tensor(dY0).cuda())
+    H1d = WL.bf16_tensor(H1).cuda()
+    dp.step(H1d, Wd)
+    dh, dw = dp.backward(WL.bf16_tensor(dY1).cuda(), H1d)
+    torch.cuda.synchronize()
+    s_x, s_w = float(dp.x.last_scale.item()), float(dp.w.last_scale.item())
+    s_dy = float(dp.g.last_scale.item())
+    assert s_dy == O.delayed_scale(O.amax(dY0, O.ACT_IDENTITY), w.margin, O.E5M2)
+    rx = O.quant(H1, O.ACT_RELU2, O.E4M3, s_x, want_act=False)
+    rw = O.quant(W_bits, O.ACT_IDENTITY, O.E4M3, s_w, want_act=False)
+    rd = O.quant(dY1, O.ACT_IDENTITY, O.E5M2, s_dy, want_act=False)
+    assert np.array_equal(host_u8(dp.x_q_t), np.ascontiguousarray(rx["q"].T))
+    assert np.array_equal(host_u8(dp.dy_q), rd["q"])
+    assert np.array_equal(host_u8(dp.dy_q_t), np.ascontiguousarray(rd["q"].T))
+    assert float(dp.g.history[0].item()) == rd["amax"]
+    rows = WL.sample_rows(M, 48, seed=9)
+    ref, S = O.gemm_dgrad_act(rd["q"], rw["q"], s_dy, s_w, H1, O.ACT_RELU2, rows=rows)
+    assert_gemm_close(dh, ref, S, rows=rows)
+    krows = WL.sample_rows(K, 48, seed=10)
+    ref, S = O.gemm_wgrad(rx["q"], rd["q"], s_x, s_dy, rows=krows)
+    assert_gemm_close(dw, ref, S, rows=krows)
+    assert int(dp.gemm_status.item()) == 0
