@@ -8,6 +8,7 @@
  *   2. fp8_gemm_fwd         Y = X_q W_q / (s_x s_w), FP32 accumulate, BF16 out
  *      (fp8_downproj_fwd    1 and 2 fused in one kernel)
  *   3. amax_history_update  push this step's amax; scale for the next step
+ *      (fp8_gemm_fwd_update 2 and 3 in one launch: the GEMM runs the updates)
  *   (fp8_gemm_dgrad         dX = dY_q W_q^T / (s_dy s_w), the gradient shape)
  *   (fp8_gemm_wgrad         dW = X_q^T dY_q / (s_x s_dy), the weight gradient)
  *   (fp8_upproj_fwd         the preceding up-projection with 1 in its epilogue)
