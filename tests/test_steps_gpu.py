@@ -15,7 +15,7 @@ from quantize_fp8_gemm_gb300 import binding as B
 from quantize_fp8_gemm_gb300 import workloads as WL
 from quantize_fp8_gemm_gb300 import downproj as dp_mod
 from quantize_fp8_gemm_gb300.downproj import Fp8DownProj
-from tests.parity import assert_gemm_close, host_u8
+from tests.parity import assert_gemm_close, host_bits16, host_u8
 
 pytestmark = pytest.mark.gpu
 
@@ -398,3 +398,37 @@ def test_backward_after_a_step_against_the_oracle():
     ref, S = O.gemm_wgrad(rx["q"], rd["q"], s_x, s_dy, rows=krows)
     assert_gemm_close(dw, ref, S, rows=krows)
     assert int(dp.gemm_status.item()) == 0
+
+
+@pytest.mark.parametrize("N", [2304, 768])
+def test_identity_activation_linear_layers(N):
+    """The other GEMMs of a GPT-2-small block as FP8 layers (the QKV
+    projection 768 -> 2304 and the attention output 768 -> 768): the same step
+    with the identity activation, forward and backward against the oracle."""
+    M, K = 1024, 768
+    rng = np.random.default_rng(N)
+    X = [WL.to_bf16_bits(rng.standard_normal((M, K)).astype(np.float32)) for _ in range(2)]
+    W_bits = WL.to_bf16_bits((rng.standard_normal((K, N)) * 0.02).astype(np.float32))
+    dY = WL.to_bf16_bits((rng.standard_normal((M, N)) * 1e-3).astype(np.float32))
+    Wd = WL.bf16_tensor(W_bits).cuda()
+    dp = Fp8DownProj(M, K, N, act=B.ACT_IDENTITY, margin=2.0, with_backward=True)
+    dp.calibrate(WL.bf16_tensor(X[0]).cuda(), Wd)
+    dp.calibrate_backward(WL.bf16_tensor(dY).cuda())
+    X1 = WL.bf16_tensor(X[1]).cuda()
+    y = dp.step(X1, Wd)
+    dh, dw = dp.backward(WL.bf16_tensor(dY).cuda(), X1)
+    torch.cuda.synchronize()
+    s_x, s_w, s_dy = (float(t.item()) for t in (dp.x.last_scale, dp.w.last_scale, dp.g.last_scale))
+    rx = O.quant(X[1], O.ACT_IDENTITY, O.E4M3, s_x)
+    rw = O.quant(W_bits, O.ACT_IDENTITY, O.E4M3, s_w, want_act=False)
+    rd = O.quant(dY, O.ACT_IDENTITY, O.E5M2, s_dy, want_act=False)
+    assert np.array_equal(host_u8(dp.x_q), rx["q"])
+    assert np.array_equal(host_bits16(dp.act_bf16), rx["act"])
+    rows = WL.sample_rows(M, 32, seed=1)
+    Yr, S = O.gemm_fwd(rx["q"][rows], rw["q"], s_x, s_w)
+    assert_gemm_close(y, Yr, S, rows=rows)
+    ref, S = O.gemm_dgrad_act(rd["q"], rw["q"], s_dy, s_w, X[1], O.ACT_IDENTITY, rows=rows)
+    assert_gemm_close(dh, ref, S, rows=rows)
+    krows = WL.sample_rows(K, 32, seed=2)
+    ref, S = O.gemm_wgrad(rx["q"], rd["q"], s_x, s_dy, rows=krows)
+    assert_gemm_close(dw, ref, S, rows=krows)
