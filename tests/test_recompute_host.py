@@ -38,3 +38,12 @@ def test_weight_decision_matches_the_oracle_cast(seed):
     for s in (edge, np.nextafter(edge, np.float32(0)), np.nextafter(edge, np.float32(np.inf)), edge * 2, edge / 2):
         r = O.quant(bits, O.ACT_IDENTITY, O.E4M3, float(s), want_act=False)
         assert fp8_overflow(0, amax, float(s))[1] == (r["sat"] > 0), (seed, float(s))
+
+
+@pytest.mark.parametrize("kw", [dict(fused=True), dict(group=True), dict(chunks=2)])
+def test_backward_needs_the_one_block_per_tensor_step(kw):
+    """backward() reads the X_q^T that the one-block per-tensor step caches; the
+    constructor refuses the other step forms before it allocates anything."""
+    from quantize_fp8_gemm_gb300.downproj import Fp8DownProj
+    with pytest.raises(ValueError):
+        Fp8DownProj(1024, 768, 768, with_backward=True, device="cpu", **kw)
