@@ -313,6 +313,19 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
                  :: "r"(bar) : "memory");
 }
+// (s0, s1) += (a0, a1) * g as one packed FP32 FMA (fma.rn.f32x2: each lane is
+// fmaf(a, g, s), rounded once): half the FMA instructions of the group
+// promotion, whose instruction stream bounds it.
+__device__ __forceinline__ void fma_f32x2(float& s0, float& s1, uint32_t a0, uint32_t a1, float g) {
+    asm("{\n\t.reg .b64 a, g, s;\n\t"
+        "mov.b64 a, {%2, %3};\n\t"
+        "mov.b64 g, {%4, %4};\n\t"
+        "mov.b64 s, {%0, %1};\n\t"
+        "fma.rn.f32x2 s, a, g, s;\n\t"
+        "mov.b64 {%0, %1}, s;\n\t}"
+        : "+f"(s0), "+f"(s1)
+        : "r"(a0), "r"(a1), "f"(g));
+}
 // 32 lanes x 32 consecutive 32-bit columns: thread t gets lane (base + t),
 // columns c..c+31.  The load's destination registers are defined only once
 // tcgen05.wait::ld has returned, so the load and its wait are one asm

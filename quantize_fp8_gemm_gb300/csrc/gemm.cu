@@ -877,6 +877,10 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 constexpr bool X16 = C::EPI_WARPS > 8;
                 constexpr int LDB = X16 ? 1 : GC > 64 ? 1 : GC / 32;
                 constexpr int LDW = X16 ? 16 : 32;  // columns per load
+                // packed FP32 FMAs (half the promotion's FMA instructions) up to 12
+                // warps; at 16 warps (a 96-register cap) their register pairs spill more
+                // than they save (85.5 -> 97.2 us at 16384 x 4096 -> 1024)
+                constexpr bool PACKED = C::EPI_WARPS <= 12;
                 static_assert(!GROUP || (GC <= 128 && 128 % GC == 0), "a warp's columns share one block scale");
                 const int cbase = ((warp - 2) / 4) * GC;
                 const int64_t nb_raw = (n_blk * BN + cbase) / 128;
@@ -904,9 +908,15 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                                 __syncwarp();
                                 if (lane == 0) mbar_arrive(tempty0 + 8u * acc);
                             }
+                            if constexpr (PACKED) {
 #pragma unroll
-                            for (int j = 0; j < 16; ++j)
-                                sum[l * 16 + j] = fmaf(__uint_as_float(r16[j]), ginv, sum[l * 16 + j]);
+                                for (int j = 0; j < 16; j += 2)
+                                    fma_f32x2(sum[l * 16 + j], sum[l * 16 + j + 1], r16[j], r16[j + 1], ginv);
+                            } else {
+#pragma unroll
+                                for (int j = 0; j < 16; ++j)
+                                    sum[l * 16 + j] = fmaf(__uint_as_float(r16[j]), ginv, sum[l * 16 + j]);
+                            }
                         }
                     }
 #pragma unroll
@@ -927,8 +937,8 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 #pragma unroll
                         for (int b = 0; b < LDB; ++b)
 #pragma unroll
-                            for (int j = 0; j < 32; ++j)
-                                sum[(c0 + b) * 32 + j] = fmaf(__uint_as_float(r[b][j]), ginv, sum[(c0 + b) * 32 + j]);
+                            for (int j = 0; j < 32; j += 2)
+                                fma_f32x2(sum[(c0 + b) * 32 + j], sum[(c0 + b) * 32 + j + 1], r[b][j], r[b][j + 1], ginv);
                     }
                     next_acc<C::ACCS>(acc, acc_phase);
                 }
@@ -1235,7 +1245,7 @@ int pick_group_bn(int64_t M, int64_t N) {
     if (ov >= 0 && (ov >> 16) == 0 && ((ov & 0xFFFF) == 256 || (ov & 0xFFFF) == 192 || (ov & 0xFFFF) == 128))
         return ov & 0xFFFF;
     struct Cand { int bn; double t; };
-    static constexpr Cand kCands[] = {{128, 1.000}, {192, 1.200}, {256, 1.500}};
+    static constexpr Cand kCands[] = {{128, 1.000}, {192, 1.240}, {256, 1.650}};
     const int64_t sms = sm_count();
     int best = 128;
     double best_cost = -1.0;
