@@ -20,9 +20,12 @@ pages:
   margin-multiplied scale.
 * "Pretraining at scale", 4a -- BF16 rounding.
 
-Parity pins (tests/test_oracle_pins.py) tie each function to printed values,
-closed forms, exhaustive code sweeps or an independent library routine; the
-group-scale GEMM is pinned only by closed-form special cases (see there).
+Parity pins (tests/test_oracle_pins.py, tests/test_oracle_mx_pins.py) tie each
+function to printed values, closed forms, exhaustive code sweeps or an
+independent library routine; the group-scale and MX GEMMs are pinned by
+closed-form special cases and exact integer sums (see there).  The MX
+functions (32-value blocks, power-of-two scales: "FP8 training: what it is
+and how it works", Trade-offs and edge cases) have no GPU counterpart yet.
 """
 import ctypes
 import os
@@ -77,6 +80,10 @@ def lib():
         L.oref_amax.argtypes = [P, i64, i32]
         L.oref_amax.restype = f32
         L.oref_gemm_fwd.argtypes = [P, i32, P, i32, i64, i64, i64, P, P, i32, P, i64, P, P, i32]
+        L.oref_mx_scale.argtypes = [f32, i32]
+        L.oref_mx_scale.restype = f32
+        L.oref_quant_mx.argtypes = [P, i64, i64, i32, i32, P, P, P, P, P, P]
+        L.oref_gemm_mx.argtypes = [P, i32, P, i32, i64, i64, i64, P, P, P, i64, P, P, i32]
         L.oref_gemm_dgrad.argtypes = [P, i32, P, i32, i64, i64, i64, f32, f32, P, i64, P, P, i32]
         L.oref_openmp_max_threads.restype = i32
         _lib = L
@@ -177,6 +184,47 @@ def quant_group(h_bf16, act_kind: int, fmt: int, group_rows: int, *, want_act=Tr
                            _p(scales), _p(amax), _p(sat), nthreads or default_threads())
     return {"act": a, "q": q, "q_t": qt, "scales": scales, "amax": float(amax[0]),
             "sat": int(sat[0])}
+
+
+def mx_scale(amax_b: float, fmt: int) -> float:
+    """The power-of-two scale of one 32-value block (see oref_mx_scale)."""
+    return lib().oref_mx_scale(amax_b, fmt)
+
+
+def quant_mx(h_bf16, act_kind: int, fmt: int, *, want_act=True):
+    """MX quantize: one power-of-two scale per 32-value block of each row of the
+    [M,K] BF16 tensor.  Returns q, act, scales [M, K/32] (float32 powers of
+    two), exps [M, K/32] (the biased exponent bytes of 1 / scale), amax, sat."""
+    h = _c(h_bf16, np.uint16)
+    M, K = h.shape
+    assert K % 32 == 0
+    a = np.empty((M, K), np.uint16) if want_act else None
+    q = np.empty((M, K), np.uint8)
+    scales = np.empty((M, K // 32), np.float32)
+    exps = np.empty((M, K // 32), np.uint8)
+    amax = np.zeros(1, np.float32)
+    sat = np.zeros(1, np.uint64)
+    lib().oref_quant_mx(_p(h), M, K, act_kind, fmt, _p(a), _p(q), _p(scales), _p(exps), _p(amax), _p(sat))
+    return {"act": a, "q": q, "scales": scales, "exps": exps, "amax": float(amax[0]), "sat": int(sat[0])}
+
+
+def gemm_mx(x_q, s_x, w_q, s_w, *, rows=None, fmt_x=E4M3, fmt_w=E4M3, nthreads=None):
+    """Y = X x W over MX-dequantised FP8: X [M,K] with s_x [M, K/32], W [K,N]
+    with s_w [N, K/32] (the blocks of W's columns).  Returns (Y, S)."""
+    X = _c(x_q, np.uint8)
+    W = _c(w_q, np.uint8)
+    M, K = X.shape
+    K2, N = W.shape
+    assert K == K2 and K % 32 == 0
+    sx = _c(s_x, np.float32)
+    sw = _c(s_w, np.float32)
+    assert sx.shape == (M, K // 32) and sw.shape == (N, K // 32)
+    rows = np.arange(M, dtype=np.int64) if rows is None else _c(rows, np.int64)
+    Y = np.empty((rows.size, N), np.float64)
+    S = np.empty((rows.size, N), np.float64)
+    lib().oref_gemm_mx(_p(X), fmt_x, _p(W), fmt_w, M, N, K, _p(sx), _p(sw), _p(rows), rows.size, _p(Y), _p(S),
+                       nthreads or default_threads())
+    return Y, S
 
 
 def amax(h_bf16, act_kind: int) -> float:

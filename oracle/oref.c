@@ -387,6 +387,80 @@ void oref_quant_group(const uint16_t* h, int64_t M, int64_t K, int act, int fmt,
     free(row_sat);
 }
 
+/* ------------------------------------------------------------------------ */
+/* Microscaling (MX): 32-value blocks with power-of-two scales                */
+/* ------------------------------------------------------------------------ */
+/*
+ * "FP8 training: what it is and how it works", Trade-offs and edge cases: the
+ * microscaling FP8 recipe gives every block of 32 adjacent values its own
+ * scale, and the scales are powers of two.  The pages do not say which power
+ * of two; the reading taken here is Step 2's scale (format max / amax) rounded
+ * down to a power of two, so that no value of the block saturates:
+ *   s_b = 2^e with e the largest integer such that amax_b * 2^e <= fmt_max,
+ *   clamped to [-127, 127] (the range of an 8-bit power-of-two exponent);
+ *   an all-zero block gets s_b = 1.
+ * The comparison amax_b * 2^e <= fmt_max is exact (scaling by a power of two
+ * is exact in double), so e is found without any rounded logarithm.
+ */
+float oref_mx_scale(float amax_b, int fmt)
+{
+    if (!(amax_b > 0.0f)) return 1.0f;
+    double fmax = fmt_of(fmt).max_value;
+    int e = 0;
+    (void)frexp(fmax / (double)amax_b, &e); /* a first guess near log2 */
+    while (ldexp((double)amax_b, e) > fmax) --e;
+    while (ldexp((double)amax_b, e + 1) <= fmax) ++e;
+    if (e > 127) e = 127;
+    if (e < -127) e = -127;
+    return (float)ldexp(1.0, e);
+}
+
+/*
+ * MX quantize of the row-major [M,K] BF16 tensor h (K a multiple of 32): for
+ * the 32-value block b of row i (columns 32b .. 32b + 31),
+ *   amax_b = max |BF16(act(h))| over the block
+ *   s_b    = oref_mx_scale(amax_b)         -> scales[i * (K/32) + b]
+ *   e8m0   = 127 - log2(s_b)               -> exps[i * (K/32) + b]: the biased
+ *            exponent byte of the dequantisation factor 1 / s_b
+ *   q      = FP8(float32(BF16(act(h)) * s_b))
+ * act_out, q_out, amax_out and sat_out as in per-tensor mode (sat against
+ * each element's own block scale; 0 for finite inputs by the choice of s_b).
+ */
+void oref_quant_mx(const uint16_t* h, int64_t M, int64_t K, int act, int fmt,
+                   uint16_t* act_out, uint8_t* q_out, float* scales, uint8_t* exps,
+                   float* amax_out, uint64_t* sat_out)
+{
+    const int64_t B = 32, nb = K / B;
+    double fmax = fmt_of(fmt).max_value;
+    uint32_t am = 0;
+    uint64_t sat = 0;
+    for (int64_t i = 0; i < M; ++i) {
+        for (int64_t b = 0; b < nb; ++b) {
+            uint32_t m = 0;
+            for (int64_t k = b * B; k < (b + 1) * B; ++k) {
+                float a = oref_act(oref_bf16_to_f32(h[i * K + k]), act);
+                uint32_t mk = mag_key(oref_bf16_to_f32(oref_f32_to_bf16(a)));
+                if (mk > m) m = mk;
+            }
+            float s = oref_mx_scale(f32_from_bits(m), fmt);
+            int e = 0;
+            (void)frexp((double)s, &e); /* s = 2^(e - 1) */
+            if (scales) scales[i * nb + b] = s;
+            if (exps) exps[i * nb + b] = (uint8_t)(127 - (e - 1));
+            if (m > am) am = m;
+            for (int64_t k = b * B; k < (b + 1) * B; ++k) {
+                uint16_t abf; float v; uint8_t q;
+                quant_one(h[i * K + k], act, fmt, s, &abf, &v, &q);
+                if (act_out) act_out[i * K + k] = abf;
+                if (q_out) q_out[i * K + k] = q;
+                if (fabs((double)v) > fmax) sat += 1;
+            }
+        }
+    }
+    if (amax_out) *amax_out = f32_from_bits(am);
+    if (sat_out) *sat_out = sat;
+}
+
 /* amax only: max |BF16(act(h))| over the tensor (the calibration pass). */
 float oref_amax(const uint16_t* h, int64_t n, int act)
 {
@@ -440,6 +514,43 @@ void oref_gemm_fwd(const uint8_t* X, int fmt_x, const uint8_t* W, int fmt_w,
                 double d = group ? (double)s_x[i * kg + k / OREF_GROUP] *
                                    (double)s_w[(k / OREF_GROUP) * ng + j / OREF_GROUP]
                                  : (double)s_x[0] * (double)s_w[0];
+                y += t / d;
+                s += fabs(t) / d;
+            }
+            Y[r * N + j] = y;
+            S[r * N + j] = s;
+        }
+    }
+}
+
+/*
+ * MX forward: the same sum with one scale per 32-value block on each side,
+ *   Y[i,j] = sum_k dec(X[i,k]) * dec(W[k,j]) / (s_x[i, k/32] * s_w[j, k/32])
+ * X [M,K] and W [K,N] row-major; s_x is [M, K/32] (the blocks of X's rows),
+ * s_w is [N, K/32] (the blocks of W's columns, i.e. of the rows of W^T, the
+ * contraction-major operand).  S is the sum of |terms|.  Rows as above.
+ */
+void oref_gemm_mx(const uint8_t* X, int fmt_x, const uint8_t* W, int fmt_w,
+                  int64_t M, int64_t N, int64_t K, const float* s_x, const float* s_w,
+                  const int64_t* rows, int64_t nrows, double* Y, double* S, int nthreads)
+{
+    double dx[256], dw[256];
+    for (int c = 0; c < 256; ++c) {
+        dx[c] = oref_fp8_decode((uint8_t)c, fmt_x);
+        dw[c] = oref_fp8_decode((uint8_t)c, fmt_w);
+    }
+    const int64_t nb = K / 32;
+    (void)M; (void)nthreads;
+#ifdef _OPENMP
+#pragma omp parallel for num_threads(nthreads > 0 ? nthreads : 1) schedule(dynamic)
+#endif
+    for (int64_t r = 0; r < nrows; ++r) {
+        int64_t i = rows[r];
+        for (int64_t j = 0; j < N; ++j) {
+            double y = 0.0, s = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                double t = dx[X[i * K + k]] * dw[W[k * N + j]];
+                double d = (double)s_x[i * nb + k / 32] * (double)s_w[j * nb + k / 32];
                 y += t / d;
                 s += fabs(t) / d;
             }
