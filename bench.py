@@ -1,31 +1,39 @@
 """Benchmark of the forward FP8 MLP down-projection on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload gpt2s] [--no-extras]
+                    [--workload gpt2xl] [--rows M] [--no-extras] [--profile]
 
 One step is one pass of the forward path over one batch: cast W [K,N] to
 E4M3 (transposed operand), fused ReLU^2 + BF16 copy + E4M3 cast + amax of H
 [M,K], FP8 GEMM Y = X_q W_q / (s_x s_w) -> BF16, and the two delayed-scale
-history updates.  The default workload is the GPT-2-small down-projection
-(M = 8192 tokens, K = 3072, N = 768, margin 2.0, history length 1).
+history updates.  The default workload is the largest one, the GPT-2-XL
+down-projection (M = 131072 tokens, K = 6400, N = 1600, margin 2.0, history
+length 1), where the step is one kernel (fp8_downproj_fwd_ex).
 
 Timing: W untimed warm-up steps, then exactly K steps; before each step a
 256 MiB buffer is written and read back to flush L2 (outside the timed
 events); each step (a CUDA graph of the step's launches) is timed on its
-stream with CUDA events at the phase boundaries.  `value` is whole-job
-TFLOP/s (2 M N K per step and GPU) over the summed step times, max over ranks.
-`e2e` repeats the step through the same public API with H and W copied in
-from pinned host memory and Y copied back inside the timed region.
+stream with CUDA events.  `value` is whole-job TFLOP/s (2 M N K per step and
+GPU) over the mean step time, max over ranks.  `e2e` repeats the step
+through the same public API with H and W copied in from pinned host memory
+and Y copied back inside the timed region.  `extras` holds the other
+workloads' steps (each with its dominant kernel's roofline), the per-step
+delayed-scaling metrics of the GPT-2-small batch, the outlier workload's
+zero-flush rates, the comparators (unfused three-pass quantize, cuBLAS BF16,
+cuBLASLt FP8) and the path's other rows.
 
 `--impl reference` times the CPU oracle (the plain C reference the tests check
 against) on a bounded sample of rows of the same workload and reports it in the
-same metric and unit.
+same metric and unit.  `--rows M` runs the workload with M rows (a smaller
+case for counter captures); `--profile` runs a few eager steps only, without
+timing, for `ncu`.
 
 Prints one JSON line on rank 0.
 """
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -46,6 +54,7 @@ METRIC = "FP8 down-proj fwd TFLOP/s (fused quant+GEMM); quant kernel HBM GB/s"
 UNIT = "TFLOP/s"
 PROFILES = os.path.join(ROOT, "profiles")
 L2_FLUSH_BYTES = 256 << 20
+DEFAULT_WORKLOAD = "gpt2xl"
 
 
 def flush_l2(buf: torch.Tensor) -> None:
@@ -197,24 +206,29 @@ def profiled_traffic(kernel_key: str, source: str):
         return None
 
 
+def workload(name: str, rows: int | None):
+    w = WL.WORKLOADS[name]
+    return w if not rows else dataclasses.replace(w, M=int(rows))
+
+
 # -------------------------------------------------------------- reference --
 def run_reference(args, world, rank):
     """The CPU oracle, timed on this host's cores on a bounded sample of rows."""
     if rank != 0:
         return
     import oracle as O
-    w = WL.WORKLOADS[args.workload]
+    w = workload(args.workload, args.rows)
     threads = O.default_threads()
-    h = WL.h_preact(w, 0)
+    rows_per_step = max(1, min(args.ref_rows, w.M))
+    h = WL.h_preact(dataclasses.replace(w, M=min(w.M, 4096)), 0)  # the rows a step samples from
     Wb = WL.w_down(w)
     sw = O.delayed_scale(O.amax(Wb, O.ACT_IDENTITY), w.margin, O.E4M3)
     wq = O.quant(Wb, O.ACT_IDENTITY, O.E4M3, sw, want_act=False, nthreads=threads)["q"]
-    rows_per_step = max(1, args.ref_rows)
-    sx = O.delayed_scale(O.amax(h[:rows_per_step], O.ACT_RELU2), w.margin, O.E4M3)
+    sx = O.delayed_scale(O.amax(h, O.ACT_RELU2), w.margin, O.E4M3)
     rng = np.random.default_rng(0)
 
     def one_step():
-        r0 = int(rng.integers(0, w.M - rows_per_step + 1))
+        r0 = int(rng.integers(0, h.shape[0] - rows_per_step + 1))
         hs = h[r0:r0 + rows_per_step]
         rq = O.quant(hs, O.ACT_RELU2, O.E4M3, sx, nthreads=threads)
         O.gemm_fwd(rq["q"], wq, sx, sw, nthreads=threads)
@@ -234,7 +248,7 @@ def run_reference(args, world, rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded numpy normals rounded to BF16)",
-        "config": {"workload": args.workload, "M": w.M, "K": w.K, "N": w.N, "act": "relu2",
+        "config": {"workload": w.name, "M": w.M, "K": w.K, "N": w.N, "act": "relu2",
                    "margin": w.margin, "l2": "sampled rows on the CPU"},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -242,176 +256,39 @@ def run_reference(args, world, rank):
     print(json.dumps(line), flush=True)
 
 
-def cpu_baseline(w, h_bits, w_bits, rows: int) -> dict:
+def cpu_baseline(w, h_bits, w_bits, gemm_rows: int) -> dict:
+    """The oracle on this host's cores, in the two parts the step has: the
+    fused quantize of the full H (and the W cast), as GB/s of the 5 bytes per
+    element the kernel moves; and the double-precision GEMM on a sample of rows,
+    per row, with the full GEMM's time extrapolated from it.  value = the
+    metric (TFLOP/s of the whole step) with that extrapolated time."""
     import oracle as O
     threads = O.default_threads()
     sw = O.delayed_scale(O.amax(w_bits, O.ACT_IDENTITY), w.margin, O.E4M3)
+    sx = O.delayed_scale(O.amax(h_bits[:4096], O.ACT_RELU2), w.margin, O.E4M3)
     t0 = time.perf_counter()
     wq = O.quant(w_bits, O.ACT_IDENTITY, O.E4M3, sw, want_act=False, nthreads=threads)["q"]
-    hs = h_bits[:rows]
-    sx = O.delayed_scale(O.amax(hs, O.ACT_RELU2), w.margin, O.E4M3)
-    rq = O.quant(hs, O.ACT_RELU2, O.E4M3, sx, nthreads=threads)
-    O.gemm_fwd(rq["q"], wq, sx, sw, nthreads=threads)
-    dt = time.perf_counter() - t0
-    return {"value": 2.0 * rows * w.N * w.K / dt / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
-            "sample": f"first {rows} rows of H: W cast, fused quantize of the rows, double-precision GEMM "
-                      f"of the rows against all {w.N} columns; {dt:.2f} s"}
+    rq = O.quant(h_bits, O.ACT_RELU2, O.E4M3, sx, nthreads=threads)
+    t_quant = time.perf_counter() - t0
+    rows = np.arange(min(gemm_rows, w.M), dtype=np.int64)
+    t0 = time.perf_counter()
+    O.gemm_fwd(rq["q"], wq, sx, sw, rows=rows, nthreads=threads)
+    t_rows = time.perf_counter() - t0
+    del rq
+    per_row = t_rows / rows.size
+    t_gemm_full = per_row * w.M
+    qbytes = 5.0 * w.M * w.K + 3.0 * w.K * w.N
+    return {"value": 2.0 * w.M * w.N * w.K / (t_quant + t_gemm_full) / 1e12, "unit": UNIT, "cores": threads,
+            "kind": "oracle",
+            "quant_gbs": qbytes / t_quant / 1e9, "quant_s": t_quant,
+            "gemm_ms_per_row": per_row * 1e3, "gemm_full_extrapolated_s": t_gemm_full,
+            "sample": (f"quantize of the full H [{w.M},{w.K}] and the W cast: {t_quant:.2f} s; double-precision "
+                       f"GEMM of the first {rows.size} rows against all {w.N} columns: {t_rows:.2f} s, "
+                       f"{per_row * 1e3:.2f} ms per row, the full {w.M}-row GEMM extrapolated to "
+                       f"{t_gemm_full:.1f} s; value = 2MNK / (quantize + extrapolated GEMM)")}
 
 
 # --------------------------------------------------------------------- ours --
-def run_ours(args, world, rank, local):
-    from quantize_fp8_gemm_gb300 import binding as B
-    from quantize_fp8_gemm_gb300.downproj import Fp8DownProj
-
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    w = WL.WORKLOADS[args.workload]
-    M, K, N = w.M, w.K, w.N
-    peaks = measured_peaks()
-    fp8 = fp8_peak(dev)
-    fp8_peak_tflops = fp8["tflops"]
-
-    # inputs: seeded host tensors, resident in HBM before timing
-    h_bits = [WL.h_preact(w, s) for s in range(2)]
-    w_bits = WL.w_down(w)
-    H = [WL.bf16_tensor(b).to(dev) for b in h_bits]
-    Wt = WL.bf16_tensor(w_bits).to(dev)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
-
-    dp = Fp8DownProj(M, K, N, margin=w.margin, history_len=w.history_len, device=dev)
-    dp.calibrate(H[0], Wt)
-
-    # Headline: the whole step as one CUDA graph (no host work between its
-    # kernels), timed with events recorded around each replay on the launching
-    # stream.  A torch build that cannot capture falls back to eager launches.
-    for i in range(args.warmup):
-        flush_l2(flush)
-        dp.step(H[i % 2], Wt)
-    torch.cuda.synchronize()
-    graphs = None
-    timing_mode = "eager"
-    if not args.eager:
-        try:
-            graphs = dp.capture(H[0], Wt, H_next=H[1])  # replays alternate H[0] / H[1]
-            timing_mode = "cuda-graph"
-        except RuntimeError as exc:  # capture refused
-            timing_mode = f"eager (graph capture unavailable: {exc})"[:200]
-            graphs = None
-
-    def run_step(i):
-        if graphs is not None:
-            graphs.replay()
-        else:
-            dp.step(H[i % 2], Wt)
-
-    for i in range(args.warmup):
-        flush_l2(flush)
-        run_step(i)
-    torch.cuda.synchronize()
-
-    pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    barrier(world)
-    torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
-        wall0 = time.perf_counter()
-        for i in range(args.steps):
-            flush_l2(flush)
-            pairs[i][0].record()
-            run_step(i)
-            pairs[i][1].record()
-        torch.cuda.synchronize()
-        wall = time.perf_counter() - wall0
-        # the step's kernels for the rooflines: each as back-to-back launches
-        # over input copies larger than L2, one event pair around them
-        kern_ms = kernel_times(dp, H, Wt, w, dev, reps=max(24, min(args.steps, 400)))
-    barrier(world)
-    step_ms = np.array([a.elapsed_time(b) for a, b in pairs])
-    local_ms = float(step_ms.mean())
-    flops_step = 2.0 * M * N * K
-    ms, total_flops = reduce_over_ranks(local_ms, flops_step, world)
-    value = total_flops / (ms * 1e-3) / 1e12
-    kern_ms["step"] = local_ms
-
-    quant_bytes = 5.0 * M * K + 3.0 * K * N  # H in, BF16 act + E4M3 out; W in, W_q^T out
-    quant_gbs = quant_bytes / (kern_ms["quant"] * 1e-3) / 1e9
-    gemm_tflops = flops_step / (kern_ms["gemm"] * 1e-3) / 1e12
-    quant_src = os.path.join(ROOT, "quantize_fp8_gemm_gb300", "csrc", "quant.cu")
-    gemm_src = os.path.join(ROOT, "quantize_fp8_gemm_gb300", "csrc", "gemm.cu")
-    roof_quant = {"bound": "hbm", "kernel": "quant_batch_kernel (fp8_quant_fused_batch: W cast + H quantize)",
-                  "achieved": quant_gbs,
-                  "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": quant_gbs / peaks["hbm_gbs"],
-                  "traffic": profiled_traffic(f"quant_batch_{args.workload}", quant_src),
-                  "algorithmic_bytes": quant_bytes, "peak_source": peaks["source"]}
-    roof_gemm = {"bound": "tensor", "kernel": "fp8_gemm_kernel (fp8_gemm_fwd)", "achieved": gemm_tflops,
-                 "peak": fp8_peak_tflops, "unit": "TFLOP/s", "frac": gemm_tflops / fp8_peak_tflops,
-                 "traffic": profiled_traffic(f"fp8_gemm_{args.workload}", gemm_src),
-                 "algorithmic_flops": flops_step,
-                 "peak_source": fp8["source"]}
-    dominant = roof_quant if kern_ms["quant"] >= kern_ms["gemm"] else roof_gemm
-    roof_fused = None
-    if "fused_step_kernel" in kern_ms:
-        fused_bytes = quant_bytes + 2.0 * M * N  # + Y
-        fused_gbs = fused_bytes / (kern_ms["fused_step_kernel"] * 1e-3) / 1e9
-        roof_fused = {"bound": "hbm", "kernel": "fp8_gemm_kernel<FUSED> (fp8_downproj_fwd_ex: the one-launch step)",
-                      "achieved": fused_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                      "frac": fused_gbs / peaks["hbm_gbs"],
-                      "traffic": profiled_traffic(f"fp8_fused_{args.workload}", gemm_src),
-                      "algorithmic_bytes": fused_bytes, "peak_source": peaks["source"],
-                      "tensor_tflops": flops_step / (kern_ms["fused_step_kernel"] * 1e-3) / 1e12}
-        dominant = roof_fused
-
-    if dp.fused:
-        step_desc = "W cast, quantize of H, FP8 GEMM and the 2 history updates in one kernel"
-        launches_per_step = 1
-    elif dp.chunks == 1:
-        step_desc = "W cast + quantize of H in one launch, then the FP8 GEMM, which also runs the 2 history updates"
-        launches_per_step = 2
-    else:
-        step_desc = f"W cast, {dp.chunks} x (row-block quantize + its GEMM), 2 history updates"
-        launches_per_step = 3 + 2 * dp.chunks
-    st = int(dp.gemm_status.item())
-    if st != 0:
-        raise RuntimeError(f"GEMM reported device status {st}")
-
-    extras = {}
-    if not args.no_extras:
-        extras = measure_extras(args, dp, H, Wt, flush, kern_ms, w, dev, fp8_peak_tflops)
-
-    e2e = measure_e2e(args, dp, h_bits, w_bits, flush, w, dev, use_graph=graphs is not None)
-
-    if rank != 0:
-        return
-    clocks = clk.summary()
-    line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "e4m3 x e4m3 -> f32 accumulate -> bf16",
-        "data": "synthetic (seeded numpy normals rounded to BF16, uploaded before timing)",
-        "config": {"workload": args.workload, "M": M, "K": K, "N": N, "act": "relu2",
-                   "scaling": "per-tensor delayed", "margin": w.margin, "history": w.history_len,
-                   "l2": "flushed before every step (256 MiB write + read, untimed)",
-                   "step": step_desc},
-        "kernel_ms": kern_ms,
-        "quant_hbm_gbs": quant_gbs,
-        "gemm_tflops": gemm_tflops,
-        "roofline": dominant,
-        "roofline_quant": roof_quant,
-        "roofline_gemm": roof_gemm,
-        "fp8_peak": fp8,
-        "roofline_fused": roof_fused,
-        "cpu_baseline": cpu_baseline(w, h_bits[0], w_bits, args.cpu_rows) if world == 1 else None,
-        "e2e": e2e,
-        "gpu_launches": launches_per_step * args.steps,
-        "kernel_ms_note": ("each kernel as back-to-back launches over input copies larger than L2, "
-                           "captured in one CUDA graph (average device time per launch, one event pair)"),
-        "timing": timing_mode,
-        "clocks": clocks,
-        "wall_s_timed_loop": wall,
-        "extras": extras,
-    }
-    print(json.dumps(line), flush=True)
-
-
 def timed_b2b(fns, reps: int) -> float:
     """Average device ms per launch of `reps` back-to-back calls cycling through
     fns (each reading its own inputs): the calls are captured into one CUDA
@@ -449,6 +326,18 @@ def timed_b2b(fns, reps: int) -> float:
     return a.elapsed_time(b) / reps
 
 
+def timed_steps(run_step, flush, steps: int) -> np.ndarray:
+    """Device ms of each of `steps` calls of run_step(i), L2 flushed before each."""
+    pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for i in range(steps):
+        flush_l2(flush)
+        pairs[i][0].record()
+        run_step(i)
+        pairs[i][1].record()
+    torch.cuda.synchronize()
+    return np.array([a.elapsed_time(b) for a, b in pairs])
+
+
 def kernel_times(dp, H, Wt, w, dev, reps: int) -> dict:
     """Device ms per launch of the step's kernels.  Inputs rotate over copies
     that together exceed L2 (4 x H for the casts, 8 x X_q for the GEMM), so no
@@ -473,7 +362,8 @@ def kernel_times(dp, H, Wt, w, dev, reps: int) -> dict:
     out["w_cast"] = timed_b2b([lambda: B.fp8_quant_fused_ex(Wt, B.ACT_IDENTITY, B.E4M3, sw, q_t_out=wtq,
                                                             amax_out=aw, flags=B.ACCUMULATE)], reps)
     del act
-    xqs = [torch.empty_like(dp.x_q).copy_(dp.x_q) for _ in range(8)]
+    nx = max(2, min(8, -(-(256 << 20) // (M * K))))
+    xqs = [torch.empty_like(dp.x_q).copy_(dp.x_q) for _ in range(nx)]
     y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
     out["gemm"] = timed_b2b([lambda x=x: B.fp8_gemm_fwd(x, dp.wt_q, sx, sw, y) for x in xqs], reps)
     del xqs
@@ -495,25 +385,318 @@ def kernel_times(dp, H, Wt, w, dev, reps: int) -> dict:
     return out
 
 
-def timed(fn, flush, reps: int) -> float:
-    """Mean device ms of fn() over reps, L2 flushed before each."""
-    ts = []
-    for _ in range(reps):
+def rooflines(w, kern_ms: dict, peaks: dict, fp8: dict, workload_key: str) -> dict:
+    """The rooflines of a per-tensor step's kernels: the one-launch cast (HBM),
+    the FP8 GEMM (tensor) and, where the step runs it, the one-launch step
+    kernel, which is bound by both: its roofline time is the larger of its
+    algorithmic bytes over the HBM peak and its FLOPs over the FP8 peak."""
+    M, K, N = w.M, w.K, w.N
+    flops = 2.0 * M * N * K
+    quant_bytes = 5.0 * M * K + 3.0 * K * N  # H in, BF16 act + E4M3 out; W in, W_q^T out
+    quant_gbs = quant_bytes / (kern_ms["quant"] * 1e-3) / 1e9
+    gemm_tflops = flops / (kern_ms["gemm"] * 1e-3) / 1e12
+    quant_src = os.path.join(ROOT, "quantize_fp8_gemm_gb300", "csrc", "quant.cu")
+    gemm_src = os.path.join(ROOT, "quantize_fp8_gemm_gb300", "csrc", "gemm.cu")
+    out = {
+        "quant": {"bound": "hbm", "kernel": "quant_batch_kernel (fp8_quant_fused_batch: W cast + H quantize)",
+                  "achieved": quant_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                  "frac": quant_gbs / peaks["hbm_gbs"],
+                  "traffic": profiled_traffic(f"quant_batch_{workload_key}", quant_src),
+                  "algorithmic_bytes": quant_bytes, "peak_source": peaks["source"] + " (burst copy)"},
+        "gemm": {"bound": "tensor", "kernel": "fp8_gemm_kernel (fp8_gemm_fwd)", "achieved": gemm_tflops,
+                 "peak": fp8["tflops"], "unit": "TFLOP/s", "frac": gemm_tflops / fp8["tflops"],
+                 "traffic": profiled_traffic(f"fp8_gemm_{workload_key}", gemm_src),
+                 "algorithmic_flops": flops, "peak_source": fp8["source"]},
+    }
+    out["dominant"] = out["quant"] if kern_ms["quant"] >= kern_ms["gemm"] else out["gemm"]
+    if "fused_step_kernel" in kern_ms:
+        t = kern_ms["fused_step_kernel"] * 1e-3
+        fbytes = quant_bytes + 2.0 * M * N  # + Y
+        t_hbm = fbytes / (peaks["hbm_gbs"] * 1e9)
+        t_mma = flops / (fp8["tflops"] * 1e12)
+        hbm_bound = t_hbm >= t_mma
+        f = {"bound": "hbm" if hbm_bound else "tensor",
+             "kernel": "fp8_gemm_kernel<FUSED> (fp8_downproj_fwd_ex: the one-launch step)",
+             "achieved": fbytes / t / 1e9 if hbm_bound else flops / t / 1e12,
+             "peak": peaks["hbm_gbs"] if hbm_bound else fp8["tflops"],
+             "unit": "GB/s" if hbm_bound else "TFLOP/s", "frac": max(t_hbm, t_mma) / t,
+             "traffic": profiled_traffic(f"fp8_fused_{workload_key}", gemm_src),
+             "algorithmic_bytes": fbytes, "algorithmic_flops": flops,
+             "hbm_gbs": fbytes / t / 1e9, "hbm_frac": t_hbm / t,
+             "tensor_tflops": flops / t / 1e12, "tensor_frac": t_mma / t,
+             "roofline_ms": max(t_hbm, t_mma) * 1e3,
+             "peak_source": f"HBM: {peaks['source']} copy; FP8: {fp8['source']}"}
+        out["fused"] = f
+        out["dominant"] = f
+    return out
+
+
+def measure_step(w, dev, steps: int, warmup: int, flush, eager: bool = False, group: bool = False):
+    """Build the step's state for workload w, calibrate, capture the step as CUDA
+    graphs, run `warmup` untimed steps and time `steps` steps (L2 flushed before
+    each).  Returns the state, the inputs, the per-step ms, the timing mode and
+    the wall time of the timed loop."""
+    from quantize_fp8_gemm_gb300.downproj import Fp8DownProj
+    h_bits = [WL.h_preact(w, s) for s in range(2)]
+    w_bits = WL.w_down(w)
+    H = [WL.bf16_tensor(b).to(dev) for b in h_bits]
+    Wt = WL.bf16_tensor(w_bits).to(dev)
+    dp = Fp8DownProj(w.M, w.K, w.N, margin=w.margin, history_len=w.history_len, group=group, device=dev)
+    dp.calibrate(H[0], Wt)
+    for i in range(warmup):
         flush_l2(flush)
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        fn()
-        b.record()
-        ts.append((a, b))
+        dp.step(H[i % 2], Wt)
     torch.cuda.synchronize()
-    return float(np.mean([a.elapsed_time(b) for a, b in ts]))
+    graphs, mode = None, "eager"
+    if not eager:
+        try:
+            graphs = dp.capture(H[0], Wt, H_next=H[1])  # replays alternate H[0] / H[1]
+            mode = "cuda-graph"
+        except RuntimeError as exc:  # capture refused
+            mode = f"eager (graph capture unavailable: {exc})"[:200]
+
+    def run_step(i):
+        if graphs is not None:
+            graphs.replay()
+        else:
+            dp.step(H[i % 2], Wt)
+
+    for i in range(warmup):
+        flush_l2(flush)
+        run_step(i)
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    step_ms = timed_steps(run_step, flush, steps)
+    wall = time.perf_counter() - wall0
+    st = int(dp.gemm_status.item())
+    if st != 0:
+        raise RuntimeError(f"GEMM reported device status {st} on {w.name}")
+    return dict(dp=dp, H=H, Wt=Wt, h_bits=h_bits, w_bits=w_bits, step_ms=step_ms, mode=mode, wall=wall,
+                graphs=graphs)
 
 
-def measure_extras(args, dp, H, Wt, flush, kern_ms, w, dev, fp8_peak_tflops: float) -> dict:
-    """Comparators, timed like kern_ms (back-to-back over 4 rotating copies of
-    H): the unfused three-pass quantize (write the activation, an amax pass, a
-    cast pass) against the fused quantize of H alone, and cuBLAS BF16 on the
-    BF16 activation against the FP8 GEMM."""
+def step_desc(dp) -> tuple[str, int]:
+    if dp.fused:
+        return "W cast, quantize of H, FP8 GEMM and the 2 history updates in one kernel", 1
+    if dp.group:
+        return ("128x128 block cast of W, 1x128 group quantize of H, group-scaled FP8 GEMM "
+                "(no delayed scales to update)"), 3
+    if dp.chunks == 1:
+        return "W cast + quantize of H in one launch, then the FP8 GEMM, which also runs the 2 history updates", 2
+    return f"W cast, {dp.chunks} x (row-block quantize + its GEMM), 2 history updates", 3 + 2 * dp.chunks
+
+
+def run_profile(args, local):
+    """A few eager steps of the workload, nothing timed: the command ncu wraps."""
+    from quantize_fp8_gemm_gb300.downproj import Fp8DownProj
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = workload(args.workload, args.rows)
+    H = WL.bf16_tensor(WL.h_preact(w, 0)).to(dev)
+    Wt = WL.bf16_tensor(WL.w_down(w)).to(dev)
+    dp = Fp8DownProj(w.M, w.K, w.N, margin=w.margin, history_len=w.history_len, device=dev)
+    dp.calibrate(H, Wt)
+    for _ in range(max(1, args.steps)):
+        dp.step(H, Wt)
+    torch.cuda.synchronize()
+    st = int(dp.gemm_status.item())
+    print(json.dumps({"profile": w.name, "M": w.M, "K": w.K, "N": w.N, "fused": dp.fused, "steps": args.steps,
+                      "status": st}), flush=True)
+    if st != 0:
+        raise SystemExit(1)
+
+
+def run_ours(args, world, rank, local):
+    from quantize_fp8_gemm_gb300 import binding as B  # noqa: F401  (fails loudly without the library)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = workload(args.workload, args.rows)
+    M, K, N = w.M, w.K, w.N
+    peaks = measured_peaks()
+    fp8 = fp8_peak(dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+
+    barrier(world)
+    torch.cuda.synchronize()
+    # clocks sampled while the steps and then the kernel rooflines run (the
+    # latter keep the GPU loaded for a few seconds, so the samples see it busy)
+    with ClockSampler(local) as clk:
+        r = measure_step(w, dev, args.steps, args.warmup, flush, eager=args.eager)
+        barrier(world)
+        dp, H, Wt = r["dp"], r["H"], r["Wt"]
+        kern_ms = kernel_times(dp, H, Wt, w, dev, reps=max(24, min(args.steps, 400)))
+    clocks = clk.summary()
+    local_ms = float(r["step_ms"].mean())
+    flops_step = 2.0 * M * N * K
+    ms, total_flops = reduce_over_ranks(local_ms, flops_step, world)
+    value = total_flops / (ms * 1e-3) / 1e12
+    kern_ms["step"] = local_ms
+    roof = rooflines(w, kern_ms, peaks, fp8, w.name if not args.rows else f"{w.name}_m{w.M}")
+    desc, launches_per_step = step_desc(dp)
+
+    extras = {}
+    if not args.no_extras:
+        extras = measure_extras(args, dp, H, Wt, flush, kern_ms, w, dev, fp8, peaks)
+
+    e2e = measure_e2e(args, dp, r["h_bits"], r["w_bits"], flush, w, dev, use_graph=r["graphs"] is not None)
+    wall, mode = r["wall"], r["mode"]
+    del r
+    if rank != 0:
+        return
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        h0 = WL.h_preact(w, 0)
+        cpu = cpu_baseline(w, h0, WL.w_down(w), args.cpu_rows)
+        del h0
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e4m3 x e4m3 -> f32 accumulate -> bf16",
+        "data": "synthetic (seeded numpy normals rounded to BF16, uploaded before timing)",
+        "config": {"workload": w.name, "M": M, "K": K, "N": N, "act": "relu2",
+                   "scaling": "per-tensor delayed", "margin": w.margin, "history": w.history_len,
+                   "l2": "flushed before every step (256 MiB write + read, untimed)",
+                   "step": desc},
+        "kernel_ms": kern_ms,
+        "quant_hbm_gbs": roof["quant"]["achieved"],
+        "gemm_tflops": roof["gemm"]["achieved"],
+        "roofline": roof["dominant"],
+        "roofline_quant": roof["quant"],
+        "roofline_gemm": roof["gemm"],
+        "roofline_fused": roof.get("fused"),
+        "fp8_peak": fp8,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+        "kernel_ms_note": ("each kernel as back-to-back launches over input copies larger than L2, "
+                           "captured in one CUDA graph (average device time per launch, one event pair)"),
+        "timing": f"{mode}: one event pair around each step on the launching stream",
+        "clocks": clocks,
+        "wall_s_timed_loop": wall,
+        "extras": extras,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def measure_other_config(name: str, dev, flush, fp8: dict, peaks: dict, steps: int, group: bool = False) -> dict:
+    """One of the smaller workloads' steps, timed like the headline (CUDA-graph
+    replays, L2 flushed before each), with its kernels' rooflines."""
+    from quantize_fp8_gemm_gb300 import binding as B
+    w = WL.WORKLOADS[name]
+    r = measure_step(w, dev, steps, 3, flush, group=group)
+    dp = r["dp"]
+    ms = float(r["step_ms"].mean())
+    flops = 2.0 * w.M * w.N * w.K
+    desc, launches = step_desc(dp)
+    row = {"shape": f"H [{w.M},{w.K}] x W [{w.K},{w.N}]", "step": desc, "launches_per_step": launches,
+           "step_ms": ms, "TFLOP/s": flops / (ms * 1e-3) / 1e12, "timing": r["mode"]}
+    reps = max(24, min(steps, 200))
+    if not group:
+        km = kernel_times(dp, r["H"], r["Wt"], w, dev, reps)
+        roof = rooflines(w, km, peaks, fp8, name)
+        row["kernel_ms"] = km
+        row["roofline"] = roof["dominant"]
+        row["roofline_quant"] = roof["quant"]
+        row["roofline_gemm"] = roof["gemm"]
+        if "fused" in roof:
+            row["roofline_fused"] = roof["fused"]
+    else:
+        M, K, N = w.M, w.K, w.N
+        Hs = r["H"] + [r["H"][0].clone(), r["H"][1].clone()]
+        act = torch.empty(M, K, dtype=torch.bfloat16, device=dev)
+        amax = torch.zeros(1, device=dev)
+        t_q = timed_b2b([lambda h=h: B.fp8_quant_fused_ex(h, dp.act, B.E4M3, None, act_out=act, q_out=dp.x_q,
+                                                          amax_out=amax, group_scales_out=dp.x_gscale,
+                                                          group_rows=1, flags=B.ACCUMULATE) for h in Hs], reps)
+        xqs = [dp.x_q.clone() for _ in range(4)]
+        y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+        t_g = timed_b2b([lambda x=x: B.fp8_gemm_fwd(x, dp.wt_q, dp.x_gscale, dp.w_gscale, y, group_mode=1)
+                         for x in xqs], reps)
+        qb = 5.0 * M * K + 4.0 * M * (K // 128)
+        row["kernel_ms"] = {"group_quant": t_q, "group_gemm": t_g}
+        rq = {"bound": "hbm", "kernel": "quant_stream_kernel<GROUP> (1x128)", "achieved": qb / (t_q * 1e-3) / 1e9,
+              "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": qb / (t_q * 1e-3) / 1e9 / peaks["hbm_gbs"],
+              "algorithmic_bytes": qb}
+        tf = flops / (t_g * 1e-3) / 1e12
+        rg = {"bound": "tensor", "kernel": "fp8_gemm_kernel<GROUP>", "achieved": tf, "peak": fp8["tflops"],
+              "unit": "TFLOP/s", "frac": tf / fp8["tflops"], "algorithmic_flops": flops}
+        row["roofline_quant"], row["roofline_gemm"] = rq, rg
+        row["roofline"] = rq if t_q >= t_g else rg
+        del Hs, act, xqs, y
+    del r, dp
+    torch.cuda.empty_cache()
+    return row
+
+
+def drift_metrics(dev, max_steps: int) -> dict:
+    """The GPT-2-small batch's delayed-scaling record: per step, the scale the
+    step used, its amax and its saturation count, over the workload's 20 steps
+    of drifting H (fresh seeded draws each step)."""
+    from quantize_fp8_gemm_gb300.downproj import Fp8DownProj
+    w = WL.WORKLOADS["gpt2s_batch"]
+    Wt = WL.bf16_tensor(WL.w_down(w)).to(dev)
+    dp = Fp8DownProj(w.M, w.K, w.N, margin=w.margin, history_len=w.history_len, keep_act=False, device=dev)
+    H = WL.bf16_tensor(WL.h_preact(w, 0, WL.drift_std(w, 0))).to(dev)
+    dp.calibrate(H, Wt)
+    rec = {"step": [], "std": [], "scale_x": [], "amax_x": [], "saturated_x": [], "scale_w": [], "amax_w": [],
+           "saturated_w": []}
+    for t in range(min(w.steps, max_steps)):
+        std = WL.drift_std(w, t)
+        H.copy_(WL.bf16_tensor(WL.h_preact(w, t, std)))
+        sx, sw = float(dp.x.scale.item()), float(dp.w.scale.item())
+        dp.step(H, Wt)
+        torch.cuda.synchronize()
+        rec["step"].append(t)
+        rec["std"].append(std)
+        rec["scale_x"].append(sx)
+        rec["scale_w"].append(sw)
+        rec["amax_x"].append(float(dp.x.last_amax.item()))
+        rec["amax_w"].append(float(dp.w.last_amax.item()))
+        rec["saturated_x"].append(int(dp.x.last_sat.item()))
+        rec["saturated_w"].append(int(dp.w.last_sat.item()))
+    rec["step_path"] = step_desc(dp)[0]
+    del dp, H, Wt
+    torch.cuda.empty_cache()
+    return rec
+
+
+def outlier_flush_rates(dev) -> dict:
+    """The outlier workload's zero flush: the share of non-zero BF16 inputs to
+    the cast (the activation) whose E4M3 code is +-0, with one per-tensor scale
+    (the current amax, margin 1) against 1x128 group scales, for ReLU^2 and the
+    identity (whose +-1e5 entries keep their signs)."""
+    from quantize_fp8_gemm_gb300 import binding as B
+    w = WL.WORKLOADS["outlier"]
+    M, K = w.M, w.K
+    H = WL.bf16_tensor(WL.h_preact(w)).to(dev)
+    act = torch.empty(M, K, dtype=torch.bfloat16, device=dev)
+    q = torch.empty(M, K, dtype=torch.uint8, device=dev)
+    amax = torch.zeros(1, device=dev)
+    gs = torch.empty(M, K // 128, device=dev)
+    out = {}
+    for name, a in (("relu2", B.ACT_RELU2), ("identity", B.ACT_IDENTITY)):
+        one = torch.ones(1, device=dev)
+        B.fp8_quant_fused(H, a, B.E4M3, one, act_out=act, amax_out=amax)  # amax pass
+        scale = (448.0 / amax).to(torch.float32)  # the current amax, margin 1 (the pages' experiment)
+        nz = (act.view(torch.int16) & 0x7FFF) != 0
+        n_nz = int(nz.sum().item())
+        B.fp8_quant_fused(H, a, B.E4M3, scale, q_out=q)
+        pt = int((nz & ((q & 0x7F) == 0)).sum().item()) / n_nz
+        B.fp8_quant_fused(H, a, B.E4M3, None, q_out=q, group_scales_out=gs, group_rows=1)
+        gr = int((nz & ((q & 0x7F) == 0)).sum().item()) / n_nz
+        out[name] = {"per_tensor_scale": float(scale.item()), "flushed_per_tensor": pt, "flushed_1x128": gr,
+                     "nonzero_inputs": n_nz}
+    del H, act, q, gs
+    torch.cuda.empty_cache()
+    return out
+
+
+def measure_extras(args, dp, H, Wt, flush, kern_ms, w, dev, fp8: dict, peaks: dict) -> dict:
+    """Comparators at the headline workload, timed like kern_ms (back-to-back
+    over 4 rotating copies of H): the unfused three-pass quantize (write the
+    activation, an amax pass, a cast pass) against the fused quantize of H
+    alone, cuBLAS BF16 on the BF16 activation against the FP8 GEMM, and the
+    BF16 path against the FP8 step; then the other workloads and rows."""
     from quantize_fp8_gemm_gb300 import binding as B
     M, K, N = w.M, w.K, w.N
     reps = max(24, min(400, args.steps))
@@ -528,19 +711,20 @@ def measure_extras(args, dp, H, Wt, flush, kern_ms, w, dev, fp8_peak_tflops: flo
         B.fp8q_naive_cast(a_naive, B.E4M3, amax, w.margin, q_naive)
 
     t_naive = timed_b2b([lambda h=h: naive(h) for h in Hs], reps)
-    acts = [torch.empty(M, K, dtype=torch.bfloat16, device=dev) for _ in range(4)]
+    del q_naive
+    acts = [torch.empty(M, K, dtype=torch.bfloat16, device=dev) for _ in range(2)]
     for h, act in zip(Hs, acts):
         B.fp8q_naive_act(h, B.ACT_RELU2, act)
     y16 = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
     t_bf16_gemm = timed_b2b([lambda a=a: torch.matmul(a, Wt, out=y16) for a in acts], reps)
     t_bf16_path = timed_b2b([lambda h=h: (B.fp8q_naive_act(h, B.ACT_RELU2, a_naive),
                                           torch.matmul(a_naive, Wt, out=y16)) for h in Hs], reps)
-    del acts, Hs
+    del acts, Hs, a_naive
     # the library's FP8 GEMM (cuBLASLt E4M3 x E4M3 -> BF16 via torch._scaled_mm) on the same
-    # operands, over the same 8 rotating copies of X_q as the FP8 GEMM's own timing
+    # operands, over rotating copies of X_q like the FP8 GEMM's own timing
     t_lib_fp8 = None
     try:
-        xqs = [dp.x_q.clone().view(torch.float8_e4m3fn) for _ in range(8)]
+        xqs = [dp.x_q.clone().view(torch.float8_e4m3fn) for _ in range(2)]
         wtq = dp.wt_q.view(torch.float8_e4m3fn).t()  # [K,N], column-major
         s_x, s_w = (1.0 / dp.x.scale).reshape(()), (1.0 / dp.w.scale).reshape(())  # dequantisation factors
         t_lib_fp8 = timed_b2b([lambda x=x: torch._scaled_mm(x, wtq, scale_a=s_x, scale_b=s_w,
@@ -548,11 +732,11 @@ def measure_extras(args, dp, H, Wt, flush, kern_ms, w, dev, fp8_peak_tflops: flo
         del xqs
     except (RuntimeError, TypeError, AttributeError):
         pass
-    rows = measure_other_rows(dev, max(16, min(64, args.steps)), fp8_peak_tflops)
+    torch.cuda.empty_cache()
     t_fused = kern_ms["quant_h_only"]
-    t_fp8_path = kern_ms["quant"] + kern_ms["gemm"]
+    t_fp8_step = kern_ms.get("fused_step_kernel", kern_ms["quant"] + kern_ms["gemm"])
     flops = 2.0 * M * N * K
-    return {
+    out = {
         "naive_3pass_ms": t_naive, "fused_quant_ms": t_fused,
         "fused_vs_naive_speedup": t_naive / t_fused, "fused_vs_naive_ideal": 9.0 / 5.0,
         "bf16_gemm_ms": t_bf16_gemm, "bf16_gemm_tflops": flops / (t_bf16_gemm * 1e-3) / 1e12,
@@ -561,11 +745,23 @@ def measure_extras(args, dp, H, Wt, flush, kern_ms, w, dev, fp8_peak_tflops: flo
         "cublaslt_fp8_gemm_tflops": flops / (t_lib_fp8 * 1e-3) / 1e12 if t_lib_fp8 else None,
         "fp8_gemm_vs_cublaslt_fp8_speedup": t_lib_fp8 / kern_ms["gemm"] if t_lib_fp8 else None,
         "bf16_path_ms (BF16 activation write + cuBLAS BF16 GEMM)": t_bf16_path,
-        "fp8_path_ms (one-launch W + H cast + FP8 GEMM)": t_fp8_path,
-        "fp8_vs_bf16_end_to_end_speedup": t_bf16_path / t_fp8_path,
-        "timing": "back-to-back launches over 4 rotating input copies (> L2) in one CUDA graph, one event pair",
-        "other_rows": rows,
+        "fp8_path_ms (the FP8 step's kernels)": t_fp8_step,
+        "fp8_vs_bf16_end_to_end_speedup": t_bf16_path / t_fp8_step,
+        "fp8_unfused_path_ms (one-launch W + H cast, then the FP8 GEMM)": kern_ms["quant"] + kern_ms["gemm"],
+        "timing": "back-to-back launches over rotating input copies (> L2) in one CUDA graph, one event pair",
+        "workload": w.name,
     }
+    cfg_steps = max(20, min(100, args.steps))
+    out["configs"] = {}
+    for name in ("gpt2s", "gpt2s_batch", "outlier"):
+        if name != w.name:
+            out["configs"][name] = measure_other_config(name, dev, flush, fp8, peaks, cfg_steps)
+    out["configs"]["outlier (1x128 / 128x128 group scales)"] = measure_other_config(
+        "outlier", dev, flush, fp8, peaks, cfg_steps, group=True)
+    out["gpt2s_batch_delayed_scaling_per_step"] = drift_metrics(dev, 20)
+    out["outlier_zero_flush"] = outlier_flush_rates(dev)
+    out["other_rows"] = measure_other_rows(dev, max(16, min(64, args.steps)), fp8["tflops"])
+    return out
 
 
 def measure_other_rows(dev, reps: int, fp8_tflops: float) -> dict:
@@ -732,16 +928,8 @@ def measure_e2e(args, dp, h_bits, w_bits, flush, w, dev, use_graph=True) -> dict
     for i in range(3):
         e2e_step(i)
     torch.cuda.synchronize()
-    ts = []
-    for i in range(steps):
-        flush_l2(flush)
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        e2e_step(i)
-        b.record()
-        ts.append((a, b))
-    torch.cuda.synchronize()
-    ms = float(np.mean([a.elapsed_time(b) for a, b in ts]))
+    ms = float(timed_steps(e2e_step, flush, steps).mean())
+    del g, Hd, Wd
     return {"value": 2.0 * M * N * K / (ms * 1e-3) / 1e12, "unit": UNIT,
             "h2d_bytes_per_step": 2 * M * K + 2 * K * N, "d2h_bytes_per_step": 2 * M * N,
             "ms_per_step": ms, "steps": steps}
@@ -750,17 +938,21 @@ def measure_e2e(args, dp, h_bits, w_bits, flush, w, dev, use_graph=True) -> dict
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=sorted(WL.WORKLOADS), default="gpt2s")
-    ap.add_argument("--cpu-rows", type=int, default=256, help="rows of H the CPU baseline processes")
+    ap.add_argument("--workload", choices=sorted(WL.WORKLOADS), default=DEFAULT_WORKLOAD)
+    ap.add_argument("--rows", type=int, default=0, help="run the workload with this many rows of H (0: its own)")
+    ap.add_argument("--cpu-rows", type=int, default=256, help="rows of the GEMM the CPU baseline times")
     ap.add_argument("--ref-rows", type=int, default=16, help="rows of H per reference-arm step")
     ap.add_argument("--no-extras", action="store_true", help="skip the comparator measurements")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the CPU oracle timing")
     ap.add_argument("--eager", action="store_true",
                     help="launch the step kernel by kernel instead of as a CUDA graph")
+    ap.add_argument("--profile", action="store_true",
+                    help="run --steps eager steps without timing (the command an ncu capture wraps)")
     args = ap.parse_args()
-    if args.warmup < 3 and args.impl == "ours":
+    if args.warmup < 3 and args.impl == "ours" and not args.profile:
         ap.error("--warmup must be at least 3")
     world, rank, local = dist_env()
     if world > 1:
@@ -770,6 +962,8 @@ def main():
     try:
         if args.impl == "reference":
             run_reference(args, world, rank)
+        elif args.profile:
+            run_profile(args, local)
         else:
             run_ours(args, world, rank, local)
     finally:

@@ -7,6 +7,7 @@
  *                           BF16 copy for backward + FP8 copy + amax
  *   2. fp8_gemm_fwd         Y = X_q W_q / (s_x s_w), FP32 accumulate, BF16 out
  *      (fp8_downproj_fwd    1 and 2 fused in one kernel)
+ *      (fp8_downproj_fwd_ex the weight cast, 1, 2 and 3 in one kernel)
  *   3. amax_history_update  push this step's amax; scale for the next step
  *      (fp8_gemm_fwd_update 2 and 3 in one launch: the GEMM runs the updates)
  *   (fp8_gemm_dgrad         dX = dY_q W_q^T / (s_dy s_w), the gradient shape)
@@ -29,6 +30,7 @@
  *    FP8Q_ERR_CUDA when a CUDA call or a launch fails.  Conditions only the
  *    GPU can see are OR-ed as FP8Q_DEV_* bits into the caller's optional
  *    device status word.  No call aborts the process or traps the GPU.
+ *  - Test and tuning hooks are declared apart, in fp8q_testing.h.
  *
  * Sources (page title, section):
  *  [fused]  "Paradigma Details FP8 and Optimizer Tricks Behind NanoGPT
@@ -326,9 +328,12 @@ int fp8_upproj_fwd(const void* x_q, const void* wt_q, const float* scale_x, cons
  *              bytes, 4-byte aligned, owned by the caller; zeroed by this call
  *              (stream-ordered), and left zero by the kernel when it
  *              finishes.  Two fused calls must not share it concurrently.
- * The kernel occupies every SM with one CTA and its CTAs wait on each
- * other's quantize work (bounded: a wait that runs out sets
- * FP8Q_DEV_TIMEOUT), so do not run two of them on the GPU at the same time.
+ * The kernel launches one CTA per SM.  Its CTAs take quantize (and weight
+ * cast) work by ticket from counters in the workspace, so a CTA only ever
+ * waits for work that a running CTA has taken: the kernel also completes
+ * when other work holds some SMs and only part of its grid is resident.
+ * Waits are bounded all the same (a wait that runs out sets
+ * FP8Q_DEV_TIMEOUT).
  * Same shape, alignment and error rules as fp8_quant_fused / fp8_gemm_fwd.
  */
 size_t fp8_downproj_workspace_bytes(int64_t M);
@@ -353,8 +358,11 @@ int fp8_downproj_fwd(const void* h, const void* wt_q, int64_t M, int64_t N, int6
  *            amax_w are ignored.
  *   w_q      device [K,N] E4M3 (the dgrad operand) or NULL.
  *   amax_w   device float or NULL: max |W|.
+ *   sat_w    device uint64 or NULL: the weight cast's count of |W * s_w| >
+ *            448, i.e. of values its scale saturated (the overflow test of
+ *            detect-and-recompute).  Needs w, like amax_w.
  *   flags    0, or FP8Q_ACCUMULATE: nothing is zeroed before the kernel
- *            (amax_x, sat_count, amax_w fold into their values; the workspace
+ *            (amax_x, sat_count, amax_w, sat_w fold into their values; the workspace
  *            must already be zero -- zero-filled before first use, then kept
  *            zero by the kernel).  After a call that reported FP8Q_DEV_TIMEOUT
  *            the workspace may hold counts: zero it again.
@@ -364,7 +372,8 @@ int fp8_downproj_fwd(const void* h, const void* wt_q, int64_t M, int64_t N, int6
  *            values, so a delayed-scaling step is this one launch.  The
  *            structs are read during the call only.  Need M > 0.
  * Results equal fp8_quant_fused_ex on W and H followed by fp8_gemm_fwd (and
- * amax_history_update_ex on X and W).
+ * amax_history_update_ex on X and W).  FP8Q_ERR_SHAPE also when W has more
+ * than 2^31 units of 8 x 256 values.
  */
 typedef struct fp8q_history_args {
     float* history;                 /* as amax_history_update_ex            */
@@ -381,7 +390,8 @@ typedef struct fp8q_history_args {
 int fp8_downproj_fwd_ex(const void* h, const void* w, void* wt_q, int64_t M, int64_t N, int64_t K,
                         int act, const float* scale_x, const float* scale_w,
                         void* act_out, void* x_q, float* amax_x, unsigned long long* sat_count,
-                        void* w_q, float* amax_w, void* y, void* workspace, size_t workspace_bytes,
+                        void* w_q, float* amax_w, unsigned long long* sat_w, void* y,
+                        void* workspace, size_t workspace_bytes,
                         const fp8q_history_args* hist_x, const fp8q_history_args* hist_w,
                         unsigned flags, int* status, cudaStream_t stream);
 
@@ -429,19 +439,21 @@ int fp8_gemm_fwd_update(const void* x_q, const void* wt_q,
  * being captured, where allocation calls are not allowed.
  *
  * Same arguments, results and error rules as fp8_downproj_fwd, minus
- * `workspace`: the per-block ready counts live in a fixed array of this
- * library's own device memory (FP8Q_NOALLOC_MAX_M / 128 + 64 counters, 8,448
- * bytes),
- * which every device that loads the library holds until the process exits.
+ * `workspace`: the kernel's counters (per-block ready counts, work tickets)
+ * live in a fixed array of this library's own device memory
+ * (FP8Q_NOALLOC_MAX_M / 128 + 64 counters, 8,448 bytes), which every device
+ * that loads the library holds until the process exits.
  *   M > FP8Q_NOALLOC_MAX_M  -> FP8Q_ERR_SHAPE (use fp8_downproj_fwd)
  * The call allocates nothing: no cudaMalloc / cudaFree, no allocating
- * library routine.  The first call with M > 0 on a device looks the array's
- * address up (cudaGetSymbolAddress, with that device current) and keeps it;
- * make that first call before any stream capture.  Every call clears the
- * counters it uses (stream-ordered) before its kernel starts, since the array
- * keeps the previous call's counts.  All calls on a device share the one
- * array: calls that overlap on the GPU race on it and give wrong results, so
- * order them on one stream (or with events).
+ * library routine.  Every call with M > 0 looks the array's address up
+ * (cudaGetSymbolAddress, on the current device), so the address stays right
+ * after a device reset, when the library's device code is loaded again in
+ * a new context.  The first call on a device is also the one that loads that
+ * code there if nothing else has: make it before any stream capture.  Every
+ * call clears the counters it uses (stream-ordered) before its kernel
+ * starts, since the array keeps what the previous call left.  All calls on a
+ * device share the one array: calls that overlap on the GPU race on it and
+ * give wrong results, so order them on one stream (or with events).
  */
 #define FP8Q_NOALLOC_MAX_M 262144
 int fp8_downproj_fwd_noalloc(const void* h, const void* wt_q, int64_t M, int64_t N, int64_t K, int act,
@@ -486,31 +498,6 @@ int amax_history_update_ex(float* history, int L, int* head, const float* amax_n
                            float margin, int fmt, const float* scale_prev, float* scale_out,
                            int* status, float* amax_clear, unsigned long long* sat_clear,
                            cudaStream_t stream);
-
-/*
- * fp8q_gemm_set_tile -- pin the GEMM tile shape (a tuning knob; "FP8 training:
- * what it is and how it works", Trade-offs and edge cases: tile size is a
- * tuning knob).  Process-wide; affects later per-tensor fp8_gemm_fwd /
- * fp8_gemm_dgrad calls.  The group-scaled GEMM takes the pins (0, 128),
- * (0, 192) and (0, 256) and ignores others.
- *   pair  -1: automatic choice (the default; bn ignored)
- *          0: one CTA per 128 x bn tile           bn in {128, 160, 192, 256}
- *          1: a CTA pair per 256 x bn tile (2-SM)  bn in {128, 160, 192, 224, 256, 384}
- *             (pairs are used only when M > 128; smaller M falls back to one CTA;
- *             384 is two 192-wide MMAs into one accumulator, plain GEMMs only:
- *             fp8_downproj_fwd takes 256 instead)
- * Returns FP8Q_ERR_UNSUPPORTED for any other combination (nothing changes).
- */
-int fp8q_gemm_set_tile(int pair, int bn);
-
-/*
- * fp8q_gemm_test_hold_loads -- failure-path test hook.  While on != 0, the
- * GEMM kernels launched afterwards issue no operand loads, so their first
- * bounded wait runs out (after about 2 s): the kernel ORs FP8Q_DEV_TIMEOUT
- * into the status word, releases its resources and exits, leaving the CUDA
- * context usable.  Process-wide; turn it off again with on = 0.
- */
-void fp8q_gemm_test_hold_loads(int on);
 
 /* Human-readable name of an fp8q_status value (static string). */
 const char* fp8q_status_string(int status);

@@ -16,6 +16,7 @@ import torch
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libfp8q.so")
+NAIVE_LIB_PATH = os.path.join(PKG, "libfp8q_naive.so")  # the unfused comparator (include/fp8q_naive.h)
 
 E4M3, E5M2 = 0, 1
 ACT_IDENTITY, ACT_RELU, ACT_RELU2 = 0, 1, 2
@@ -26,6 +27,7 @@ GROUP = 128
 NOALLOC_MAX_M = 262144  # FP8Q_NOALLOC_MAX_M
 
 _lib = None
+_naive = None
 
 
 class Fp8qError(RuntimeError):
@@ -61,12 +63,9 @@ def lib() -> ctypes.CDLL:
         L.fp8_downproj_workspace_bytes.argtypes = [i64]
         L.fp8_downproj_workspace_bytes.restype = ctypes.c_size_t
         L.fp8_downproj_fwd.argtypes = [P, P, i64, i64, i64, i32, P, P, P, P, P, P, P, P, ctypes.c_size_t, P, P]
-        L.fp8_downproj_fwd_ex.argtypes = [P, P, P, i64, i64, i64, i32, P, P, P, P, P, P, P, P, P, P,
+        L.fp8_downproj_fwd_ex.argtypes = [P, P, P, i64, i64, i64, i32, P, P, P, P, P, P, P, P, P, P, P,
                                           ctypes.c_size_t, P, P, ctypes.c_uint, P, P]
         L.fp8_downproj_fwd_noalloc.argtypes = [P, P, i64, i64, i64, i32, P, P, P, P, P, P, P, P, P]
-        L.fp8q_naive_act.argtypes = [P, i64, i64, i32, P, P]
-        L.fp8q_naive_amax.argtypes = [P, i64, P, P]
-        L.fp8q_naive_cast.argtypes = [P, i64, i32, P, f32, P, P, P]
         L.fp8q_status_string.argtypes = [i32]
         L.fp8q_status_string.restype = ctypes.c_char_p
         L.fp8q_version.restype = i32
@@ -74,12 +73,34 @@ def lib() -> ctypes.CDLL:
         L.fp8q_gemm_test_hold_loads.restype = None
         L.fp8q_gemm_set_tile.argtypes = [i32, i32]
         L.fp8q_gemm_set_tile.restype = i32
+        L.fp8q_test_set_fused_grid.argtypes = [i32]
+        L.fp8q_test_set_fused_grid.restype = i32
+        L.fp8q_test_noalloc_fill.argtypes = [i32, P]
+        L.fp8q_test_noalloc_fill.restype = i32
         for fn in ("fp8_quant_fused", "fp8_quant_fused_ex", "fp8_quant_fused_batch", "fp8_downproj_fwd",
                    "fp8_downproj_fwd_noalloc", "fp8_downproj_fwd_ex", "fp8_gemm_fwd", "fp8_gemm_fwd_update", "fp8_gemm_dgrad", "fp8_gemm_wgrad", "fp8_gemm_dgrad_act", "fp8_upproj_fwd", "amax_history_update",
-                   "amax_history_update_ex", "fp8q_naive_act", "fp8q_naive_amax", "fp8q_naive_cast"):
+                   "amax_history_update_ex"):
             getattr(L, fn).restype = i32
         _lib = L
     return _lib
+
+
+def naive_lib() -> ctypes.CDLL:
+    """Load libfp8q_naive.so, the unfused three-pass comparator; raise if it is missing."""
+    global _naive
+    if _naive is None:
+        lib()  # the status strings live in the main library
+        if not os.path.exists(NAIVE_LIB_PATH):
+            raise RuntimeError(f"{NAIVE_LIB_PATH} is not built: run quantize_fp8_gemm_gb300.build.build() first")
+        L = ctypes.CDLL(NAIVE_LIB_PATH)
+        P, i64, i32, f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
+        L.fp8q_naive_act.argtypes = [P, i64, i64, i32, P, P]
+        L.fp8q_naive_amax.argtypes = [P, i64, P, P]
+        L.fp8q_naive_cast.argtypes = [P, i64, i32, P, f32, P, P, P]
+        for fn in ("fp8q_naive_act", "fp8q_naive_amax", "fp8q_naive_cast"):
+            getattr(L, fn).restype = i32
+        _naive = L
+    return _naive
 
 
 def _check(fn: str, status: int) -> None:
@@ -308,9 +329,9 @@ def history_args(history: torch.Tensor, head: torch.Tensor, margin: float, fmt: 
 
 def fp8_downproj_fwd_ex(h: torch.Tensor, wt_q: torch.Tensor, scale_x: torch.Tensor, scale_w: torch.Tensor,
                         x_q: torch.Tensor, y: torch.Tensor, workspace: torch.Tensor, *, w=None, w_q=None,
-                        amax_w=None, act: int = ACT_RELU2, act_out=None, amax_out=None, sat_count=None,
+                        amax_w=None, sat_w=None, act: int = ACT_RELU2, act_out=None, amax_out=None, sat_count=None,
                         hist_x=None, hist_w=None, flags: int = 0, status=None, stream=None) -> None:
-    """fp8_downproj_fwd with the weight cast (w [K,N] -> wt_q, w_q, amax_w) in the same kernel;
+    """fp8_downproj_fwd with the weight cast (w [K,N] -> wt_q, w_q, amax_w, sat_w) in the same kernel;
     hist_x / hist_w (HistoryArgs): the delayed-scale updates, run by the kernel's last CTA;
     flags=ACCUMULATE: nothing is zeroed first (the workspace must be zero)."""
     M, K = h.shape
@@ -322,7 +343,7 @@ def fp8_downproj_fwd_ex(h: torch.Tensor, wt_q: torch.Tensor, scale_x: torch.Tens
         _ptr(h, 2 * M * K, "h"), _ptr(w, 2 * K * N, "w"), _ptr(wt_q, N * K, "wt_q"), M, N, K, act,
         _ptr(scale_x, 4, "scale_x"), _ptr(scale_w, 4, "scale_w"), _ptr(act_out, 2 * M * K, "act_out"),
         _ptr(x_q, M * K, "x_q"), _ptr(amax_out, 4, "amax_out"), _ptr(sat_count, 8, "sat_count"),
-        _ptr(w_q, K * N, "w_q"), _ptr(amax_w, 4, "amax_w"), _ptr(y, 2 * M * N, "y"),
+        _ptr(w_q, K * N, "w_q"), _ptr(amax_w, 4, "amax_w"), _ptr(sat_w, 8, "sat_w"), _ptr(y, 2 * M * N, "y"),
         _ptr(workspace, ws, "workspace"), workspace.numel() * workspace.element_size(),
         None if hist_x is None else ctypes.byref(hist_x), None if hist_w is None else ctypes.byref(hist_w), flags,
         _ptr(status, 4, "status"), _stream(stream))
@@ -368,26 +389,27 @@ def amax_history_update_ex(history: torch.Tensor, head: torch.Tensor, amax_new: 
     _check("amax_history_update_ex", st)
 
 
-# -- the unfused three-pass comparator (include/fp8q_naive.h) -----------------
+# -- the unfused three-pass comparator (include/fp8q_naive.h, libfp8q_naive.so) --
 def fp8q_naive_act(h, act: int, act_out, *, stream=None) -> None:
     M, K = h.shape
-    _check("fp8q_naive_act", lib().fp8q_naive_act(
+    _check("fp8q_naive_act", naive_lib().fp8q_naive_act(
         _ptr(h, 2 * M * K, "h"), M, K, act, _ptr(act_out, 2 * M * K, "act_out"), _stream(stream)))
 
 
 def fp8q_naive_amax(x, amax_out, *, stream=None) -> None:
     n = x.numel()
-    _check("fp8q_naive_amax", lib().fp8q_naive_amax(
+    _check("fp8q_naive_amax", naive_lib().fp8q_naive_amax(
         _ptr(x, 2 * n, "x"), n, _ptr(amax_out, 4, "amax_out"), _stream(stream)))
 
 
 def fp8q_naive_cast(x, fmt: int, amax, margin: float, q_out, *, scale_out=None, stream=None) -> None:
     n = x.numel()
-    _check("fp8q_naive_cast", lib().fp8q_naive_cast(
+    _check("fp8q_naive_cast", naive_lib().fp8q_naive_cast(
         _ptr(x, 2 * n, "x"), n, fmt, _ptr(amax, 4, "amax"), float(margin),
         _ptr(scale_out, 4, "scale_out"), _ptr(q_out, n, "q_out"), _stream(stream)))
 
 
+# -- test and tuning hooks (include/fp8q_testing.h): process-wide, not for use in programs --
 def fp8q_gemm_set_tile(pair: int, bn: int = 0) -> None:
     """Pin the GEMM tile shape (pair -1 = automatic, 0 = 1-CTA, 1 = 2-SM pair)."""
     _check("fp8q_gemm_set_tile", lib().fp8q_gemm_set_tile(pair, bn))
@@ -396,6 +418,16 @@ def fp8q_gemm_set_tile(pair: int, bn: int = 0) -> None:
 def fp8q_gemm_test_hold_loads(on: bool) -> None:
     """Failure-path test hook: later GEMMs issue no loads and report FP8Q_DEV_TIMEOUT."""
     lib().fp8q_gemm_test_hold_loads(1 if on else 0)
+
+
+def fp8q_test_set_fused_grid(ctas: int) -> None:
+    """Launch the one-launch step kernels with this many CTAs (0 = one per SM)."""
+    _check("fp8q_test_set_fused_grid", lib().fp8q_test_set_fused_grid(int(ctas)))
+
+
+def fp8q_test_noalloc_fill(byte: int, stream=None) -> None:
+    """Fill the no-allocation entry's static counter array with a byte value."""
+    _check("fp8q_test_noalloc_fill", lib().fp8q_test_noalloc_fill(int(byte), _stream(stream)))
 
 
 def version() -> int:

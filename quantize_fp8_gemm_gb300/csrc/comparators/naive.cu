@@ -1,12 +1,14 @@
 // naive.cu -- the unfused three-pass quantize (measured comparator only).
+// Built into its own library, libfp8q_naive.so, not into libfp8q.so: it is
+// not part of the down-projection path.
 //
 // "Paradigma Details FP8 and Optimizer Tricks Behind NanoGPT Records", second
 // paragraph: write the intermediate tensor, scan it for its maximum, read it
 // again to convert it.  Each pass is its own grid-stride kernel with 16-byte
 // accesses, so the comparison with the fused kernel is about passes over HBM,
 // not about code quality.
-#include "common.cuh"
-#include "../../include/fp8q_naive.h"
+#include "../common.cuh"
+#include "../../../include/fp8q_naive.h"
 
 #include <algorithm>
 
@@ -15,9 +17,19 @@ namespace {
 
 constexpr int kT = 256;
 
+int device_sms() {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1) {
+        (void)cudaGetLastError();
+        return 1;
+    }
+    return sms;
+}
+
 unsigned grid_for(int64_t nchunks) {
     const int64_t want = (nchunks + kT - 1) / kT;
-    const int64_t cap = static_cast<int64_t>(sm_count()) * (2048 / kT);
+    const int64_t cap = static_cast<int64_t>(device_sms()) * (2048 / kT);
     return static_cast<unsigned>(std::max<int64_t>(1, std::min(want, cap)));
 }
 

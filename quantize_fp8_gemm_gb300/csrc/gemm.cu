@@ -49,6 +49,7 @@
 #include "common.cuh"
 #include "quant_ops.cuh"
 #include "history_ops.cuh"
+#include "../../include/fp8q_testing.h"
 
 #include <algorithm>
 #include <atomic>
@@ -95,12 +96,16 @@ constexpr int gemm_threads() {
 
 // Operands of the fused quantize.  ready[b] counts the rows of 128-row block b
 // whose E4M3 codes are written; the GEMM's producer loads a tile's A rows once
-// its block is complete.  With w set, the quantize warps first cast the weight
-// W [K,N] into the GEMM's B operand W_q^T [N,K] (and W_q [K,N]); w_ready counts
-// finished weight units and every producer waits for all of them before its
-// first B load.  The CTA that finishes last resets ready, w_ready and done, so
-// the workspace is zero again for the next launch, and then runs the
-// delayed-scale history updates of X and W on the final amax values.
+// its block is complete.  Work is handed out by tickets: a CTA's quantize warps
+// take the next row unit from q_next, and each epilogue warp the next weight
+// unit from w_next, so only CTAs that are running claim work and no wait can
+// depend on a CTA that has not been scheduled.  With w set, the epilogue warps
+// first cast the weight W [K,N] into the GEMM's B operand W_q^T [N,K] (and
+// W_q [K,N]); w_ready counts finished weight units and every producer waits
+// for all w_units of them before its first B load.  The CTA that finishes
+// last resets ready, w_ready, done and both ticket counters, so the workspace
+// is zero again for the next launch, and then runs the delayed-scale history
+// updates of X and W on the final amax values.
 struct FusedArgs {
     const uint4* h;               // H [M,K] BF16, 8 elements per 16 bytes
     uint4* act_out;               // [M,K] BF16 activation copy, or nullptr
@@ -111,14 +116,17 @@ struct FusedArgs {
     int act;                      // fp8q_act
     int64_t nblocks;              // ceil(M / 128)
     unsigned* done;               // CTAs finished; zero at the launch
+    unsigned* q_next;             // next quantize ticket; zero at the launch
+    unsigned* w_next;             // next weight-unit ticket; zero at the launch
     const uint4* w;               // W [K,N] BF16, or nullptr (W_q^T is then an input)
     const float* scale_w;         // W's scale (the GEMM's scale_b)
     uint8_t* wt_q;                // [N,K] E4M3, written when w is set
     uint8_t* w_q;                 // [K,N] E4M3 or nullptr
     float* amax_w;                // or nullptr; zero at the launch
+    unsigned long long* sat_w;    // or nullptr: W's saturations; zero at the launch
     int64_t wn;                   // N
-    unsigned* w_ready;            // epilogue warps done with the weight; zero at the launch
-    unsigned w_units;             // epilogue warps of the launch (set by launch_gemm)
+    unsigned* w_ready;            // weight units finished; zero at the launch
+    unsigned w_units;             // weight units of the launch: (K / 8) * ceil(N / 256)
     HistoryArgs hx, hw;           // delayed-scale updates the last CTA runs (history == nullptr: none)
 };
 
@@ -289,11 +297,6 @@ __device__ __forceinline__ void fused_quantize_rows(const FusedArgs& fz, float s
     }
 }
 
-// The quantize warps of the fused kernel.  Full rounds: every CTA takes one
-// 16-row unit per round, units in row order (CTA c: units c, c + gridDim.x,
-// ...), so rows finish in order across the GPU.  The rows left after the last
-// full round are split evenly over all CTAs (at most 17 rows each), so no SM
-// carries a whole extra unit at the end.
 // The last CTA's history update (once per launch: kept out of line).
 __device__ __noinline__ void history_update_once(const HistoryArgs& a, const float* amax_new) {
     history_update_warp(a, amax_new);
@@ -306,31 +309,37 @@ __device__ __noinline__ void history_update_once(const HistoryArgs& a, const flo
 // otherwise wait for their first accumulator.  A unit is 8 rows of W x 256
 // columns, one warp, each lane 8 columns: the lane loads its 8 x 8 block row
 // by row, casts it, and writes the block's transpose as 8 eight-byte pieces
-// (8 consecutive k of one output row n).  Warp slot ew * gridDim.x + cta
-// takes units slot, slot + all epilogue warps, ...  Every epilogue warp then
-// adds 1 to w_ready with release semantics, once, after all its units (the
+// (8 consecutive k of one output row n).  A warp takes units by ticket
+// (w_next), asking for the next one before it casts the current one, so the
+// atomic's latency hides behind the loads.  Every epilogue warp then adds
+// the number of units it cast to w_ready with release semantics, once (the
 // producers wait for the whole weight, so one drain of the scattered stores
-// per warp is enough).  The warp's max |W| goes to amax_w with one atomic.
-__device__ __forceinline__ void fused_cast_w(const FusedArgs& fz, int64_t K, int ew, int lane) {
+// per warp is enough).  The warp's max |W| goes to amax_w and its count of
+// |v| > 448 to sat_w, one atomic each.
+__device__ __forceinline__ void fused_cast_w(const FusedArgs& fz, int64_t K, int lane) {
     const int64_t N = fz.wn;
     const int64_t nbn = (N + 255) / 256;
-    const int64_t units = (K / 8) * nbn;
-    const int64_t num_warps = int64_t(gridDim.x) * kEpiWarps;
+    const unsigned units = fz.w_units;
     const float s = __ldg(fz.scale_w);
-    uint32_t amax2w = 0;
-    for (int64_t u = int64_t(ew) * gridDim.x + blockIdx.x; u < units; u += num_warps) {
-        const int64_t k0 = (u / nbn) * 8;
-        const int64_t n = (u % nbn) * 256 + lane * 8;
+    uint32_t amax2w = 0, nsat = 0;
+    unsigned cast = 0;
+    unsigned u = 0;
+    if (lane == 0) u = atomicAdd(fz.w_next, 1u);
+    u = __shfl_sync(0xFFFFFFFFu, u, 0);
+    while (u < units) {
+        unsigned nxt = 0;
+        if (lane == 0) nxt = atomicAdd(fz.w_next, 1u);
+        const int64_t k0 = (int64_t(u) / nbn) * 8;
+        const int64_t n = (int64_t(u) % nbn) * 256 + lane * 8;
         if (n < N) {
             uint4 x[8];
 #pragma unroll
             for (int r = 0; r < 8; ++r) x[r] = ld_stream_v4(fz.w + ((k0 + r) * N + n) / 8);
             uint2 q[8];
-            uint32_t nsat_unused = 0;
 #pragma unroll
             for (int r = 0; r < 8; ++r) {
                 const uint4 a = act8<FP8Q_ACT_IDENTITY>(x[r], amax2w);
-                q[r] = cast8<FP8Q_E4M3>(a, s, nsat_unused);
+                q[r] = cast8<FP8Q_E4M3>(a, s, nsat);
                 if (fz.w_q) st_v2(reinterpret_cast<uint2*>(fz.w_q + (k0 + r) * N + n), q[r]);
             }
 #pragma unroll
@@ -344,30 +353,58 @@ __device__ __forceinline__ void fused_cast_w(const FusedArgs& fz, int64_t K, int
                 st_v2(reinterpret_cast<uint2*>(fz.wt_q + (n + j) * K + k0), make_uint2(lo, hi));
             }
         }
+        ++cast;
+        u = __shfl_sync(0xFFFFFFFFu, nxt, 0);
     }
     // the warp's codes, written by all lanes, are ordered before the count,
     // which every producer reads before its TMA loads of W_q^T
     fence_proxy_async_global();
     __syncwarp();
-    if (lane == 0) red_release_add(fz.w_ready, 1u);
+    if (lane == 0 && cast) red_release_add(fz.w_ready, cast);
     const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, max16x2(amax2w));
+    const uint32_t c = __reduce_add_sync(0xFFFFFFFFu, nsat);
     if (lane == 0 && fz.amax_w && m) atomicMax(reinterpret_cast<unsigned int*>(fz.amax_w), m << 16);
+    if (lane == 0 && fz.sat_w && c) atomicAdd(fz.sat_w, static_cast<unsigned long long>(c));
 }
 
+// The quantize warps of the fused kernel.  Row units are handed out by
+// ticket (q_next), in row order, so rows finish in order across the GPU and
+// only running CTAs take work.  Tickets 0 .. full - 1 are 16-row units; the
+// rows after them (gridDim.x x 16 rows or more when M allows) are split into
+// gridDim.x equal units of at most 17 rows, so the last units end together
+// instead of one SM carrying a whole extra unit at the end.  One thread asks
+// for the next ticket before the CTA quantizes the current unit; the unit's
+// closing barrier publishes it to the other quantize threads.
 __device__ __forceinline__ void fused_quantize(const FusedArgs& fz, const float* scale, int64_t M, int64_t K) {
+    __shared__ unsigned s_ticket[2];
     const float s = __ldg(scale);
-    uint32_t amax2 = 0, nsat = 0;
-    const int64_t rounds = (M / kUnitRows) / gridDim.x;
-    for (int64_t k = 0; k < rounds; ++k) {
-        const int64_t r0 = (k * gridDim.x + blockIdx.x) * kUnitRows;
-        fused_quantize_rows(fz, s, r0, r0 + kUnitRows, K, amax2, nsat);
-    }
-    const int64_t t0 = rounds * gridDim.x * kUnitRows;
-    const int64_t share = (M - t0 + gridDim.x - 1) / gridDim.x;
-    const int64_t r0 = t0 + blockIdx.x * share;
-    const int64_t r1 = r0 + share < M ? r0 + share : M;
-    if (r0 < r1) fused_quantize_rows(fz, s, r0, r1, K, amax2, nsat);
     const int qt = threadIdx.x - kThreadsGemm;
+    uint32_t amax2 = 0, nsat = 0;
+    const int64_t G = gridDim.x;
+    const int64_t full = M / kUnitRows > G ? M / kUnitRows - G : 0;
+    const int64_t share = (M - full * kUnitRows + G - 1) / G;
+    const int64_t nunits = full + G;
+    if (qt == 0) s_ticket[0] = atomicAdd(fz.q_next, 1u);
+    named_barrier(1, kQuantThreads);
+    int par = 0;
+    int64_t t = s_ticket[0];
+    while (t < nunits) {
+        if (qt == 0) s_ticket[par ^ 1] = atomicAdd(fz.q_next, 1u);
+        int64_t r0, r1;
+        if (t < full) {
+            r0 = t * kUnitRows;
+            r1 = r0 + kUnitRows;
+        } else {
+            r0 = full * kUnitRows + (t - full) * share;
+            r1 = r0 + share < M ? r0 + share : M;
+        }
+        // fused_quantize_rows ends with a barrier of all quantize threads, after
+        // which the next ticket is visible to all of them
+        if (r0 < r1) fused_quantize_rows(fz, s, r0, r1, K, amax2, nsat);
+        else named_barrier(1, kQuantThreads);
+        par ^= 1;
+        t = s_ticket[par];
+    }
     __shared__ uint32_t s_amax[kQuantWarps], s_sat[kQuantWarps];
     uint32_t m = __reduce_max_sync(0xFFFFFFFFu, max16x2(amax2));
     uint32_t c = __reduce_add_sync(0xFFFFFFFFu, nsat);
@@ -788,7 +825,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     } else {
         // ---------------------------------------------------------- epilogue
         if constexpr (FUSED) {
-            if (fz.w) fused_cast_w(fz, K, warp - 2, lane);
+            if (fz.w) fused_cast_w(fz, K, lane);
         } else {
             // fp8_gemm_fwd_update: the step's delayed-scale updates, by one warp of
             // the first CTA while its first accumulator fills (the amax values
@@ -996,7 +1033,9 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         if (s_last_cta && warp == 0) {
             for (int64_t b = lane; b < fz.nblocks; b += 32) fz.ready[b] = 0u;
             if (lane == 0) {
-                if (fz.w_ready) *fz.w_ready = 0u;
+                *fz.w_ready = 0u;
+                *fz.q_next = 0u;
+                *fz.w_next = 0u;
                 *fz.done = 0u;
             }
             if (fz.hx.history) history_update_once(fz.hx, fz.amax_out);
@@ -1071,7 +1110,8 @@ bool make_q_out_map(CUtensorMap* map, void* base, int64_t rows, int64_t cols) {
     return r == CUDA_SUCCESS;
 }
 
-std::atomic<int> g_hold_loads{0};  // fp8q_gemm_test_hold_loads
+std::atomic<int> g_hold_loads{0};   // fp8q_gemm_test_hold_loads
+std::atomic<int> g_fused_grid{0};   // fp8q_test_set_fused_grid: CTAs of the fused kernel, 0 = one per SM
 
 struct LaunchInfo {
     cudaError_t attr_err = cudaSuccess;
@@ -1153,9 +1193,12 @@ int launch_gemm(const void* a, const void* b, const float* sa, const float* sb, 
     auto kern = fp8_gemm_kernel<BN, GROUP, PAIR, FUSED, EQ, DACT>;
     if constexpr (PAIR) {
         if (info.max_clusters < 1) return FP8Q_ERR_CUDA;
-        const int clusters = static_cast<int>(FUSED ? info.max_clusters : std::min<int64_t>(tiles, info.max_clusters));
-        FusedArgs f = fz;
-        if (f.w) f.w_units = static_cast<unsigned>(2 * clusters * kEpiWarps);  // each epilogue warp reports once
+        // the fused kernel takes every co-resident cluster (its CTAs take work
+        // by ticket, so a grid larger or smaller than that is also correct)
+        const int fg = g_fused_grid.load();
+        const int clusters = static_cast<int>(FUSED ? (fg > 0 ? std::max(1, fg / 2) : info.max_clusters)
+                                                    : std::min<int64_t>(tiles, info.max_clusters));
+        const FusedArgs& f = fz;
         cudaLaunchConfig_t cfg = {};
         cudaLaunchAttribute attr[2];
         attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1176,11 +1219,11 @@ int launch_gemm(const void* a, const void* b, const float* sa, const float* sb, 
             return FP8Q_ERR_CUDA;
         }
     } else {
-        // the fused kernel needs every CTA resident at once (the producers wait on
-        // quantize work spread over all CTAs): one CTA per SM, never more
-        const int grid = static_cast<int>(FUSED ? sm_count() : std::min<int64_t>(tiles, sm_count()));
-        FusedArgs f = fz;
-        if (f.w) f.w_units = static_cast<unsigned>(grid * kEpiWarps);  // each epilogue warp reports once
+        // the fused kernel: one CTA per SM (its CTAs take work by ticket, so a
+        // grid larger or smaller than that is also correct)
+        const int fg = g_fused_grid.load();
+        const int grid = static_cast<int>(FUSED ? (fg > 0 ? fg : sm_count()) : std::min<int64_t>(tiles, sm_count()));
+        const FusedArgs& f = fz;
         if (launch_pdl(kern, dim3(grid), dim3(gemm_threads<BN, GROUP, FUSED, EQ>()), C::SMEM_BYTES, stream, mapA, mapB, mapD, sa,
                        sb, M, N, K, idesc, status, g_hold_loads.load(), f, mapE1, mapE2, eq) != cudaSuccess) {
             (void)cudaGetLastError();
@@ -1412,6 +1455,12 @@ using namespace fp8q;
 
 extern "C" void fp8q_gemm_test_hold_loads(int on) { g_hold_loads.store(on != 0 ? 1 : 0); }
 
+extern "C" int fp8q_test_set_fused_grid(int ctas) {
+    if (ctas < 0 || ctas > 65535) return FP8Q_ERR_SHAPE;
+    g_fused_grid.store(ctas);
+    return FP8Q_OK;
+}
+
 extern "C" int fp8q_gemm_set_tile(int pair, int bn) {
     if (pair == -1) {
         g_tile_override.store(-1);
@@ -1520,7 +1569,7 @@ extern "C" int fp8_gemm_wgrad(const void* x_q_t, const void* dy_q_t, const float
 extern "C" size_t fp8_downproj_workspace_bytes(int64_t M) {
     if (M <= 0) return 0;
     const size_t blocks = static_cast<size_t>((M + BM - 1) / BM);
-    return ((blocks + 2) * sizeof(unsigned) + 255) / 256 * 256;  // ready[blocks], w_ready, done
+    return ((blocks + 4) * sizeof(unsigned) + 255) / 256 * 256;  // ready[blocks], w_ready, done, q_next, w_next
 }
 
 namespace {
@@ -1538,6 +1587,8 @@ FusedArgs fused_args(const void* h, int act, void* act_out, void* x_q, float* am
     fz.ready = ws;
     fz.w_ready = ws + fz.nblocks;
     fz.done = ws + fz.nblocks + 1;
+    fz.q_next = ws + fz.nblocks + 2;
+    fz.w_next = ws + fz.nblocks + 3;
     return fz;
 }
 
@@ -1548,19 +1599,18 @@ extern "C" int fp8_downproj_fwd(const void* h, const void* wt_q, int64_t M, int6
                                 float* amax_out, unsigned long long* sat_count, void* y, void* workspace,
                                 size_t workspace_bytes, int* status, cudaStream_t stream) {
     return fp8_downproj_fwd_ex(h, nullptr, const_cast<void*>(wt_q), M, N, K, act, scale_x, scale_w, act_out, x_q,
-                               amax_out, sat_count, nullptr, nullptr, y, workspace, workspace_bytes, nullptr,
-                               nullptr, 0u, status, stream);
+                               amax_out, sat_count, nullptr, nullptr, nullptr, y, workspace, workspace_bytes,
+                               nullptr, nullptr, 0u, status, stream);
 }
 
 namespace {
-
-// Host checks of one history update (as amax_history_update_ex) and its device form.
 
 }  // namespace
 
 extern "C" int fp8_downproj_fwd_ex(const void* h, const void* w, void* wt_q, int64_t M, int64_t N, int64_t K,
                                    int act, const float* scale_x, const float* scale_w, void* act_out, void* x_q,
-                                   float* amax_x, unsigned long long* sat_count, void* w_q, float* amax_w, void* y,
+                                   float* amax_x, unsigned long long* sat_count, void* w_q, float* amax_w,
+                                   unsigned long long* sat_w, void* y,
                                    void* workspace, size_t workspace_bytes, const fp8q_history_args* hist_x,
                                    const fp8q_history_args* hist_w, unsigned flags, int* status,
                                    cudaStream_t stream) {
@@ -1569,9 +1619,12 @@ extern "C" int fp8_downproj_fwd_ex(const void* h, const void* w, void* wt_q, int
     if ((!h || !x_q || !workspace) && M != 0) return FP8Q_ERR_NULL;
     if (!aligned16(h) || !aligned16(act_out) || !aligned16(w) || !aligned16(w_q) ||
         (reinterpret_cast<uintptr_t>(workspace) & 3u) || (reinterpret_cast<uintptr_t>(amax_x) & 3u) ||
-        (reinterpret_cast<uintptr_t>(amax_w) & 3u) || (reinterpret_cast<uintptr_t>(sat_count) & 7u))
+        (reinterpret_cast<uintptr_t>(amax_w) & 3u) || (reinterpret_cast<uintptr_t>(sat_count) & 7u) ||
+        (reinterpret_cast<uintptr_t>(sat_w) & 7u))
         return FP8Q_ERR_ALIGN;
     if (workspace_bytes < fp8_downproj_workspace_bytes(M)) return FP8Q_ERR_SHAPE;
+    // weight units are counted in 32 bits: (K / 8) * ceil(N / 256) of them
+    if (w && (K / 8) * ((N + 255) / 256) > (int64_t(1) << 31)) return FP8Q_ERR_SHAPE;
     HistoryArgs hx = {}, hw = {};
     if (hist_w && !w) return FP8Q_ERR_NULL;  // W's amax exists only when the kernel casts W
     if (hist_x) {
@@ -1591,12 +1644,14 @@ extern "C" int fp8_downproj_fwd_ex(const void* h, const void* w, void* wt_q, int
         if (sat_count && cudaMemsetAsync(sat_count, 0, sizeof(unsigned long long), stream) != cudaSuccess)
             return FP8Q_ERR_CUDA;
         if (w && amax_w && cudaMemsetAsync(amax_w, 0, sizeof(float), stream) != cudaSuccess) return FP8Q_ERR_CUDA;
+        if (w && sat_w && cudaMemsetAsync(sat_w, 0, sizeof(unsigned long long), stream) != cudaSuccess)
+            return FP8Q_ERR_CUDA;
     }
     if (M == 0) {
         // no GEMM: a weight to cast still is (the step's W_q^T and amax stay defined)
         if (!w) return FP8Q_OK;
         return fp8_quant_fused_ex(w, K, N, FP8Q_ACT_IDENTITY, FP8Q_E4M3, scale_w, nullptr, w_q, wt_q,
-                                  amax_w, nullptr, nullptr, 1, FP8Q_ACCUMULATE, stream);
+                                  amax_w, sat_w, nullptr, 1, FP8Q_ACCUMULATE, stream);
     }
     if (zero && cudaMemsetAsync(workspace, 0, fp8_downproj_workspace_bytes(M), stream) != cudaSuccess)
         return FP8Q_ERR_CUDA;
@@ -1607,8 +1662,9 @@ extern "C" int fp8_downproj_fwd_ex(const void* h, const void* w, void* wt_q, int
         fz.wt_q = static_cast<uint8_t*>(wt_q);
         fz.w_q = static_cast<uint8_t*>(w_q);
         fz.amax_w = amax_w;
+        fz.sat_w = sat_w;
         fz.wn = N;
-        fz.w_units = 0;  // set at launch: the number of epilogue warps, which each report once
+        fz.w_units = static_cast<unsigned>((K / 8) * ((N + 255) / 256));
     }
     fz.hx = hx;
     fz.hw = hw;
@@ -1617,38 +1673,31 @@ extern "C" int fp8_downproj_fwd_ex(const void* h, const void* w, void* wt_q, int
 }
 
 // ---------------------------------------------------------------------------
-// fp8_downproj_fwd_noalloc: the fused kernel with its ready counts in this
+// fp8_downproj_fwd_noalloc: the fused kernel with its counters in this
 // library's own device memory, for callers that cannot allocate (see
 // include/fp8q.h).  The array lives in the module's global memory on every
 // device that loads the library, until the process exits.  In host code
 // g_noalloc_ready only names the symbol: its device address comes from
-// cudaGetSymbolAddress, once per device, with that device current.
+// cudaGetSymbolAddress with the device current.  The address is looked up
+// on every call rather than cached: after a device reset the module is
+// loaded again in a new context, possibly at another address.
 
 static __device__ __align__(256) unsigned g_noalloc_ready[FP8Q_NOALLOC_MAX_M / BM + 64];
 
 static_assert(FP8Q_NOALLOC_MAX_M % BM == 0, "whole 128-row blocks");
-static_assert(sizeof(g_noalloc_ready) == ((FP8Q_NOALLOC_MAX_M / BM + 2) * sizeof(unsigned) + 255) / 256 * 256,
+static_assert(sizeof(g_noalloc_ready) == ((FP8Q_NOALLOC_MAX_M / BM + 4) * sizeof(unsigned) + 255) / 256 * 256,
               "the array is exactly the workspace of the largest M");
 
 namespace {
 
-constexpr int kNoAllocMaxDevices = 64;
-std::mutex g_noalloc_mutex;
-unsigned* g_noalloc_ptr[kNoAllocMaxDevices] = {};
-
-// The array's device address on the current device (set up on first use).
+// The array's device address on the current device.
 int noalloc_scratch(unsigned** out) {
-    int dev = -1;
-    if (cudaGetDevice(&dev) != cudaSuccess) return FP8Q_ERR_CUDA;
-    if (dev < 0 || dev >= kNoAllocMaxDevices) return FP8Q_ERR_UNSUPPORTED;
-    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-    if (!g_noalloc_ptr[dev]) {
-        unsigned* ptr = nullptr;
-        if (cudaGetSymbolAddress(reinterpret_cast<void**>(&ptr), g_noalloc_ready) != cudaSuccess || !ptr)
-            return FP8Q_ERR_CUDA;
-        g_noalloc_ptr[dev] = ptr;
+    unsigned* ptr = nullptr;
+    if (cudaGetSymbolAddress(reinterpret_cast<void**>(&ptr), g_noalloc_ready) != cudaSuccess || !ptr) {
+        (void)cudaGetLastError();
+        return FP8Q_ERR_CUDA;
     }
-    *out = g_noalloc_ptr[dev];
+    *out = ptr;
     return FP8Q_OK;
 }
 
@@ -1672,9 +1721,21 @@ extern "C" int fp8_downproj_fwd_noalloc(const void* h, const void* wt_q, int64_t
     if (sat_count && cudaMemsetAsync(sat_count, 0, sizeof(unsigned long long), stream) != cudaSuccess)
         return FP8Q_ERR_CUDA;
     if (M == 0) return FP8Q_OK;
-    // the previous call's counts are still there: this call's blocks start from zero
+    // the array still holds what the previous call left (zero after a call that
+    // ran to the end, but not after one that was cut short): start from zero
     if (cudaMemsetAsync(ready, 0, fp8_downproj_workspace_bytes(M), stream) != cudaSuccess) return FP8Q_ERR_CUDA;
     const FusedArgs fz = fused_args(h, act, act_out, x_q, amax_out, sat_count, ready, M);
     return gemm_dispatch_t<true>(x_q, wt_q, scale_x, scale_w, 0, y, M, N, K, FP8Q_E4M3, FP8Q_E4M3, status, stream,
                                  fz);
+}
+
+extern "C" int fp8q_test_noalloc_fill(int byte, cudaStream_t stream) {
+    unsigned* ptr = nullptr;
+    const int st = noalloc_scratch(&ptr);
+    if (st != FP8Q_OK) return st;
+    if (cudaMemsetAsync(ptr, byte & 0xFF, sizeof(g_noalloc_ready), stream) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return FP8Q_ERR_CUDA;
+    }
+    return FP8Q_OK;
 }

@@ -17,7 +17,6 @@ end of the step, so the GEMM dequantises with the scale actually used.
 """
 from __future__ import annotations
 
-import numpy as np
 import torch
 
 from . import binding as B
@@ -26,19 +25,6 @@ from . import binding as B
 FUSED_MIN_ROWS = 32768  # default switch to the fused kernel (per-tensor scales)
 
 RECOMPUTE_X, RECOMPUTE_W = 1, 2  # recompute_on_overflow(): which operand was cast again
-
-
-def fp8_overflow(sat_x: int, amax_w: float, scale_w: float, fmt: int = B.E4M3) -> tuple[bool, bool]:
-    """Whether a step's casts overflowed their delayed scales ("FP8 Training &
-    Inference", Delayed Scaling: a scale too large for the step's values is
-    detected and the step recomputed with a corrected scale).  The casts
-    saturate instead of producing infinities, so the signal is a value past
-    the format's maximum: for X the quantize's saturation count, for W its
-    largest value, |v| = fp32(amax_w * s_w) with the cast's own rounded
-    product, against the maximum (448 for E4M3, 57344 for E5M2)."""
-    fmax = np.float32(448.0 if fmt == B.E4M3 else 57344.0)
-    w_over = bool(np.float32(amax_w) * np.float32(scale_w) > fmax)
-    return int(sat_x) > 0, w_over
 
 
 class DelayedScale:
@@ -217,7 +203,7 @@ class Fp8DownProj:
                               group_rows=B.GROUP)
         else:
             B.fp8_quant_fused(W, B.ACT_IDENTITY, B.E4M3, scale, q_out=self.w_q,
-                              q_t_out=self.wt_q, amax_out=self.w.amax)
+                              q_t_out=self.wt_q, amax_out=self.w.amax, sat_count=self.w.sat)
 
     # -- a1-a5 ----------------------------------------------------------------
     def quantize(self, H: torch.Tensor, scale: torch.Tensor | None = None, rows=None) -> None:
@@ -340,7 +326,7 @@ class Fp8DownProj:
         sx, sw = self.x.scale, self.w.scale
         flags = B.ACCUMULATE if (self.x.clean and self.w.clean) else 0
         B.fp8_downproj_fwd_ex(H, self.wt_q, sx, sw, self.x_q, self.y, self.workspace, w=W, w_q=self.w_q,
-                              amax_w=self.w.amax, act=self.act, act_out=self.act_bf16, amax_out=self.x.amax,
+                              amax_w=self.w.amax, sat_w=self.w.sat, act=self.act, act_out=self.act_bf16, amax_out=self.x.amax,
                               sat_count=self.x.sat, hist_x=self.x.kernel_update_args(),
                               hist_w=self.w.kernel_update_args(), flags=flags, status=self.gemm_status)
         self.x.advance()
@@ -361,7 +347,7 @@ class Fp8DownProj:
         fw = B.ACCUMULATE if self.w.clean else 0
         B.fp8_quant_fused_batch([
             B.quant_args(W, B.ACT_IDENTITY, B.E4M3, sw, q_out=self.w_q, q_t_out=self.wt_q,
-                         amax_out=self.w.amax, flags=fw),
+                         amax_out=self.w.amax, sat_count=self.w.sat, flags=fw),
             B.quant_args(H, self.act, B.E4M3, sx, act_out=self.act_bf16, q_out=self.x_q, q_t_out=self.x_q_t,
                          amax_out=self.x.amax, sat_count=self.x.sat, flags=fx),
         ])
@@ -379,13 +365,16 @@ class Fp8DownProj:
     def recompute_on_overflow(self, H: torch.Tensor, W: torch.Tensor) -> int:
         """Detect-and-recompute ("FP8 Training & Inference", Delayed Scaling:
         when the delayed scale is too large for this step's values, detect it
-        and recompute with a corrected scale).  Call after step(H, W); reads
-        the step's saturation count and the weight's amax and scale back to
-        the host (one synchronisation).  If the quantize of H saturated, H is
-        cast again with the scale this step's own amax gives under the same
-        rule, 448 / fp32(margin * amax_t) (amax_history_update on a one-entry
+        and recompute with a corrected scale).  Call after step(H, W).  The
+        casts saturate instead of producing infinities, so the overflow
+        signal is a value past the format's maximum, which each cast counts on
+        the device (the saturation counts of X and of W); the host reads the
+        two counts back (one synchronisation) and does no arithmetic on them
+        beyond "is it zero".  If the quantize of H saturated, H is cast again
+        with the scale this step's own amax gives under the same rule,
+        448 / fp32(margin * amax_t) (amax_history_update on a one-entry
         history; the act copy is unchanged and not rewritten); likewise W
-        (both layouts) when its largest value passed 448.  The GEMM then runs
+        (both layouts) when its cast saturated.  The GEMM then runs
         again on the new operands.  The delayed-scale state is untouched: the
         history update of the step already holds amax_t, so the next step's
         scale accounts for it.  Returns RECOMPUTE_X | RECOMPUTE_W for what
@@ -396,8 +385,8 @@ class Fp8DownProj:
         self.x_scale_used, self.w_scale_used = sx_prev, sw_prev
         if self.group:
             return 0
-        x_over, w_over = fp8_overflow(int(self.x.last_sat.item()), float(self.w.last_amax.item()),
-                                      float(sw_prev.item()))
+        counts = torch.cat([self.x.last_sat, self.w.last_sat]).cpu()
+        x_over, w_over = int(counts[0]) > 0, int(counts[1]) > 0
         if not (x_over or w_over):
             return 0
         redo = 0

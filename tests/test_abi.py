@@ -26,10 +26,14 @@ def lib():
     return binding.lib()
 
 
-def declared_functions():
+# which library exports the functions each header declares
+HEADER_LIBS = {"fp8q.h": "libfp8q.so", "fp8q_testing.h": "libfp8q.so", "fp8q_naive.h": "libfp8q_naive.so"}
+
+
+def declared_functions(header=None):
     names = []
     for h in sorted(os.listdir(INCLUDE)):
-        if h.endswith(".h"):
+        if h.endswith(".h") and (header is None or h == header):
             text = open(os.path.join(INCLUDE, h)).read()
             text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
             names += re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_\s\*]*?\b([a-z][a-z0-9_]*)\s*\(", text, re.M)
@@ -44,11 +48,23 @@ def test_header_declares_the_four_calls():
 
 def test_library_exports_every_declared_symbol(lib):
     from quantize_fp8_gemm_gb300 import binding
+    headers = sorted(h for h in os.listdir(INCLUDE) if h.endswith(".h"))
+    assert set(headers) == set(HEADER_LIBS), "a header without a library to check it against"
+    for h in headers:
+        path = os.path.join(binding.PKG, HEADER_LIBS[h])
+        out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True).stdout
+        exported = set(re.findall(r"\s[TW]\s+(\S+)$", out, re.M))
+        dl = ctypes.CDLL(path)
+        for fn in declared_functions(h):
+            assert fn in exported, f"{fn} declared in include/{h} but not exported by {HEADER_LIBS[h]}"
+            assert hasattr(dl, fn)
+
+
+def test_product_library_holds_no_comparator(lib):
+    """The unfused three-pass comparator lives in libfp8q_naive.so only."""
+    from quantize_fp8_gemm_gb300 import binding
     out = subprocess.run(["nm", "-D", "--defined-only", binding.LIB_PATH], capture_output=True, text=True).stdout
-    exported = set(re.findall(r"\s[TW]\s+(\S+)$", out, re.M))
-    for fn in declared_functions():
-        assert fn in exported, f"{fn} declared in include/ but not exported"
-        assert hasattr(lib, fn)
+    assert "fp8q_naive" not in out
 
 
 def test_status_strings_and_version(lib):
@@ -251,6 +267,32 @@ def test_fused_argument_checks(lib):
     assert f(act=5) == ERR_UNSUPPORTED
     assert f(h=A + 8) == ERR_ALIGN
     assert f() == ERR_UNSUPPORTED  # no sm_103 device here
+
+
+def test_ex_argument_checks(lib):
+    """fp8_downproj_fwd_ex: the weight's saturation counter is checked like the other counters."""
+    P, i64 = ctypes.c_void_p, ctypes.c_int64
+    f = lib.fp8_downproj_fwd_ex
+    f.argtypes = [P, P, P, i64, i64, i64, ctypes.c_int] + [P] * 11 + [ctypes.c_size_t, P, P, ctypes.c_uint, P, P]
+    f.restype = ctypes.c_int
+
+    def call(sat_w=A, w=A, flags=0, M=256):
+        return f(A, w, A, M, 128, 256, 2, A, A, A, A, A, A, A, A, sat_w, A, A, 1 << 20, None, None, flags, None, None)
+
+    assert call(sat_w=A + 4) == ERR_ALIGN
+    assert call(flags=4) == ERR_UNSUPPORTED
+    assert call() == ERR_UNSUPPORTED  # valid: only the missing sm_103 device is left
+
+
+def test_testing_hooks_arguments(lib):
+    assert lib.fp8q_test_set_fused_grid(-1) == ERR_SHAPE
+    assert lib.fp8q_test_set_fused_grid(70000) == ERR_SHAPE
+    assert lib.fp8q_test_set_fused_grid(5) == OK
+    assert lib.fp8q_test_set_fused_grid(0) == OK
+    import torch
+    if not torch.cuda.is_available():
+        # no device: the static array has no address to look up
+        assert lib.fp8q_test_noalloc_fill(0, None) == ERR_CUDA
 
 
 def test_noalloc_argument_checks(lib):

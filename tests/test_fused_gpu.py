@@ -198,3 +198,72 @@ def test_fused_step_runs_history_updates():
         else:
             assert scales_x[1].item() == O.delayed_scale(ro["amax"], 2.0, O.E4M3) and st_x.item() == 0
         assert int(ws.sum().item()) == 0
+
+
+@pytest.mark.parametrize("ctas", [2, 37, 64, 400])
+def test_fused_any_grid_gives_the_same_result(ctas):
+    """The one-launch step's CTAs take their quantize and weight-cast work by
+    ticket, so no CTA waits on work held by a CTA that is not running.  A grid
+    smaller than the SM count (2, 37, 64 CTAs) and one larger than the GPU
+    holds at once (400 CTAs: the last ones can only start after earlier ones
+    have finished) give the default grid's outputs bit for bit, and the
+    workspace ends zero."""
+    M, N, K = 2048, 768, 3072
+    h, w = _inputs(M, N, K, seed=ctas)
+    H, Wd = dev_bf16(h), dev_bf16(w)
+    sx, sw = dev_f32(20.0), dev_f32(300.0)
+    outs = []
+    try:
+        for grid in (0, ctas):
+            B.fp8q_test_set_fused_grid(grid)
+            o = dict(wt=torch.empty(N, K, dtype=torch.uint8, device="cuda"),
+                     wq=torch.empty(K, N, dtype=torch.uint8, device="cuda"),
+                     a=torch.empty(M, K, dtype=torch.bfloat16, device="cuda"),
+                     q=torch.empty(M, K, dtype=torch.uint8, device="cuda"),
+                     y=torch.empty(M, N, dtype=torch.bfloat16, device="cuda"),
+                     aw=torch.zeros(1, device="cuda"), ax=torch.zeros(1, device="cuda"),
+                     sx=torch.zeros(1, dtype=torch.int64, device="cuda"),
+                     sw=torch.zeros(1, dtype=torch.int64, device="cuda"),
+                     st=torch.zeros(1, dtype=torch.int32, device="cuda"),
+                     ws=torch.zeros(B.fp8_downproj_workspace_bytes(M), dtype=torch.uint8, device="cuda"))
+            B.fp8_downproj_fwd_ex(H, o["wt"], sx, sw, o["q"], o["y"], o["ws"], w=Wd, w_q=o["wq"], amax_w=o["aw"],
+                                  sat_w=o["sw"], act=B.ACT_RELU2, act_out=o["a"], amax_out=o["ax"],
+                                  sat_count=o["sx"], status=o["st"])
+            torch.cuda.synchronize()
+            assert o["st"].item() == 0 and int(o["ws"].sum().item()) == 0
+            outs.append(o)
+    finally:
+        B.fp8q_test_set_fused_grid(0)
+    ref, got = outs
+    for k in ("wt", "wq", "q", "aw", "ax", "sx", "sw"):
+        assert torch.equal(ref[k], got[k]), k
+    for k in ("a", "y"):
+        assert torch.equal(ref[k].view(torch.int16), got[k].view(torch.int16)), k
+    ro = O.quant(h, O.ACT_RELU2, O.E4M3, 20.0, want_act=False)
+    assert np.array_equal(host_u8(got["q"]), ro["q"]) and got["sx"].item() == ro["sat"]
+
+
+def test_fused_weight_saturation_count():
+    """The kernel's weight cast counts the values its scale saturates (the
+    overflow test of detect-and-recompute), like the standalone cast and the
+    oracle: a scale with margin 2 saturates nothing, one 8x larger (margin
+    0.25) exactly the oracle's count of values."""
+    M, N, K = 512, 272, 640
+    h, w = _inputs(M, N, K, seed=8)
+    amax_w = O.amax(w, O.ACT_IDENTITY)
+    for big in (False, True):
+        s_w = O.delayed_scale(amax_w, 0.25 if big else 2.0, O.E4M3)
+        sat_w = torch.full((1,), 5, dtype=torch.int64, device="cuda")
+        sat_w2 = torch.full((1,), 5, dtype=torch.int64, device="cuda")
+        wt = torch.empty(N, K, dtype=torch.uint8, device="cuda")
+        q = torch.empty(M, K, dtype=torch.uint8, device="cuda")
+        y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+        ws = torch.zeros(B.fp8_downproj_workspace_bytes(M), dtype=torch.uint8, device="cuda")
+        B.fp8_downproj_fwd_ex(dev_bf16(h), wt, dev_f32(20.0), dev_f32(s_w), q, y, ws, w=dev_bf16(w),
+                              sat_w=sat_w, act=B.ACT_RELU2)
+        B.fp8_quant_fused(dev_bf16(w), B.ACT_IDENTITY, B.E4M3, dev_f32(s_w), q_t_out=torch.empty_like(wt),
+                          sat_count=sat_w2)
+        torch.cuda.synchronize()
+        rw = O.quant(w, O.ACT_IDENTITY, O.E4M3, s_w, want_act=False)
+        assert sat_w.item() == sat_w2.item() == rw["sat"]
+        assert (rw["sat"] > 0) == big

@@ -471,6 +471,50 @@ def test_dgrad_act_closed_forms():
     assert np.array_equal(dr, d2[rows])
 
 
+def _pow2_step(h: np.ndarray) -> np.ndarray:
+    """delta = 2^(floor(log2|h|) - 8): h is a BF16 value (8 significant bits), so
+    h +- delta has at most 10 and its square at most 20 -- both exact in float32,
+    which is what the oracle's forward activation computes in."""
+    return np.exp2(np.floor(np.log2(np.abs(h))) - 8.0)
+
+
+@pytest.mark.parametrize("which", [O.ACT_RELU2, O.ACT_RELU, O.ACT_IDENTITY])
+def test_act_grad_is_the_derivative_of_the_forward_activation(which):
+    """act_grad against a central difference of the oracle's own forward
+    activation O.act (pinned separately by its closed forms), computed in
+    float64: (act(h + d) - act(h - d)) / 2d.  For the quadratic ReLU^2 and the
+    piecewise-linear ReLU / identity the central difference has no truncation
+    error once |h| > d, and with d a power of two 2^-8 |h| every evaluation is
+    exact, so the two must agree bit for bit over a sweep of BF16 values of
+    both signs across 60 binades.  A derivative taken as h instead of 2h, as
+    2 relu(h)^2, or at the activation's output instead of its input fails."""
+    rng = np.random.default_rng(26)
+    mags = np.exp2(rng.uniform(-30, 30, 3000)) * rng.uniform(1.0, 2.0, 3000)
+    hv = (mags * rng.choice([-1.0, 1.0], 3000)).astype(np.float32)
+    hb = O.f32_to_bf16(hv)
+    h = O.bf16_to_f32(hb).astype(np.float64)
+    d = _pow2_step(h)
+    fd = np.array([(O.act(float(x + e), which) - O.act(float(x - e), which)) / (2.0 * e)
+                   for x, e in zip(h, d)], dtype=np.float64)
+    g = O.act_grad(hb, which)
+    assert np.array_equal(g, fd)
+    # one-sided differences where the activation has its kink: at h = +0 and
+    # -0 the right difference of ReLU^2 is d (-> 0) and of ReLU is 1, the left
+    # one 0; the oracle takes the forward's own comparison h > 0 there, i.e.
+    # the left derivative 0 for both, and 1 for the identity
+    e = 2.0 ** -20
+    for z in (0.0, -0.0):
+        zb = O.f32_to_bf16(np.array([z], np.float32))
+        left = (O.act(z, which) - O.act(z - e, which)) / e
+        right = (O.act(z + e, which) - O.act(z, which)) / e
+        assert O.act_grad(zb, which)[0] == left
+        assert right == {O.ACT_RELU2: e, O.ACT_RELU: 1.0, O.ACT_IDENTITY: 1.0}[which]
+    # far into the negative half the activation is flat (ReLU, ReLU^2)
+    neg = O.f32_to_bf16(np.array([-1.0, -3.5e-30, -6.0e20], np.float32))
+    want = 1.0 if which == O.ACT_IDENTITY else 0.0
+    assert np.array_equal(O.act_grad(neg, which), [want] * 3)
+
+
 def test_group_gemm_reductions():
     """Group mode: equal scales reduce to per-tensor; power-of-two scales that
     differ per row, per 128-slice of K and per 128-block of N reduce to numpy's

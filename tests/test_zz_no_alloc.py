@@ -1,25 +1,32 @@
-"""fp8_downproj_fwd_noalloc (the fused quantize + GEMM with its ready counts
-in the library's static device array) against fp8_downproj_fwd (the same
-kernel with a caller workspace).  Two no-alloc calls in a row, with different
-inputs and a smaller M the second time, into the same output buffers: counts
-left over from the first call would let the second call's GEMM load stale
-codes, so a missing clear shows up as a mismatch.  The two entry points run
-one kernel, so every output must agree bit for bit (inside the GEMM
-tolerance of the other tests)."""
+"""fp8_downproj_fwd_noalloc -- the fused quantize + GEMM for callers that
+cannot allocate device memory -- against fp8_downproj_fwd (the same kernel
+with a caller workspace) and against the oracle.
+
+The entry point keeps the kernel's counters in one static array of the
+library.  Before each call here the array is filled with 0xFF bytes through a
+test hook, as a call that was cut short could leave it: ready counts that
+claim every row is quantized, work tickets past the end and a finished-CTA
+count that never reaches the grid.  The entry point must clear what it uses
+before its kernel starts, or the GEMM reads codes that are not written yet
+and the outputs differ.  Two calls in a row, with different inputs and a
+smaller M the second time, into the same output buffers; every output must
+equal the workspace entry's bit for bit (inside the GEMM tolerance of the
+other tests), and the first call's outputs also the oracle's."""
 import numpy as np
 import pytest
 import torch
 
+import oracle as O
 from quantize_fp8_gemm_gb300 import binding as B
 from quantize_fp8_gemm_gb300 import workloads as WL
-from tests.parity import dev_bf16, dev_f32
+from tests.parity import assert_gemm_close, dev_bf16, dev_f32, host_bits16, host_u8
 
 pytestmark = pytest.mark.gpu
 
 
 def _outputs(M, N, K):
-    return dict(a=torch.empty(M, K, dtype=torch.bfloat16, device="cuda"),
-                q=torch.empty(M, K, dtype=torch.uint8, device="cuda"),
+    return dict(a=torch.full((M, K), 1.0, dtype=torch.bfloat16, device="cuda"),
+                q=torch.full((M, K), 0x33, dtype=torch.uint8, device="cuda"),
                 y=torch.empty(M, N, dtype=torch.bfloat16, device="cuda"),
                 amax=torch.full((1,), -1.0, device="cuda"),
                 sat=torch.full((1,), 99, dtype=torch.int64, device="cuda"),
@@ -39,23 +46,34 @@ def test_noalloc_matches_workspace_entry_two_calls():
     rng = np.random.default_rng(2024)
     w_bits = WL.to_bf16_bits(rng.standard_normal((K, N)).astype(np.float32) * np.float32(0.05))
     wt = torch.empty(N, K, dtype=torch.uint8, device="cuda")
-    sw = dev_f32(300.0)
+    s_w, s_x = 300.0, 40.0
+    sw, sx = dev_f32(s_w), dev_f32(s_x)
     B.fp8_quant_fused(dev_bf16(w_bits), B.ACT_IDENTITY, B.E4M3, sw, q_t_out=wt)
-    sx = dev_f32(40.0)
     Mmax = 1000
     mine = _outputs(Mmax, N, K)  # shared by both no-alloc calls
-    for M, std in ((1000, 1.5), (700, 2.5)):
-        h = dev_bf16(WL.to_bf16_bits(rng.standard_normal((M, K)).astype(np.float32) * np.float32(std)))
+    for i, (M, std) in enumerate(((1000, 1.5), (700, 2.5))):
+        h_bits = WL.to_bf16_bits(rng.standard_normal((M, K)).astype(np.float32) * np.float32(std))
+        h = dev_bf16(h_bits)
         ref = _outputs(M, N, K)
         ws = torch.empty(B.fp8_downproj_workspace_bytes(M), dtype=torch.uint8, device="cuda")
         B.fp8_downproj_fwd(h, wt, sx, sw, ref["q"], ref["y"], ws, act=B.ACT_RELU2, act_out=ref["a"],
                            amax_out=ref["amax"], sat_count=ref["sat"], status=ref["st"])
+        B.fp8q_test_noalloc_fill(0xFF)  # what a call cut short could leave behind
         B.fp8_downproj_fwd_noalloc(h, wt, sx, sw, mine["q"][:M], mine["y"][:M], act=B.ACT_RELU2,
                                    act_out=mine["a"][:M], amax_out=mine["amax"], sat_count=mine["sat"],
                                    status=mine["st"])
         torch.cuda.synchronize()
         _same(mine, ref, M)
         assert ref["sat"].item() > 0  # the scale saturates some of these rows
+        if i == 0:
+            ro = O.quant(h_bits, O.ACT_RELU2, O.E4M3, s_x)
+            assert np.array_equal(host_u8(mine["q"][:M]), ro["q"])
+            assert np.array_equal(host_bits16(mine["a"][:M]), ro["act"])
+            assert mine["amax"].item() == ro["amax"] and mine["sat"].item() == ro["sat"]
+            rw = O.quant(w_bits, O.ACT_IDENTITY, O.E4M3, s_w, want_act=False)
+            rows = WL.sample_rows(M, 64, seed=31)
+            Yr, S = O.gemm_fwd(ro["q"][rows], rw["q"], s_x, s_w)
+            assert_gemm_close(mine["y"][:M], Yr, S, rows=rows)
 
 
 def test_noalloc_rejects_rows_beyond_its_array():
