@@ -487,14 +487,18 @@ def step_desc(dp) -> tuple[str, int]:
 
 
 def run_profile(args, local):
-    """A few eager steps of the workload, nothing timed: the command ncu wraps."""
-    from quantize_fp8_gemm_gb300.downproj import Fp8DownProj
+    """A few eager steps of the workload, nothing timed: the command ncu wraps.
+    With --rows the step takes the path the full-size workload takes (the
+    one-launch kernel or the two-launch cast + GEMM), so a smaller capture
+    shows the same kernels."""
+    from quantize_fp8_gemm_gb300.downproj import FUSED_MIN_ROWS, Fp8DownProj
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     w = workload(args.workload, args.rows)
     H = WL.bf16_tensor(WL.h_preact(w, 0)).to(dev)
     Wt = WL.bf16_tensor(WL.w_down(w)).to(dev)
-    dp = Fp8DownProj(w.M, w.K, w.N, margin=w.margin, history_len=w.history_len, device=dev)
+    fused = WL.WORKLOADS[args.workload].M >= FUSED_MIN_ROWS
+    dp = Fp8DownProj(w.M, w.K, w.N, margin=w.margin, history_len=w.history_len, fused=fused, device=dev)
     dp.calibrate(H, Wt)
     for _ in range(max(1, args.steps)):
         dp.step(H, Wt)

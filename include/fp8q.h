@@ -14,6 +14,8 @@
  *   (fp8_gemm_wgrad         dW = X_q^T dY_q / (s_x s_dy), the weight gradient)
  *   (fp8_upproj_fwd         the preceding up-projection with 1 in its epilogue)
  *   (fp8_gemm_dgrad_act     dgrad with the activation backward in its epilogue)
+ *   (fp8_quant_mx,          MXFP8: 32-value blocks with power-of-two scales,
+ *    fp8_gemm_mx             on the block-scaled tensor cores)
  *
  * Conventions shared by every call:
  *  - All tensor pointers are DEVICE pointers to caller-owned memory; the
@@ -43,6 +45,8 @@
  *           E5M2 for gradients; Step 3 -- FP8 inputs, a wider running sum.
  *  [tiles]  same page, Trade-offs and edge cases -- amax computed online per
  *           1x128 activation tile and per 128x128 weight block.
+ *  [mx]     same page, Trade-offs and edge cases -- MXFP8 (Blackwell): one
+ *           power-of-two scale per block of 32 adjacent values.
  *  [gemms]  "FP8 Training & Inference", FP8 Training Recipe -- Y = X x W in
  *           E4M3; dX = dY x W^T with dY in E5M2 and W in E4M3; Per-Tensor
  *           Scaling for FP8 -- the scales are factored out of the matmul and
@@ -460,6 +464,66 @@ int fp8_downproj_fwd_noalloc(const void* h, const void* wt_q, int64_t M, int64_t
                              const float* scale_x, const float* scale_w,
                              void* act_out, void* x_q, float* amax_out, unsigned long long* sat_count,
                              void* y, int* status, cudaStream_t stream);
+
+/*
+ * fp8_quant_mx -- MXFP8 quantize: one power-of-two scale per 32 adjacent values  [mx]
+ *
+ * "FP8 training: what it is and how it works", Trade-offs and edge cases: the
+ * microscaling recipe gives every block of 32 adjacent values its own scale,
+ * and the scales are powers of two.  The pages fix neither which power of two
+ * nor how it is stored; here (Step 2's scale = format max / amax, rounded
+ * down so that no value of the block saturates):
+ *     a = act(h), abf = BF16(a)                     as in fp8_quant_fused
+ *     amax_b = max |abf| over the block
+ *     s_b = 2^e, e = the largest integer with amax_b * 2^e <= fmt_max,
+ *           clamped to [-127, 127]; e = 0 for an all-zero block
+ *     q = FP8(float32(abf * s_b))                   (never saturates)
+ *     scale byte = 127 - e: the biased 8-bit exponent of the dequantisation
+ *           factor 1 / s_b, i.e. the E8M0 scale the block-scaled tensor-core
+ *           MMA takes (2^(byte - 127) multiplies the block's codes)
+ * Two modes, exactly one per call:
+ *   rows:     blocks run along the rows of h [M,K] (K % 32 == 0):
+ *             q_out [M,K] codes, sf_out [M, K/32] bytes (row-major), act_out
+ *             [M,K] BF16 or NULL.  The activation X of the forward GEMM.
+ *   columns:  blocks run down the columns of h [M,K] (M % 32 == 0), and the
+ *             codes are written transposed: q_t_out [K,M], sf_t_out [K, M/32]
+ *             (block b of row k of the copy covers h[32b .. 32b + 31, k]).  The
+ *             weight W [K_w, N_w] of the forward GEMM: its copy W_q^T [N_w, K_w]
+ *             is the GEMM's K-major operand with blocks along K_w.  act_out must
+ *             be NULL.
+ *   amax_out, sat_count  device float / uint64 or NULL; zeroed by the call
+ *             (sat_count counts |abf * s_b| > fmt_max: 0 for finite inputs).
+ * Errors: FP8Q_ERR_UNSUPPORTED for both or neither mode, act_out in column
+ * mode, a bad act or fmt, or no sm_103 device; FP8Q_ERR_NULL for a missing
+ * output of the chosen mode; FP8Q_ERR_SHAPE for M < 0, (row mode) K < 32 or
+ * K % 32 != 0, (column mode) M % 32 != 0, K < 16 or K % 16 != 0;
+ * FP8Q_ERR_ALIGN for tensors not 16-byte aligned.
+ */
+int fp8_quant_mx(const void* h, int64_t M, int64_t K, int act, int fmt, void* act_out, void* q_out,
+                 uint8_t* sf_out, void* q_t_out, uint8_t* sf_t_out, float* amax_out,
+                 unsigned long long* sat_count, cudaStream_t stream);
+
+/*
+ * fp8_gemm_mx -- the MXFP8 GEMM on the block-scaled tensor cores  [mx][gemms]
+ *
+ *   y[i,j] = BF16( sum_k dec(x_q[i,k]) 2^(sf_x[i, k/32] - 127)
+ *                        dec(wt_q[j,k]) 2^(sf_w[j, k/32] - 127) )
+ * with FP32 accumulation; the scales are applied by the MMA
+ * (tcgen05.mma.kind::mxf8f6f4.block_scale), block by block.
+ *   x_q     device [M,K] codes (fmt_x), K contiguous: the rows-mode output of
+ *           fp8_quant_mx.
+ *   sf_x    device [M, K/32] scale bytes.
+ *   wt_q    device [N,K] codes (fmt_w): the column-mode output of
+ *           fp8_quant_mx run on W [K,N].
+ *   sf_w    device [N, K/32] scale bytes.
+ *   y       device [M,N] BF16.
+ *   M, N, K M >= 0 (0: nothing is enqueued); N >= 16, N % 16 == 0; K >= 32,
+ *           K % 32 == 0.
+ *   fmt_x, fmt_w  FP8Q_E4M3 or FP8Q_E5M2.
+ *   status  device int or NULL: FP8Q_DEV_TIMEOUT if a bounded wait gave up.
+ */
+int fp8_gemm_mx(const void* x_q, const uint8_t* sf_x, const void* wt_q, const uint8_t* sf_w, void* y,
+                int64_t M, int64_t N, int64_t K, int fmt_x, int fmt_w, int* status, cudaStream_t stream);
 
 /*
  * amax_history_update -- delayed per-tensor scale for the next step  [fused][gemms]

@@ -36,6 +36,13 @@ extern "C" {
 int fp8q_gemm_set_tile(int pair, int bn);
 
 /*
+ * fp8q_mx_set_tile -- pin the tile width of fp8_gemm_mx: 128, 192 or 256
+ * (one CTA per 128 x bn tile), or 0 for the automatic choice (the default).
+ * Returns FP8Q_ERR_UNSUPPORTED for any other value (nothing changes).
+ */
+int fp8q_mx_set_tile(int bn);
+
+/*
  * fp8q_gemm_test_hold_loads -- failure-path hook.  While on != 0, the GEMM
  * kernels launched afterwards issue no operand loads, so their first bounded
  * wait runs out (after about 2 s): the kernel ORs FP8Q_DEV_TIMEOUT into the

@@ -25,7 +25,8 @@ function to printed values, closed forms, exhaustive code sweeps or an
 independent library routine; the group-scale and MX GEMMs are pinned by
 closed-form special cases and exact integer sums (see there).  The MX
 functions (32-value blocks, power-of-two scales: "FP8 training: what it is
-and how it works", Trade-offs and edge cases) have no GPU counterpart yet.
+and how it works", Trade-offs and edge cases) are the reference of the
+block-scaled GPU path (fp8_quant_mx, fp8_gemm_mx).
 """
 import ctypes
 import os
@@ -82,7 +83,7 @@ def lib():
         L.oref_gemm_fwd.argtypes = [P, i32, P, i32, i64, i64, i64, P, P, i32, P, i64, P, P, i32]
         L.oref_mx_scale.argtypes = [f32, i32]
         L.oref_mx_scale.restype = f32
-        L.oref_quant_mx.argtypes = [P, i64, i64, i32, i32, P, P, P, P, P, P]
+        L.oref_quant_mx.argtypes = [P, i64, i64, i32, i32, P, P, P, P, P, P, i32]
         L.oref_gemm_mx.argtypes = [P, i32, P, i32, i64, i64, i64, P, P, P, i64, P, P, i32]
         L.oref_gemm_dgrad.argtypes = [P, i32, P, i32, i64, i64, i64, f32, f32, P, i64, P, P, i32]
         L.oref_openmp_max_threads.restype = i32
@@ -191,7 +192,7 @@ def mx_scale(amax_b: float, fmt: int) -> float:
     return lib().oref_mx_scale(amax_b, fmt)
 
 
-def quant_mx(h_bf16, act_kind: int, fmt: int, *, want_act=True):
+def quant_mx(h_bf16, act_kind: int, fmt: int, *, want_act=True, nthreads=None):
     """MX quantize: one power-of-two scale per 32-value block of each row of the
     [M,K] BF16 tensor.  Returns q, act, scales [M, K/32] (float32 powers of
     two), exps [M, K/32] (the biased exponent bytes of 1 / scale), amax, sat."""
@@ -204,7 +205,8 @@ def quant_mx(h_bf16, act_kind: int, fmt: int, *, want_act=True):
     exps = np.empty((M, K // 32), np.uint8)
     amax = np.zeros(1, np.float32)
     sat = np.zeros(1, np.uint64)
-    lib().oref_quant_mx(_p(h), M, K, act_kind, fmt, _p(a), _p(q), _p(scales), _p(exps), _p(amax), _p(sat))
+    lib().oref_quant_mx(_p(h), M, K, act_kind, fmt, _p(a), _p(q), _p(scales), _p(exps), _p(amax), _p(sat),
+                        nthreads or default_threads())
     return {"act": a, "q": q, "scales": scales, "exps": exps, "amax": float(amax[0]), "sat": int(sat[0])}
 
 

@@ -428,12 +428,18 @@ float oref_mx_scale(float amax_b, int fmt)
  */
 void oref_quant_mx(const uint16_t* h, int64_t M, int64_t K, int act, int fmt,
                    uint16_t* act_out, uint8_t* q_out, float* scales, uint8_t* exps,
-                   float* amax_out, uint64_t* sat_out)
+                   float* amax_out, uint64_t* sat_out, int nthreads)
 {
     const int64_t B = 32, nb = K / B;
     double fmax = fmt_of(fmt).max_value;
-    uint32_t am = 0;
-    uint64_t sat = 0;
+    uint32_t* row_amax = (uint32_t*)calloc((size_t)(M > 0 ? M : 1), sizeof(uint32_t));
+    uint64_t* row_sat = (uint64_t*)calloc((size_t)(M > 0 ? M : 1), sizeof(uint64_t));
+    (void)nthreads;
+    /* rows are independent: they are split over host threads, each row's
+       maximum and count kept apart and combined below */
+#ifdef _OPENMP
+#pragma omp parallel for num_threads(nthreads > 0 ? nthreads : 1) schedule(static)
+#endif
     for (int64_t i = 0; i < M; ++i) {
         for (int64_t b = 0; b < nb; ++b) {
             uint32_t m = 0;
@@ -447,18 +453,26 @@ void oref_quant_mx(const uint16_t* h, int64_t M, int64_t K, int act, int fmt,
             (void)frexp((double)s, &e); /* s = 2^(e - 1) */
             if (scales) scales[i * nb + b] = s;
             if (exps) exps[i * nb + b] = (uint8_t)(127 - (e - 1));
-            if (m > am) am = m;
+            if (m > row_amax[i]) row_amax[i] = m;
             for (int64_t k = b * B; k < (b + 1) * B; ++k) {
                 uint16_t abf; float v; uint8_t q;
                 quant_one(h[i * K + k], act, fmt, s, &abf, &v, &q);
                 if (act_out) act_out[i * K + k] = abf;
                 if (q_out) q_out[i * K + k] = q;
-                if (fabs((double)v) > fmax) sat += 1;
+                if (fabs((double)v) > fmax) row_sat[i] += 1;
             }
         }
     }
+    uint32_t am = 0;
+    uint64_t sat = 0;
+    for (int64_t i = 0; i < M; ++i) {
+        if (row_amax[i] > am) am = row_amax[i];
+        sat += row_sat[i];
+    }
     if (amax_out) *amax_out = f32_from_bits(am);
     if (sat_out) *sat_out = sat;
+    free(row_amax);
+    free(row_sat);
 }
 
 /* amax only: max |BF16(act(h))| over the tensor (the calibration pass). */

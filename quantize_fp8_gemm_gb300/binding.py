@@ -77,9 +77,13 @@ def lib() -> ctypes.CDLL:
         L.fp8q_test_set_fused_grid.restype = i32
         L.fp8q_test_noalloc_fill.argtypes = [i32, P]
         L.fp8q_test_noalloc_fill.restype = i32
+        L.fp8q_mx_set_tile.argtypes = [i32]
+        L.fp8q_mx_set_tile.restype = i32
+        L.fp8_quant_mx.argtypes = [P, i64, i64, i32, i32, P, P, P, P, P, P, P, P]
+        L.fp8_gemm_mx.argtypes = [P, P, P, P, P, i64, i64, i64, i32, i32, P, P]
         for fn in ("fp8_quant_fused", "fp8_quant_fused_ex", "fp8_quant_fused_batch", "fp8_downproj_fwd",
                    "fp8_downproj_fwd_noalloc", "fp8_downproj_fwd_ex", "fp8_gemm_fwd", "fp8_gemm_fwd_update", "fp8_gemm_dgrad", "fp8_gemm_wgrad", "fp8_gemm_dgrad_act", "fp8_upproj_fwd", "amax_history_update",
-                   "amax_history_update_ex"):
+                   "amax_history_update_ex", "fp8_quant_mx", "fp8_gemm_mx"):
             getattr(L, fn).restype = i32
         _lib = L
     return _lib
@@ -366,6 +370,33 @@ def fp8_downproj_fwd_noalloc(h: torch.Tensor, wt_q: torch.Tensor, scale_x: torch
     _check("fp8_downproj_fwd_noalloc", st)
 
 
+def fp8_quant_mx(h: torch.Tensor, act: int, fmt: int, *, act_out=None, q_out=None, sf_out=None, q_t_out=None,
+                 sf_t_out=None, amax_out=None, sat_count=None, stream=None) -> None:
+    """MXFP8 quantize of h [M,K]: one power-of-two scale byte per 32 values, along the rows
+    (q_out [M,K], sf_out [M,K/32]) or down the columns, transposed (q_t_out [K,M], sf_t_out [K,M/32])."""
+    M, K = h.shape
+    n = M * K
+    st = lib().fp8_quant_mx(
+        _ptr(h, 2 * n, "h"), M, K, act, fmt, _ptr(act_out, 2 * n, "act_out"), _ptr(q_out, n, "q_out"),
+        _ptr(sf_out, n // 32, "sf_out"), _ptr(q_t_out, n, "q_t_out"), _ptr(sf_t_out, n // 32, "sf_t_out"),
+        _ptr(amax_out, 4, "amax_out"), _ptr(sat_count, 8, "sat_count"), _stream(stream))
+    _check("fp8_quant_mx", st)
+
+
+def fp8_gemm_mx(x_q: torch.Tensor, sf_x: torch.Tensor, wt_q: torch.Tensor, sf_w: torch.Tensor, y: torch.Tensor, *,
+                fmt_x: int = E4M3, fmt_w: int = E4M3, status=None, stream=None) -> None:
+    """y[M,N] = BF16(sum_k x_q 2^(sf_x - 127) wt_q 2^(sf_w - 127)) on the block-scaled tensor cores."""
+    M, K = x_q.shape
+    N = wt_q.shape[0]
+    if wt_q.shape[1] != K:
+        raise ValueError("x_q [M,K] and wt_q [N,K] disagree on K")
+    st = lib().fp8_gemm_mx(
+        _ptr(x_q, M * K, "x_q"), _ptr(sf_x, M * (K // 32), "sf_x"), _ptr(wt_q, N * K, "wt_q"),
+        _ptr(sf_w, N * (K // 32), "sf_w"), _ptr(y, 2 * M * N, "y"), M, N, K, fmt_x, fmt_w,
+        _ptr(status, 4, "status"), _stream(stream))
+    _check("fp8_gemm_mx", st)
+
+
 def amax_history_update(history: torch.Tensor, head: torch.Tensor, amax_new: torch.Tensor, margin: float,
                         fmt: int, scale_out: torch.Tensor, *, status=None, stream=None) -> None:
     """Push amax_new into the device ring; scale_out = fmt_max / (margin * max(history))."""
@@ -418,6 +449,11 @@ def fp8q_gemm_set_tile(pair: int, bn: int = 0) -> None:
 def fp8q_gemm_test_hold_loads(on: bool) -> None:
     """Failure-path test hook: later GEMMs issue no loads and report FP8Q_DEV_TIMEOUT."""
     lib().fp8q_gemm_test_hold_loads(1 if on else 0)
+
+
+def fp8q_mx_set_tile(bn: int) -> None:
+    """Pin fp8_gemm_mx's tile width (128, 192, 256; 0 = automatic)."""
+    _check("fp8q_mx_set_tile", lib().fp8q_mx_set_tile(int(bn)))
 
 
 def fp8q_test_set_fused_grid(ctas: int) -> None:

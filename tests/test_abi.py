@@ -324,3 +324,41 @@ def test_batch_quant_argument_checks(lib):
     assert lib.fp8_quant_fused_batch(arr, 2, None) == ERR_UNSUPPORTED
     arr[1].flags = 1
     assert lib.fp8_quant_fused_batch(arr, 2, None) == ERR_UNSUPPORTED  # valid: no sm_103 device here
+
+
+def test_mx_argument_checks(lib):
+    """fp8_quant_mx / fp8_gemm_mx check their arguments on the host."""
+    P, i64 = ctypes.c_void_p, ctypes.c_int64
+    q = lib.fp8_quant_mx
+    q.argtypes = [P, i64, i64, ctypes.c_int, ctypes.c_int] + [P] * 8
+    q.restype = ctypes.c_int
+
+    def quant(M=64, K=256, act=2, fmt=0, a=None, qo=A, sf=A, qt=None, sft=None):
+        return q(A, M, K, act, fmt, a, qo, sf, qt, sft, None, None, None)
+
+    assert quant(qo=None, sf=None) == ERR_UNSUPPORTED            # no mode
+    assert quant(qt=A, sft=A) == ERR_UNSUPPORTED                 # both modes
+    assert quant(qo=None, sf=None, qt=A, sft=A, a=A) == ERR_UNSUPPORTED  # act copy in column mode
+    assert quant(sf=None) == ERR_NULL
+    assert quant(K=48) == ERR_SHAPE                              # rows: K % 32
+    assert quant(qo=None, sf=None, qt=A, sft=A, M=48) == ERR_SHAPE  # columns: M % 32
+    assert quant(qo=None, sf=None, qt=A, sft=A, K=24) == ERR_SHAPE  # columns: K % 16
+    assert quant(act=4) == ERR_UNSUPPORTED
+    assert quant(a=A + 8) == ERR_ALIGN
+    assert quant() == ERR_UNSUPPORTED                            # valid: no sm_103 device here
+    assert quant(qo=None, sf=None, qt=A, sft=A, K=272) == ERR_UNSUPPORTED
+    g = lib.fp8_gemm_mx
+    g.argtypes = [P] * 5 + [i64] * 3 + [ctypes.c_int] * 2 + [P] * 2
+    g.restype = ctypes.c_int
+
+    def gemm(M=128, N=256, K=512, fx=0, fw=0, x=A, y=A):
+        return g(x, A, A, A, y, M, N, K, fx, fw, None, None)
+
+    assert gemm(fx=2) == ERR_UNSUPPORTED
+    assert gemm(x=None) == ERR_NULL
+    assert gemm(K=48) == ERR_SHAPE
+    assert gemm(N=24) == ERR_SHAPE
+    assert gemm(y=A + 2) == ERR_ALIGN
+    assert gemm() == ERR_UNSUPPORTED
+    assert lib.fp8q_mx_set_tile(96) == ERR_UNSUPPORTED
+    assert lib.fp8q_mx_set_tile(192) == OK and lib.fp8q_mx_set_tile(0) == OK

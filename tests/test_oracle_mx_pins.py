@@ -4,7 +4,8 @@ and how it works", Trade-offs and edge cases).  The scale is read as Step 2's
 format max / amax rounded down to a power of two; these tests pin that
 reading, the quantize's reduction to the per-tensor quantize, the property the
 pages give for small blocks (an outlier changes only its own block), and the
-GEMM's exact sums on small integers.  No GPU counterpart exists yet."""
+GEMM's exact sums on small integers.  The GPU path (fp8_quant_mx, fp8_gemm_mx) is
+tested against these functions in tests/test_mx_gpu.py."""
 import numpy as np
 import pytest
 
