@@ -873,6 +873,36 @@ def measure_other_rows(dev, reps: int, fp8_tflops: float) -> dict:
     t = timed_b2b([lambda x=x: B.fp8_gemm_fwd(x, wt_q, gsx, gsw, y, group_mode=1) for x in xqs], reps)
     out["a12 group-scaled GEMM"] = mma_row(t, 2.0 * M * N * K, f"X_q [{M},{K}] x W_q^T [{N},{K}]")
     del xqs, xq, W, wt_q, y
+    # next: MXFP8 (one power-of-two scale per 32 values) at the outlier and GPT-2-XL shapes: the
+    # quantize of H (row blocks), the weight cast (column blocks, transposed) and the block-scaled GEMM
+    for wl_name in ("outlier", "gpt2xl"):
+        wl = WL.WORKLOADS[wl_name]
+        Mx, Kx, Nx = wl.M, wl.K, wl.N
+        g = torch.Generator(device=dev).manual_seed(wl.seed)
+        Hx = copies(torch.randn(Mx, Kx, device=dev, generator=g).to(torch.bfloat16))
+        Wx = torch.randn(Kx, Nx, device=dev, generator=g).mul_(0.02).to(torch.bfloat16)
+        qx = torch.empty(Mx, Kx, dtype=torch.uint8, device=dev)
+        sfx = torch.empty(Mx, Kx // 32, dtype=torch.uint8, device=dev)
+        ax = torch.empty(Mx, Kx, dtype=torch.bfloat16, device=dev)
+        r = max(4, reps // (1 if wl_name == "outlier" else 8))
+        t = timed_b2b([lambda h=h: B.fp8_quant_mx(h, B.ACT_RELU2, B.E4M3, act_out=ax, q_out=qx, sf_out=sfx,
+                                                  amax_out=amax) for h in Hx], r)
+        out[f"next: MX quantize of H, 32-value blocks ({wl_name})"] = mem_row(
+            t, 5.0 * Mx * Kx + Mx * Kx / 32, f"H [{Mx},{Kx}] -> act + E4M3 + scale bytes")
+        del Hx, ax
+        qwt = torch.empty(Nx, Kx, dtype=torch.uint8, device=dev)
+        sfw = torch.empty(Nx, Kx // 32, dtype=torch.uint8, device=dev)
+        t = timed_b2b([lambda: B.fp8_quant_mx(Wx, B.ACT_IDENTITY, B.E4M3, q_t_out=qwt, sf_t_out=sfw, amax_out=amax)],
+                      r)
+        out[f"next: MX weight cast, transposed ({wl_name})"] = mem_row(
+            t, 3.0 * Kx * Nx + Kx * Nx / 32, f"W [{Kx},{Nx}] -> W_q^T + scale bytes")
+        B.fp8_quant_mx(Wx, B.ACT_IDENTITY, B.E4M3, q_t_out=qwt, sf_t_out=sfw)
+        yx = torch.empty(Mx, Nx, dtype=torch.bfloat16, device=dev)
+        xs = copies(qx)
+        t = timed_b2b([lambda x=x: B.fp8_gemm_mx(x, sfx, qwt, sfw, yx) for x in xs], r)
+        out[f"next: MX GEMM, block-scaled tcgen05 ({wl_name})"] = mma_row(
+            t, 2.0 * Mx * Nx * Kx, f"X_q [{Mx},{Kx}] x W_q^T [{Nx},{Kx}], scales per 32 values")
+        del xs, qx, sfx, Wx, qwt, sfw, yx
     # next: the up-projection H = X_in W_up with the activation quantize in its epilogue, against
     # the same outputs from the unfused pair (the GEMM writing H, then the quantize of H); operands
     # are E4M3 codes (the GEMM's time does not depend on their values)

@@ -283,11 +283,22 @@ __device__ __forceinline__ uint32_t sf_word(const uint8_t* __restrict__ sf, int6
                                             int64_t g, bool words) {
     if (row >= rows) return 0x7F7F7F7Fu;
     const uint8_t* p = sf + row * KB + 4 * g;
-    if (words) return __ldg(reinterpret_cast<const uint32_t*>(p));
+    if (words) return __ldg(reinterpret_cast<const uint32_t*>(p));  // (unused by the cp.async route)
     uint32_t w = 0;
 #pragma unroll
     for (int b = 0; b < 4; ++b) w |= static_cast<uint32_t>(4 * g + b < KB ? __ldg(p + b) : 0x7Fu) << (8 * b);
     return w;
+}
+
+// 4-byte asynchronous copy global -> shared (no register holds it in flight);
+// src_bytes = 0 writes zeros instead of reading.
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" :: "r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+// Arrive on the mbarrier once every cp.async this thread issued so far has
+// landed (the barrier's expected count includes this arrival).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" :: "r"(bar) : "memory");
 }
 
 template <int BN>
@@ -316,10 +327,17 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     const int64_t num_tiles = num_m * num_n;
     const int num_kb = static_cast<int>((K + BK - 1) / BK);
     const int64_t KB = K / kMxBlock;  // scale bytes per row
+    // Whole 32-bit words of scale bytes per row and stage (K % 128 == 0, aligned
+    // arrays): the producer's lanes copy them into place with cp.async and the
+    // stage's barrier counts each lane's completion; otherwise they are read
+    // into registers a stage ahead and stored (bytes past K read as 127).
+    const bool words = (KB % 4 == 0) &&
+                       ((reinterpret_cast<uintptr_t>(sf_a) | reinterpret_cast<uintptr_t>(sf_b)) & 3u) == 0;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
-            mbar_init(smem_u32(&full[s]), 2);  // the TMA bytes' arrival + the scale writes' arrival
+            // the TMA bytes' arrival + the scale block's arrival(s)
+            mbar_init(smem_u32(&full[s]), words ? 1 + 32 : 2);
             mbar_init(smem_u32(&empty[s]), 1);
         }
         for (int a = 0; a < C::ACCS; ++a) {
@@ -348,22 +366,21 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 
     if (warp == 0) {
         // ------------------------------------------------ producer (whole warp)
-        const bool words = (KB % 4 == 0) && ((reinterpret_cast<uintptr_t>(sf_a) | reinterpret_cast<uintptr_t>(sf_b)) & 3u) == 0;
         uint32_t wa[4], wb[4 * C::BNC];
         auto load_sf = [&](int64_t tile, int kb) {
             const int64_t m0 = (tile / num_n) * BM, n0 = (tile % num_n) * BN;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) wa[c] = sf_word(sf_a, m0 + 32 * c + lane, M, KB, kb, words);
+            for (int c = 0; c < 4; ++c) wa[c] = sf_word(sf_a, m0 + 32 * c + lane, M, KB, kb, false);
 #pragma unroll
             for (int j = 0; j < 4 * C::BNC; ++j)
-                wb[j] = 32 * j < BN ? sf_word(sf_b, n0 + 32 * j + lane, N, KB, kb, words) : 0x7F7F7F7Fu;
+                wb[j] = 32 * j < BN ? sf_word(sf_b, n0 + 32 * j + lane, N, KB, kb, false) : 0x7F7F7F7Fu;
         };
         int stage = 0;
         uint32_t phase = 0;
         int64_t issued = 0;
         int64_t tile = blockIdx.x;
         int kb = 0;
-        if (tile < num_tiles) load_sf(tile, kb);
+        if (tile < num_tiles && !words) load_sf(tile, kb);
         while (tile < num_tiles) {
             int64_t ntile = tile;
             int nkb = kb + 1;
@@ -381,20 +398,40 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 tma_load_2d(smem_u32(sa + C::A_BYTES), &tmB, fb, kb * BK, n0);
             }
             uint8_t* sf = sf_smem + stage * C::SF_BYTES;
-            *reinterpret_cast<uint4*>(sf + lane * 16) = make_uint4(wa[0], wa[1], wa[2], wa[3]);
+            if (words) {
+                // word c of lane l: rows 32 c + l of the tile; rows past the
+                // matrix are zero-filled (their codes are zero-filled too)
 #pragma unroll
-            for (int j = 0; j < C::BNC; ++j)
-                *reinterpret_cast<uint4*>(sf + 512 * (j + 1) + lane * 16) =
-                    make_uint4(wb[4 * j], wb[4 * j + 1], wb[4 * j + 2], wb[4 * j + 3]);
-            if (ntile < num_tiles) load_sf(ntile, nkb);  // in flight while the next stage is awaited
-            fence_proxy_async_smem();  // the scale block is read by tcgen05.cp (async proxy)
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&full[stage]));
+                for (int c = 0; c < 4; ++c) {
+                    const int64_t row = m0 + 32 * c + lane;
+                    const bool in = row < M;
+                    cp_async4(smem_u32(sf + lane * 16 + 4 * c), sf_a + (in ? row * KB + 4 * kb : 0), in ? 4u : 0u);
+                }
+#pragma unroll
+                for (int j = 0; j < 4 * C::BNC; ++j) {
+                    const int64_t row = n0 + 32 * j + lane;
+                    const bool in = 32 * j < BN && row < N;
+                    cp_async4(smem_u32(sf + 512 + 512 * (j / 4) + lane * 16 + 4 * (j % 4)),
+                              sf_b + (in ? row * KB + 4 * kb : 0), in ? 4u : 0u);
+                }
+                cp_async_arrive_noinc(smem_u32(&full[stage]));
+            } else {
+                *reinterpret_cast<uint4*>(sf + lane * 16) = make_uint4(wa[0], wa[1], wa[2], wa[3]);
+#pragma unroll
+                for (int j = 0; j < C::BNC; ++j)
+                    *reinterpret_cast<uint4*>(sf + 512 * (j + 1) + lane * 16) =
+                        make_uint4(wb[4 * j], wb[4 * j + 1], wb[4 * j + 2], wb[4 * j + 3]);
+                if (ntile < num_tiles) load_sf(ntile, nkb);  // in flight while the next stage is awaited
+                fence_proxy_async_smem();  // the scale block is read by tcgen05.cp (async proxy)
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&full[stage]));
+            }
             ++issued;
             if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
             tile = ntile;
             kb = nkb;
         }
+        asm volatile("cp.async.wait_all;" ::: "memory");  // this lane's scale copies have landed
         if (lane == 0) {
             // no copy may still be landing in shared memory when the CTA exits
             const int64_t tail = issued < C::STAGES ? issued : C::STAGES;
@@ -419,6 +456,9 @@ mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 for (int kb = 0; kb < num_kb; ++kb) {
                     if (!wait_phase(&full[stage], phase, abort_flag, status)) { ok = false; break; }
                     tc_fence_after();
+                    // the scale block was written through the generic proxy (st.shared or
+                    // cp.async); tcgen05.cp reads it through the async proxy
+                    fence_proxy_async_smem();
                     const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
                     const uint32_t sf_t = tmem_base + static_cast<uint32_t>(C::ACCS * BN + stage * C::SF_COLS);
                     const uint32_t sf_s = smem_u32(sf_smem + stage * C::SF_BYTES);
