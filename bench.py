@@ -843,7 +843,15 @@ def measure_other_rows(dev, reps: int, fp8_tflops: float) -> dict:
     row["unfused_ms (dgrad writing dX, then dH = dX * 2 relu(H) elementwise)"] = t2
     row["speedup_vs_unfused"] = t2 / t
     out["next: dgrad with the ReLU^2 backward epilogue"] = row
-    del Hb, dx, dh, tmp, dyq, w_q, wt_q
+    # the same with H read from its E4M3 cache (1 byte per element instead of 2)
+    hq = torch.randint(0, 0x7E, (M, K), dtype=torch.uint8, device=dev, generator=g)
+    s_h = torch.full((1,), 38.0, device=dev)
+    t3 = timed_b2b([lambda: B.fp8_gemm_dgrad_act_q(dyq, w_q, sdy, one, hq, s_h, dh, act=B.ACT_RELU2)],
+                   max(4, reps // 8))
+    row = mma_row(t3, 2.0 * M * N * K, f"dY_q [{M},{N}] x W_q [{K},{N}]^T, H's E4M3 cache [{M},{K}] -> dH")
+    row["vs_bf16_h"] = t / t3
+    out["next: dgrad with the ReLU^2 backward epilogue, H from its FP8 cache"] = row
+    del Hb, dx, dh, tmp, dyq, w_q, wt_q, hq
     # wgrad dW = X^T dY: X_q^T [K,M] (E4M3 codes; the GEMM's time does not depend on their values)
     g = torch.Generator(device=dev).manual_seed(xl.seed)
     xqt = torch.randint(0, 120, (K, M), dtype=torch.uint8, device=dev, generator=g)

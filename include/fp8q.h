@@ -169,6 +169,16 @@ int fp8_quant_fused_ex(const void* h, int64_t M, int64_t K, int act, int fmt,
  * Every entry is checked before anything is enqueued: the first failing
  * entry's status is returned and nothing runs.  amax_out / sat_count of an
  * entry without FP8Q_ACCUMULATE are zeroed (stream-ordered) before the launch.
+ *
+ * The pre-activation's FP8 cache ("FP8 training: what it is and how it
+ * works", Trade-offs and edge cases: the activations kept for the backward
+ * pass are stored in FP8): with hq_out set, the same pass also writes
+ *     hq_out[i,k] = E4M3(float32(h[i,k] * s_h))   (h: the BF16 INPUT, before
+ *                                                   the activation; s_h = *scale_h)
+ * and folds max |h| into amax_h and #{|h * s_h| > 448} into sat_h (both
+ * optional; zeroed first unless FP8Q_ACCUMULATE), so that a backward needing
+ * act'(H) (fp8_gemm_dgrad_act_q) reads one byte per element instead of H's
+ * two.  hq_out [M,K] bytes, 16-byte aligned; scale_h required with it.
  */
 #define FP8Q_BATCH_MAX 4
 typedef struct fp8q_quant_args {
@@ -184,6 +194,10 @@ typedef struct fp8q_quant_args {
     float* group_scales_out;
     int group_rows;
     unsigned flags;
+    void* hq_out;                   /* or NULL: the FP8 cache of the pre-activation (see below) */
+    const float* scale_h;
+    float* amax_h;
+    unsigned long long* sat_h;
 } fp8q_quant_args;
 int fp8_quant_fused_batch(const fp8q_quant_args* args, int n, cudaStream_t stream);
 
@@ -266,6 +280,26 @@ int fp8_gemm_dgrad_act(const void* dy_q, const void* w_q,
                        const float* scale_dy, const float* scale_w,
                        const void* h, int act, void* dh, int64_t M, int64_t N, int64_t K,
                        int* status, cudaStream_t stream);
+
+/*
+ * fp8_gemm_dgrad_act_q -- fp8_gemm_dgrad_act with the pre-activation read from
+ * its FP8 cache  [gemms][fused]
+ *
+ * "FP8 training: what it is and how it works", Trade-offs and edge cases: the
+ * activations kept for the backward pass are stored in FP8.  H is not kept in
+ * BF16: the forward's quantize (fp8q_quant_args.hq_out) wrote h_q =
+ * E4M3(float32(h * s_h)), and the derivative is taken at its dequantised value
+ *     h~ = dec(h_q) * float32(1 / s_h)        (float32)
+ *     dh[i,k] = BF16( dX[i,k] (float32) * act'(h~) ),  act' as in
+ *     fp8_gemm_dgrad_act (2 max(h~, 0), (h~ > 0), or 1)
+ * so the epilogue reads one byte per element of H instead of two.
+ *   dy_q, w_q, scale_dy, scale_w, act, dh, M, N, K, status  as for fp8_gemm_dgrad_act.
+ *   h_q      device [M,K] E4M3 (16-byte aligned).
+ *   scale_h  device float: the scale h_q was cast with.
+ */
+int fp8_gemm_dgrad_act_q(const void* dy_q, const void* w_q, const float* scale_dy, const float* scale_w,
+                         const void* h_q, const float* scale_h, int act, void* dh, int64_t M, int64_t N, int64_t K,
+                         int* status, cudaStream_t stream);
 
 /*
  * fp8_gemm_wgrad -- dW = (X_q^T . dY_q) / (s_x s_dy), FP32 accumulation, BF16 out  [gemms]

@@ -281,6 +281,33 @@ def act_grad(h_bf16, act_kind: int):
     return np.ones_like(h)
 
 
+def act_grad_q(h_q, s_h: float, act_kind: int):
+    """The activation derivative at the pre-activation cached in FP8 ("FP8
+    training: what it is and how it works", Trade-offs and edge cases: the
+    activations kept for the backward pass are stored in FP8): h~ =
+    dec(h_q) / s_h, the E4M3 code of H dequantised with the scale it was cast
+    with (float64, exact), then the derivative of act_grad at h~."""
+    h = fp8_decode(_c(h_q, np.uint8), E4M3) / float(s_h)
+    if act_kind == ACT_RELU2:
+        return np.where(h > 0, 2.0 * h, 0.0)
+    if act_kind == ACT_RELU:
+        return np.where(h > 0, 1.0, 0.0)
+    return np.ones_like(h)
+
+
+def gemm_dgrad_act_q(dy_q, w_q, s_dy: float, s_w: float, h_q, s_h: float, act_kind: int, *, rows=None,
+                     fmt_dy=E5M2, fmt_w=E4M3, nthreads=None):
+    """gemm_dgrad_act with the pre-activation taken from its E4M3 cache h_q [M,K]
+    (cast with the scale s_h): dH = (dY x W^T) * act'(dec(h_q) / s_h).
+    Returns (dH, S): S is the dgrad's sum of |terms| times |act'|."""
+    dX, S = gemm_dgrad(dy_q, w_q, s_dy, s_w, rows=rows, fmt_dy=fmt_dy, fmt_w=fmt_w, nthreads=nthreads)
+    hq = _c(h_q, np.uint8)
+    if rows is not None:
+        hq = hq[_c(rows, np.int64)]
+    g = act_grad_q(hq, s_h, act_kind)
+    return dX * g, S * np.abs(g)
+
+
 def gemm_dgrad_act(dy_q, w_q, s_dy: float, s_w: float, h_bf16, act_kind: int, *, rows=None, fmt_dy=E5M2,
                    fmt_w=E4M3, nthreads=None):
     """The activation backward through the down-projection's dgrad:

@@ -57,6 +57,7 @@ def lib() -> ctypes.CDLL:
         L.fp8_gemm_dgrad.argtypes = [P, P, P, P, P, i64, i64, i64, P, P]
         L.fp8_gemm_wgrad.argtypes = [P, P, P, P, P, i64, i64, i64, P, P]
         L.fp8_gemm_dgrad_act.argtypes = [P, P, P, P, P, i32, P, i64, i64, i64, P, P]
+        L.fp8_gemm_dgrad_act_q.argtypes = [P, P, P, P, P, P, i32, P, i64, i64, i64, P, P]
         L.fp8_upproj_fwd.argtypes = [P, P, P, P, i32, P, P, P, P, P, P, i64, i64, i64, ctypes.c_uint, P, P]
         L.amax_history_update.argtypes = [P, i32, P, P, f32, i32, P, P, P]
         L.amax_history_update_ex.argtypes = [P, i32, P, P, f32, i32, P, P, P, P, P, P]
@@ -82,7 +83,7 @@ def lib() -> ctypes.CDLL:
         L.fp8_quant_mx.argtypes = [P, i64, i64, i32, i32, P, P, P, P, P, P, P, P]
         L.fp8_gemm_mx.argtypes = [P, P, P, P, P, i64, i64, i64, i32, i32, P, P]
         for fn in ("fp8_quant_fused", "fp8_quant_fused_ex", "fp8_quant_fused_batch", "fp8_downproj_fwd",
-                   "fp8_downproj_fwd_noalloc", "fp8_downproj_fwd_ex", "fp8_gemm_fwd", "fp8_gemm_fwd_update", "fp8_gemm_dgrad", "fp8_gemm_wgrad", "fp8_gemm_dgrad_act", "fp8_upproj_fwd", "amax_history_update",
+                   "fp8_downproj_fwd_noalloc", "fp8_downproj_fwd_ex", "fp8_gemm_fwd", "fp8_gemm_fwd_update", "fp8_gemm_dgrad", "fp8_gemm_wgrad", "fp8_gemm_dgrad_act", "fp8_gemm_dgrad_act_q", "fp8_upproj_fwd", "amax_history_update",
                    "amax_history_update_ex", "fp8_quant_mx", "fp8_gemm_mx"):
             getattr(L, fn).restype = i32
         _lib = L
@@ -162,21 +163,25 @@ class QuantArgs(ctypes.Structure):
                 ("fmt", ctypes.c_int), ("scale", ctypes.c_void_p), ("act_out", ctypes.c_void_p),
                 ("q_out", ctypes.c_void_p), ("q_t_out", ctypes.c_void_p), ("amax_out", ctypes.c_void_p),
                 ("sat_count", ctypes.c_void_p), ("group_scales_out", ctypes.c_void_p),
-                ("group_rows", ctypes.c_int), ("flags", ctypes.c_uint)]
+                ("group_rows", ctypes.c_int), ("flags", ctypes.c_uint), ("hq_out", ctypes.c_void_p),
+                ("scale_h", ctypes.c_void_p), ("amax_h", ctypes.c_void_p), ("sat_h", ctypes.c_void_p)]
 
 
 def quant_args(h: torch.Tensor, act: int, fmt: int, scale: torch.Tensor, *, act_out=None, q_out=None,
-               q_t_out=None, amax_out=None, sat_count=None, flags: int = 0) -> QuantArgs:
+               q_t_out=None, amax_out=None, sat_count=None, flags: int = 0, hq_out=None, scale_h=None,
+               amax_h=None, sat_h=None) -> QuantArgs:
     """One entry of fp8_quant_fused_batch (per-tensor scale), with the byte-size
-    checks of fp8_quant_fused.  The entry holds references to its tensors, so
-    temporaries passed here live as long as the entry."""
+    checks of fp8_quant_fused; hq_out / scale_h / amax_h / sat_h: the E4M3 cache
+    of the pre-activation h itself.  The entry holds references to its tensors,
+    so temporaries passed here live as long as the entry."""
     M, K = h.shape
     n = M * K
     v = lambda t, nb, name: (lambda p: None if p is None else p.value)(_ptr(t, nb, name))
     a = QuantArgs(v(h, 2 * n, "h"), M, K, act, fmt, v(scale, 4, "scale"), v(act_out, 2 * n, "act_out"),
                   v(q_out, n, "q_out"), v(q_t_out, n, "q_t_out"), v(amax_out, 4, "amax_out"),
-                  v(sat_count, 8, "sat_count"), None, 1, flags)
-    a._tensors = (h, scale, act_out, q_out, q_t_out, amax_out, sat_count)
+                  v(sat_count, 8, "sat_count"), None, 1, flags, v(hq_out, n, "hq_out"), v(scale_h, 4, "scale_h"),
+                  v(amax_h, 4, "amax_h"), v(sat_h, 8, "sat_h"))
+    a._tensors = (h, scale, act_out, q_out, q_t_out, amax_out, sat_count, hq_out, scale_h, amax_h, sat_h)
     return a
 
 
@@ -256,6 +261,21 @@ def fp8_gemm_dgrad_act(dy_q: torch.Tensor, w_q: torch.Tensor, scale_dy: torch.Te
         _ptr(scale_w, 4, "scale_w"), _ptr(h, 2 * M * K, "h"), act, _ptr(dh, 2 * M * K, "dh"), M, N, K,
         _ptr(status, 4, "status"), _stream(stream))
     _check("fp8_gemm_dgrad_act", st)
+
+
+def fp8_gemm_dgrad_act_q(dy_q: torch.Tensor, w_q: torch.Tensor, scale_dy: torch.Tensor, scale_w: torch.Tensor,
+                         h_q: torch.Tensor, scale_h: torch.Tensor, dh: torch.Tensor, *, act: int = ACT_RELU2,
+                         status=None, stream=None) -> None:
+    """fp8_gemm_dgrad_act with the pre-activation from its E4M3 cache h_q [M,K] (cast with scale_h)."""
+    M, N = dy_q.shape
+    K = w_q.shape[0]
+    if w_q.shape[1] != N:
+        raise ValueError("dy_q [M,N] and w_q [K,N] disagree on N")
+    st = lib().fp8_gemm_dgrad_act_q(
+        _ptr(dy_q, M * N, "dy_q"), _ptr(w_q, K * N, "w_q"), _ptr(scale_dy, 4, "scale_dy"),
+        _ptr(scale_w, 4, "scale_w"), _ptr(h_q, M * K, "h_q"), _ptr(scale_h, 4, "scale_h"), act,
+        _ptr(dh, 2 * M * K, "dh"), M, N, K, _ptr(status, 4, "status"), _stream(stream))
+    _check("fp8_gemm_dgrad_act_q", st)
 
 
 def fp8_gemm_wgrad(x_q_t: torch.Tensor, dy_q_t: torch.Tensor, scale_x: torch.Tensor, scale_dy: torch.Tensor,

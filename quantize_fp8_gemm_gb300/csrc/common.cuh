@@ -11,6 +11,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "../../include/fp8q.h"
 
@@ -98,6 +99,14 @@ __device__ __forceinline__ uint32_t cvt_bf16x2(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
+}
+
+// Two E4M3 codes (`v`'s low byte first) -> two float32 values; exact (every
+// E4M3 value is a half-precision value).
+__device__ __forceinline__ float2 e4m3x2_to_f32x2(uint16_t v) {
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(v));
+    return __half22float2(*reinterpret_cast<const __half2*>(&h2));
 }
 
 __device__ __forceinline__ float bf16lo_to_f32(uint32_t packed) { return __uint_as_float(packed << 16); }

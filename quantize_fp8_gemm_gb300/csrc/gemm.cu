@@ -192,7 +192,7 @@ struct Cfg {
 // DACT (the activation backward in the dgrad epilogue) adds a load buffer for
 // every 32-column chunk of H in the tile (BN / 16 KB) and one mbarrier: 5 KB +
 // BN / 16 KB per warp, keeping each warp's buffers 1024-byte aligned.
-template <int BN, bool GROUP, bool PAIR, bool FUSED, bool EQ = false, bool DACT = false>
+template <int BN, bool GROUP, bool PAIR, bool FUSED, bool EQ = false, int DACT = 0>
 using KernelCfg = Cfg<BN, PAIR, epi_warps<BN, GROUP, FUSED, EQ>(), GROUP ? 512 / BN : (2 * BN <= 512 ? 2 : 1),
                       EQ ? 4 * kEpiChunkBytes : DACT ? (5 + BN / 16) * 1024 : GROUP && BN == 256 ? kEpiChunkBytes : 2 * kEpiChunkBytes,
                       GROUP && BN == 256 ? kGroupRingTotal : kRingTotal>;
@@ -478,14 +478,15 @@ __device__ __forceinline__ void epi_quant_tile(const CUtensorMap* tmH, const CUt
 // (the barrier's phase is ldn & 1); epi_dact_tile waits for them once.
 // Returns false when a bounded wait gave up.
 __device__ __forceinline__ void issue_h_loads(const CUtensorMap* tmH, uint8_t* lbuf, uint64_t* lbar, uint32_t& ldn,
-                                              int lane, int nck, int c0, int step, int64_t col_base, int64_t row0) {
+                                              int lane, int nck, int c0, int step, int64_t col_base, int64_t row0,
+                                              uint32_t box_bytes) {
     fence_proxy_async_smem();  // the buffers' last reads (the previous tile) come first
     __syncwarp();
     if (lane == 0) {
         const uint32_t bar = smem_u32(lbar);
         int n = 0;
         for (int c = c0; c < nck; c += step) ++n;
-        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(n) * kEpiChunkBytes);
+        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(n) * box_bytes);
         for (int c = c0, i = 0; c < nck; c += step, ++i)
             tma_load_2d(smem_u32(lbuf + i * kEpiChunkBytes), tmH, bar, static_cast<int32_t>(col_base + c * 32),
                         static_cast<int32_t>(row0));
@@ -493,10 +494,13 @@ __device__ __forceinline__ void issue_h_loads(const CUtensorMap* tmH, uint8_t* l
     ++ldn;
 }
 
-template <int BN>
+// HFMT 1: H is BF16 (32 x 32 boxes, 64-byte swizzle); HFMT 2: H is the
+// pre-activation's E4M3 cache (32 x 32-byte boxes, unswizzled: lane r's row
+// is 32 contiguous codes), decoded exactly and multiplied by inv_h = 1 / s_h.
+template <int BN, int HFMT>
 __device__ __forceinline__ bool epi_dact_tile(const CUtensorMap* tmD, int act, uint8_t* warp_stage,
                                               const uint8_t* lbuf, uint64_t* lbar, int& nchunk, uint32_t& ldw,
-                                              int lane, uint32_t taddr, float inv, int c0, int step,
+                                              int lane, uint32_t taddr, float inv, float inv_h, int c0, int step,
                                               int64_t col_base, int64_t row0, int64_t M, int64_t N,
                                               volatile int* abort_flag, int* status) {
     const int sw = (lane >> 1) & 3;
@@ -507,23 +511,43 @@ __device__ __forceinline__ bool epi_dact_tile(const CUtensorMap* tmD, int act, u
     for (int c = c0, i = 0; c < BN / 32; c += step, ++i) {
         uint32_t r[32];
         tmem_ld_x32_sync(taddr + static_cast<uint32_t>(c * 32), r);
-        const uint8_t* hrow = lbuf + i * kEpiChunkBytes + lane * 64;
-        float v[32];
+        float hv[32];
+        if constexpr (HFMT == 2) {
+            const uint8_t* hrow = lbuf + i * kEpiChunkBytes + lane * 32;
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-            const uint4 h = *reinterpret_cast<const uint4*>(hrow + ((g ^ sw) << 4));
-            const uint32_t hw[4] = {h.x, h.y, h.z, h.w};
+            for (int g = 0; g < 2; ++g) {
+                const uint4 q = *reinterpret_cast<const uint4*>(hrow + 16 * g);
+                const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const float hv = e ? bf16hi_to_f32(hw[k]) : bf16lo_to_f32(hw[k]);
-                    const float d = hv > 0.0f ? (act == FP8Q_ACT_RELU2 ? 2.0f * hv : 1.0f) : 0.0f;
-                    const float f = act == FP8Q_ACT_IDENTITY ? 1.0f : d;
-                    const int j = g * 8 + k * 2 + e;
-                    v[j] = __uint_as_float(r[j]) * inv * f;
+                for (int k = 0; k < 4; ++k) {
+                    const float2 lo = e4m3x2_to_f32x2(static_cast<uint16_t>(qw[k] & 0xFFFFu));
+                    const float2 hi = e4m3x2_to_f32x2(static_cast<uint16_t>(qw[k] >> 16));
+                    const int j = g * 16 + k * 4;
+                    hv[j] = lo.x * inv_h;
+                    hv[j + 1] = lo.y * inv_h;
+                    hv[j + 2] = hi.x * inv_h;
+                    hv[j + 3] = hi.y * inv_h;
                 }
             }
+        } else {
+            const uint8_t* hrow = lbuf + i * kEpiChunkBytes + lane * 64;
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+                const uint4 h = *reinterpret_cast<const uint4*>(hrow + ((g ^ sw) << 4));
+                const uint32_t hw[4] = {h.x, h.y, h.z, h.w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    hv[g * 8 + k * 2] = bf16lo_to_f32(hw[k]);
+                    hv[g * 8 + k * 2 + 1] = bf16hi_to_f32(hw[k]);
+                }
+            }
+        }
+        float v[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const float d = hv[j] > 0.0f ? (act == FP8Q_ACT_RELU2 ? 2.0f * hv[j] : 1.0f) : 0.0f;
+            const float f = act == FP8Q_ACT_IDENTITY ? 1.0f : d;
+            v[j] = __uint_as_float(r[j]) * inv * f;
         }
         epi_store_chunk(tmD, warp_stage, nchunk, lane, v, static_cast<int32_t>(col_base + c * 32),
                         static_cast<int32_t>(row0), M, N);
@@ -541,7 +565,7 @@ __device__ __forceinline__ bool epi_dact_tile(const CUtensorMap* tmD, int act, u
 // FUSED = true : the fused quantize + GEMM (per-tensor scales): the extra
 //                quantize warps produce A = X_q from H while the GEMM consumes
 //                finished 128-row blocks.
-template <int BN, bool GROUP, bool PAIR, bool FUSED, bool EQ, bool DACT>
+template <int BN, bool GROUP, bool PAIR, bool FUSED, bool EQ, int DACT>
 __global__ void __launch_bounds__(gemm_threads<BN, GROUP, FUSED, EQ>(), 1)
 fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmD,
@@ -783,6 +807,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         bool ok = true;
         float inv = 1.0f;
         if (!GROUP) inv = 1.0f / (__ldg(scale_a) * __ldg(scale_b));
+        const float inv_h = DACT == 2 ? 1.0f / __ldg(eq.scale_h) : 1.0f;  // the E4M3 cache's dequantisation
         const int64_t kg = K / BK;                    // group mode: K % 128 == 0
         const int64_t ng = (N + 127) / 128;
         for (int64_t tile = first_tile; tile < num_tiles && ok; tile += tile_stride) {
@@ -793,7 +818,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                 // DACT: the first chunk's H is on its way while the accumulator fills
                 if constexpr (DACT)
                     issue_h_loads(&tmE1, lbuf, lbar, ldn, lane, BN / 32, (warp - 2) / 4, C::EPI_WARPS / 4,
-                                  n_blk * BN, row0);
+                                  n_blk * BN, row0, DACT == 2 ? 32 * 32 : kEpiChunkBytes);
                 ok = wait_phase(&tfull[acc], acc_phase, abort_flag, status);
                 ok = __all_sync(0xFFFFFFFFu, ok);
                 if (!ok) break;
@@ -804,8 +829,8 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                                        (warp - 2) / 4, C::EPI_WARPS / 4, n_blk * BN, row0, M, N, eq_amax2, eq_nsat);
                 }
                 if constexpr (DACT) {
-                    ok = epi_dact_tile<BN>(&tmD, eq.act, warp_stage, lbuf, lbar, nchunk, ldw, lane,
-                                           tmem_base + lane_base + static_cast<uint32_t>(acc * BN), inv,
+                    ok = epi_dact_tile<BN, DACT>(&tmD, eq.act, warp_stage, lbuf, lbar, nchunk, ldw, lane,
+                                           tmem_base + lane_base + static_cast<uint32_t>(acc * BN), inv, inv_h,
                                            (warp - 2) / 4, C::EPI_WARPS / 4, n_blk * BN, row0, M, N, abort_flag,
                                            status);
                 }
@@ -989,6 +1014,20 @@ bool make_q_out_map(CUtensorMap* map, void* base, int64_t rows, int64_t cols) {
     return r == CUDA_SUCCESS;
 }
 
+// E4M3 input [rows, cols] read by the epilogue: box = 32 bytes x 32 rows, no swizzle.
+bool make_q_in_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols)};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                    CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 std::atomic<int> g_hold_loads{0};   // fp8q_gemm_test_hold_loads
 std::atomic<int> g_fused_grid{0};   // fp8q_test_set_fused_grid: CTAs of the fused kernel, 0 = one per SM
 
@@ -997,7 +1036,7 @@ struct LaunchInfo {
     int max_clusters = 0;  // co-resident 2-CTA clusters (PAIR only)
 };
 
-template <int BN, bool GROUP, bool PAIR, bool FUSED, bool EQ = false, bool DACT = false>
+template <int BN, bool GROUP, bool PAIR, bool FUSED, bool EQ = false, int DACT = 0>
 const LaunchInfo& launch_info() {
     using C = KernelCfg<BN, GROUP, PAIR, FUSED, EQ, DACT>;
     static LaunchInfo info;
@@ -1035,7 +1074,7 @@ struct EpiQuantHost {
     EpiQuantArgs args;
 };
 
-template <int BN, bool GROUP, bool PAIR, bool FUSED, bool EQ = false, bool DACT = false>
+template <int BN, bool GROUP, bool PAIR, bool FUSED, bool EQ = false, int DACT = 0>
 int launch_gemm(const void* a, const void* b, const float* sa, const float* sb, void* d, int64_t M,
                 int64_t N, int64_t K, uint32_t afmt, uint32_t bfmt, int* status, cudaStream_t stream,
                 const FusedArgs& fz, const EpiQuantHost* eqh = nullptr, const void* h_in = nullptr,
@@ -1061,10 +1100,16 @@ int launch_gemm(const void* a, const void* b, const float* sa, const float* sb, 
         if (!make_out_map(&mapD, d, M, N)) return FP8Q_ERR_CUDA;
         mapE1 = mapD;
         mapE2 = mapD;
-        if constexpr (DACT) {
+        if constexpr (DACT == 1) {
             // H [M,N] (BF16), loaded in the same 32 x 32 boxes the output is stored in
             if (!make_out_map(&mapE1, const_cast<void*>(h_in), M, N)) return FP8Q_ERR_CUDA;
             eq.act = act;
+        }
+        if constexpr (DACT == 2) {
+            // H's E4M3 cache [M,N]: 32-byte x 32-row boxes, unswizzled
+            if (!make_q_in_map(&mapE1, h_in, M, N)) return FP8Q_ERR_CUDA;
+            eq.act = act;
+            eq.scale_h = eqh ? eqh->args.scale_h : nullptr;
         }
     }
     const int64_t tiles = ((M + C::TILE_M - 1) / C::TILE_M) * ((N + BN - 1) / BN);
@@ -1293,11 +1338,13 @@ Shape pick_shape_dact(int64_t M, int64_t N) {
     return best;
 }
 
+template <int HFMT>
 int launch_dact(const Shape& s, const void* a, const void* b, const float* sa, const float* sb, void* d, int64_t M,
-                int64_t N, int64_t K, const void* h, int act, int* status, cudaStream_t stream) {
+                int64_t N, int64_t K, const void* h, int act, int* status, cudaStream_t stream,
+                const EpiQuantHost* eqh = nullptr) {
 #define FP8Q_LAUNCH_DACT(BNV, PR) \
-    return launch_gemm<BNV, false, PR, false, false, true>(a, b, sa, sb, d, M, N, K, FP8Q_E5M2, FP8Q_E4M3, status, \
-                                                           stream, FusedArgs{}, nullptr, h, act)
+    return launch_gemm<BNV, false, PR, false, false, HFMT>(a, b, sa, sb, d, M, N, K, FP8Q_E5M2, FP8Q_E4M3, status, \
+                                                           stream, FusedArgs{}, eqh, h, act)
     if (s.pair) {
         if (s.bn == 256) FP8Q_LAUNCH_DACT(256, true);
         if (s.bn == 224) FP8Q_LAUNCH_DACT(224, true);
@@ -1432,7 +1479,23 @@ extern "C" int fp8_gemm_dgrad_act(const void* dy_q, const void* w_q, const float
     int st = check_gemm_args(dy_q, w_q, scale_dy, scale_w, dh, M, K, N, status);
     if (st != FP8Q_OK) return st;
     if (M == 0) return FP8Q_OK;
-    return launch_dact(pick_shape_dact(M, K), dy_q, w_q, scale_dy, scale_w, dh, M, K, N, h, act, status, stream);
+    return launch_dact<1>(pick_shape_dact(M, K), dy_q, w_q, scale_dy, scale_w, dh, M, K, N, h, act, status, stream);
+}
+
+extern "C" int fp8_gemm_dgrad_act_q(const void* dy_q, const void* w_q, const float* scale_dy, const float* scale_w,
+                                    const void* h_q, const float* scale_h, int act, void* dh, int64_t M, int64_t N,
+                                    int64_t K, int* status, cudaStream_t stream) {
+    // D = dH [M,K], A = dY [M,N] (contraction N), B = W [K,N]; H's E4M3 cache [M,K] read in the epilogue
+    if (act < FP8Q_ACT_IDENTITY || act > FP8Q_ACT_RELU2) return FP8Q_ERR_UNSUPPORTED;
+    if ((h_q == nullptr && M != 0) || scale_h == nullptr) return FP8Q_ERR_NULL;
+    if (!aligned16(h_q) || (reinterpret_cast<uintptr_t>(scale_h) & 3u)) return FP8Q_ERR_ALIGN;
+    int st = check_gemm_args(dy_q, w_q, scale_dy, scale_w, dh, M, K, N, status);
+    if (st != FP8Q_OK) return st;
+    if (M == 0) return FP8Q_OK;
+    EpiQuantHost e{};
+    e.args.scale_h = scale_h;
+    return launch_dact<2>(pick_shape_dact(M, K), dy_q, w_q, scale_dy, scale_w, dh, M, K, N, h_q, act, status, stream,
+                          &e);
 }
 
 extern "C" int fp8_gemm_wgrad(const void* x_q_t, const void* dy_q_t, const float* scale_x,

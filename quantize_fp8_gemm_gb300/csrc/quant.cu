@@ -57,12 +57,34 @@ __device__ __forceinline__ void block_reduce_publish(uint32_t amax16, uint32_t n
     }
 }
 
+// The optional FP8 cache of the pre-activation itself ("FP8 training: what
+// it is and how it works", Trade-offs and edge cases: the activations kept for
+// the backward pass are stored in FP8): h_q = E4M3(float32(h * s_h)) of the
+// BF16 input h, with its own delayed scale, maximum and saturation count, so a
+// backward that needs act'(H) reads 1 byte per element instead of 2.
+struct HCache {
+    uint2* hq;           // [M,K] E4M3, or nullptr
+    float s;             // s_h
+    uint32_t amax2 = 0;  // max |h| (two 16-bit lanes)
+    uint32_t nsat = 0;   // #{|h s_h| > 448}
+};
+
+__device__ __forceinline__ void h_cache8(HCache& c, uint4 x, uint2* dst) {
+    c.amax2 = __vmaxu2(c.amax2, x.x & 0x7FFF7FFFu);
+    c.amax2 = __vmaxu2(c.amax2, x.y & 0x7FFF7FFFu);
+    c.amax2 = __vmaxu2(c.amax2, x.z & 0x7FFF7FFFu);
+    c.amax2 = __vmaxu2(c.amax2, x.w & 0x7FFF7FFFu);
+    st_v2(dst, cast8<FP8Q_E4M3>(x, c.s, c.nsat));
+}
+
 // Per-tensor streaming pass of CTA `cta` out of `ncta`: each thread owns
-// 8-element chunks, U loads in flight, grid-stride over the tensor.
-template <int ACT, int FMT, int U = 4>
+// 8-element chunks, U loads in flight, grid-stride over the tensor.  HQ: the
+// chunk is also cast into the pre-activation cache.
+template <int ACT, int FMT, int U = 4, bool HQ = false>
 __device__ __forceinline__ void stream_body(const uint4* __restrict__ h, int64_t nchunks, float s,
                                             uint4* __restrict__ act_out, uint2* __restrict__ q_out,
-                                            int64_t cta, int64_t ncta, uint32_t& amax2, uint32_t& nsat) {
+                                            int64_t cta, int64_t ncta, uint32_t& amax2, uint32_t& nsat,
+                                            HCache* hc = nullptr) {
     const int64_t tid = cta * blockDim.x + threadIdx.x;
     const int64_t nthreads = ncta * blockDim.x;
     int64_t i = tid;
@@ -72,6 +94,7 @@ __device__ __forceinline__ void stream_body(const uint4* __restrict__ h, int64_t
         for (int u = 0; u < U; ++u) x[u] = ld_stream_v4(h + i + u * nthreads);
 #pragma unroll
         for (int u = 0; u < U; ++u) {
+            if constexpr (HQ) h_cache8(*hc, x[u], hc->hq + i + u * nthreads);
             uint4 a = act8<ACT>(x[u], amax2);
             if (act_out) st_stream_v4(act_out + i + u * nthreads, a);
             uint2 q = cast8<FMT>(a, s, nsat);
@@ -79,7 +102,9 @@ __device__ __forceinline__ void stream_body(const uint4* __restrict__ h, int64_t
         }
     }
     for (; i < nchunks; i += nthreads) {
-        uint4 a = act8<ACT>(ld_stream_v4(h + i), amax2);
+        const uint4 x = ld_stream_v4(h + i);
+        if constexpr (HQ) h_cache8(*hc, x, hc->hq + i);
+        uint4 a = act8<ACT>(x, amax2);
         if (act_out) st_stream_v4(act_out + i, a);
         uint2 q = cast8<FMT>(a, s, nsat);
         if (q_out) st_v2(q_out + i, q);
@@ -429,6 +454,10 @@ struct BatchEntry {
     uint8_t* q_t_out;
     float* amax_out;
     unsigned long long* sat_out;
+    uint8_t* hq_out;                // the pre-activation's E4M3 cache, or nullptr
+    const float* scale_h;
+    float* amax_h;
+    unsigned long long* sat_h;
     int64_t block0, nblocks;  // this entry's CTAs
     int64_t tiles_x;          // tile pass: tiles along K
     int act, fmt;
@@ -448,11 +477,11 @@ constexpr int kBatchCtasPerSm = 4;   // 64 registers per thread: no spills in ei
 // occupancy) set by the streaming pass.  Measured back to back on GB300 at
 // 8192 x 3072 (+ the 3072 x 768 weight): 21.8 us for both tensors in one
 // launch, against 19.5 + 12.0 us as two launches.
-template <int ACT, int FMT>
+template <int ACT, int FMT, bool HQ = false>
 __device__ __forceinline__ void tile_pt_body(const uint16_t* __restrict__ h, int64_t M, int64_t K, float s,
                                              uint16_t* __restrict__ act_out, uint8_t* __restrict__ q_out,
                                              uint8_t* __restrict__ q_t_out, int64_t bx, int64_t by, uint8_t* tq,
-                                             uint32_t& amax2, uint32_t& nsat) {
+                                             uint32_t& amax2, uint32_t& nsat, HCache* hc = nullptr) {
     const int tid = threadIdx.x;
     const int64_t row0 = by * kTile;
     const int64_t col0 = bx * kTile;
@@ -471,6 +500,9 @@ __device__ __forceinline__ void tile_pt_body(const uint16_t* __restrict__ h, int
             const int r = c >> 4;
             const int64_t row = row0 + r, col = col0 + (c & 15) * 8;
             const bool ok = row < M && col < K;
+            if constexpr (HQ) {
+                if (ok) h_cache8(*hc, a[it], reinterpret_cast<uint2*>(hc->hq) + (row * K + col) / 8);
+            }
             uint32_t m2 = 0;
             a[it] = act8<ACT>(a[it], m2);
             amax2 = __vmaxu2(amax2, m2);
@@ -490,19 +522,31 @@ __device__ __forceinline__ void tile_pt_body(const uint16_t* __restrict__ h, int
     }
 }
 
-template <int ACT, int FMT>
-__device__ __forceinline__ void batch_entry_body(const BatchEntry& e, int64_t cta, uint8_t* tq, uint32_t* s_blk,
-                                                 uint32_t& amax2, uint32_t& nsat) {
+template <int ACT, int FMT, bool HQ>
+__device__ __forceinline__ void batch_entry_body_t(const BatchEntry& e, int64_t cta, uint8_t* tq,
+                                                   uint32_t& amax2, uint32_t& nsat, HCache* hc) {
     if (e.q_t_out) {
-        tile_pt_body<ACT, FMT>(e.h, e.M, e.K, *e.scale, e.act_out, e.q_out, e.q_t_out, cta % e.tiles_x,
-                               cta / e.tiles_x, tq, amax2, nsat);
+        tile_pt_body<ACT, FMT, HQ>(e.h, e.M, e.K, *e.scale, e.act_out, e.q_out, e.q_t_out, cta % e.tiles_x,
+                                   cta / e.tiles_x, tq, amax2, nsat, hc);
     } else {
-        stream_body<ACT, FMT, kBatchU>(reinterpret_cast<const uint4*>(e.h), e.M * e.K / 8, *e.scale,
-                              reinterpret_cast<uint4*>(e.act_out), reinterpret_cast<uint2*>(e.q_out), cta,
-                              e.nblocks, amax2, nsat);
+        // with the cache a thread holds four loads in flight, not eight: the
+        // extra cast keeps the 64-register budget without spills
+        stream_body<ACT, FMT, HQ ? 4 : kBatchU, HQ>(reinterpret_cast<const uint4*>(e.h), e.M * e.K / 8, *e.scale,
+                                           reinterpret_cast<uint4*>(e.act_out), reinterpret_cast<uint2*>(e.q_out),
+                                           cta, e.nblocks, amax2, nsat, hc);
     }
 }
 
+template <int ACT, int FMT, bool HQ>
+__device__ __forceinline__ void batch_entry_body(const BatchEntry& e, int64_t cta, uint8_t* tq, uint32_t* s_blk,
+                                                 uint32_t& amax2, uint32_t& nsat, HCache* hc) {
+    if (HQ && e.hq_out) batch_entry_body_t<ACT, FMT, HQ>(e, cta, tq, amax2, nsat, hc);
+    else batch_entry_body_t<ACT, FMT, false>(e, cta, tq, amax2, nsat, hc);
+}
+
+// HQ: some entry writes the pre-activation's E4M3 cache (a kernel of its own,
+// so the plain batch keeps its registers).
+template <bool HQ>
 __global__ void __launch_bounds__(kThreads, kBatchCtasPerSm)
 quant_batch_kernel(const __grid_constant__ BatchParams p) {
     __shared__ __align__(16) uint8_t tq[kTile * kTqPitch];
@@ -512,30 +556,37 @@ quant_batch_kernel(const __grid_constant__ BatchParams p) {
     const BatchEntry& e = p.e[i];
     const int64_t cta = static_cast<int64_t>(blockIdx.x) - e.block0;
     uint32_t amax2 = 0, nsat = 0;
+    HCache hc;
+    hc.hq = reinterpret_cast<uint2*>(e.hq_out);
     pdl_wait();
+    hc.s = e.hq_out ? *e.scale_h : 1.0f;
     const int key = e.act * 2 + e.fmt;
     switch (key) {
         case FP8Q_ACT_IDENTITY * 2 + FP8Q_E4M3:
-            batch_entry_body<FP8Q_ACT_IDENTITY, FP8Q_E4M3>(e, cta, tq, s_blk, amax2, nsat);
+            batch_entry_body<FP8Q_ACT_IDENTITY, FP8Q_E4M3, HQ>(e, cta, tq, s_blk, amax2, nsat, &hc);
             break;
         case FP8Q_ACT_IDENTITY * 2 + FP8Q_E5M2:
-            batch_entry_body<FP8Q_ACT_IDENTITY, FP8Q_E5M2>(e, cta, tq, s_blk, amax2, nsat);
+            batch_entry_body<FP8Q_ACT_IDENTITY, FP8Q_E5M2, HQ>(e, cta, tq, s_blk, amax2, nsat, &hc);
             break;
         case FP8Q_ACT_RELU * 2 + FP8Q_E4M3:
-            batch_entry_body<FP8Q_ACT_RELU, FP8Q_E4M3>(e, cta, tq, s_blk, amax2, nsat);
+            batch_entry_body<FP8Q_ACT_RELU, FP8Q_E4M3, HQ>(e, cta, tq, s_blk, amax2, nsat, &hc);
             break;
         case FP8Q_ACT_RELU * 2 + FP8Q_E5M2:
-            batch_entry_body<FP8Q_ACT_RELU, FP8Q_E5M2>(e, cta, tq, s_blk, amax2, nsat);
+            batch_entry_body<FP8Q_ACT_RELU, FP8Q_E5M2, HQ>(e, cta, tq, s_blk, amax2, nsat, &hc);
             break;
         case FP8Q_ACT_RELU2 * 2 + FP8Q_E4M3:
-            batch_entry_body<FP8Q_ACT_RELU2, FP8Q_E4M3>(e, cta, tq, s_blk, amax2, nsat);
+            batch_entry_body<FP8Q_ACT_RELU2, FP8Q_E4M3, HQ>(e, cta, tq, s_blk, amax2, nsat, &hc);
             break;
         default:
-            batch_entry_body<FP8Q_ACT_RELU2, FP8Q_E5M2>(e, cta, tq, s_blk, amax2, nsat);
+            batch_entry_body<FP8Q_ACT_RELU2, FP8Q_E5M2, HQ>(e, cta, tq, s_blk, amax2, nsat, &hc);
             break;
     }
     pdl_launch_dependents();  // late: the next kernel's CTAs fill SMs as this grid drains
     block_reduce_publish(max16x2(amax2), nsat, e.amax_out, e.sat_out);
+    if (HQ && e.hq_out) {
+        __syncthreads();  // the reduction's shared words are reused
+        block_reduce_publish(max16x2(hc.amax2), hc.nsat, e.amax_h, e.sat_h);
+    }
 }
 
 // CTAs of the streaming pass over nchunks 16-byte chunks: each thread takes
@@ -747,6 +798,12 @@ extern "C" int fp8_quant_fused_batch(const fp8q_quant_args* args, int n, cudaStr
         const int st = check_quant_args(a.h, a.M, a.K, a.act, a.fmt, a.scale, a.act_out, a.q_out, a.q_t_out,
                                         a.amax_out, a.sat_count, nullptr, a.group_rows, a.flags);
         if (st != FP8Q_OK) return st;
+        if (a.hq_out) {  // the pre-activation's E4M3 cache
+            if (!a.scale_h) return FP8Q_ERR_NULL;
+            if (!aligned16(a.hq_out) || (reinterpret_cast<uintptr_t>(a.scale_h) & 3u) ||
+                (reinterpret_cast<uintptr_t>(a.amax_h) & 3u) || (reinterpret_cast<uintptr_t>(a.sat_h) & 7u))
+                return FP8Q_ERR_ALIGN;
+        }
         if (a.M == 0) continue;
         BatchEntry& e = p.e[p.n++];
         e.h = static_cast<const uint16_t*>(a.h);
@@ -758,6 +815,10 @@ extern "C" int fp8_quant_fused_batch(const fp8q_quant_args* args, int n, cudaStr
         e.q_t_out = static_cast<uint8_t*>(a.q_t_out);
         e.amax_out = a.amax_out;
         e.sat_out = a.sat_count;
+        e.hq_out = static_cast<uint8_t*>(a.hq_out);
+        e.scale_h = a.scale_h;
+        e.amax_h = a.amax_h;
+        e.sat_h = a.sat_h;
         e.act = a.act;
         e.fmt = a.fmt;
         e.tiles_x = (a.K + kTile - 1) / kTile;
@@ -773,10 +834,16 @@ extern "C" int fp8_quant_fused_batch(const fp8q_quant_args* args, int n, cudaStr
         if (a.amax_out && cudaMemsetAsync(a.amax_out, 0, sizeof(float), stream) != cudaSuccess) return FP8Q_ERR_CUDA;
         if (a.sat_count && cudaMemsetAsync(a.sat_count, 0, sizeof(unsigned long long), stream) != cudaSuccess)
             return FP8Q_ERR_CUDA;
+        if (a.hq_out && a.amax_h && cudaMemsetAsync(a.amax_h, 0, sizeof(float), stream) != cudaSuccess)
+            return FP8Q_ERR_CUDA;
+        if (a.hq_out && a.sat_h && cudaMemsetAsync(a.sat_h, 0, sizeof(unsigned long long), stream) != cudaSuccess)
+            return FP8Q_ERR_CUDA;
     }
     if (p.n == 0) return FP8Q_OK;
-    if (launch_pdl(quant_batch_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kThreads), 0, stream, p) !=
-        cudaSuccess) {
+    bool hq = false;
+    for (int i = 0; i < p.n; ++i) hq = hq || p.e[i].hq_out != nullptr;
+    if (launch_pdl(hq ? quant_batch_kernel<true> : quant_batch_kernel<false>, dim3(static_cast<unsigned>(blocks)),
+                   dim3(kThreads), 0, stream, p) != cudaSuccess) {
         (void)cudaGetLastError();
         return FP8Q_ERR_CUDA;
     }

@@ -123,9 +123,12 @@ class Fp8DownProj:
     def __init__(self, M: int, K: int, N: int, *, act: int = B.ACT_RELU2, margin: float = 2.0,
                  history_len: int = 1, group: bool = False, with_dgrad: bool = False,
                  keep_act: bool = True, chunks: int | None = None, fused: bool | None = None,
-                 with_backward: bool = False, device="cuda"):
+                 with_backward: bool = False, fp8_cache: bool = False, device="cuda"):
         self.M, self.K, self.N, self.act, self.group = M, K, N, act, group
         self.with_backward = with_backward
+        if fp8_cache and not with_backward:
+            raise ValueError("fp8_cache keeps the pre-activation for backward(): it needs with_backward")
+        self.fp8_cache = fp8_cache
         if with_backward and (group or (chunks or 1) != 1 or fused):
             raise ValueError("backward() runs after the per-tensor one-block step (not fused, not grouped)")
         with_dgrad = with_dgrad or with_backward
@@ -174,6 +177,12 @@ class Fp8DownProj:
             self.dy_q_t = torch.empty(N, M, dtype=torch.uint8, device=dev)
             self.dh = torch.empty(M, K, dtype=torch.bfloat16, device=dev)
             self.dw = torch.empty(K, N, dtype=torch.bfloat16, device=dev)
+        # fp8_cache: the pre-activation kept for backward in E4M3 under its own
+        # delayed scale (written by the forward's quantize in the same pass)
+        self.h_q = self.hs = None
+        if fp8_cache:
+            self.h_q = torch.empty(M, K, dtype=torch.uint8, device=dev)
+            self.hs = DelayedScale(B.E4M3, margin, history_len, dev)
         self.workspace = None
         if self.fused:
             # zero-filled once; the fused kernel leaves it zero
@@ -343,19 +352,24 @@ class Fp8DownProj:
         first CTA, beside its first tile), so the step is two launches on one
         stream."""
         sx, sw = self.x.scale, self.w.scale
-        fx = B.ACCUMULATE if self.x.clean else 0
+        hs = self.hs
+        fx = B.ACCUMULATE if self.x.clean and (hs is None or hs.clean) else 0
         fw = B.ACCUMULATE if self.w.clean else 0
+        cache = {} if hs is None else dict(hq_out=self.h_q, scale_h=hs.scale, amax_h=hs.amax, sat_h=hs.sat)
         B.fp8_quant_fused_batch([
             B.quant_args(W, B.ACT_IDENTITY, B.E4M3, sw, q_out=self.w_q, q_t_out=self.wt_q,
                          amax_out=self.w.amax, sat_count=self.w.sat, flags=fw),
             B.quant_args(H, self.act, B.E4M3, sx, act_out=self.act_bf16, q_out=self.x_q, q_t_out=self.x_q_t,
-                         amax_out=self.x.amax, sat_count=self.x.sat, flags=fx),
+                         amax_out=self.x.amax, sat_count=self.x.sat, flags=fx, **cache),
         ])
         self.x.clean = self.w.clean = False
         B.fp8_gemm_fwd(self.x_q, self.wt_q, sx, sw, self.y, amax_x=self.x.amax, hist_x=self.x.kernel_update_args(),
                        amax_w=self.w.amax, hist_w=self.w.kernel_update_args(), status=self.gemm_status)
         self.x.advance()
         self.w.advance()
+        if hs is not None:
+            hs.clean = False
+            hs.update()  # the cache's own delayed scale for the next step
         return self.y
 
     def capture(self, H: torch.Tensor, W: torch.Tensor, H_next: torch.Tensor | None = None) -> "StepGraph":
@@ -409,7 +423,7 @@ class Fp8DownProj:
         self.gemm(self.x_scale_used, self.w_scale_used)
         return redo
 
-    def backward(self, dY: torch.Tensor, H: torch.Tensor) -> tuple[torch.Tensor, torch.Tensor]:
+    def backward(self, dY: torch.Tensor, H: torch.Tensor | None = None) -> tuple[torch.Tensor, torch.Tensor]:
         """The down-projection's backward on the forward's FP8 operands ("FP8
         Training & Inference", FP8 Training Recipe: gradients in E5M2, weights
         and activations in E4M3), after step(H, W) and before the next step:
@@ -422,7 +436,11 @@ class Fp8DownProj:
         X_q^T is the transposed copy the forward's quantize cached, W_q the
         weight's own layout; both carry the scales they were cast with (the
         recompute's, if recompute_on_overflow() ran).  H is the forward's BF16
-        pre-activation.  Needs with_backward.  Returns views of (dH, dW)."""
+        pre-activation; with fp8_cache it is not needed: act'(H) is taken at the
+        E4M3 cache the forward wrote ("FP8 training: what it is and how it
+        works", Trade-offs and edge cases: cached activations in FP8),
+        dequantised with the scale it was cast with.  Needs with_backward.
+        Returns views of (dH, dW)."""
         if not self.with_backward:
             raise RuntimeError("backward() needs Fp8DownProj(..., with_backward=True)")
         sx = self.x_scale_used if self.x_scale_used is not None else self.x.last_scale
@@ -432,7 +450,13 @@ class Fp8DownProj:
         B.fp8_quant_fused_ex(dY, B.ACT_IDENTITY, B.E5M2, sdy, q_out=self.dy_q, q_t_out=self.dy_q_t,
                              amax_out=self.g.amax, sat_count=self.g.sat, flags=fl)
         self.g.clean = False
-        B.fp8_gemm_dgrad_act(self.dy_q, self.w_q, sdy, sw, H, self.dh, act=self.act, status=self.gemm_status)
+        if self.fp8_cache:
+            B.fp8_gemm_dgrad_act_q(self.dy_q, self.w_q, sdy, sw, self.h_q, self.hs.last_scale, self.dh, act=self.act,
+                                   status=self.gemm_status)
+        else:
+            if H is None:
+                raise ValueError("backward() needs the forward's pre-activation H (or fp8_cache=True)")
+            B.fp8_gemm_dgrad_act(self.dy_q, self.w_q, sdy, sw, H, self.dh, act=self.act, status=self.gemm_status)
         B.fp8_gemm_wgrad(self.x_q_t, self.dy_q_t, sx, sdy, self.dw, status=self.gemm_status)
         self.g.update()
         return self.dh, self.dw
@@ -460,6 +484,11 @@ class Fp8DownProj:
         self.quantize(H)
         self.x.update()
         self.w.update()
+        if self.hs is not None:  # the pre-activation cache's scale: an amax pass over H itself
+            self.hs.scales.fill_(1.0)
+            B.fp8_quant_fused(H, B.ACT_IDENTITY, B.E4M3, self.hs.scale, amax_out=self.hs.amax)
+            self.hs.clean = False
+            self.hs.update()
 
 
 class StepGraph:

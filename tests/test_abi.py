@@ -308,7 +308,7 @@ def test_noalloc_argument_checks(lib):
 def test_batch_quant_argument_checks(lib):
     from quantize_fp8_gemm_gb300 import binding as B
     lib.fp8_quant_fused_batch.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p]
-    assert ctypes.sizeof(B.QuantArgs) == 96
+    assert ctypes.sizeof(B.QuantArgs) == 128
     good = B.QuantArgs(A, 64, 256, 2, 0, A, A, A, None, A, A, None, 1, 0)
     arr = (B.QuantArgs * 2)(good, good)
     assert lib.fp8_quant_fused_batch(None, 1, None) == ERR_NULL

@@ -515,6 +515,32 @@ def test_act_grad_is_the_derivative_of_the_forward_activation(which):
     assert np.array_equal(O.act_grad(neg, which), [want] * 3)
 
 
+def test_act_grad_at_the_fp8_cache():
+    """act_grad_q dequantises the E4M3 cache and then is act_grad: on H values
+    that lie on the E4M3 grid divided by a power-of-two scale the cache is
+    exact and the two agree bit for bit; the scale divides (a code cast with
+    s_h = 4 is a quarter of its value); and against values off the grid the
+    cached derivative differs from the exact one by at most the E4M3
+    rounding of s_h h (half a code step: 2^-4 relative for normals)."""
+    codes = np.arange(256, dtype=np.uint8)
+    codes = codes[(codes & 0x7F) != 0x7F]                # no NaN codes
+    vals = O.fp8_decode(codes, O.E4M3)
+    for s_h in (1.0, 4.0, 0.125):
+        h = O.f32_to_bf16((vals / s_h).astype(np.float32))  # exact: E4M3 values have 4 significant bits
+        for which in (O.ACT_RELU2, O.ACT_RELU, O.ACT_IDENTITY):
+            assert np.array_equal(O.act_grad_q(codes, s_h, which), O.act_grad(h, which))
+    assert O.act_grad_q(np.array([0x38], np.uint8), 4.0, O.ACT_RELU2)[0] == 0.5   # 1.0 / 4, times 2
+    rng = np.random.default_rng(27)
+    hv = (rng.standard_normal((50, 100)) * 2.0).astype(np.float32)
+    hb = O.f32_to_bf16(hv)
+    s_h = O.delayed_scale(O.amax(hb, O.ACT_IDENTITY), 2.0, O.E4M3)
+    q = O.quant(hb, O.ACT_IDENTITY, O.E4M3, s_h)["q"]
+    exact, cached = O.act_grad(hb, O.ACT_RELU2), O.act_grad_q(q, s_h, O.ACT_RELU2)
+    big = np.abs(O.bf16_to_f32(hb).astype(np.float64)) * s_h >= 2.0 ** -6   # normal E4M3 range
+    assert np.all(np.abs(cached - exact)[big] <= exact[big] * 2.0 ** -4 + 1e-12)
+    assert np.array_equal(cached > 0, (O.fp8_decode(q, O.E4M3) > 0))
+
+
 def test_group_gemm_reductions():
     """Group mode: equal scales reduce to per-tensor; power-of-two scales that
     differ per row, per 128-slice of K and per 128-block of N reduce to numpy's

@@ -15,7 +15,7 @@ from quantize_fp8_gemm_gb300 import binding as B
 from quantize_fp8_gemm_gb300 import workloads as WL
 from quantize_fp8_gemm_gb300 import downproj as dp_mod
 from quantize_fp8_gemm_gb300.downproj import Fp8DownProj
-from tests.parity import assert_gemm_close, host_bits16, host_u8
+from tests.parity import assert_gemm_close, dev_f32, dev_u8, host_bits16, host_u8
 
 pytestmark = pytest.mark.gpu
 
@@ -418,6 +418,80 @@ def test_backward_after_a_step_against_the_oracle():
     ref, S = O.gemm_wgrad(rx["q"], rd["q"], s_x, s_dy, rows=krows)
     assert_gemm_close(dw, ref, S, rows=krows)
     assert int(dp.gemm_status.item()) == 0
+
+
+@pytest.mark.parametrize("act", [B.ACT_RELU2, B.ACT_RELU])
+def test_backward_from_the_fp8_cache_against_the_oracle(act):
+    """Fp8DownProj(fp8_cache=True): the forward's quantize also writes H in
+    E4M3 under its own delayed scale (bit for bit the oracle's identity
+    quantize of H with that scale; its amax is max |H|), the BF16 H is not
+    kept, and the backward takes act'(H) at the dequantised cache: dH within
+    the GEMM tolerance of the oracle's dgrad times act'(dec(h_q) / s_h); dW as
+    before.  Two steps, so the cache's scale comes from the history."""
+    w = WL.WORKLOADS["gpt2s"]
+    M, K, N = 2048, w.K, w.N
+    W_bits = WL.w_down(w)
+    Wd = WL.bf16_tensor(W_bits).cuda()
+    Hs = [WL.h_preact(w, t)[:M] for t in range(3)]
+    rng = np.random.default_rng(18)
+    dY0, dY1 = (WL.to_bf16_bits((rng.standard_normal((M, N)) * 1e-3).astype(np.float32)) for _ in range(2))
+    dp = Fp8DownProj(M, K, N, act=act, margin=w.margin, with_backward=True, fp8_cache=True)
+    dp.calibrate(WL.bf16_tensor(Hs[0]).cuda(), Wd)
+    dp.calibrate_backward(WL.bf16_tensor(dY0).cuda())
+    oh = OracleRecurrence(w.history_len, w.margin)
+    oh.push(O.amax(Hs[0], O.ACT_IDENTITY))
+    for t in (1, 2):
+        assert float(dp.hs.scale.item()) == oh.scale
+        dp.step(WL.bf16_tensor(Hs[t]).cuda(), Wd)
+        torch.cuda.synchronize()
+        rh = O.quant(Hs[t], O.ACT_IDENTITY, O.E4M3, oh.scale, want_act=False)
+        assert np.array_equal(host_u8(dp.h_q), rh["q"]), f"step {t}: E4M3 cache of H"
+        assert float(dp.hs.last_amax.item()) == O.amax(Hs[t], O.ACT_IDENTITY) == rh["amax"]
+        assert int(dp.hs.last_sat.item()) == rh["sat"]
+        s_h = oh.scale
+        oh.push(rh["amax"])
+    dh, dw = dp.backward(WL.bf16_tensor(dY1).cuda())
+    torch.cuda.synchronize()
+    s_x, s_w, s_dy = (float(t.item()) for t in (dp.x.last_scale, dp.w.last_scale, dp.g.last_scale))
+    assert float(dp.hs.last_scale.item()) == s_h
+    rx = O.quant(Hs[2], act, O.E4M3, s_x, want_act=False)
+    rw = O.quant(W_bits, O.ACT_IDENTITY, O.E4M3, s_w, want_act=False)
+    rd = O.quant(dY1, O.ACT_IDENTITY, O.E5M2, s_dy, want_act=False)
+    rows = WL.sample_rows(M, 48, seed=19)
+    ref, S = O.gemm_dgrad_act_q(rd["q"], rw["q"], s_dy, s_w, host_u8(dp.h_q), s_h, act, rows=rows)
+    assert_gemm_close(dh, ref, S, rows=rows)
+    krows = WL.sample_rows(K, 48, seed=20)
+    ref, S = O.gemm_wgrad(rx["q"], rd["q"], s_x, s_dy, rows=krows)
+    assert_gemm_close(dw, ref, S, rows=krows)
+    assert int(dp.gemm_status.item()) == 0 and int(dp.hs.status.item()) == 0
+
+
+@pytest.mark.parametrize("act", [B.ACT_RELU2, B.ACT_RELU, B.ACT_IDENTITY])
+@pytest.mark.parametrize("pair,bn", [(-1, 0), (0, 128), (0, 192), (1, 256), (1, 224)])
+def test_dgrad_act_from_the_fp8_cache_every_tile(act, pair, bn):
+    """fp8_gemm_dgrad_act_q on ragged shapes with every tile the dispatcher
+    offers, against the oracle over all rows; the cache holds codes of both
+    signs, zeros and subnormals."""
+    M, N, K = 300, 272, 400
+    rng = np.random.default_rng(bn + act)
+    dyq = O.fp8_encode((rng.standard_normal((M, N)) * 50).astype(np.float32), O.E5M2)
+    wq = O.fp8_encode(rng.standard_normal((K, N)).astype(np.float32), O.E4M3)
+    hq = rng.integers(0, 256, (M, K)).astype(np.uint8)
+    hq[(hq & 0x7F) == 0x7F] = 0x00  # no NaN codes
+    s_dy, s_w, s_h = 3.0, 5.0, 37.5
+    dh = torch.empty(M, K, dtype=torch.bfloat16, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    try:
+        if pair >= 0:
+            B.fp8q_gemm_set_tile(pair, bn)
+        B.fp8_gemm_dgrad_act_q(dev_u8(dyq), dev_u8(wq), dev_f32(s_dy), dev_f32(s_w), dev_u8(hq), dev_f32(s_h), dh,
+                               act=act, status=st)
+        torch.cuda.synchronize()
+    finally:
+        B.fp8q_gemm_set_tile(-1)
+    assert st.item() == 0
+    ref, S = O.gemm_dgrad_act_q(dyq, wq, s_dy, s_w, hq, s_h, act)
+    assert_gemm_close(dh, ref, S)
 
 
 @pytest.mark.parametrize("N", [2304, 768])
