@@ -873,10 +873,36 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
 #pragma unroll
                 for (int j = 0; j < GC; ++j) sum[j] = 0.0f;
                 const int64_t srow = row < M ? row : M - 1;
+                // up to 12 warps the two scales of a slice are loaded two slices
+                // ahead, so the promotion never waits on a load once its
+                // accumulator is ready (131072 x 6400 -> 1600 on the 192-wide
+                // tile: 1523 -> 1335 us); the 16-warp tile (a 96-register cap)
+                // spills the extra registers and keeps the loads in the slice
+                constexpr bool PREFETCH = C::EPI_WARPS <= 12;
+                const float* sa_p = scale_a + srow * kg;
+                const float* sb_p = scale_b + nb;
+                float sa0 = 1.0f, sb0 = 1.0f, sa1 = 1.0f, sb1 = 1.0f;
+                if constexpr (PREFETCH) {
+                    sa0 = __ldg(sa_p);
+                    sb0 = __ldg(sb_p);
+                    if (num_kb > 1) {
+                        sa1 = __ldg(sa_p + 1);
+                        sb1 = __ldg(sb_p + ng);
+                    }
+                }
                 for (int kb = 0; kb < num_kb; ++kb) {
-                    const float sa = __ldg(scale_a + srow * kg + kb);
-                    const float sb = __ldg(scale_b + kb * ng + nb);
-                    const float ginv = 1.0f / (sa * sb);
+                    float ginv;
+                    if constexpr (PREFETCH) {
+                        ginv = 1.0f / (sa0 * sb0);
+                        sa0 = sa1;
+                        sb0 = sb1;
+                        if (kb + 2 < num_kb) {
+                            sa1 = __ldg(sa_p + kb + 2);
+                            sb1 = __ldg(sb_p + (kb + 2) * ng);
+                        }
+                    } else {
+                        ginv = 1.0f / (__ldg(sa_p + kb) * __ldg(sb_p + kb * ng));
+                    }
                     ok = wait_phase(&tfull[acc], acc_phase, abort_flag, status);
                     ok = __all_sync(0xFFFFFFFFu, ok);
                     if (!ok) break;
@@ -1204,15 +1230,15 @@ Shape pick_shape(int64_t M, int64_t N, bool wide) {
 // Group-mode tile width (1-CTA tiles, four accumulators' worth of TMEM): 128
 // with 8 promotion warps, 192 with 12 or 256 with 16 (64 columns per warp, so
 // each warp stays inside one 128-column scale block).  Scored like pick_shape,
-// with per-tile times relative to the 128-wide tile from sweeps of the three
+// with per-wave times relative to the 128-wide tile from sweeps of the three
 // widths over the workloads' shapes on GB300 (8192 to 131072 rows, N 768 to
-// 1600).  A tile override (0, 128), (0, 192) or (0, 256) pins it.
+// 1600; 192 wide 1.19 - 1.25x, 256 wide 1.68 - 1.75x).  A tile override (0, 128), (0, 192) or (0, 256) pins it.
 int pick_group_bn(int64_t M, int64_t N) {
     const int ov = g_tile_override.load(std::memory_order_relaxed);
     if (ov >= 0 && (ov >> 16) == 0 && ((ov & 0xFFFF) == 256 || (ov & 0xFFFF) == 192 || (ov & 0xFFFF) == 128))
         return ov & 0xFFFF;
     struct Cand { int bn; double t; };
-    static constexpr Cand kCands[] = {{128, 1.000}, {192, 1.240}, {256, 1.650}};
+    static constexpr Cand kCands[] = {{128, 1.000}, {192, 1.210}, {256, 1.720}};
     const int64_t sms = sm_count();
     int best = 128;
     double best_cost = -1.0;
