@@ -755,6 +755,7 @@ def measure_extras(args, dp, H, Wt, flush, kern_ms, w, dev, fp8: dict, peaks: di
         "timing": "back-to-back launches over rotating input copies (> L2) in one CUDA graph, one event pair",
         "workload": w.name,
     }
+    out["interference"] = measure_interference(dp, H, w, dev, flush)
     cfg_steps = max(20, min(100, args.steps))
     out["configs"] = {}
     for name in ("gpt2s", "gpt2s_batch", "outlier"):
@@ -765,6 +766,61 @@ def measure_extras(args, dp, H, Wt, flush, kern_ms, w, dev, fp8: dict, peaks: di
     out["gpt2s_batch_delayed_scaling_per_step"] = drift_metrics(dev, 20)
     out["outlier_zero_flush"] = outlier_flush_rates(dev)
     out["other_rows"] = measure_other_rows(dev, max(16, min(64, args.steps)), fp8["tflops"])
+    return out
+
+
+def measure_interference(dp, H, w, dev, flush) -> dict:
+    """Why the one-launch step does not reach max(HBM, tensor) time: the FP8
+    GEMM of the workload run alone, beside a plain device write of the bytes
+    the quantize writes (the BF16 copy and the E4M3 codes, 3 B per element),
+    and beside the quantize kernel itself, each pair on two streams (the GEMM
+    launched first, its persistent CTAs resident on every SM, the other
+    kernel's CTAs filling the remaining slots).  Median device time of each,
+    L2 flushed before each sample."""
+    from quantize_fp8_gemm_gb300 import binding as B
+    M, K, N = w.M, w.K, w.N
+    xq = dp.x_q.clone()
+    y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+    sx, sw = dp.x.scale.clone(), dp.w.scale.clone()
+    wbuf = torch.empty(3 * M * K // 4, dtype=torch.int32, device=dev)
+    act = torch.empty(M, K, dtype=torch.bfloat16, device=dev)
+    q = torch.empty(M, K, dtype=torch.uint8, device=dev)
+    amax = torch.zeros(1, device=dev)
+    s1, s2 = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+
+    def gemm():
+        B.fp8_gemm_fwd(xq, dp.wt_q, sx, sw, y)
+
+    def write():
+        wbuf.zero_()
+
+    def quant():
+        B.fp8_quant_fused_ex(H[0], dp.act, B.E4M3, sx, act_out=act, q_out=q, amax_out=amax, flags=B.ACCUMULATE)
+
+    def pair(other):
+        def f():
+            main = torch.cuda.current_stream()
+            s1.wait_stream(main)
+            s2.wait_stream(main)
+            with torch.cuda.stream(s1):
+                gemm()
+            with torch.cuda.stream(s2):
+                other()
+            main.wait_stream(s1)
+            main.wait_stream(s2)
+        return f
+
+    out = {}
+    for name, fn in [("gemm", gemm), ("write 3 B/elem", write), ("quantize", quant),
+                     ("gemm beside the write", pair(write)), ("gemm beside the quantize", pair(quant))]:
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        out[name + " ms"] = float(np.median(timed_steps(lambda i: fn(), flush, 12)))
+    out["serial sum with the write ms"] = out["gemm ms"] + out["write 3 B/elem ms"]
+    out["serial sum with the quantize ms"] = out["gemm ms"] + out["quantize ms"]
+    del xq, y, wbuf, act, q
+    torch.cuda.empty_cache()
     return out
 
 
