@@ -63,6 +63,17 @@ void fp8q_gemm_test_hold_loads(int on);
 int fp8q_test_set_fused_grid(int ctas);
 
 /*
+ * fp8q_test_set_fused_layout -- pin the layout of the one-launch step's
+ * quantize warps: 1 = quantize-first (24 warps, 8 loads in flight each),
+ * 2 = GEMM-first (12 working warps, none on the MMA issuer's scheduler, 12
+ * loads in flight each; taken on 256- and 400-wide pair tiles only, else
+ * layout 1), 0 = chosen by N (GEMM-first for N above ~1430, where the step's
+ * GEMM outlasts its quantize).  The layouts give identical results.  Returns
+ * FP8Q_ERR_UNSUPPORTED unless 0 <= layout <= 2.
+ */
+int fp8q_test_set_fused_layout(int layout);
+
+/*
  * fp8q_test_noalloc_fill -- fill every byte of the static counter array of
  * fp8_downproj_fwd_noalloc on the current device with `byte` (stream-ordered
  * on `stream`), as a call that was cut short could leave it.  The next

@@ -76,6 +76,8 @@ def lib() -> ctypes.CDLL:
         L.fp8q_gemm_set_tile.restype = i32
         L.fp8q_test_set_fused_grid.argtypes = [i32]
         L.fp8q_test_set_fused_grid.restype = i32
+        L.fp8q_test_set_fused_layout.argtypes = [i32]
+        L.fp8q_test_set_fused_layout.restype = i32
         L.fp8q_test_noalloc_fill.argtypes = [i32, P]
         L.fp8q_test_noalloc_fill.restype = i32
         L.fp8q_mx_set_tile.argtypes = [i32]
@@ -479,6 +481,11 @@ def fp8q_mx_set_tile(bn: int) -> None:
 def fp8q_test_set_fused_grid(ctas: int) -> None:
     """Launch the one-launch step kernels with this many CTAs (0 = one per SM)."""
     _check("fp8q_test_set_fused_grid", lib().fp8q_test_set_fused_grid(int(ctas)))
+
+
+def fp8q_test_set_fused_layout(layout: int) -> None:
+    """Pin the one-launch step's quantize layout (1 quantize-first, 2 GEMM-first, 0 = by N)."""
+    _check("fp8q_test_set_fused_layout", lib().fp8q_test_set_fused_layout(int(layout)))
 
 
 def fp8q_test_noalloc_fill(byte: int, stream=None) -> None:

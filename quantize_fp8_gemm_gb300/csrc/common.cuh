@@ -393,4 +393,9 @@ __host__ __device__ constexpr uint32_t idesc_f8(uint32_t afmt, uint32_t bfmt, ui
     return (1u << 4) | (afmt << 7) | (bfmt << 10) | ((n >> 3) << 17) | ((m >> 4) << 24);
 }
 
+// The same descriptor with another N (bits 17-22 hold N / 8).
+__host__ __device__ constexpr uint32_t idesc_with_n(uint32_t idesc, uint32_t n) {
+    return (idesc & ~(0x3Fu << 17)) | ((n >> 3) << 17);
+}
+
 }  // namespace fp8q

@@ -65,12 +65,42 @@ constexpr int kThreadsGemm = 192;  // 6 warps
 constexpr int kEpiWarps = 4;
 constexpr int kWideEpiWarps = 8;  // two warps per TMEM lane quarter, each half the columns
 
-// Fused quantize (FUSED = true): extra warps per CTA turn the BF16
-// pre-activation into the GEMM's E4M3 A operand, a few rows at a time.
-constexpr int kQuantWarps = 24;
-constexpr int kQuantThreads = kQuantWarps * 32;
-constexpr int kUnitRows = 16;   // rows per quantize unit in the full rounds
-constexpr int kQuantBatch = 8;  // 16-byte loads in flight per quantize thread
+// Fused quantize (FUSED != 0): extra warps per CTA (warps 6, 7, ...) turn the
+// BF16 pre-activation into the GEMM's E4M3 A operand, a few rows at a time.
+// They share the SM's issue slots with the producer, the MMA issuer and the
+// epilogue, and the GEMM loses time wherever they run (at 131072 x 6400 ->
+// 1600 the step takes 0.81 ms with the quantize loop removed, 1.01 ms with
+// its arithmetic but no loads or stores, 1.22 ms whole).  Two layouts:
+//   FUSED == 1  the quantize is the longer part of the step (few output
+//               columns per byte of H): 24 warps, 8 loads in flight each;
+//   FUSED == 2  the GEMM is the longer part: 16 warps, of which the four on
+//               the MMA issuer's scheduler (warp id % 4 == 1) stay idle, and
+//               12 loads in flight each -- the same bytes in flight from 12
+//               warps, and none competing with the MMA issuer (1.19 -> 1.11 ms
+//               at 131072 x 6400 -> 1600 on 400-wide tiles; slower where the
+//               quantize is the longer part: 0.217 -> 0.235 ms at 65536 x
+//               3072 -> 768).
+template <int FUSED>
+struct QuantLayout {
+    static constexpr int WARPS = FUSED == 2 ? 16 : 24;  // warps the CTA launches for the quantize
+    static constexpr int SKIP = FUSED == 2 ? 1 : -1;    // the scheduler left to the GEMM (warp id % 4)
+    static constexpr int BATCH = FUSED == 2 ? 12 : 8;   // 16-byte loads in flight per thread
+    static constexpr int FIRST_SKIP = 6 + ((SKIP - 6) % 4 + 4) % 4;  // lowest idle warp id
+    static constexpr int active_warps() {
+        int n = 0;
+        for (int w = 6; w < 6 + WARPS; ++w) n += (SKIP < 0 || w % 4 != SKIP) ? 1 : 0;
+        return n;
+    }
+    static constexpr int ACTIVE = active_warps();  // warps that quantize
+    static constexpr int THREADS = ACTIVE * 32;
+    // the thread's index among the quantize threads that work, or -1
+    __device__ static int index(int warp, int lane) {
+        if (SKIP >= 0 && warp % 4 == SKIP) return -1;
+        const int idle_below = (SKIP >= 0 && warp > FIRST_SKIP) ? (warp - FIRST_SKIP + 3) / 4 : 0;
+        return (warp - 6 - idle_below) * 32 + lane;
+    }
+};
+constexpr int kUnitRows = 16;  // rows per quantize unit in the full rounds
 
 // Epilogue warps: 8 where the epilogue is exposed -- group mode (a promotion
 // per 128-long K slice; 12 and 16 on its 192- and 256-wide tiles, 64 columns
@@ -79,15 +109,16 @@ constexpr int kQuantBatch = 8;  // 16-byte loads in flight per quantize thread
 // else 4 (8 would take a stage of the operand ring: 87.6 -> 92.6 us at 65536
 // rows with 256-wide tiles) -- and the activation-quantize epilogue (EQ),
 // whose per-element work is several times a plain epilogue's.
-template <int BN, bool GROUP, bool FUSED, bool EQ = false>
+template <int BN, bool GROUP, int FUSED, bool EQ = false>
 constexpr int epi_warps() {
     // group mode on 192 / 256-wide tiles: three / four promotion warps per lane quarter, 64 columns each
-    return GROUP && BN == 256 ? 16 : GROUP && BN == 192 ? 12 : !FUSED && (GROUP || EQ || BN > 256) ? kWideEpiWarps : kEpiWarps;
+    return GROUP && BN == 256 ? 16 : GROUP && BN == 192 ? 12
+         : !FUSED && (GROUP || EQ || (BN > 256 && BN != 400)) ? kWideEpiWarps : kEpiWarps;
 }
 
-template <int BN, bool GROUP, bool FUSED, bool EQ = false>
+template <int BN, bool GROUP, int FUSED, bool EQ = false>
 constexpr int gemm_threads() {
-    return kThreadsGemm + (FUSED ? kQuantThreads : 0) + (epi_warps<BN, GROUP, FUSED, EQ>() - kEpiWarps) * 32;
+    return kThreadsGemm + (FUSED ? QuantLayout<FUSED>::WARPS * 32 : 0) + (epi_warps<BN, GROUP, FUSED, EQ>() - kEpiWarps) * 32;
 }
 
 // Operands of the fused quantize.  ready[b] counts the rows of 128-row block b
@@ -149,11 +180,20 @@ template <int BN, bool PAIR, int EPI = kEpiWarps, int ACC = (2 * BN <= 512 ? 2 :
           int STAGE_PER_WARP = 2 * kEpiChunkBytes, int RING_TOTAL = kRingTotal>
 struct Cfg {
     // A tile wider than 256 columns takes two MMAs per k-step (N <= 256 each)
-    // into one accumulator; B then arrives as one box per MMA.
+    // into one accumulator; B then arrives as one box per MMA.  The 400-wide
+    // pair tile (four tiles across N = 1600) splits unevenly: 192 + 208
+    // columns, so each MMA's N is a multiple of 16 and each CTA's share of
+    // its B rows (96, 104) a whole number of 8-row swizzle atoms.
     static constexpr int NSPLIT = BN > 256 ? 2 : 1;
-    static constexpr int MMA_N = BN / NSPLIT;
+    static constexpr int MMA_N = BN == 400 ? 192 : BN / NSPLIT;  // the first MMA's N
     static constexpr int B_ROWS = PAIR ? BN / 2 : BN;  // rows of B this CTA loads
-    static constexpr int B_BOX = B_ROWS / NSPLIT;      // rows of B per TMA box (one per MMA)
+    static constexpr int B_BOX = B_ROWS * MMA_N / BN;  // rows of B in the first TMA box
+    // MMA j: its N, first accumulator / output column, this CTA's B rows
+    // (one TMA box) and their offset in the stage's B area
+    static constexpr int split_n(int j) { return j == 0 ? MMA_N : BN - MMA_N; }
+    static constexpr int split_col(int j) { return j == 0 ? 0 : MMA_N; }
+    static constexpr int split_rows(int j) { return j == 0 ? B_BOX : B_ROWS - B_BOX; }
+    static constexpr int split_off(int j) { return j == 0 ? 0 : B_BOX * BK; }
     static constexpr int ACCS = ACC;                   // TMEM accumulators (512 columns)
     static constexpr int A_BYTES = BM * BK;
     static constexpr int B_BYTES = B_ROWS * BK;
@@ -170,9 +210,11 @@ struct Cfg {
     static constexpr int MMA_M = PAIR ? 2 * BM : BM;
     static constexpr int TILE_M = MMA_M;                              // output rows per tile
     static constexpr int EPI_ARRIVALS = EPI * (PAIR ? 2 : 1);         // per accumulator drain
-    static_assert(BN % 32 == 0 && BN >= 64 && BN <= 384, "BN: multiple of 32 in [64, 384]");
-    static_assert(MMA_N % 16 == 0 && MMA_N <= 256, "MMA N: multiple of 16, at most 256");
-    static_assert(B_BOX % 8 == 0 && (B_BOX * BK) % 1024 == 0, "B boxes: whole 8-row swizzle atoms");
+    static_assert((BN % 32 == 0 && BN >= 64 && BN <= 384) || (BN == 400 && PAIR),
+                  "BN: multiple of 32 in [64, 384], or the 400-wide pair tile");
+    static_assert(split_n(0) % 16 == 0 && split_n(0) <= 256 && split_n(NSPLIT - 1) % 16 == 0 &&
+                      split_n(NSPLIT - 1) <= 256, "MMA N: multiple of 16, at most 256");
+    static_assert(split_rows(0) % 8 == 0 && split_rows(NSPLIT - 1) % 8 == 0, "B boxes: whole 8-row swizzle atoms");
     static_assert(B_BYTES % 1024 == 0, "stage tiles stay 1024-byte aligned");
     static_assert(STAGES >= 2, "at least a double-buffered ring");
     static_assert(ACCS >= 1 && ACCS * BN <= 512, "accumulators fit TMEM's 512 columns");
@@ -192,10 +234,10 @@ struct Cfg {
 // DACT (the activation backward in the dgrad epilogue) adds a load buffer for
 // every 32-column chunk of H in the tile (BN / 16 KB) and one mbarrier: 5 KB +
 // BN / 16 KB per warp, keeping each warp's buffers 1024-byte aligned.
-template <int BN, bool GROUP, bool PAIR, bool FUSED, bool EQ = false, int DACT = 0>
+template <int BN, bool GROUP, bool PAIR, int FUSED, bool EQ = false, int DACT = 0>
 using KernelCfg = Cfg<BN, PAIR, epi_warps<BN, GROUP, FUSED, EQ>(), GROUP ? 512 / BN : (2 * BN <= 512 ? 2 : 1),
                       EQ ? 4 * kEpiChunkBytes : DACT ? (5 + BN / 16) * 1024 : GROUP && BN == 256 ? kEpiChunkBytes : 2 * kEpiChunkBytes,
-                      GROUP && BN == 256 ? kGroupRingTotal : kRingTotal>;
+                      (GROUP && BN == 256) || BN == 400 ? kGroupRingTotal : kRingTotal>;
 
 // Bounded wait until a GPU-scope counter reaches `need` (acquire).
 __device__ __forceinline__ bool wait_ready(const unsigned* counter, unsigned need, volatile int* abort_flag,
@@ -220,34 +262,73 @@ __device__ __forceinline__ uint4 act8_any(int act, uint4 x, uint32_t& amax2) {
     return act8<FP8Q_ACT_IDENTITY>(x, amax2);
 }
 
+// 16 accumulator columns of one row (this lane's) to D [M,N] BF16 with two
+// 16-byte stores.  c0 and N are multiples of 16, so the columns lie wholly
+// inside D or wholly past it, and the stores are aligned.
+__device__ __forceinline__ void epi_store_tail16(uint16_t* d, uint32_t taddr, float inv, int64_t row, int64_t c0,
+                                                 int64_t M, int64_t N) {
+    uint32_t r[16];
+    tmem_ld_x16_sync(taddr, r);
+    if (row >= M || c0 >= N) return;
+    uint32_t p[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) p[j] = cvt_bf16x2(__uint_as_float(r[2 * j]) * inv, __uint_as_float(r[2 * j + 1]) * inv);
+    uint4* dst = reinterpret_cast<uint4*>(d + row * N + c0);
+    dst[0] = make_uint4(p[0], p[1], p[2], p[3]);
+    dst[1] = make_uint4(p[4], p[5], p[6], p[7]);
+}
+
 // One unit of the fused quantize: rows [r0, r1) by all quantize threads of
 // the CTA, then one thread publishes the rows with a release add to the count
-// of each 128-row block they touch.
-__device__ __forceinline__ void fused_quantize_rows(const FusedArgs& fz, float s, int64_t r0, int64_t r1,
-                                                    int64_t K, uint32_t& amax2, uint32_t& nsat) {
-    const int qt = threadIdx.x - kThreadsGemm;
+// of each 128-row block they touch.  The quantize warps share their SM with
+// the GEMM's warps, whose issue slots they take, so the per-element work is
+// kept short: ReLU^2 as two packed BF16 instructions per pair, the scale as
+// one packed float32 multiply per pair, and the saturation count taken once
+// per batch of loads -- exactly, through sat_count8, only when the
+// batch's largest magnitude can saturate.
+template <int FUSED, int ACT>
+__device__ __forceinline__ void fused_rows_body(const FusedArgs& fz, float s, int64_t r0, int64_t r1, int64_t K,
+                                                int qt, uint32_t& amax2, uint32_t& nsat) {
+    using L = QuantLayout<FUSED>;
     const int64_t c_end = r1 * (K / 8);
-    for (int64_t c0 = r0 * (K / 8) + qt; c0 < c_end; c0 += int64_t(kQuantThreads) * kQuantBatch) {
-        uint4 x[kQuantBatch];
+    for (int64_t c0 = r0 * (K / 8) + qt; c0 < c_end; c0 += int64_t(L::THREADS) * L::BATCH) {
+        uint4 x[L::BATCH];
 #pragma unroll
-        for (int j = 0; j < kQuantBatch; ++j) {
-            const int64_t c = c0 + int64_t(j) * kQuantThreads;
+        for (int j = 0; j < L::BATCH; ++j) {
+            const int64_t c = c0 + int64_t(j) * L::THREADS;
             x[j] = c < c_end ? ld_stream_v4(fz.h + c) : make_uint4(0, 0, 0, 0);
         }
+        uint32_t bm2 = 0;  // this batch's magnitudes (act(0) = 0 for the padding)
 #pragma unroll
-        for (int j = 0; j < kQuantBatch; ++j) {
-            const int64_t c = c0 + int64_t(j) * kQuantThreads;
+        for (int j = 0; j < L::BATCH; ++j) x[j] = act8<ACT>(x[j], bm2);
+        if (may_saturate<FP8Q_E4M3>(bm2, s)) {
+#pragma unroll
+            for (int j = 0; j < L::BATCH; ++j)
+                if (c0 + int64_t(j) * L::THREADS < c_end) nsat += sat_count8<FP8Q_E4M3>(x[j], s);
+        }
+        amax2 = __vmaxu2(amax2, bm2);
+#pragma unroll
+        for (int j = 0; j < L::BATCH; ++j) {
+            const int64_t c = c0 + int64_t(j) * L::THREADS;
             if (c < c_end) {
-                const uint4 a = act8_any(fz.act, x[j], amax2);
-                if (fz.act_out) st_stream_v4(fz.act_out + c, a);
-                st_v2(fz.x_q + c, cast8<FP8Q_E4M3>(a, s, nsat));
+                if (fz.act_out) st_stream_v4(fz.act_out + c, x[j]);
+                st_v2(fz.x_q + c, cast8_codes<FP8Q_E4M3>(x[j], s));
             }
         }
     }
+}
+
+template <int FUSED>
+__device__ __forceinline__ void fused_quantize_rows(const FusedArgs& fz, float s, int64_t r0, int64_t r1,
+                                                    int64_t K, int qt, uint32_t& amax2, uint32_t& nsat) {
+    using L = QuantLayout<FUSED>;
+    if (fz.act == FP8Q_ACT_RELU2) fused_rows_body<FUSED, FP8Q_ACT_RELU2>(fz, s, r0, r1, K, qt, amax2, nsat);
+    else if (fz.act == FP8Q_ACT_RELU) fused_rows_body<FUSED, FP8Q_ACT_RELU>(fz, s, r0, r1, K, qt, amax2, nsat);
+    else fused_rows_body<FUSED, FP8Q_ACT_IDENTITY>(fz, s, r0, r1, K, qt, amax2, nsat);
     // the unit's E4M3 codes are written by every quantize thread: order them
     // before the counts, which the producer reads before its TMA loads
     fence_proxy_async_global();
-    named_barrier(1, kQuantThreads);
+    named_barrier(1, L::THREADS);
     if (qt == 0) {
         for (int64_t b = r0 / BM; b * BM < r1; ++b) {
             const int64_t lo = b * BM > r0 ? b * BM : r0;
@@ -335,17 +416,20 @@ __device__ __forceinline__ void fused_cast_w(const FusedArgs& fz, int64_t K, int
 // instead of one SM carrying a whole extra unit at the end.  One thread asks
 // for the next ticket before the CTA quantizes the current unit; the unit's
 // closing barrier publishes it to the other quantize threads.
+template <int FUSED>
 __device__ __forceinline__ void fused_quantize(const FusedArgs& fz, const float* scale, int64_t M, int64_t K) {
+    using L = QuantLayout<FUSED>;
     __shared__ unsigned s_ticket[2];
+    const int qt = L::index(threadIdx.x >> 5, threadIdx.x & 31);
+    if (qt < 0) return;  // a warp the layout leaves idle
     const float s = __ldg(scale);
-    const int qt = threadIdx.x - kThreadsGemm;
     uint32_t amax2 = 0, nsat = 0;
     const int64_t G = gridDim.x;
     const int64_t full = M / kUnitRows > G ? M / kUnitRows - G : 0;
     const int64_t share = (M - full * kUnitRows + G - 1) / G;
     const int64_t nunits = full + G;
     if (qt == 0) s_ticket[0] = atomicAdd(fz.q_next, 1u);
-    named_barrier(1, kQuantThreads);
+    named_barrier(1, L::THREADS);
     int par = 0;
     int64_t t = s_ticket[0];
     while (t < nunits) {
@@ -360,18 +444,18 @@ __device__ __forceinline__ void fused_quantize(const FusedArgs& fz, const float*
         }
         // fused_quantize_rows ends with a barrier of all quantize threads, after
         // which the next ticket is visible to all of them
-        if (r0 < r1) fused_quantize_rows(fz, s, r0, r1, K, amax2, nsat);
-        else named_barrier(1, kQuantThreads);
+        if (r0 < r1) fused_quantize_rows<FUSED>(fz, s, r0, r1, K, qt, amax2, nsat);
+        else named_barrier(1, L::THREADS);
         par ^= 1;
         t = s_ticket[par];
     }
-    __shared__ uint32_t s_amax[kQuantWarps], s_sat[kQuantWarps];
+    __shared__ uint32_t s_amax[L::ACTIVE], s_sat[L::ACTIVE];
     uint32_t m = __reduce_max_sync(0xFFFFFFFFu, max16x2(amax2));
     uint32_t c = __reduce_add_sync(0xFFFFFFFFu, nsat);
     if ((qt & 31) == 0) { s_amax[qt >> 5] = m; s_sat[qt >> 5] = c; }
-    named_barrier(1, kQuantThreads);
+    named_barrier(1, L::THREADS);
     if (qt == 0) {
-        for (int w = 1; w < kQuantWarps; ++w) { m = max(m, s_amax[w]); c += s_sat[w]; }
+        for (int w = 1; w < L::ACTIVE; ++w) { m = max(m, s_amax[w]); c += s_sat[w]; }
         if (fz.amax_out && m) atomicMax(reinterpret_cast<unsigned int*>(fz.amax_out), m << 16);
         if (fz.sat_out && c) atomicAdd(fz.sat_out, static_cast<unsigned long long>(c));
     }
@@ -565,14 +649,14 @@ __device__ __forceinline__ bool epi_dact_tile(const CUtensorMap* tmD, int act, u
 // FUSED = true : the fused quantize + GEMM (per-tensor scales): the extra
 //                quantize warps produce A = X_q from H while the GEMM consumes
 //                finished 128-row blocks.
-template <int BN, bool GROUP, bool PAIR, bool FUSED, bool EQ, int DACT>
+template <int BN, bool GROUP, bool PAIR, int FUSED, bool EQ, int DACT>
 __global__ void __launch_bounds__(gemm_threads<BN, GROUP, FUSED, EQ>(), 1)
 fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const __grid_constant__ CUtensorMap tmD,
+                const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmD,
                 const float* __restrict__ scale_a, const float* __restrict__ scale_b,
                 int64_t M, int64_t N, int64_t K, uint32_t idesc, int* __restrict__ status,
                 int hold_loads, const FusedArgs fz, const __grid_constant__ CUtensorMap tmE1,
-                const __grid_constant__ CUtensorMap tmE2, const EpiQuantArgs eq) {
+                const __grid_constant__ CUtensorMap tmE2, const EpiQuantArgs eq, uint16_t* __restrict__ d_raw) {
     using C = KernelCfg<BN, GROUP, PAIR, FUSED, EQ, DACT>;
     static_assert(!DACT || (!GROUP && !FUSED && !EQ), "the activation backward runs in the per-tensor dgrad epilogue");
     static_assert(!EQ || (!GROUP && !FUSED && BN % 64 == 0 && BN <= 256),
@@ -617,6 +701,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
     if (warp == 0 && lane == 0) {
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
+        if constexpr (C::MMA_N * C::NSPLIT != BN) tma_prefetch_desc(&tmB2);
         tma_prefetch_desc(&tmD);
         if constexpr (EQ) {
             tma_prefetch_desc(&tmE1);
@@ -659,7 +744,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
             // hold_loads (test hook): issue nothing, so the MMA issuer's first wait runs out
             for (int64_t tile = first_tile; tile < num_tiles && ok && !hold_loads; tile += tile_stride) {
                 const int32_t m0 = static_cast<int32_t>((tile / num_n) * C::TILE_M + rank * BM);
-                const int32_t n0 = static_cast<int32_t>((tile % num_n) * BN + rank * C::B_BOX);
+                const int32_t n0 = static_cast<int32_t>((tile % num_n) * BN);
                 if constexpr (FUSED) {
                     // this tile's A rows exist once every unit of their block is quantized
                     if (m0 < M) {
@@ -680,16 +765,17 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                         tma_load_2d_pair(smem_u32(sa), &tmA, fb, kb * BK, m0);
 #pragma unroll
                         for (int j = 0; j < C::NSPLIT; ++j)
-                            tma_load_2d_pair(smem_u32(sa + C::A_BYTES + j * C::B_BOX * BK), &tmB, fb, kb * BK,
-                                             n0 + j * C::MMA_N);
+                            tma_load_2d_pair(smem_u32(sa + C::A_BYTES + C::split_off(j)),
+                                             C::MMA_N * C::NSPLIT != BN && j ? &tmB2 : &tmB, fb, kb * BK,
+                                             n0 + C::split_col(j) + static_cast<int32_t>(rank) * C::split_rows(j));
                     } else {
                         const uint32_t fb = smem_u32(&full[stage]);
                         mbar_arrive_expect_tx(fb, C::TX_BYTES);
                         tma_load_2d(smem_u32(sa), &tmA, fb, kb * BK, m0);
 #pragma unroll
                         for (int j = 0; j < C::NSPLIT; ++j)
-                            tma_load_2d(smem_u32(sa + C::A_BYTES + j * C::B_BOX * BK), &tmB, fb, kb * BK,
-                                        n0 + j * C::MMA_N);
+                            tma_load_2d(smem_u32(sa + C::A_BYTES + C::split_off(j)), &tmB, fb, kb * BK,
+                                        n0 + C::split_col(j));
                     }
                     ++issued;
                     if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
@@ -737,10 +823,11 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                         const uint64_t ad = smem_desc_k_sw128(a_addr + k * UMMA_K);
 #pragma unroll
                         for (int j = 0; j < C::NSPLIT; ++j) {
-                            const uint64_t bd = smem_desc_k_sw128(b_addr + j * C::B_BOX * BK + k * UMMA_K);
-                            const uint32_t dj = d_tmem + static_cast<uint32_t>(j * C::MMA_N);
-                            if constexpr (PAIR) mma_f8f6f4_pair(dj, ad, bd, idesc, accumulate);
-                            else mma_f8f6f4(dj, ad, bd, idesc, accumulate);
+                            const uint64_t bd = smem_desc_k_sw128(b_addr + C::split_off(j) + k * UMMA_K);
+                            const uint32_t dj = d_tmem + static_cast<uint32_t>(C::split_col(j));
+                            const uint32_t idj = j == 0 ? idesc : idesc_with_n(idesc, C::split_n(j));
+                            if constexpr (PAIR) mma_f8f6f4_pair(dj, ad, bd, idj, accumulate);
+                            else mma_f8f6f4(dj, ad, bd, idj, accumulate);
                         }
                     }
                     // the stage is free (in both CTAs of a pair) once these MMAs finish
@@ -767,7 +854,7 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
         }
     } else if (FUSED && warp >= 2 + kEpiWarps) {
         // ---------------------------------------------------- fused quantize
-        if constexpr (FUSED) fused_quantize(fz, scale_a, M, K);
+        if constexpr (FUSED) fused_quantize<FUSED>(fz, scale_a, M, K);
     } else {
         // ---------------------------------------------------------- epilogue
         if constexpr (FUSED) {
@@ -844,6 +931,14 @@ fp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__
                     for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]) * inv;
                     epi_store_chunk(&tmD, warp_stage, nchunk, lane, v, static_cast<int32_t>(n_blk * BN + c * 32),
                                     static_cast<int32_t>(row0), M, N);
+                }
+                if constexpr (BN % 32 == 16) {
+                    // the last 16 columns (the 400-wide tile): no 32-column box fits
+                    // them without covering the next tile's columns, so each lane
+                    // stores its row's 32 bytes directly
+                    if ((warp - 2) / 4 == (BN / 32) % (C::EPI_WARPS / 4))
+                        epi_store_tail16(d_raw, tmem_base + lane_base + static_cast<uint32_t>(acc * BN + BN - 16), inv,
+                                         row, n_blk * BN + BN - 16, M, N);
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -1062,7 +1157,7 @@ struct LaunchInfo {
     int max_clusters = 0;  // co-resident 2-CTA clusters (PAIR only)
 };
 
-template <int BN, bool GROUP, bool PAIR, bool FUSED, bool EQ = false, int DACT = 0>
+template <int BN, bool GROUP, bool PAIR, int FUSED, bool EQ = false, int DACT = 0>
 const LaunchInfo& launch_info() {
     using C = KernelCfg<BN, GROUP, PAIR, FUSED, EQ, DACT>;
     static LaunchInfo info;
@@ -1100,7 +1195,7 @@ struct EpiQuantHost {
     EpiQuantArgs args;
 };
 
-template <int BN, bool GROUP, bool PAIR, bool FUSED, bool EQ = false, int DACT = 0>
+template <int BN, bool GROUP, bool PAIR, int FUSED, bool EQ = false, int DACT = 0>
 int launch_gemm(const void* a, const void* b, const float* sa, const float* sb, void* d, int64_t M,
                 int64_t N, int64_t K, uint32_t afmt, uint32_t bfmt, int* status, cudaStream_t stream,
                 const FusedArgs& fz, const EpiQuantHost* eqh = nullptr, const void* h_in = nullptr,
@@ -1108,8 +1203,11 @@ int launch_gemm(const void* a, const void* b, const float* sa, const float* sb, 
     using C = KernelCfg<BN, GROUP, PAIR, FUSED, EQ, DACT>;
     const LaunchInfo& info = launch_info<BN, GROUP, PAIR, FUSED, EQ, DACT>();
     if (info.attr_err != cudaSuccess) return FP8Q_ERR_CUDA;
-    alignas(64) CUtensorMap mapA, mapB, mapD, mapE1, mapE2;
+    alignas(64) CUtensorMap mapA, mapB, mapB2, mapD, mapE1, mapE2;
     if (!make_kmajor_map(&mapA, a, M, K, BM) || !make_kmajor_map(&mapB, b, N, K, C::B_BOX)) return FP8Q_ERR_CUDA;
+    mapB2 = mapB;  // the second MMA's B box, where it differs from the first's
+    if constexpr (C::MMA_N * C::NSPLIT != BN)
+        if (!make_kmajor_map(&mapB2, b, N, K, C::split_rows(1))) return FP8Q_ERR_CUDA;
     EpiQuantArgs eq = {};
     if constexpr (EQ) {
         // every map handed to the kernel is a valid one: an output not asked
@@ -1163,8 +1261,8 @@ int launch_gemm(const void* a, const void* b, const float* sa, const float* sb, 
         cfg.stream = stream;
         cfg.attrs = attr;
         cfg.numAttrs = 2;
-        if (cudaLaunchKernelEx(&cfg, kern, mapA, mapB, mapD, sa, sb, M, N, K, idesc, status,
-                               g_hold_loads.load(), f, mapE1, mapE2, eq) != cudaSuccess) {
+        if (cudaLaunchKernelEx(&cfg, kern, mapA, mapB, mapB2, mapD, sa, sb, M, N, K, idesc, status,
+                               g_hold_loads.load(), f, mapE1, mapE2, eq, static_cast<uint16_t*>(d)) != cudaSuccess) {
             (void)cudaGetLastError();
             return FP8Q_ERR_CUDA;
         }
@@ -1174,8 +1272,9 @@ int launch_gemm(const void* a, const void* b, const float* sa, const float* sb, 
         const int fg = g_fused_grid.load();
         const int grid = static_cast<int>(FUSED ? (fg > 0 ? fg : sm_count()) : std::min<int64_t>(tiles, sm_count()));
         const FusedArgs& f = fz;
-        if (launch_pdl(kern, dim3(grid), dim3(gemm_threads<BN, GROUP, FUSED, EQ>()), C::SMEM_BYTES, stream, mapA, mapB, mapD, sa,
-                       sb, M, N, K, idesc, status, g_hold_loads.load(), f, mapE1, mapE2, eq) != cudaSuccess) {
+        if (launch_pdl(kern, dim3(grid), dim3(gemm_threads<BN, GROUP, FUSED, EQ>()), C::SMEM_BYTES, stream, mapA, mapB,
+                       mapB2, mapD, sa, sb, M, N, K, idesc, status, g_hold_loads.load(), f, mapE1, mapE2, eq,
+                       static_cast<uint16_t*>(d)) != cudaSuccess) {
             (void)cudaGetLastError();
             return FP8Q_ERR_CUDA;
         }
@@ -1204,14 +1303,18 @@ Shape pick_shape(int64_t M, int64_t N, bool wide) {
         const bool pair = (ov >> 16) != 0;
         const int bn = ov & 0xFFFF;
         if (!pair || M > BM) return Shape{pair, bn};
-        return Shape{false, bn == 224 || bn == 384 ? 256 : bn};
+        return Shape{false, bn == 224 || bn == 384 || bn == 400 ? 256 : bn};
     }
     struct Cand { bool pair; int bn; double t; };
     // {true, 384}: one accumulator, so its epilogue is not hidden; 1.70 measured
-    // at 8192 x 3072 -> 768, where its 64 tiles fit one wave of 76 pairs
+    // at 8192 x 3072 -> 768, where its 64 tiles fit one wave of 76 pairs.
+    // {true, 400}: one accumulator too; 1.74 measured at 131072 x 6400 -> 1600,
+    // where four of its tiles span N exactly (the 256-wide tile computes 1792
+    // columns there and reads each A row block seven times instead of four)
     static constexpr Cand kCands[] = {
         {true, 256, 1.000}, {true, 224, 0.946}, {true, 192, 0.909}, {true, 160, 0.837}, {true, 128, 0.858},
         {false, 192, 0.897}, {false, 160, 0.834}, {false, 128, 0.843}, {false, 256, 1.102}, {true, 384, 1.700},
+        {true, 400, 1.740},
     };
     const int64_t sms = sm_count();
     Shape best{false, 128};
@@ -1250,7 +1353,7 @@ int pick_group_bn(int64_t M, int64_t N) {
     return best;
 }
 
-template <bool FUSED>
+template <int FUSED>
 int gemm_dispatch_t(const void* a, const void* b, const float* sa, const float* sb, int group, void* d,
                     int64_t M, int64_t N, int64_t K, uint32_t afmt, uint32_t bfmt, int* status,
                     cudaStream_t stream, const FusedArgs& fz) {
@@ -1268,8 +1371,15 @@ int gemm_dispatch_t(const void* a, const void* b, const float* sa, const float* 
     if (FUSED && s.bn == 384) s.bn = 256;  // the one-launch step keeps two accumulators
 #define FP8Q_LAUNCH(BNV, PR) \
     return launch_gemm<BNV, false, PR, FUSED>(a, b, sa, sb, d, M, N, K, afmt, bfmt, status, stream, fz)
+    if constexpr (FUSED == 2) {
+        // the GEMM-first layout is built for the pair tiles of the wide steps
+        if (s.pair && s.bn == 400) FP8Q_LAUNCH(400, true);
+        if (s.pair && s.bn == 256) FP8Q_LAUNCH(256, true);
+        return gemm_dispatch_t<1>(a, b, sa, sb, group, d, M, N, K, afmt, bfmt, status, stream, fz);
+    } else {
     if (s.pair) {
         switch (s.bn) {
+            case 400: FP8Q_LAUNCH(400, true);
             case 384:
                 if constexpr (!FUSED) FP8Q_LAUNCH(384, true);
                 [[fallthrough]];
@@ -1286,13 +1396,31 @@ int gemm_dispatch_t(const void* a, const void* b, const float* sa, const float* 
         case 160: FP8Q_LAUNCH(160, false);
         default: FP8Q_LAUNCH(128, false);
     }
+    }
 #undef FP8Q_LAUNCH
+}
+
+// The one-launch step's quantize layout (QuantLayout): GEMM-first where the
+// GEMM is the longer part of the step.  Its 2 M N K FLOPs against the
+// quantize's 5 M K bytes, at the rates the two kernels reach alone on GB300
+// (about 3.7 PFLOP/s and 6.45 TB/s), make the GEMM longer once
+// 2 N / 3.7e15 > 5 / 6.45e12, i.e. N above ~1430 (GPT-2-XL's 1600; GPT-2's
+// 768 is quantize-first).  fp8q_test_set_fused_layout pins either one.
+std::atomic<int> g_fused_layout{0};
+
+int fused_dispatch(const void* x_q, const void* wt_q, const float* sx, const float* sw, void* y, int64_t M,
+                   int64_t N, int64_t K, int* status, cudaStream_t stream, const FusedArgs& fz) {
+    const int ov = g_fused_layout.load(std::memory_order_relaxed);
+    const bool gemm_first = ov ? ov == 2 : 2.0 * static_cast<double>(N) * 6.45e12 > 5.0 * 3.7e15;
+    if (gemm_first)
+        return gemm_dispatch_t<2>(x_q, wt_q, sx, sw, 0, y, M, N, K, FP8Q_E4M3, FP8Q_E4M3, status, stream, fz);
+    return gemm_dispatch_t<1>(x_q, wt_q, sx, sw, 0, y, M, N, K, FP8Q_E4M3, FP8Q_E4M3, status, stream, fz);
 }
 
 int gemm_dispatch(const void* a, const void* b, const float* sa, const float* sb, int group, void* d,
                   int64_t M, int64_t N, int64_t K, uint32_t afmt, uint32_t bfmt, int* status,
                   cudaStream_t stream) {
-    return gemm_dispatch_t<false>(a, b, sa, sb, group, d, M, N, K, afmt, bfmt, status, stream, FusedArgs{});
+    return gemm_dispatch_t<0>(a, b, sa, sb, group, d, M, N, K, afmt, bfmt, status, stream, FusedArgs{});
 }
 
 int check_gemm_args(const void* a, const void* b, const float* sa, const float* sb, const void* d,
@@ -1407,6 +1535,12 @@ using namespace fp8q;
 
 extern "C" void fp8q_gemm_test_hold_loads(int on) { g_hold_loads.store(on != 0 ? 1 : 0); }
 
+extern "C" int fp8q_test_set_fused_layout(int layout) {
+    if (layout < 0 || layout > 2) return FP8Q_ERR_UNSUPPORTED;
+    g_fused_layout.store(layout);
+    return FP8Q_OK;
+}
+
 extern "C" int fp8q_test_set_fused_grid(int ctas) {
     if (ctas < 0 || ctas > 65535) return FP8Q_ERR_SHAPE;
     g_fused_grid.store(ctas);
@@ -1419,7 +1553,7 @@ extern "C" int fp8q_gemm_set_tile(int pair, int bn) {
         return FP8Q_OK;
     }
     const bool ok1 = pair == 0 && (bn == 128 || bn == 160 || bn == 192 || bn == 256);
-    const bool ok2 = pair == 1 && (bn == 128 || bn == 160 || bn == 192 || bn == 224 || bn == 256 || bn == 384);
+    const bool ok2 = pair == 1 && (bn == 128 || bn == 160 || bn == 192 || bn == 224 || bn == 256 || bn == 384 || bn == 400);
     if (!ok1 && !ok2) return FP8Q_ERR_UNSUPPORTED;
     g_tile_override.store((pair << 16) | bn);
     return FP8Q_OK;
@@ -1459,7 +1593,7 @@ extern "C" int fp8_gemm_fwd_update(const void* x_q, const void* wt_q, const floa
     if (M == 0) return (hist_x || hist_w) ? FP8Q_ERR_SHAPE : FP8Q_OK;  // the updates ride on the launch
     fz.amax_out = amax_x;
     fz.amax_w = amax_w;
-    return gemm_dispatch_t<false>(x_q, wt_q, scale_x, scale_w, 0, y, M, N, K, FP8Q_E4M3, FP8Q_E4M3, status,
+    return gemm_dispatch_t<0>(x_q, wt_q, scale_x, scale_w, 0, y, M, N, K, FP8Q_E4M3, FP8Q_E4M3, status,
                                   stream, fz);
 }
 
@@ -1636,8 +1770,7 @@ extern "C" int fp8_downproj_fwd_ex(const void* h, const void* w, void* wt_q, int
     }
     fz.hx = hx;
     fz.hw = hw;
-    return gemm_dispatch_t<true>(x_q, wt_q, scale_x, scale_w, 0, y, M, N, K, FP8Q_E4M3, FP8Q_E4M3, status, stream,
-                                 fz);
+    return fused_dispatch(x_q, wt_q, scale_x, scale_w, y, M, N, K, status, stream, fz);
 }
 
 // ---------------------------------------------------------------------------
@@ -1693,8 +1826,7 @@ extern "C" int fp8_downproj_fwd_noalloc(const void* h, const void* wt_q, int64_t
     // ran to the end, but not after one that was cut short): start from zero
     if (cudaMemsetAsync(ready, 0, fp8_downproj_workspace_bytes(M), stream) != cudaSuccess) return FP8Q_ERR_CUDA;
     const FusedArgs fz = fused_args(h, act, act_out, x_q, amax_out, sat_count, ready, M);
-    return gemm_dispatch_t<true>(x_q, wt_q, scale_x, scale_w, 0, y, M, N, K, FP8Q_E4M3, FP8Q_E4M3, status, stream,
-                                 fz);
+    return fused_dispatch(x_q, wt_q, scale_x, scale_w, y, M, N, K, status, stream, fz);
 }
 
 extern "C" int fp8q_test_noalloc_fill(int byte, cudaStream_t stream) {

@@ -289,6 +289,10 @@ def test_testing_hooks_arguments(lib):
     assert lib.fp8q_test_set_fused_grid(70000) == ERR_SHAPE
     assert lib.fp8q_test_set_fused_grid(5) == OK
     assert lib.fp8q_test_set_fused_grid(0) == OK
+    assert lib.fp8q_test_set_fused_layout(3) == ERR_UNSUPPORTED
+    assert lib.fp8q_test_set_fused_layout(-1) == ERR_UNSUPPORTED
+    assert lib.fp8q_test_set_fused_layout(2) == OK
+    assert lib.fp8q_test_set_fused_layout(0) == OK
     import torch
     if not torch.cuda.is_available():
         # no device: the static array has no address to look up

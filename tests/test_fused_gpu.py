@@ -14,7 +14,8 @@ from tests.parity import assert_gemm_close, dev_bf16, dev_f32, host_u8
 
 pytestmark = pytest.mark.gpu
 
-TILES = [(-1, 0), (0, 128), (0, 160), (0, 192), (0, 256), (1, 128), (1, 160), (1, 192), (1, 224), (1, 256)]
+TILES = [(-1, 0), (0, 128), (0, 160), (0, 192), (0, 256), (1, 128), (1, 160), (1, 192), (1, 224), (1, 256),
+         (1, 400)]
 
 
 def _inputs(M, N, K, seed):
@@ -52,13 +53,19 @@ def _run_both(h_bits, w_bits, act, sx, sw):
     return out
 
 
+@pytest.mark.parametrize("layout", [1, 2])
 @pytest.mark.parametrize("pair,bn", TILES)
-def test_fused_equals_separate_calls(pair, bn):
+def test_fused_equals_separate_calls(pair, bn, layout):
+    """The one-launch step against the separate quantize and GEMM, bit for bit,
+    on every tile and both layouts of its quantize warps (the GEMM-first layout
+    exists on the 256- and 400-wide pair tiles; elsewhere the request falls back
+    to the quantize-first one)."""
     try:
+        B.fp8q_test_set_fused_layout(layout)
         if pair >= 0:
             B.fp8q_gemm_set_tile(pair, bn)
         for (M, N, K) in [(1000, 1600, 640), (300, 272, 400), (129, 144, 1600), (2048, 768, 3072), (16, 64, 96),
-                          (1001, 160, 48), (130, 32, 16)]:
+                          (1001, 160, 48), (130, 32, 16), (260, 1584, 272)]:
             h, w = _inputs(M, N, K, seed=M + N + K + bn)
             r = _run_both(h, w, B.ACT_RELU2, 20.0, 300.0)
             a1, q1, y1, am1, s1, _ = r["separate"]
@@ -68,6 +75,7 @@ def test_fused_equals_separate_calls(pair, bn):
             assert torch.equal(y1.view(torch.int16), y2.view(torch.int16)), (M, N, K)
             assert (am1, s1) == (am2, s2)
     finally:
+        B.fp8q_test_set_fused_layout(0)
         B.fp8q_gemm_set_tile(-1)
 
 
@@ -200,8 +208,9 @@ def test_fused_step_runs_history_updates():
         assert int(ws.sum().item()) == 0
 
 
+@pytest.mark.parametrize("layout", [1, 2])
 @pytest.mark.parametrize("ctas", [2, 37, 64, 400])
-def test_fused_any_grid_gives_the_same_result(ctas):
+def test_fused_any_grid_gives_the_same_result(ctas, layout):
     """The one-launch step's CTAs take their quantize and weight-cast work by
     ticket, so no CTA waits on work held by a CTA that is not running.  A grid
     smaller than the SM count (2, 37, 64 CTAs) and one larger than the GPU
@@ -214,6 +223,7 @@ def test_fused_any_grid_gives_the_same_result(ctas):
     sx, sw = dev_f32(20.0), dev_f32(300.0)
     outs = []
     try:
+        B.fp8q_test_set_fused_layout(layout)
         for grid in (0, ctas):
             B.fp8q_test_set_fused_grid(grid)
             o = dict(wt=torch.empty(N, K, dtype=torch.uint8, device="cuda"),
@@ -234,6 +244,7 @@ def test_fused_any_grid_gives_the_same_result(ctas):
             outs.append(o)
     finally:
         B.fp8q_test_set_fused_grid(0)
+        B.fp8q_test_set_fused_layout(0)
     ref, got = outs
     for k in ("wt", "wq", "q", "aw", "ax", "sx", "sw"):
         assert torch.equal(ref[k], got[k]), k

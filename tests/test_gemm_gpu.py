@@ -234,7 +234,8 @@ def test_constant_sign_long_contraction():
     assert_gemm_close(y, Yr, S)
 
 
-TILES = [(0, 128), (0, 160), (0, 192), (0, 256), (1, 128), (1, 160), (1, 192), (1, 224), (1, 256), (1, 384)]
+TILES = [(0, 128), (0, 160), (0, 192), (0, 256), (1, 128), (1, 160), (1, 192), (1, 224), (1, 256), (1, 384),
+         (1, 400)]
 
 
 @pytest.mark.parametrize("pair,bn", TILES)
@@ -243,7 +244,7 @@ def test_every_tile_shape_on_ragged_problems(pair, bn):
     and K all leave partial tiles: forward, dgrad and wgrad."""
     try:
         B.fp8q_gemm_set_tile(pair, bn)
-        for M, N, K in [(1000, 1600, 640), (300, 272, 400), (129, 144, 1600), (513, 96, 48)]:
+        for M, N, K in [(1000, 1600, 640), (300, 272, 400), (129, 144, 1600), (513, 96, 48), (260, 1584, 272)]:
             xq = rand_e4m3((M, K), seed=M + 7 * N + K, scale=30.0)
             wq = rand_e4m3((K, N), seed=3 * M + N + K, scale=30.0)
             Yr, S = O.gemm_fwd(xq, wq, 2.5, 0.5)
