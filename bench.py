@@ -497,7 +497,12 @@ def run_profile(args, local):
     w = workload(args.workload, args.rows)
     H = WL.bf16_tensor(WL.h_preact(w, 0)).to(dev)
     Wt = WL.bf16_tensor(WL.w_down(w)).to(dev)
-    fused = WL.WORKLOADS[args.workload].M >= FUSED_MIN_ROWS
+    full = WL.WORKLOADS[args.workload]
+    fused = full.M >= FUSED_MIN_ROWS
+    if fused and w.M != full.M:
+        # the full size's tile too (the tile choice depends on M)
+        from quantize_fp8_gemm_gb300 import binding as B
+        B.fp8q_gemm_set_tile(*B.fp8q_test_fused_tile(full.M, full.N))
     dp = Fp8DownProj(w.M, w.K, w.N, margin=w.margin, history_len=w.history_len, fused=fused, device=dev)
     dp.calibrate(H, Wt)
     for _ in range(max(1, args.steps)):
@@ -506,6 +511,8 @@ def run_profile(args, local):
     st = int(dp.gemm_status.item())
     print(json.dumps({"profile": w.name, "M": w.M, "K": w.K, "N": w.N, "fused": dp.fused, "steps": args.steps,
                       "status": st}), flush=True)
+    if fused and w.M != full.M:
+        B.fp8q_gemm_set_tile(-1)
     if st != 0:
         raise SystemExit(1)
 
@@ -755,7 +762,7 @@ def measure_extras(args, dp, H, Wt, flush, kern_ms, w, dev, fp8: dict, peaks: di
         "timing": "back-to-back launches over rotating input copies (> L2) in one CUDA graph, one event pair",
         "workload": w.name,
     }
-    out["interference"] = measure_interference(dp, H, w, dev, flush)
+    out["fused_layouts"] = measure_fused_layouts(dp, H, Wt, w, dev, 10)
     cfg_steps = max(20, min(100, args.steps))
     out["configs"] = {}
     for name in ("gpt2s", "gpt2s_batch", "outlier"):
@@ -769,60 +776,36 @@ def measure_extras(args, dp, H, Wt, flush, kern_ms, w, dev, fp8: dict, peaks: di
     return out
 
 
-def measure_interference(dp, H, w, dev, flush) -> dict:
-    """Why the one-launch step does not reach max(HBM, tensor) time: the FP8
-    GEMM of the workload run alone, beside a plain device write of the bytes
-    the quantize writes (the BF16 copy and the E4M3 codes, 3 B per element),
-    and beside the quantize kernel itself, each pair on two streams (the GEMM
-    launched first, its persistent CTAs resident on every SM, the other
-    kernel's CTAs filling the remaining slots).  Median device time of each,
-    L2 flushed before each sample."""
+def measure_fused_layouts(dp, H, Wt, w, dev, reps: int) -> dict:
+    """The one-launch step kernel with each layout of its quantize warps pinned
+    (1: quantize-first, 24 warps; 2: GEMM-first, 12 working warps off the MMA
+    issuer's scheduler), timed like the rooflines' kernels: back-to-back
+    launches over copies of H that together exceed L2."""
     from quantize_fp8_gemm_gb300 import binding as B
+    if not dp.fused:
+        return {}
     M, K, N = w.M, w.K, w.N
-    xq = dp.x_q.clone()
-    y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
-    sx, sw = dp.x.scale.clone(), dp.w.scale.clone()
-    wbuf = torch.empty(3 * M * K // 4, dtype=torch.int32, device=dev)
+    Hs = list(H) + [torch.empty_like(H[0]).copy_(H[i % len(H)]) for i in range(4 - len(H))]
+    ws = torch.zeros(B.fp8_downproj_workspace_bytes(M), dtype=torch.uint8, device=dev)
+    xq = torch.empty(M, K, dtype=torch.uint8, device=dev)
     act = torch.empty(M, K, dtype=torch.bfloat16, device=dev)
-    q = torch.empty(M, K, dtype=torch.uint8, device=dev)
-    amax = torch.zeros(1, device=dev)
-    s1, s2 = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-
-    def gemm():
-        B.fp8_gemm_fwd(xq, dp.wt_q, sx, sw, y)
-
-    def write():
-        wbuf.zero_()
-
-    def quant():
-        B.fp8_quant_fused_ex(H[0], dp.act, B.E4M3, sx, act_out=act, q_out=q, amax_out=amax, flags=B.ACCUMULATE)
-
-    def pair(other):
-        def f():
-            main = torch.cuda.current_stream()
-            s1.wait_stream(main)
-            s2.wait_stream(main)
-            with torch.cuda.stream(s1):
-                gemm()
-            with torch.cuda.stream(s2):
-                other()
-            main.wait_stream(s1)
-            main.wait_stream(s2)
-        return f
-
+    wtq = torch.empty(N, K, dtype=torch.uint8, device=dev)
+    y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+    ax, aw = torch.zeros(1, device=dev), torch.zeros(1, device=dev)
+    sx, sw = dp.x.scale.clone(), dp.w.scale.clone()
     out = {}
-    for name, fn in [("gemm", gemm), ("write 3 B/elem", write), ("quantize", quant),
-                     ("gemm beside the write", pair(write)), ("gemm beside the quantize", pair(quant))]:
-        for _ in range(3):
-            fn()
-        torch.cuda.synchronize()
-        out[name + " ms"] = float(np.median(timed_steps(lambda i: fn(), flush, 12)))
-    out["serial sum with the write ms"] = out["gemm ms"] + out["write 3 B/elem ms"]
-    out["serial sum with the quantize ms"] = out["gemm ms"] + out["quantize ms"]
-    del xq, y, wbuf, act, q
+    try:
+        for layout, name in ((1, "quantize-first"), (2, "GEMM-first")):
+            B.fp8q_test_set_fused_layout(layout)
+            out[name + " ms"] = timed_b2b([lambda h=h: B.fp8_downproj_fwd_ex(
+                h, wtq, sx, sw, xq, y, ws, w=Wt, amax_w=aw, act=dp.act, act_out=act, amax_out=ax,
+                flags=B.ACCUMULATE) for h in Hs], reps)
+    finally:
+        B.fp8q_test_set_fused_layout(0)
+    out["default"] = "GEMM-first" if 2.0 * N * 6.45e12 > 5.0 * 3.7e15 else "quantize-first"
+    del Hs, ws, xq, act, wtq, y
     torch.cuda.empty_cache()
     return out
-
 
 def measure_other_rows(dev, reps: int, fp8_tflops: float) -> dict:
     """The path's other rows, each on the workload it belongs to and timed like

@@ -78,6 +78,8 @@ def lib() -> ctypes.CDLL:
         L.fp8q_test_set_fused_grid.restype = i32
         L.fp8q_test_set_fused_layout.argtypes = [i32]
         L.fp8q_test_set_fused_layout.restype = i32
+        L.fp8q_test_fused_tile.argtypes = [i64, i64, P, P]
+        L.fp8q_test_fused_tile.restype = i32
         L.fp8q_test_noalloc_fill.argtypes = [i32, P]
         L.fp8q_test_noalloc_fill.restype = i32
         L.fp8q_mx_set_tile.argtypes = [i32]
@@ -486,6 +488,13 @@ def fp8q_test_set_fused_grid(ctas: int) -> None:
 def fp8q_test_set_fused_layout(layout: int) -> None:
     """Pin the one-launch step's quantize layout (1 quantize-first, 2 GEMM-first, 0 = by N)."""
     _check("fp8q_test_set_fused_layout", lib().fp8q_test_set_fused_layout(int(layout)))
+
+
+def fp8q_test_fused_tile(M: int, N: int) -> tuple:
+    """(pair, bn): the tile the one-launch step takes at M x N."""
+    pair, bn = ctypes.c_int(0), ctypes.c_int(0)
+    _check("fp8q_test_fused_tile", lib().fp8q_test_fused_tile(int(M), int(N), ctypes.byref(pair), ctypes.byref(bn)))
+    return pair.value, bn.value
 
 
 def fp8q_test_noalloc_fill(byte: int, stream=None) -> None:

@@ -300,7 +300,7 @@ __device__ __forceinline__ void fused_rows_body(const FusedArgs& fz, float s, in
         }
         uint32_t bm2 = 0;  // this batch's magnitudes (act(0) = 0 for the padding)
 #pragma unroll
-        for (int j = 0; j < L::BATCH; ++j) x[j] = act8<ACT>(x[j], bm2);
+        for (int j = 0; j < L::BATCH; ++j) x[j] = act8<ACT, true>(x[j], bm2);
         if (may_saturate<FP8Q_E4M3>(bm2, s)) {
 #pragma unroll
             for (int j = 0; j < L::BATCH; ++j)
@@ -1534,6 +1534,16 @@ int launch_eq(const Shape& s, const void* a, const void* b, const float* sa, con
 using namespace fp8q;
 
 extern "C" void fp8q_gemm_test_hold_loads(int on) { g_hold_loads.store(on != 0 ? 1 : 0); }
+
+extern "C" int fp8q_test_fused_tile(int64_t M, int64_t N, int* pair, int* bn) {
+    if (!pair || !bn) return FP8Q_ERR_NULL;
+    if (M < 1 || N < 16) return FP8Q_ERR_SHAPE;
+    Shape s = pick_shape(M, N, false);
+    if (s.bn == 384) s.bn = 256;  // as gemm_dispatch_t does for the one-launch step
+    *pair = s.pair ? 1 : 0;
+    *bn = s.bn;
+    return FP8Q_OK;
+}
 
 extern "C" int fp8q_test_set_fused_layout(int layout) {
     if (layout < 0 || layout > 2) return FP8Q_ERR_UNSUPPORTED;

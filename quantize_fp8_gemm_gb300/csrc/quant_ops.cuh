@@ -33,15 +33,19 @@ __device__ __forceinline__ float act_f32(float h) {
 // square reaches 2^-134 -- there float32 holds it exactly -- and a square below
 // 2^-134 (under half the smallest BF16 subnormal) gives 0 by either route.
 __device__ __forceinline__ uint32_t relu2_bf16x2(uint32_t h2) {
-    uint32_t r;
-    asm("{\n\t.reg .b32 z;\n\tmov.b32 z, 0;\n\tmax.bf16x2 %0, %1, z;\n\tmul.rn.bf16x2 %0, %0, %0;\n\t}"
-        : "=r"(r) : "r"(h2));
-    return r;
+    const __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162*>(&h2);
+    const __nv_bfloat162 r = __hmax2(h, __float2bfloat162_rn(0.0f));  // a NaN lane gives the 0
+    const __nv_bfloat162 q = __hmul2(r, r);
+    return *reinterpret_cast<const uint32_t*>(&q);
 }
 
 // act + BF16 rounding of 8 packed BF16 inputs; returns the packed BF16 results
-// and folds their magnitudes into `amax2` (two 16-bit lanes).
-template <int ACT>
+// and folds their magnitudes into `amax2` (two 16-bit lanes).  PACKED takes
+// ReLU^2 through relu2_bf16x2 (the same results in fewer instructions: the
+// fused kernel, whose quantize warps share issue slots with the GEMM); the
+// stand-alone kernels, bound by HBM, keep the float32 route, with which they
+// need no spills.
+template <int ACT, bool PACKED = false>
 __device__ __forceinline__ uint4 act8(uint4 x, uint32_t& amax2) {
     uint32_t in[4] = {x.x, x.y, x.z, x.w};
     uint32_t out[4];
@@ -50,7 +54,7 @@ __device__ __forceinline__ uint4 act8(uint4 x, uint32_t& amax2) {
         if constexpr (ACT == FP8Q_ACT_IDENTITY) {
             out[j] = in[j];
             amax2 = __vmaxu2(amax2, out[j] & 0x7FFF7FFFu);
-        } else if constexpr (ACT == FP8Q_ACT_RELU2) {
+        } else if constexpr (ACT == FP8Q_ACT_RELU2 && PACKED) {
             out[j] = relu2_bf16x2(in[j]);
             amax2 = __vmaxu2(amax2, out[j]);  // a square carries no sign
         } else {

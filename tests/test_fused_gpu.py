@@ -10,7 +10,7 @@ import torch
 import oracle as O
 from quantize_fp8_gemm_gb300 import binding as B
 from quantize_fp8_gemm_gb300 import workloads as WL
-from tests.parity import assert_gemm_close, dev_bf16, dev_f32, host_u8
+from tests.parity import assert_gemm_close, dev_bf16, dev_f32, dev_u8, host_bits16, host_u8
 
 pytestmark = pytest.mark.gpu
 
@@ -77,6 +77,34 @@ def test_fused_equals_separate_calls(pair, bn, layout):
     finally:
         B.fp8q_test_set_fused_layout(0)
         B.fp8q_gemm_set_tile(-1)
+
+
+@pytest.mark.parametrize("act", [B.ACT_RELU2, B.ACT_RELU])
+def test_fused_every_bf16_input(act):
+    """The one-launch step's quantize (ReLU^2 as packed BF16 max and multiply)
+    on every BF16 pattern, NaNs, +-0, subnormals and +-inf included: the BF16
+    activation, the E4M3 codes, amax and the saturation count against the
+    oracle."""
+    M, K, N = 1024, 64, 32
+    pats = np.arange(65536, dtype=np.uint32).astype(np.uint16).reshape(M, K)
+    H = dev_bf16(pats)
+    wt = dev_u8(np.random.default_rng(5).integers(0, 0x7F, (N, K), dtype=np.uint8))  # finite E4M3 codes
+    for s in (1.0, 3.0, 2.0 ** -20):
+        a = torch.empty(M, K, dtype=torch.bfloat16, device="cuda")
+        q = torch.empty(M, K, dtype=torch.uint8, device="cuda")
+        y = torch.empty(M, N, dtype=torch.bfloat16, device="cuda")
+        amax = torch.zeros(1, device="cuda")
+        sat = torch.zeros(1, dtype=torch.int64, device="cuda")
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        ws = torch.zeros(B.fp8_downproj_workspace_bytes(M), dtype=torch.uint8, device="cuda")
+        B.fp8_downproj_fwd(H, wt, dev_f32(s), dev_f32(1.0), q, y, ws, act=act, act_out=a, amax_out=amax,
+                           sat_count=sat, status=st)
+        torch.cuda.synchronize()
+        assert st.item() == 0
+        r = O.quant(pats, act, O.E4M3, np.float32(s))
+        assert np.array_equal(host_bits16(a), r["act"]), s
+        assert np.array_equal(host_u8(q), r["q"]), s
+        assert amax.item() == r["amax"] and sat.item() == r["sat"], s
 
 
 @pytest.mark.parametrize("act", [B.ACT_IDENTITY, B.ACT_RELU, B.ACT_RELU2])

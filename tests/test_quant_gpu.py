@@ -98,6 +98,19 @@ def test_every_bf16_input(fmt):
         assert_same(g, r, ["q", "amax", "sat"])
 
 
+@pytest.mark.parametrize("act", [B.ACT_RELU2, B.ACT_RELU])
+def test_every_bf16_input_through_the_activation(act):
+    """Every BF16 pattern, NaNs, +-0, subnormals and +-inf included, through
+    ReLU^2 and ReLU: the BF16 activation, the E4M3 codes, amax and the
+    saturation count against the oracle, under scales that put the codes in
+    every range."""
+    allp = np.arange(65536, dtype=np.uint32).astype(np.uint16).reshape(-1, 64)
+    for s in [1.0, 3.0, 2.0 ** -20, 1e-30, 3e30]:
+        g = run_quant(allp, act, B.E4M3, s)
+        r = O.quant(allp, act, O.E4M3, np.float32(s))
+        assert_same(g, r, ["act", "q", "amax", "sat"])
+
+
 @pytest.mark.parametrize("fmt", [B.E4M3, B.E5M2])
 def test_cast_every_fp32_pattern(fmt):
     """The kernels' FP32 -> FP8 conversion over all 2^32 float32 bit patterns
