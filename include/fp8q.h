@@ -530,7 +530,8 @@ int fp8_downproj_fwd_noalloc(const void* h, const void* wt_q, int64_t M, int64_t
  * Errors: FP8Q_ERR_UNSUPPORTED for both or neither mode, act_out in column
  * mode, a bad act or fmt, or no sm_103 device; FP8Q_ERR_NULL for a missing
  * output of the chosen mode; FP8Q_ERR_SHAPE for M < 0, (row mode) K < 32 or
- * K % 32 != 0, (column mode) M % 32 != 0, K < 16 or K % 16 != 0;
+ * K % 32 != 0, (column mode) M % 32 != 0, K < 16, K % 16 != 0 or
+ * K > 4,194,240 (65535 tiles of 64 columns);
  * FP8Q_ERR_ALIGN for tensors not 16-byte aligned.
  */
 int fp8_quant_mx(const void* h, int64_t M, int64_t K, int act, int fmt, void* act_out, void* q_out,
