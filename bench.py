@@ -488,9 +488,10 @@ def step_desc(dp) -> tuple[str, int]:
 
 def run_profile(args, local):
     """A few eager steps of the workload, nothing timed: the command ncu wraps.
-    With --rows the step takes the path the full-size workload takes (the
-    one-launch kernel or the two-launch cast + GEMM), so a smaller capture
-    shows the same kernels."""
+    With --rows the step takes the path and the GEMM tile the full-size
+    workload takes (the one-launch kernel, or with --unfused or below the
+    one-launch size the two-launch cast + GEMM), so a smaller capture shows
+    the same kernels."""
     from quantize_fp8_gemm_gb300.downproj import FUSED_MIN_ROWS, Fp8DownProj
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
@@ -498,11 +499,11 @@ def run_profile(args, local):
     H = WL.bf16_tensor(WL.h_preact(w, 0)).to(dev)
     Wt = WL.bf16_tensor(WL.w_down(w)).to(dev)
     full = WL.WORKLOADS[args.workload]
-    fused = full.M >= FUSED_MIN_ROWS
-    if fused and w.M != full.M:
+    fused = full.M >= FUSED_MIN_ROWS and not args.unfused
+    if w.M != full.M:
         # the full size's tile too (the tile choice depends on M)
         from quantize_fp8_gemm_gb300 import binding as B
-        B.fp8q_gemm_set_tile(*B.fp8q_test_fused_tile(full.M, full.N))
+        B.fp8q_gemm_set_tile(*B.fp8q_test_gemm_tile(full.M, full.N, fused))
     dp = Fp8DownProj(w.M, w.K, w.N, margin=w.margin, history_len=w.history_len, fused=fused, device=dev)
     dp.calibrate(H, Wt)
     for _ in range(max(1, args.steps)):
@@ -511,7 +512,7 @@ def run_profile(args, local):
     st = int(dp.gemm_status.item())
     print(json.dumps({"profile": w.name, "M": w.M, "K": w.K, "N": w.N, "fused": dp.fused, "steps": args.steps,
                       "status": st}), flush=True)
-    if fused and w.M != full.M:
+    if w.M != full.M:
         B.fp8q_gemm_set_tile(-1)
     if st != 0:
         raise SystemExit(1)
@@ -932,15 +933,18 @@ def measure_other_rows(dev, reps: int, fp8_tflops: float) -> dict:
         sfx = torch.empty(Mx, Kx // 32, dtype=torch.uint8, device=dev)
         ax = torch.empty(Mx, Kx, dtype=torch.bfloat16, device=dev)
         r = max(4, reps // (1 if wl_name == "outlier" else 8))
-        t = timed_b2b([lambda h=h: B.fp8_quant_mx(h, B.ACT_RELU2, B.E4M3, act_out=ax, q_out=qx, sf_out=sfx,
-                                                  amax_out=amax) for h in Hx], r)
+        # MX scales are per block, so no per-tensor amax is asked for (it would add a zeroing memset per call)
+        t = timed_b2b([lambda h=h: B.fp8_quant_mx(h, B.ACT_RELU2, B.E4M3, act_out=ax, q_out=qx, sf_out=sfx)
+                       for h in Hx], r)
         out[f"next: MX quantize of H, 32-value blocks ({wl_name})"] = mem_row(
             t, 5.0 * Mx * Kx + Mx * Kx / 32, f"H [{Mx},{Kx}] -> act + E4M3 + scale bytes")
         del Hx, ax
         qwt = torch.empty(Nx, Kx, dtype=torch.uint8, device=dev)
         sfw = torch.empty(Nx, Kx // 32, dtype=torch.uint8, device=dev)
-        t = timed_b2b([lambda: B.fp8_quant_mx(Wx, B.ACT_IDENTITY, B.E4M3, q_t_out=qwt, sf_t_out=sfw, amax_out=amax)],
+        Wxs = copies(Wx)
+        t = timed_b2b([lambda w=w: B.fp8_quant_mx(w, B.ACT_IDENTITY, B.E4M3, q_t_out=qwt, sf_t_out=sfw) for w in Wxs],
                       r)
+        del Wxs
         out[f"next: MX weight cast, transposed ({wl_name})"] = mem_row(
             t, 3.0 * Kx * Nx + Kx * Nx / 32, f"W [{Kx},{Nx}] -> W_q^T + scale bytes")
         B.fp8_quant_mx(Wx, B.ACT_IDENTITY, B.E4M3, q_t_out=qwt, sf_t_out=sfw)
@@ -1032,6 +1036,8 @@ def main():
                     help="launch the step kernel by kernel instead of as a CUDA graph")
     ap.add_argument("--profile", action="store_true",
                     help="run --steps eager steps without timing (the command an ncu capture wraps)")
+    ap.add_argument("--unfused", action="store_true",
+                    help="with --profile: the two-launch path (batched cast, then the GEMM) instead of the one-launch step")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours" and not args.profile:
         ap.error("--warmup must be at least 3")

@@ -74,13 +74,14 @@ int fp8q_test_set_fused_grid(int ctas);
 int fp8q_test_set_fused_layout(int layout);
 
 /*
- * fp8q_test_fused_tile -- the tile (*pair: 1 = 2-SM pair, 0 = one CTA; *bn:
- * its width) the one-launch step takes at M x N under the current tile
- * override, so a profile of a smaller M can pin the full size's tile with
- * fp8q_gemm_set_tile.  Needs a device (the choice depends on its SM count).
- * Errors: FP8Q_ERR_NULL, FP8Q_ERR_SHAPE (M < 1 or N < 16).
+ * fp8q_test_gemm_tile -- the tile (*pair: 1 = 2-SM pair, 0 = one CTA; *bn:
+ * its width) that the one-launch step (fused != 0) or fp8_gemm_fwd (fused ==
+ * 0) takes at M x N under the current tile override, so a profile of a
+ * smaller M can pin the full size's tile with fp8q_gemm_set_tile.  Needs a
+ * device (the choice depends on its SM count).  Errors: FP8Q_ERR_NULL,
+ * FP8Q_ERR_SHAPE (M < 1 or N < 16).
  */
-int fp8q_test_fused_tile(int64_t M, int64_t N, int* pair, int* bn);
+int fp8q_test_gemm_tile(int64_t M, int64_t N, int fused, int* pair, int* bn);
 
 /*
  * fp8q_test_noalloc_fill -- fill every byte of the static counter array of

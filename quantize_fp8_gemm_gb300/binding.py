@@ -78,8 +78,8 @@ def lib() -> ctypes.CDLL:
         L.fp8q_test_set_fused_grid.restype = i32
         L.fp8q_test_set_fused_layout.argtypes = [i32]
         L.fp8q_test_set_fused_layout.restype = i32
-        L.fp8q_test_fused_tile.argtypes = [i64, i64, P, P]
-        L.fp8q_test_fused_tile.restype = i32
+        L.fp8q_test_gemm_tile.argtypes = [i64, i64, i32, P, P]
+        L.fp8q_test_gemm_tile.restype = i32
         L.fp8q_test_noalloc_fill.argtypes = [i32, P]
         L.fp8q_test_noalloc_fill.restype = i32
         L.fp8q_mx_set_tile.argtypes = [i32]
@@ -490,10 +490,11 @@ def fp8q_test_set_fused_layout(layout: int) -> None:
     _check("fp8q_test_set_fused_layout", lib().fp8q_test_set_fused_layout(int(layout)))
 
 
-def fp8q_test_fused_tile(M: int, N: int) -> tuple:
-    """(pair, bn): the tile the one-launch step takes at M x N."""
+def fp8q_test_gemm_tile(M: int, N: int, fused: bool) -> tuple:
+    """(pair, bn): the tile the one-launch step (fused) or fp8_gemm_fwd takes at M x N."""
     pair, bn = ctypes.c_int(0), ctypes.c_int(0)
-    _check("fp8q_test_fused_tile", lib().fp8q_test_fused_tile(int(M), int(N), ctypes.byref(pair), ctypes.byref(bn)))
+    _check("fp8q_test_gemm_tile", lib().fp8q_test_gemm_tile(int(M), int(N), 1 if fused else 0, ctypes.byref(pair),
+                                                           ctypes.byref(bn)))
     return pair.value, bn.value
 
 

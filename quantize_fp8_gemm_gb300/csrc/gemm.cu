@@ -1535,11 +1535,11 @@ using namespace fp8q;
 
 extern "C" void fp8q_gemm_test_hold_loads(int on) { g_hold_loads.store(on != 0 ? 1 : 0); }
 
-extern "C" int fp8q_test_fused_tile(int64_t M, int64_t N, int* pair, int* bn) {
+extern "C" int fp8q_test_gemm_tile(int64_t M, int64_t N, int fused, int* pair, int* bn) {
     if (!pair || !bn) return FP8Q_ERR_NULL;
     if (M < 1 || N < 16) return FP8Q_ERR_SHAPE;
-    Shape s = pick_shape(M, N, false);
-    if (s.bn == 384) s.bn = 256;  // as gemm_dispatch_t does for the one-launch step
+    Shape s = pick_shape(M, N, !fused);
+    if (fused && s.bn == 384) s.bn = 256;  // as gemm_dispatch_t does for the one-launch step
     *pair = s.pair ? 1 : 0;
     *bn = s.bn;
     return FP8Q_OK;
