@@ -372,9 +372,10 @@ class Fp8DownProj:
             hs.update()  # the cache's own delayed scale for the next step
         return self.y
 
-    def capture(self, H: torch.Tensor, W: torch.Tensor, H_next: torch.Tensor | None = None) -> "StepGraph":
+    def capture(self, H: torch.Tensor, W: torch.Tensor, H_next: torch.Tensor | None = None,
+                W_next: torch.Tensor | None = None) -> "StepGraph":
         """Capture the step as CUDA graphs on fixed buffers (see StepGraph)."""
-        return StepGraph(self, H, W, H_next)
+        return StepGraph(self, H, W, H_next, W_next)
 
     def recompute_on_overflow(self, H: torch.Tensor, W: torch.Tensor) -> int:
         """Detect-and-recompute ("FP8 Training & Inference", Delayed Scaling:
@@ -499,32 +500,39 @@ class StepGraph:
     Consecutive steps use alternating scale slots, so two graphs are
     captured (one per slot); ``replay()`` runs the one matching the current
     slot and switches slots, so replays and eager steps mix freely.  The
-    graph for the slot current at capture reads H, the other H_next
-    (default H).  The amax histories live in device memory, so replays carry
-    the delayed scaling forward exactly as eager steps do.  Run at least one
-    eager step first (it performs the one-time per-kernel set-up).
+    graph for the slot current at capture reads H and W, the other H_next and
+    W_next (default H and W), so a caller can fill one pair of buffers while
+    the step reads the other (``buffer()`` names the pair the next replay
+    reads).  The amax histories live in device memory, so replays carry the
+    delayed scaling forward exactly as eager steps do.  Run at least one eager
+    step first (it performs the one-time per-kernel set-up).
     """
 
-    def __init__(self, dp: Fp8DownProj, H: torch.Tensor, W: torch.Tensor, H_next: torch.Tensor | None = None):
+    def __init__(self, dp: Fp8DownProj, H: torch.Tensor, W: torch.Tensor, H_next: torch.Tensor | None = None,
+                 W_next: torch.Tensor | None = None):
         self.dp = dp
         self.slot0 = dp.x.slot  # the scale slot graph 0 reads; graph 1 reads the other
         self.graphs = []
         side = torch.cuda.Stream()
         side.wait_stream(torch.cuda.current_stream())
-        for h in (H, H if H_next is None else H_next):
+        for h, w in ((H, W), (H if H_next is None else H_next, W if W_next is None else W_next)):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.stream(side):
                 with torch.cuda.graph(g, stream=side):
-                    self.y = dp.step(h, W)
+                    self.y = dp.step(h, w)
             self.graphs.append(g)
         torch.cuda.current_stream().wait_stream(side)
         self._next = 0
+
+    def buffer(self) -> int:
+        """0 if the next replay reads (H, W), 1 if it reads (H_next, W_next)."""
+        return self._next if self.dp.group else int(self.dp.x.slot != self.slot0)
 
     def replay(self) -> torch.Tensor:
         """Run one step: the graph whose scale slot is current, then switch
         the host-side slots as an eager step would."""
         dp = self.dp
-        k = self._next if dp.group else int(dp.x.slot != self.slot0)
+        k = self.buffer()
         self.graphs[k].replay()
         self._next = k ^ 1
         if not dp.group:
