@@ -79,12 +79,17 @@ constexpr int kWideEpiWarps = 8;  // two warps per TMEM lane quarter, each half 
 //               warps, and none competing with the MMA issuer (1.19 -> 1.11 ms
 //               at 131072 x 6400 -> 1600 on 400-wide tiles; slower where the
 //               quantize is the longer part: 0.217 -> 0.235 ms at 65536 x
-//               3072 -> 768).
+//               3072 -> 768) -- and units of 4 rows instead of 16, about one
+//               batch of loads per thread per unit at K = 6400, so the unit's
+//               closing barrier paces the warps (1.10 -> 1.05 ms there; 1, 2,
+//               3, 5, 8, 12 rows: 2.10, 1.35, 1.07, 1.09, 1.08, 1.09 ms; 8 rows
+//               at 65536 x 3072 -> 768 in layout 1: 0.215 -> 0.238 ms).
 template <int FUSED>
 struct QuantLayout {
     static constexpr int WARPS = FUSED == 2 ? 16 : 24;  // warps the CTA launches for the quantize
     static constexpr int SKIP = FUSED == 2 ? 1 : -1;    // the scheduler left to the GEMM (warp id % 4)
     static constexpr int BATCH = FUSED == 2 ? 12 : 8;   // 16-byte loads in flight per thread
+    static constexpr int UNIT = FUSED == 2 ? 4 : 16;     // rows per quantize unit in the full rounds
     static constexpr int FIRST_SKIP = 6 + ((SKIP - 6) % 4 + 4) % 4;  // lowest idle warp id
     static constexpr int active_warps() {
         int n = 0;
@@ -100,7 +105,6 @@ struct QuantLayout {
         return (warp - 6 - idle_below) * 32 + lane;
     }
 };
-constexpr int kUnitRows = 16;  // rows per quantize unit in the full rounds
 
 // Epilogue warps: 8 where the epilogue is exposed -- group mode (a promotion
 // per 128-long K slice; 12 and 16 on its 192- and 256-wide tiles, 64 columns
@@ -410,10 +414,10 @@ __device__ __forceinline__ void fused_cast_w(const FusedArgs& fz, int64_t K, int
 
 // The quantize warps of the fused kernel.  Row units are handed out by
 // ticket (q_next), in row order, so rows finish in order across the GPU and
-// only running CTAs take work.  Tickets 0 .. full - 1 are 16-row units; the
-// rows after them (gridDim.x x 16 rows or more when M allows) are split into
-// gridDim.x equal units of at most 17 rows, so the last units end together
-// instead of one SM carrying a whole extra unit at the end.  One thread asks
+// only running CTAs take work.  Tickets 0 .. full - 1 are units of L::UNIT
+// rows; the rows after them (gridDim.x x UNIT rows or more when M allows) are
+// split into gridDim.x equal units of at most UNIT + 1 rows, so the last
+// units end together instead of one SM carrying a whole extra unit at the end.  One thread asks
 // for the next ticket before the CTA quantizes the current unit; the unit's
 // closing barrier publishes it to the other quantize threads.
 template <int FUSED>
@@ -425,8 +429,8 @@ __device__ __forceinline__ void fused_quantize(const FusedArgs& fz, const float*
     const float s = __ldg(scale);
     uint32_t amax2 = 0, nsat = 0;
     const int64_t G = gridDim.x;
-    const int64_t full = M / kUnitRows > G ? M / kUnitRows - G : 0;
-    const int64_t share = (M - full * kUnitRows + G - 1) / G;
+    const int64_t full = M / L::UNIT > G ? M / L::UNIT - G : 0;
+    const int64_t share = (M - full * L::UNIT + G - 1) / G;
     const int64_t nunits = full + G;
     if (qt == 0) s_ticket[0] = atomicAdd(fz.q_next, 1u);
     named_barrier(1, L::THREADS);
@@ -436,10 +440,10 @@ __device__ __forceinline__ void fused_quantize(const FusedArgs& fz, const float*
         if (qt == 0) s_ticket[par ^ 1] = atomicAdd(fz.q_next, 1u);
         int64_t r0, r1;
         if (t < full) {
-            r0 = t * kUnitRows;
-            r1 = r0 + kUnitRows;
+            r0 = t * L::UNIT;
+            r1 = r0 + L::UNIT;
         } else {
-            r0 = full * kUnitRows + (t - full) * share;
+            r0 = full * L::UNIT + (t - full) * share;
             r1 = r0 + share < M ? r0 + share : M;
         }
         // fused_quantize_rows ends with a barrier of all quantize threads, after
