@@ -779,7 +779,7 @@ def measure_extras(args, dp, H, Wt, flush, kern_ms, w, dev, fp8: dict, peaks: di
 
 def measure_fused_layouts(dp, H, Wt, w, dev, reps: int) -> dict:
     """The one-launch step kernel with each layout of its quantize warps pinned
-    (1: quantize-first, 24 warps; 2: GEMM-first, 12 working warps off the MMA
+    (1: quantize-first, 24 warps; 2: GEMM-first, 9 working warps off the MMA
     issuer's scheduler), timed like the rooflines' kernels: back-to-back
     launches over copies of H that together exceed L2."""
     from quantize_fp8_gemm_gb300 import binding as B

@@ -65,8 +65,8 @@ int fp8q_test_set_fused_grid(int ctas);
 /*
  * fp8q_test_set_fused_layout -- pin the layout of the one-launch step's
  * quantize warps: 1 = quantize-first (24 warps, 8 loads in flight each),
- * 2 = GEMM-first (12 working warps, none on the MMA issuer's scheduler, 12
- * loads in flight each; taken on 256- and 400-wide pair tiles only, else
+ * 2 = GEMM-first (9 working warps, none on the MMA issuer's scheduler, 16
+ * loads in flight each, 4-row units; taken on 256- and 400-wide pair tiles only, else
  * layout 1), 0 = chosen by N (GEMM-first for N above ~1430, where the step's
  * GEMM outlasts its quantize).  The layouts give identical results.  Returns
  * FP8Q_ERR_UNSUPPORTED unless 0 <= layout <= 2.

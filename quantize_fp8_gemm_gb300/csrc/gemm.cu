@@ -73,22 +73,24 @@ constexpr int kWideEpiWarps = 8;  // two warps per TMEM lane quarter, each half 
 // its arithmetic but no loads or stores, 1.22 ms whole).  Two layouts:
 //   FUSED == 1  the quantize is the longer part of the step (few output
 //               columns per byte of H): 24 warps, 8 loads in flight each;
-//   FUSED == 2  the GEMM is the longer part: 16 warps, of which the four on
+//   FUSED == 2  the GEMM is the longer part: 12 warps, of which the three on
 //               the MMA issuer's scheduler (warp id % 4 == 1) stay idle, and
-//               12 loads in flight each -- the same bytes in flight from 12
-//               warps, and none competing with the MMA issuer (1.19 -> 1.11 ms
-//               at 131072 x 6400 -> 1600 on 400-wide tiles; slower where the
-//               quantize is the longer part: 0.217 -> 0.235 ms at 65536 x
-//               3072 -> 768) -- and units of 4 rows instead of 16, about one
-//               batch of loads per thread per unit at K = 6400, so the unit's
-//               closing barrier paces the warps (1.10 -> 1.05 ms there; 1, 2,
-//               3, 5, 8, 12 rows: 2.10, 1.35, 1.07, 1.09, 1.08, 1.09 ms; 8 rows
-//               at 65536 x 3072 -> 768 in layout 1: 0.215 -> 0.238 ms).
+//               16 loads in flight each -- the same bytes in flight from 9
+//               warps, none competing with the MMA issuer (at 131072 x 6400 ->
+//               1600 on 400-wide tiles, 1.19 -> 1.11 ms with 12 working warps x
+//               12 loads; 9 x 16 a further 1 %; 7 x 20 and 6 x 24 slower; and
+//               slower where the quantize is the longer part: 0.217 -> 0.235
+//               ms at 65536 x 3072 -> 768) -- and units of 4 rows instead of
+//               16, about one batch of loads per thread per unit at K = 6400,
+//               so the unit's closing barrier paces the warps (1.10 -> 1.05 ms
+//               there; 1, 2, 3, 5, 8, 12 rows: 2.10, 1.35, 1.07, 1.09, 1.08,
+//               1.09 ms; 8 rows at 65536 x 3072 -> 768 in layout 1: 0.215 ->
+//               0.238 ms).
 template <int FUSED>
 struct QuantLayout {
-    static constexpr int WARPS = FUSED == 2 ? 16 : 24;  // warps the CTA launches for the quantize
+    static constexpr int WARPS = FUSED == 2 ? 12 : 24;  // warps the CTA launches for the quantize
     static constexpr int SKIP = FUSED == 2 ? 1 : -1;    // the scheduler left to the GEMM (warp id % 4)
-    static constexpr int BATCH = FUSED == 2 ? 12 : 8;   // 16-byte loads in flight per thread
+    static constexpr int BATCH = FUSED == 2 ? 16 : 8;   // 16-byte loads in flight per thread
     static constexpr int UNIT = FUSED == 2 ? 4 : 16;     // rows per quantize unit in the full rounds
     static constexpr int FIRST_SKIP = 6 + ((SKIP - 6) % 4 + 4) % 4;  // lowest idle warp id
     static constexpr int active_warps() {
