@@ -293,6 +293,15 @@ def test_testing_hooks_arguments(lib):
     assert lib.fp8q_test_set_fused_layout(-1) == ERR_UNSUPPORTED
     assert lib.fp8q_test_set_fused_layout(2) == OK
     assert lib.fp8q_test_set_fused_layout(0) == OK
+    pair, bn = ctypes.c_int(-1), ctypes.c_int(-1)
+    f = lib.fp8q_test_gemm_tile
+    f.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
+    f.restype = ctypes.c_int
+    assert f(1024, 1600, 1, None, ctypes.byref(bn)) == ERR_NULL
+    assert f(1024, 1600, 1, ctypes.byref(pair), None) == ERR_NULL
+    assert f(0, 1600, 0, ctypes.byref(pair), ctypes.byref(bn)) == ERR_SHAPE
+    assert f(1024, 8, 0, ctypes.byref(pair), ctypes.byref(bn)) == ERR_SHAPE
+    assert (pair.value, bn.value) == (-1, -1)  # untouched on error
     import torch
     if not torch.cuda.is_available():
         # no device: the static array has no address to look up
