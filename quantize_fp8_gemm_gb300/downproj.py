@@ -22,7 +22,11 @@ import torch
 from . import binding as B
 
 
-FUSED_MIN_ROWS = 32768  # default switch to the fused kernel (per-tensor scales)
+# Default switch to the one-launch step (per-tensor scales).  On GB300 it beats
+# the batched cast + GEMM pair from 16,384 rows (16384 x 4096 -> 1024: 100.0
+# against 103.4 us; 16384 x 3072 -> 768: 70.6 against 72.0 us) and loses at
+# 8192 (55.4 against 41.3 us at 8192 x 3072 -> 768).
+FUSED_MIN_ROWS = 16384
 
 RECOMPUTE_X, RECOMPUTE_W = 1, 2  # recompute_on_overflow(): which operand was cast again
 
