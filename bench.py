@@ -499,6 +499,8 @@ def run_profile(args, local):
     H = WL.bf16_tensor(WL.h_preact(w, 0)).to(dev)
     Wt = WL.bf16_tensor(WL.w_down(w)).to(dev)
     full = WL.WORKLOADS[args.workload]
+    if args.mx:
+        return run_profile_mx(args, w, H, Wt, dev)
     fused = full.M >= FUSED_MIN_ROWS and not args.unfused
     if w.M != full.M:
         # the full size's tile too (the tile choice depends on M)
@@ -515,6 +517,29 @@ def run_profile(args, local):
     if w.M != full.M:
         B.fp8q_gemm_set_tile(-1)
     if st != 0:
+        raise SystemExit(1)
+
+
+def run_profile_mx(args, w, H, Wt, dev):
+    """--profile --mx: the MXFP8 path on the workload, nothing timed: the
+    activation's block quantize, the weight's transposed block cast and the
+    block-scaled GEMM, --steps times."""
+    from quantize_fp8_gemm_gb300 import binding as B
+    M, K, N = w.M, w.K, w.N
+    q = torch.empty(M, K, dtype=torch.uint8, device=dev)
+    sf = torch.empty(M, K // 32, dtype=torch.uint8, device=dev)
+    qt = torch.empty(N, K, dtype=torch.uint8, device=dev)
+    sft = torch.empty(N, K // 32, dtype=torch.uint8, device=dev)
+    y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    for _ in range(max(1, args.steps)):
+        B.fp8_quant_mx(H, B.ACT_RELU2, B.E4M3, q_out=q, sf_out=sf)
+        B.fp8_quant_mx(Wt, B.ACT_IDENTITY, B.E4M3, q_t_out=qt, sf_t_out=sft)
+        B.fp8_gemm_mx(q, sf, qt, sft, y, status=st)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile": w.name + " (MXFP8)", "M": M, "K": K, "N": N, "steps": args.steps,
+                      "status": int(st.item())}), flush=True)
+    if st.item() != 0:
         raise SystemExit(1)
 
 
@@ -1076,6 +1101,8 @@ def main():
                     help="launch the step kernel by kernel instead of as a CUDA graph")
     ap.add_argument("--profile", action="store_true",
                     help="run --steps eager steps without timing (the command an ncu capture wraps)")
+    ap.add_argument("--mx", action="store_true",
+                    help="with --profile: the MXFP8 path (block quantize, block cast, block-scaled GEMM)")
     ap.add_argument("--unfused", action="store_true",
                     help="with --profile: the two-launch path (batched cast, then the GEMM) instead of the one-launch step")
     args = ap.parse_args()
