@@ -113,7 +113,7 @@ quant_mx_rows_kernel(const uint4* __restrict__ h, int64_t nchunks, uint4* __rest
         for (int u = 0; u < U; ++u) {
             const int64_t c = w0 + u * 32 + lane;
             uint32_t m2 = 0;
-            const uint4 a = act8<ACT>(x[u], m2);
+            const uint4 a = act8<ACT, true>(x[u], m2);
             uint32_t m = max16x2(m2);
             m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
             m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
@@ -121,7 +121,13 @@ quant_mx_rows_kernel(const uint4* __restrict__ h, int64_t nchunks, uint4* __rest
             if (c < nchunks) {  // nchunks % 4 == 0: a block is wholly inside or outside
                 amax2 = max(amax2, m);
                 if (act_out) st_stream_v4(act_out + c, a);
-                st_v2(q_out + c, cast8<FMT>(a, pow2f(e), nsat));
+                const float sc = pow2f(e);
+                st_v2(q_out + c, cast8_codes<FMT>(a, sc));
+                // a finite block saturates nothing: e is the largest exponent with
+                // amax 2^e <= max, and its clamp at -127 would need amax above
+                // max 2^127 > FLT_MAX; only a block holding an inf or a NaN (e = 0)
+                // is counted, value by value
+                if (m >= 0x7F80u) nsat += sat_count8<FMT>(a, sc);
                 if ((lane & 3) == 0) sf_out[c >> 2] = static_cast<uint8_t>(127 - e);
             }
         }
