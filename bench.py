@@ -527,9 +527,9 @@ def run_profile_mx(args, w, H, Wt, dev):
     from quantize_fp8_gemm_gb300 import binding as B
     M, K, N = w.M, w.K, w.N
     q = torch.empty(M, K, dtype=torch.uint8, device=dev)
-    sf = torch.empty(M, K // 32, dtype=torch.uint8, device=dev)
+    sf = torch.empty(B.fp8_mx_scale_bytes(M, K), dtype=torch.uint8, device=dev)
     qt = torch.empty(N, K, dtype=torch.uint8, device=dev)
-    sft = torch.empty(N, K // 32, dtype=torch.uint8, device=dev)
+    sft = torch.empty(B.fp8_mx_scale_bytes(N, K), dtype=torch.uint8, device=dev)
     y = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
     st = torch.zeros(1, dtype=torch.int32, device=dev)
     for _ in range(max(1, args.steps)):
@@ -955,7 +955,7 @@ def measure_other_rows(dev, reps: int, fp8_tflops: float) -> dict:
         Hx = copies(torch.randn(Mx, Kx, device=dev, generator=g).to(torch.bfloat16))
         Wx = torch.randn(Kx, Nx, device=dev, generator=g).mul_(0.02).to(torch.bfloat16)
         qx = torch.empty(Mx, Kx, dtype=torch.uint8, device=dev)
-        sfx = torch.empty(Mx, Kx // 32, dtype=torch.uint8, device=dev)
+        sfx = torch.empty(B.fp8_mx_scale_bytes(Mx, Kx), dtype=torch.uint8, device=dev)
         ax = torch.empty(Mx, Kx, dtype=torch.bfloat16, device=dev)
         r = max(4, reps // (1 if wl_name == "outlier" else 8))
         # MX scales are per block, so no per-tensor amax is asked for (it would add a zeroing memset per call)
@@ -965,7 +965,7 @@ def measure_other_rows(dev, reps: int, fp8_tflops: float) -> dict:
             t, 5.0 * Mx * Kx + Mx * Kx / 32, f"H [{Mx},{Kx}] -> act + E4M3 + scale bytes")
         del Hx, ax
         qwt = torch.empty(Nx, Kx, dtype=torch.uint8, device=dev)
-        sfw = torch.empty(Nx, Kx // 32, dtype=torch.uint8, device=dev)
+        sfw = torch.empty(B.fp8_mx_scale_bytes(Nx, Kx), dtype=torch.uint8, device=dev)
         Wxs = copies(Wx)
         t = timed_b2b([lambda w=w: B.fp8_quant_mx(w, B.ACT_IDENTITY, B.E4M3, q_t_out=qwt, sf_t_out=sfw) for w in Wxs],
                       r)

@@ -515,24 +515,34 @@ int fp8_downproj_fwd_noalloc(const void* h, const void* wt_q, int64_t M, int64_t
  *     scale byte = 127 - e: the biased 8-bit exponent of the dequantisation
  *           factor 1 / s_b, i.e. the E8M0 scale the block-scaled tensor-core
  *           MMA takes (2^(byte - 127) multiplies the block's codes)
+ * Scale layout (both modes; the one fp8_gemm_mx reads): the scale bytes of a
+ * block grid of R rows x KB blocks are stored in atoms of 128 rows x 4 blocks,
+ * 512 bytes each -- the layout the block-scaled MMA's tensor-memory copy
+ * takes, so one copy per 128 rows feeds a GEMM stage of 128 K values:
+ *     byte of (row r, block b) = 512 * ((r / 128) * G + b / 4)
+ *                                + 16 * (r % 32) + 4 * ((r / 32) % 4) + b % 4,
+ *     G = ceil(KB / 4); size fp8_mx_scale_bytes(R, 32 * KB).
+ * Blocks KB .. 4G - 1 of a row are padding and are written as 127; bytes of
+ * rows past R in the last 128-row atom are left as they were.
  * Two modes, exactly one per call:
- *   rows:     blocks run along the rows of h [M,K] (K % 32 == 0):
- *             q_out [M,K] codes, sf_out [M, K/32] bytes (row-major), act_out
- *             [M,K] BF16 or NULL.  The activation X of the forward GEMM.
+ *   rows:     blocks run along the rows of h [M,K] (K % 32 == 0, M * K / 32 <
+ *             2^32): q_out [M,K] codes, sf_out the scale layout of the
+ *             [M, K/32] grid, act_out [M,K] BF16 or NULL.  The activation X of
+ *             the forward GEMM.
  *   columns:  blocks run down the columns of h [M,K] (M % 32 == 0), and the
- *             codes are written transposed: q_t_out [K,M], sf_t_out [K, M/32]
- *             (block b of row k of the copy covers h[32b .. 32b + 31, k]).  The
- *             weight W [K_w, N_w] of the forward GEMM: its copy W_q^T [N_w, K_w]
- *             is the GEMM's K-major operand with blocks along K_w.  act_out must
- *             be NULL.
+ *             codes are written transposed: q_t_out [K,M], sf_t_out the scale
+ *             layout of the [K, M/32] grid (block b of row k of the copy covers
+ *             h[32b .. 32b + 31, k]).  The weight W [K_w, N_w] of the forward
+ *             GEMM: its copy W_q^T [N_w, K_w] is the GEMM's K-major operand with
+ *             blocks along K_w.  act_out must be NULL.
  *   amax_out, sat_count  device float / uint64 or NULL; zeroed by the call
  *             (sat_count counts |abf * s_b| > fmt_max: 0 for finite inputs).
  * Errors: FP8Q_ERR_UNSUPPORTED for both or neither mode, act_out in column
  * mode, a bad act or fmt, or no sm_103 device; FP8Q_ERR_NULL for a missing
  * output of the chosen mode; FP8Q_ERR_SHAPE for M < 0, (row mode) K < 32 or
  * K % 32 != 0, (column mode) M % 32 != 0, K < 16, K % 16 != 0 or
- * K > 4,194,240 (65535 tiles of 64 columns);
- * FP8Q_ERR_ALIGN for tensors not 16-byte aligned.
+ * K > 4,194,240 (65535 tiles of 64 columns), (row mode) M * K / 32 >= 2^32;
+ * FP8Q_ERR_ALIGN for tensors (scale arrays included) not 16-byte aligned.
  */
 int fp8_quant_mx(const void* h, int64_t M, int64_t K, int act, int fmt, void* act_out, void* q_out,
                  uint8_t* sf_out, void* q_t_out, uint8_t* sf_t_out, float* amax_out,
@@ -547,18 +557,32 @@ int fp8_quant_mx(const void* h, int64_t M, int64_t K, int act, int fmt, void* ac
  * (tcgen05.mma.kind::mxf8f6f4.block_scale), block by block.
  *   x_q     device [M,K] codes (fmt_x), K contiguous: the rows-mode output of
  *           fp8_quant_mx.
- *   sf_x    device [M, K/32] scale bytes.
+ *   sf_x    device scale bytes of x_q's [M, K/32] block grid in the tiled
+ *           layout of fp8_quant_mx (fp8_mx_scale_bytes(M, K) bytes).
  *   wt_q    device [N,K] codes (fmt_w): the column-mode output of
  *           fp8_quant_mx run on W [K,N].
- *   sf_w    device [N, K/32] scale bytes.
+ *   sf_w    device scale bytes of wt_q's [N, K/32] grid, the same layout
+ *           (fp8_mx_scale_bytes(N, K) bytes).
  *   y       device [M,N] BF16.
  *   M, N, K M >= 0 (0: nothing is enqueued); N >= 16, N % 16 == 0; K >= 32,
  *           K % 32 == 0.
  *   fmt_x, fmt_w  FP8Q_E4M3 or FP8Q_E5M2.
  *   status  device int or NULL: FP8Q_DEV_TIMEOUT if a bounded wait gave up.
+ * Errors: FP8Q_ERR_UNSUPPORTED for a bad format or no sm_103 device;
+ * FP8Q_ERR_NULL for a missing pointer; FP8Q_ERR_SHAPE for the sizes above;
+ * FP8Q_ERR_ALIGN for x_q, wt_q, y, sf_x or sf_w not 16-byte aligned.
  */
 int fp8_gemm_mx(const void* x_q, const uint8_t* sf_x, const void* wt_q, const uint8_t* sf_w, void* y,
                 int64_t M, int64_t N, int64_t K, int fmt_x, int fmt_w, int* status, cudaStream_t stream);
+
+/*
+ * fp8_mx_scale_bytes -- size of the MX scale layout  [mx]
+ *
+ * Bytes of the tiled scale layout (fp8_quant_mx) of a block grid of `rows`
+ * rows x K/32 blocks: ceil(rows / 128) * ceil(K / 128) * 512.  Host only;
+ * returns -1 for rows < 0, K < 0 or K % 32 != 0.
+ */
+int64_t fp8_mx_scale_bytes(int64_t rows, int64_t K);
 
 /*
  * amax_history_update -- delayed per-tensor scale for the next step  [fused][gemms]

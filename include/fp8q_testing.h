@@ -36,11 +36,16 @@ extern "C" {
 int fp8q_gemm_set_tile(int pair, int bn);
 
 /*
- * fp8q_mx_set_tile -- pin the tile width of fp8_gemm_mx: 128, 192 or 256
- * (one CTA per 128 x bn tile), or 0 for the automatic choice (the default).
- * Returns FP8Q_ERR_UNSUPPORTED for any other value (nothing changes).
+ * fp8q_mx_set_tile -- pin the tile shape of fp8_gemm_mx (a tuning knob), or
+ * (0, 0) for the automatic choice (the default):
+ *   pair  0: one CTA per 128 x bn tile
+ *         1: a CTA pair per 256 x bn tile (2-SM); used only when M > 128 and
+ *            the scale rows are whole aligned 4-byte words (K % 128 == 0, both
+ *            scale arrays 4-byte aligned), else the 1-CTA tile of that width
+ *   bn    128, 192 or 256
+ * Returns FP8Q_ERR_UNSUPPORTED for any other combination (nothing changes).
  */
-int fp8q_mx_set_tile(int bn);
+int fp8q_mx_set_tile(int pair, int bn);
 
 /*
  * fp8q_gemm_test_hold_loads -- failure-path hook.  While on != 0, the GEMM

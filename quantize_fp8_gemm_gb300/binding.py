@@ -82,10 +82,12 @@ def lib() -> ctypes.CDLL:
         L.fp8q_test_gemm_tile.restype = i32
         L.fp8q_test_noalloc_fill.argtypes = [i32, P]
         L.fp8q_test_noalloc_fill.restype = i32
-        L.fp8q_mx_set_tile.argtypes = [i32]
+        L.fp8q_mx_set_tile.argtypes = [i32, i32]
         L.fp8q_mx_set_tile.restype = i32
         L.fp8_quant_mx.argtypes = [P, i64, i64, i32, i32, P, P, P, P, P, P, P, P]
         L.fp8_gemm_mx.argtypes = [P, P, P, P, P, i64, i64, i64, i32, i32, P, P]
+        L.fp8_mx_scale_bytes.argtypes = [i64, i64]
+        L.fp8_mx_scale_bytes.restype = i64
         for fn in ("fp8_quant_fused", "fp8_quant_fused_ex", "fp8_quant_fused_batch", "fp8_downproj_fwd",
                    "fp8_downproj_fwd_noalloc", "fp8_downproj_fwd_ex", "fp8_gemm_fwd", "fp8_gemm_fwd_update", "fp8_gemm_dgrad", "fp8_gemm_wgrad", "fp8_gemm_dgrad_act", "fp8_gemm_dgrad_act_q", "fp8_upproj_fwd", "amax_history_update",
                    "amax_history_update_ex", "fp8_quant_mx", "fp8_gemm_mx"):
@@ -394,29 +396,41 @@ def fp8_downproj_fwd_noalloc(h: torch.Tensor, wt_q: torch.Tensor, scale_x: torch
     _check("fp8_downproj_fwd_noalloc", st)
 
 
+def fp8_mx_scale_bytes(rows: int, K: int) -> int:
+    """Bytes of the tiled scale layout of a [rows, K/32] MX block grid (K % 32 == 0)."""
+    n = lib().fp8_mx_scale_bytes(int(rows), int(K))
+    if n < 0:
+        raise ValueError(f"no MX scale layout for rows={rows}, K={K}")
+    return n
+
+
 def fp8_quant_mx(h: torch.Tensor, act: int, fmt: int, *, act_out=None, q_out=None, sf_out=None, q_t_out=None,
                  sf_t_out=None, amax_out=None, sat_count=None, stream=None) -> None:
     """MXFP8 quantize of h [M,K]: one power-of-two scale byte per 32 values, along the rows
-    (q_out [M,K], sf_out [M,K/32]) or down the columns, transposed (q_t_out [K,M], sf_t_out [K,M/32])."""
+    (q_out [M,K], sf_out: the tiled layout of the [M, K/32] grid) or down the columns, transposed
+    (q_t_out [K,M], sf_t_out: the tiled layout of the [K, M/32] grid)."""
     M, K = h.shape
     n = M * K
+    sf_n = fp8_mx_scale_bytes(M, K) if sf_out is not None else None
+    sf_t_n = fp8_mx_scale_bytes(K, M) if sf_t_out is not None else None
     st = lib().fp8_quant_mx(
         _ptr(h, 2 * n, "h"), M, K, act, fmt, _ptr(act_out, 2 * n, "act_out"), _ptr(q_out, n, "q_out"),
-        _ptr(sf_out, n // 32, "sf_out"), _ptr(q_t_out, n, "q_t_out"), _ptr(sf_t_out, n // 32, "sf_t_out"),
+        _ptr(sf_out, sf_n, "sf_out"), _ptr(q_t_out, n, "q_t_out"), _ptr(sf_t_out, sf_t_n, "sf_t_out"),
         _ptr(amax_out, 4, "amax_out"), _ptr(sat_count, 8, "sat_count"), _stream(stream))
     _check("fp8_quant_mx", st)
 
 
 def fp8_gemm_mx(x_q: torch.Tensor, sf_x: torch.Tensor, wt_q: torch.Tensor, sf_w: torch.Tensor, y: torch.Tensor, *,
                 fmt_x: int = E4M3, fmt_w: int = E4M3, status=None, stream=None) -> None:
-    """y[M,N] = BF16(sum_k x_q 2^(sf_x - 127) wt_q 2^(sf_w - 127)) on the block-scaled tensor cores."""
+    """y[M,N] = BF16(sum_k x_q 2^(sf_x - 127) wt_q 2^(sf_w - 127)) on the block-scaled tensor cores
+    (sf_x, sf_w: the tiled scale layouts of fp8_quant_mx's outputs)."""
     M, K = x_q.shape
     N = wt_q.shape[0]
     if wt_q.shape[1] != K:
         raise ValueError("x_q [M,K] and wt_q [N,K] disagree on K")
     st = lib().fp8_gemm_mx(
-        _ptr(x_q, M * K, "x_q"), _ptr(sf_x, M * (K // 32), "sf_x"), _ptr(wt_q, N * K, "wt_q"),
-        _ptr(sf_w, N * (K // 32), "sf_w"), _ptr(y, 2 * M * N, "y"), M, N, K, fmt_x, fmt_w,
+        _ptr(x_q, M * K, "x_q"), _ptr(sf_x, fp8_mx_scale_bytes(M, K), "sf_x"), _ptr(wt_q, N * K, "wt_q"),
+        _ptr(sf_w, fp8_mx_scale_bytes(N, K), "sf_w"), _ptr(y, 2 * M * N, "y"), M, N, K, fmt_x, fmt_w,
         _ptr(status, 4, "status"), _stream(stream))
     _check("fp8_gemm_mx", st)
 
@@ -475,9 +489,9 @@ def fp8q_gemm_test_hold_loads(on: bool) -> None:
     lib().fp8q_gemm_test_hold_loads(1 if on else 0)
 
 
-def fp8q_mx_set_tile(bn: int) -> None:
-    """Pin fp8_gemm_mx's tile width (128, 192, 256; 0 = automatic)."""
-    _check("fp8q_mx_set_tile", lib().fp8q_mx_set_tile(int(bn)))
+def fp8q_mx_set_tile(pair: int, bn: int = 0) -> None:
+    """Pin fp8_gemm_mx's tile: pair 0/1, width 128, 192 or 256; (0, 0) = automatic."""
+    _check("fp8q_mx_set_tile", lib().fp8q_mx_set_tile(int(pair), int(bn)))
 
 
 def fp8q_test_set_fused_grid(ctas: int) -> None:

@@ -33,6 +33,33 @@ def dev_f32(x) -> torch.Tensor:
     return torch.tensor(np.atleast_1d(np.asarray(x, dtype=np.float32)), device="cuda")
 
 
+# The MX scale layout (include/fp8q.h, fp8_quant_mx): atoms of 128 rows x 4
+# blocks, 512 bytes; (row 128 i + 32 j + l, block 4 g + k) at byte
+# 512 (i G + g) + 16 l + 4 j + k, G = ceil(KB / 4).  Written out here from that
+# definition, as a plain reshape and transpose.
+def mx_scale_bytes(rows: int, KB: int) -> int:
+    return -(-rows // 128) * -(-KB // 4) * 512
+
+
+def mx_untile(sf: np.ndarray, rows: int, KB: int, pad=False):
+    """The [rows, KB] scale bytes of a tiled buffer (and, with pad=True, also the
+    padding blocks KB .. 4G - 1 of each row)."""
+    RB, G = -(-rows // 128), -(-KB // 4)
+    a = np.asarray(sf, dtype=np.uint8).reshape(-1)[:RB * G * 512].reshape(RB, G, 32, 4, 4)  # [i, g, l, j, k]
+    full = a.transpose(0, 3, 2, 1, 4).reshape(RB * 128, G * 4)                                # [i j l, g k]
+    return (full[:rows, :KB], full[:rows, KB:]) if pad else full[:rows, :KB]
+
+
+def mx_tile(sf_rows: np.ndarray) -> np.ndarray:
+    """The tiled buffer of a [rows, KB] array of scale bytes (padding blocks 127,
+    rows past the grid 127)."""
+    rows, KB = sf_rows.shape
+    RB, G = -(-rows // 128), -(-KB // 4)
+    full = np.full((RB * 128, G * 4), 127, np.uint8)
+    full[:rows, :KB] = sf_rows
+    return np.ascontiguousarray(full.reshape(RB, 4, 32, G, 4).transpose(0, 3, 2, 1, 4)).reshape(-1)
+
+
 def bf16_ulp(y: np.ndarray) -> np.ndarray:
     a = np.abs(y)
     with np.errstate(divide="ignore"):

@@ -358,20 +358,38 @@ def test_mx_argument_checks(lib):
     assert quant(qo=None, sf=None, qt=A, sft=A, K=24) == ERR_SHAPE  # columns: K % 16
     assert quant(act=4) == ERR_UNSUPPORTED
     assert quant(a=A + 8) == ERR_ALIGN
+    assert quant(sf=A + 4) == ERR_ALIGN                          # scale arrays: 16-byte aligned
+    assert quant(qo=None, sf=None, qt=A, sft=A + 4) == ERR_ALIGN
     assert quant() == ERR_UNSUPPORTED                            # valid: no sm_103 device here
     assert quant(qo=None, sf=None, qt=A, sft=A, K=272) == ERR_UNSUPPORTED
     g = lib.fp8_gemm_mx
     g.argtypes = [P] * 5 + [i64] * 3 + [ctypes.c_int] * 2 + [P] * 2
     g.restype = ctypes.c_int
 
-    def gemm(M=128, N=256, K=512, fx=0, fw=0, x=A, y=A):
-        return g(x, A, A, A, y, M, N, K, fx, fw, None, None)
+    def gemm(M=128, N=256, K=512, fx=0, fw=0, x=A, y=A, sfx=A, sfw=A):
+        return g(x, sfx, A, sfw, y, M, N, K, fx, fw, None, None)
 
     assert gemm(fx=2) == ERR_UNSUPPORTED
     assert gemm(x=None) == ERR_NULL
     assert gemm(K=48) == ERR_SHAPE
     assert gemm(N=24) == ERR_SHAPE
     assert gemm(y=A + 2) == ERR_ALIGN
+    assert gemm(sfx=A + 4) == ERR_ALIGN and gemm(sfw=A + 8) == ERR_ALIGN
     assert gemm() == ERR_UNSUPPORTED
-    assert lib.fp8q_mx_set_tile(96) == ERR_UNSUPPORTED
-    assert lib.fp8q_mx_set_tile(192) == OK and lib.fp8q_mx_set_tile(0) == OK
+    assert lib.fp8q_mx_set_tile(0, 96) == ERR_UNSUPPORTED
+    assert lib.fp8q_mx_set_tile(0, 192) == ERR_UNSUPPORTED      # B's scale atoms: whole 128-row blocks
+    assert lib.fp8q_mx_set_tile(2, 128) == ERR_UNSUPPORTED
+    assert lib.fp8q_mx_set_tile(1, 0) == ERR_UNSUPPORTED
+    assert lib.fp8q_mx_set_tile(0, 128) == OK and lib.fp8q_mx_set_tile(1, 256) == OK
+    assert lib.fp8q_mx_set_tile(0, 0) == OK
+
+
+def test_mx_scale_layout_size(lib):
+    """fp8_mx_scale_bytes: 512-byte atoms of 128 rows x 4 blocks of 32 values."""
+    sb = lib.fp8_mx_scale_bytes
+    sb.argtypes = [ctypes.c_int64, ctypes.c_int64]
+    sb.restype = ctypes.c_int64
+    assert sb(128, 128) == 512 and sb(1, 32) == 512 and sb(0, 64) == 0
+    assert sb(129, 128) == 1024 and sb(128, 160) == 1024
+    assert sb(131072, 6400) == 1024 * 50 * 512 and sb(1600, 6400) == 13 * 50 * 512
+    assert sb(-1, 32) == -1 and sb(10, 48) == -1 and sb(10, -32) == -1
