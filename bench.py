@@ -385,11 +385,14 @@ def kernel_times(dp, H, Wt, w, dev, reps: int) -> dict:
     return out
 
 
-def rooflines(w, kern_ms: dict, peaks: dict, fp8: dict, workload_key: str) -> dict:
+def rooflines(w, kern_ms: dict, peaks: dict, fp8: dict, workload_key: str, step_ms=None) -> dict:
     """The rooflines of a per-tensor step's kernels: the one-launch cast (HBM),
     the FP8 GEMM (tensor) and, where the step runs it, the one-launch step
     kernel, which is bound by both: its roofline time is the larger of its
-    algorithmic bytes over the HBM peak and its FLOPs over the FP8 peak."""
+    algorithmic bytes over the HBM peak and its FLOPs over the FP8 peak.
+    step_ms: the timed steps' mean event time when each step is that one
+    launch; its duration is then taken over the timed region (the
+    back-to-back figure is kept beside it as b2b_ms)."""
     M, K, N = w.M, w.K, w.N
     flops = 2.0 * M * N * K
     quant_bytes = 5.0 * M * K + 3.0 * K * N  # H in, BF16 act + E4M3 out; W in, W_q^T out
@@ -410,7 +413,7 @@ def rooflines(w, kern_ms: dict, peaks: dict, fp8: dict, workload_key: str) -> di
     }
     out["dominant"] = out["quant"] if kern_ms["quant"] >= kern_ms["gemm"] else out["gemm"]
     if "fused_step_kernel" in kern_ms:
-        t = kern_ms["fused_step_kernel"] * 1e-3
+        t = (step_ms if step_ms is not None else kern_ms["fused_step_kernel"]) * 1e-3
         fbytes = quant_bytes + 2.0 * M * N  # + Y
         t_hbm = fbytes / (peaks["hbm_gbs"] * 1e9)
         t_mma = flops / (fp8["tflops"] * 1e12)
@@ -425,6 +428,11 @@ def rooflines(w, kern_ms: dict, peaks: dict, fp8: dict, workload_key: str) -> di
              "hbm_gbs": fbytes / t / 1e9, "hbm_frac": t_hbm / t,
              "tensor_tflops": flops / t / 1e12, "tensor_frac": t_mma / t,
              "roofline_ms": max(t_hbm, t_mma) * 1e3,
+             "duration_ms": t * 1e3,
+             "duration_source": ("the timed steps (one launch per step; CUDA events around each step's "
+                                 "graph replay on the launching stream)" if step_ms is not None else
+                                 "back-to-back launches over input copies larger than L2"),
+             "b2b_ms": kern_ms["fused_step_kernel"],
              "peak_source": f"HBM: {peaks['source']} copy; FP8: {fp8['source']}"}
         out["fused"] = f
         out["dominant"] = f
@@ -568,8 +576,9 @@ def run_ours(args, world, rank, local):
     ms, total_flops = reduce_over_ranks(local_ms, flops_step, world)
     value = total_flops / (ms * 1e-3) / 1e12
     kern_ms["step"] = local_ms
-    roof = rooflines(w, kern_ms, peaks, fp8, w.name if not args.rows else f"{w.name}_m{w.M}")
     desc, launches_per_step = step_desc(dp)
+    roof = rooflines(w, kern_ms, peaks, fp8, w.name if not args.rows else f"{w.name}_m{w.M}",
+                     step_ms=local_ms if launches_per_step == 1 and r["graphs"] is not None else None)
 
     extras = {}
     if not args.no_extras:
@@ -630,7 +639,8 @@ def measure_other_config(name: str, dev, flush, fp8: dict, peaks: dict, steps: i
     reps = max(24, min(steps, 200))
     if not group:
         km = kernel_times(dp, r["H"], r["Wt"], w, dev, reps)
-        roof = rooflines(w, km, peaks, fp8, name)
+        roof = rooflines(w, km, peaks, fp8, name,
+                         step_ms=ms if launches == 1 and r["graphs"] is not None else None)
         row["kernel_ms"] = km
         row["roofline"] = roof["dominant"]
         row["roofline_quant"] = roof["quant"]
