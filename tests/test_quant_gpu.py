@@ -188,11 +188,13 @@ def test_weight_blocks_128x128(M, K):
 
 
 @pytest.mark.parametrize("mode", ["tensor", "relu2_act", "blocks_128x128", "groups_1x128"])
-def test_large_tiled_grid_every_mode(mode):
+@pytest.mark.parametrize("M,K", [(2000, 10240), (2000, 5120)])
+def test_large_tiled_grid_every_mode(mode, M, K):
     """Grids past two rounds of the register-landing tile kernel run the
     shared-memory one: 2000 x 10240 is 16 x 80 = 1280 tiles (a ragged last
-    tile row), in each tiled mode, with the transposed copy."""
-    M, K = 2000, 10240
+    tile row), in each tiled mode, with the transposed copy.  2000 x 5120 is
+    640 tiles: the register-landing kernel in two rounds (608 resident CTAs on
+    GB300's 152 SMs), the ragged tile row in the second."""
     h = _rand_bits(M, K, seed=77, std=0.5)
     h[7, 300] = WL.to_bf16_bits(np.array([60.0], np.float32))[0]
     if mode == "tensor":
