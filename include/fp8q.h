@@ -564,8 +564,8 @@ int fp8_quant_mx(const void* h, int64_t M, int64_t K, int act, int fmt, void* ac
  *   sf_w    device scale bytes of wt_q's [N, K/32] grid, the same layout
  *           (fp8_mx_scale_bytes(N, K) bytes).
  *   y       device [M,N] BF16.
- *   M, N, K M >= 0 (0: nothing is enqueued); N >= 16, N % 16 == 0; K >= 32,
- *           K % 32 == 0.
+ *   M, N, K 0 <= M <= 2^31 - 256 (0: nothing is enqueued); N >= 16,
+ *           N % 16 == 0; K >= 32, K % 32 == 0.
  *   fmt_x, fmt_w  FP8Q_E4M3 or FP8Q_E5M2.
  *   status  device int or NULL: FP8Q_DEV_TIMEOUT if a bounded wait gave up.
  * Errors: FP8Q_ERR_UNSUPPORTED for a bad format or no sm_103 device;

@@ -827,7 +827,9 @@ extern "C" int fp8_gemm_mx(const void* x_q, const uint8_t* sf_x, const void* wt_
     if (!wt_q || !sf_w) return FP8Q_ERR_NULL;
     if ((!x_q || !sf_x || !y) && M != 0) return FP8Q_ERR_NULL;
     if (M < 0 || N < 16 || N % 16 != 0 || K < 32 || K % 32 != 0) return FP8Q_ERR_SHAPE;
-    if (M > (int64_t(1) << 31) - BM || N > (int64_t(1) << 31) - 256 || K > (int64_t(1) << 31) - BK)
+    // TMA coordinates are 32-bit: the second CTA of the last pair tile starts at
+    // row ceil(M / 256) * 256 - 128
+    if (M > (int64_t(1) << 31) - 2 * BM || N > (int64_t(1) << 31) - 256 || K > (int64_t(1) << 31) - BK)
         return FP8Q_ERR_SHAPE;
     if (!aligned16(x_q) || !aligned16(wt_q) || !aligned16(y) || !aligned16(sf_x) || !aligned16(sf_w) ||
         (reinterpret_cast<uintptr_t>(status) & 3u))

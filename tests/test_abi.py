@@ -373,6 +373,8 @@ def test_mx_argument_checks(lib):
     assert gemm(x=None) == ERR_NULL
     assert gemm(K=48) == ERR_SHAPE
     assert gemm(N=24) == ERR_SHAPE
+    assert gemm(M=(1 << 31) - 255) == ERR_SHAPE                 # 32-bit TMA row coordinates of pair tiles
+    assert quant(M=(1 << 27) + 1, K=1024) == ERR_SHAPE           # rows: 2^32 blocks or more
     assert gemm(y=A + 2) == ERR_ALIGN
     assert gemm(sfx=A + 4) == ERR_ALIGN and gemm(sfw=A + 8) == ERR_ALIGN
     assert gemm() == ERR_UNSUPPORTED
