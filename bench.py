@@ -509,12 +509,13 @@ def run_profile(args, local):
     full = WL.WORKLOADS[args.workload]
     if args.mx:
         return run_profile_mx(args, w, H, Wt, dev)
-    fused = full.M >= FUSED_MIN_ROWS and not args.unfused
+    fused = full.M >= FUSED_MIN_ROWS and not args.unfused and not args.group
     if w.M != full.M:
         # the full size's tile too (the tile choice depends on M)
         from quantize_fp8_gemm_gb300 import binding as B
         B.fp8q_gemm_set_tile(*B.fp8q_test_gemm_tile(full.M, full.N, fused))
-    dp = Fp8DownProj(w.M, w.K, w.N, margin=w.margin, history_len=w.history_len, fused=fused, device=dev)
+    dp = Fp8DownProj(w.M, w.K, w.N, margin=w.margin, history_len=w.history_len, fused=fused, group=args.group,
+                     device=dev)
     dp.calibrate(H, Wt)
     for _ in range(max(1, args.steps)):
         dp.step(H, Wt)
@@ -1113,6 +1114,8 @@ def main():
                     help="run --steps eager steps without timing (the command an ncu capture wraps)")
     ap.add_argument("--mx", action="store_true",
                     help="with --profile: the MXFP8 path (block quantize, block cast, block-scaled GEMM)")
+    ap.add_argument("--group", action="store_true",
+                    help="with --profile: 1x128 / 128x128 group scales (block cast, group quantize, group-scaled GEMM)")
     ap.add_argument("--unfused", action="store_true",
                     help="with --profile: the two-launch path (batched cast, then the GEMM) instead of the one-launch step")
     args = ap.parse_args()
