@@ -73,3 +73,27 @@ def test_reference_arm_under_torchrun_two_ranks():
     assert r.returncode == 0, r.stderr[-3000:]
     lines = _json_lines(r.stdout)
     assert len(lines) == 1 and lines[0]["n_gpus"] == 2
+
+
+def test_fused_roofline_duration_source():
+    """The one-launch step kernel's roofline takes the timed steps' own time
+    when each step is that one launch, else the back-to-back figure; its
+    fraction is max(HBM time, tensor time) over that duration, and its
+    algorithmic bytes are 5 M K + 3 K N + 2 M N."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from quantize_fp8_gemm_gb300 import workloads as WL
+    w = WL.WORKLOADS["gpt2xl"]
+    km = {"quant": 0.67, "gemm": 0.72, "fused_step_kernel": 1.2}
+    peaks = {"hbm_gbs": 6788.6, "source": "measured"}
+    fp8 = {"tflops": 3900.0, "source": "burst"}
+    M, K, N = w.M, w.K, w.N
+    fbytes = 5.0 * M * K + 3.0 * K * N + 2.0 * M * N
+    t_roof = max(fbytes / (6788.6e9), 2.0 * M * N * K / 3900e12)
+    timed = bench.rooflines(w, km, peaks, fp8, "gpt2xl", step_ms=1.05)["fused"]
+    assert timed["duration_ms"] == 1.05 and timed["b2b_ms"] == 1.2
+    assert timed["frac"] == pytest.approx(t_roof / 1.05e-3)
+    assert timed["algorithmic_bytes"] == fbytes
+    b2b = bench.rooflines(w, km, peaks, fp8, "gpt2xl")["fused"]
+    assert b2b["duration_ms"] == 1.2 and b2b["frac"] == pytest.approx(t_roof / 1.2e-3)
+    assert bench.rooflines(w, km, peaks, fp8, "gpt2xl")["dominant"]["kernel"].startswith("fp8_gemm_kernel<FUSED>")
