@@ -1,6 +1,7 @@
 """Host-side logic of bench.py on the CPU: the max-over-ranks / sum-of-units
-reduction under a world-size-2 gloo group, and the reference (oracle) arm,
-alone and under torchrun with two ranks (rank 0 prints the only line)."""
+reduction under a world-size-2 gloo group, the reference (oracle) arm, alone
+and under torchrun with two ranks (rank 0 prints the only line), and the
+roofline of the one-launch step kernel."""
 import json
 import os
 import socket
