@@ -39,10 +39,9 @@ int fp8q_gemm_set_tile(int pair, int bn);
  * fp8q_mx_set_tile -- pin the tile shape of fp8_gemm_mx (a tuning knob), or
  * (0, 0) for the automatic choice (the default):
  *   pair  0: one CTA per 128 x bn tile
- *         1: a CTA pair per 256 x bn tile (2-SM); used only when M > 128 and
- *            the scale rows are whole aligned 4-byte words (K % 128 == 0, both
- *            scale arrays 4-byte aligned), else the 1-CTA tile of that width
- *   bn    128, 192 or 256
+ *         1: a CTA pair per 256 x bn tile (2-SM); used only when M > 128, else
+ *            the 1-CTA tile of that width
+ *   bn    128 or 256 (whole 128-row scale atoms of B per tile)
  * Returns FP8Q_ERR_UNSUPPORTED for any other combination (nothing changes).
  */
 int fp8q_mx_set_tile(int pair, int bn);
