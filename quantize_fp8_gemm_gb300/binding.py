@@ -490,7 +490,7 @@ def fp8q_gemm_test_hold_loads(on: bool) -> None:
 
 
 def fp8q_mx_set_tile(pair: int, bn: int = 0) -> None:
-    """Pin fp8_gemm_mx's tile: pair 0/1, width 128, 192 or 256; (0, 0) = automatic."""
+    """Pin fp8_gemm_mx's tile: pair 0/1, width 128 or 256; (0, 0) = automatic."""
     _check("fp8q_mx_set_tile", lib().fp8q_mx_set_tile(int(pair), int(bn)))
 
 
