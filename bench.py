@@ -1,7 +1,8 @@
 """Benchmark of the forward FP8 MLP down-projection on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload gpt2xl] [--rows M] [--no-extras] [--profile]
+                    [--workload gpt2xl] [--rows M] [--no-extras]
+                    [--profile [--mx | --group | --unfused]]
 
 One step is one pass of the forward path over one batch: cast W [K,N] to
 E4M3 (transposed operand), fused ReLU^2 + BF16 copy + E4M3 cast + amax of H
@@ -26,7 +27,8 @@ cuBLASLt FP8) and the path's other rows.
 against) on a bounded sample of rows of the same workload and reports it in the
 same metric and unit.  `--rows M` runs the workload with M rows (a smaller
 case for counter captures); `--profile` runs a few eager steps only, without
-timing, for `ncu`.
+timing, for `ncu` (with `--mx` the MXFP8 path, with `--group` the 1x128 /
+128x128 group-scaled path, with `--unfused` the two-launch path).
 
 Prints one JSON line on rank 0.
 """
